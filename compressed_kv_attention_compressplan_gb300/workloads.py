@@ -1,0 +1,241 @@
+"""Seeded synthetic inputs for the compressor -- shared by tests and the benchmark.
+
+This module only draws numbers: request lengths, request pool indices, the
+``kv_score`` rows, the ``ape`` bias and the prior state contents.  It holds none
+of the compressor's arithmetic.  Everything is generated on the CPU from a
+``torch.Generator`` seeded per tensor, so the GPU library and the CPU oracle
+receive byte-identical inputs (bf16 values are drawn in fp32 and rounded to
+nearest-even by ``Tensor.to``).
+
+The five named workloads follow the shapes, value distributions and length
+mixes of the compressor's serving regimes:
+
+* ``c4_prefill_small``  C4 ragged prefill, one request, prefix 0, extend 64,
+  head_dim 128, fp32 in/out, token-layout output, sentinel-filled 8-slot ring.
+* ``c4_decode``         C4 decode, batch 256, seq_len ~ U[1, 8192], head_dim 512,
+  bf16 input, fp32 output, ring pre-filled N(0,1).
+* ``c128_decode``       C128 decode, batch 512, seq_len ~ U[1, 32768] with a
+  seeded 25 % subset forced to multiples of 128, head_dim 512, bf16 -> fp32.
+* ``c4_prefill``        C4 ragged prefill, batch 64, prefix ~ U[0, 4096],
+  extend ~ U[1, 4096], head_dim 512, bf16 in/out, token layout.
+* ``c128_prefill``      C128 ragged prefill, batch 1024: 896 requests extend by 4
+  (speculative-decoding verify shape), 128 requests extend by U[128, 16384],
+  prefix ~ U[0, 65536], head_dim 512, bf16 input with 1 % of the score entries
+  set to +8, fp32 compact output.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+
+# Bit patterns used to fill state slots that no step has written: a quiet NaN
+# with a payload, so a read of such a slot by a pooled window is visible.
+SENTINEL_F32 = 0x7FC0DEAD
+SENTINEL_BF16 = 0x7FDE
+
+TOKEN = "token"
+COMPACT = "compact"
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    mode: str                     # "prefill" or "decode"
+    ratio: int                    # 4 or 128
+    head_dim: int
+    in_dtype: torch.dtype         # torch.float32 or torch.bfloat16
+    out_dtype: torch.dtype
+    out_layout: str               # TOKEN or COMPACT (prefill only)
+    rid: torch.Tensor             # [B] int64 request pool index
+    seq_lens: torch.Tensor        # [B] int64, length after this step
+    extend_lens: Optional[torch.Tensor]  # [B] int64 (prefill) or None (decode: 1 each)
+    kv_score: torch.Tensor        # [N, width] in_dtype, ragged rows (decode: N = B)
+    ape: torch.Tensor             # [window, head_dim] in_dtype
+    state: torch.Tensor           # [rows, width] in_dtype (C4: 8 rows per ring, C128: 128 per page)
+
+    @property
+    def batch(self) -> int:
+        return int(self.rid.numel())
+
+    @property
+    def num_q_tokens(self) -> int:
+        return int(self.kv_score.shape[0])
+
+    @property
+    def width(self) -> int:
+        return int(self.kv_score.shape[1])
+
+    @property
+    def window(self) -> int:
+        return 8 if self.ratio == 4 else self.ratio
+
+    def describe(self) -> dict:
+        d = {"workload": self.name, "mode": self.mode, "ratio": self.ratio, "head_dim": self.head_dim,
+             "batch": self.batch, "num_q_tokens": self.num_q_tokens,
+             "in_dtype": str(self.in_dtype).replace("torch.", ""),
+             "out_dtype": str(self.out_dtype).replace("torch.", "")}
+        if self.mode == "prefill":
+            d["out_layout"] = self.out_layout
+        return d
+
+
+def width_of(ratio: int, head_dim: int) -> int:
+    """Columns of one kv_score row: C4 |kv-ovl|kv|score-ovl|score|, C128 |kv|score|."""
+    return 4 * head_dim if ratio == 4 else 2 * head_dim
+
+
+def slots_of(ratio: int) -> int:
+    """State rows owned by one request: an 8-slot ring (C4) or a 128-slot page (C128)."""
+    return 8 if ratio == 4 else 128
+
+
+def _gen(seed: int, k: int) -> torch.Generator:
+    return torch.Generator().manual_seed(int(seed) * 1_000_003 + int(k))
+
+
+def normal(shape, dtype: torch.dtype, std: float, gen: torch.Generator, chunk: int = 1 << 24) -> torch.Tensor:
+    """N(0, std^2) draws in fp32, rounded to ``dtype``; filled in fixed chunks."""
+    out = torch.empty(shape, dtype=dtype)
+    flat = out.view(-1)
+    n = flat.numel()
+    tmp = torch.empty(min(chunk, max(n, 1)), dtype=torch.float32)
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        t = tmp[: e - s]
+        t.normal_(0.0, std, generator=gen)
+        flat[s:e].copy_(t)
+    return out
+
+
+def sentinel(shape, dtype: torch.dtype) -> torch.Tensor:
+    if dtype == torch.bfloat16:
+        return torch.full(shape, SENTINEL_BF16, dtype=torch.int16).view(torch.bfloat16)
+    return torch.full(shape, SENTINEL_F32, dtype=torch.int32).view(torch.float32)
+
+
+def set_score_outliers(kv_score: torch.Tensor, ratio: int, head_dim: int, frac: float, value: float,
+                       gen: torch.Generator, chunk_rows: int = 1 << 14) -> None:
+    """Sets a seeded fraction of the score entries (not kv) to ``value``."""
+    cols = slice(2 * head_dim, 4 * head_dim) if ratio == 4 else slice(head_dim, 2 * head_dim)
+    n = kv_score.shape[0]
+    for s in range(0, n, chunk_rows):
+        e = min(n, s + chunk_rows)
+        block = kv_score[s:e, cols]
+        mask = torch.rand(block.shape, generator=gen) < frac
+        block[mask] = value
+
+
+def make(name: str, mode: str, ratio: int, head_dim: int, in_dtype, out_dtype, out_layout, rid, seq_lens,
+         extend_lens, seed: int, num_requests_state: Optional[int] = None, state_fill: str = "normal",
+         outlier_frac: float = 0.0) -> Workload:
+    """Builds the tensors of one workload from its lengths."""
+    rid = torch.as_tensor(rid, dtype=torch.int64)
+    seq_lens = torch.as_tensor(seq_lens, dtype=torch.int64)
+    if extend_lens is not None:
+        extend_lens = torch.as_tensor(extend_lens, dtype=torch.int64)
+        n = int(extend_lens.sum())
+    else:
+        n = int(rid.numel())
+    width = width_of(ratio, head_dim)
+    window = 8 if ratio == 4 else ratio
+    kv_score = normal((n, width), in_dtype, 1.0, _gen(seed, 11))
+    if outlier_frac > 0:
+        set_score_outliers(kv_score, ratio, head_dim, outlier_frac, 8.0, _gen(seed, 12))
+    ape = normal((window, head_dim), in_dtype, 0.1, _gen(seed, 13))
+    nreq = int(num_requests_state if num_requests_state is not None else (int(rid.max()) + 1 if rid.numel() else 1))
+    rows = nreq * slots_of(ratio)
+    if state_fill == "normal":
+        state = normal((rows, width), in_dtype, 1.0, _gen(seed, 14))
+    else:
+        state = sentinel((rows, width), in_dtype)
+    return Workload(name, mode, ratio, head_dim, in_dtype, out_dtype, out_layout, rid, seq_lens, extend_lens,
+                    kv_score, ape, state)
+
+
+# ----------------------------------------------------------------------------- named workloads
+def c4_prefill_small(seed: int = 0) -> Workload:
+    return make("c4_prefill_small", "prefill", 4, 128, torch.float32, torch.float32, TOKEN,
+                rid=[0], seq_lens=[64], extend_lens=[64], seed=seed, num_requests_state=1, state_fill="sentinel")
+
+
+def c4_decode(seed: int = 0, batch: int = 256, head_dim: int = 512) -> Workload:
+    g = _gen(seed, 1)
+    seq_lens = torch.randint(1, 8192 + 1, (batch,), generator=g, dtype=torch.int64)
+    rid = torch.randperm(batch, generator=_gen(seed, 2))
+    return make("c4_decode", "decode", 4, head_dim, torch.bfloat16, torch.float32, TOKEN, rid, seq_lens, None,
+                seed, num_requests_state=batch)
+
+
+def c128_decode(seed: int = 0, batch: int = 512, head_dim: int = 512) -> Workload:
+    g = _gen(seed, 1)
+    seq_lens = torch.randint(1, 32768 + 1, (batch,), generator=g, dtype=torch.int64)
+    forced = torch.randperm(batch, generator=_gen(seed, 3))[: batch // 4]
+    seq_lens[forced] = 128 * torch.randint(1, 256 + 1, (forced.numel(),), generator=_gen(seed, 4),
+                                           dtype=torch.int64)
+    rid = torch.randperm(batch, generator=_gen(seed, 2))
+    return make("c128_decode", "decode", 128, head_dim, torch.bfloat16, torch.float32, TOKEN, rid, seq_lens,
+                None, seed, num_requests_state=batch)
+
+
+def c4_prefill(seed: int = 0, batch: int = 64, head_dim: int = 512, max_prefix: int = 4096,
+               max_extend: int = 4096) -> Workload:
+    pl = torch.randint(0, max_prefix + 1, (batch,), generator=_gen(seed, 1), dtype=torch.int64)
+    el = torch.randint(1, max_extend + 1, (batch,), generator=_gen(seed, 5), dtype=torch.int64)
+    rid = torch.randperm(batch, generator=_gen(seed, 2))
+    return make("c4_prefill", "prefill", 4, head_dim, torch.bfloat16, torch.bfloat16, TOKEN, rid, pl + el, el,
+                seed, num_requests_state=batch)
+
+
+def c128_prefill(seed: int = 0, batch: int = 1024, head_dim: int = 512, num_long: int = 128,
+                 short_extend: int = 4, long_extend=(128, 16384), max_prefix: int = 65536) -> Workload:
+    el = torch.full((batch,), short_extend, dtype=torch.int64)
+    long_ids = torch.randperm(batch, generator=_gen(seed, 6))[:num_long]
+    el[long_ids] = torch.randint(long_extend[0], long_extend[1] + 1, (num_long,), generator=_gen(seed, 5),
+                                 dtype=torch.int64)
+    pl = torch.randint(0, max_prefix + 1, (batch,), generator=_gen(seed, 1), dtype=torch.int64)
+    rid = torch.randperm(batch, generator=_gen(seed, 2))
+    return make("c128_prefill", "prefill", 128, head_dim, torch.bfloat16, torch.float32, COMPACT, rid, pl + el,
+                el, seed, num_requests_state=batch, outlier_frac=0.01)
+
+
+NAMED = {
+    "c4_prefill_small": c4_prefill_small,
+    "c4_decode": c4_decode,
+    "c128_decode": c128_decode,
+    "c4_prefill": c4_prefill,
+    "c128_prefill": c128_prefill,
+}
+
+
+def random_prefill(ratio: int, head_dim: int, in_dtype, out_dtype, out_layout: str, prefix_lens, extend_lens,
+                   seed: int, num_requests_state: Optional[int] = None, rid=None,
+                   state_fill: str = "normal", outlier_frac: float = 0.0) -> Workload:
+    """A prefill workload with the given per-request lengths (rid = seeded permutation by default)."""
+    pl = torch.as_tensor(prefix_lens, dtype=torch.int64)
+    el = torch.as_tensor(extend_lens, dtype=torch.int64)
+    if rid is None:
+        nreq = num_requests_state if num_requests_state is not None else len(pl)
+        rid = torch.randperm(nreq, generator=_gen(seed, 2))[: len(pl)]
+    rid = torch.as_tensor(rid, dtype=torch.int64)
+    return make("random_prefill", "prefill", ratio, head_dim, in_dtype, out_dtype, out_layout, rid, pl + el, el,
+                seed, num_requests_state=num_requests_state, state_fill=state_fill, outlier_frac=outlier_frac)
+
+
+def random_decode(ratio: int, head_dim: int, in_dtype, out_dtype, seq_lens, seed: int,
+                  num_requests_state: Optional[int] = None, rid=None) -> Workload:
+    sl = torch.as_tensor(seq_lens, dtype=torch.int64)
+    if rid is None:
+        nreq = num_requests_state if num_requests_state is not None else len(sl)
+        rid = torch.randperm(nreq, generator=_gen(seed, 2))[: len(sl)]
+    return make("random_decode", "decode", ratio, head_dim, in_dtype, out_dtype, TOKEN, rid, sl, None, seed,
+                num_requests_state=num_requests_state)
+
+
+def bits(t: torch.Tensor):
+    """numpy view of a CPU tensor as the oracle takes it (bf16 -> uint16 bit patterns)."""
+    t = t.contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view("uint16")
+    return t.numpy()
