@@ -1,0 +1,571 @@
+#!/usr/bin/env python
+"""Throughput of the KV compressor on one GB300 (or N, one process each).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  C128 ragged prefill, batch 1024 (896 requests extending by 4, 128 by
+  U[128,16384], prefix U[0,65536]), head_dim 512, bf16 -> fp32 compact:
+      plan_prefill -> compress_pool_prefill -> compress_write
+  then C128 decode, batch 512 (seq_len U[1,32768], 25 % forced to page
+  boundaries), head_dim 512, bf16 -> fp32:
+      plan_decode -> compress_decode
+Metric: compressed KV rows per second (prefill compress records + decode rows
+on a page boundary), and the achieved HBM bandwidth of the dominant kernel
+(the C128 prefill pool) against the measured GB300 copy bandwidth.
+
+Inputs live in HBM when the timed region starts.  Before every step (outside
+the timed region) the prefill state is restored from a pristine copy and L2
+is flushed by writing a buffer of twice its size.  Each step's four segments
+(plan_prefill | pool | write + plan_decode | decode) are CUDA graphs replayed
+between CUDA events on one stream.  ``e2e`` repeats the step through the same
+API with the step's inputs copied from pinned host memory and its outputs
+copied back inside the timed region.
+
+``--config NAME`` times one workload alone (c4_prefill_small, c4_decode,
+c128_decode, c4_prefill, c128_prefill; ``all`` for each in turn) and prints
+one line per workload.  ``--impl reference`` times the CPU oracle on the
+host cores over a bounded sample of the same step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from compressed_kv_attention_compressplan_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "compressed KV rows/sec and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
+UNIT = "rows/s"
+STEP_WORKLOAD = ("c128_prefill B=1024 (896 x extend 4 + 128 x extend U[128,16384], prefix U[0,65536]) "
+                 "+ c128_decode B=512 (seq_len U[1,32768], 25% on page boundaries); head_dim 512, bf16 in, "
+                 "fp32 out")
+
+
+# ----------------------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def elem(dt: torch.dtype) -> int:
+    return 2 if dt == torch.bfloat16 else 4
+
+
+def prefill_events(ratio, sl, el):
+    """Per compress event: (buffer_len, masked-entry count) in plan order, from
+    the request lengths (closed forms of the per-request loops)."""
+    R = ratio
+    W = 8 if R == 4 else 128
+    sl = np.asarray(sl, np.int64)
+    el = np.asarray(el, np.int64)
+    pl = sl - el
+    nc = sl // R - pl // R
+    b = np.repeat(np.arange(len(sl)), nc)
+    k = np.arange(int(nc.sum())) - np.repeat(np.cumsum(nc) - nc, nc)
+    p = (pl[b] // R + k + 1) * R - 1
+    j = p - pl[b]
+    bl = W - np.minimum(j + 1, W)
+    first = np.where((R == 4) & (p == 3), 4, 0)
+    first_w = (sl // R) * R - (4 if R == 4 else 0)
+    nw = sl - np.maximum(pl, first_w)
+    return bl, first, int(nc.sum()), int(nw.sum())
+
+
+def algorithmic_bytes(w: wl.Workload) -> dict:
+    """Bytes each kernel must move at minimum, each counted once (see DESIGN)."""
+    hd, R, W = w.head_dim, w.ratio, w.window
+    ein, eout = elem(w.in_dtype), elem(w.out_dtype)
+    entry = 2 * hd * ein                      # one window entry: kv + score (C4: one half row)
+    row = w.width * ein                       # one kv_score row
+    ape = W * hd * ein
+    B = w.batch
+    if w.mode == "prefill":
+        bl, first, nc, nw = prefill_events(R, w.seq_lens.numpy(), w.extend_lens.numpy())
+        n_state = np.maximum(bl - first, 0)
+        n_input = W - np.maximum(bl, first)
+        out_rows = w.num_q_tokens if w.out_layout == wl.TOKEN else nc
+        pool = int((n_state + n_input).sum()) * entry + out_rows * hd * eout + ape + 16 * nc
+        write = nw * (2 * row + 8)
+        plan = 24 * B + 16 * nc + 8 * nw + 16
+        return {"plan": plan, "pool": pool, "write": write, "rows": nc, "num_c": nc, "num_w": nw,
+                "total": plan + pool + write}
+    sl = w.seq_lens.numpy()
+    bnd = sl % R == 0
+    first = np.where((R == 4) & (sl == 4), 4, 0)
+    reads = int(((W - 1 - first) * bnd).sum()) * entry
+    dec = B * (2 * row + hd * eout + 16) + reads + ape
+    plan = B * (16 + 16)
+    return {"plan": plan, "decode": dec, "rows": int(bnd.sum()), "total": plan + dec}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        sel = str(device_index)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            if uuid:
+                sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        self.sel = sel
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.sel, f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- device runners
+class PrefillRunner:
+    """Device buffers + the three prefill segments of one workload."""
+
+    def __init__(self, ckv, w: wl.Workload, dev):
+        self.ckv, self.w, self.dev = ckv, w, dev
+        self.kv = w.kv_score.to(dev)
+        self.ape = w.ape.to(dev)
+        self.rid, self.sl, self.el = w.rid.to(dev), w.seq_lens.to(dev), w.extend_lens.to(dev)
+        self.state = w.state.to(dev)
+        self.pristine = self.state.clone()
+        nq = w.num_q_tokens
+        self.cap_c = ckv.capacity_compress(w.ratio, w.batch, nq)
+        self.cap_w = ckv.capacity_write(w.ratio, w.batch, nq)
+        self.plan_c = torch.empty(max(self.cap_c, 1), 16, dtype=torch.uint8, device=dev)
+        self.plan_w = torch.empty(max(self.cap_w, 1), 8, dtype=torch.uint8, device=dev)
+        self.counts = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.status = ckv.new_status(dev)
+        self.layout = ckv.OUT_TOKEN if w.out_layout == wl.TOKEN else ckv.OUT_COMPACT
+        rows = nq if self.layout == ckv.OUT_TOKEN else self.cap_c
+        self.out = torch.empty(max(rows, 1), w.head_dim, dtype=w.out_dtype, device=dev)
+
+    def plan(self):
+        c = self.ckv
+        c.plan_prefill(self.w.ratio, self.rid, self.sl, self.el, self.w.num_q_tokens, self.cap_c, self.cap_w,
+                       False, self.plan_c[: self.cap_c], self.plan_w[: self.cap_w], self.counts, self.status)
+
+    def pool(self):
+        self.ckv.compress_pool_prefill(self.w.ratio, self.w.head_dim, self.state, self.kv, self.ape,
+                                       self.plan_c[: self.cap_c], self.counts, self.layout, self.w.out_dtype,
+                                       self.out, self.status)
+
+    def write(self):
+        self.ckv.compress_write(self.w.ratio, self.w.head_dim, self.state, self.kv, self.plan_w[: self.cap_w],
+                                self.counts, self.status)
+
+    def restore(self):
+        self.state.copy_(self.pristine)
+
+
+class DecodeRunner:
+    def __init__(self, ckv, w: wl.Workload, dev):
+        self.ckv, self.w, self.dev = ckv, w, dev
+        self.kv = w.kv_score.to(dev)
+        self.ape = w.ape.to(dev)
+        self.rid, self.sl = w.rid.to(dev), w.seq_lens.to(dev)
+        self.state = w.state.to(dev)
+        self.pristine = self.state.clone()
+        self.plan_d = torch.empty(max(w.batch, 1), 16, dtype=torch.uint8, device=dev)
+        self.status = ckv.new_status(dev)
+        self.out = torch.empty(max(w.batch, 1), w.head_dim, dtype=w.out_dtype, device=dev)
+
+    def plan(self):
+        self.ckv.plan_decode(self.w.ratio, self.rid, self.sl, self.plan_d[: self.w.batch], self.status)
+
+    def decode(self):
+        self.ckv.compress_decode(self.w.ratio, self.w.head_dim, self.state, self.kv, self.ape,
+                                 self.plan_d[: self.w.batch], self.w.out_dtype, self.out[: self.w.batch],
+                                 self.status)
+
+    def restore(self):
+        self.state.copy_(self.pristine)
+
+
+def capture(fn):
+    fn()  # eager warm-up outside capture (sets function attributes, loads modules)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def l2_flush_buffer(dev):
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    return torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+
+
+def run_segments(segs, flush, restore, steps, warmup, ws, sampler=None):
+    """segs: list of (name, graph).  Returns per-step segment times (ms)."""
+    n = len(segs)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    for _ in range(warmup):
+        restore()
+        flush.zero_()
+        for _, g in segs:
+            g.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    t0 = time.perf_counter()
+    for s in range(steps):
+        restore()
+        flush.zero_()
+        evs[s][0].record()
+        for i, (_, g) in enumerate(segs):
+            g.replay()
+            evs[s][i + 1].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(ws)
+    clocks = sampler.stop() if sampler else None
+    seg_ms = np.array([[evs[s][i].elapsed_time(evs[s][i + 1]) for i in range(n)] for s in range(steps)])
+    return seg_ms, wall, clocks
+
+
+# ----------------------------------------------------------------------------- CPU baseline (oracle)
+def oracle_step(o, w5, w3, frac5=1.0):
+    """The oracle over (a sample of) the step: C128 prefill pool + write, then
+    C128 decode.  Returns (rows, seconds)."""
+    t0 = time.perf_counter()
+    pc, pw, (nc, nw), _ = o.plan_prefill(128, w5.rid, w5.seq_lens, w5.extend_lens)
+    k = max(1, int(round(nc * frac5)))
+    st5 = wl.bits(w5.state).copy() if frac5 >= 1.0 else None
+    if st5 is None:
+        st5 = wl.bits(w5.state)  # read-only use below (the write step is skipped for a sample)
+    o.compress_pool_prefill(128, 512, o.BF16, o.F32, st5, wl.bits(w5.kv_score), wl.bits(w5.ape), pc[:k], k,
+                            w5.num_q_tokens, o.OUT_COMPACT)
+    if frac5 >= 1.0:
+        o.compress_write(128, 512, o.BF16, st5, wl.bits(w5.kv_score), pw, nw)
+    st3 = wl.bits(w3.state).copy()
+    pd = o.plan_decode(128, w3.rid, w3.seq_lens)
+    o.compress_decode(128, 512, o.BF16, o.F32, st3, wl.bits(w3.kv_score), wl.bits(w3.ape), pd)
+    rows = k + int((w3.seq_lens.numpy() % 128 == 0).sum())
+    return rows, time.perf_counter() - t0
+
+
+def cores_used() -> dict:
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except Exception:
+        aff = os.cpu_count()
+    return {"host_cores": aff}
+
+
+# ----------------------------------------------------------------------------- main modes
+def bench_step(args, ws, rank, local):
+    from compressed_kv_attention_compressplan_gb300 import build as B
+    from compressed_kv_attention_compressplan_gb300 import ckv
+
+    B.build()
+    ckv.load_library()
+    dev = torch.device("cuda", local)
+    seed = args.seed + rank
+    w5 = wl.c128_prefill(seed)
+    w3 = wl.c128_decode(seed)
+    pre = PrefillRunner(ckv, w5, dev)
+    dec = DecodeRunner(ckv, w3, dev)
+    flush = l2_flush_buffer(dev)
+
+    def restore():
+        pre.restore()
+
+    g_plan = capture(pre.plan)
+    g_pool = capture(pre.pool)
+
+    def write_and_plan_d():
+        pre.write()
+        dec.plan()
+
+    g_wp = capture(write_and_plan_d)
+    g_dec = capture(dec.decode)
+    segs = [("plan_prefill", g_plan), ("pool_prefill", g_pool), ("write+plan_decode", g_wp), ("decode", g_dec)]
+    launches_per_step = 5
+    sampler = ClockSampler(local)
+    seg_ms, wall, clocks = run_segments(segs, flush, restore, args.steps, args.warmup, ws, sampler)
+    if int(pre.status[0]) or int(dec.status[0]):
+        raise RuntimeError(f"device status set: prefill {int(pre.status[0])} decode {int(dec.status[0])}")
+    b5 = algorithmic_bytes(w5)
+    b3 = algorithmic_bytes(w3)
+    nc = int(pre.counts[0])
+    assert nc == b5["num_c"] and int(pre.counts[1]) == b5["num_w"], "plan counts differ from the closed forms"
+    rows_per_step = b5["rows"] + b3["rows"]
+    step_ms = seg_ms.sum(1)
+    total_s = float(step_ms.sum()) / 1e3
+    total_s = max_over_ranks(total_s, ws)
+    rows_all = sum_over_ranks(rows_per_step * args.steps, ws)
+    value = rows_all / total_s
+    peak, peak_kind = peaks()
+    pool_ms = float(seg_ms[:, 1].mean())
+    pool_gbs = b5["pool"] / (pool_ms * 1e-3) / 1e9
+    dec_ms = float(seg_ms[:, 3].mean())
+    dec_gbs = b3["decode"] / (dec_ms * 1e-3) / 1e9
+    step_bytes = b5["total"] + b3["total"]
+
+    # ---- end to end: inputs from pinned host memory, outputs back, inside the timed region
+    h_kv5 = w5.kv_score.pin_memory()
+    h_len5 = [t.pin_memory() for t in (w5.rid, w5.seq_lens, w5.extend_lens)]
+    h_kv3 = w3.kv_score.pin_memory()
+    h_len3 = [t.pin_memory() for t in (w3.rid, w3.seq_lens)]
+    h_out5 = torch.empty(nc, w5.head_dim, dtype=w5.out_dtype).pin_memory()
+    h_out3 = torch.empty(w3.batch, w3.head_dim, dtype=w3.out_dtype).pin_memory()
+    h2d = (h_kv5.numel() * elem(w5.in_dtype) + sum(t.numel() * 8 for t in h_len5) +
+           h_kv3.numel() * elem(w3.in_dtype) + sum(t.numel() * 8 for t in h_len3))
+    d2h = h_out5.numel() * elem(w5.out_dtype) + h_out3.numel() * elem(w3.out_dtype)
+    e2e_s = 0.0
+    e2e_steps = max(1, min(args.steps, 10))
+    for s in range(e2e_steps + 1):
+        pre.restore()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pre.kv.copy_(h_kv5, non_blocking=True)
+        for d, h in zip((pre.rid, pre.sl, pre.el), h_len5):
+            d.copy_(h, non_blocking=True)
+        dec.kv.copy_(h_kv3, non_blocking=True)
+        for d, h in zip((dec.rid, dec.sl), h_len3):
+            d.copy_(h, non_blocking=True)
+        for _, g in segs:
+            g.replay()
+        h_out5.copy_(pre.out[:nc], non_blocking=True)
+        h_out3.copy_(dec.out[: w3.batch], non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        if s > 0:  # the first pass warms the copy engines
+            e2e_s += e0.elapsed_time(e1) / 1e3
+    e2e_s = max_over_ranks(e2e_s, ws)
+    e2e_value = sum_over_ranks(rows_per_step * e2e_steps, ws) / e2e_s
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": float(step_ms.mean()), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded CPU generator; shapes and length mixes of the serving regimes)",
+        "config": {"workload": STEP_WORKLOAD, "global_batch": ws * (w5.batch + w3.batch),
+                   "num_q_tokens": w5.num_q_tokens, "compress_rows_prefill": b5["rows"],
+                   "compress_rows_decode": b3["rows"], "head_dim": 512, "in_dtype": "bf16", "out_dtype": "f32",
+                   "parallelism": f"independent requests x{ws} (no collective)",
+                   "l2": "flushed before every step (2x L2 written), prefill state restored outside the timing",
+                   "algorithmic_bytes_per_step": step_bytes},
+        "roofline": {"bound": "hbm", "kernel": "c128_pool_kernel (prefill)", "achieved": pool_gbs, "peak": peak,
+                     "unit": "GB/s", "frac": pool_gbs / peak, "peak_kind": f"{peak_kind} hbm_gbs",
+                     "traffic": None, "algorithmic_bytes": b5["pool"], "avg_launch_ms": pool_ms},
+        "kernels": {
+            "plan_prefill_us": float(seg_ms[:, 0].mean()) * 1e3,
+            "pool_prefill_us": pool_ms * 1e3, "pool_prefill_gbs": pool_gbs,
+            "write_plus_plan_decode_us": float(seg_ms[:, 2].mean()) * 1e3,
+            "decode_us": dec_ms * 1e3, "decode_gbs": dec_gbs, "decode_frac": dec_gbs / peak,
+            "step_gbs": step_bytes / (float(step_ms.mean()) * 1e-3) / 1e9},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle as o
+
+        o.build()
+        rows, secs = oracle_step(o, w5, w3, 1.0)
+        line["cpu_baseline"] = {"value": rows / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": "one whole step (all c128_prefill compress records + write, all "
+                                          "c128_decode rows), single-threaded C, fp64 pool",
+                                "seconds": secs, **cores_used()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def bench_config(args, name, ws, rank, local):
+    """One workload alone; prints one line (not the headline contract line)."""
+    from compressed_kv_attention_compressplan_gb300 import build as B
+    from compressed_kv_attention_compressplan_gb300 import ckv
+
+    B.build()
+    ckv.load_library()
+    dev = torch.device("cuda", local)
+    w = wl.NAMED[name](args.seed + rank)
+    flush = l2_flush_buffer(dev)
+    b = algorithmic_bytes(w)
+    if w.mode == "prefill":
+        r = PrefillRunner(ckv, w, dev)
+        segs = [("plan_prefill", capture(r.plan)), ("pool_prefill", capture(r.pool)), ("write", capture(r.write))]
+        main_i, main_key = 1, "pool"
+    else:
+        r = DecodeRunner(ckv, w, dev)
+        segs = [("plan_decode", capture(r.plan)), ("decode", capture(r.decode))]
+        main_i, main_key = 1, "decode"
+    seg_ms, wall, _ = run_segments(segs, flush, r.restore, args.steps, args.warmup, ws)
+    if int(r.status[0]):
+        raise RuntimeError(f"device status {int(r.status[0])}")
+    peak, kind = peaks()
+    step_ms = seg_ms.sum(1)
+    main_ms = float(seg_ms[:, main_i].mean())
+    gbs = b[main_key] / (main_ms * 1e-3) / 1e9
+    line = {"workload": name, **w.describe(), "rows_per_step": b["rows"],
+            "rows_per_s": b["rows"] / (float(step_ms.mean()) * 1e-3), "ms_per_step": float(step_ms.mean()),
+            "step_gbs": b["total"] / (float(step_ms.mean()) * 1e-3) / 1e9,
+            "segments_us": {n: float(seg_ms[:, i].mean()) * 1e3 for i, (n, _) in enumerate(segs)},
+            "segments_us_min": {n: float(seg_ms[:, i].min()) * 1e3 for i, (n, _) in enumerate(segs)},
+            "main_kernel": segs[main_i][0], "main_bytes": b[main_key], "main_gbs": gbs, "main_frac": gbs / peak,
+            "peak_gbs": peak, "peak_kind": kind, "algorithmic_bytes": b}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def bench_reference(args, ws, rank):
+    """The oracle as it stands on the host cores, each step a bounded sample."""
+    if rank != 0:
+        return
+    import oracle as o
+
+    o.build()
+    w5 = wl.c128_prefill(args.seed)
+    w3 = wl.c128_decode(args.seed)
+    frac = args.ref_fraction
+    for _ in range(args.warmup):
+        oracle_step(o, w5, w3, frac)
+    rows_total, secs_total = 0, 0.0
+    for _ in range(args.steps):
+        rows, secs = oracle_step(o, w5, w3, frac)
+        rows_total += rows
+        secs_total += secs
+    value = rows_total / secs_total
+    sample = (f"each step: the first {frac:.4g} of the c128_prefill compress records (pool only) + all "
+              f"c128_decode rows, single-threaded C oracle, fp64 pool")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": secs_total / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": STEP_WORKLOAD, "head_dim": 512, "in_dtype": "bf16", "out_dtype": "f32"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                             **cores_used()},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="step", help="step (default) | all | " + " | ".join(wl.NAMED))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-fraction", type=float, default=0.125,
+                    help="share of the prefill compress records the reference arm pools per step")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        bench_reference(args, ws, rank)
+    elif args.config == "step":
+        bench_step(args, ws, rank, local)
+    else:
+        names = list(wl.NAMED) if args.config == "all" else [args.config]
+        for n in names:
+            bench_config(args, n, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

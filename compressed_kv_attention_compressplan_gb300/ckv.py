@@ -1,0 +1,250 @@
+"""Python binding of libckv (the GB300 KV compressor) over its C ABI.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Functions take CUDA ``torch.Tensor`` arguments, pass their device pointers and
+the current CUDA stream to the C entry point of the same name, and raise
+``CkvError`` for a non-zero return code.  There is no CPU path: without the
+built library (``build()`` / ``__graft_entry__.build()``) every call raises.
+
+Layouts (see include/ckv.h): kv_score rows are C4 ``[kv-ovl|kv|score-ovl|score]``
+(4*hd) or C128 ``[kv|score]`` (2*hd); the state is ``[rows, width]`` in the
+input dtype with 8 rows per request (C4) or 128 (C128); plans are uint8
+tensors of 16-byte (compress, decode) or 8-byte (write) records.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+F32 = 0
+BF16 = 1
+OUT_TOKEN = 0
+OUT_COMPACT = 1
+
+STATUS_BAD_LENGTH = 1
+STATUS_BAD_TOTAL = 2
+STATUS_CAPACITY = 4
+STATUS_BAD_INDEX = 8
+STATUS_TIMEOUT = 16
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CkvError(RuntimeError):
+    def __init__(self, code: int, func: str, msg: str):
+        super().__init__(f"{func}: {msg} (code {code})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Loads libckv.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libckv.so is not built ({path}); run "
+                               "compressed_kv_attention_compressplan_gb300.build.build() first")
+        lib = ctypes.CDLL(path)
+        vp, u32, i32, u64 = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int, ctypes.c_uint64
+        lib.ckv_capacity_compress.argtypes = [i32, u32, u32]
+        lib.ckv_capacity_compress.restype = u32
+        lib.ckv_capacity_write.argtypes = [i32, u32, u32]
+        lib.ckv_capacity_write.restype = u32
+        lib.ckv_plan_decode.argtypes = [i32, vp, vp, u32, vp, vp, vp]
+        lib.ckv_plan_prefill.argtypes = [i32, vp, vp, vp, u32, u32, u32, u32, i32, vp, vp, vp, vp, vp]
+        lib.ckv_compress_write.argtypes = [i32, i32, i32, vp, u64, vp, u32, vp, vp, u32, vp, vp]
+        lib.ckv_compress_pool_prefill.argtypes = [i32, i32, i32, i32, vp, u64, vp, u32, vp, vp, vp, u32, i32, vp,
+                                                  vp, vp]
+        lib.ckv_compress_prefill.argtypes = [i32, i32, i32, i32, vp, u64, vp, u32, vp, vp, vp, vp, u32, u32, i32,
+                                             vp, vp, vp]
+        lib.ckv_compress_decode.argtypes = [i32, i32, i32, i32, vp, u64, vp, vp, vp, u32, vp, vp, vp]
+        lib.ckv_error_string.argtypes = [i32]
+        lib.ckv_error_string.restype = ctypes.c_char_p
+        lib.ckv_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, func: str):
+    if rc != 0:
+        msg = load_library().ckv_error_string(rc).decode()
+        raise CkvError(rc, func, msg)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libckv takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libckv takes contiguous tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return F32
+    if dt == torch.bfloat16:
+        return BF16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def width_of(ratio: int, head_dim: int) -> int:
+    return 4 * head_dim if ratio == 4 else 2 * head_dim
+
+
+def window_of(ratio: int) -> int:
+    return 8 if ratio == 4 else ratio
+
+
+def capacity_compress(ratio: int, batch: int, num_q_tokens: int) -> int:
+    return int(load_library().ckv_capacity_compress(ratio, batch, num_q_tokens))
+
+
+def capacity_write(ratio: int, batch: int, num_q_tokens: int) -> int:
+    return int(load_library().ckv_capacity_write(ratio, batch, num_q_tokens))
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word (uint32 bits, stored in an int32 tensor)."""
+    return torch.zeros(4, dtype=torch.int32, device=device or "cuda")
+
+
+# ------------------------------------------------------------------------------ plans
+def plan_decode(ratio: int, rid: torch.Tensor, seq_lens: torch.Tensor, plan_d: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """DecodePlan records ``[batch, 16]`` uint8."""
+    batch = rid.numel()
+    if plan_d is None:
+        plan_d = torch.empty(max(batch, 1), 16, dtype=torch.uint8, device=rid.device)
+    _check(load_library().ckv_plan_decode(ratio, _ptr(rid), _ptr(seq_lens), batch, _ptr(plan_d), _ptr(status),
+                                          _stream(stream)), "ckv_plan_decode")
+    return plan_d[:batch]
+
+
+def plan_prefill(ratio: int, rid: torch.Tensor, seq_lens: torch.Tensor, extend_lens: torch.Tensor,
+                 num_q_tokens: int, capacity_c: Optional[int] = None, capacity_w: Optional[int] = None,
+                 pad_invalid: bool = False, plan_c: Optional[torch.Tensor] = None,
+                 plan_w: Optional[torch.Tensor] = None, counts: Optional[torch.Tensor] = None,
+                 status: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Returns ``(plan_c [cap_c,16] u8, plan_w [cap_w,8] u8, counts [4] int32)``; counts stay on the device:
+    ``{num_c, num_w, min extend_len, max extend_len}``."""
+    batch = rid.numel()
+    dev = rid.device
+    if capacity_c is None:
+        capacity_c = capacity_compress(ratio, batch, num_q_tokens)
+    if capacity_w is None:
+        capacity_w = capacity_write(ratio, batch, num_q_tokens)
+    if plan_c is None:
+        plan_c = torch.empty(max(capacity_c, 1), 16, dtype=torch.uint8, device=dev)
+    if plan_w is None:
+        plan_w = torch.empty(max(capacity_w, 1), 8, dtype=torch.uint8, device=dev)
+    if counts is None:
+        counts = torch.empty(4, dtype=torch.int32, device=dev)
+    _check(load_library().ckv_plan_prefill(ratio, _ptr(rid), _ptr(seq_lens), _ptr(extend_lens), batch, num_q_tokens,
+                                           capacity_c, capacity_w, int(pad_invalid), _ptr(plan_c), _ptr(plan_w),
+                                           _ptr(counts), _ptr(status), _stream(stream)), "ckv_plan_prefill")
+    return plan_c[:capacity_c], plan_w[:capacity_w], counts
+
+
+# ------------------------------------------------------------------------------ compute
+def _state_rows(state: torch.Tensor, ratio: int, head_dim: int) -> int:
+    w = width_of(ratio, head_dim)
+    if state.numel() % w:
+        raise ValueError("state width does not match ratio / head_dim")
+    return state.numel() // w
+
+
+def compress_write(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, plan_w: torch.Tensor,
+                   counts: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    _check(load_library().ckv_compress_write(ratio, head_dim, dtype_code(state.dtype), _ptr(state),
+                                             _state_rows(state, ratio, head_dim), _ptr(kv_score),
+                                             kv_score.shape[0], _ptr(plan_w), _ptr(counts), plan_w.shape[0],
+                                             _ptr(status), _stream(stream)), "ckv_compress_write")
+
+
+def compress_pool_prefill(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
+                          plan_c: torch.Tensor, counts: Optional[torch.Tensor] = None,
+                          out_layout: int = OUT_TOKEN, out_dtype: torch.dtype = torch.float32,
+                          out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    nq = kv_score.shape[0]
+    rows = nq if out_layout == OUT_TOKEN else plan_c.shape[0]
+    if out is None:
+        out = torch.empty(max(rows, 1), head_dim, dtype=out_dtype, device=kv_score.device)
+    _check(load_library().ckv_compress_pool_prefill(ratio, head_dim, dtype_code(kv_score.dtype), dtype_code(out.dtype),
+                                                    _ptr(state), _state_rows(state, ratio, head_dim), _ptr(kv_score),
+                                                    nq, _ptr(ape), _ptr(plan_c), _ptr(counts), plan_c.shape[0],
+                                                    out_layout, _ptr(out), _ptr(status), _stream(stream)),
+           "ckv_compress_pool_prefill")
+    return out[:rows]
+
+
+def compress_prefill(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
+                     plan_c: torch.Tensor, plan_w: torch.Tensor, counts: Optional[torch.Tensor] = None,
+                     out_layout: int = OUT_TOKEN, out_dtype: torch.dtype = torch.float32,
+                     out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """Pool, then write the state (one stream, in that order)."""
+    nq = kv_score.shape[0]
+    rows = nq if out_layout == OUT_TOKEN else plan_c.shape[0]
+    if out is None:
+        out = torch.empty(max(rows, 1), head_dim, dtype=out_dtype, device=kv_score.device)
+    _check(load_library().ckv_compress_prefill(ratio, head_dim, dtype_code(kv_score.dtype), dtype_code(out.dtype),
+                                               _ptr(state), _state_rows(state, ratio, head_dim), _ptr(kv_score), nq,
+                                               _ptr(ape), _ptr(plan_c), _ptr(plan_w), _ptr(counts), plan_c.shape[0],
+                                               plan_w.shape[0], out_layout, _ptr(out), _ptr(status),
+                                               _stream(stream)), "ckv_compress_prefill")
+    return out[:rows]
+
+
+def compress_decode(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
+                    plan_d: torch.Tensor, out_dtype: torch.dtype = torch.float32, out: Optional[torch.Tensor] = None,
+                    status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    batch = plan_d.shape[0]
+    if out is None:
+        out = torch.empty(max(batch, 1), head_dim, dtype=out_dtype, device=kv_score.device)
+    _check(load_library().ckv_compress_decode(ratio, head_dim, dtype_code(kv_score.dtype), dtype_code(out.dtype),
+                                              _ptr(state), _state_rows(state, ratio, head_dim), _ptr(kv_score),
+                                              _ptr(ape), _ptr(plan_d), batch, _ptr(out), _ptr(status),
+                                              _stream(stream)), "ckv_compress_decode")
+    return out[:batch]
+
+
+# ------------------------------------------------------------------------------ convenience
+def prefill_step(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
+                 rid: torch.Tensor, seq_lens: torch.Tensor, extend_lens: torch.Tensor, out_layout: int = OUT_TOKEN,
+                 out_dtype: torch.dtype = torch.float32, status: Optional[torch.Tensor] = None, stream=None):
+    """plan_prefill -> pool -> write.  Returns ``(out, plan_c, plan_w, counts)`` (all on the device)."""
+    plan_c, plan_w, counts = plan_prefill(ratio, rid, seq_lens, extend_lens, kv_score.shape[0], status=status,
+                                          stream=stream)
+    out = compress_prefill(ratio, head_dim, state, kv_score, ape, plan_c, plan_w, counts, out_layout, out_dtype,
+                           status=status, stream=stream)
+    return out, plan_c, plan_w, counts
+
+
+def decode_step(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
+                rid: torch.Tensor, seq_lens: torch.Tensor, out_dtype: torch.dtype = torch.float32,
+                status: Optional[torch.Tensor] = None, stream=None):
+    """plan_decode -> decode.  Returns ``(out, plan_d)``."""
+    plan_d = plan_decode(ratio, rid, seq_lens, status=status, stream=stream)
+    out = compress_decode(ratio, head_dim, state, kv_score, ape, plan_d, out_dtype, status=status, stream=stream)
+    return out, plan_d

@@ -1,0 +1,103 @@
+// api.cu -- the compute entry points of the C ABI: argument checks on the
+// host, then dispatch to the ratio-specific launchers.
+#include "common.cuh"
+#include "launch.h"
+
+using namespace ckv;
+
+namespace {
+
+int check_pool_args(int ratio, int head_dim, int in_dtype, int out_dtype) {
+  if (ratio != 4 && ratio != 128) return CKV_ERR_RATIO;
+  if (head_dim <= 0 || head_dim % 128 != 0 || head_dim > 1024) return CKV_ERR_HEAD_DIM;
+  if ((in_dtype != CKV_F32 && in_dtype != CKV_BF16) || (out_dtype != CKV_F32 && out_dtype != CKV_BF16))
+    return CKV_ERR_DTYPE;
+  return CKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ckv_compress_pool_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, const void* state,
+                              uint64_t state_rows, const void* kv_score_input, uint32_t num_q_tokens,
+                              const void* ape, const ckv_compress_plan_t* plan_c, const uint32_t* d_counts,
+                              uint32_t capacity_c, int out_layout, void* out, uint32_t* d_status,
+                              ckv_stream_t stream) {
+  int rc = check_pool_args(ratio, head_dim, in_dtype, out_dtype);
+  if (rc) return rc;
+  if (out_layout != CKV_OUT_TOKEN && out_layout != CKV_OUT_COMPACT) return CKV_ERR_DTYPE;
+  if (num_q_tokens > CKV_MAX_TOKENS || capacity_c > CKV_MAX_TOKENS + 1u) return CKV_ERR_SIZE;
+  const bool token = out_layout == CKV_OUT_TOKEN;
+  if ((token ? num_q_tokens : capacity_c) == 0) return CKV_OK;
+  if (!aligned16(out) || !aligned16(ape)) return CKV_ERR_POINTER;
+  if (capacity_c > 0 && (!aligned16(plan_c) || !aligned16(kv_score_input) || !aligned16(state)))
+    return CKV_ERR_POINTER;
+  if (d_counts && (reinterpret_cast<uintptr_t>(d_counts) & 3u)) return CKV_ERR_POINTER;
+  PoolArgs a{};
+  a.ratio = ratio;
+  a.head_dim = head_dim;
+  a.in_dtype = in_dtype;
+  a.out_dtype = out_dtype;
+  a.state = state;
+  a.state_rows = state_rows;
+  a.input = kv_score_input;
+  a.num_q_tokens = num_q_tokens;
+  a.ape = ape;
+  a.plan_c = plan_c;
+  a.d_counts = d_counts;
+  a.capacity = capacity_c;
+  a.out_layout = out_layout;
+  a.out = out;
+  a.d_status = d_status;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return ratio == 4 ? launch_c4_pool_prefill(a, s) : launch_c128_pool_prefill(a, s);
+}
+
+int ckv_compress_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, void* state, uint64_t state_rows,
+                         const void* kv_score_input, uint32_t num_q_tokens, const void* ape,
+                         const ckv_compress_plan_t* plan_c, const ckv_write_plan_t* plan_w,
+                         const uint32_t* d_counts, uint32_t capacity_c, uint32_t capacity_w, int out_layout,
+                         void* out, uint32_t* d_status, ckv_stream_t stream) {
+  // validate both halves before launching either
+  int rc = check_pool_args(ratio, head_dim, in_dtype, out_dtype);
+  if (rc) return rc;
+  if (capacity_w > 0 && (!aligned16(state) || !aligned16(kv_score_input) || plan_w == nullptr ||
+                         (reinterpret_cast<uintptr_t>(plan_w) & 7u)))
+    return CKV_ERR_POINTER;
+  rc = ckv_compress_pool_prefill(ratio, head_dim, in_dtype, out_dtype, state, state_rows, kv_score_input,
+                                 num_q_tokens, ape, plan_c, d_counts, capacity_c, out_layout, out, d_status, stream);
+  if (rc) return rc;
+  return ckv_compress_write(ratio, head_dim, in_dtype, state, state_rows, kv_score_input, num_q_tokens, plan_w,
+                            d_counts, capacity_w, d_status, stream);
+}
+
+int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, void* state, uint64_t state_rows,
+                        const void* kv_score_input, const void* ape, const ckv_decode_plan_t* plan_d,
+                        uint32_t batch, void* out, uint32_t* d_status, ckv_stream_t stream) {
+  int rc = check_pool_args(ratio, head_dim, in_dtype, out_dtype);
+  if (rc) return rc;
+  if (batch == 0) return CKV_OK;
+  if (!aligned16(state) || !aligned16(kv_score_input) || !aligned16(ape) || !aligned16(plan_d) || !aligned16(out))
+    return CKV_ERR_POINTER;
+  PoolArgs a{};
+  a.ratio = ratio;
+  a.head_dim = head_dim;
+  a.in_dtype = in_dtype;
+  a.out_dtype = out_dtype;
+  a.state = state;
+  a.state_mut = state;
+  a.state_rows = state_rows;
+  a.input = kv_score_input;
+  a.num_q_tokens = batch;
+  a.ape = ape;
+  a.plan_d = plan_d;
+  a.capacity = batch;
+  a.out_layout = CKV_OUT_TOKEN;
+  a.out = out;
+  a.d_status = d_status;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return ratio == 4 ? launch_c4_decode(a, s) : launch_c128_decode(a, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,351 @@
+// plan.cu -- the plan builders (decode and prefill) and small host helpers.
+//
+// Prefill planning follows the sequential CPU loop of c_plan.cuh
+// plan_compress_prefill_legacy (requests in batch order, positions ascending,
+// compress and write records in separate lists) together with the legacy
+// ring / page translation of plan_compress_prefill_legacy_kernel.  The pages'
+// GPU builder (plan_compress_prefill_kernel0) walks requests serially inside
+// one CTA and hands out slots with shared-memory atomics, so its order varies
+// run to run.  Here every record's index is a closed form of block-wide
+// exclusive scans of the per-request counts, so the GPU plan is bit-identical
+// to the CPU loop, and the work is O(records) spread over the whole grid.
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace ckv {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;  // one thread per request (batch <= 1024)
+constexpr int kWarps = kPlanThreads / 32;
+
+__device__ __forceinline__ int32_t legacy_page(int ratio, int32_t rid, int32_t position) {
+  // c_plan.cuh legacy_compute_page: C4 uses two 4-slot pages per request,
+  // alternating with the group index; C128 uses one page per request.
+  return ratio == 4 ? rid * 2 + ((position / 4) & 1) : rid;
+}
+
+__device__ __forceinline__ int32_t legacy_loc(int ratio, int32_t rid, int32_t position) {
+  return legacy_page(ratio, rid, position) * ratio + position % ratio;
+}
+
+// Inclusive warp scan of a 32-bit value (Kogge-Stone over __shfl_up_sync).
+__device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t v, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xFFFFFFFFu, v, off);
+    if (lane >= off) v += n;
+  }
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_inclusive_sum64(unsigned long long v, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, v, off);
+    if (lane >= off) v += n;
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint32_t warp_max(uint32_t v) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t warp_min(uint32_t v) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) v = min(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+  return v;
+}
+
+__global__ void plan_decode_kernel(int ratio, const int64_t* __restrict__ rid, const int64_t* __restrict__ seq_lens,
+                                   uint32_t batch, ckv_decode_plan_t* __restrict__ plan_d, uint32_t* d_status) {
+  const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  const int64_t sl = seq_lens[b];
+  const int64_t r = rid[b];
+  const int64_t slots = ratio == 4 ? 8 : 128;
+  uint4 rec = make_uint4(kInvalidU32, kInvalidU32, kInvalidU32, kInvalidU32);
+  if (sl >= 1 && sl <= INT32_MAX && r >= 0 && r * slots + slots - 1 <= INT32_MAX) {
+    const int32_t p1 = static_cast<int32_t>(sl - 1);
+    const int32_t p0 = max(p1 - ratio, 0);
+    const int32_t rr = static_cast<int32_t>(r);
+    rec = make_uint4(static_cast<uint32_t>(sl), static_cast<uint32_t>(legacy_loc(ratio, rr, p1)),
+                     static_cast<uint32_t>(legacy_page(ratio, rr, p0)),
+                     static_cast<uint32_t>(legacy_page(ratio, rr, p1)));
+  } else {
+    status_or(d_status, CKV_STATUS_BAD_LENGTH);
+  }
+  *reinterpret_cast<uint4*>(plan_d + b) = rec;
+}
+
+struct PrefillPlanArgs {
+  int ratio;
+  const int64_t* rid;
+  const int64_t* seq_lens;
+  const int64_t* extend_lens;
+  uint32_t batch;
+  uint32_t num_q_tokens;
+  uint32_t cap_c;
+  uint32_t cap_w;
+  int pad_invalid;
+  ckv_compress_plan_t* plan_c;
+  ckv_write_plan_t* plan_w;
+  uint32_t* d_counts;
+  uint32_t* d_status;
+};
+
+// Every CTA loads the <= 1024 request lengths, derives per request
+//   pl = sl - el, nc = sl/R - pl/R, first_w = (sl/R)*R - (R == 4 ? 4 : 0),
+//   wstart = max(pl, first_w), nw = sl - wstart,
+// scans el, nc and nw (exclusive, block-wide), reduces min / max of el, and
+// then emits records k = global thread, global thread + grid stride, ...:
+// record k of the compress list belongs to the request b with
+// off_c[b] <= k < off_c[b+1] (binary search), whose (k - off_c[b])-th event is
+// at position (pl/R + k - off_c[b] + 1) * R - 1.  Likewise for writes, which
+// cover positions wstart .. sl-1.
+__global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const PrefillPlanArgs a) {
+  __shared__ uint32_t s_off_c[kMaxBatch + 1];
+  __shared__ uint32_t s_off_w[kMaxBatch + 1];
+  __shared__ uint32_t s_off_e[kMaxBatch + 1];
+  __shared__ int32_t s_pl[kMaxBatch];
+  __shared__ int32_t s_wstart[kMaxBatch];
+  __shared__ int32_t s_rid[kMaxBatch];
+  __shared__ uint32_t s_wsum[3][kWarps];
+  __shared__ uint32_t s_wmin[kWarps], s_wmax[kWarps];
+  __shared__ uint32_t s_flags;
+  __shared__ unsigned long long s_total_e;
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int R = a.ratio;
+  const int64_t slots = R == 4 ? 8 : 128;
+  if (tid == 0) s_flags = 0;
+
+  uint32_t el_eff = 0, nc = 0, nw = 0;
+  uint32_t el_min = kInvalidU32, el_max = 0;
+  if (tid < static_cast<int>(a.batch)) {
+    const int64_t sl = a.seq_lens[tid];
+    const int64_t el = a.extend_lens[tid];
+    const int64_t r = a.rid[tid];
+    const bool ok = el > 0 && el <= sl && sl <= INT32_MAX && r >= 0 && r * slots + slots - 1 <= INT32_MAX &&
+                    el <= CKV_MAX_TOKENS;
+    el_eff = (el > 0 && el <= CKV_MAX_TOKENS) ? static_cast<uint32_t>(el) : 0u;
+    el_min = el_max = el_eff;
+    if (ok) {
+      const int32_t s32 = static_cast<int32_t>(sl);
+      const int32_t pl = s32 - static_cast<int32_t>(el);
+      const int32_t first_w = (s32 / R) * R - (R == 4 ? 4 : 0);
+      const int32_t wstart = max(pl, first_w);
+      nc = static_cast<uint32_t>(s32 / R - pl / R);
+      nw = static_cast<uint32_t>(s32 - wstart);
+      s_pl[tid] = pl;
+      s_wstart[tid] = wstart;
+      s_rid[tid] = static_cast<int32_t>(r);
+    } else {
+      s_pl[tid] = 0;
+      s_wstart[tid] = 0;
+      s_rid[tid] = 0;
+    }
+    if (!ok) atomicOr(&s_flags, CKV_STATUS_BAD_LENGTH);
+  }
+
+  // Block-wide exclusive scans of (el_eff, nc, nw): warp scans, then a scan of
+  // the 32 warp totals by warp 0.  A warp's token sum is below 32 * 2^24; the
+  // token grand total is also formed in 64 bits so that garbage lengths cannot
+  // wrap around to a plausible total (records are only emitted when it equals
+  // num_q_tokens < 2^24, and then no partial sum can overflow).
+  const uint32_t ie = warp_inclusive_sum(el_eff, lane);
+  const uint32_t ic = warp_inclusive_sum(nc, lane);
+  const uint32_t iw = warp_inclusive_sum(nw, lane);
+  const uint32_t wmn = warp_min(el_min), wmx = warp_max(el_max);
+  if (lane == 31) {
+    s_wsum[0][warp] = ie;
+    s_wsum[1][warp] = ic;
+    s_wsum[2][warp] = iw;
+  }
+  if (lane == 0) {
+    s_wmin[warp] = wmn;
+    s_wmax[warp] = wmx;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t te = warp_inclusive_sum(s_wsum[0][lane], lane);
+    const unsigned long long te64 = warp_inclusive_sum64(s_wsum[0][lane], lane);
+    const uint32_t tc = warp_inclusive_sum(s_wsum[1][lane], lane);
+    const uint32_t tw = warp_inclusive_sum(s_wsum[2][lane], lane);
+    const uint32_t mn = warp_min(s_wmin[lane]), mx = warp_max(s_wmax[lane]);
+    s_wsum[0][lane] = te - s_wsum[0][lane];  // exclusive warp offsets
+    s_wsum[1][lane] = tc - s_wsum[1][lane];
+    s_wsum[2][lane] = tw - s_wsum[2][lane];
+    if (lane == 31) {
+      s_total_e = te64;
+      s_off_e[kMaxBatch] = te;
+      s_off_c[kMaxBatch] = tc;
+      s_off_w[kMaxBatch] = tw;
+    }
+    if (lane == 0) {
+      s_wmin[0] = mn;
+      s_wmax[0] = mx;
+    }
+  }
+  __syncthreads();
+  s_off_e[tid] = s_wsum[0][warp] + ie - el_eff;
+  s_off_c[tid] = s_wsum[1][warp] + ic - nc;
+  s_off_w[tid] = s_wsum[2][warp] + iw - nw;
+  __syncthreads();
+
+  const uint32_t B = a.batch;
+  const unsigned long long total_e = s_total_e;
+  const uint32_t num_c = s_off_c[kMaxBatch];
+  const uint32_t num_w = s_off_w[kMaxBatch];
+  if (blockIdx.x == 0 && tid == 0) {
+    uint32_t flags = s_flags;
+    if (total_e != a.num_q_tokens) flags |= CKV_STATUS_BAD_TOTAL;
+    if (num_c > a.cap_c || num_w > a.cap_w) flags |= CKV_STATUS_CAPACITY;
+    if (flags) status_or(a.d_status, flags);
+    a.d_counts[0] = num_c;
+    a.d_counts[1] = num_w;
+    a.d_counts[2] = B ? s_wmin[0] : 0u;
+    a.d_counts[3] = B ? s_wmax[0] : 0u;
+  }
+  // Entries past the end of a short ragged buffer would name rows that do not
+  // exist: with a bad token total, emit nothing but padding.
+  const bool usable = total_e == a.num_q_tokens;
+  const uint32_t emit_c = usable ? min(num_c, a.cap_c) : 0u;
+  const uint32_t emit_w = usable ? min(num_w, a.cap_w) : 0u;
+  const int W = R == 4 ? 8 : 128;
+
+  const uint32_t stride = gridDim.x * blockDim.x;
+  const uint32_t work = max(a.cap_c, a.cap_w);
+  for (uint32_t k = blockIdx.x * blockDim.x + tid; k < work; k += stride) {
+    if (k < a.cap_c) {
+      uint4 rec = make_uint4(kInvalidU32, kInvalidU32, kInvalidU32, kInvalidU32);
+      bool store = a.pad_invalid != 0;
+      if (k < emit_c) {
+        uint32_t lo = 0, hi = B;  // largest b with off_c[b] <= k
+        while (hi - lo > 1) {
+          const uint32_t mid = (lo + hi) >> 1;
+          if (s_off_c[mid] <= k) lo = mid; else hi = mid;
+        }
+        const int32_t pl = s_pl[lo];
+        const int32_t p = (pl / R + static_cast<int32_t>(k - s_off_c[lo]) + 1) * R - 1;
+        const int32_t j = p - pl;
+        const uint32_t ragged = s_off_e[lo] + static_cast<uint32_t>(j);
+        const uint32_t bl = static_cast<uint32_t>(W - min(j + 1, W));
+        const int32_t rid = s_rid[lo];
+        rec = make_uint4(static_cast<uint32_t>(p + 1), ragged | (bl << CKV_BUFFER_LEN_SHIFT),
+                         static_cast<uint32_t>(legacy_page(R, rid, max(p - R, 0))),
+                         static_cast<uint32_t>(legacy_page(R, rid, p)));
+        store = true;
+      }
+      if (store) *reinterpret_cast<uint4*>(a.plan_c + k) = rec;
+    }
+    if (k < a.cap_w) {
+      uint2 rec = make_uint2(kInvalidU32, kInvalidU32);
+      bool store = a.pad_invalid != 0;
+      if (k < emit_w) {
+        uint32_t lo = 0, hi = B;
+        while (hi - lo > 1) {
+          const uint32_t mid = (lo + hi) >> 1;
+          if (s_off_w[mid] <= k) lo = mid; else hi = mid;
+        }
+        const int32_t p = s_wstart[lo] + static_cast<int32_t>(k - s_off_w[lo]);
+        const uint32_t ragged = s_off_e[lo] + static_cast<uint32_t>(p - s_pl[lo]);
+        rec = make_uint2(ragged, static_cast<uint32_t>(legacy_loc(R, s_rid[lo], p)));
+        store = true;
+      }
+      if (store) *reinterpret_cast<uint2*>(a.plan_w + k) = rec;
+    }
+  }
+}
+
+}  // namespace
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace ckv
+
+using namespace ckv;
+
+extern "C" {
+
+uint32_t ckv_capacity_compress(int ratio, uint32_t batch, uint32_t num_q_tokens) {
+  if (ratio != 4 && ratio != 128) return 0;
+  const uint64_t c = static_cast<uint64_t>(num_q_tokens) / ratio + batch;
+  return static_cast<uint32_t>(std::min<uint64_t>(c, num_q_tokens));
+}
+
+uint32_t ckv_capacity_write(int ratio, uint32_t batch, uint32_t num_q_tokens) {
+  if (ratio != 4 && ratio != 128) return 0;
+  const uint64_t w = static_cast<uint64_t>(batch) * (ratio == 4 ? 7 : 127);
+  return static_cast<uint32_t>(std::min<uint64_t>(w, num_q_tokens));
+}
+
+int ckv_plan_decode(int ratio, const int64_t* rid, const int64_t* seq_lens, uint32_t batch,
+                    ckv_decode_plan_t* plan_d, uint32_t* d_status, ckv_stream_t stream) {
+  if (ratio != 4 && ratio != 128) return CKV_ERR_RATIO;
+  if (batch == 0) return CKV_OK;
+  if (!rid || !seq_lens || !aligned16(plan_d)) return CKV_ERR_POINTER;
+  if ((reinterpret_cast<uintptr_t>(rid) | reinterpret_cast<uintptr_t>(seq_lens)) & 7u) return CKV_ERR_POINTER;
+  const uint32_t threads = 256;
+  plan_decode_kernel<<<(batch + threads - 1) / threads, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      ratio, rid, seq_lens, batch, plan_d, d_status);
+  return check_launch();
+}
+
+int ckv_plan_prefill(int ratio, const int64_t* rid, const int64_t* seq_lens, const int64_t* extend_lens,
+                     uint32_t batch, uint32_t num_q_tokens, uint32_t capacity_c, uint32_t capacity_w,
+                     int pad_invalid, ckv_compress_plan_t* plan_c, ckv_write_plan_t* plan_w, uint32_t* d_counts,
+                     uint32_t* d_status, ckv_stream_t stream) {
+  if (ratio != 4 && ratio != 128) return CKV_ERR_RATIO;
+  if (batch > CKV_MAX_BATCH || num_q_tokens > CKV_MAX_TOKENS) return CKV_ERR_SIZE;
+  if (capacity_c > CKV_MAX_TOKENS + 1u || capacity_w > CKV_MAX_TOKENS + 1u) return CKV_ERR_SIZE;
+  if (d_counts == nullptr || (reinterpret_cast<uintptr_t>(d_counts) & 3u)) return CKV_ERR_POINTER;
+  if (batch > 0 && (!rid || !seq_lens || !extend_lens)) return CKV_ERR_POINTER;
+  if ((reinterpret_cast<uintptr_t>(rid) | reinterpret_cast<uintptr_t>(seq_lens) |
+       reinterpret_cast<uintptr_t>(extend_lens)) & 7u)
+    return CKV_ERR_POINTER;
+  if (capacity_c > 0 && !aligned16(plan_c)) return CKV_ERR_POINTER;
+  if (capacity_w > 0 && (plan_w == nullptr || (reinterpret_cast<uintptr_t>(plan_w) & 7u))) return CKV_ERR_POINTER;
+  PrefillPlanArgs a{ratio, rid, seq_lens, extend_lens, batch, num_q_tokens, capacity_c, capacity_w, pad_invalid,
+                    plan_c, plan_w, d_counts, d_status};
+  const uint32_t work = std::max(capacity_c, capacity_w);
+  uint32_t grid = (work + kPlanThreads - 1) / kPlanThreads;
+  grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 2u * static_cast<uint32_t>(sm_count())));
+  plan_prefill_kernel<<<grid, kPlanThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  return check_launch();
+}
+
+const char* ckv_error_string(int code) {
+  switch (code) {
+    case CKV_OK: return "ok";
+    case CKV_ERR_RATIO: return "ratio must be 4 or 128";
+    case CKV_ERR_HEAD_DIM: return "head_dim must be a positive multiple of 128 and at most 1024";
+    case CKV_ERR_SIZE: return "a batch, token count or capacity is out of range";
+    case CKV_ERR_POINTER: return "a required pointer is NULL or misaligned";
+    case CKV_ERR_DTYPE: return "unsupported dtype or layout";
+    case CKV_ERR_LAUNCH: return "CUDA launch failed";
+    default: return "unknown ckv error";
+  }
+}
+
+int ckv_version(void) { return 100; }
+
+}  // extern "C"

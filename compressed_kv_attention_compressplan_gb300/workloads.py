@@ -25,7 +25,9 @@ mixes of the compressor's serving regimes:
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
+import os
 from typing import Optional
 
 import torch
@@ -91,21 +93,37 @@ def slots_of(ratio: int) -> int:
     return 8 if ratio == 4 else 128
 
 
+def _seed(seed: int, k: int) -> int:
+    return int(seed) * 1_000_003 + int(k)
+
+
 def _gen(seed: int, k: int) -> torch.Generator:
-    return torch.Generator().manual_seed(int(seed) * 1_000_003 + int(k))
+    return torch.Generator().manual_seed(_seed(seed, k))
 
 
-def normal(shape, dtype: torch.dtype, std: float, gen: torch.Generator, chunk: int = 1 << 24) -> torch.Tensor:
-    """N(0, std^2) draws in fp32, rounded to ``dtype``; filled in fixed chunks."""
+def normal(shape, dtype: torch.dtype, std: float, gen_seed: int, chunk: int = 1 << 22) -> torch.Tensor:
+    """N(0, std^2) draws in fp32, rounded to ``dtype``.  The tensor is filled in
+    fixed chunks, each from its own generator seeded by (gen_seed, chunk index),
+    so the values do not depend on how many threads fill it."""
     out = torch.empty(shape, dtype=dtype)
     flat = out.view(-1)
     n = flat.numel()
-    tmp = torch.empty(min(chunk, max(n, 1)), dtype=torch.float32)
-    for s in range(0, n, chunk):
+
+    def fill(ci):
+        s = ci * chunk
         e = min(n, s + chunk)
-        t = tmp[: e - s]
-        t.normal_(0.0, std, generator=gen)
+        g = torch.Generator().manual_seed(int(gen_seed) * 7919 + ci)
+        t = torch.empty(e - s, dtype=torch.float32)
+        t.normal_(0.0, std, generator=g)
         flat[s:e].copy_(t)
+
+    nchunks = (n + chunk - 1) // chunk
+    if nchunks <= 1:
+        for ci in range(nchunks):
+            fill(ci)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+            list(ex.map(fill, range(nchunks)))
     return out
 
 
@@ -116,15 +134,17 @@ def sentinel(shape, dtype: torch.dtype) -> torch.Tensor:
 
 
 def set_score_outliers(kv_score: torch.Tensor, ratio: int, head_dim: int, frac: float, value: float,
-                       gen: torch.Generator, chunk_rows: int = 1 << 14) -> None:
-    """Sets a seeded fraction of the score entries (not kv) to ``value``."""
-    cols = slice(2 * head_dim, 4 * head_dim) if ratio == 4 else slice(head_dim, 2 * head_dim)
+                       gen: torch.Generator) -> None:
+    """Sets ``value`` at round(frac * #score entries) seeded positions of the score
+    columns (positions are drawn with replacement, so a few may repeat)."""
+    c0 = 2 * head_dim if ratio == 4 else head_dim
+    ncols = kv_score.shape[1] - c0
     n = kv_score.shape[0]
-    for s in range(0, n, chunk_rows):
-        e = min(n, s + chunk_rows)
-        block = kv_score[s:e, cols]
-        mask = torch.rand(block.shape, generator=gen) < frac
-        block[mask] = value
+    k = int(round(frac * n * ncols))
+    if k == 0:
+        return
+    idx = torch.randint(0, n * ncols, (k,), generator=gen, dtype=torch.int64)
+    kv_score[idx // ncols, c0 + idx % ncols] = value
 
 
 def make(name: str, mode: str, ratio: int, head_dim: int, in_dtype, out_dtype, out_layout, rid, seq_lens,
@@ -140,14 +160,14 @@ def make(name: str, mode: str, ratio: int, head_dim: int, in_dtype, out_dtype, o
         n = int(rid.numel())
     width = width_of(ratio, head_dim)
     window = 8 if ratio == 4 else ratio
-    kv_score = normal((n, width), in_dtype, 1.0, _gen(seed, 11))
+    kv_score = normal((n, width), in_dtype, 1.0, _seed(seed, 11))
     if outlier_frac > 0:
         set_score_outliers(kv_score, ratio, head_dim, outlier_frac, 8.0, _gen(seed, 12))
-    ape = normal((window, head_dim), in_dtype, 0.1, _gen(seed, 13))
+    ape = normal((window, head_dim), in_dtype, 0.1, _seed(seed, 13))
     nreq = int(num_requests_state if num_requests_state is not None else (int(rid.max()) + 1 if rid.numel() else 1))
     rows = nreq * slots_of(ratio)
     if state_fill == "normal":
-        state = normal((rows, width), in_dtype, 1.0, _gen(seed, 14))
+        state = normal((rows, width), in_dtype, 1.0, _seed(seed, 14))
     else:
         state = sentinel((rows, width), in_dtype)
     return Workload(name, mode, ratio, head_dim, in_dtype, out_dtype, out_layout, rid, seq_lens, extend_lens,

@@ -1,0 +1,212 @@
+/*
+ * ckv.h -- C ABI of libckv, the GB300 (sm_103a) KV compressor for
+ * DeepSeek-V4-style compressed attention caches.
+ *
+ * What it computes.  Every request owns a small state buffer: an 8-slot ring
+ * for compress ratio 4 ("C4") and a 128-slot page for ratio 128 ("C128").
+ * Each new token contributes one kv_score row:
+ *     C4   row = | kv-overlap | kv | score-overlap | score |   (4 * head_dim)
+ *     C128 row = | kv | score |                               (2 * head_dim)
+ * Whenever a request's length reaches a multiple of the ratio, one compressed
+ * KV row of head_dim values is emitted: per channel c, a softmax over the
+ * window of (score + ape[i]) weights the kv values,
+ *     out[c] = sum_i kv_i[c] * exp(s_i[c] - m) / sum_i exp(s_i[c] - m),
+ *     s_i[c] = fp32(score_i[c]) + fp32(ape[i][c]),  m = max_i s_i[c].
+ * C4's window is 8 tokens: the previous group's 4 overlap halves followed by
+ * the current group's 4 main halves; for the first group (length 4) the
+ * previous group does not exist and is left out.  C128's window is the 128
+ * tokens of the page.
+ *
+ * Sources (SGLang DeepSeek-V4 compressor): c_plan.cuh (the CompressPlan /
+ * WritePlan / DecodePlan builders and the legacy ring/page addressing),
+ * c4.cuh (C4 write and pool: c4_write, c4_forward, flash_c4_decode,
+ * flash_c4_prefill, FlashCompress4Kernel::run_prefill launch order),
+ * compressor_v2.py (C128 write and pool: _c128_compress_decode_kernel,
+ * _c128_compress_prefill_write_kernel, _compress_forward_c128_fallback).
+ *
+ * Conventions for every entry point:
+ *  - All pointers are DEVICE pointers owned by the caller (for example PyTorch
+ *    allocations).  The library allocates no device or host memory.
+ *  - Work is enqueued on `stream` and the call returns without synchronising;
+ *    results are valid once the stream has reached that point.  No call reads
+ *    device data on the host, so every call can be captured in a CUDA graph.
+ *  - The return value reports argument errors found on the host (CKV_OK or a
+ *    negative CKV_ERR_* code; nothing is launched on error).  Problems found in
+ *    device-resident data (bad lengths, out-of-range indices) are OR-ed into
+ *    the caller's `d_status` word (a device uint32, CKV_STATUS_* bits; may be
+ *    NULL to ignore them); the affected records are skipped, never trapped on.
+ *  - Pointers must be 16-byte aligned; head_dim must be a multiple of 128 and
+ *    at most 1024; dtypes are CKV_F32 or CKV_BF16.
+ *  - State buffers: C4 state is [num_requests * 8, 4 * head_dim] (request rid
+ *    owns rows rid*8 .. rid*8+7, i.e. two 4-slot pages 2*rid and 2*rid+1);
+ *    C128 state is [num_requests * 128, 2 * head_dim] (page rid = rows
+ *    rid*128 .. rid*128+127).  The state dtype is the input dtype.
+ *  - Invalid plan records have every byte 0xFF and are skipped.
+ */
+#ifndef CKV_H_
+#define CKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ckv_stream_t; /* the same handle as cudaStream_t */
+
+/* ------------------------------------------------------------------ codes */
+enum { CKV_F32 = 0, CKV_BF16 = 1 };
+enum { CKV_OUT_TOKEN = 0, CKV_OUT_COMPACT = 1 };
+
+enum {
+  CKV_OK = 0,
+  CKV_ERR_RATIO = -1,    /* ratio is not 4 or 128 */
+  CKV_ERR_HEAD_DIM = -2, /* head_dim not a positive multiple of 128, or > 1024 */
+  CKV_ERR_SIZE = -3,     /* batch > 1024, num_q_tokens >= 2^24, or a size/capacity out of range */
+  CKV_ERR_POINTER = -4,  /* a required pointer is NULL or not 16-byte aligned */
+  CKV_ERR_DTYPE = -5,    /* unsupported dtype / layout code */
+  CKV_ERR_LAUNCH = -6    /* the CUDA launch failed (cudaGetLastError) */
+};
+
+/* Bits OR-ed into *d_status by device code. */
+enum {
+  CKV_STATUS_BAD_LENGTH = 1u,  /* a request with extend_len <= 0, extend_len > seq_len,
+                                  seq_len >= 2^31, or a negative / too large rid */
+  CKV_STATUS_BAD_TOTAL = 2u,   /* sum(extend_lens) != num_q_tokens */
+  CKV_STATUS_CAPACITY = 4u,    /* more plan records than capacity_c / capacity_w */
+  CKV_STATUS_BAD_INDEX = 8u,   /* a plan record points outside the state or the input */
+  CKV_STATUS_TIMEOUT = 16u     /* a bounded wait on an asynchronous copy expired */
+};
+
+enum { CKV_MAX_BATCH = 1024, CKV_MAX_TOKENS = (1 << 24) - 1 };
+
+/* ------------------------------------------------------------------ plans */
+/* One compress event (16 bytes).  seq_len = position + 1 (a multiple of the
+ * ratio); ragged_bl = ragged_id | buffer_len << 24 where ragged_id is the row of
+ * the event's own token in the ragged input and buffer_len is the number of
+ * leading window entries held in the state (the rest are ragged rows
+ * ragged_id - (W-1) + i); read_page_0 / read_page_1 are the state pages of
+ * position max(position - ratio, 0) and of position (C4: 4-slot pages, window
+ * entries 0..3 live in read_page_0, entries 4..7 in read_page_1, slot i % 4;
+ * C128: page read_page_0, slot i).  c_plan.cuh: plan_compress_prefill (the
+ * CPU loop) and plan_compress_prefill_legacy_kernel; ragged_id widened from 16
+ * to 24 bits. */
+typedef struct ckv_compress_plan {
+  uint32_t seq_len;
+  uint32_t ragged_bl;
+  int32_t read_page_0;
+  int32_t read_page_1;
+} ckv_compress_plan_t;
+
+/* One state write (8 bytes): state[write_loc] = input[ragged_id].
+ * c_plan.cuh: WritePlan after plan_compress_prefill_legacy_kernel. */
+typedef struct ckv_write_plan {
+  uint32_t ragged_id;
+  int32_t write_loc;
+} ckv_write_plan_t;
+
+/* One decode row (16 bytes): seq_len, the state row the new token goes to, and
+ * the pages of positions max(seq_len-1-ratio, 0) and seq_len-1.
+ * c_plan.cuh: plan_compress_decode_legacy_kernel. */
+typedef struct ckv_decode_plan {
+  uint32_t seq_len;
+  int32_t write_loc;
+  int32_t read_page_0;
+  int32_t read_page_1;
+} ckv_decode_plan_t;
+
+#define CKV_RAGGED_MASK 0x00FFFFFFu
+#define CKV_BUFFER_LEN_SHIFT 24
+
+/* Upper bounds a caller can size plan buffers with (host arithmetic only):
+ * compress records <= num_q_tokens / ratio + batch, and
+ * write records <= min(num_q_tokens, batch * (ratio == 4 ? 7 : 127)). */
+uint32_t ckv_capacity_compress(int ratio, uint32_t batch, uint32_t num_q_tokens);
+uint32_t ckv_capacity_write(int ratio, uint32_t batch, uint32_t num_q_tokens);
+
+/* Decode plan (c_plan.cuh plan_compress_decode_legacy_kernel).
+ * rid[batch], seq_lens[batch]: int64 device arrays (seq_len counts the new
+ * token).  plan_d[batch]: output.  Rows with bad values get an invalid record
+ * and set CKV_STATUS_BAD_LENGTH.  One launch of ceil(batch/256) x 256. */
+int ckv_plan_decode(int ratio, const int64_t* rid, const int64_t* seq_lens, uint32_t batch,
+                    ckv_decode_plan_t* plan_d, uint32_t* d_status, ckv_stream_t stream);
+
+/* Prefill plans (c_plan.cuh plan_compress_prefill_kernel0 / _kernel_1 and the
+ * CPU loop of plan_compress_prefill_legacy, whose order is reproduced exactly):
+ * requests in batch order, positions ascending; compress records and write
+ * records are separate lists.  A request b with prefix pl = seq_lens[b] -
+ * extend_lens[b] emits a compress record for every extend position p with
+ * (p+1) % ratio == 0 and a write record for every extend position
+ * p >= (seq_len/ratio)*ratio - (ratio == 4 ? 4 : 0).
+ * Inputs: rid, seq_lens, extend_lens int64 device arrays [batch], batch <= 1024,
+ * num_q_tokens = sum(extend_lens) < 2^24 (checked on the device).
+ * Outputs: plan_c[capacity_c], plan_w[capacity_w]; d_counts[4] = {num_c, num_w,
+ * min extend_len, max extend_len} (num_c / num_w are the true counts even when
+ * they exceed the capacity; records past the capacity are dropped and
+ * CKV_STATUS_CAPACITY is set).  With pad_invalid != 0 the records
+ * [count, capacity) are filled with the invalid record (fixed-shape buffers for
+ * CUDA graphs).  One launch: every CTA scans the <= 1024 lengths itself and then
+ * emits its share of records, so no workspace is needed. */
+int ckv_plan_prefill(int ratio, const int64_t* rid, const int64_t* seq_lens, const int64_t* extend_lens,
+                     uint32_t batch, uint32_t num_q_tokens, uint32_t capacity_c, uint32_t capacity_w,
+                     int pad_invalid, ckv_compress_plan_t* plan_c, ckv_write_plan_t* plan_w, uint32_t* d_counts,
+                     uint32_t* d_status, ckv_stream_t stream);
+
+/* ------------------------------------------------------------------ compute */
+/* Prefill state write (c4.cuh c4_write / flash_c4_prefill<kWrite=true>,
+ * compressor_v2.py _c128_compress_prefill_write_kernel): for each of the first
+ * min(d_counts[1], capacity_w) records (all capacity_w records when d_counts is
+ * NULL), copy input row ragged_id (width 4*hd for C4, 2*hd for C128) to state
+ * row write_loc, bit for bit.  state_rows = rows of the state buffer.  Must run
+ * after ckv_compress_pool_prefill of the same step (writes may overwrite slots
+ * that the step's windows still read). */
+int ckv_compress_write(int ratio, int head_dim, int dtype, void* state, uint64_t state_rows,
+                       const void* kv_score_input, uint32_t num_q_tokens, const ckv_write_plan_t* plan_w,
+                       const uint32_t* d_counts, uint32_t capacity_w, uint32_t* d_status, ckv_stream_t stream);
+
+/* Prefill pool (c4.cuh c4_forward via flash_c4_prefill<kWrite=false>;
+ * compressor_v2.py _compress_forward_c128_fallback): for each compress record
+ * (the first min(d_counts[0], capacity_c)), window entry i < buffer_len is read
+ * from the state, the rest from input rows ragged_id - (W-1) + i; C4 records
+ * with seq_len == 4 leave out entries 0..3.  Output, in out_dtype:
+ *   CKV_OUT_TOKEN:   out is [num_q_tokens, head_dim]; row ragged_id holds the
+ *                    compressed row, every other row is written with +0.0.
+ *   CKV_OUT_COMPACT: out is [capacity_c, head_dim]; row k holds record k
+ *                    (rows of invalid / missing records are left untouched).
+ * ape is [W, head_dim] in the input dtype (W = 8 or 128).  Only reads the state. */
+int ckv_compress_pool_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, const void* state,
+                              uint64_t state_rows, const void* kv_score_input, uint32_t num_q_tokens,
+                              const void* ape, const ckv_compress_plan_t* plan_c, const uint32_t* d_counts,
+                              uint32_t capacity_c, int out_layout, void* out, uint32_t* d_status,
+                              ckv_stream_t stream);
+
+/* Prefill step: ckv_compress_pool_prefill followed by ckv_compress_write on
+ * the same stream (the order of c4.cuh FlashCompress4Kernel::run_prefill). */
+int ckv_compress_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, void* state, uint64_t state_rows,
+                         const void* kv_score_input, uint32_t num_q_tokens, const void* ape,
+                         const ckv_compress_plan_t* plan_c, const ckv_write_plan_t* plan_w,
+                         const uint32_t* d_counts, uint32_t capacity_c, uint32_t capacity_w, int out_layout,
+                         void* out, uint32_t* d_status, ckv_stream_t stream);
+
+/* Decode (c4.cuh flash_c4_decode; compressor_v2.py _c128_compress_decode_kernel):
+ * for each row b, write input row b to state row plan_d[b].write_loc; when
+ * seq_len % ratio == 0 emit the pool of the window (the new token's entry is
+ * taken from the input row, the others from the state), otherwise write +0.0
+ * to out row b.  kv_score_input is [batch, width], out is [batch, head_dim].
+ * Two rows of one batch must not name the same request. */
+int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, void* state, uint64_t state_rows,
+                        const void* kv_score_input, const void* ape, const ckv_decode_plan_t* plan_d,
+                        uint32_t batch, void* out, uint32_t* d_status, ckv_stream_t stream);
+
+/* ------------------------------------------------------------------ misc */
+/* Short text for a CKV_OK / CKV_ERR_* code (static storage). */
+const char* ckv_error_string(int code);
+/* Library ABI version: major * 100 + minor. */
+int ckv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CKV_H_ */

@@ -177,3 +177,85 @@ def np_bits(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
     return t.numpy()
+
+
+# --------------------------------------------------------------------------- GPU-side helpers
+def torch_dtype(code: int):
+    return torch.bfloat16 if code == 1 else torch.float32
+
+
+def to_torch(a: np.ndarray, code: int) -> torch.Tensor:
+    """numpy array (bf16 as uint16 bits, or float32) -> CPU torch tensor of that dtype."""
+    a = np.ascontiguousarray(a)
+    if code == 1:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(a)
+
+
+def as_f32(a: np.ndarray) -> np.ndarray:
+    return bf16_to_f32(a) if a.dtype == np.uint16 else a.astype(np.float32)
+
+
+def window_kv_absmax(ratio, hd, state, inp, seq_len, ragged, bl, rp0, rp1):
+    """max_i |kv_i[c]| over each event's window (masked entries excluded): [n, hd] float64.
+    ``state`` / ``inp`` are numpy row arrays (bf16 bits or fp32) of the kv_score layout."""
+    W = window(ratio)
+    n = len(seq_len)
+    out = np.zeros((n, hd))
+    for k in range(n):
+        first = 4 if (ratio == 4 and int(seq_len[k]) == 4) else 0
+        m = np.zeros(hd)
+        for i in range(first, W):
+            off = (0 if i < 4 else hd) if ratio == 4 else 0
+            if i < bl[k]:
+                row = state[state_row_of_entry(ratio, i, int(rp0[k]), int(rp1[k]))]
+            else:
+                row = inp[int(ragged[k]) - (W - 1) + i]
+            m = np.maximum(m, np.abs(as_f32(row[off:off + hd]).astype(np.float64)))
+        out[k] = m
+    return out
+
+
+def assert_pool_close(got: np.ndarray, want: np.ndarray, out_code: int, kvmax: np.ndarray = None, what=""):
+    """The parity bar: fp32 outputs within 2e-6 * max|kv| of the window (per
+    channel); bf16 outputs within 1 ulp (ordered-integer distance of the bits)."""
+    assert got.shape == want.shape, (got.shape, want.shape, what)
+    if out_code == 1:
+        d = ulp_distance(got, want)
+        assert d.max(initial=0) <= 1, f"{what}: bf16 ulp distance {d.max()}"
+    else:
+        err = np.abs(got.astype(np.float64) - want.astype(np.float64))
+        tol = 2e-6 * kvmax
+        bad = err > tol
+        assert not bad.any(), f"{what}: {bad.sum()} channels over tolerance, worst err/kvmax " \
+                              f"{(err / np.maximum(kvmax, 1e-30)).max():.3e}"
+
+
+class GpuBackend:
+    """Prefill / decode steps through libckv (state: a CUDA tensor, updated in place)."""
+
+    def __init__(self, device="cuda"):
+        from compressed_kv_attention_compressplan_gb300 import ckv
+
+        self.ckv = ckv
+        self.dev = torch.device(device)
+        self.status = ckv.new_status(self.dev)
+
+    def prefill(self, ratio, hd, in_dt, out_dt, state, rows, ape, rid, sl, el):
+        c = self.ckv
+        d = self.dev
+        out, _, _, _ = c.prefill_step(ratio, hd, state, to_torch(rows, in_dt).to(d), to_torch(ape, in_dt).to(d),
+                                      torch.tensor(rid, dtype=torch.int64, device=d),
+                                      torch.tensor(sl, dtype=torch.int64, device=d),
+                                      torch.tensor(el, dtype=torch.int64, device=d), c.OUT_TOKEN,
+                                      torch_dtype(out_dt), status=self.status)
+        return np_bits(out)
+
+    def decode(self, ratio, hd, in_dt, out_dt, state, rows, ape, rid, sl):
+        c = self.ckv
+        d = self.dev
+        out, _ = c.decode_step(ratio, hd, state, to_torch(rows, in_dt).to(d), to_torch(ape, in_dt).to(d),
+                               torch.tensor(rid, dtype=torch.int64, device=d),
+                               torch.tensor(sl, dtype=torch.int64, device=d), torch_dtype(out_dt),
+                               status=self.status)
+        return np_bits(out)

@@ -1,0 +1,63 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and
+exports every function include/ckv.h declares, plan records have the declared
+sizes, and argument errors are reported before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from compressed_kv_attention_compressplan_gb300 import build as B
+from compressed_kv_attention_compressplan_gb300 import ckv
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ckv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return ckv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ckv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_record_sizes_match_header():
+    text = open(HEADER).read()
+    for struct, size in [("ckv_compress_plan", 16), ("ckv_write_plan", 8), ("ckv_decode_plan", 16)]:
+        body = re.search(r"typedef struct %s \{(.*?)\}" % struct, text, flags=re.S).group(1)
+        fields = re.findall(r"(u?int32_t)\s+\w+;", body)
+        assert 4 * len(fields) == size, struct
+
+
+def test_capacity_bounds(lib):
+    assert ckv.capacity_compress(4, 64, 131072) == 131072 // 4 + 64
+    assert ckv.capacity_compress(128, 1024, 100) == 100       # never more than the tokens
+    assert ckv.capacity_write(4, 64, 10 ** 6) == 64 * 7
+    assert ckv.capacity_write(128, 1024, 5000) == 5000
+    assert ckv.capacity_compress(5, 1, 1) == 0
+
+
+def test_argument_errors_are_returned_before_any_launch(lib):
+    vp = ctypes.c_void_p
+    # bad ratio / head_dim / dtype / layout / pointers: rejected on the host
+    assert lib.ckv_plan_decode(3, None, None, 1, None, None, None) == -1
+    assert lib.ckv_plan_prefill(4, None, None, None, 2000, 0, 0, 0, 0, None, None, vp(16), None, None) == -3
+    assert lib.ckv_plan_prefill(4, None, None, None, 1, 0, 0, 0, 0, None, None, vp(16), None, None) == -4
+    assert lib.ckv_compress_decode(4, 100, 1, 0, None, 0, None, None, None, 1, None, None, None) == -2
+    assert lib.ckv_compress_decode(4, 128, 7, 0, None, 0, None, None, None, 1, None, None, None) == -5
+    assert lib.ckv_compress_decode(4, 128, 1, 0, vp(8), 8, vp(16), vp(16), vp(16), 1, vp(16), None, None) == -4
+    assert lib.ckv_compress_pool_prefill(128, 512, 1, 0, None, 0, None, 10, None, None, None, 1, 9, None, None,
+                                         None) == -5
+    assert lib.ckv_compress_write(4, 2048, 1, None, 0, None, 0, None, None, 1, None, None) == -2
+    assert lib.ckv_error_string(-4) != lib.ckv_error_string(0)

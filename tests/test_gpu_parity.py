@@ -1,0 +1,353 @@
+"""GPU parity: libckv (through its C ABI) against the CPU oracle.
+
+Bar: plans, write locations and state buffers bit-exact; fp32 outputs within
+2e-6 * max|kv| of the window per channel; bf16 outputs within 1 ulp.  Sizes
+span several tiles / grid-stride rounds and ragged tails; the edge cases
+(empty batch, maximum batch, first C4 group, capacity overflow, bad lengths,
+out-of-range plan records) are covered here too.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from compressed_kv_attention_compressplan_gb300 import workloads as wl
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": 0, "bf16": 1}
+
+
+@pytest.fixture(scope="module")
+def env(oracle_mod):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from compressed_kv_attention_compressplan_gb300 import build as B
+    from compressed_kv_attention_compressplan_gb300 import ckv
+
+    B.build()
+    ckv.load_library()
+    return oracle_mod, ckv, torch.device("cuda")
+
+
+def _dev_i64(x, dev):
+    return torch.as_tensor(np.asarray(x), dtype=torch.int64).to(dev)
+
+
+# ----------------------------------------------------------------------------- plans
+@pytest.mark.parametrize("ratio", [4, 128])
+def test_plan_decode_bit_exact(env, ratio):
+    o, ckv, dev = env
+    rng = np.random.default_rng(ratio)
+    B = 777
+    rid = rng.permutation(4096)[:B]
+    sl = rng.integers(1, 70000, B)
+    sl[:40] = np.arange(1, 41)
+    sl[40:80] = ratio * rng.integers(1, 300, 40)
+    got = ckv.plan_decode(ratio, _dev_i64(rid, dev), _dev_i64(sl, dev)).cpu().numpy()
+    assert (got == o.plan_decode(ratio, rid, sl)).all()
+
+
+def _prefill_case(name, ratio, rng):
+    if name == "random":
+        B = 37
+        pl = rng.integers(0, 3 * ratio + 50, B)
+        el = rng.integers(1, 5 * ratio + 40, B)
+    elif name == "mtp_uniform":
+        B = 1024
+        pl = rng.integers(0, 70000, B)
+        el = np.full(B, 4)
+    elif name == "decode_like":
+        B = 1000
+        pl = rng.integers(0, 5000, B)
+        el = np.ones(B, np.int64)
+    elif name == "one_long":
+        B = 1
+        pl = np.array([rng.integers(0, 1000)])
+        el = np.array([20000 + int(rng.integers(0, 999))])
+    elif name == "max_batch_mixed":
+        B = 1024
+        pl = rng.integers(0, 65536, B)
+        el = np.where(rng.random(B) < 0.875, 4, rng.integers(128, 2000, B))
+    else:
+        raise ValueError(name)
+    rid = rng.permutation(max(B, 2048))[:B]
+    return rid, pl + el, el
+
+
+@pytest.mark.parametrize("ratio", [4, 128])
+@pytest.mark.parametrize("case", ["random", "mtp_uniform", "decode_like", "one_long", "max_batch_mixed"])
+@pytest.mark.parametrize("pad", [False, True])
+def test_plan_prefill_bit_exact(env, ratio, case, pad):
+    o, ckv, dev = env
+    rng = np.random.default_rng(zlib.crc32(f"{ratio}-{case}".encode()))
+    rid, sl, el = _prefill_case(case, ratio, rng)
+    nq = int(el.sum())
+    cap_c = ckv.capacity_compress(ratio, len(rid), nq)
+    cap_w = ckv.capacity_write(ratio, len(rid), nq)
+    status = ckv.new_status(dev)
+    pc, pw, counts = ckv.plan_prefill(ratio, _dev_i64(rid, dev), _dev_i64(sl, dev), _dev_i64(el, dev), nq, cap_c,
+                                      cap_w, pad_invalid=pad, status=status)
+    torch.cuda.synchronize()
+    wc, ww, (nc, nw), rc = o.plan_prefill(ratio, rid, sl, el, nq, cap_c, cap_w, pad_invalid=pad)
+    assert rc == 0 and int(status[0]) == 0
+    cnt = counts.cpu().numpy()
+    assert (cnt[0], cnt[1]) == (nc, nw)
+    assert (cnt[2], cnt[3]) == (el.min(), el.max())
+    n_c = cap_c if pad else nc
+    n_w = cap_w if pad else nw
+    assert (pc[:n_c].cpu().numpy() == wc[:n_c]).all()
+    assert (pw[:n_w].cpu().numpy() == ww[:n_w]).all()
+
+
+def test_plan_prefill_empty_and_errors(env):
+    o, ckv, dev = env
+    status = ckv.new_status(dev)
+    e = torch.empty(0, dtype=torch.int64, device=dev)
+    pc, pw, counts = ckv.plan_prefill(4, e, e, e, 0, 4, 4, pad_invalid=True, status=status)
+    torch.cuda.synchronize()
+    assert counts[:2].tolist() == [0, 0] and int(status[0]) == 0
+    assert (pc.cpu().numpy() == 0xFF).all() and (pw.cpu().numpy() == 0xFF).all()
+    # capacity overflow: true counts reported, CAPACITY set, no record past the buffer
+    rid, sl, el = [0, 1], [9, 12], [9, 4]
+    pc, pw, counts = ckv.plan_prefill(4, _dev_i64(rid, dev), _dev_i64(sl, dev), _dev_i64(el, dev), 13, 2, 3,
+                                      status=status)
+    torch.cuda.synchronize()
+    assert counts[:2].tolist() == [3, 9] and int(status[0]) & ckv.STATUS_CAPACITY
+    wc, ww, _, _ = o.plan_prefill(4, rid, sl, el, 13, 2, 3, check=False)
+    assert (pc.cpu().numpy() == wc).all() and (pw.cpu().numpy() == ww).all()
+    # bad lengths and a wrong token total: flagged, nothing emitted, no fault
+    for sl_, el_, nq, bit in [([9, 5], [9, 6], 15, ckv.STATUS_BAD_LENGTH), ([9, 5], [9, 0], 9, ckv.STATUS_BAD_LENGTH),
+                              ([9, 5], [9, 5], 13, ckv.STATUS_BAD_TOTAL)]:
+        status.zero_()
+        pc, pw, counts = ckv.plan_prefill(128, _dev_i64([0, 1], dev), _dev_i64(sl_, dev), _dev_i64(el_, dev), nq, 8,
+                                          8, pad_invalid=True, status=status)
+        torch.cuda.synchronize()
+        assert int(status[0]) & bit
+    # decode plan: a bad row is invalid, the rest are fine
+    status.zero_()
+    pd = ckv.plan_decode(4, _dev_i64([0, -1, 2], dev), _dev_i64([5, 5, 0], dev), status=status).cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(status[0]) & ckv.STATUS_BAD_LENGTH
+    assert (pd[1] == 0xFF).all() and (pd[2] == 0xFF).all()
+    assert (pd[0] == o.plan_decode(4, [0], [5])[0]).all()
+
+
+# ----------------------------------------------------------------------------- prefill pool + write
+def _run_prefill_parity(env, ratio, hd, in_dt, out_dt, layout, pl, el, seed, state_fill="normal", outliers=0.0):
+    o, ckv, dev = env
+    w = wl.random_prefill(ratio, hd, H.torch_dtype(in_dt), H.torch_dtype(out_dt),
+                          wl.TOKEN if layout == 0 else wl.COMPACT, pl, el, seed,
+                          num_requests_state=len(pl) + 3, state_fill=state_fill, outlier_frac=outliers)
+    nq = w.num_q_tokens
+    state_d = w.state.to(dev)
+    status = ckv.new_status(dev)
+    pc, pw, counts = ckv.plan_prefill(ratio, w.rid.to(dev), w.seq_lens.to(dev), w.extend_lens.to(dev), nq,
+                                      status=status)
+    out = ckv.compress_prefill(ratio, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), pc, pw, counts, layout,
+                               H.torch_dtype(out_dt), status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    st = wl.bits(w.state).copy()
+    inp = wl.bits(w.kv_score)
+    wc, ww, (nc, nw), _ = o.plan_prefill(ratio, w.rid, w.seq_lens, w.extend_lens)
+    want = o.compress_pool_prefill(ratio, hd, in_dt, out_dt, st, inp, wl.bits(w.ape), wc, nc, nq, layout)
+    f = H.plan_c_fields(wc)
+    kvmax = H.window_kv_absmax(ratio, hd, st, inp, f["seq_len"], f["ragged_id"], f["buffer_len"],
+                               f["read_page_0"], f["read_page_1"])
+    got = H.np_bits(out)
+    if layout == 0:
+        rows = f["ragged_id"]
+        H.assert_pool_close(got[rows], want[rows], out_dt, kvmax, "compress rows")
+        others = np.setdiff1d(np.arange(nq), rows)
+        assert (got[others].view(np.uint16 if out_dt else np.uint32) == 0).all(), "non-compress rows not zero"
+    else:
+        H.assert_pool_close(got[:nc], want, out_dt, kvmax, "compact rows")
+    o.compress_write(ratio, hd, in_dt, st, inp, ww, nw)
+    assert (H.np_bits(state_d).view(np.uint8) == st.view(np.uint8)).all(), "state after write"
+
+
+@pytest.mark.parametrize("hd", [128, 384, 512])
+@pytest.mark.parametrize("dts", [("bf16", "f32"), ("bf16", "bf16"), ("f32", "f32"), ("f32", "bf16")])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_c4_prefill_parity(env, hd, dts, layout):
+    rng = np.random.default_rng(hd + 7 * layout)
+    pl = list(rng.integers(0, 40, 9)) + [0, 2, 5, 0]
+    el = list(rng.integers(1, 70, 9)) + [4, 2, 4, 1]
+    _run_prefill_parity(env, 4, hd, DT[dts[0]], DT[dts[1]], layout, pl, el, seed=hd + layout)
+
+
+@pytest.mark.parametrize("hd", [128, 512])
+@pytest.mark.parametrize("dts", [("bf16", "f32"), ("bf16", "bf16"), ("f32", "f32"), ("f32", "bf16")])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_c128_prefill_parity(env, hd, dts, layout):
+    rng = np.random.default_rng(hd + 11 * layout)
+    pl = list(rng.integers(0, 400, 5)) + [0, 127, 1]
+    el = list(rng.integers(1, 420, 5)) + [128, 1, 300]
+    _run_prefill_parity(env, 128, hd, DT[dts[0]], DT[dts[1]], layout, pl, el, seed=hd + layout, outliers=0.01)
+
+
+def test_c4_prefill_first_group_ignores_nan_state(env):
+    # sentinel-filled (NaN) ring: the first group of each request must not read it
+    _run_prefill_parity(env, 4, 128, 0, 0, 0, [0, 0, 1, 2], [4, 64, 3, 9], seed=3, state_fill="sentinel")
+
+
+# ----------------------------------------------------------------------------- decode
+@pytest.mark.parametrize("ratio", [4, 128])
+@pytest.mark.parametrize("hd", [128, 512])
+@pytest.mark.parametrize("dts", [("bf16", "f32"), ("bf16", "bf16"), ("f32", "f32")])
+def test_decode_parity(env, ratio, hd, dts):
+    o, ckv, dev = env
+    in_dt, out_dt = DT[dts[0]], DT[dts[1]]
+    rng = np.random.default_rng(ratio + hd)
+    B = 203
+    sl = rng.integers(1, 5000, B)
+    sl[:60] = ratio * rng.integers(1, 30, 60)
+    sl[60:64] = [1, 4, 8, ratio]
+    w = wl.random_decode(ratio, hd, H.torch_dtype(in_dt), H.torch_dtype(out_dt), sl, seed=ratio + hd,
+                         num_requests_state=256)
+    state_d = w.state.to(dev)
+    status = ckv.new_status(dev)
+    out, pd = ckv.decode_step(ratio, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), w.rid.to(dev),
+                              w.seq_lens.to(dev), H.torch_dtype(out_dt), status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    st0 = wl.bits(w.state).copy()
+    st = st0.copy()
+    wpd = o.plan_decode(ratio, w.rid, w.seq_lens)
+    assert (pd.cpu().numpy() == wpd).all()
+    inp = wl.bits(w.kv_score)
+    want = o.compress_decode(ratio, hd, in_dt, out_dt, st, inp, wl.bits(w.ape), wpd)
+    got = H.np_bits(out)
+    f = H.plan_d_fields(wpd)
+    bnd = np.nonzero(f["seq_len"] % ratio == 0)[0]
+    W = H.window(ratio)
+    kvmax = H.window_kv_absmax(ratio, hd, st0, inp, f["seq_len"][bnd], bnd, np.full(len(bnd), W - 1),
+                               f["read_page_0"][bnd], f["read_page_1"][bnd])
+    H.assert_pool_close(got[bnd], want[bnd], out_dt, kvmax, "decode boundary rows")
+    nb = np.setdiff1d(np.arange(B), bnd)
+    assert (got[nb].view(np.uint16 if out_dt else np.uint32) == 0).all()
+    assert (H.np_bits(state_d).view(np.uint8) == st.view(np.uint8)).all(), "state after decode"
+
+
+def test_out_of_range_records_are_flagged_not_faulted(env):
+    """Plan records that point outside the state or the input are skipped by the
+    kernels' own bounds checks and reported in the status word."""
+    o, ckv, dev = env
+    for ratio in (4, 128):
+        hd = 128
+        w = wl.random_decode(ratio, hd, torch.bfloat16, torch.float32, [ratio, 3], seed=1, num_requests_state=2)
+        status = ckv.new_status(dev)
+        bad = torch.tensor([[ratio, 10 ** 6, 10 ** 6, 10 ** 6], [3, 1, 0, 0]], dtype=torch.int32)
+        pd = bad.view(torch.uint8).reshape(2, 16).to(dev)
+        out = ckv.compress_decode(ratio, hd, w.state.to(dev), w.kv_score.to(dev), w.ape.to(dev), pd,
+                                  status=status)
+        torch.cuda.synchronize()
+        assert int(status[0]) & ckv.STATUS_BAD_INDEX
+        assert (out[0] == 0).all()
+        # prefill: a compress record whose page is outside the state, one whose
+        # window reaches before input row 0
+        W = H.window(ratio)
+        recs = torch.tensor([[2 * ratio, (W - 1) | (3 << 24), 10 ** 6, 10 ** 6],
+                             [ratio, 2 | (0 << 24), 0, 0]], dtype=torch.int32)
+        pc = recs.view(torch.uint8).reshape(2, 16).to(dev)
+        kv = torch.randn(W + 2, wl.width_of(ratio, hd)).to(torch.bfloat16).to(dev)
+        status.zero_()
+        ckv.compress_pool_prefill(ratio, hd, w.state.to(dev), kv, w.ape.to(dev), pc, None, ckv.OUT_COMPACT,
+                                  status=status)
+        torch.cuda.synchronize()
+        assert int(status[0]) & ckv.STATUS_BAD_INDEX
+        # write records outside the state / input
+        pw = torch.tensor([[0, 10 ** 7], [10 ** 6, 0]], dtype=torch.int32).view(torch.uint8).reshape(2, 8).to(dev)
+        status.zero_()
+        ckv.compress_write(ratio, hd, w.state.to(dev), kv, pw, None, status=status)
+        torch.cuda.synchronize()
+        assert int(status[0]) & ckv.STATUS_BAD_INDEX
+
+
+# ----------------------------------------------------------------------------- invariants on the GPU
+@pytest.mark.parametrize("ratio", [4, 128])
+def test_modes_bitwise_identical_on_gpu(env, ratio):
+    """One prefill, chunked prefills, token-by-token decode and a random mix of
+    both produce bit-identical rows on the GPU, and match the oracle's
+    whole-history definition within the parity bar."""
+    o, ckv, dev = env
+    hd = 512 if ratio == 4 else 256
+    rng = np.random.default_rng(ratio)
+    nreq = 6
+    lens = [int(rng.integers(1, 3 * ratio + 40)) for _ in range(nreq)]
+    rids = list(rng.permutation(8)[:nreq])
+    g = torch.Generator().manual_seed(ratio)
+    width = wl.width_of(ratio, hd)
+    hist = [wl.bits(torch.randn(n, width, generator=g).to(torch.bfloat16)).copy() for n in lens]
+    ape = wl.bits((torch.randn(H.window(ratio), hd, generator=g) * 0.1).to(torch.bfloat16)).copy()
+    want = [o.compress_history(ratio, hd, 1, 0, h, ape) for h in hist]
+    backend = H.GpuBackend(dev)
+    results = {}
+    for mode in ["oneshot", "chunked", "decode", "mixed"]:
+        if mode == "oneshot":
+            sched = [[("prefill", n)] for n in lens]
+        elif mode == "chunked":
+            sched = [H.split_schedule(n, rng, ratio + 5, 0.0) for n in lens]
+        elif mode == "decode":
+            sched = [[("decode", 1)] * n for n in lens]
+        else:
+            sched = [H.split_schedule(n, rng, ratio // 2 + 3, 0.5) for n in lens]
+        state = wl.sentinel((8 * H.slots(ratio), width), torch.bfloat16).to(dev)
+        results[mode] = H.run_schedule(backend, ratio, hd, 1, 0, hist, rids, sched, ape, state)
+        assert int(backend.status[0]) == 0
+    for b in range(nreq):
+        ref = results["oneshot"][b]
+        for mode in ["chunked", "decode", "mixed"]:
+            assert (results[mode][b].view(np.uint32) == ref.view(np.uint32)).all(), (mode, b)
+        emit = [p for p in range(lens[b]) if (p + 1) % ratio == 0]
+        if emit:
+            seq = np.array(emit) + 1
+            tok = hist[b]
+            # the window of a whole-history row: all from the token history
+            kvmax = H.window_kv_absmax(ratio, hd, tok, tok, seq, np.array(emit),
+                                       np.zeros(len(emit), np.int64), np.zeros(len(emit)), np.zeros(len(emit)))
+            H.assert_pool_close(ref[emit], want[b][emit], 0, kvmax, f"history b={b}")
+
+
+@pytest.mark.parametrize("ratio", [4, 128])
+def test_closed_forms_on_gpu(env, ratio):
+    """Equal scores + zero ape -> the exact window mean, bit for bit (the score
+    0.5 is a power of two, so max*log2(e) is exact and every weight is exactly
+    1); a dominant ape entry -> that entry's kv (within the parity bar)."""
+    o, ckv, dev = env
+    hd = 128
+    W = H.window(ratio)
+    T = 3 * ratio + 8
+    width = wl.width_of(ratio, hd)
+    rng = np.random.default_rng(3)
+    ncol = 2 * hd if ratio == 4 else hd
+    tok = np.zeros((T, width), np.float32)
+    tok[:, :ncol] = rng.integers(-50, 51, (T, ncol))
+    tok[:, ncol:] = 0.5
+    ape0 = np.zeros((W, hd), np.float32)
+    backend = H.GpuBackend(dev)
+    state = wl.sentinel((H.slots(ratio), width), torch.float32).to(dev)
+    got = H.run_schedule(backend, ratio, hd, 0, 0, [tok], [0], [[("prefill", T)]], ape0, state)[0]
+    want = o.compress_history(ratio, hd, 0, 0, tok, ape0)
+    assert (got.view(np.uint32) == want.view(np.uint32)).all()
+    q = np.arange(T, dtype=np.float32)[:, None]
+    ch = np.arange(hd, dtype=np.float32)[None, :] / 256.0
+    tok[:, :hd] = (1000.0 + q + ch) if ratio == 4 else (1.0 + q + ch)
+    if ratio == 4:
+        tok[:, hd:2 * hd] = 1.0 + q + ch
+    pick = (np.arange(hd) * 5 + 1) % W
+    ape = np.zeros((W, hd), np.float32)
+    ape[pick, np.arange(hd)] = 60.0
+    state = wl.sentinel((H.slots(ratio), width), torch.float32).to(dev)
+    got = H.run_schedule(backend, ratio, hd, 0, 0, [tok], [0], [[("prefill", T)]], ape, state)[0]
+    want = o.compress_history(ratio, hd, 0, 0, tok, ape)
+    for p in range(W - 1, T, ratio):
+        i = pick
+        pos = p - (W - 1) + i
+        tag = np.where(i < 4, 1000.0 + pos, 1.0 + pos) if ratio == 4 else 1.0 + pos
+        tag = (tag + np.arange(hd) / 256.0).astype(np.float32)
+        assert (want[p] == tag).all()
+        assert np.abs(got[p] - tag).max() <= 2e-6 * np.abs(tag).max(), p
