@@ -122,7 +122,7 @@ __device__ __forceinline__ void store_zero_chunk(TOut* p) {
 // scores s_i = fp32(score_i) + fp32(ape_i) (one rounding, __fadd_rn) and kv_i:
 //   M      = max_i s_i                                   (exact)
 //   t_i    = fma(s_i, log2e, -(M*log2e))                 (one rounding)
-//   e_i    = exp2f(t_i)
+//   e_i    = 2^t_i                                       (ex2.approx.ftz)
 //   l_g    = e_i summed in index order within each group of 16 entries
 //   a_g    = fma(kv_i, e_i, a) in index order within the group
 //   L, A   = balanced pairwise tree over the groups (1 group for C4's 8 entries,
@@ -135,7 +135,15 @@ __device__ __forceinline__ float score_plus_bias(float score, float bias) { retu
 
 __device__ __forceinline__ float neg_max_log2e(float m) { return __fmul_rn(m, -kLog2e); }
 
-__device__ __forceinline__ float weight_of(float s, float nml) { return exp2f(__fmaf_rn(s, kLog2e, nml)); }
+// 2^x by the hardware approximation (ex2.approx.ftz: a few ulp; results below
+// 2^-126 flush to zero, which only drops weights under 1e-38 of the largest).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float weight_of(float s, float nml) { return ex2(__fmaf_rn(s, kLog2e, nml)); }
 
 struct PoolAcc {
   float l;

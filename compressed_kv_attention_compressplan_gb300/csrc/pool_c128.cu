@@ -8,15 +8,29 @@
 // input row ragged_id - 127 + i otherwise; in decode entries 0..126 come from
 // the page and entry 127 is the new token.
 //
-// Mapping: one CTA per tile = (event, slice of CS channels).  The tile's 128
-// entries x CS channels of kv and of score (64 KB) are staged in shared
-// memory by 256 one-dimensional bulk copies (cp.async.bulk, the TMA engine)
-// that all signal one mbarrier, so every byte of the tile is in flight at once
-// and no register holds staged data.  The arithmetic then reads shared memory:
-// 8 groups of 16 consecutive entries x CS/4 channel quads; pass 1 forms the
-// scores and the exact per-channel maximum, pass 2 the group sums of weights
-// and weighted kv, pass 3 the fixed pairwise tree over the 8 groups.
+// Work unit: a tile = (event, slice of CS channels).  The tile's 128 entries x
+// CS channels of kv and of score (64 KB) are staged in shared memory by the TMA
+// engine and signal one mbarrier, so no register holds staged data.  When all
+// 128 entries are consecutive rows of one tensor (a prefill window that lies
+// in the extend; the 127 page slots of a decode window) the tile is two 2-D
+// tensor-map boxes (kv slice, score slice); a prefill window that starts in the
+// state is gathered with 256 one-dimensional bulk copies, one per row segment.  The arithmetic then reads shared
+// memory with 8 groups of 16 consecutive entries x CS/4 channel quads: pass 1
+// forms the scores and the exact per-channel maximum, pass 2 the group sums of
+// weights and weighted kv, pass 3 the fixed pairwise tree over the 8 groups.
+// Both kernels below run this same per-thread arithmetic (c128_pass1/2/3), so a
+// window gives the same bits whether it is pooled in prefill or in decode.
+//
+// Prefill kernel: persistent and warp-specialised.  One CTA per SM owns one
+// channel slice (its ape slice stays in registers); a producer warp streams the
+// CTA's tiles through a 3-stage shared-memory ring while 8 consumer warps
+// reduce the previous tiles.
+// Decode kernel: one CTA per (row, slice); rows that are not on a page
+// boundary only write their state slot and a zero output row.
+#include <cuda.h>  // CUtensorMap and its enums (types only; the encoder is fetched at run time)
+
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "launch.h"
@@ -26,14 +40,19 @@ namespace {
 
 template <typename TIn>
 struct C128Cfg {
-  static constexpr int CS = sizeof(TIn) == 2 ? 128 : 64;          // channels per tile
-  static constexpr int QUADS = CS / 4;                            // 4 channels per thread
-  static constexpr int THREADS = QUADS * 8;                       // 8 entry groups
+  static constexpr int CS = sizeof(TIn) == 2 ? 128 : 64;                // channels per tile
+  static constexpr int QUADS = CS / 4;                                  // 4 channels per thread
+  static constexpr int CONSUMERS = QUADS * 8;                           // 8 entry groups
   static constexpr int SEG_BYTES = CS * static_cast<int>(sizeof(TIn));  // one entry's kv (or score) slice
-  static constexpr int TILE_BYTES = 128 * SEG_BYTES * 2;          // 64 KB
-  static constexpr int RED_BYTES = 2 * 8 * CS * 4;                // group partials (l, a)
-  static constexpr int SMEM_BYTES = TILE_BYTES + RED_BYTES;
+  static constexpr int TILE_BYTES = 128 * SEG_BYTES * 2;                // 64 KB
+  static constexpr int RED_FLOATS = 2 * 8 * CS;                         // group partials (l, a)
+  static constexpr int STAGES = 3;                                      // prefill ring depth
+  static constexpr int PREFILL_THREADS = CONSUMERS + 32;                // + one producer warp
+  static constexpr int PREFILL_SMEM = STAGES * TILE_BYTES + 2 * RED_FLOATS * 4;
+  static constexpr int DECODE_SMEM = TILE_BYTES + RED_FLOATS * 4;
 };
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any real copy
 
 // ---------------------------------------------------------------- TMA / mbarrier
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -42,12 +61,17 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -68,7 +92,7 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Waits for phase `parity` of the barrier for at most `limit_ns` nanoseconds.
+// Waits for the phase of parity `parity` to complete, for at most `limit_ns`.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
@@ -87,9 +111,42 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any real copy
+// One 2-D tensor-map box (x = column, y = row) -> shared memory.
+__device__ __forceinline__ void tma_box_g2s(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
 
-// 4 consecutive channels of a staged entry / of ape as fp32.
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Barrier among the consumer warps only (the producer warp does not take part).
+template <int N>
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
+}
+
+// The same barrier, returning the OR of `pred` over the consumer threads, so
+// that every consumer takes the same decision.
+template <int N>
+__device__ __forceinline__ bool consumer_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "n"(N)
+      : "memory");
+  return r != 0;
+}
+
+// ---------------------------------------------------------------- element helpers
 template <typename TIn>
 __device__ __forceinline__ void load4(const TIn* p, float (&v)[4]);
 
@@ -143,27 +200,259 @@ __device__ __forceinline__ void store1<__nv_bfloat16>(__nv_bfloat16* p, float v)
   *p = __float2bfloat16_rn(v);
 }
 
-// Zero rows [r0, r1) of out, columns [c0, c0 + CS).
-template <typename TIn, typename TOut>
-__device__ __forceinline__ void zero_rows(TOut* out, int hd, int c0, int64_t r0, int64_t r1) {
-  using Cfg = C128Cfg<TIn>;
-  constexpr int kPerRow = Cfg::CS * static_cast<int>(sizeof(TOut)) / 16;
+// Zero rows [r0, r1) of out, columns [c0, c0 + CS), with NT threads.
+template <typename TIn, typename TOut, int NT>
+__device__ __forceinline__ void zero_rows(TOut* out, int hd, int c0, int64_t r0, int64_t r1, int t) {
+  constexpr int kPerRow = C128Cfg<TIn>::CS * static_cast<int>(sizeof(TOut)) / 16;
   constexpr int kElems = 16 / static_cast<int>(sizeof(TOut));
   const int64_t total = (r1 - r0) * kPerRow;
-  for (int64_t idx = threadIdx.x; idx < total; idx += Cfg::THREADS) {
+  for (int64_t idx = t; idx < total; idx += NT) {
     const int64_t r = r0 + idx / kPerRow;
     const int c = c0 + static_cast<int>(idx % kPerRow) * kElems;
     st16(out + r * hd + c, make_uint4(0, 0, 0, 0));
   }
 }
 
-// The C128 pooling kernel.  kDecode: tiles are (batch row, slice) of a decode
-// step; otherwise (compress record, slice) of a prefill step.
-template <typename TIn, typename TOut, bool kDecode>
-__global__ __launch_bounds__(C128Cfg<TIn>::THREADS, 2) void c128_pool_kernel(const PoolArgs a, uint32_t slices,
-                                                                               uint32_t tiles) {
+// ---------------------------------------------------------------- the per-thread arithmetic
+// Thread (q, g) owns channels cq = 4q .. 4q+3 of the tile and entries
+// 16g .. 16g+15.  ape_at(k, v) yields ape[16g + k][c0 + cq + 0..3] as fp32.
+template <typename TIn, int CS, typename ApeAt>
+__device__ __forceinline__ void c128_pass1(const TIn* sc_s, int g, int cq, ApeAt ape_at, float (&s)[16][4],
+                                           float (&m)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) m[j] = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    float sc[4], bias[4];
+    load4<TIn>(sc_s + (16 * g + k) * CS + cq, sc);
+    ape_at(k, bias);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      s[k][j] = score_plus_bias(sc[j], bias[j]);
+      m[j] = fmaxf(m[j], s[k][j]);
+    }
+  }
+}
+
+template <typename TIn, int CS>
+__device__ __forceinline__ void c128_pass2(const TIn* kv_s, int g, int cq, const float (&s)[16][4],
+                                           const float (&nml)[4], PoolAcc (&acc)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j].init();
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    float kv[4];
+    load4<TIn>(kv_s + (16 * g + k) * CS + cq, kv);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j].add(kv[j], weight_of(s[k][j], nml[j]));
+  }
+}
+
+// Channel maximum over the 8 groups' partial maxima (exact in any order).
+template <int CS>
+__device__ __forceinline__ void c128_nml(const float* red_m, int cq, float (&nml)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float mm = red_m[cq + j];
+#pragma unroll
+    for (int gg = 1; gg < 8; ++gg) mm = fmaxf(mm, red_m[gg * CS + cq + j]);
+    nml[j] = neg_max_log2e(mm);
+  }
+}
+
+template <typename TIn>
+__device__ __forceinline__ void load_ape_regs(const TIn* ape, int hd, int c0, int g, int cq, float (&ape_r)[16][4]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) ldg4<TIn>(ape + static_cast<size_t>(16 * g + k) * hd + c0 + cq, ape_r[k]);
+}
+
+// Issues the 256 bulk copies of one tile (called by all 32 lanes of a warp).
+template <typename TIn>
+__device__ __forceinline__ void issue_tile(TIn* kv_s, const TIn* state, const TIn* input, size_t width, int hd,
+                                           int c0, uint32_t ragged, int bl, int64_t rp0, uint32_t bar, int lane) {
   using Cfg = C128Cfg<TIn>;
   constexpr int CS = Cfg::CS;
+  TIn* sc_s = kv_s + 128 * CS;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = lane + 32 * k;
+    const TIn* row = i < bl ? state + (static_cast<size_t>(rp0) * 128 + i) * width
+                            : input + (static_cast<size_t>(ragged) + i - 127) * width;
+    bulk_g2s(smem_addr(kv_s + i * CS), row + c0, Cfg::SEG_BYTES, bar);
+    bulk_g2s(smem_addr(sc_s + i * CS), row + hd + c0, Cfg::SEG_BYTES, bar);
+  }
+}
+
+// Decodes and bounds-checks prefill record e.  Invalid (padding) records and
+// records that point outside the state / input return false.
+__device__ __forceinline__ bool prefill_record(const PoolArgs& a, uint32_t e, uint32_t& ragged, int& bl,
+                                               int64_t& rp0, bool& bad) {
+  const ckv_compress_plan_t P = load_plan_c(a.plan_c + e);
+  bad = false;
+  if (plan_c_invalid(P)) return false;
+  ragged = P.ragged_bl & CKV_RAGGED_MASK;
+  bl = static_cast<int>(P.ragged_bl >> CKV_BUFFER_LEN_SHIFT);
+  rp0 = P.read_page_0;
+  bool ok = ragged < a.num_q_tokens && bl <= 127 && static_cast<int64_t>(ragged) - 127 + bl >= 0;
+  if (bl > 0) ok = ok && rp0 >= 0 && static_cast<uint64_t>(rp0) * 128 + 127 < a.state_rows;
+  bad = !ok;
+  return ok;
+}
+
+// ---------------------------------------------------------------- prefill (persistent)
+template <typename TIn, typename TOut>
+__global__ __launch_bounds__(C128Cfg<TIn>::PREFILL_THREADS, 1) void c128_prefill_kernel(
+    const PoolArgs a, uint32_t slices, const __grid_constant__ CUtensorMap in_map) {
+  using Cfg = C128Cfg<TIn>;
+  constexpr int CS = Cfg::CS;
+  constexpr int NC = Cfg::CONSUMERS;
+  constexpr int NS = Cfg::STAGES;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[NS];
+  __shared__ __align__(8) uint64_t empty_bar[NS];
+  __shared__ volatile int abort_flag;
+  float* red_base = reinterpret_cast<float*>(smem + NS * Cfg::TILE_BYTES);
+
+  const int t = threadIdx.x;
+  const int warp = t >> 5;
+  const int lane = t & 31;
+  const uint32_t slice = blockIdx.x % slices;
+  const uint32_t first = blockIdx.x / slices;
+  const uint32_t stride = gridDim.x / slices;
+  const int c0 = static_cast<int>(slice) * CS;
+  const int hd = a.head_dim;
+  const size_t width = 2 * static_cast<size_t>(hd);
+  const TIn* input = static_cast<const TIn*>(a.input);
+  const TIn* state = static_cast<const TIn*>(a.state);
+  TOut* out = static_cast<TOut*>(a.out);
+  const bool token = a.out_layout == CKV_OUT_TOKEN;
+  const uint32_t num_c = count_or_capacity(a.d_counts, 0, a.capacity);
+
+  if (t == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), NC / 32);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == NC / 32) {
+    // ---------------- producer warp
+    if (lane == 0) prefetch_map(&in_map);
+    uint32_t n = 0;
+    for (uint32_t e = first; e < num_c; e += stride, ++n) {
+      const int stage = static_cast<int>(n % NS);
+      const uint32_t phase = (n / NS) & 1u;
+      if (!mbar_wait_bounded(smem_addr(&empty_bar[stage]), phase ^ 1u, kWaitLimitNs)) {
+        if (lane == 0) {
+          status_or(a.d_status, CKV_STATUS_TIMEOUT);
+          abort_flag = 1;
+        }
+        break;
+      }
+      if (abort_flag) break;
+      uint32_t ragged = 0;
+      int bl = 0;
+      int64_t rp0 = 0;
+      bool bad;
+      const bool ok = prefill_record(a, e, ragged, bl, rp0, bad);
+      if (bad && lane == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+      const uint32_t bar = smem_addr(&full_bar[stage]);
+      if (lane == 0) mbar_arrive_expect_tx(bar, ok ? Cfg::TILE_BYTES : 0u);
+      __syncwarp();
+      if (ok) {
+        TIn* kv_s = reinterpret_cast<TIn*>(smem + stage * Cfg::TILE_BYTES);
+        if (bl == 0) {  // rows ragged-127 .. ragged of the input: two boxes
+          if (lane == 0) {
+            tma_box_g2s(smem_addr(kv_s), &in_map, c0, static_cast<int>(ragged) - 127, bar);
+            tma_box_g2s(smem_addr(kv_s + 128 * CS), &in_map, hd + c0, static_cast<int>(ragged) - 127, bar);
+          }
+        } else {
+          issue_tile<TIn>(kv_s, state, input, width, hd, c0, ragged, bl, rp0, bar, lane);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumer warps
+  const int q = t % Cfg::QUADS;
+  const int g = t / Cfg::QUADS;
+  const int cq = 4 * q;
+  float ape_r[16][4];
+  load_ape_regs<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
+  uint32_t n = 0;
+  for (uint32_t e = first; e < num_c; e += stride, ++n) {
+    // one decision for all consumers (also orders the reuse of the reduction buffers)
+    if (consumer_any<NC>(abort_flag != 0)) break;
+    const int stage = static_cast<int>(n % NS);
+    const uint32_t phase = (n / NS) & 1u;
+    if (!mbar_wait_bounded(smem_addr(&full_bar[stage]), phase, kWaitLimitNs)) {
+      status_or(a.d_status, CKV_STATUS_TIMEOUT);
+      abort_flag = 1;
+    }
+    uint32_t ragged = 0;
+    int bl = 0;
+    int64_t rp0 = 0;
+    bool bad;
+    const bool ok = prefill_record(a, e, ragged, bl, rp0, bad);
+    float* red_l = red_base + (n & 1u) * Cfg::RED_FLOATS;
+    float* red_a = red_l + 8 * CS;
+    PoolAcc acc[4];
+    if (ok) {
+      const TIn* kv_s = reinterpret_cast<const TIn*>(smem + stage * Cfg::TILE_BYTES);
+      const TIn* sc_s = kv_s + 128 * CS;
+      float s[16][4], m[4], nml[4];
+      c128_pass1<TIn, CS>(sc_s, g, cq,
+                          [&](int k, float (&v)[4]) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) v[j] = ape_r[k][j];
+                          },
+                          s, m);
+      *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(m[0], m[1], m[2], m[3]);
+      consumer_sync<NC>();
+      c128_nml<CS>(red_l, cq, nml);
+      consumer_sync<NC>();
+      c128_pass2<TIn, CS>(kv_s, g, cq, s, nml, acc);
+      *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(acc[0].l, acc[1].l, acc[2].l, acc[3].l);
+      *reinterpret_cast<float4*>(red_a + g * CS + cq) = make_float4(acc[0].a, acc[1].a, acc[2].a, acc[3].a);
+      consumer_sync<NC>();
+    }
+    // the stage is no longer read: hand it back to the producer
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
+    if (ok) {
+      const size_t orow = token ? ragged : e;
+      if (t < CS) store1<TOut>(out + orow * hd + c0 + t, finish(tree8(red_a + t, CS), tree8(red_l + t, CS)));
+      if (token) {  // rows between the previous compress row and this one
+        int64_t prev = -1;
+        if (e > 0) {
+          const ckv_compress_plan_t Q = load_plan_c(a.plan_c + e - 1);
+          prev = plan_c_invalid(Q) ? static_cast<int64_t>(ragged) : static_cast<int64_t>(Q.ragged_bl & CKV_RAGGED_MASK);
+        }
+        zero_rows<TIn, TOut, NC>(out, hd, c0, prev + 1, ragged, t);
+      }
+    }
+  }
+  if (token && first == 0) {  // rows after the last compress row (and all rows when there is none)
+    int64_t last = -1;
+    if (num_c > 0) {
+      const ckv_compress_plan_t Q = load_plan_c(a.plan_c + num_c - 1);
+      last = plan_c_invalid(Q) ? static_cast<int64_t>(a.num_q_tokens) : static_cast<int64_t>(Q.ragged_bl & CKV_RAGGED_MASK);
+    }
+    zero_rows<TIn, TOut, NC>(out, hd, c0, last + 1, a.num_q_tokens, t);
+  }
+}
+
+// ---------------------------------------------------------------- decode (one tile per CTA)
+template <typename TIn, typename TOut>
+__global__ __launch_bounds__(C128Cfg<TIn>::CONSUMERS, 2) void c128_decode_kernel(
+    const PoolArgs a, uint32_t slices, uint32_t tiles, const __grid_constant__ CUtensorMap page_map) {
+  using Cfg = C128Cfg<TIn>;
+  constexpr int CS = Cfg::CS;
+  constexpr int NT = Cfg::CONSUMERS;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bar_storage;
   TIn* kv_s = reinterpret_cast<TIn*>(smem);
@@ -173,193 +462,184 @@ __global__ __launch_bounds__(C128Cfg<TIn>::THREADS, 2) void c128_pool_kernel(con
 
   const uint32_t tile = blockIdx.x;
   if (tile >= tiles) return;
-  const uint32_t e = tile / slices;
+  const uint32_t b = tile / slices;
   const int c0 = static_cast<int>(tile % slices) * CS;
   const int hd = a.head_dim;
   const size_t width = 2 * static_cast<size_t>(hd);
   const int t = threadIdx.x;
   const TIn* input = static_cast<const TIn*>(a.input);
-  const TIn* state = kDecode ? static_cast<const TIn*>(a.state_mut) : static_cast<const TIn*>(a.state);
+  TIn* state = static_cast<TIn*>(a.state_mut);
   TOut* out = static_cast<TOut*>(a.out);
 
-  uint32_t ragged;
-  int bl;
-  int64_t rp0;
-  size_t orow;
-  if constexpr (kDecode) {
-    const ckv_decode_plan_t P = load_plan_d(a.plan_d + e);
-    orow = e;
-    if (P.seq_len == kInvalidU32) {
-      zero_rows<TIn, TOut>(out, hd, c0, e, e + 1);
-      return;
-    }
-    const bool boundary = P.seq_len % 128 == 0;
-    rp0 = P.read_page_0;
-    bool ok = P.write_loc >= 0 && static_cast<uint64_t>(P.write_loc) < a.state_rows;
-    if (boundary) ok = ok && rp0 >= 0 && static_cast<uint64_t>(rp0) * 128 + 127 < a.state_rows;
-    if (!ok) {
-      if (t == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
-      zero_rows<TIn, TOut>(out, hd, c0, e, e + 1);
-      return;
-    }
-    // the new token's slice of kv and score goes to its page slot
-    if (t < 2 * Cfg::SEG_BYTES / 16) {
-      const int half = t / (Cfg::SEG_BYTES / 16);
-      const int off = (t % (Cfg::SEG_BYTES / 16)) * (16 / static_cast<int>(sizeof(TIn)));
-      const TIn* src = input + static_cast<size_t>(e) * width + half * hd + c0 + off;
-      TIn* dst = static_cast<TIn*>(a.state_mut) + static_cast<size_t>(P.write_loc) * width + half * hd + c0 + off;
-      st16(dst, ld_stream16(src));
-    }
-    if (!boundary) {
-      zero_rows<TIn, TOut>(out, hd, c0, e, e + 1);
-      return;
-    }
-    ragged = e;
-    bl = 127;
-  } else {
-    const uint32_t num_c = count_or_capacity(a.d_counts, 0, a.capacity);
-    const bool token = a.out_layout == CKV_OUT_TOKEN;
-    if (e >= num_c) {
-      if (token && e == num_c) {  // rows after the last compress row
-        int64_t last = -1;
-        if (num_c > 0) {
-          const ckv_compress_plan_t Q = load_plan_c(a.plan_c + num_c - 1);
-          last = plan_c_invalid(Q) ? static_cast<int64_t>(a.num_q_tokens)
-                                   : static_cast<int64_t>(Q.ragged_bl & CKV_RAGGED_MASK);
-        }
-        zero_rows<TIn, TOut>(out, hd, c0, last + 1, a.num_q_tokens);
-      }
-      return;
-    }
-    const ckv_compress_plan_t P = load_plan_c(a.plan_c + e);
-    if (plan_c_invalid(P)) return;
-    ragged = P.ragged_bl & CKV_RAGGED_MASK;
-    bl = static_cast<int>(P.ragged_bl >> CKV_BUFFER_LEN_SHIFT);
-    rp0 = P.read_page_0;
-    bool ok = ragged < a.num_q_tokens && bl <= 127 && static_cast<int64_t>(ragged) - 127 + bl >= 0;
-    if (bl > 0) ok = ok && rp0 >= 0 && static_cast<uint64_t>(rp0) * 128 + 127 < a.state_rows;
-    if (!ok) {
-      if (t == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
-      return;
-    }
-    orow = token ? ragged : e;
-    if (token) {  // rows between the previous compress row and this one
-      int64_t prev = -1;
-      if (e > 0) {
-        const ckv_compress_plan_t Q = load_plan_c(a.plan_c + e - 1);
-        prev = plan_c_invalid(Q) ? static_cast<int64_t>(ragged) : static_cast<int64_t>(Q.ragged_bl & CKV_RAGGED_MASK);
-      }
-      zero_rows<TIn, TOut>(out, hd, c0, prev + 1, ragged);
-    }
+  const ckv_decode_plan_t P = load_plan_d(a.plan_d + b);
+  if (P.seq_len == kInvalidU32) {
+    zero_rows<TIn, TOut, NT>(out, hd, c0, b, b + 1, t);
+    return;
   }
-
-  // ---- stage the tile: 128 entries x (kv slice, score slice)
+  const bool boundary = P.seq_len % 128 == 0;
+  const int64_t rp0 = P.read_page_0;
+  bool ok = P.write_loc >= 0 && static_cast<uint64_t>(P.write_loc) < a.state_rows;
+  if (boundary) ok = ok && rp0 >= 0 && static_cast<uint64_t>(rp0) * 128 + 127 < a.state_rows;
+  if (!ok) {
+    if (t == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+    zero_rows<TIn, TOut, NT>(out, hd, c0, b, b + 1, t);
+    return;
+  }
+  // the new token's slice of kv and score goes to its page slot
+  if (t < 2 * Cfg::SEG_BYTES / 16) {
+    const int half = t / (Cfg::SEG_BYTES / 16);
+    const int off = (t % (Cfg::SEG_BYTES / 16)) * (16 / static_cast<int>(sizeof(TIn)));
+    const TIn* src = input + static_cast<size_t>(b) * width + half * hd + c0 + off;
+    TIn* dst = state + static_cast<size_t>(P.write_loc) * width + half * hd + c0 + off;
+    st16(dst, ld_stream16(src));
+  }
+  if (!boundary) {
+    zero_rows<TIn, TOut, NT>(out, hd, c0, b, b + 1, t);
+    return;
+  }
+  // entries 0..126 from the page (the slot being written is entry 127), entry 127 = the new token
   const uint32_t bar = smem_addr(&bar_storage);
-  if (t == 0) mbar_init(bar, 1);
-  __syncthreads();
-  if (t < 32) {
-    if (t == 0) mbar_arrive_expect_tx(bar, Cfg::TILE_BYTES);
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = t + 32 * k;
-      const TIn* row = i < bl ? state + (static_cast<size_t>(rp0) * 128 + i) * width
-                              : input + (static_cast<size_t>(ragged) + i - 127) * width;
-      bulk_g2s(smem_addr(kv_s + i * CS), row + c0, Cfg::SEG_BYTES, bar);
-      bulk_g2s(smem_addr(sc_s + i * CS), row + hd + c0, Cfg::SEG_BYTES, bar);
-    }
+  if (t == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
   }
+  __syncthreads();
+  if (t == 0) {
+    // slots 0..126 of the page: one 127-row box each for kv and score; the new
+    // token (entry 127) comes straight from its input row
+    mbar_arrive_expect_tx(bar, Cfg::TILE_BYTES);
+    const int y = static_cast<int>(rp0 * 128);
+    tma_box_g2s(smem_addr(kv_s), &page_map, c0, y, bar);
+    tma_box_g2s(smem_addr(sc_s), &page_map, hd + c0, y, bar);
+    const TIn* row = input + static_cast<size_t>(b) * width;
+    bulk_g2s(smem_addr(kv_s + 127 * CS), row + c0, Cfg::SEG_BYTES, bar);
+    bulk_g2s(smem_addr(sc_s + 127 * CS), row + hd + c0, Cfg::SEG_BYTES, bar);
+  }
+  const int q = t % Cfg::QUADS;
+  const int g = t / Cfg::QUADS;
+  const int cq = 4 * q;
+  const TIn* ape = static_cast<const TIn*>(a.ape) + static_cast<size_t>(16 * g) * hd + c0 + cq;
   if (!mbar_wait_bounded(bar, 0, kWaitLimitNs)) {
     status_or(a.d_status, CKV_STATUS_TIMEOUT);
     mbar_wait_bounded(bar, 0, kWaitLimitNs);  // let copies in flight land before the CTA can exit
   }
-
-  // ---- pass 1: scores and the per-channel maximum
-  const int q = t % Cfg::QUADS;
-  const int g = t / Cfg::QUADS;
-  const int cq = 4 * q;
-  const TIn* ape = static_cast<const TIn*>(a.ape) + c0 + cq;
-  float s[16][4];
-  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const int i = 16 * g + k;
-    float sc[4], bias[4];
-    load4<TIn>(sc_s + i * CS + cq, sc);
-    ldg4<TIn>(ape + static_cast<size_t>(i) * hd, bias);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      s[k][j] = score_plus_bias(sc[j], bias[j]);
-      m[j] = fmaxf(m[j], s[k][j]);
-    }
-  }
+  float s[16][4], m[4], nml[4];
+  c128_pass1<TIn, CS>(sc_s, g, cq, [&](int k, float (&v)[4]) { ldg4<TIn>(ape + static_cast<size_t>(k) * hd, v); },
+                      s, m);
   *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(m[0], m[1], m[2], m[3]);
   __syncthreads();
-  float nml[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float mm = red_l[cq + j];
-#pragma unroll
-    for (int gg = 1; gg < 8; ++gg) mm = fmaxf(mm, red_l[gg * CS + cq + j]);
-    nml[j] = neg_max_log2e(mm);
-  }
+  c128_nml<CS>(red_l, cq, nml);
   __syncthreads();
-
-  // ---- pass 2: group sums of weights and of weighted kv
   PoolAcc acc[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j].init();
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const int i = 16 * g + k;
-    float kv[4];
-    load4<TIn>(kv_s + i * CS + cq, kv);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j].add(kv[j], weight_of(s[k][j], nml[j]));
-  }
+  c128_pass2<TIn, CS>(kv_s, g, cq, s, nml, acc);
   *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(acc[0].l, acc[1].l, acc[2].l, acc[3].l);
   *reinterpret_cast<float4*>(red_a + g * CS + cq) = make_float4(acc[0].a, acc[1].a, acc[2].a, acc[3].a);
   __syncthreads();
-
-  // ---- pass 3: tree over the 8 groups, one channel per thread
-  if (t < CS) {
-    const float L = tree8(red_l + t, CS);
-    const float A = tree8(red_a + t, CS);
-    store1<TOut>(out + orow * hd + c0 + t, finish(A, L));
-  }
+  if (t < CS) store1<TOut>(out + static_cast<size_t>(b) * hd + c0 + t, finish(tree8(red_a + t, CS), tree8(red_l + t, CS)));
 }
 
-template <typename TIn, typename TOut, bool kDecode>
-int launch_t(const PoolArgs& a, cudaStream_t s) {
-  using Cfg = C128Cfg<TIn>;
-  const uint32_t slices = static_cast<uint32_t>(a.head_dim / Cfg::CS);
-  const uint64_t items = kDecode ? a.capacity
-                                 : static_cast<uint64_t>(a.capacity) + (a.out_layout == CKV_OUT_TOKEN ? 1 : 0);
-  const uint64_t tiles64 = items * slices;
-  if (tiles64 == 0) return CKV_OK;
-  if (tiles64 > 0x7FFFFFFFull) return CKV_ERR_SIZE;
-  // The dynamic shared-memory opt-in is a per-device function attribute.
-  static bool configured[64] = {};
+// ---------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// A [rows, cols] row-major tensor read in boxes of [box_rows, box_cols].
+int make_map(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uint64_t rows, uint32_t box_cols,
+             uint32_t box_rows) {
+  EncodeTiledFn fn = encoder();
+  if (fn == nullptr) return CKV_ERR_LAUNCH;
+  const uint64_t esz = dtype == CKV_BF16 ? 2 : 4;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * esz};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, dtype == CKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CKV_OK : CKV_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------- launchers
+template <typename K>
+int opt_in_smem(K kernel, int bytes, bool* configured) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CKV_ERR_LAUNCH;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    if (cudaFuncSetAttribute(c128_pool_kernel<TIn, TOut, kDecode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
       return CKV_ERR_LAUNCH;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
+  return CKV_OK;
+}
+
+template <typename TIn, typename TOut>
+int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
+  using Cfg = C128Cfg<TIn>;
+  const uint32_t slices = static_cast<uint32_t>(a.head_dim / Cfg::CS);
+  const bool token = a.out_layout == CKV_OUT_TOKEN;
+  if (a.capacity == 0 && !(token && a.num_q_tokens > 0)) return CKV_OK;
+  static bool configured[64] = {};
+  int rc = opt_in_smem(c128_prefill_kernel<TIn, TOut>, Cfg::PREFILL_SMEM, configured);
+  if (rc) return rc;
+  // one persistent CTA per SM; every CTA serves one channel slice
+  const uint32_t per_slice = std::max<uint32_t>(
+      1, std::min<uint32_t>(static_cast<uint32_t>(sm_count()) / slices, std::max<uint32_t>(a.capacity, 1)));
+  alignas(64) CUtensorMap in_map;
+  memset(&in_map, 0, sizeof in_map);
+  if (a.num_q_tokens > 0) {
+    rc = make_map(&in_map, a.input, a.in_dtype, 2ull * a.head_dim, a.num_q_tokens, Cfg::CS, 128);
+    if (rc) return rc;
+  }
+  c128_prefill_kernel<TIn, TOut><<<per_slice * slices, Cfg::PREFILL_THREADS, Cfg::PREFILL_SMEM, s>>>(a, slices,
+                                                                                                    in_map);
+  return check_launch();
+}
+
+template <typename TIn, typename TOut>
+int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
+  using Cfg = C128Cfg<TIn>;
+  const uint32_t slices = static_cast<uint32_t>(a.head_dim / Cfg::CS);
+  const uint64_t tiles64 = static_cast<uint64_t>(a.capacity) * slices;
+  if (tiles64 == 0) return CKV_OK;
+  if (tiles64 > 0x7FFFFFFFull) return CKV_ERR_SIZE;
+  static bool configured[64] = {};
+  int rc = opt_in_smem(c128_decode_kernel<TIn, TOut>, Cfg::DECODE_SMEM, configured);
+  if (rc) return rc;
+  if (a.state_rows == 0 || a.state_rows > 0x7FFFFFFFull) return CKV_ERR_SIZE;
+  alignas(64) CUtensorMap page_map;
+  rc = make_map(&page_map, a.state_mut, a.in_dtype, 2ull * a.head_dim, a.state_rows, Cfg::CS, 127);
+  if (rc) return rc;
   const uint32_t tiles = static_cast<uint32_t>(tiles64);
-  c128_pool_kernel<TIn, TOut, kDecode><<<tiles, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(a, slices, tiles);
+  c128_decode_kernel<TIn, TOut><<<tiles, Cfg::CONSUMERS, Cfg::DECODE_SMEM, s>>>(a, slices, tiles, page_map);
   return check_launch();
 }
 
 template <bool kDecode>
 int dispatch(const PoolArgs& a, cudaStream_t s) {
-  if (a.in_dtype == CKV_BF16)
-    return a.out_dtype == CKV_BF16 ? launch_t<__nv_bfloat16, __nv_bfloat16, kDecode>(a, s)
-                                   : launch_t<__nv_bfloat16, float, kDecode>(a, s);
-  return a.out_dtype == CKV_BF16 ? launch_t<float, __nv_bfloat16, kDecode>(a, s)
-                                 : launch_t<float, float, kDecode>(a, s);
+  if (a.in_dtype == CKV_BF16) {
+    if (a.out_dtype == CKV_BF16)
+      return kDecode ? launch_decode_t<__nv_bfloat16, __nv_bfloat16>(a, s)
+                     : launch_prefill_t<__nv_bfloat16, __nv_bfloat16>(a, s);
+    return kDecode ? launch_decode_t<__nv_bfloat16, float>(a, s) : launch_prefill_t<__nv_bfloat16, float>(a, s);
+  }
+  if (a.out_dtype == CKV_BF16)
+    return kDecode ? launch_decode_t<float, __nv_bfloat16>(a, s) : launch_prefill_t<float, __nv_bfloat16>(a, s);
+  return kDecode ? launch_decode_t<float, float>(a, s) : launch_prefill_t<float, float>(a, s);
 }
 
 }  // namespace

@@ -10,8 +10,8 @@
 // score = -1e9 there, which gives them weight exactly 0).
 //
 // Mapping: a "unit" is (event, 16-byte chunk of channels).  A thread owns one
-// chunk (8 bf16 or 4 fp32 channels) for the whole grid-stride loop, so its
-// slice of ape stays in registers; per event it issues 16 independent 16-byte
+// chunk (8 bf16 or 4 fp32 channels) for the whole grid-stride loop, so the
+// ape slice it reads stays in L1; per event it issues 16 independent 16-byte
 // loads (kv and score of 8 entries) before any arithmetic.  The window is
 // small enough that the fp32 safe softmax runs entirely in registers.
 #include <algorithm>
@@ -54,7 +54,7 @@ __device__ __forceinline__ void c4_pool_chunk(const uint4 (&kv)[8], const uint4 
 }
 
 template <typename TIn, typename TOut>
-__global__ __launch_bounds__(kC4Threads) void c4_pool_prefill_kernel(const PoolArgs a, uint32_t chunks,
+__global__ __launch_bounds__(kC4Threads, 2) void c4_pool_prefill_kernel(const PoolArgs a, uint32_t chunks,
                                                                      uint32_t units) {
   constexpr int VEC = C4Vec<TIn>::VEC;
   const int hd = a.head_dim;
@@ -69,10 +69,6 @@ __global__ __launch_bounds__(kC4Threads) void c4_pool_prefill_kernel(const PoolA
   const uint32_t stride = gridDim.x * blockDim.x;  // a multiple of `chunks`
   const uint32_t ch = gid % chunks;
   const int c0 = static_cast<int>(ch) * VEC;
-
-  uint4 ap[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) ap[i] = ld_cached16(ape + static_cast<size_t>(i) * hd + c0);
 
   const uint32_t num_c = count_or_capacity(a.d_counts, 0, a.capacity);
   for (uint32_t u = gid; u < units; u += stride) {
@@ -91,7 +87,7 @@ __global__ __launch_bounds__(kC4Threads) void c4_pool_prefill_kernel(const PoolA
         if (ch == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
         continue;
       }
-      uint4 kv[8], sc[8];
+      uint4 kv[8], sc[8], ap[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (i < first) {
@@ -103,6 +99,8 @@ __global__ __launch_bounds__(kC4Threads) void c4_pool_prefill_kernel(const PoolA
         kv[i] = ld_stream16(row + (i < 4 ? 0 : hd) + c0);
         sc[i] = ld_stream16(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ap[i] = ld_cached16(ape + static_cast<size_t>(i) * hd + c0);  // L1-resident
       float res[VEC];
       c4_pool_chunk<TIn, VEC>(kv, sc, ap, first, res);
       const size_t orow = token ? ragged : e;

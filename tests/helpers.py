@@ -217,18 +217,30 @@ def window_kv_absmax(ratio, hd, state, inp, seq_len, ragged, bl, rp0, rp1):
 
 
 def assert_pool_close(got: np.ndarray, want: np.ndarray, out_code: int, kvmax: np.ndarray = None, what=""):
-    """The parity bar: fp32 outputs within 2e-6 * max|kv| of the window (per
-    channel); bf16 outputs within 1 ulp (ordered-integer distance of the bits)."""
+    """The parity bar.  fp32 outputs: |got - want| <= 2e-6 * max|kv| of the
+    window, per channel.  bf16 outputs: at most 1 ulp apart (ordered-integer
+    distance of the bit patterns) -- except where the output is so much smaller
+    than its window's kv that the fp32 accumulation error alone exceeds a bf16
+    ulp of it (cancellation, e.g. an output of 1e-5 from kv values of ~2); there
+    the fp32 bar applies to the bf16 values."""
     assert got.shape == want.shape, (got.shape, want.shape, what)
     if out_code == 1:
         d = ulp_distance(got, want)
-        assert d.max(initial=0) <= 1, f"{what}: bf16 ulp distance {d.max()}"
+        err = np.abs(bf16_to_f32(got).astype(np.float64) - bf16_to_f32(want).astype(np.float64))
+        bad = (d > 1) & (err > 2e-6 * kvmax)
+        if bad.any():
+            k = tuple(np.argwhere(bad)[0])
+            raise AssertionError(f"{what}: {bad.sum()} bf16 values off by >1 ulp and > 2e-6 max|kv|; first at "
+                                 f"{k}: got {bf16_to_f32(got)[k]} want {bf16_to_f32(want)[k]} kvmax {kvmax[k]}")
     else:
         err = np.abs(got.astype(np.float64) - want.astype(np.float64))
         tol = 2e-6 * kvmax
         bad = err > tol
-        assert not bad.any(), f"{what}: {bad.sum()} channels over tolerance, worst err/kvmax " \
-                              f"{(err / np.maximum(kvmax, 1e-30)).max():.3e}"
+        if bad.any():
+            k = tuple(np.argwhere(bad)[0])
+            raise AssertionError(f"{what}: {bad.sum()} channels over tolerance, worst err/kvmax "
+                                 f"{(err / np.maximum(kvmax, 1e-30)).max():.3e}; first at {k}: got {got[k]} "
+                                 f"want {want[k]} kvmax {kvmax[k]}")
 
 
 class GpuBackend:
