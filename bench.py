@@ -15,8 +15,9 @@ on a page boundary), and the achieved HBM bandwidth of the dominant kernel
 Inputs live in HBM when the timed region starts.  Before every step (outside
 the timed region) the prefill state is restored from a pristine copy and L2
 is flushed by writing a buffer of twice its size.  Each step's four segments
-(plan_prefill | pool | write + plan_decode | decode) are CUDA graphs replayed
-between CUDA events on one stream.  ``e2e`` repeats the step through the same
+(plan_prefill | pool | write + plan_decode | decode) are captured in one CUDA
+graph with event-record nodes between them; per-kernel times are those GPU
+timestamps.  ``e2e`` repeats the step through the same
 API with the step's inputs copied from pinned host memory and its outputs
 copied back inside the timed region.
 
@@ -278,13 +279,61 @@ class DecodeRunner:
         self.state.copy_(self.pristine)
 
 
-def capture(fn):
-    fn()  # eager warm-up outside capture (sets function attributes, loads modules)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        fn()
-    return g
+_cudart = None
+
+
+def cudart():
+    """The CUDA runtime library this process already loaded (through torch)."""
+    global _cudart
+    if _cudart is None:
+        import ctypes
+
+        path = None
+        with open("/proc/self/maps") as f:
+            for line in f:
+                if "libcudart.so" in line:
+                    path = line.split()[-1]
+                    break
+        lib = ctypes.CDLL(path) if path else ctypes.CDLL("libcudart.so")
+        lib.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        lib.cudaEventRecordWithFlags.restype = ctypes.c_int
+        _cudart = lib
+    return _cudart
+
+
+class StepGraph:
+    """One CUDA graph for a whole step.  With inner_events the segments are
+    separated by event-record nodes, so per-kernel times are GPU timestamps of
+    one graph execution; without, only the whole step is bracketed and the
+    kernels overlap their launches through programmatic dependent launch."""
+
+    def __init__(self, segments, inner_events: bool = True):
+        if not inner_events:  # one timed segment: the kernels keep their programmatic launch edges
+            fns = [fn for _, fn in segments]
+            segments = [("step", lambda: [f() for f in fns])]
+        self.names = [n for n, _ in segments]
+        for _, fn in segments:  # eager warm-up outside capture (function attributes, modules)
+            fn()
+        self.evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(segments) + 1)]
+        for e in self.evs:
+            e.record()  # creates the underlying events
+        torch.cuda.synchronize()
+        lib = cudart()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            st = torch.cuda.current_stream().cuda_stream
+            rc = lib.cudaEventRecordWithFlags(self.evs[0].cuda_event, st, 1)  # cudaEventRecordExternal
+            for i, (_, fn) in enumerate(segments):
+                fn()
+                rc |= lib.cudaEventRecordWithFlags(self.evs[i + 1].cuda_event, st, 1)
+        if rc != 0:
+            raise RuntimeError("cudaEventRecordWithFlags failed during capture")
+
+    def replay(self):
+        self.graph.replay()
+
+    def times_ms(self):
+        return [self.evs[i].elapsed_time(self.evs[i + 1]) for i in range(len(self.names))]
 
 
 def l2_flush_buffer(dev):
@@ -292,34 +341,29 @@ def l2_flush_buffer(dev):
     return torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
 
 
-def run_segments(segs, flush, restore, steps, warmup, ws, sampler=None):
-    """segs: list of (name, graph).  Returns per-step segment times (ms)."""
-    n = len(segs)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+def run_graph(step: StepGraph, flush, restore, steps, warmup, ws, sampler=None):
+    """Per-step segment times (ms) of `steps` timed replays after `warmup` untimed ones."""
     for _ in range(warmup):
         restore()
         flush.zero_()
-        for _, g in segs:
-            g.replay()
+        step.replay()
     torch.cuda.synchronize()
     barrier(ws)
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
+    seg = []
     t0 = time.perf_counter()
-    for s in range(steps):
+    for _ in range(steps):
         restore()
         flush.zero_()
-        evs[s][0].record()
-        for i, (_, g) in enumerate(segs):
-            g.replay()
-            evs[s][i + 1].record()
-    torch.cuda.synchronize()
+        step.replay()
+        torch.cuda.synchronize()
+        seg.append(step.times_ms())
     wall = time.perf_counter() - t0
     barrier(ws)
     clocks = sampler.stop() if sampler else None
-    seg_ms = np.array([[evs[s][i].elapsed_time(evs[s][i + 1]) for i in range(n)] for s in range(steps)])
-    return seg_ms, wall, clocks
+    return np.array(seg), wall, clocks
 
 
 # ----------------------------------------------------------------------------- CPU baseline (oracle)
@@ -369,19 +413,20 @@ def bench_step(args, ws, rank, local):
     def restore():
         pre.restore()
 
-    g_plan = capture(pre.plan)
-    g_pool = capture(pre.pool)
-
     def write_and_plan_d():
         pre.write()
         dec.plan()
 
-    g_wp = capture(write_and_plan_d)
-    g_dec = capture(dec.decode)
-    segs = [("plan_prefill", g_plan), ("pool_prefill", g_pool), ("write+plan_decode", g_wp), ("decode", g_dec)]
+    segments = [("plan_prefill", pre.plan), ("pool_prefill", pre.pool), ("write+plan_decode", write_and_plan_d),
+                ("decode", dec.decode)]
+    step = StepGraph(segments, inner_events=False)
+    timed = StepGraph(segments, inner_events=True)
     launches_per_step = 5
     sampler = ClockSampler(local)
-    seg_ms, wall, clocks = run_segments(segs, flush, restore, args.steps, args.warmup, ws, sampler)
+    step_ms, wall, clocks = run_graph(step, flush, restore, args.steps, args.warmup, ws, sampler)
+    step_ms = step_ms[:, 0]
+    # per-kernel breakdown (event nodes between the kernels; not part of the headline)
+    seg_ms, _, _ = run_graph(timed, flush, restore, args.steps, args.warmup, ws)
     if int(pre.status[0]) or int(dec.status[0]):
         raise RuntimeError(f"device status set: prefill {int(pre.status[0])} decode {int(dec.status[0])}")
     b5 = algorithmic_bytes(w5)
@@ -389,7 +434,6 @@ def bench_step(args, ws, rank, local):
     nc = int(pre.counts[0])
     assert nc == b5["num_c"] and int(pre.counts[1]) == b5["num_w"], "plan counts differ from the closed forms"
     rows_per_step = b5["rows"] + b3["rows"]
-    step_ms = seg_ms.sum(1)
     total_s = float(step_ms.sum()) / 1e3
     total_s = max_over_ranks(total_s, ws)
     rows_all = sum_over_ranks(rows_per_step * args.steps, ws)
@@ -424,8 +468,7 @@ def bench_step(args, ws, rank, local):
         dec.kv.copy_(h_kv3, non_blocking=True)
         for d, h in zip((dec.rid, dec.sl), h_len3):
             d.copy_(h, non_blocking=True)
-        for _, g in segs:
-            g.replay()
+        step.replay()
         h_out5.copy_(pre.out[:nc], non_blocking=True)
         h_out3.copy_(dec.out[: w3.batch], non_blocking=True)
         e1.record()
@@ -453,6 +496,7 @@ def bench_step(args, ws, rank, local):
             "pool_prefill_us": pool_ms * 1e3, "pool_prefill_gbs": pool_gbs,
             "write_plus_plan_decode_us": float(seg_ms[:, 2].mean()) * 1e3,
             "decode_us": dec_ms * 1e3, "decode_gbs": dec_gbs, "decode_frac": dec_gbs / peak,
+            "sum_of_kernel_segments_us": float(seg_ms.sum(1).mean()) * 1e3,
             "step_gbs": step_bytes / (float(step_ms.mean()) * 1e-3) / 1e9},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * args.steps,
@@ -471,6 +515,16 @@ def bench_step(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def small_workload(name: str, seed: int) -> wl.Workload:
+    """Scaled-down variants for profiler captures: same shapes and mixes, fewer
+    long requests, inputs still larger than L2."""
+    if name == "c128_prefill":
+        return wl.c128_prefill(seed, num_long=16)
+    if name == "c4_prefill":
+        return wl.c4_prefill(seed, batch=16)
+    return wl.NAMED[name](seed)
+
+
 def bench_config(args, name, ws, rank, local):
     """One workload alone; prints one line (not the headline contract line)."""
     from compressed_kv_attention_compressplan_gb300 import build as B
@@ -479,30 +533,33 @@ def bench_config(args, name, ws, rank, local):
     B.build()
     ckv.load_library()
     dev = torch.device("cuda", local)
-    w = wl.NAMED[name](args.seed + rank)
+    w = small_workload(name, args.seed + rank) if args.small else wl.NAMED[name](args.seed + rank)
     flush = l2_flush_buffer(dev)
     b = algorithmic_bytes(w)
     if w.mode == "prefill":
         r = PrefillRunner(ckv, w, dev)
-        segs = [("plan_prefill", capture(r.plan)), ("pool_prefill", capture(r.pool)), ("write", capture(r.write))]
+        segs = [("plan_prefill", r.plan), ("pool_prefill", r.pool), ("write", r.write)]
         main_i, main_key = 1, "pool"
     else:
         r = DecodeRunner(ckv, w, dev)
-        segs = [("plan_decode", capture(r.plan)), ("decode", capture(r.decode))]
+        segs = [("plan_decode", r.plan), ("decode", r.decode)]
         main_i, main_key = 1, "decode"
-    seg_ms, wall, _ = run_segments(segs, flush, r.restore, args.steps, args.warmup, ws)
+    step = StepGraph(segs)
+    seg_ms, wall, _ = run_graph(step, flush, r.restore, args.steps, args.warmup, ws)
+    whole = StepGraph(segs, inner_events=False)
+    whole_ms, _, _ = run_graph(whole, flush, r.restore, args.steps, args.warmup, ws)
     if int(r.status[0]):
         raise RuntimeError(f"device status {int(r.status[0])}")
     peak, kind = peaks()
-    step_ms = seg_ms.sum(1)
+    step_ms = whole_ms[:, 0]
     main_ms = float(seg_ms[:, main_i].mean())
     gbs = b[main_key] / (main_ms * 1e-3) / 1e9
     line = {"workload": name, **w.describe(), "rows_per_step": b["rows"],
             "rows_per_s": b["rows"] / (float(step_ms.mean()) * 1e-3), "ms_per_step": float(step_ms.mean()),
             "step_gbs": b["total"] / (float(step_ms.mean()) * 1e-3) / 1e9,
-            "segments_us": {n: float(seg_ms[:, i].mean()) * 1e3 for i, (n, _) in enumerate(segs)},
-            "segments_us_min": {n: float(seg_ms[:, i].min()) * 1e3 for i, (n, _) in enumerate(segs)},
-            "main_kernel": segs[main_i][0], "main_bytes": b[main_key], "main_gbs": gbs, "main_frac": gbs / peak,
+            "segments_us": {n: float(seg_ms[:, i].mean()) * 1e3 for i, n in enumerate(step.names)},
+            "segments_us_min": {n: float(seg_ms[:, i].min()) * 1e3 for i, n in enumerate(step.names)},
+            "main_kernel": step.names[main_i], "main_bytes": b[main_key], "main_gbs": gbs, "main_frac": gbs / peak,
             "peak_gbs": peak, "peak_kind": kind, "algorithmic_bytes": b}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -547,6 +604,7 @@ def main():
     ap.add_argument("--config", default="step", help="step (default) | all | " + " | ".join(wl.NAMED))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true", help="with --config: scaled-down workloads for profiling")
     ap.add_argument("--ref-fraction", type=float, default=0.125,
                     help="share of the prefill compress records the reference arm pools per step")
     args = ap.parse_args()

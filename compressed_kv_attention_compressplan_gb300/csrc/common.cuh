@@ -13,7 +13,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ckv.h"
+#include "ckv.h"  // include/ (on the include path)
 
 namespace ckv {
 
@@ -25,6 +25,14 @@ constexpr int kMaxBatch = CKV_MAX_BATCH;
 // (see PoolAcc), so the rounding of -max*log2(e) is common to every entry of a
 // window and cancels in the normalised result.
 constexpr float kLog2e = 1.44269504088896340736f;
+
+// Programmatic dependent launch.  Every kernel is launched so that it may
+// start while its predecessor on the stream is still running: it first does
+// work that depends on nothing a predecessor writes, then pdl_wait() (which
+// returns once the preceding grid has completed and its memory is visible),
+// and it lets its own successor start launching with pdl_release().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void status_or(uint32_t* d_status, uint32_t bits) {
   if (d_status != nullptr) atomicOr(d_status, bits);

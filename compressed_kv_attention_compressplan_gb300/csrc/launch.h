@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ckv.h"
+#include "ckv.h"  // include/ (on the include path)
 
 namespace ckv {
 
@@ -40,5 +40,27 @@ int launch_c128_decode(const PoolArgs& a, cudaStream_t s);
 inline bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline int check_launch() { return cudaGetLastError() == cudaSuccess ? CKV_OK : CKV_ERR_LAUNCH; }
+
+// Launches `kernel` on `s` with programmatic stream serialisation allowed: the
+// grid may begin while the previous kernel on the stream finishes (the kernel
+// itself waits, with griddepcontrol.wait, before it touches dependent data).
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return CKV_ERR_LAUNCH;
+  }
+  return check_launch();
+}
 
 }  // namespace ckv

@@ -64,6 +64,8 @@ __device__ __forceinline__ uint32_t warp_min(uint32_t v) {
 
 __global__ void plan_decode_kernel(int ratio, const int64_t* __restrict__ rid, const int64_t* __restrict__ seq_lens,
                                    uint32_t batch, ckv_decode_plan_t* __restrict__ plan_d, uint32_t* d_status) {
+  pdl_wait();
+  pdl_release();
   const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
   const int64_t sl = seq_lens[b];
@@ -126,6 +128,8 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
   const int R = a.ratio;
   const int64_t slots = R == 4 ? 8 : 128;
   if (tid == 0) s_flags = 0;
+  pdl_wait();
+  pdl_release();
 
   uint32_t el_eff = 0, nc = 0, nw = 0;
   uint32_t el_min = kInvalidU32, el_max = 0;
@@ -305,9 +309,8 @@ int ckv_plan_decode(int ratio, const int64_t* rid, const int64_t* seq_lens, uint
   if (!rid || !seq_lens || !aligned16(plan_d)) return CKV_ERR_POINTER;
   if ((reinterpret_cast<uintptr_t>(rid) | reinterpret_cast<uintptr_t>(seq_lens)) & 7u) return CKV_ERR_POINTER;
   const uint32_t threads = 256;
-  plan_decode_kernel<<<(batch + threads - 1) / threads, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      ratio, rid, seq_lens, batch, plan_d, d_status);
-  return check_launch();
+  return launch_pdl(plan_decode_kernel, dim3((batch + threads - 1) / threads), dim3(threads), 0,
+                    reinterpret_cast<cudaStream_t>(stream), ratio, rid, seq_lens, batch, plan_d, d_status);
 }
 
 int ckv_plan_prefill(int ratio, const int64_t* rid, const int64_t* seq_lens, const int64_t* extend_lens,
@@ -329,8 +332,7 @@ int ckv_plan_prefill(int ratio, const int64_t* rid, const int64_t* seq_lens, con
   const uint32_t work = std::max(capacity_c, capacity_w);
   uint32_t grid = (work + kPlanThreads - 1) / kPlanThreads;
   grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 2u * static_cast<uint32_t>(sm_count())));
-  plan_prefill_kernel<<<grid, kPlanThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-  return check_launch();
+  return launch_pdl(plan_prefill_kernel, dim3(grid), dim3(kPlanThreads), 0, reinterpret_cast<cudaStream_t>(stream), a);
 }
 
 const char* ckv_error_string(int code) {

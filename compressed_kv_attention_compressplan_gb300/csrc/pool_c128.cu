@@ -21,12 +21,14 @@
 // Both kernels below run this same per-thread arithmetic (c128_pass1/2/3), so a
 // window gives the same bits whether it is pooled in prefill or in decode.
 //
-// Prefill kernel: persistent and warp-specialised.  One CTA per SM owns one
-// channel slice (its ape slice stays in registers); a producer warp streams the
-// CTA's tiles through a 3-stage shared-memory ring while 8 consumer warps
-// reduce the previous tiles.
-// Decode kernel: one CTA per (row, slice); rows that are not on a page
-// boundary only write their state slot and a zero output row.
+// Both steps run one persistent, warp-specialised kernel: one CTA per SM owns
+// one channel slice (its ape slice stays in registers); a producer warp
+// streams the CTA's tiles through a shared-memory ring while the consumer
+// warps reduce the previous tiles.  Prefill tiles are 128 channels wide (64 KB,
+// 3 stages); decode tiles 64 channels (32 KB, 6 stages), and every decode CTA
+// first finds the page-boundary rows by a block-wide scan of the plan so that
+// the page reads are spread evenly over the SMs.  Decode batches too large for
+// that use a kernel with one CTA per (row, slice).
 #include <cuda.h>  // CUtensorMap and its enums (types only; the encoder is fetched at run time)
 
 #include <algorithm>
@@ -38,18 +40,23 @@
 namespace ckv {
 namespace {
 
-template <typename TIn>
-struct C128Cfg {
-  static constexpr int CS = sizeof(TIn) == 2 ? 128 : 64;                // channels per tile
-  static constexpr int QUADS = CS / 4;                                  // 4 channels per thread
-  static constexpr int CONSUMERS = QUADS * 8;                           // 8 entry groups
+// A tile of CS channels x 128 entries; 4 channels per thread, 8 entry groups.
+template <typename TIn, int CS_>
+struct TileCfg {
+  static constexpr int CS = CS_;
+  static constexpr int QUADS = CS / 4;
+  static constexpr int THREADS = QUADS * 8;
   static constexpr int SEG_BYTES = CS * static_cast<int>(sizeof(TIn));  // one entry's kv (or score) slice
-  static constexpr int TILE_BYTES = 128 * SEG_BYTES * 2;                // 64 KB
+  static constexpr int TILE_BYTES = 128 * SEG_BYTES * 2;
   static constexpr int RED_FLOATS = 2 * 8 * CS;                         // group partials (l, a)
-  static constexpr int STAGES = 3;                                      // prefill ring depth
-  static constexpr int PREFILL_THREADS = CONSUMERS + 32;                // + one producer warp
-  static constexpr int PREFILL_SMEM = STAGES * TILE_BYTES + 2 * RED_FLOATS * 4;
-  static constexpr int DECODE_SMEM = TILE_BYTES + RED_FLOATS * 4;
+};
+
+// Decode: half-width tiles (32 KB) so that several boundary tiles per SM are
+// in flight at once.
+template <typename TIn>
+struct DecodeCfg : TileCfg<TIn, sizeof(TIn) == 2 ? 64 : 32> {
+  using Base = TileCfg<TIn, sizeof(TIn) == 2 ? 64 : 32>;
+  static constexpr int SMEM = Base::TILE_BYTES + Base::RED_FLOATS * 4;
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any real copy
@@ -124,28 +131,6 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// Barrier among the consumer warps only (the producer warp does not take part).
-template <int N>
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
-}
-
-// The same barrier, returning the OR of `pred` over the consumer threads, so
-// that every consumer takes the same decision.
-template <int N>
-__device__ __forceinline__ bool consumer_any(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "n"(N)
-      : "memory");
-  return r != 0;
-}
-
 // ---------------------------------------------------------------- element helpers
 template <typename TIn>
 __device__ __forceinline__ void load4(const TIn* p, float (&v)[4]);
@@ -201,9 +186,9 @@ __device__ __forceinline__ void store1<__nv_bfloat16>(__nv_bfloat16* p, float v)
 }
 
 // Zero rows [r0, r1) of out, columns [c0, c0 + CS), with NT threads.
-template <typename TIn, typename TOut, int NT>
+template <int CS, typename TOut, int NT>
 __device__ __forceinline__ void zero_rows(TOut* out, int hd, int c0, int64_t r0, int64_t r1, int t) {
-  constexpr int kPerRow = C128Cfg<TIn>::CS * static_cast<int>(sizeof(TOut)) / 16;
+  constexpr int kPerRow = CS * static_cast<int>(sizeof(TOut)) / 16;
   constexpr int kElems = 16 / static_cast<int>(sizeof(TOut));
   const int64_t total = (r1 - r0) * kPerRow;
   for (int64_t idx = t; idx < total; idx += NT) {
@@ -248,6 +233,39 @@ __device__ __forceinline__ void c128_pass2(const TIn* kv_s, int g, int cq, const
   }
 }
 
+// The same pass 2 without cached scores: s is formed again from the staged
+// score and ape with the same single rounding, so the result is identical.
+template <typename TIn, int CS, typename ApeAt>
+__device__ __forceinline__ void c128_pass2_recompute(const TIn* kv_s, const TIn* sc_s, int g, int cq, ApeAt ape_at,
+                                                     const float (&nml)[4], PoolAcc (&acc)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j].init();
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    float kv[4], sc[4], bias[4];
+    load4<TIn>(kv_s + (16 * g + k) * CS + cq, kv);
+    load4<TIn>(sc_s + (16 * g + k) * CS + cq, sc);
+    ape_at(k, bias);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j].add(kv[j], weight_of(score_plus_bias(sc[j], bias[j]), nml[j]));
+  }
+}
+
+// Pass 1 without keeping the scores: only the per-channel maximum.
+template <typename TIn, int CS, typename ApeAt>
+__device__ __forceinline__ void c128_max_only(const TIn* sc_s, int g, int cq, ApeAt ape_at, float (&m)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) m[j] = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    float sc[4], bias[4];
+    load4<TIn>(sc_s + (16 * g + k) * CS + cq, sc);
+    ape_at(k, bias);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m[j] = fmaxf(m[j], score_plus_bias(sc[j], bias[j]));
+  }
+}
+
 // Channel maximum over the 8 groups' partial maxima (exact in any order).
 template <int CS>
 __device__ __forceinline__ void c128_nml(const float* red_m, int cq, float (&nml)[4]) {
@@ -267,11 +285,11 @@ __device__ __forceinline__ void load_ape_regs(const TIn* ape, int hd, int c0, in
 }
 
 // Issues the 256 bulk copies of one tile (called by all 32 lanes of a warp).
-template <typename TIn>
+template <typename TIn, int CS_>
 __device__ __forceinline__ void issue_tile(TIn* kv_s, const TIn* state, const TIn* input, size_t width, int hd,
                                            int c0, uint32_t ragged, int bl, int64_t rp0, uint32_t bar, int lane) {
-  using Cfg = C128Cfg<TIn>;
-  constexpr int CS = Cfg::CS;
+  using Cfg = TileCfg<TIn, CS_>;
+  constexpr int CS = CS_;
   TIn* sc_s = kv_s + 128 * CS;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -299,19 +317,121 @@ __device__ __forceinline__ bool prefill_record(const PoolArgs& a, uint32_t e, ui
   return ok;
 }
 
-// ---------------------------------------------------------------- prefill (persistent)
-template <typename TIn, typename TOut>
-__global__ __launch_bounds__(C128Cfg<TIn>::PREFILL_THREADS, 1) void c128_prefill_kernel(
-    const PoolArgs a, uint32_t slices, const __grid_constant__ CUtensorMap in_map) {
-  using Cfg = C128Cfg<TIn>;
-  constexpr int CS = Cfg::CS;
-  constexpr int NC = Cfg::CONSUMERS;
-  constexpr int NS = Cfg::STAGES;
+// ---------------------------------------------------------------- persistent kernel
+// One CTA per SM, bound to one channel slice; its ape slice stays in
+// registers.  A producer warp streams the CTA's tiles through an NS-stage ring
+// of shared-memory tiles; the consumer warps reduce them.
+//   prefill: the CTA's tiles are compress records first, first + per_slice, ...
+//   decode:  every CTA first block-scans the decode plan for page-boundary rows
+//            and keeps the ones of rank first, first + per_slice, ...; it also
+//            does the state write / zero output of rows blockIdx, blockIdx +
+//            gridDim, ... (the part of decode that reads no page).
+constexpr int kOwnRows = 512;   // decode: rows one CTA may own (boundary rows; rows it writes)
+constexpr int kScanK = 4;       // decode: plan rows each thread examines per scan pass
+
+template <typename TIn, int CS, int NS, int NG, bool kDecode>
+struct PersistCfg {
+  using T = TileCfg<TIn, CS>;
+  static constexpr int NCG = T::THREADS;   // threads of one consumer group
+  static constexpr int NC = NG * NCG;      // all consumer threads
+  static constexpr int THREADS = NC + 32;  // + the producer warp
+  static constexpr int SMEM = NS * T::TILE_BYTES + 2 * NG * T::RED_FLOATS * 4 + (kDecode ? kOwnRows * 24 : 0);
+  static_assert(NS % NG == 0, "each consumer group owns every NG-th stage");
+};
+
+// Decode plan row r: valid (in range) and on a page boundary?
+__device__ __forceinline__ bool decode_row(const PoolArgs& a, uint32_t r, bool& valid, bool& boundary,
+                                           ckv_decode_plan_t& P) {
+  P = load_plan_d(a.plan_d + r);
+  valid = false;
+  boundary = false;
+  if (P.seq_len == kInvalidU32) return false;  // invalid record: zero output, nothing else
+  boundary = P.seq_len % 128 == 0;
+  valid = P.write_loc >= 0 && static_cast<uint64_t>(P.write_loc) < a.state_rows;
+  if (boundary)
+    valid = valid && P.read_page_0 >= 0 && static_cast<uint64_t>(P.read_page_0) * 128 + 127 < a.state_rows;
+  return true;
+}
+
+// The rows of a decode step that read no page, by NTH threads of one CTA:
+// every row in `rows` ({row, write_loc, flags}) writes its new token to its
+// slot (never one of the 127 slots any window reads), and rows that emit
+// nothing get a zero output row.  Each thread owns fixed 16-byte chunk
+// positions and batches several rows, so its loads are all in flight at once.
+constexpr uint32_t kRowValid = 1u, kRowBoundary = 2u;
+
+template <typename TIn, typename TOut, int NTH>
+__device__ __forceinline__ void decode_rows_without_window(const PoolArgs& a, const uint4* rows, uint32_t nrows,
+                                                           int tl) {
+  constexpr int kVec = 16 / static_cast<int>(sizeof(TIn));
+  constexpr int kOutVec = 16 / static_cast<int>(sizeof(TOut));
+  constexpr int kRows = 4;  // rows per batch: all their loads are issued before any store
+  const int hd = a.head_dim;
+  const int width = 2 * hd;
+  const int in_chunks = width / kVec;
+  const int out_chunks = hd / kOutVec;
+  const TIn* input = static_cast<const TIn*>(a.input);
+  TIn* state = static_cast<TIn*>(a.state_mut);
+  TOut* out = static_cast<TOut*>(a.out);
+  // thread position c: chunk c of the state copy, or chunk c - in_chunks of the zero row
+  for (int c = tl; c < in_chunks + out_chunks; c += NTH) {
+    for (uint32_t base = 0; base < nrows; base += kRows) {
+      uint4 v[kRows];
+      uint4 rec[kRows];
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        rec[k] = base + k < nrows ? rows[base + k] : make_uint4(0, 0, 0, 0);
+        if (c < in_chunks && (rec[k].z & kRowValid))
+          v[k] = ld_stream16(input + static_cast<size_t>(rec[k].x) * width + c * kVec);
+      }
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        if (base + k >= nrows) break;
+        if (c < in_chunks) {
+          if (rec[k].z & kRowValid) st16(state + static_cast<size_t>(rec[k].y) * width + c * kVec, v[k]);
+        } else if (!((rec[k].z & kRowValid) && (rec[k].z & kRowBoundary))) {
+          st16(out + static_cast<size_t>(rec[k].x) * hd + (c - in_chunks) * kOutVec, make_uint4(0, 0, 0, 0));
+        }
+      }
+    }
+  }
+}
+
+// Consumer barrier of group `grp` (ids 1 .. NG), N threads.
+__device__ __forceinline__ void group_sync(int grp, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ bool group_any(int grp, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(1 + grp), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+template <typename TIn, typename TOut, int CS, int NS, int NG, bool kDecode>
+__global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) void c128_persistent_kernel(
+    const PoolArgs a, uint32_t slices, const __grid_constant__ CUtensorMap in_map,
+    const __grid_constant__ CUtensorMap page_map) {
+  using T = TileCfg<TIn, CS>;
+  using Cfg = PersistCfg<TIn, CS, NS, NG, kDecode>;
+  constexpr int NCG = Cfg::NCG;
+  constexpr int NC = Cfg::NC;
+  constexpr int NT = Cfg::THREADS;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[NS];
   __shared__ __align__(8) uint64_t empty_bar[NS];
   __shared__ volatile int abort_flag;
-  float* red_base = reinterpret_cast<float*>(smem + NS * Cfg::TILE_BYTES);
+  __shared__ uint32_t s_warp_count[NT / 32];
+  float* red_base = reinterpret_cast<float*>(smem + NS * T::TILE_BYTES);
+  uint4* trivrow = reinterpret_cast<uint4*>(smem + NS * T::TILE_BYTES + 2 * NG * T::RED_FLOATS * 4);
+  uint2* own = reinterpret_cast<uint2*>(trivrow + kOwnRows);
 
   const int t = threadIdx.x;
   const int warp = t >> 5;
@@ -323,26 +443,95 @@ __global__ __launch_bounds__(C128Cfg<TIn>::PREFILL_THREADS, 1) void c128_prefill
   const int hd = a.head_dim;
   const size_t width = 2 * static_cast<size_t>(hd);
   const TIn* input = static_cast<const TIn*>(a.input);
-  const TIn* state = static_cast<const TIn*>(a.state);
+  const TIn* state = kDecode ? static_cast<const TIn*>(a.state_mut) : static_cast<const TIn*>(a.state);
   TOut* out = static_cast<TOut*>(a.out);
-  const bool token = a.out_layout == CKV_OUT_TOKEN;
-  const uint32_t num_c = count_or_capacity(a.d_counts, 0, a.capacity);
+  const bool token = !kDecode && a.out_layout == CKV_OUT_TOKEN;
 
   if (t == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), NC / 32);
+      mbar_init(smem_addr(&empty_bar[s]), NCG / 32);
     }
     abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
+  // the consumers' ape slice is loaded first, so that it overlaps the plan scan
+  const int grp = t / NCG;
+  const int tl = t % NCG;
+  const int q = tl % T::QUADS;
+  const int g = tl / T::QUADS;
+  const int cq = 4 * q;
+  float ape_r[16][4];
+  if (kDecode && warp < NC / 32) load_ape_regs<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
+
+  pdl_wait();  // everything below may read what the previous kernel wrote
+  pdl_release();
+  const uint32_t num_c = kDecode ? 0u : count_or_capacity(a.d_counts, 0, a.capacity);
+  uint32_t items, ntriv = 0;
+  if constexpr (kDecode) {
+    // Ranks of the page-boundary rows (in row order) by block-wide scans: in
+    // each pass thread t looks at kScanK consecutive rows.  This CTA owns the
+    // boundary rows of rank first, first + stride, ... ({row, page} pairs) and
+    // writes the state / zero rows of rows blockIdx, blockIdx + gridDim, ...
+    // (the host keeps both counts below kOwnRows).
+    const uint32_t B = a.capacity;
+    uint32_t seen = 0;
+    for (uint32_t base = 0; base < B; base += kScanK * NT) {
+      bool take[kScanK];
+      ckv_decode_plan_t P[kScanK];
+      uint32_t cnt = 0;
+#pragma unroll
+      for (int k = 0; k < kScanK; ++k) {
+        const uint32_t r = base + t * kScanK + k;
+        bool valid = false, boundary = false;
+        if (r < B) {
+          const bool rec = decode_row(a, r, valid, boundary, P[k]);
+          if (r % gridDim.x == blockIdx.x) {
+            trivrow[r / gridDim.x] = make_uint4(r, static_cast<uint32_t>(P[k].write_loc),
+                                                (valid ? kRowValid : 0u) | (boundary ? kRowBoundary : 0u), 0u);
+            if (rec && !valid) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+          }
+        }
+        take[k] = r < B && valid && boundary;
+        cnt += take[k] ? 1u : 0u;
+      }
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      if (lane == 31) s_warp_count[warp] = incl;
+      __syncthreads();
+      uint32_t rank = seen + incl - cnt, total = seen;
+#pragma unroll
+      for (int w = 0; w < NT / 32; ++w) {
+        const uint32_t c = s_warp_count[w];
+        if (w < warp) rank += c;
+        total += c;
+      }
+#pragma unroll
+      for (int k = 0; k < kScanK; ++k) {
+        if (take[k]) {
+          if (rank % stride == first)
+            own[rank / stride] = make_uint2(base + t * kScanK + k, static_cast<uint32_t>(P[k].read_page_0));
+          ++rank;
+        }
+      }
+      seen = total;
+      __syncthreads();
+    }
+    items = seen > first ? (seen - first + stride - 1) / stride : 0u;
+    ntriv = B > blockIdx.x ? (B - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
+  } else {
+    __syncthreads();
+    items = num_c > first ? (num_c - first + stride - 1) / stride : 0u;
+  }
 
   if (warp == NC / 32) {
     // ---------------- producer warp
-    if (lane == 0) prefetch_map(&in_map);
-    uint32_t n = 0;
-    for (uint32_t e = first; e < num_c; e += stride, ++n) {
+    if (lane == 0) prefetch_map(kDecode ? &page_map : &in_map);
+    for (uint32_t n = 0; n < items; ++n) {
       const int stage = static_cast<int>(n % NS);
       const uint32_t phase = (n / NS) & 1u;
       if (!mbar_wait_bounded(smem_addr(&empty_bar[stage]), phase ^ 1u, kWaitLimitNs)) {
@@ -353,56 +542,82 @@ __global__ __launch_bounds__(C128Cfg<TIn>::PREFILL_THREADS, 1) void c128_prefill
         break;
       }
       if (abort_flag) break;
-      uint32_t ragged = 0;
-      int bl = 0;
-      int64_t rp0 = 0;
-      bool bad;
-      const bool ok = prefill_record(a, e, ragged, bl, rp0, bad);
-      if (bad && lane == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
       const uint32_t bar = smem_addr(&full_bar[stage]);
-      if (lane == 0) mbar_arrive_expect_tx(bar, ok ? Cfg::TILE_BYTES : 0u);
-      __syncwarp();
-      if (ok) {
-        TIn* kv_s = reinterpret_cast<TIn*>(smem + stage * Cfg::TILE_BYTES);
-        if (bl == 0) {  // rows ragged-127 .. ragged of the input: two boxes
-          if (lane == 0) {
-            tma_box_g2s(smem_addr(kv_s), &in_map, c0, static_cast<int>(ragged) - 127, bar);
-            tma_box_g2s(smem_addr(kv_s + 128 * CS), &in_map, hd + c0, static_cast<int>(ragged) - 127, bar);
+      TIn* kv_s = reinterpret_cast<TIn*>(smem + stage * T::TILE_BYTES);
+      if constexpr (kDecode) {
+        // page slots 0..126 as two 127-row boxes; entry 127 = the new token's input row
+        const uint2 rp = own[n];
+        const uint32_t b = rp.x;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, T::TILE_BYTES);
+          const int y = static_cast<int>(static_cast<int64_t>(static_cast<int32_t>(rp.y)) * 128);
+          tma_box_g2s(smem_addr(kv_s), &page_map, c0, y, bar);
+          tma_box_g2s(smem_addr(kv_s + 128 * CS), &page_map, hd + c0, y, bar);
+          const TIn* row = input + static_cast<size_t>(b) * width;
+          bulk_g2s(smem_addr(kv_s + 127 * CS), row + c0, T::SEG_BYTES, bar);
+          bulk_g2s(smem_addr(kv_s + 128 * CS + 127 * CS), row + hd + c0, T::SEG_BYTES, bar);
+        }
+      } else {
+        const uint32_t e = first + n * stride;
+        uint32_t ragged = 0;
+        int bl = 0;
+        int64_t rp0 = 0;
+        bool bad;
+        const bool ok = prefill_record(a, e, ragged, bl, rp0, bad);
+        if (bad && lane == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+        if (lane == 0) mbar_arrive_expect_tx(bar, ok ? T::TILE_BYTES : 0u);
+        __syncwarp();
+        if (ok) {
+          if (bl == 0) {  // rows ragged-127 .. ragged of the input: two boxes
+            if (lane == 0) {
+              tma_box_g2s(smem_addr(kv_s), &in_map, c0, static_cast<int>(ragged) - 127, bar);
+              tma_box_g2s(smem_addr(kv_s + 128 * CS), &in_map, hd + c0, static_cast<int>(ragged) - 127, bar);
+            }
+          } else {
+            issue_tile<TIn, CS>(kv_s, state, input, width, hd, c0, ragged, bl, rp0, bar, lane);
           }
-        } else {
-          issue_tile<TIn>(kv_s, state, input, width, hd, c0, ragged, bl, rp0, bar, lane);
         }
       }
+      __syncwarp();
     }
     return;
   }
 
-  // ---------------- consumer warps
-  const int q = t % Cfg::QUADS;
-  const int g = t / Cfg::QUADS;
-  const int cq = 4 * q;
-  float ape_r[16][4];
-  load_ape_regs<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
-  uint32_t n = 0;
-  for (uint32_t e = first; e < num_c; e += stride, ++n) {
-    // one decision for all consumers (also orders the reuse of the reduction buffers)
-    if (consumer_any<NC>(abort_flag != 0)) break;
+  // ---------------- consumer warps: group grp takes items grp, grp + NG, ...
+  // (decode: first the rows that read no page, while the first tiles load)
+  if constexpr (kDecode) {
+    decode_rows_without_window<TIn, TOut, NC>(a, trivrow, ntriv, t);
+  } else {
+    load_ape_regs<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
+  }
+  uint32_t local = 0;
+  for (uint32_t n = grp; n < items; n += NG, ++local) {
+    // one decision for the whole group (also orders the reuse of its reduction buffers)
+    if (group_any(grp, NCG, abort_flag != 0)) break;
     const int stage = static_cast<int>(n % NS);
     const uint32_t phase = (n / NS) & 1u;
     if (!mbar_wait_bounded(smem_addr(&full_bar[stage]), phase, kWaitLimitNs)) {
       status_or(a.d_status, CKV_STATUS_TIMEOUT);
       abort_flag = 1;
     }
-    uint32_t ragged = 0;
-    int bl = 0;
-    int64_t rp0 = 0;
-    bool bad;
-    const bool ok = prefill_record(a, e, ragged, bl, rp0, bad);
-    float* red_l = red_base + (n & 1u) * Cfg::RED_FLOATS;
+    bool ok = true;
+    uint32_t e = 0, ragged = 0;
+    size_t orow;
+    if constexpr (kDecode) {
+      orow = own[n].x;
+    } else {
+      e = first + n * stride;
+      int bl = 0;
+      int64_t rp0 = 0;
+      bool bad;
+      ok = prefill_record(a, e, ragged, bl, rp0, bad);
+      orow = token ? ragged : e;
+    }
+    float* red_l = red_base + (2 * grp + (local & 1u)) * T::RED_FLOATS;
     float* red_a = red_l + 8 * CS;
     PoolAcc acc[4];
     if (ok) {
-      const TIn* kv_s = reinterpret_cast<const TIn*>(smem + stage * Cfg::TILE_BYTES);
+      const TIn* kv_s = reinterpret_cast<const TIn*>(smem + stage * T::TILE_BYTES);
       const TIn* sc_s = kv_s + 128 * CS;
       float s[16][4], m[4], nml[4];
       c128_pass1<TIn, CS>(sc_s, g, cq,
@@ -412,47 +627,46 @@ __global__ __launch_bounds__(C128Cfg<TIn>::PREFILL_THREADS, 1) void c128_prefill
                           },
                           s, m);
       *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(m[0], m[1], m[2], m[3]);
-      consumer_sync<NC>();
+      group_sync(grp, NCG);
       c128_nml<CS>(red_l, cq, nml);
-      consumer_sync<NC>();
+      group_sync(grp, NCG);
       c128_pass2<TIn, CS>(kv_s, g, cq, s, nml, acc);
       *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(acc[0].l, acc[1].l, acc[2].l, acc[3].l);
       *reinterpret_cast<float4*>(red_a + g * CS + cq) = make_float4(acc[0].a, acc[1].a, acc[2].a, acc[3].a);
-      consumer_sync<NC>();
+      group_sync(grp, NCG);
     }
     // the stage is no longer read: hand it back to the producer
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
     if (ok) {
-      const size_t orow = token ? ragged : e;
-      if (t < CS) store1<TOut>(out + orow * hd + c0 + t, finish(tree8(red_a + t, CS), tree8(red_l + t, CS)));
+      if (tl < CS) store1<TOut>(out + orow * hd + c0 + tl, finish(tree8(red_a + tl, CS), tree8(red_l + tl, CS)));
       if (token) {  // rows between the previous compress row and this one
         int64_t prev = -1;
         if (e > 0) {
           const ckv_compress_plan_t Q = load_plan_c(a.plan_c + e - 1);
           prev = plan_c_invalid(Q) ? static_cast<int64_t>(ragged) : static_cast<int64_t>(Q.ragged_bl & CKV_RAGGED_MASK);
         }
-        zero_rows<TIn, TOut, NC>(out, hd, c0, prev + 1, ragged, t);
+        zero_rows<CS, TOut, NCG>(out, hd, c0, prev + 1, ragged, tl);
       }
     }
   }
-  if (token && first == 0) {  // rows after the last compress row (and all rows when there is none)
+  if (token && first == 0 && grp == 0) {  // rows after the last compress row (and all rows when there is none)
     int64_t last = -1;
     if (num_c > 0) {
       const ckv_compress_plan_t Q = load_plan_c(a.plan_c + num_c - 1);
       last = plan_c_invalid(Q) ? static_cast<int64_t>(a.num_q_tokens) : static_cast<int64_t>(Q.ragged_bl & CKV_RAGGED_MASK);
     }
-    zero_rows<TIn, TOut, NC>(out, hd, c0, last + 1, a.num_q_tokens, t);
+    zero_rows<CS, TOut, NCG>(out, hd, c0, last + 1, a.num_q_tokens, tl);
   }
 }
 
 // ---------------------------------------------------------------- decode (one tile per CTA)
 template <typename TIn, typename TOut>
-__global__ __launch_bounds__(C128Cfg<TIn>::CONSUMERS, 2) void c128_decode_kernel(
+__global__ __launch_bounds__(DecodeCfg<TIn>::THREADS, 6) void c128_decode_kernel(
     const PoolArgs a, uint32_t slices, uint32_t tiles, const __grid_constant__ CUtensorMap page_map) {
-  using Cfg = C128Cfg<TIn>;
+  using Cfg = DecodeCfg<TIn>;
   constexpr int CS = Cfg::CS;
-  constexpr int NT = Cfg::CONSUMERS;
+  constexpr int NT = Cfg::THREADS;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bar_storage;
   TIn* kv_s = reinterpret_cast<TIn*>(smem);
@@ -460,6 +674,8 @@ __global__ __launch_bounds__(C128Cfg<TIn>::CONSUMERS, 2) void c128_decode_kernel
   float* red_l = reinterpret_cast<float*>(smem + Cfg::TILE_BYTES);
   float* red_a = red_l + 8 * CS;
 
+  pdl_wait();
+  pdl_release();
   const uint32_t tile = blockIdx.x;
   if (tile >= tiles) return;
   const uint32_t b = tile / slices;
@@ -473,7 +689,7 @@ __global__ __launch_bounds__(C128Cfg<TIn>::CONSUMERS, 2) void c128_decode_kernel
 
   const ckv_decode_plan_t P = load_plan_d(a.plan_d + b);
   if (P.seq_len == kInvalidU32) {
-    zero_rows<TIn, TOut, NT>(out, hd, c0, b, b + 1, t);
+    zero_rows<CS, TOut, NT>(out, hd, c0, b, b + 1, t);
     return;
   }
   const bool boundary = P.seq_len % 128 == 0;
@@ -482,31 +698,15 @@ __global__ __launch_bounds__(C128Cfg<TIn>::CONSUMERS, 2) void c128_decode_kernel
   if (boundary) ok = ok && rp0 >= 0 && static_cast<uint64_t>(rp0) * 128 + 127 < a.state_rows;
   if (!ok) {
     if (t == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
-    zero_rows<TIn, TOut, NT>(out, hd, c0, b, b + 1, t);
+    zero_rows<CS, TOut, NT>(out, hd, c0, b, b + 1, t);
     return;
   }
-  // the new token's slice of kv and score goes to its page slot
-  if (t < 2 * Cfg::SEG_BYTES / 16) {
-    const int half = t / (Cfg::SEG_BYTES / 16);
-    const int off = (t % (Cfg::SEG_BYTES / 16)) * (16 / static_cast<int>(sizeof(TIn)));
-    const TIn* src = input + static_cast<size_t>(b) * width + half * hd + c0 + off;
-    TIn* dst = state + static_cast<size_t>(P.write_loc) * width + half * hd + c0 + off;
-    st16(dst, ld_stream16(src));
-  }
-  if (!boundary) {
-    zero_rows<TIn, TOut, NT>(out, hd, c0, b, b + 1, t);
-    return;
-  }
-  // entries 0..126 from the page (the slot being written is entry 127), entry 127 = the new token
   const uint32_t bar = smem_addr(&bar_storage);
-  if (t == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (t == 0) {
+  if (boundary && t == 0) {
     // slots 0..126 of the page: one 127-row box each for kv and score; the new
     // token (entry 127) comes straight from its input row
+    mbar_init(bar, 1);
+    fence_mbar_init();
     mbar_arrive_expect_tx(bar, Cfg::TILE_BYTES);
     const int y = static_cast<int>(rp0 * 128);
     tma_box_g2s(smem_addr(kv_s), &page_map, c0, y, bar);
@@ -515,23 +715,37 @@ __global__ __launch_bounds__(C128Cfg<TIn>::CONSUMERS, 2) void c128_decode_kernel
     bulk_g2s(smem_addr(kv_s + 127 * CS), row + c0, Cfg::SEG_BYTES, bar);
     bulk_g2s(smem_addr(sc_s + 127 * CS), row + hd + c0, Cfg::SEG_BYTES, bar);
   }
+  // the new token's slice of kv and score goes to its page slot (never one of
+  // the 127 slots read above)
+  for (int i = t; i < 2 * Cfg::SEG_BYTES / 16; i += NT) {
+    const int half = i / (Cfg::SEG_BYTES / 16);
+    const int off = (i % (Cfg::SEG_BYTES / 16)) * (16 / static_cast<int>(sizeof(TIn)));
+    const TIn* src = input + static_cast<size_t>(b) * width + half * hd + c0 + off;
+    TIn* dst = state + static_cast<size_t>(P.write_loc) * width + half * hd + c0 + off;
+    st16(dst, ld_stream16(src));
+  }
+  if (!boundary) {
+    zero_rows<CS, TOut, NT>(out, hd, c0, b, b + 1, t);
+    return;
+  }
+  __syncthreads();  // barrier initialisation is visible to every waiting thread
   const int q = t % Cfg::QUADS;
   const int g = t / Cfg::QUADS;
   const int cq = 4 * q;
   const TIn* ape = static_cast<const TIn*>(a.ape) + static_cast<size_t>(16 * g) * hd + c0 + cq;
+  auto ape_at = [&](int k, float (&v)[4]) { ldg4<TIn>(ape + static_cast<size_t>(k) * hd, v); };
   if (!mbar_wait_bounded(bar, 0, kWaitLimitNs)) {
     status_or(a.d_status, CKV_STATUS_TIMEOUT);
     mbar_wait_bounded(bar, 0, kWaitLimitNs);  // let copies in flight land before the CTA can exit
   }
-  float s[16][4], m[4], nml[4];
-  c128_pass1<TIn, CS>(sc_s, g, cq, [&](int k, float (&v)[4]) { ldg4<TIn>(ape + static_cast<size_t>(k) * hd, v); },
-                      s, m);
+  float m[4], nml[4];
+  c128_max_only<TIn, CS>(sc_s, g, cq, ape_at, m);
   *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(m[0], m[1], m[2], m[3]);
   __syncthreads();
   c128_nml<CS>(red_l, cq, nml);
   __syncthreads();
   PoolAcc acc[4];
-  c128_pass2<TIn, CS>(kv_s, g, cq, s, nml, acc);
+  c128_pass2_recompute<TIn, CS>(kv_s, sc_s, g, cq, ape_at, nml, acc);
   *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(acc[0].l, acc[1].l, acc[2].l, acc[3].l);
   *reinterpret_cast<float4*>(red_a + g * CS + cq) = make_float4(acc[0].a, acc[1].a, acc[2].a, acc[3].a);
   __syncthreads();
@@ -589,12 +803,14 @@ int opt_in_smem(K kernel, int bytes, bool* configured) {
 
 template <typename TIn, typename TOut>
 int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
-  using Cfg = C128Cfg<TIn>;
-  const uint32_t slices = static_cast<uint32_t>(a.head_dim / Cfg::CS);
+  constexpr int CS = sizeof(TIn) == 2 ? 128 : 64;
+  constexpr int NS = 3;
+  using Cfg = PersistCfg<TIn, CS, NS, 1, false>;
+  const uint32_t slices = static_cast<uint32_t>(a.head_dim / CS);
   const bool token = a.out_layout == CKV_OUT_TOKEN;
   if (a.capacity == 0 && !(token && a.num_q_tokens > 0)) return CKV_OK;
   static bool configured[64] = {};
-  int rc = opt_in_smem(c128_prefill_kernel<TIn, TOut>, Cfg::PREFILL_SMEM, configured);
+  int rc = opt_in_smem(c128_persistent_kernel<TIn, TOut, CS, NS, 1, false>, Cfg::SMEM, configured);
   if (rc) return rc;
   // one persistent CTA per SM; every CTA serves one channel slice
   const uint32_t per_slice = std::max<uint32_t>(
@@ -602,31 +818,46 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
   alignas(64) CUtensorMap in_map;
   memset(&in_map, 0, sizeof in_map);
   if (a.num_q_tokens > 0) {
-    rc = make_map(&in_map, a.input, a.in_dtype, 2ull * a.head_dim, a.num_q_tokens, Cfg::CS, 128);
+    rc = make_map(&in_map, a.input, a.in_dtype, 2ull * a.head_dim, a.num_q_tokens, CS, 128);
     if (rc) return rc;
   }
-  c128_prefill_kernel<TIn, TOut><<<per_slice * slices, Cfg::PREFILL_THREADS, Cfg::PREFILL_SMEM, s>>>(a, slices,
-                                                                                                    in_map);
-  return check_launch();
+  return launch_pdl(c128_persistent_kernel<TIn, TOut, CS, NS, 1, false>, dim3(per_slice * slices), dim3(Cfg::THREADS),
+                    Cfg::SMEM, s, a, slices, in_map, in_map);
 }
 
 template <typename TIn, typename TOut>
 int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
-  using Cfg = C128Cfg<TIn>;
-  const uint32_t slices = static_cast<uint32_t>(a.head_dim / Cfg::CS);
+  if (a.capacity == 0) return CKV_OK;
+  if (a.state_rows == 0 || a.state_rows > 0x7FFFFFFFull) return CKV_ERR_SIZE;
+  constexpr int CS = DecodeCfg<TIn>::CS;
+  const uint32_t slices = static_cast<uint32_t>(a.head_dim / CS);
+  alignas(64) CUtensorMap page_map;
+  int rc = make_map(&page_map, a.state_mut, a.in_dtype, 2ull * a.head_dim, a.state_rows, CS, 127);
+  if (rc) return rc;
+  const uint32_t per_slice = std::max<uint32_t>(1, static_cast<uint32_t>(sm_count()) / slices);
+  // each CTA owns at most ceil(batch / per_slice) boundary rows and
+  // ceil(batch / grid) rows without a window: both lists live in shared memory
+  if ((a.capacity + per_slice - 1) / per_slice <= static_cast<uint32_t>(kOwnRows)) {
+    // persistent: every CTA scans the plan and streams its share of boundary tiles
+    constexpr int NS = 6;
+    constexpr int NG = 2;  // two consumer groups reduce alternate tiles
+    using Cfg = PersistCfg<TIn, CS, NS, NG, true>;
+    static bool configured_p[64] = {};
+    rc = opt_in_smem(c128_persistent_kernel<TIn, TOut, CS, NS, NG, true>, Cfg::SMEM, configured_p);
+    if (rc) return rc;
+    return launch_pdl(c128_persistent_kernel<TIn, TOut, CS, NS, NG, true>, dim3(per_slice * slices),
+                      dim3(Cfg::THREADS), Cfg::SMEM, s, a, slices, page_map, page_map);
+  }
+  // very large batches: one CTA per (row, slice)
+  using Cfg = DecodeCfg<TIn>;
   const uint64_t tiles64 = static_cast<uint64_t>(a.capacity) * slices;
-  if (tiles64 == 0) return CKV_OK;
   if (tiles64 > 0x7FFFFFFFull) return CKV_ERR_SIZE;
   static bool configured[64] = {};
-  int rc = opt_in_smem(c128_decode_kernel<TIn, TOut>, Cfg::DECODE_SMEM, configured);
-  if (rc) return rc;
-  if (a.state_rows == 0 || a.state_rows > 0x7FFFFFFFull) return CKV_ERR_SIZE;
-  alignas(64) CUtensorMap page_map;
-  rc = make_map(&page_map, a.state_mut, a.in_dtype, 2ull * a.head_dim, a.state_rows, Cfg::CS, 127);
+  rc = opt_in_smem(c128_decode_kernel<TIn, TOut>, Cfg::SMEM, configured);
   if (rc) return rc;
   const uint32_t tiles = static_cast<uint32_t>(tiles64);
-  c128_decode_kernel<TIn, TOut><<<tiles, Cfg::CONSUMERS, Cfg::DECODE_SMEM, s>>>(a, slices, tiles, page_map);
-  return check_launch();
+  return launch_pdl(c128_decode_kernel<TIn, TOut>, dim3(tiles), dim3(Cfg::THREADS), Cfg::SMEM, s, a, slices, tiles,
+                    page_map);
 }
 
 template <bool kDecode>

@@ -65,6 +65,8 @@ __global__ __launch_bounds__(kC4Threads, 2) void c4_pool_prefill_kernel(const Po
   TOut* out = static_cast<TOut*>(a.out);
   const bool token = a.out_layout == CKV_OUT_TOKEN;
 
+  pdl_wait();
+  pdl_release();
   const uint32_t gid = blockIdx.x * blockDim.x + threadIdx.x;
   const uint32_t stride = gridDim.x * blockDim.x;  // a multiple of `chunks`
   const uint32_t ch = gid % chunks;
@@ -134,6 +136,8 @@ __global__ __launch_bounds__(kC4Threads, 2) void c4_pool_prefill_kernel(const Po
 template <typename TIn, typename TOut>
 __global__ __launch_bounds__(kC4Threads) void c4_decode_kernel(const PoolArgs a, uint32_t chunks, uint32_t units) {
   constexpr int VEC = C4Vec<TIn>::VEC;
+  pdl_wait();
+  pdl_release();
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= units) return;
   const int hd = a.head_dim;
@@ -208,8 +212,7 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
   const uint32_t units = static_cast<uint32_t>(units64);
   uint32_t grid = (units + threads - 1) / threads;
   grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 16u * static_cast<uint32_t>(sm_count())));
-  c4_pool_prefill_kernel<TIn, TOut><<<grid, threads, 0, s>>>(a, chunks, units);
-  return check_launch();
+  return launch_pdl(c4_pool_prefill_kernel<TIn, TOut>, dim3(grid), dim3(threads), 0, s, a, chunks, units);
 }
 
 template <typename TIn, typename TOut>
@@ -221,8 +224,8 @@ int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
   if (units64 == 0) return CKV_OK;
   if (units64 > 0xFFFFFFFFull) return CKV_ERR_SIZE;
   const uint32_t units = static_cast<uint32_t>(units64);
-  c4_decode_kernel<TIn, TOut><<<(units + threads - 1) / threads, threads, 0, s>>>(a, chunks, units);
-  return check_launch();
+  return launch_pdl(c4_decode_kernel<TIn, TOut>, dim3((units + threads - 1) / threads), dim3(threads), 0, s, a,
+                    chunks, units);
 }
 
 }  // namespace

@@ -28,6 +28,8 @@ struct WriteArgs {
 };
 
 __global__ __launch_bounds__(kWriteThreads) void write_kernel(const WriteArgs a) {
+  pdl_wait();  // the pool of this step must have finished reading the state
+  pdl_release();
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t warps_total = gridDim.x * (kWriteThreads / 32);
   const uint32_t n = count_or_capacity(a.d_counts, 1, a.cap_w);
@@ -80,6 +82,5 @@ extern "C" int ckv_compress_write(int ratio, int head_dim, int dtype, void* stat
   const uint32_t warps_per_cta = kWriteThreads / 32;
   uint32_t grid = (capacity_w + warps_per_cta - 1) / warps_per_cta;
   grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 8u * static_cast<uint32_t>(sm_count())));
-  write_kernel<<<grid, kWriteThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-  return check_launch();
+  return launch_pdl(write_kernel, dim3(grid), dim3(kWriteThreads), 0, reinterpret_cast<cudaStream_t>(stream), a);
 }

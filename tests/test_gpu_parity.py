@@ -351,3 +351,33 @@ def test_closed_forms_on_gpu(env, ratio):
         tag = (tag + np.arange(hd) / 256.0).astype(np.float32)
         assert (want[p] == tag).all()
         assert np.abs(got[p] - tag).max() <= 2e-6 * np.abs(tag).max(), p
+
+
+def test_c128_decode_large_batch_path_matches(env):
+    """A decode batch too large for the persistent kernel's per-CTA row list
+    (here 40000 rows, almost all invalid records) takes the one-CTA-per-(row,
+    slice) kernel; its rows must be bit-identical to the same rows decoded in a
+    small batch, and the invalid rows must be zero."""
+    o, ckv, dev = env
+    hd = 512
+    sl = [128, 256, 5, 384, 1280, 7, 512, 130]
+    w = wl.random_decode(128, hd, torch.bfloat16, torch.float32, sl, seed=9, num_requests_state=8)
+    small_state = w.state.to(dev)
+    out_small, pd_small = ckv.decode_step(128, hd, small_state, w.kv_score.to(dev), w.ape.to(dev), w.rid.to(dev),
+                                          w.seq_lens.to(dev), torch.float32)
+    B = 40000
+    pos = np.sort(np.random.default_rng(1).choice(B, len(sl), replace=False))
+    plan = torch.full((B, 16), 0xFF, dtype=torch.uint8, device=dev)
+    plan[torch.as_tensor(pos, device=dev)] = pd_small
+    kv = torch.zeros(B, 2 * hd, dtype=torch.bfloat16, device=dev)
+    kv[torch.as_tensor(pos, device=dev)] = w.kv_score.to(dev)
+    big_state = w.state.to(dev)
+    status = ckv.new_status(dev)
+    out_big = ckv.compress_decode(128, hd, big_state, kv, w.ape.to(dev), plan, status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    assert torch.equal(out_big[torch.as_tensor(pos, device=dev)].view(torch.int32), out_small.view(torch.int32))
+    mask = torch.ones(B, dtype=torch.bool, device=dev)
+    mask[torch.as_tensor(pos, device=dev)] = False
+    assert (out_big[mask].view(torch.int32) == 0).all()
+    assert torch.equal(big_state.view(torch.int16), small_state.view(torch.int16))
