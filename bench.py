@@ -61,6 +61,26 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def profiled_traffic(num_c: int):
+    """DRAM bytes of one c128_prefill pool launch, from the committed ncu summary:
+    its per-record traffic times the records of this launch, reported only
+    while the pool kernel's source is the one that was profiled (else None)."""
+    import hashlib
+    import re
+
+    path = os.path.join(ROOT, "profiles", "c128_prefill_pool__c128_prefill_small.md")
+    try:
+        text = open(path).read()
+        per = float(re.search(r"traffic_bytes_per_compress_record: ([0-9.]+)", text).group(1))
+        want = re.search(r"source_sha256: ([0-9a-f]+)", text).group(1)
+        h = hashlib.sha256()
+        for f in ("pool_c128.cu", "common.cuh"):
+            h.update(open(os.path.join(ROOT, "compressed_kv_attention_compressplan_gb300", "csrc", f), "rb").read())
+        return per * num_c if h.hexdigest() == want else None
+    except Exception:
+        return None
+
+
 def elem(dt: torch.dtype) -> int:
     return 2 if dt == torch.bfloat16 else 4
 
@@ -490,7 +510,9 @@ def bench_step(args, ws, rank, local):
                    "algorithmic_bytes_per_step": step_bytes},
         "roofline": {"bound": "hbm", "kernel": "c128_pool_kernel (prefill)", "achieved": pool_gbs, "peak": peak,
                      "unit": "GB/s", "frac": pool_gbs / peak, "peak_kind": f"{peak_kind} hbm_gbs",
-                     "traffic": None, "algorithmic_bytes": b5["pool"], "avg_launch_ms": pool_ms},
+                     "traffic": profiled_traffic(b5["num_c"]), "traffic_source": "profiles/c128_prefill_pool__c128_prefill_small.md "
+                     "(ncu dram bytes per compress record x records)", "algorithmic_bytes": b5["pool"],
+                     "avg_launch_ms": pool_ms},
         "kernels": {
             "plan_prefill_us": float(seg_ms[:, 0].mean()) * 1e3,
             "pool_prefill_us": pool_ms * 1e3, "pool_prefill_gbs": pool_gbs,

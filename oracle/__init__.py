@@ -52,25 +52,39 @@ class OracleError(RuntimeError):
         self.code = code
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (plain C11, -O2, no fp contraction)."""
+def build(force: bool = False, mutant: int = 0) -> str:
+    """Compile the oracle with gcc (plain C11, -O2, no fp contraction).
+
+    ``mutant`` > 0 builds a test-only variant with one planted mistake (the
+    mutation check of the pins); the oracle proper is mutant 0."""
     os.makedirs(_LIB_DIR, exist_ok=True)
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
-        return _LIB
-    tmp = _LIB + f".tmp{os.getpid()}"
+    lib = _LIB if mutant == 0 else os.path.join(_LIB_DIR, f"libckv_oracle_mutant{mutant}.so")
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= os.path.getmtime(_SRC):
+        return lib
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-Wall", "-shared", "-fPIC",
-           "-o", tmp, _SRC, "-lm"]
+           f"-DORC_MUTANT={int(mutant)}", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB)
-    return _LIB
+    os.replace(tmp, lib)
+    return lib
 
 
-def _load():
+def use_library(path: str | None):
+    """Test-only: route the functions of this module to another build (None = the oracle)."""
+    global _lib
+    with _lock:
+        _lib = None
+    if path is not None:
+        _load(path)
+
+
+def _load(path: str | None = None):
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB)
+            if path is None:
+                path = build()
+            lib = ctypes.CDLL(path)
             vp, u32, i32, u64 = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int, ctypes.c_uint64
             lib.orc_plan_decode.argtypes = [i32, vp, vp, u32, vp]
             lib.orc_plan_prefill.argtypes = [i32, vp, vp, vp, u32, u32, u32, u32, i32, vp, vp, vp]

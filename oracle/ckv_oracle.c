@@ -23,6 +23,13 @@
  */
 #include <math.h>
 #include <stdint.h>
+
+/* Test-only: a build with ORC_MUTANT = k > 0 plants one plausible mistake
+ * (see the numbered sites below), so that the test-suite can show that every
+ * such mistake fails at least one pin.  The oracle proper is ORC_MUTANT = 0. */
+#ifndef ORC_MUTANT
+#define ORC_MUTANT 0
+#endif
 #include <stdlib.h>
 #include <string.h>
 
@@ -156,7 +163,8 @@ static void pool_window(int ratio, int hd, int in_dtype, int out_dtype, const vo
       if (!entries[i]) continue;
       int sc_col = ratio == 4 ? (i < 4 ? 2 * hd : 3 * hd) + c : hd + c;
       float score = load_elem(entries[i], (size_t)sc_col, in_dtype);
-      float bias = load_elem(ape, (size_t)i * hd + c, in_dtype);
+      int arow = ORC_MUTANT == 1 ? (i + 1) % W : i; /* mutant 1: ape row off by one */
+      float bias = load_elem(ape, (size_t)arow * hd + c, in_dtype);
       float si = score + bias; /* one fp32 rounding */
       s[i] = si;
       if (!have || si > m) m = si;
@@ -165,11 +173,11 @@ static void pool_window(int ratio, int hd, int in_dtype, int out_dtype, const vo
     double num = 0.0, den = 0.0;
     for (int i = 0; i < W; ++i) {
       if (!entries[i]) continue;
-      int kv_col = (ratio == 4) ? (i < 4 ? 0 : hd) + c : c;
+      int kv_col = (ratio == 4) ? (i < 4 ? (ORC_MUTANT == 2 ? hd : 0) : hd) + c : c; /* mutant 2: halves */
       double kv = (double)load_elem(entries[i], (size_t)kv_col, in_dtype);
-      double w = exp((double)s[i] - (double)m);
+      double w = ORC_MUTANT == 10 ? exp((double)m - (double)s[i]) : exp((double)s[i] - (double)m); /* 10: sign */
       num += kv * w;
-      den += w;
+      if (!(ORC_MUTANT == 9 && i == W - 1)) den += w; /* mutant 9: a dropped term */
     }
     store_elem(out_row, (size_t)c, out_dtype, have ? num / den : 0.0);
   }
@@ -200,7 +208,7 @@ int orc_plan_decode(int ratio, const int64_t* rid, const int64_t* seq_lens, uint
     if (seq_lens[b] < 1 || seq_lens[b] > INT32_MAX || rid[b] < 0) return ORC_BAD_LENGTH;
     int64_t p1 = seq_lens[b] - 1;
     int64_t p0 = p1 - ratio > 0 ? p1 - ratio : 0;
-    int64_t loc = legacy_loc(ratio, rid[b], p1);
+    int64_t loc = legacy_loc(ratio, rid[b], ORC_MUTANT == 6 ? p1 + 1 : p1); /* mutant 6: write slot */
     if (loc > INT32_MAX) return ORC_BAD_INDEX;
     plan[b].seq_len = (uint32_t)seq_lens[b];
     plan[b].write_loc = (int32_t)loc;
@@ -237,14 +245,14 @@ int orc_plan_prefill(int ratio, const int64_t* rid, const int64_t* seq_lens, con
     const int64_t sl = seq_lens[b], el = extend_lens[b];
     if (!(0 < el && el <= sl) || sl > INT32_MAX || rid[b] < 0) return ORC_BAD_LENGTH;
     const int64_t pl = sl - el;
-    const int64_t first_w = (sl / ratio) * ratio - overlap;
+    const int64_t first_w = (sl / ratio) * ratio - (ORC_MUTANT == 5 ? 0 : overlap); /* mutant 5: write set */
     for (int64_t j = 0; j < el; ++j) {
       const int64_t p = pl + j;
-      const uint64_t ragged = token_base + (uint64_t)j;
+      const uint64_t ragged = (ORC_MUTANT == 7 ? 0 : token_base) + (uint64_t)j; /* mutant 7: ragged base */
       if ((p + 1) % ratio == 0) {
         if (nc < cap_c) {
-          const int64_t bl = W - (j + 1 < W ? j + 1 : W);
-          const int64_t p0 = p - ratio > 0 ? p - ratio : 0;
+          const int64_t bl = W - (j + 1 < W ? j + 1 : W) - (ORC_MUTANT == 4 && j + 1 < W ? 1 : 0); /* 4 */
+          const int64_t p0 = ORC_MUTANT == 8 ? p : (p - ratio > 0 ? p - ratio : 0); /* mutant 8 */
           pc[nc].seq_len = (uint32_t)(p + 1);
           pc[nc].ragged_bl = (uint32_t)ragged | ((uint32_t)bl << 24);
           pc[nc].read_page_0 = (int32_t)legacy_page(ratio, rid[b], p0);
@@ -304,7 +312,7 @@ int orc_compress_pool_prefill(int ratio, int hd, int in_dtype, int out_dtype, co
     const int64_t seq_len = P->seq_len;
     if (ragged >= num_q_tokens) { free(entries); return ORC_BAD_INDEX; }
     for (int i = 0; i < W; ++i) {
-      if (ratio == 4 && seq_len == 4 && i < 4) { /* first group: no previous group */
+      if (ORC_MUTANT != 3 && ratio == 4 && seq_len == 4 && i < 4) { /* first group: no previous group */
         entries[i] = NULL;
         continue;
       }
@@ -314,7 +322,7 @@ int orc_compress_pool_prefill(int ratio, int hd, int in_dtype, int out_dtype, co
         if (srow < 0 || (uint64_t)srow >= state_rows) { free(entries); return ORC_BAD_INDEX; }
         entries[i] = row_ptr(state, srow, width, in_dtype);
       } else {
-        int64_t irow = ragged - (W - 1) + i;
+        int64_t irow = ragged - (W - 1) + i - (ORC_MUTANT == 11 ? 1 : 0); /* mutant 11: input row */
         if (irow < 0) { free(entries); return ORC_BAD_INDEX; }
         entries[i] = row_ptr(input, irow, width, in_dtype);
       }
@@ -366,7 +374,7 @@ int orc_compress_decode(int ratio, int hd, int in_dtype, int out_dtype, void* st
     memcpy((char*)state + (size_t)P->write_loc * row_bytes, row_ptr(input, b, width, in_dtype), row_bytes);
     if (P->seq_len % (uint32_t)ratio != 0) continue;
     for (int i = 0; i < W; ++i) {
-      if (ratio == 4 && P->seq_len == 4 && i < 4) {
+      if (ORC_MUTANT != 3 && ratio == 4 && P->seq_len == 4 && i < 4) {
         entries[i] = NULL;
         continue;
       }

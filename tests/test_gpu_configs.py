@@ -1,0 +1,106 @@
+"""Parity at the five workloads' full sizes, in the launch configuration the
+benchmark times (capacities from ckv_capacity_*, no padding, plan -> pool ->
+write on one stream; plan -> decode).
+
+Plans and state buffers are compared with the oracle byte for byte; decode
+outputs in full; prefill outputs on a seeded sample of compress records that
+the oracle pools one by one, plus every non-compress row of token layouts
+(which must be +0.0).
+"""
+import numpy as np
+import pytest
+import torch
+
+from compressed_kv_attention_compressplan_gb300 import workloads as wl
+from tests import helpers as H
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module")
+def env(oracle_mod):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from compressed_kv_attention_compressplan_gb300 import build as B
+    from compressed_kv_attention_compressplan_gb300 import ckv
+
+    B.build()
+    ckv.load_library()
+    return oracle_mod, ckv, torch.device("cuda")
+
+
+def code(dt):
+    return 1 if dt == torch.bfloat16 else 0
+
+
+@pytest.mark.parametrize("name", ["c4_prefill_small", "c4_prefill", "c128_prefill"])
+def test_prefill_workload_full_size(env, name):
+    o, ckv, dev = env
+    w = wl.NAMED[name](0)
+    R, hd = w.ratio, w.head_dim
+    ci, co = code(w.in_dtype), code(w.out_dtype)
+    nq = w.num_q_tokens
+    cap_c = ckv.capacity_compress(R, w.batch, nq)
+    cap_w = ckv.capacity_write(R, w.batch, nq)
+    state_d = w.state.to(dev)
+    kv_d = w.kv_score.to(dev)
+    status = ckv.new_status(dev)
+    layout = ckv.OUT_TOKEN if w.out_layout == wl.TOKEN else ckv.OUT_COMPACT
+    pc, pw, counts = ckv.plan_prefill(R, w.rid.to(dev), w.seq_lens.to(dev), w.extend_lens.to(dev), nq, cap_c, cap_w,
+                                      status=status)
+    out = ckv.compress_prefill(R, hd, state_d, kv_d, w.ape.to(dev), pc, pw, counts, layout, w.out_dtype,
+                               status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    wc, ww, (nc, nw), _ = o.plan_prefill(R, w.rid, w.seq_lens, w.extend_lens)
+    assert counts[:2].tolist() == [nc, nw]
+    assert (pc[:nc].cpu().numpy() == wc).all(), "compress plan"
+    assert (pw[:nw].cpu().numpy() == ww).all(), "write plan"
+    st = wl.bits(w.state).copy()
+    inp = wl.bits(w.kv_score)
+    ape = wl.bits(w.ape)
+    rng = np.random.default_rng(7)
+    sample = np.unique(np.concatenate([rng.choice(nc, min(nc, 192), replace=False), [0, nc - 1]]))
+    want = o.compress_pool_prefill(R, hd, ci, co, st, inp, ape, np.ascontiguousarray(wc[sample]), len(sample), nq,
+                                   o.OUT_COMPACT)
+    f = H.plan_c_fields(wc[sample])
+    kvmax = H.window_kv_absmax(R, hd, st, inp, f["seq_len"], f["ragged_id"], f["buffer_len"], f["read_page_0"],
+                               f["read_page_1"])
+    got_all = H.np_bits(out)
+    rows = f["ragged_id"] if layout == ckv.OUT_TOKEN else sample
+    H.assert_pool_close(got_all[rows], want, co, kvmax, f"{name} sampled records")
+    if layout == ckv.OUT_TOKEN:
+        others = np.setdiff1d(np.arange(nq), H.plan_c_fields(wc)["ragged_id"])
+        zero = got_all[others].view(np.uint16 if co else np.uint32)
+        assert (zero == 0).all(), "non-compress rows"
+    o.compress_write(R, hd, ci, st, inp, ww, nw)
+    assert (H.np_bits(state_d).view(np.uint8) == st.view(np.uint8)).all(), "state after write"
+
+
+@pytest.mark.parametrize("name", ["c4_decode", "c128_decode"])
+def test_decode_workload_full_size(env, name):
+    o, ckv, dev = env
+    w = wl.NAMED[name](0)
+    R, hd = w.ratio, w.head_dim
+    ci, co = code(w.in_dtype), code(w.out_dtype)
+    state_d = w.state.to(dev)
+    status = ckv.new_status(dev)
+    out, pd = ckv.decode_step(R, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), w.rid.to(dev), w.seq_lens.to(dev),
+                              w.out_dtype, status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    wpd = o.plan_decode(R, w.rid, w.seq_lens)
+    assert (pd.cpu().numpy() == wpd).all()
+    st0 = wl.bits(w.state).copy()
+    st = st0.copy()
+    inp = wl.bits(w.kv_score)
+    want = o.compress_decode(R, hd, ci, co, st, inp, wl.bits(w.ape), wpd)
+    got = H.np_bits(out)
+    f = H.plan_d_fields(wpd)
+    bnd = np.nonzero(f["seq_len"] % R == 0)[0]
+    kvmax = H.window_kv_absmax(R, hd, st0, inp, f["seq_len"][bnd], bnd, np.full(len(bnd), H.window(R) - 1),
+                               f["read_page_0"][bnd], f["read_page_1"][bnd])
+    H.assert_pool_close(got[bnd], want[bnd], co, kvmax, f"{name} boundary rows")
+    nb = np.setdiff1d(np.arange(w.batch), bnd)
+    assert (got[nb].view(np.uint16 if co else np.uint32) == 0).all()
+    assert (H.np_bits(state_d).view(np.uint8) == st.view(np.uint8)).all(), "state after decode"
