@@ -199,37 +199,74 @@ __device__ __forceinline__ void zero_rows(TOut* out, int hd, int c0, int64_t r0,
 }
 
 // ---------------------------------------------------------------- the per-thread arithmetic
-// Thread (q, g) owns channels cq = 4q .. 4q+3 of the tile and entries
-// 16g .. 16g+15.  ape_at(k, v) yields ape[16g + k][c0 + cq + 0..3] as fp32.
+// Thread (q, g) owns channels cq = 4q .. 4q+3 of the tile (two fp32 pairs) and
+// entries 16g .. 16g+15.  ape_at(k, v) yields ape[16g + k][c0 + cq + 0..3] as
+// two fp32 pairs.
+
+// Four channels of a staged entry as two fp32 pairs.
+template <typename TIn>
+__device__ __forceinline__ void load4x2(const TIn* p, F2 (&v)[2]);
+
+template <>
+__device__ __forceinline__ void load4x2<__nv_bfloat16>(const __nv_bfloat16* p, F2 (&v)[2]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  v[0] = f2_from_bf16x2(u.x);
+  v[1] = f2_from_bf16x2(u.y);
+}
+
+template <>
+__device__ __forceinline__ void load4x2<float>(const float* p, F2 (&v)[2]) {
+  const float4 u = *reinterpret_cast<const float4*>(p);
+  v[0] = f2_pack(u.x, u.y);
+  v[1] = f2_pack(u.z, u.w);
+}
+
+// The same from global memory through the read-only path (ape).
+template <typename TIn>
+__device__ __forceinline__ void ldg4x2(const TIn* p, F2 (&v)[2]) {
+  float f[4];
+  ldg4<TIn>(p, f);
+  v[0] = f2_pack(f[0], f[1]);
+  v[1] = f2_pack(f[2], f[3]);
+}
+
+__device__ __forceinline__ void max_into(float (&m)[4], const F2 (&s)[2]) {
+  float x0, x1, x2, x3;
+  f2_unpack(s[0], x0, x1);
+  f2_unpack(s[1], x2, x3);
+  m[0] = fmaxf(m[0], x0);
+  m[1] = fmaxf(m[1], x1);
+  m[2] = fmaxf(m[2], x2);
+  m[3] = fmaxf(m[3], x3);
+}
+
 template <typename TIn, int CS, typename ApeAt>
-__device__ __forceinline__ void c128_pass1(const TIn* sc_s, int g, int cq, ApeAt ape_at, float (&s)[16][4],
+__device__ __forceinline__ void c128_pass1(const TIn* sc_s, int g, int cq, ApeAt ape_at, F2 (&s)[16][2],
                                            float (&m)[4]) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) m[j] = -INFINITY;
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
-    float sc[4], bias[4];
-    load4<TIn>(sc_s + (16 * g + k) * CS + cq, sc);
+    F2 sc[2], bias[2];
+    load4x2<TIn>(sc_s + (16 * g + k) * CS + cq, sc);
     ape_at(k, bias);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      s[k][j] = score_plus_bias(sc[j], bias[j]);
-      m[j] = fmaxf(m[j], s[k][j]);
-    }
+    s[k][0] = score_plus_bias2(sc[0], bias[0]);
+    s[k][1] = score_plus_bias2(sc[1], bias[1]);
+    max_into(m, s[k]);
   }
 }
 
 template <typename TIn, int CS>
-__device__ __forceinline__ void c128_pass2(const TIn* kv_s, int g, int cq, const float (&s)[16][4],
-                                           const float (&nml)[4], PoolAcc (&acc)[4]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j].init();
+__device__ __forceinline__ void c128_pass2(const TIn* kv_s, int g, int cq, const F2 (&s)[16][2], const F2 (&nml)[2],
+                                           PoolAcc2 (&acc)[2]) {
+  acc[0].init();
+  acc[1].init();
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
-    float kv[4];
-    load4<TIn>(kv_s + (16 * g + k) * CS + cq, kv);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j].add(kv[j], weight_of(s[k][j], nml[j]));
+    F2 kv[2];
+    load4x2<TIn>(kv_s + (16 * g + k) * CS + cq, kv);
+    acc[0].add(kv[0], weight_of2(s[k][0], nml[0]));
+    acc[1].add(kv[1], weight_of2(s[k][1], nml[1]));
   }
 }
 
@@ -237,17 +274,17 @@ __device__ __forceinline__ void c128_pass2(const TIn* kv_s, int g, int cq, const
 // score and ape with the same single rounding, so the result is identical.
 template <typename TIn, int CS, typename ApeAt>
 __device__ __forceinline__ void c128_pass2_recompute(const TIn* kv_s, const TIn* sc_s, int g, int cq, ApeAt ape_at,
-                                                     const float (&nml)[4], PoolAcc (&acc)[4]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j].init();
+                                                     const F2 (&nml)[2], PoolAcc2 (&acc)[2]) {
+  acc[0].init();
+  acc[1].init();
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
-    float kv[4], sc[4], bias[4];
-    load4<TIn>(kv_s + (16 * g + k) * CS + cq, kv);
-    load4<TIn>(sc_s + (16 * g + k) * CS + cq, sc);
+    F2 kv[2], sc[2], bias[2];
+    load4x2<TIn>(kv_s + (16 * g + k) * CS + cq, kv);
+    load4x2<TIn>(sc_s + (16 * g + k) * CS + cq, sc);
     ape_at(k, bias);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j].add(kv[j], weight_of(score_plus_bias(sc[j], bias[j]), nml[j]));
+    acc[0].add(kv[0], weight_of2(score_plus_bias2(sc[0], bias[0]), nml[0]));
+    acc[1].add(kv[1], weight_of2(score_plus_bias2(sc[1], bias[1]), nml[1]));
   }
 }
 
@@ -258,30 +295,47 @@ __device__ __forceinline__ void c128_max_only(const TIn* sc_s, int g, int cq, Ap
   for (int j = 0; j < 4; ++j) m[j] = -INFINITY;
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
-    float sc[4], bias[4];
-    load4<TIn>(sc_s + (16 * g + k) * CS + cq, sc);
+    F2 sc[2], bias[2], s[2];
+    load4x2<TIn>(sc_s + (16 * g + k) * CS + cq, sc);
     ape_at(k, bias);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) m[j] = fmaxf(m[j], score_plus_bias(sc[j], bias[j]));
+    s[0] = score_plus_bias2(sc[0], bias[0]);
+    s[1] = score_plus_bias2(sc[1], bias[1]);
+    max_into(m, s);
   }
 }
 
-// Channel maximum over the 8 groups' partial maxima (exact in any order).
+// Channel maximum over the 8 groups' partial maxima (exact in any order),
+// returned as -max*log2(e) for the channel pairs.
 template <int CS>
-__device__ __forceinline__ void c128_nml(const float* red_m, int cq, float (&nml)[4]) {
+__device__ __forceinline__ void c128_nml(const float* red_m, int cq, F2 (&nml)[2]) {
+  float n[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     float mm = red_m[cq + j];
 #pragma unroll
     for (int gg = 1; gg < 8; ++gg) mm = fmaxf(mm, red_m[gg * CS + cq + j]);
-    nml[j] = neg_max_log2e(mm);
+    n[j] = neg_max_log2e(mm);
   }
+  nml[0] = f2_pack(n[0], n[1]);
+  nml[1] = f2_pack(n[2], n[3]);
+}
+
+// Group partials (l, a) of the four channels into the reduction buffers.
+template <int CS>
+__device__ __forceinline__ void store_partials(float* red_l, float* red_a, int g, int cq, const PoolAcc2 (&acc)[2]) {
+  float l0, l1, l2, l3, a0, a1, a2, a3;
+  f2_unpack(acc[0].l, l0, l1);
+  f2_unpack(acc[1].l, l2, l3);
+  f2_unpack(acc[0].a, a0, a1);
+  f2_unpack(acc[1].a, a2, a3);
+  *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(l0, l1, l2, l3);
+  *reinterpret_cast<float4*>(red_a + g * CS + cq) = make_float4(a0, a1, a2, a3);
 }
 
 template <typename TIn>
-__device__ __forceinline__ void load_ape_regs(const TIn* ape, int hd, int c0, int g, int cq, float (&ape_r)[16][4]) {
+__device__ __forceinline__ void load_ape_regs(const TIn* ape, int hd, int c0, int g, int cq, F2 (&ape_r)[16][2]) {
 #pragma unroll
-  for (int k = 0; k < 16; ++k) ldg4<TIn>(ape + static_cast<size_t>(16 * g + k) * hd + c0 + cq, ape_r[k]);
+  for (int k = 0; k < 16; ++k) ldg4x2<TIn>(ape + static_cast<size_t>(16 * g + k) * hd + c0 + cq, ape_r[k]);
 }
 
 // Issues the 256 bulk copies of one tile (called by all 32 lanes of a warp).
@@ -461,7 +515,7 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
   const int q = tl % T::QUADS;
   const int g = tl / T::QUADS;
   const int cq = 4 * q;
-  float ape_r[16][4];
+  F2 ape_r[16][2];
   if (kDecode && warp < NC / 32) load_ape_regs<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
 
   pdl_wait();  // everything below may read what the previous kernel wrote
@@ -615,24 +669,24 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
     }
     float* red_l = red_base + (2 * grp + (local & 1u)) * T::RED_FLOATS;
     float* red_a = red_l + 8 * CS;
-    PoolAcc acc[4];
     if (ok) {
       const TIn* kv_s = reinterpret_cast<const TIn*>(smem + stage * T::TILE_BYTES);
       const TIn* sc_s = kv_s + 128 * CS;
-      float s[16][4], m[4], nml[4];
+      F2 s[16][2], nml[2];
+      float m[4];
       c128_pass1<TIn, CS>(sc_s, g, cq,
-                          [&](int k, float (&v)[4]) {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) v[j] = ape_r[k][j];
+                          [&](int k, F2 (&v)[2]) {
+                            v[0] = ape_r[k][0];
+                            v[1] = ape_r[k][1];
                           },
                           s, m);
       *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(m[0], m[1], m[2], m[3]);
       group_sync(grp, NCG);
       c128_nml<CS>(red_l, cq, nml);
       group_sync(grp, NCG);
+      PoolAcc2 acc[2];
       c128_pass2<TIn, CS>(kv_s, g, cq, s, nml, acc);
-      *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(acc[0].l, acc[1].l, acc[2].l, acc[3].l);
-      *reinterpret_cast<float4*>(red_a + g * CS + cq) = make_float4(acc[0].a, acc[1].a, acc[2].a, acc[3].a);
+      store_partials<CS>(red_l, red_a, g, cq, acc);
       group_sync(grp, NCG);
     }
     // the stage is no longer read: hand it back to the producer
@@ -733,21 +787,21 @@ __global__ __launch_bounds__(DecodeCfg<TIn>::THREADS, 6) void c128_decode_kernel
   const int g = t / Cfg::QUADS;
   const int cq = 4 * q;
   const TIn* ape = static_cast<const TIn*>(a.ape) + static_cast<size_t>(16 * g) * hd + c0 + cq;
-  auto ape_at = [&](int k, float (&v)[4]) { ldg4<TIn>(ape + static_cast<size_t>(k) * hd, v); };
+  auto ape_at = [&](int k, F2 (&v)[2]) { ldg4x2<TIn>(ape + static_cast<size_t>(k) * hd, v); };
   if (!mbar_wait_bounded(bar, 0, kWaitLimitNs)) {
     status_or(a.d_status, CKV_STATUS_TIMEOUT);
     mbar_wait_bounded(bar, 0, kWaitLimitNs);  // let copies in flight land before the CTA can exit
   }
-  float m[4], nml[4];
+  float m[4];
+  F2 nml[2];
   c128_max_only<TIn, CS>(sc_s, g, cq, ape_at, m);
   *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(m[0], m[1], m[2], m[3]);
   __syncthreads();
   c128_nml<CS>(red_l, cq, nml);
   __syncthreads();
-  PoolAcc acc[4];
+  PoolAcc2 acc[2];
   c128_pass2_recompute<TIn, CS>(kv_s, sc_s, g, cq, ape_at, nml, acc);
-  *reinterpret_cast<float4*>(red_l + g * CS + cq) = make_float4(acc[0].l, acc[1].l, acc[2].l, acc[3].l);
-  *reinterpret_cast<float4*>(red_a + g * CS + cq) = make_float4(acc[0].a, acc[1].a, acc[2].a, acc[3].a);
+  store_partials<CS>(red_l, red_a, g, cq, acc);
   __syncthreads();
   if (t < CS) store1<TOut>(out + static_cast<size_t>(b) * hd + c0 + t, finish(tree8(red_a + t, CS), tree8(red_l + t, CS)));
 }

@@ -30,6 +30,8 @@ struct C4Vec {
 };
 
 // The C4 window pool for VEC channels.  Entries below `first` are masked.
+// (Scalar form: with 16 kv/score vectors live, the packed fp32x2 form of the
+// same operations needs more registers than this kernel can spare.)
 template <typename TIn, int VEC>
 __device__ __forceinline__ void c4_pool_chunk(const uint4 (&kv)[8], const uint4 (&sc)[8], const uint4 (&ap)[8],
                                               int first, float (&res)[VEC]) {
