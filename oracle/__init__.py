@@ -92,6 +92,10 @@ def _load(path: str | None = None):
             lib.orc_compress_write.argtypes = [i32, i32, i32, vp, u64, vp, u32, vp, u32]
             lib.orc_compress_decode.argtypes = [i32, i32, i32, i32, vp, u64, vp, vp, vp, u32, vp]
             lib.orc_compress_history.argtypes = [i32, i32, i32, i32, vp, u32, vp, vp]
+            i64 = ctypes.c_int64
+            lib.orc_plan_prefill_paged.argtypes = [i32, vp, vp, i64, u32, vp, u64, i32, i32, vp, vp, u32, u32, u32,
+                                                   u32, i32, vp, vp, vp]
+            lib.orc_plan_decode_paged.argtypes = [i32, vp, vp, i64, u32, vp, u64, i32, i32, vp, u32, vp]
             lib.orc_double_to_bf16.argtypes = [ctypes.c_double]
             lib.orc_double_to_bf16.restype = ctypes.c_uint16
             _lib = lib
@@ -155,6 +159,49 @@ def plan_prefill(ratio: int, rid, seq_lens, extend_lens, num_q_tokens: int | Non
     if check and rc:
         raise OracleError(rc, "plan_prefill")
     return pc[:cap_c], pw[:cap_w], (int(counts[0]), int(counts[1])), rc
+
+
+def _maps(req_to_token, full_to_state):
+    """The two SWA maps as C arrays (C128 reads neither: None stands for none)."""
+    if req_to_token is None:
+        return np.zeros((1, 1), np.int32), np.zeros(1, np.int64)
+    return np.ascontiguousarray(np.asarray(req_to_token, dtype=np.int32)), _i64(full_to_state)
+
+
+def plan_prefill_paged(ratio: int, rid, req_to_token, full_to_state, swa_page_size: int, ring_size: int, seq_lens,
+                       extend_lens, num_q_tokens: int | None = None, cap_c: int | None = None,
+                       cap_w: int | None = None, pad_invalid: bool = False, check: bool = True):
+    """SWA-paged prefill plans (see ckv_oracle.c); same return value as plan_prefill."""
+    rid, sl, el = _i64(rid), _i64(seq_lens), _i64(extend_lens)
+    r2t, f2s = _maps(req_to_token, full_to_state)
+    nq = int(el.sum()) if num_q_tokens is None else int(num_q_tokens)
+    lib = _load()
+    counts = np.zeros(2, dtype=np.uint32)
+    args = (ratio, _p(rid), _p(r2t), r2t.shape[1], r2t.shape[0], _p(f2s), f2s.size, swa_page_size, ring_size,
+            _p(sl), _p(el), len(rid), nq)
+    if cap_c is None or cap_w is None:
+        dc, dw = np.zeros((1, 16), np.uint8), np.zeros((1, 8), np.uint8)
+        lib.orc_plan_prefill_paged(*args, 0, 0, 0, _p(dc), _p(dw), _p(counts))
+        cap_c = int(counts[0]) if cap_c is None else cap_c
+        cap_w = int(counts[1]) if cap_w is None else cap_w
+    pc = np.zeros((max(cap_c, 1), 16), dtype=np.uint8)
+    pw = np.zeros((max(cap_w, 1), 8), dtype=np.uint8)
+    rc = lib.orc_plan_prefill_paged(*args, cap_c, cap_w, int(pad_invalid), _p(pc), _p(pw), _p(counts))
+    if check and rc:
+        raise OracleError(rc, "plan_prefill_paged")
+    return pc[:cap_c], pw[:cap_w], (int(counts[0]), int(counts[1])), rc
+
+
+def plan_decode_paged(ratio: int, rid, req_to_token, full_to_state, swa_page_size: int, ring_size: int,
+                      seq_lens) -> np.ndarray:
+    rid, sl = _i64(rid), _i64(seq_lens)
+    r2t, f2s = _maps(req_to_token, full_to_state)
+    out = np.zeros((len(rid), 16), dtype=np.uint8)
+    rc = _load().orc_plan_decode_paged(ratio, _p(rid), _p(r2t), r2t.shape[1], r2t.shape[0], _p(f2s), f2s.size,
+                                       swa_page_size, ring_size, _p(sl), len(rid), _p(out))
+    if rc:
+        raise OracleError(rc, "plan_decode_paged")
+    return out
 
 
 def decode_plan_fields(plan_c: np.ndarray) -> dict:
@@ -232,7 +279,7 @@ def compress_history(ratio, hd, in_dtype, out_dtype, tokens, ape) -> np.ndarray:
 
 def compress_prefill(ratio, hd, in_dtype, out_dtype, state: np.ndarray, inp, ape, rid, seq_lens, extend_lens,
                      out_layout=OUT_TOKEN):
-    """Plan, pool, then write (the order the pages' prefill launcher uses)."""
+    """Plan, pool, then write (the order of compressor_v2.py's prefill launcher)."""
     pc, pw, (nc, nw), _ = plan_prefill(ratio, rid, seq_lens, extend_lens)
     out = compress_pool_prefill(ratio, hd, in_dtype, out_dtype, state, inp, ape, pc, nc,
                                 num_q_tokens=int(_i64(extend_lens).sum()), out_layout=out_layout)

@@ -281,6 +281,130 @@ int orc_plan_prefill(int ratio, const int64_t* rid, const int64_t* seq_lens, con
   return ORC_OK;
 }
 
+/* ----- SWA-paged plans ([c_plan] plan_compress_prefill / _decode, main path) */
+
+/* State row of position p of request rid through the SWA mapping ([c_plan]
+ * compute_loc): swa = full_to_state[req_to_token[rid][p]], row =
+ * (swa / swa_page_size) * ring_size + swa % ring_size.  -1 when a map entry is
+ * out of range. */
+static int64_t paged_row(const int32_t* r2t, int64_t stride, const int64_t* f2s, uint64_t nfull, int32_t sps,
+                         int32_t ring, int64_t rid, int64_t p) {
+  const int32_t raw = r2t[rid * stride + p];
+  if (raw < 0 || (uint64_t)raw >= nfull) return -1;
+  const int64_t swa = f2s[raw];
+  if (swa < 0) return -1;
+  return (swa / sps) * ring + swa % (ORC_MUTANT == 13 ? sps : ring); /* mutant 13: ring offset */
+}
+
+/* State row of position p under the paged addressing: C4 through the SWA
+ * mapping (paged_row), C128 request-scoped rid * ring + p % ring ([c_plan]
+ * compute_c128_loc). */
+static int64_t paged_or_c128_row(int ratio, const int32_t* r2t, int64_t stride, const int64_t* f2s, uint64_t nfull,
+                                 int32_t sps, int32_t ring, int64_t rid, int64_t p) {
+  if (ratio == 128) return rid * ring + p % ring;
+  return paged_row(r2t, stride, f2s, nfull, sps, ring, rid, p);
+}
+
+/* Prefill plans with SWA-paged state: the CPU loop of [c_plan]
+ * plan_compress_prefill (C4 writes every p >= first_w and, as the ratio
+ * overlaps, the last ratio positions of every SWA page), with first_w =
+ * min((sl/R)*R - (C4 ? 4 : 0), sl - mtp_pad), mtp_pad = min(ring - R, 4) as the
+ * GPU-input planner has it; then kernel_1's translation of positions into
+ * rows and pages, which it applies to compress records with buffer_len > 0
+ * only -- the others keep read_page_0 = -1, read_page_1 = batch index.
+ * C128 needs ring 128 (its pooling reads the window from read_page_0). */
+int orc_plan_prefill_paged(int ratio, const int64_t* rid, const int32_t* r2t, int64_t stride, uint32_t num_reqs,
+                           const int64_t* f2s, uint64_t nfull, int32_t sps, int32_t ring, const int64_t* seq_lens,
+                           const int64_t* extend_lens, uint32_t batch, uint32_t num_q_tokens, uint32_t cap_c,
+                           uint32_t cap_w, int pad_invalid, void* plan_c_out, void* plan_w_out, uint32_t* counts) {
+  if (ratio != 4 && ratio != 128) return ORC_BAD_RATIO;
+  if (batch > 1024 || num_q_tokens >= (1u << 24)) return ORC_BAD_BATCH;
+  if (ratio == 128 && ring != 128) return ORC_BAD_BATCH;
+  if (ratio == 4 && (sps <= 0 || ring < 8 || ring % 4 || sps % ring)) return ORC_BAD_BATCH;
+  const int W = ratio == 4 ? 8 : 128;
+  const int64_t mtp_pad = ring - ratio < 4 ? ring - ratio : 4;
+  orc_plan_c* pc = (orc_plan_c*)plan_c_out;
+  orc_plan_w* pw = (orc_plan_w*)plan_w_out;
+  uint64_t token_base = 0, nc = 0, nw = 0;
+  for (uint32_t b = 0; b < batch; ++b) {
+    const int64_t sl = seq_lens[b], el = extend_lens[b];
+    if (!(0 < el && el <= sl) || sl > INT32_MAX || rid[b] < 0) return ORC_BAD_LENGTH;
+    if (ratio == 4 && ((uint64_t)rid[b] >= num_reqs || sl > stride)) return ORC_BAD_INDEX;
+    const int64_t pl = sl - el;
+    int64_t first_w = (sl / ratio) * ratio - (ratio == 4 ? 4 : 0);
+    if (sl - mtp_pad < first_w) first_w = sl - mtp_pad;
+    for (int64_t j = 0; j < el; ++j) {
+      const int64_t p = pl + j;
+      const uint64_t ragged = token_base + (uint64_t)j;
+      if ((p + 1) % ratio == 0) {
+        if (nc < cap_c) {
+          const int64_t bl = W - (j + 1 < W ? j + 1 : W);
+          int64_t page0 = -1, page1 = b;
+          if (bl > 0 || ORC_MUTANT == 14) { /* mutant 14: records without state reads translated */
+            const int64_t p0 = p - ratio > 0 ? p - ratio : 0;
+            const int64_t row0 = paged_or_c128_row(ratio, r2t, stride, f2s, nfull, sps, ring, rid[b], p0);
+            const int64_t row1 = paged_or_c128_row(ratio, r2t, stride, f2s, nfull, sps, ring, rid[b], p);
+            if (row0 < 0 || row1 < 0) return ORC_BAD_INDEX;
+            page0 = row0 / ratio;
+            page1 = row1 / ratio;
+          }
+          pc[nc].seq_len = (uint32_t)(p + 1);
+          pc[nc].ragged_bl = (uint32_t)ragged | ((uint32_t)bl << 24);
+          pc[nc].read_page_0 = (int32_t)page0;
+          pc[nc].read_page_1 = (int32_t)page1;
+        }
+        ++nc;
+      }
+      if (p >= first_w || (ORC_MUTANT != 12 && ratio == 4 && p % sps >= sps - ratio)) { /* 12: page ends */
+        if (nw < cap_w) {
+          const int64_t row = paged_or_c128_row(ratio, r2t, stride, f2s, nfull, sps, ring, rid[b], p);
+          if (row < 0) return ORC_BAD_INDEX;
+          pw[nw].ragged_id = (uint32_t)ragged;
+          pw[nw].write_loc = (int32_t)row;
+        }
+        ++nw;
+      }
+    }
+    token_base += (uint64_t)el;
+  }
+  counts[0] = (uint32_t)nc;
+  counts[1] = (uint32_t)nw;
+  if (token_base != num_q_tokens) return ORC_BAD_TOTAL;
+  if (nc > cap_c || nw > cap_w) return ORC_CAPACITY;
+  if (pad_invalid) {
+    if (cap_c > nc) memset(pc + nc, 0xFF, sizeof(orc_plan_c) * (cap_c - nc));
+    if (cap_w > nw) memset(pw + nw, 0xFF, sizeof(orc_plan_w) * (cap_w - nw));
+  }
+  return ORC_OK;
+}
+
+/* Decode plan with SWA-paged state ([c_plan] plan_compress_decode_kernel):
+ * write_loc = row of position seq_len-1, read pages = rows of positions
+ * max(seq_len-1-4, 0) and seq_len-1, divided by 4.  C128 with its 128-row ring
+ * (compute_c128_loc) is the legacy plan. */
+int orc_plan_decode_paged(int ratio, const int64_t* rid, const int32_t* r2t, int64_t stride, uint32_t num_reqs,
+                          const int64_t* f2s, uint64_t nfull, int32_t sps, int32_t ring, const int64_t* seq_lens,
+                          uint32_t batch, void* plan_d_out) {
+  if (ratio == 128) return ring == 128 ? orc_plan_decode(ratio, rid, seq_lens, batch, plan_d_out) : ORC_BAD_BATCH;
+  if (ratio != 4) return ORC_BAD_RATIO;
+  if (sps <= 0 || ring < 8 || ring % 4 || sps % ring) return ORC_BAD_BATCH;
+  orc_plan_d* plan = (orc_plan_d*)plan_d_out;
+  for (uint32_t b = 0; b < batch; ++b) {
+    if (seq_lens[b] < 1 || seq_lens[b] > INT32_MAX || rid[b] < 0) return ORC_BAD_LENGTH;
+    if ((uint64_t)rid[b] >= num_reqs || seq_lens[b] > stride) return ORC_BAD_INDEX;
+    const int64_t p1 = seq_lens[b] - 1;
+    const int64_t p0 = p1 - 4 > 0 ? p1 - 4 : 0;
+    const int64_t row1 = paged_row(r2t, stride, f2s, nfull, sps, ring, rid[b], p1);
+    const int64_t row0 = paged_row(r2t, stride, f2s, nfull, sps, ring, rid[b], p0);
+    if (row0 < 0 || row1 < 0) return ORC_BAD_INDEX;
+    plan[b].seq_len = (uint32_t)seq_lens[b];
+    plan[b].write_loc = (int32_t)row1;
+    plan[b].read_page_0 = (int32_t)(row0 / 4);
+    plan[b].read_page_1 = (int32_t)(row1 / 4);
+  }
+  return ORC_OK;
+}
+
 /* ----- the compute steps ------------------------------------------------- */
 
 /* Prefill pooling, one compressed row per compress-plan entry ([c4]

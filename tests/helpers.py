@@ -116,16 +116,18 @@ def split_schedule(total: int, rng: np.random.Generator, max_chunk: int, decode_
     return steps
 
 
-def run_schedule(backend, ratio, hd, in_dt, out_dt, histories, rids, schedules, ape, state):
+def run_schedule(backend, ratio, hd, in_dt, out_dt, histories, rids, schedules, ape, state, start=None):
     """Feeds every request's token history through its schedule.
 
     Each round takes, for every request, its next step; all requests whose next
     step is a prefill go into one ragged prefill call, those whose next step is
     a decode go into one decode call.  Returns per-request [T, hd] outputs in
     token layout (rows of positions that emit nothing are zero).  ``backend``
-    supplies prefill(...) and decode(...)."""
+    supplies prefill(...) and decode(...).  ``start`` gives, per request, the
+    number of leading positions whose state is already in place (a cached
+    prefix); their output rows stay zero."""
     nreq = len(histories)
-    pos = [0] * nreq
+    pos = [0] * nreq if start is None else list(start)
     cursor = [0] * nreq
     outs = [np.zeros((h.shape[0], hd), dtype=np.uint16 if out_dt == 1 else np.float32) for h in histories]
     while any(cursor[b] < len(schedules[b]) for b in range(nreq)):
@@ -170,6 +172,71 @@ class OracleBackend:
     def decode(self, ratio, hd, in_dt, out_dt, state, rows, ape, rid, sl):
         plan = self.o.plan_decode(ratio, rid, sl)
         return self.o.compress_decode(ratio, hd, in_dt, out_dt, state, rows, ape, plan)
+
+
+class SwaPagedPool:
+    """Token maps of an SWA-paged KV pool, as the paged planners read them.
+
+    Every position of a request gets a slot of the full pool (req_to_token) and
+    an SWA slot (full_to_state).  SWA slots come in pages of swa_page_size
+    consecutive slots handed out in random order; position p of a request sits
+    at offset p % swa_page_size of its (p // swa_page_size)-th page.  Full slots
+    are a random permutation.  ``share`` lets a request reuse another's first
+    pages, as a prefix-cache hit does."""
+
+    def __init__(self, num_reqs: int, stride: int, swa_page_size: int, num_swa_pages: int,
+                 rng: np.random.Generator):
+        self.S = swa_page_size
+        self.r2t = np.full((num_reqs, stride), -1, np.int32)
+        self.num_full = num_reqs * stride + 5
+        self.f2s = np.full(self.num_full, -1, np.int64)
+        self.free_full = [int(x) for x in rng.permutation(self.num_full)]
+        self.free_pages = [int(x) for x in rng.permutation(num_swa_pages)]
+        self.num_swa_pages = num_swa_pages
+        self.page_of = {}
+        self.upto = [0] * num_reqs
+
+    def ensure(self, rid: int, n: int) -> None:
+        """Maps positions upto[rid] .. n-1 of request rid."""
+        for p in range(self.upto[rid], n):
+            full = self.free_full.pop()
+            k = p // self.S
+            if (rid, k) not in self.page_of:
+                self.page_of[(rid, k)] = self.free_pages.pop()
+            self.r2t[rid, p] = full
+            self.f2s[full] = self.page_of[(rid, k)] * self.S + p % self.S
+        self.upto[rid] = max(self.upto[rid], n)
+
+    def share(self, rid_b: int, rid_a: int, n: int) -> None:
+        """Request rid_b takes over the first n positions (whole pages) of rid_a."""
+        assert n % self.S == 0 and self.upto[rid_a] >= n
+        self.r2t[rid_b, :n] = self.r2t[rid_a, :n]
+        for k in range(n // self.S):
+            self.page_of[(rid_b, k)] = self.page_of[(rid_a, k)]
+        self.upto[rid_b] = n
+
+
+class PagedOracleBackend:
+    """Prefill / decode steps through the oracle with SWA-paged plans."""
+
+    def __init__(self, oracle, pool: SwaPagedPool, ring: int):
+        self.o, self.pool, self.ring = oracle, pool, ring
+
+    def prefill(self, ratio, hd, in_dt, out_dt, state, rows, ape, rid, sl, el):
+        o, pool = self.o, self.pool
+        for r, s in zip(rid, sl):
+            pool.ensure(r, s)
+        pc, pw, (nc, nw), _ = o.plan_prefill_paged(ratio, rid, pool.r2t, pool.f2s, pool.S, self.ring, sl, el)
+        out = o.compress_pool_prefill(ratio, hd, in_dt, out_dt, state, rows, ape, pc, nc, len(rows), o.OUT_TOKEN)
+        o.compress_write(ratio, hd, in_dt, state, rows, pw, nw)
+        return out
+
+    def decode(self, ratio, hd, in_dt, out_dt, state, rows, ape, rid, sl):
+        o, pool = self.o, self.pool
+        for r, s in zip(rid, sl):
+            pool.ensure(r, s)
+        plan = o.plan_decode_paged(ratio, rid, pool.r2t, pool.f2s, pool.S, self.ring, sl)
+        return o.compress_decode(ratio, hd, in_dt, out_dt, state, rows, ape, plan)
 
 
 def np_bits(t: torch.Tensor) -> np.ndarray:
@@ -270,4 +337,47 @@ class GpuBackend:
                                torch.tensor(rid, dtype=torch.int64, device=d),
                                torch.tensor(sl, dtype=torch.int64, device=d), torch_dtype(out_dt),
                                status=self.status)
+        return np_bits(out)
+
+
+class PagedGpuBackend:
+    """Prefill / decode steps through libckv with SWA-paged plans built on the GPU."""
+
+    def __init__(self, pool: SwaPagedPool, ring: int, device="cuda"):
+        from compressed_kv_attention_compressplan_gb300 import ckv
+
+        self.ckv, self.pool, self.ring = ckv, pool, ring
+        self.dev = torch.device(device)
+        self.status = ckv.new_status(self.dev)
+
+    def _maps(self):
+        d = self.dev
+        return torch.from_numpy(self.pool.r2t).to(d), torch.from_numpy(self.pool.f2s).to(d)
+
+    def prefill(self, ratio, hd, in_dt, out_dt, state, rows, ape, rid, sl, el):
+        c, d, pool = self.ckv, self.dev, self.pool
+        for r, s in zip(rid, sl):
+            pool.ensure(r, s)
+        r2t, f2s = self._maps()
+        nq = len(rows)
+        i64 = dict(dtype=torch.int64, device=d)
+        rid_t, sl_t, el_t = torch.tensor(rid, **i64), torch.tensor(sl, **i64), torch.tensor(el, **i64)
+        cap_c = c.capacity_compress(ratio, len(rid), nq)
+        cap_w = c.capacity_write_paged(ratio, len(rid), nq, pool.S)
+        pc, pw, counts = c.plan_prefill_paged(ratio, rid_t, r2t, f2s, pool.S, self.ring, sl_t, el_t, nq, cap_c,
+                                              cap_w, status=self.status)
+        out = c.compress_prefill(ratio, hd, state, to_torch(rows, in_dt).to(d), to_torch(ape, in_dt).to(d), pc, pw,
+                                 counts, c.OUT_TOKEN, torch_dtype(out_dt), status=self.status)
+        return np_bits(out)
+
+    def decode(self, ratio, hd, in_dt, out_dt, state, rows, ape, rid, sl):
+        c, d, pool = self.ckv, self.dev, self.pool
+        for r, s in zip(rid, sl):
+            pool.ensure(r, s)
+        r2t, f2s = self._maps()
+        i64 = dict(dtype=torch.int64, device=d)
+        pd = c.plan_decode_paged(ratio, torch.tensor(rid, **i64), r2t, f2s, pool.S, self.ring,
+                                 torch.tensor(sl, **i64), status=self.status)
+        out = c.compress_decode(ratio, hd, state, to_torch(rows, in_dt).to(d), to_torch(ape, in_dt).to(d), pd,
+                                torch_dtype(out_dt), status=self.status)
         return np_bits(out)

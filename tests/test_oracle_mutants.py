@@ -2,9 +2,12 @@
 planted, plausible mistake (a wrong ape row, swapped kv halves, a missing
 first-group mask, buffer_len off by one, a short write set, a decode slot off
 by one, a ragged id without its request offset, a wrong read page, a dropped
-term, a sign error, an input row off by one) must fail at least one pin."""
+term, a sign error, an input row off by one; in the SWA-paged planner: no
+page-end writes, the ring offset taken modulo the page size, records without
+state reads translated) must fail at least one pin."""
 import pytest
 
+from tests import test_oracle_paged as Q
 from tests import test_oracle_pins as P
 
 MUTANTS = {
@@ -19,6 +22,9 @@ MUTANTS = {
     9: "a dropped denominator term",
     10: "sign error in the exponent",
     11: "input row off by one",
+    12: "paged C4 write set without the SWA page ends",
+    13: "paged ring offset modulo the SWA page size",
+    14: "paged records without state reads translated",
 }
 
 
@@ -34,6 +40,10 @@ def pins(o):
     yield lambda: P.test_decode_nonboundary_rows_are_zero(o)
     for ratio in (4, 128):
         yield lambda ratio=ratio: P.test_modes_equal_history(o, ratio, 0)
+    for ratio in (4, 128):
+        yield lambda ratio=ratio: Q.test_identity_mapping_gives_legacy_plans(o, ratio, 0)
+    yield lambda: Q.test_page_end_positions_are_written_before_first_write(o)
+    yield lambda: Q.test_paged_schedules_equal_history(o, 0)
 
 
 @pytest.mark.parametrize("mutant", sorted(MUTANTS))
