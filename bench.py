@@ -239,7 +239,7 @@ def sum_over_ranks(x: float, ws: int) -> float:
 class PrefillRunner:
     """Device buffers + the three prefill segments of one workload."""
 
-    def __init__(self, ckv, w: wl.Workload, dev):
+    def __init__(self, ckv, w: wl.Workload, dev, padded: bool = False):
         self.ckv, self.w, self.dev = ckv, w, dev
         self.kv = w.kv_score.to(dev)
         self.ape = w.ape.to(dev)
@@ -247,8 +247,11 @@ class PrefillRunner:
         self.state = w.state.to(dev)
         self.pristine = self.state.clone()
         nq = w.num_q_tokens
-        self.cap_c = ckv.capacity_compress(w.ratio, w.batch, nq)
-        self.cap_w = ckv.capacity_write(w.ratio, w.batch, nq)
+        # padded: fixed-shape plan buffers of num_q_tokens records, tails filled with
+        # the invalid record (the shape a captured graph replays for any lengths)
+        self.padded = padded
+        self.cap_c = nq if padded else ckv.capacity_compress(w.ratio, w.batch, nq)
+        self.cap_w = nq if padded else ckv.capacity_write(w.ratio, w.batch, nq)
         self.plan_c = torch.empty(max(self.cap_c, 1), 16, dtype=torch.uint8, device=dev)
         self.plan_w = torch.empty(max(self.cap_w, 1), 8, dtype=torch.uint8, device=dev)
         self.counts = torch.zeros(4, dtype=torch.int32, device=dev)
@@ -260,7 +263,7 @@ class PrefillRunner:
     def plan(self):
         c = self.ckv
         c.plan_prefill(self.w.ratio, self.rid, self.sl, self.el, self.w.num_q_tokens, self.cap_c, self.cap_w,
-                       False, self.plan_c[: self.cap_c], self.plan_w[: self.cap_w], self.counts, self.status)
+                       self.padded, self.plan_c[: self.cap_c], self.plan_w[: self.cap_w], self.counts, self.status)
 
     def pool(self):
         self.ckv.compress_pool_prefill(self.w.ratio, self.w.head_dim, self.state, self.kv, self.ape,
@@ -559,9 +562,9 @@ def bench_config(args, name, ws, rank, local):
     flush = l2_flush_buffer(dev)
     b = algorithmic_bytes(w)
     if w.mode == "prefill":
-        r = PrefillRunner(ckv, w, dev)
+        r = PrefillRunner(ckv, w, dev, padded=name.endswith("_mtp"))
         segs = [("plan_prefill", r.plan), ("pool_prefill", r.pool), ("write", r.write)]
-        main_i, main_key = 1, "pool"
+        main_i, main_key = (1, "pool") if b["pool"] >= b["write"] else (2, "write")
     else:
         r = DecodeRunner(ckv, w, dev)
         segs = [("plan_decode", r.plan), ("decode", r.decode)]

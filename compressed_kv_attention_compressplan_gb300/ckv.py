@@ -64,6 +64,12 @@ def load_library():
         lib.ckv_capacity_write.argtypes = [i32, u32, u32]
         lib.ckv_capacity_write.restype = u32
         lib.ckv_plan_decode.argtypes = [i32, vp, vp, u32, vp, vp, vp]
+        i64 = ctypes.c_int64
+        lib.ckv_capacity_write_paged.argtypes = [i32, u32, u32, i32]
+        lib.ckv_capacity_write_paged.restype = u32
+        lib.ckv_plan_prefill_paged.argtypes = [i32, vp, vp, i64, u32, vp, u64, i32, i32, vp, vp, u32, u32, u32, u32,
+                                               i32, vp, vp, vp, vp, vp]
+        lib.ckv_plan_decode_paged.argtypes = [i32, vp, vp, i64, u32, vp, u64, i32, i32, vp, u32, vp, vp, vp]
         lib.ckv_plan_prefill.argtypes = [i32, vp, vp, vp, u32, u32, u32, u32, i32, vp, vp, vp, vp, vp]
         lib.ckv_compress_write.argtypes = [i32, i32, i32, vp, u64, vp, u32, vp, vp, u32, vp, vp]
         lib.ckv_compress_pool_prefill.argtypes = [i32, i32, i32, i32, vp, u64, vp, u32, vp, vp, vp, u32, i32, vp,
@@ -163,6 +169,57 @@ def plan_prefill(ratio: int, rid: torch.Tensor, seq_lens: torch.Tensor, extend_l
                                            capacity_c, capacity_w, int(pad_invalid), _ptr(plan_c), _ptr(plan_w),
                                            _ptr(counts), _ptr(status), _stream(stream)), "ckv_plan_prefill")
     return plan_c[:capacity_c], plan_w[:capacity_w], counts
+
+
+def capacity_write_paged(ratio: int, batch: int, num_q_tokens: int, swa_page_size: int) -> int:
+    return int(load_library().ckv_capacity_write_paged(ratio, batch, num_q_tokens, swa_page_size))
+
+
+def _paged_maps(req_to_token: Optional[torch.Tensor], full_to_state: Optional[torch.Tensor]):
+    """(pointer, stride, rows) of req_to_token and (pointer, size) of full_to_state; C128 takes None for both."""
+    if req_to_token is None:
+        return None, 0, 0, None, 0
+    if req_to_token.dtype != torch.int32 or full_to_state.dtype != torch.int64 or req_to_token.dim() != 2:
+        raise ValueError("req_to_token must be 2-D int32 and full_to_state int64")
+    return (_ptr(req_to_token), req_to_token.shape[1], req_to_token.shape[0], _ptr(full_to_state),
+            full_to_state.numel())
+
+
+def plan_prefill_paged(ratio: int, rid: torch.Tensor, req_to_token: torch.Tensor, full_to_state: torch.Tensor,
+                       swa_page_size: int, ring_size: int, seq_lens: torch.Tensor, extend_lens: torch.Tensor,
+                       num_q_tokens: int, capacity_c: Optional[int] = None, capacity_w: Optional[int] = None,
+                       pad_invalid: bool = False, counts: Optional[torch.Tensor] = None,
+                       status: Optional[torch.Tensor] = None, stream=None):
+    """SWA-paged prefill plans; req_to_token is ``[num_reqs, stride]`` int32, full_to_state int64."""
+    batch = rid.numel()
+    dev = rid.device
+    if capacity_c is None:
+        capacity_c = capacity_compress(ratio, batch, num_q_tokens)
+    if capacity_w is None:
+        capacity_w = capacity_write_paged(ratio, batch, num_q_tokens, swa_page_size)
+    plan_c = torch.empty(max(capacity_c, 1), 16, dtype=torch.uint8, device=dev)
+    plan_w = torch.empty(max(capacity_w, 1), 8, dtype=torch.uint8, device=dev)
+    if counts is None:
+        counts = torch.empty(4, dtype=torch.int32, device=dev)
+    r2t, stride, nreq, f2s, nfull = _paged_maps(req_to_token, full_to_state)
+    _check(load_library().ckv_plan_prefill_paged(ratio, _ptr(rid), r2t, stride, nreq, f2s, nfull, swa_page_size,
+                                                 ring_size, _ptr(seq_lens), _ptr(extend_lens), batch, num_q_tokens, capacity_c,
+                                                 capacity_w, int(pad_invalid), _ptr(plan_c), _ptr(plan_w),
+                                                 _ptr(counts), _ptr(status), _stream(stream)),
+           "ckv_plan_prefill_paged")
+    return plan_c[:capacity_c], plan_w[:capacity_w], counts
+
+
+def plan_decode_paged(ratio: int, rid: torch.Tensor, req_to_token: torch.Tensor, full_to_state: torch.Tensor,
+                      swa_page_size: int, ring_size: int, seq_lens: torch.Tensor,
+                      status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    batch = rid.numel()
+    plan_d = torch.empty(max(batch, 1), 16, dtype=torch.uint8, device=rid.device)
+    r2t, stride, nreq, f2s, nfull = _paged_maps(req_to_token, full_to_state)
+    _check(load_library().ckv_plan_decode_paged(ratio, _ptr(rid), r2t, stride, nreq, f2s, nfull, swa_page_size,
+                                                ring_size, _ptr(seq_lens), batch, _ptr(plan_d), _ptr(status), _stream(stream)),
+           "ckv_plan_decode_paged")
+    return plan_d[:batch]
 
 
 # ------------------------------------------------------------------------------ compute

@@ -3,8 +3,10 @@
 // Prefill planning follows the sequential CPU loop of c_plan.cuh
 // plan_compress_prefill_legacy (requests in batch order, positions ascending,
 // compress and write records in separate lists) together with the legacy
-// ring / page translation of plan_compress_prefill_legacy_kernel.  The pages'
-// GPU builder (plan_compress_prefill_kernel0) walks requests serially inside
+// ring / page translation of plan_compress_prefill_legacy_kernel, or, for
+// SWA-paged state, the loop and translation of plan_compress_prefill /
+// plan_compress_prefill_kernel_1.  c_plan.cuh's own GPU builder
+// (plan_compress_prefill_kernel0) walks requests serially inside
 // one CTA and hands out slots with shared-memory atomics, so its order varies
 // run to run.  Here every record's index is a closed form of block-wide
 // exclusive scans of the per-request counts, so the GPU plan is bit-identical
@@ -85,6 +87,78 @@ __global__ void plan_decode_kernel(int ratio, const int64_t* __restrict__ rid, c
   *reinterpret_cast<uint4*>(plan_d + b) = rec;
 }
 
+// c_plan.cuh compute_loc: an SWA slot swa lives in the ring of its SWA page,
+// state row = (swa / swa_page_size) * ring_size + swa % ring_size.
+__device__ __forceinline__ int64_t paged_loc(const int32_t* r2t, int64_t stride, const int64_t* f2s,
+                                             uint64_t num_full, int32_t sps, int32_t ring, int32_t rid, int32_t p,
+                                             bool& ok) {
+  const int32_t raw = r2t[static_cast<int64_t>(rid) * stride + p];
+  if (raw < 0 || static_cast<uint64_t>(raw) >= num_full) {
+    ok = false;
+    return -1;
+  }
+  const int64_t swa = f2s[raw];
+  const int64_t loc = swa >= 0 ? (swa / sps) * ring + swa % ring : -1;
+  if (loc < 0 || loc > INT32_MAX - 4) {
+    ok = false;
+    return -1;
+  }
+  return loc;
+}
+
+// Positions x' < x with x' % S >= S - 4: the last group of every SWA page,
+// which paged C4 always writes (c_plan.cuh plan_compress_prefill, should_write).
+__device__ __forceinline__ int32_t page_end_count(int32_t x, int32_t S) {
+  return (x / S) * 4 + max(0, x % S - (S - 4));
+}
+
+struct DecodePagedArgs {
+  const int64_t* rid;
+  const int64_t* seq_lens;
+  uint32_t batch;
+  const int32_t* r2t;
+  int64_t r2t_stride;
+  uint32_t num_reqs;
+  const int64_t* f2s;
+  uint64_t num_full;
+  int32_t sps;
+  int32_t ring;
+  ckv_decode_plan_t* plan_d;
+  uint32_t* d_status;
+};
+
+// c_plan.cuh plan_compress_decode_kernel (C4 through the SWA mapping):
+// write_loc = ring(state of position seq_len-1), read pages of positions
+// max(seq_len-1-4, 0) and seq_len-1.
+__global__ void plan_decode_paged_kernel(const DecodePagedArgs a) {
+  pdl_wait();
+  pdl_release();
+  const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= a.batch) return;
+  const int64_t sl = a.seq_lens[b];
+  const int64_t r = a.rid[b];
+  uint4 rec = make_uint4(kInvalidU32, kInvalidU32, kInvalidU32, kInvalidU32);
+  if (sl >= 1 && sl <= INT32_MAX && r >= 0) {
+    if (r < a.num_reqs && sl <= a.r2t_stride) {
+      const int32_t p1 = static_cast<int32_t>(sl - 1);
+      const int32_t p0 = max(p1 - 4, 0);
+      bool ok = true;
+      const int64_t loc1 = paged_loc(a.r2t, a.r2t_stride, a.f2s, a.num_full, a.sps, a.ring, static_cast<int32_t>(r), p1, ok);
+      const int64_t loc0 = paged_loc(a.r2t, a.r2t_stride, a.f2s, a.num_full, a.sps, a.ring, static_cast<int32_t>(r), p0, ok);
+      if (ok)
+        rec = make_uint4(static_cast<uint32_t>(sl), static_cast<uint32_t>(loc1), static_cast<uint32_t>(loc0 / 4),
+                         static_cast<uint32_t>(loc1 / 4));
+      else
+        status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+    } else {
+      status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+    }
+  } else {
+    status_or(a.d_status, CKV_STATUS_BAD_LENGTH);
+  }
+  *reinterpret_cast<uint4*>(a.plan_d + b) = rec;
+}
+
 struct PrefillPlanArgs {
   int ratio;
   const int64_t* rid;
@@ -99,6 +173,16 @@ struct PrefillPlanArgs {
   ckv_write_plan_t* plan_w;
   uint32_t* d_counts;
   uint32_t* d_status;
+  // SWA-paged C4 addressing (paged != 0): state row of position p of request
+  // rid = ring(full_to_state[req_to_token[rid][p]]), see paged_loc.
+  int paged;
+  const int32_t* r2t;
+  int64_t r2t_stride;
+  uint32_t num_reqs;
+  const int64_t* f2s;
+  uint64_t num_full;
+  int32_t sps;
+  int32_t ring;
 };
 
 // Every CTA loads the <= 1024 request lengths, derives per request
@@ -117,6 +201,8 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
   __shared__ int32_t s_pl[kMaxBatch];
   __shared__ int32_t s_wstart[kMaxBatch];
   __shared__ int32_t s_rid[kMaxBatch];
+  __shared__ int32_t s_pe0[kMaxBatch];      // paged: page_end_count(prefix)
+  __shared__ uint32_t s_nextra[kMaxBatch];  // paged: page-end writes before wstart
   __shared__ uint32_t s_wsum[3][kWarps];
   __shared__ uint32_t s_wmin[kWarps], s_wmax[kWarps];
   __shared__ uint32_t s_flags;
@@ -141,20 +227,38 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
                     el <= CKV_MAX_TOKENS;
     el_eff = (el > 0 && el <= CKV_MAX_TOKENS) ? static_cast<uint32_t>(el) : 0u;
     el_min = el_max = el_eff;
-    if (ok) {
+    bool ok_paged = true;
+    if (ok && a.paged && R == 4) ok_paged = r < a.num_reqs && sl <= a.r2t_stride;
+    if (ok && ok_paged) {
       const int32_t s32 = static_cast<int32_t>(sl);
       const int32_t pl = s32 - static_cast<int32_t>(el);
-      const int32_t first_w = (s32 / R) * R - (R == 4 ? 4 : 0);
+      int32_t first_w = (s32 / R) * R - (R == 4 ? 4 : 0);
+      uint32_t nextra = 0;
+      int32_t pe0 = 0;
+      if (a.paged) {
+        // c_plan.cuh's GPU-input planner also keeps the last mtp_pad positions
+        const int32_t mtp_pad = min(a.ring - R, 4);
+        first_w = min(first_w, s32 - mtp_pad);
+      }
       const int32_t wstart = max(pl, first_w);
+      if (a.paged && R == 4 && wstart > pl) {
+        pe0 = page_end_count(pl, a.sps);
+        nextra = static_cast<uint32_t>(page_end_count(wstart, a.sps) - pe0);
+      }
       nc = static_cast<uint32_t>(s32 / R - pl / R);
-      nw = static_cast<uint32_t>(s32 - wstart);
+      nw = static_cast<uint32_t>(s32 - wstart) + nextra;
       s_pl[tid] = pl;
       s_wstart[tid] = wstart;
       s_rid[tid] = static_cast<int32_t>(r);
+      s_pe0[tid] = pe0;
+      s_nextra[tid] = nextra;
     } else {
       s_pl[tid] = 0;
       s_wstart[tid] = 0;
       s_rid[tid] = 0;
+      s_pe0[tid] = 0;
+      s_nextra[tid] = 0;
+      if (ok) atomicOr(&s_flags, CKV_STATUS_BAD_INDEX);
     }
     if (!ok) atomicOr(&s_flags, CKV_STATUS_BAD_LENGTH);
   }
@@ -243,9 +347,24 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
         const uint32_t ragged = s_off_e[lo] + static_cast<uint32_t>(j);
         const uint32_t bl = static_cast<uint32_t>(W - min(j + 1, W));
         const int32_t rid = s_rid[lo];
-        rec = make_uint4(static_cast<uint32_t>(p + 1), ragged | (bl << CKV_BUFFER_LEN_SHIFT),
-                         static_cast<uint32_t>(legacy_page(R, rid, max(p - R, 0))),
-                         static_cast<uint32_t>(legacy_page(R, rid, p)));
+        int64_t page0, page1;
+        bool ok = true;
+        if (a.paged && bl == 0) {  // reads no state; c_plan.cuh kernel_1 leaves (-1, batch index)
+          page0 = -1;
+          page1 = static_cast<int64_t>(lo);
+        } else if (a.paged && R == 4) {
+          page0 = paged_loc(a.r2t, a.r2t_stride, a.f2s, a.num_full, a.sps, a.ring, rid, max(p - R, 0), ok) / R;
+          page1 = paged_loc(a.r2t, a.r2t_stride, a.f2s, a.num_full, a.sps, a.ring, rid, p, ok) / R;
+        } else {
+          page0 = legacy_page(R, rid, max(p - R, 0));
+          page1 = legacy_page(R, rid, p);
+        }
+        if (ok) {
+          rec = make_uint4(static_cast<uint32_t>(p + 1), ragged | (bl << CKV_BUFFER_LEN_SHIFT),
+                           static_cast<uint32_t>(page0), static_cast<uint32_t>(page1));
+        } else {
+          status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+        }
         store = true;
       }
       if (store) *reinterpret_cast<uint4*>(a.plan_c + k) = rec;
@@ -259,9 +378,21 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
           const uint32_t mid = (lo + hi) >> 1;
           if (s_off_w[mid] <= k) lo = mid; else hi = mid;
         }
-        const int32_t p = s_wstart[lo] + static_cast<int32_t>(k - s_off_w[lo]);
+        const uint32_t kk = k - s_off_w[lo];
+        const uint32_t nx = s_nextra[lo];
+        int32_t p;
+        if (kk < nx) {  // the kk-th last-group position of an SWA page before wstart
+          const int32_t m = s_pe0[lo] + static_cast<int32_t>(kk);
+          p = (m / 4) * a.sps + (a.sps - 4) + m % 4;
+        } else {
+          p = s_wstart[lo] + static_cast<int32_t>(kk - nx);
+        }
         const uint32_t ragged = s_off_e[lo] + static_cast<uint32_t>(p - s_pl[lo]);
-        rec = make_uint2(ragged, static_cast<uint32_t>(legacy_loc(R, s_rid[lo], p)));
+        bool ok = true;
+        const int64_t loc = a.paged && R == 4 ? paged_loc(a.r2t, a.r2t_stride, a.f2s, a.num_full, a.sps, a.ring, s_rid[lo], p, ok)
+                                    : legacy_loc(R, s_rid[lo], p);
+        if (ok) rec = make_uint2(ragged, static_cast<uint32_t>(loc));
+        else status_or(a.d_status, CKV_STATUS_BAD_INDEX);
         store = true;
       }
       if (store) *reinterpret_cast<uint2*>(a.plan_w + k) = rec;
@@ -313,26 +444,120 @@ int ckv_plan_decode(int ratio, const int64_t* rid, const int64_t* seq_lens, uint
                     reinterpret_cast<cudaStream_t>(stream), ratio, rid, seq_lens, batch, plan_d, d_status);
 }
 
+namespace {
+
+int launch_plan_prefill(PrefillPlanArgs a, cudaStream_t stream) {
+  const uint32_t batch = a.batch;
+  if (a.ratio != 4 && a.ratio != 128) return CKV_ERR_RATIO;
+  if (batch > CKV_MAX_BATCH || a.num_q_tokens > CKV_MAX_TOKENS) return CKV_ERR_SIZE;
+  if (a.cap_c > CKV_MAX_TOKENS + 1u || a.cap_w > CKV_MAX_TOKENS + 1u) return CKV_ERR_SIZE;
+  if (a.d_counts == nullptr || (reinterpret_cast<uintptr_t>(a.d_counts) & 3u)) return CKV_ERR_POINTER;
+  if (batch > 0 && (!a.rid || !a.seq_lens || !a.extend_lens)) return CKV_ERR_POINTER;
+  if ((reinterpret_cast<uintptr_t>(a.rid) | reinterpret_cast<uintptr_t>(a.seq_lens) |
+       reinterpret_cast<uintptr_t>(a.extend_lens)) & 7u)
+    return CKV_ERR_POINTER;
+  if (a.cap_c > 0 && !aligned16(a.plan_c)) return CKV_ERR_POINTER;
+  if (a.cap_w > 0 && (a.plan_w == nullptr || (reinterpret_cast<uintptr_t>(a.plan_w) & 7u))) return CKV_ERR_POINTER;
+  const uint32_t work = std::max(a.cap_c, a.cap_w);
+  uint32_t grid = (work + kPlanThreads - 1) / kPlanThreads;
+  grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 2u * static_cast<uint32_t>(sm_count())));
+  return launch_pdl(plan_prefill_kernel, dim3(grid), dim3(kPlanThreads), 0, stream, a);
+}
+
+// Paged arguments shared by both paged planners: C4 needs a mapping; C128
+// state is request-scoped (c_plan.cuh compute_c128_loc) and ring_size must be
+// 128, the only ring in which read_page_0 -- the page the C128 pooling reads
+// (compressor_v2.py) -- is the page of the record's own window.
+int check_paged(int ratio, const int32_t* r2t, int64_t stride, const int64_t* f2s, int32_t sps, int32_t ring) {
+  if (ratio == 128) return ring == 128 ? CKV_OK : CKV_ERR_SIZE;
+  if (ratio != 4) return CKV_ERR_RATIO;
+  if (sps <= 0 || ring < 8 || ring % 4 != 0 || sps % ring != 0 || stride <= 0) return CKV_ERR_SIZE;
+  if (r2t == nullptr || f2s == nullptr || (reinterpret_cast<uintptr_t>(r2t) & 3u) ||
+      (reinterpret_cast<uintptr_t>(f2s) & 7u))
+    return CKV_ERR_POINTER;
+  return CKV_OK;
+}
+
+}  // namespace
+
 int ckv_plan_prefill(int ratio, const int64_t* rid, const int64_t* seq_lens, const int64_t* extend_lens,
                      uint32_t batch, uint32_t num_q_tokens, uint32_t capacity_c, uint32_t capacity_w,
                      int pad_invalid, ckv_compress_plan_t* plan_c, ckv_write_plan_t* plan_w, uint32_t* d_counts,
                      uint32_t* d_status, ckv_stream_t stream) {
-  if (ratio != 4 && ratio != 128) return CKV_ERR_RATIO;
-  if (batch > CKV_MAX_BATCH || num_q_tokens > CKV_MAX_TOKENS) return CKV_ERR_SIZE;
-  if (capacity_c > CKV_MAX_TOKENS + 1u || capacity_w > CKV_MAX_TOKENS + 1u) return CKV_ERR_SIZE;
-  if (d_counts == nullptr || (reinterpret_cast<uintptr_t>(d_counts) & 3u)) return CKV_ERR_POINTER;
-  if (batch > 0 && (!rid || !seq_lens || !extend_lens)) return CKV_ERR_POINTER;
-  if ((reinterpret_cast<uintptr_t>(rid) | reinterpret_cast<uintptr_t>(seq_lens) |
-       reinterpret_cast<uintptr_t>(extend_lens)) & 7u)
-    return CKV_ERR_POINTER;
-  if (capacity_c > 0 && !aligned16(plan_c)) return CKV_ERR_POINTER;
-  if (capacity_w > 0 && (plan_w == nullptr || (reinterpret_cast<uintptr_t>(plan_w) & 7u))) return CKV_ERR_POINTER;
-  PrefillPlanArgs a{ratio, rid, seq_lens, extend_lens, batch, num_q_tokens, capacity_c, capacity_w, pad_invalid,
-                    plan_c, plan_w, d_counts, d_status};
-  const uint32_t work = std::max(capacity_c, capacity_w);
-  uint32_t grid = (work + kPlanThreads - 1) / kPlanThreads;
-  grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 2u * static_cast<uint32_t>(sm_count())));
-  return launch_pdl(plan_prefill_kernel, dim3(grid), dim3(kPlanThreads), 0, reinterpret_cast<cudaStream_t>(stream), a);
+  PrefillPlanArgs a{};
+  a.ratio = ratio;
+  a.rid = rid;
+  a.seq_lens = seq_lens;
+  a.extend_lens = extend_lens;
+  a.batch = batch;
+  a.num_q_tokens = num_q_tokens;
+  a.cap_c = capacity_c;
+  a.cap_w = capacity_w;
+  a.pad_invalid = pad_invalid;
+  a.plan_c = plan_c;
+  a.plan_w = plan_w;
+  a.d_counts = d_counts;
+  a.d_status = d_status;
+  a.sps = 1;
+  a.ring = 1;
+  return launch_plan_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ckv_plan_prefill_paged(int ratio, const int64_t* rid, const int32_t* req_to_token, int64_t r2t_stride,
+                           uint32_t num_reqs, const int64_t* full_to_state, uint64_t num_full_slots,
+                           int32_t swa_page_size, int32_t ring_size, const int64_t* seq_lens,
+                           const int64_t* extend_lens, uint32_t batch, uint32_t num_q_tokens, uint32_t capacity_c,
+                           uint32_t capacity_w, int pad_invalid, ckv_compress_plan_t* plan_c,
+                           ckv_write_plan_t* plan_w, uint32_t* d_counts, uint32_t* d_status, ckv_stream_t stream) {
+  const int rc = check_paged(ratio, req_to_token, r2t_stride, full_to_state, swa_page_size, ring_size);
+  if (rc) return rc;
+  PrefillPlanArgs a{};
+  a.ratio = ratio;
+  a.rid = rid;
+  a.seq_lens = seq_lens;
+  a.extend_lens = extend_lens;
+  a.batch = batch;
+  a.num_q_tokens = num_q_tokens;
+  a.cap_c = capacity_c;
+  a.cap_w = capacity_w;
+  a.pad_invalid = pad_invalid;
+  a.plan_c = plan_c;
+  a.plan_w = plan_w;
+  a.d_counts = d_counts;
+  a.d_status = d_status;
+  a.paged = 1;
+  a.r2t = req_to_token;
+  a.r2t_stride = r2t_stride;
+  a.num_reqs = num_reqs;
+  a.f2s = full_to_state;
+  a.num_full = num_full_slots;
+  a.sps = swa_page_size;
+  a.ring = ring_size;
+  return launch_plan_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ckv_plan_decode_paged(int ratio, const int64_t* rid, const int32_t* req_to_token, int64_t r2t_stride,
+                          uint32_t num_reqs, const int64_t* full_to_state, uint64_t num_full_slots,
+                          int32_t swa_page_size, int32_t ring_size, const int64_t* seq_lens, uint32_t batch,
+                          ckv_decode_plan_t* plan_d, uint32_t* d_status, ckv_stream_t stream) {
+  const int rc = check_paged(ratio, req_to_token, r2t_stride, full_to_state, swa_page_size, ring_size);
+  if (rc) return rc;
+  if (ratio == 128) return ckv_plan_decode(ratio, rid, seq_lens, batch, plan_d, d_status, stream);
+  if (batch == 0) return CKV_OK;
+  if (!rid || !seq_lens || !aligned16(plan_d)) return CKV_ERR_POINTER;
+  if ((reinterpret_cast<uintptr_t>(rid) | reinterpret_cast<uintptr_t>(seq_lens)) & 7u) return CKV_ERR_POINTER;
+  DecodePagedArgs a{rid, seq_lens, batch, req_to_token, r2t_stride, num_reqs, full_to_state, num_full_slots,
+                    swa_page_size, ring_size, plan_d, d_status};
+  const uint32_t threads = 256;
+  return launch_pdl(plan_decode_paged_kernel, dim3((batch + threads - 1) / threads), dim3(threads), 0,
+                    reinterpret_cast<cudaStream_t>(stream), a);
+}
+
+uint32_t ckv_capacity_write_paged(int ratio, uint32_t batch, uint32_t num_q_tokens, int32_t swa_page_size) {
+  if (ratio != 4 || swa_page_size <= 0) return ckv_capacity_write(ratio, batch, num_q_tokens);
+  const uint64_t w = static_cast<uint64_t>(batch) * 7 +
+                     4ull * (static_cast<uint64_t>(num_q_tokens) / static_cast<uint64_t>(swa_page_size) + batch);
+  return static_cast<uint32_t>(std::min<uint64_t>(w, num_q_tokens));
 }
 
 const char* ckv_error_string(int code) {

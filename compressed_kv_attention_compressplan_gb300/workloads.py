@@ -22,6 +22,9 @@ mixes of the compressor's serving regimes:
   (speculative-decoding verify shape), 128 requests extend by U[128, 16384],
   prefix ~ U[0, 65536], head_dim 512, bf16 input with 1 % of the score entries
   set to +8, fp32 compact output.
+* ``c4_prefill_mtp`` / ``c128_prefill_mtp``  the speculative-decoding verify
+  step: batch 1024, every request extends by 4, prefix ~ U[0, 65536], head_dim
+  512, bf16 input (C4: bf16 token-layout output; C128: fp32 compact output).
 """
 from __future__ import annotations
 
@@ -220,12 +223,33 @@ def c128_prefill(seed: int = 0, batch: int = 1024, head_dim: int = 512, num_long
                 el, seed, num_requests_state=batch, outlier_frac=0.01)
 
 
+def c128_prefill_mtp(seed: int = 0, batch: int = 1024, extend: int = 4, head_dim: int = 512,
+                     max_prefix: int = 65536) -> Workload:
+    """Speculative-decoding verify step: every request extends by the same few tokens."""
+    el = torch.full((batch,), extend, dtype=torch.int64)
+    pl = torch.randint(0, max_prefix + 1, (batch,), generator=_gen(seed, 1), dtype=torch.int64)
+    rid = torch.randperm(batch, generator=_gen(seed, 2))
+    return make("c128_prefill_mtp", "prefill", 128, head_dim, torch.bfloat16, torch.float32, COMPACT, rid, pl + el,
+                el, seed, num_requests_state=batch)
+
+
+def c4_prefill_mtp(seed: int = 0, batch: int = 1024, extend: int = 4, head_dim: int = 512,
+                   max_prefix: int = 65536) -> Workload:
+    el = torch.full((batch,), extend, dtype=torch.int64)
+    pl = torch.randint(0, max_prefix + 1, (batch,), generator=_gen(seed, 1), dtype=torch.int64)
+    rid = torch.randperm(batch, generator=_gen(seed, 2))
+    return make("c4_prefill_mtp", "prefill", 4, head_dim, torch.bfloat16, torch.bfloat16, TOKEN, rid, pl + el, el,
+                seed, num_requests_state=batch)
+
+
 NAMED = {
     "c4_prefill_small": c4_prefill_small,
     "c4_decode": c4_decode,
     "c128_decode": c128_decode,
     "c4_prefill": c4_prefill,
     "c128_prefill": c128_prefill,
+    "c4_prefill_mtp": c4_prefill_mtp,
+    "c128_prefill_mtp": c128_prefill_mtp,
 }
 
 

@@ -153,6 +153,47 @@ int ckv_plan_prefill(int ratio, const int64_t* rid, const int64_t* seq_lens, con
                      int pad_invalid, ckv_compress_plan_t* plan_c, ckv_write_plan_t* plan_w, uint32_t* d_counts,
                      uint32_t* d_status, ckv_stream_t stream);
 
+/* SWA-paged planners (c_plan.cuh plan_compress_prefill / plan_compress_decode
+ * with plan_compress_prefill_kernel_1 / plan_compress_decode_kernel: the main,
+ * non-legacy path of that page).
+ * C4: state rows come from the request's token map.  For position p of
+ * request rid, full = req_to_token[rid * r2t_stride + p] (int32), swa =
+ * full_to_state[full] (int64), and the row is
+ *     (swa / swa_page_size) * ring_size + swa % ring_size,
+ * i.e. every SWA page owns a ring of ring_size rows; read pages are rows / 4.
+ * The write set adds, to the legacy one, the last 4 positions of every SWA
+ * page in the extend (the next page's first window reads them as its previous
+ * group), and keeps positions >= seq_len - mtp_pad with mtp_pad =
+ * min(ring_size - ratio, 4) (the GPU-input planner's rule; with the rings
+ * accepted here it adds nothing).  Requirements: swa_page_size % ring_size ==
+ * 0, ring_size % 4 == 0, ring_size >= 8 (a 4-row ring would put a window's two
+ * groups in one page); the pooling kernels assume that the 4 positions of a
+ * group sit in the 4 slots of one 4-slot page, true for any page-granular SWA
+ * allocation.  A request with rid >= num_reqs or seq_len > r2t_stride, or a
+ * mapping entry out of range or negative, yields invalid records and
+ * CKV_STATUS_BAD_INDEX (device-side).
+ * C128: state is request-scoped (rid * ring_size + p % ring_size) and the maps
+ * are not read (they may be NULL).  ring_size must be 128: the C128 pooling
+ * reads its window from read_page_0, which is the window's own page only for a
+ * 128-row ring.  Decode plans and write records are then the legacy ones.
+ * Prefill compress records with buffer_len == 0 read no state; as kernel_1
+ * leaves them, their read_page_0 is -1 and read_page_1 the request's index in
+ * the batch (both ratios).  Capacities: compress records as
+ * ckv_capacity_compress, write records <= ckv_capacity_write_paged. */
+uint32_t ckv_capacity_write_paged(int ratio, uint32_t batch, uint32_t num_q_tokens, int32_t swa_page_size);
+
+int ckv_plan_prefill_paged(int ratio, const int64_t* rid, const int32_t* req_to_token, int64_t r2t_stride,
+                           uint32_t num_reqs, const int64_t* full_to_state, uint64_t num_full_slots,
+                           int32_t swa_page_size, int32_t ring_size, const int64_t* seq_lens,
+                           const int64_t* extend_lens, uint32_t batch, uint32_t num_q_tokens, uint32_t capacity_c,
+                           uint32_t capacity_w, int pad_invalid, ckv_compress_plan_t* plan_c,
+                           ckv_write_plan_t* plan_w, uint32_t* d_counts, uint32_t* d_status, ckv_stream_t stream);
+
+int ckv_plan_decode_paged(int ratio, const int64_t* rid, const int32_t* req_to_token, int64_t r2t_stride,
+                          uint32_t num_reqs, const int64_t* full_to_state, uint64_t num_full_slots,
+                          int32_t swa_page_size, int32_t ring_size, const int64_t* seq_lens, uint32_t batch,
+                          ckv_decode_plan_t* plan_d, uint32_t* d_status, ckv_stream_t stream);
+
 /* ------------------------------------------------------------------ compute */
 /* Prefill state write (c4.cuh c4_write / flash_c4_prefill<kWrite=true>,
  * compressor_v2.py _c128_compress_prefill_write_kernel): for each of the first

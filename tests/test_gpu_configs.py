@@ -1,4 +1,4 @@
-"""Parity at the five workloads' full sizes, in the launch configuration the
+"""Parity at the seven named workloads' full sizes, in the launch configuration the
 benchmark times (capacities from ckv_capacity_*, no padding, plan -> pool ->
 write on one stream; plan -> decode).
 
@@ -33,21 +33,26 @@ def code(dt):
     return 1 if dt == torch.bfloat16 else 0
 
 
-@pytest.mark.parametrize("name", ["c4_prefill_small", "c4_prefill", "c128_prefill"])
+@pytest.mark.parametrize("name", ["c4_prefill_small", "c4_prefill", "c128_prefill", "c4_prefill_mtp",
+                                  "c128_prefill_mtp"])
 def test_prefill_workload_full_size(env, name):
+    """The speculative-decoding workloads (``*_mtp``) run with fixed-shape plan
+    buffers of num_q_tokens records whose tails are the invalid record, as a
+    captured graph would."""
     o, ckv, dev = env
     w = wl.NAMED[name](0)
     R, hd = w.ratio, w.head_dim
     ci, co = code(w.in_dtype), code(w.out_dtype)
     nq = w.num_q_tokens
-    cap_c = ckv.capacity_compress(R, w.batch, nq)
-    cap_w = ckv.capacity_write(R, w.batch, nq)
+    padded = name.endswith("_mtp")
+    cap_c = nq if padded else ckv.capacity_compress(R, w.batch, nq)
+    cap_w = nq if padded else ckv.capacity_write(R, w.batch, nq)
     state_d = w.state.to(dev)
     kv_d = w.kv_score.to(dev)
     status = ckv.new_status(dev)
     layout = ckv.OUT_TOKEN if w.out_layout == wl.TOKEN else ckv.OUT_COMPACT
     pc, pw, counts = ckv.plan_prefill(R, w.rid.to(dev), w.seq_lens.to(dev), w.extend_lens.to(dev), nq, cap_c, cap_w,
-                                      status=status)
+                                      pad_invalid=padded, status=status)
     out = ckv.compress_prefill(R, hd, state_d, kv_d, w.ape.to(dev), pc, pw, counts, layout, w.out_dtype,
                                status=status)
     torch.cuda.synchronize()
@@ -56,6 +61,9 @@ def test_prefill_workload_full_size(env, name):
     assert counts[:2].tolist() == [nc, nw]
     assert (pc[:nc].cpu().numpy() == wc).all(), "compress plan"
     assert (pw[:nw].cpu().numpy() == ww).all(), "write plan"
+    if padded:
+        pcp, pwp, _, _ = o.plan_prefill(R, w.rid, w.seq_lens, w.extend_lens, nq, cap_c, cap_w, pad_invalid=True)
+        assert (pc.cpu().numpy() == pcp).all() and (pw.cpu().numpy() == pwp).all(), "padded plans"
     st = wl.bits(w.state).copy()
     inp = wl.bits(w.kv_score)
     ape = wl.bits(w.ape)
