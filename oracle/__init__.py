@@ -96,6 +96,8 @@ def _load(path: str | None = None):
             lib.orc_plan_prefill_paged.argtypes = [i32, vp, vp, i64, u32, vp, u64, i32, i32, vp, vp, u32, u32, u32,
                                                    u32, i32, vp, vp, vp]
             lib.orc_plan_decode_paged.argtypes = [i32, vp, vp, i64, u32, vp, u64, i32, i32, vp, u32, vp]
+            lib.orc_norm_rope_store.argtypes = [i32, i32, i32, i32, i32, vp, i32, u64, vp, u32, vp, ctypes.c_float,
+                                                vp, u32, vp, u64, i32, vp, u64]
             lib.orc_double_to_bf16.argtypes = [ctypes.c_double]
             lib.orc_double_to_bf16.restype = ctypes.c_uint16
             _lib = lib
@@ -285,6 +287,24 @@ def compress_prefill(ratio, hd, in_dtype, out_dtype, state: np.ndarray, inp, ape
                                 num_q_tokens=int(_i64(extend_lens).sum()), out_layout=out_layout)
     compress_write(ratio, hd, in_dtype, state, inp, pw, nw)
     return out, pc, pw
+
+
+def norm_rope_store(ratio: int, mode: int, hd: int, rope_dim: int, in_dtype: int, rows, in_layout: int, plan,
+                    weight, eps: float, freqs, out_loc, cache_dtype: int, cache: np.ndarray) -> None:
+    """RMSNorm + RoPE + store of compressed rows into ``cache`` (in place); mode 0 prefill (plan = CompressPlan
+    records), 1 decode (plan = DecodePlan records).  freqs: fp32 ``[max_pos, rope_dim/2, 2]`` (cos, sin)."""
+    assert cache.flags["C_CONTIGUOUS"]
+    rows = np.ascontiguousarray(rows)
+    plan = np.ascontiguousarray(plan).reshape(-1, 16)
+    weight = np.ascontiguousarray(weight, dtype=np.float32)
+    freqs = np.ascontiguousarray(freqs, dtype=np.float32)
+    out_loc = _i64(out_loc)
+    n_rows = rows.size // hd
+    rc = _load().orc_norm_rope_store(ratio, mode, hd, rope_dim, in_dtype, _p(rows), in_layout, n_rows, _p(plan),
+                                     plan.shape[0], _p(weight), float(eps), _p(freqs), freqs.shape[0], _p(out_loc),
+                                     out_loc.size, cache_dtype, _p(cache), cache.size // hd)
+    if rc:
+        raise OracleError(rc, "norm_rope_store")
 
 
 def double_to_bf16(x: float) -> int:

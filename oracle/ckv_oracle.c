@@ -542,4 +542,84 @@ int orc_compress_history(int ratio, int hd, int in_dtype, int out_dtype, const v
 }
 
 /* Exposed for the rounding pin (bf16 RNE from a double). */
+/* ----- norm + RoPE + store ([cv2] compress_norm_rope_store step) ---------- */
+
+/* After pooling, each compressed row goes through RMSNorm (weight, eps), then
+ * RoPE at position seq_len - ratio (clamped at 0), and is stored into the KV
+ * cache at out_loc ([cv2] _forward_compress_all_in_one step 2 and the unified
+ * path's steps 2 and 4):
+ *   decode  (mode 1): one record per batch row b (a DecodePlan); rows whose
+ *                     seq_len is not a multiple of the ratio are zeroed before
+ *                     the norm and still stored, at out_loc[b];
+ *   prefill (mode 0): one record per CompressPlan entry k; its row is k
+ *                     (compact layout) or ragged_id (token layout) and it is
+ *                     stored at out_loc[ragged_id].
+ * Invalid (all-ones) records are skipped.  RMSNorm: y_c = x_c * w_c /
+ * sqrt(mean_c x_c^2 + eps).  RoPE acts on the last rope_dim channels as
+ * rope_dim/2 interleaved pairs (2i, 2i+1): (a, b) -> (a cos - b sin,
+ * a sin + b cos) with (cos, sin) = freqs[pos][i] (fp32 table, [max_pos,
+ * rope_dim/2, 2]).  eps must be positive (the norm of a zeroed row is 0).
+ * Everything after reading x is carried in double and rounded once to the
+ * cache dtype (RNE). */
+int orc_norm_rope_store(int ratio, int mode, int hd, int rope_dim, int in_dtype, const void* rows, int in_layout,
+                        uint64_t n_rows, const void* plan, uint32_t n_records, const float* weight, float eps,
+                        const float* freqs, uint32_t max_pos, const int64_t* out_loc, uint64_t n_loc,
+                        int cache_dtype, void* cache, uint64_t cache_rows) {
+  if (ratio != 4 && ratio != 128) return ORC_BAD_RATIO;
+  if (hd <= 0 || hd % 128 != 0 || hd > 1024 || rope_dim < 0 || rope_dim % 2 || rope_dim > hd) return ORC_BAD_HEAD_DIM;
+  if ((in_dtype != ORC_F32 && in_dtype != ORC_BF16) || (cache_dtype != ORC_F32 && cache_dtype != ORC_BF16))
+    return ORC_BAD_DTYPE;
+  if (!(eps > 0.0f) || !isfinite(eps)) return ORC_BAD_LENGTH; /* a zero row would give 0 * inf */
+  double* y = (double*)malloc(sizeof(double) * (size_t)hd);
+  if (!y) return ORC_BAD_BATCH;
+  int rc = ORC_OK;
+  for (uint32_t k = 0; k < n_records && rc == ORC_OK; ++k) {
+    int64_t row, loc_index, pos;
+    int zero = 0;
+    if (mode == 1) {
+      const orc_plan_d* P = (const orc_plan_d*)plan + k;
+      if (P->seq_len == 0xFFFFFFFFu) continue;
+      row = k;
+      loc_index = k;
+      zero = P->seq_len % (uint32_t)ratio != 0;
+      pos = (int64_t)P->seq_len - (ORC_MUTANT == 16 ? 0 : ratio); /* mutant 16: position */
+      if (pos < 0) pos = 0;
+    } else {
+      const orc_plan_c* P = (const orc_plan_c*)plan + k;
+      if (P->seq_len == 0xFFFFFFFFu) continue;
+      const int64_t ragged = P->ragged_bl & 0x00FFFFFFu;
+      row = in_layout == ORC_OUT_COMPACT ? (int64_t)k : ragged;
+      loc_index = ragged;
+      pos = (int64_t)P->seq_len - (ORC_MUTANT == 16 ? 0 : ratio);
+    }
+    if ((uint64_t)row >= n_rows || (uint64_t)loc_index >= n_loc || pos < 0 || pos >= (int64_t)max_pos) {
+      rc = ORC_BAD_INDEX;
+      break;
+    }
+    const int64_t loc = out_loc[loc_index];
+    if (loc < 0 || (uint64_t)loc >= cache_rows) {
+      rc = ORC_BAD_INDEX;
+      break;
+    }
+    double ss = 0.0;
+    for (int c = 0; c < hd; ++c) {
+      y[c] = zero ? 0.0 : (double)load_elem(rows, (size_t)row * hd + c, in_dtype);
+      ss += y[c] * y[c];
+    }
+    const double r = 1.0 / sqrt(ss / hd + (double)eps);
+    for (int c = 0; c < hd; ++c) y[c] = y[c] * r * (double)weight[c];
+    const int base = ORC_MUTANT == 17 ? 0 : hd - rope_dim; /* mutant 17: rope on the first channels */
+    for (int i = 0; i < rope_dim / 2; ++i) {
+      const double cs = freqs[((size_t)pos * (rope_dim / 2) + i) * 2];
+      const double sn = freqs[((size_t)pos * (rope_dim / 2) + i) * 2 + 1];
+      const double a = y[base + 2 * i], b = y[base + 2 * i + 1];
+      y[base + 2 * i] = ORC_MUTANT == 15 ? a * cs + b * sn : a * cs - b * sn; /* mutant 15: rotation sign */
+      y[base + 2 * i + 1] = a * sn + b * cs;
+    }
+    for (int c = 0; c < hd; ++c) store_elem(cache, (size_t)loc * hd + c, cache_dtype, y[c]);
+  }
+  free(y);
+  return rc;
+}
+
 uint16_t orc_double_to_bf16(double x) { return double_to_bf16_bits(x); }

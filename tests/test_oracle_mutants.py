@@ -4,9 +4,11 @@ first-group mask, buffer_len off by one, a short write set, a decode slot off
 by one, a ragged id without its request offset, a wrong read page, a dropped
 term, a sign error, an input row off by one; in the SWA-paged planner: no
 page-end writes, the ring offset taken modulo the page size, records without
-state reads translated) must fail at least one pin."""
+state reads translated; in norm + RoPE: a rotation sign, the position, the
+rotated channels) must fail at least one pin."""
 import pytest
 
+from tests import test_oracle_norm_rope as N
 from tests import test_oracle_paged as Q
 from tests import test_oracle_pins as P
 
@@ -25,6 +27,9 @@ MUTANTS = {
     12: "paged C4 write set without the SWA page ends",
     13: "paged ring offset modulo the SWA page size",
     14: "paged records without state reads translated",
+    15: "RoPE rotation sign",
+    16: "RoPE position seq_len instead of seq_len - ratio",
+    17: "RoPE on the first rope_dim channels",
 }
 
 
@@ -44,6 +49,10 @@ def pins(o):
         yield lambda ratio=ratio: Q.test_identity_mapping_gives_legacy_plans(o, ratio, 0)
     yield lambda: Q.test_page_end_positions_are_written_before_first_write(o)
     yield lambda: Q.test_paged_schedules_equal_history(o, 0)
+    yield lambda: N.test_constant_row_normalises_to_the_weight(o)
+    yield lambda: N.test_matches_float64_torch(o, 1)
+    yield lambda: N.test_rotation_keeps_pair_lengths_and_relative_positions(o)
+    yield lambda: N.test_position_is_seq_len_minus_ratio(o)
 
 
 @pytest.mark.parametrize("mutant", sorted(MUTANTS))
