@@ -592,7 +592,9 @@ int orc_norm_rope_store(int ratio, int mode, int hd, int rope_dim, int in_dtype,
       loc_index = ragged;
       pos = (int64_t)P->seq_len - (ORC_MUTANT == 16 ? 0 : ratio);
     }
-    if ((uint64_t)row >= n_rows || (uint64_t)loc_index >= n_loc || pos < 0 || pos >= (int64_t)max_pos) {
+    /* the table is read only when there is something to rotate */
+    if ((uint64_t)row >= n_rows || (uint64_t)loc_index >= n_loc || pos < 0 ||
+        (rope_dim > 0 && pos >= (int64_t)max_pos)) {
       rc = ORC_BAD_INDEX;
       break;
     }
