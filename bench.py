@@ -22,8 +22,10 @@ API with the step's inputs copied from pinned host memory and its outputs
 copied back inside the timed region.
 
 ``--config NAME`` times one workload alone (c4_prefill_small, c4_decode,
-c128_decode, c4_prefill, c128_prefill; ``all`` for each in turn) and prints
-one line per workload.  ``--impl reference`` times the CPU oracle on the
+c128_decode, c4_prefill, c128_prefill, the speculative-decoding verify shapes
+c4_prefill_mtp / c128_prefill_mtp, and the norm + RoPE + store step on the
+C128 rows, norm_rope_c128_prefill / norm_rope_c128_decode; ``all`` for each
+in turn) and prints one line per workload.  ``--impl reference`` times the CPU oracle on the
 host cores over a bounded sample of the same step.
 """
 from __future__ import annotations
@@ -301,8 +303,90 @@ class DecodeRunner:
     def restore(self):
         self.state.copy_(self.pristine)
 
+    def steady_fns(self, n: int):
+        """n launches of the decode kernel, each on its own copy of the state, input, plan and output."""
+        self.plan()
+        torch.cuda.synchronize()
+        fns = []
+        for i in range(n):
+            st = self.state if i == 0 else self.pristine.clone()
+            kv, pd, out = self.kv.clone(), self.plan_d[: self.w.batch].clone(), self.out[: self.w.batch].clone()
+
+            def fn(st=st, kv=kv, pd=pd, out=out):
+                self.ckv.compress_decode(self.w.ratio, self.w.head_dim, st, kv, self.ape, pd, self.w.out_dtype, out,
+                                         self.status)
+            fns.append(fn)
+        return fns
+
 
 _cudart = None
+
+
+class NormRopeRunner:
+    """Device buffers of the norm + RoPE + store step over one set of compressed rows.  The plan it reads is
+    built once, by the library's planner, before any timing."""
+
+    def __init__(self, ckv, x: wl.NormRopeInputs, dev):
+        self.ckv, self.x, self.dev = ckv, x, dev
+        self.status = ckv.new_status(dev)
+        self.rows = x.rows.to(dev)
+        self.weight = x.weight.to(dev)
+        self.freqs = x.freqs.to(dev)
+        self.out_loc = x.out_loc.to(dev)
+        self.cache = torch.zeros(x.cache_rows, x.head_dim, dtype=x.cache_dtype, device=dev)
+        rid, sl = x.rid.to(dev), x.seq_lens.to(dev)
+        if x.extend_lens is not None:
+            nq = int(x.extend_lens.sum())
+            self.plan_c, _, self.counts = ckv.plan_prefill(x.ratio, rid, sl, x.extend_lens.to(dev), nq,
+                                                           status=self.status)
+            torch.cuda.synchronize()
+            self.records = int(self.counts[0])
+            if self.records > self.rows.shape[0]:
+                raise RuntimeError("fewer rows than compress records")
+        else:
+            self.plan_d = ckv.plan_decode(x.ratio, rid, sl, status=self.status)
+            self.records = rid.numel()
+        self.boundary = int((x.seq_lens % x.ratio == 0).sum()) if x.extend_lens is None else self.records
+
+    def run(self):
+        c, x = self.ckv, self.x
+        if x.extend_lens is not None:
+            c.norm_rope_store_prefill(x.ratio, self.rows, self.plan_c, self.counts, self.weight, x.eps, self.freqs,
+                                      self.out_loc, self.cache, in_layout=c.OUT_COMPACT, status=self.status)
+        else:
+            c.norm_rope_store_decode(x.ratio, self.rows, self.plan_d, self.weight, x.eps, self.freqs, self.out_loc,
+                                     self.cache, status=self.status)
+
+    def restore(self):
+        pass
+
+    def steady_fns(self, n: int):
+        """n launches, each on its own copy of the rows, plan and out_loc (table, weight and cache shared)."""
+        c, x = self.ckv, self.x
+        fns = []
+        for i in range(n):
+            rows, loc = self.rows.clone(), self.out_loc.clone()
+            if x.extend_lens is not None:
+                pc, cnt = self.plan_c.clone(), self.counts.clone()
+
+                def fn(rows=rows, loc=loc, pc=pc, cnt=cnt):
+                    c.norm_rope_store_prefill(x.ratio, rows, pc, cnt, self.weight, x.eps, self.freqs, loc,
+                                              self.cache, in_layout=c.OUT_COMPACT, status=self.status)
+            else:
+                pd = self.plan_d.clone()
+
+                def fn(rows=rows, loc=loc, pd=pd):
+                    c.norm_rope_store_decode(x.ratio, rows, pd, self.weight, x.eps, self.freqs, loc, self.cache,
+                                             status=self.status)
+            fns.append(fn)
+        return fns
+
+    def algorithmic_bytes(self) -> int:
+        """Rows read (decode: boundary rows only; the rest are zero), cache rows written, plan and out_loc
+        entries, one table row per record and the weight."""
+        x = self.x
+        per_write = x.head_dim * elem(x.cache_dtype) + 16 + 8 + 4 * x.rope_dim
+        return self.boundary * x.head_dim * 4 + self.records * per_write + x.head_dim * 4
 
 
 def cudart():
@@ -359,9 +443,60 @@ class StepGraph:
         return [self.evs[i].elapsed_time(self.evs[i + 1]) for i in range(len(self.names))]
 
 
+class L2Flush:
+    """Writes a buffer of twice the L2 size, then reads another one of the same
+    size: the timed region that follows starts with an L2 that holds none of
+    its inputs and no dirty lines (whose write-back would otherwise compete
+    with the timed kernel's own traffic)."""
+
+    def __init__(self, dev):
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        n = 2 * max(l2, 64 << 20)
+        self.w = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(n // 4, dtype=torch.int32, device=dev)
+
+    def zero_(self):
+        self.w.zero_()
+        self.r.max()
+
+
 def l2_flush_buffer(dev):
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    return torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+    return L2Flush(dev)
+
+
+def l2_bytes(dev) -> int:
+    return torch.cuda.get_device_properties(dev).L2_cache_size
+
+
+def copies_for(bytes_per_launch: int, dev, cap: int = 16) -> int:
+    """Input copies needed so that the other copies' traffic between two uses of one copy exceeds twice the L2."""
+    return int(min(cap, max(2, -(-2 * l2_bytes(dev) // max(bytes_per_launch, 1)) + 1)))
+
+
+def steady_state_us(fns, reps: int = 10, samples: int = 5) -> float:
+    """Mean device time of one launch when launches run back to back, each of
+    `fns` on its own copy of the inputs (the copies together exceed the L2, so
+    every launch reads its inputs from HBM): one CUDA graph of reps x len(fns)
+    launches bracketed by two events; the median of `samples` replays."""
+    for f in fns:
+        f()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            for f in fns:
+                f()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g.replay()
+    ts = []
+    for _ in range(samples):
+        torch.cuda.synchronize()
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts) * 1e3 / (reps * len(fns))
 
 
 def run_graph(step: StepGraph, flush, restore, steps, warmup, ws, sampler=None):
@@ -467,6 +602,11 @@ def bench_step(args, ws, rank, local):
     dec_ms = float(seg_ms[:, 3].mean())
     dec_gbs = b3["decode"] / (dec_ms * 1e-3) / 1e9
     step_bytes = b5["total"] + b3["total"]
+    # the decode kernel back to back over copies of its inputs that together exceed the L2 (a kernel of ~10 us
+    # is not resolved by event nodes around it: they add the graph's node-to-node latency)
+    n_dec = copies_for(b3["decode"], dev)
+    dec_steady_us = steady_state_us(dec.steady_fns(n_dec))
+    dec_steady_gbs = b3["decode"] / (dec_steady_us * 1e-6) / 1e9
 
     # ---- end to end: inputs from pinned host memory, outputs back, inside the timed region
     h_kv5 = w5.kv_score.pin_memory()
@@ -509,7 +649,8 @@ def bench_step(args, ws, rank, local):
                    "num_q_tokens": w5.num_q_tokens, "compress_rows_prefill": b5["rows"],
                    "compress_rows_decode": b3["rows"], "head_dim": 512, "in_dtype": "bf16", "out_dtype": "f32",
                    "parallelism": f"independent requests x{ws} (no collective)",
-                   "l2": "flushed before every step (2x L2 written), prefill state restored outside the timing",
+                   "l2": "flushed before every step (2x L2 written, then 2x L2 read), prefill state restored "
+                         "outside the timing",
                    "algorithmic_bytes_per_step": step_bytes},
         "roofline": {"bound": "hbm", "kernel": "c128_pool_kernel (prefill)", "achieved": pool_gbs, "peak": peak,
                      "unit": "GB/s", "frac": pool_gbs / peak, "peak_kind": f"{peak_kind} hbm_gbs",
@@ -521,6 +662,8 @@ def bench_step(args, ws, rank, local):
             "pool_prefill_us": pool_ms * 1e3, "pool_prefill_gbs": pool_gbs,
             "write_plus_plan_decode_us": float(seg_ms[:, 2].mean()) * 1e3,
             "decode_us": dec_ms * 1e3, "decode_gbs": dec_gbs, "decode_frac": dec_gbs / peak,
+            "decode_back_to_back_us": dec_steady_us, "decode_back_to_back_gbs": dec_steady_gbs,
+            "decode_back_to_back_frac": dec_steady_gbs / peak, "decode_back_to_back_copies": n_dec,
             "sum_of_kernel_segments_us": float(seg_ms.sum(1).mean()) * 1e3,
             "step_gbs": step_bytes / (float(step_ms.mean()) * 1e-3) / 1e9},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
@@ -558,6 +701,8 @@ def bench_config(args, name, ws, rank, local):
     B.build()
     ckv.load_library()
     dev = torch.device("cuda", local)
+    if name in wl.NORM_ROPE:
+        return bench_norm_rope(args, name, ws, rank, ckv, dev)
     w = small_workload(name, args.seed + rank) if args.small else wl.NAMED[name](args.seed + rank)
     flush = l2_flush_buffer(dev)
     b = algorithmic_bytes(w)
@@ -579,13 +724,46 @@ def bench_config(args, name, ws, rank, local):
     step_ms = whole_ms[:, 0]
     main_ms = float(seg_ms[:, main_i].mean())
     gbs = b[main_key] / (main_ms * 1e-3) / 1e9
+    steady = {}
+    if w.mode == "decode":
+        n = copies_for(b["decode"], dev)
+        us = steady_state_us(r.steady_fns(n))
+        sg = b["decode"] / (us * 1e-6) / 1e9
+        steady = {"back_to_back_us": us, "back_to_back_gbs": sg, "back_to_back_frac": sg / peak,
+                  "back_to_back_copies": n}
     line = {"workload": name, **w.describe(), "rows_per_step": b["rows"],
             "rows_per_s": b["rows"] / (float(step_ms.mean()) * 1e-3), "ms_per_step": float(step_ms.mean()),
             "step_gbs": b["total"] / (float(step_ms.mean()) * 1e-3) / 1e9,
             "segments_us": {n: float(seg_ms[:, i].mean()) * 1e3 for i, n in enumerate(step.names)},
             "segments_us_min": {n: float(seg_ms[:, i].min()) * 1e3 for i, n in enumerate(step.names)},
             "main_kernel": step.names[main_i], "main_bytes": b[main_key], "main_gbs": gbs, "main_frac": gbs / peak,
-            "peak_gbs": peak, "peak_kind": kind, "algorithmic_bytes": b}
+            "peak_gbs": peak, "peak_kind": kind, "algorithmic_bytes": b, **steady}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def bench_norm_rope(args, name, ws, rank, ckv, dev):
+    """The norm + RoPE + store step alone on one set of compressed rows; prints one line."""
+    x = wl.NORM_ROPE[name](args.seed + rank)
+    flush = l2_flush_buffer(dev)
+    r = NormRopeRunner(ckv, x, dev)
+    step = StepGraph([("norm_rope_store", r.run)])
+    seg_ms, _, _ = run_graph(step, flush, r.restore, args.steps, args.warmup, ws)
+    if int(r.status[0]):
+        raise RuntimeError(f"device status {int(r.status[0])}")
+    peak, kind = peaks()
+    ms = float(seg_ms[:, 0].mean())
+    b = r.algorithmic_bytes()
+    gbs = b / (ms * 1e-3) / 1e9
+    n = copies_for(b, dev)
+    us = steady_state_us(r.steady_fns(n))
+    sg = b / (us * 1e-6) / 1e9
+    line = {"workload": name, "ratio": x.ratio, "head_dim": x.head_dim, "rope_dim": x.rope_dim,
+            "records": r.records, "rows_read": r.boundary, "cache_dtype": str(x.cache_dtype).replace("torch.", ""),
+            "rows_per_s": r.records / (ms * 1e-3), "us": ms * 1e3, "us_min": float(seg_ms[:, 0].min()) * 1e3,
+            "main_kernel": "norm_rope_store_kernel", "main_bytes": b, "main_gbs": gbs, "main_frac": gbs / peak,
+            "peak_gbs": peak, "peak_kind": kind, "back_to_back_us": us, "back_to_back_gbs": sg,
+            "back_to_back_frac": sg / peak, "back_to_back_copies": n}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -626,7 +804,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="step", help="step (default) | all | " + " | ".join(wl.NAMED))
+    ap.add_argument("--config", default="step",
+                    help="step (default) | all | " + " | ".join(list(wl.NAMED) + list(wl.NORM_ROPE)))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true", help="with --config: scaled-down workloads for profiling")
@@ -641,7 +820,7 @@ def main():
     elif args.config == "step":
         bench_step(args, ws, rank, local)
     else:
-        names = list(wl.NAMED) if args.config == "all" else [args.config]
+        names = list(wl.NAMED) + list(wl.NORM_ROPE) if args.config == "all" else [args.config]
         for n in names:
             bench_config(args, n, ws, rank, local)
     if ws > 1:

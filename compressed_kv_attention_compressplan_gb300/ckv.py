@@ -77,6 +77,11 @@ def load_library():
         lib.ckv_compress_prefill.argtypes = [i32, i32, i32, i32, vp, u64, vp, u32, vp, vp, vp, vp, u32, u32, i32,
                                              vp, vp, vp]
         lib.ckv_compress_decode.argtypes = [i32, i32, i32, i32, vp, u64, vp, vp, vp, u32, vp, vp, vp]
+        f32 = ctypes.c_float
+        lib.ckv_norm_rope_store_prefill.argtypes = [i32, i32, i32, i32, vp, i32, u64, vp, vp, u32, vp, f32, vp, u32,
+                                                    vp, u64, i32, vp, u64, vp, vp]
+        lib.ckv_norm_rope_store_decode.argtypes = [i32, i32, i32, i32, vp, vp, u32, vp, f32, vp, u32, vp, i32, vp,
+                                                   u64, vp, vp]
         lib.ckv_error_string.argtypes = [i32]
         lib.ckv_error_string.restype = ctypes.c_char_p
         lib.ckv_version.restype = i32
@@ -284,6 +289,42 @@ def compress_decode(ratio: int, head_dim: int, state: torch.Tensor, kv_score: to
                                               _ptr(ape), _ptr(plan_d), batch, _ptr(out), _ptr(status),
                                               _stream(stream)), "ckv_compress_decode")
     return out[:batch]
+
+
+# ------------------------------------------------------------------------------ norm, RoPE, store
+def _nr_common(rows: torch.Tensor, norm_weight: torch.Tensor, freqs: torch.Tensor, kv_cache: torch.Tensor):
+    if norm_weight.dtype != torch.float32 or freqs.dtype != torch.float32 or freqs.dim() != 3 or freqs.shape[2] != 2:
+        raise ValueError("norm_weight must be fp32 [head_dim] and freqs fp32 [max_pos, rope_dim/2, 2]")
+    head_dim = kv_cache.shape[-1]
+    return head_dim, 2 * freqs.shape[1], dtype_code(rows.dtype), dtype_code(kv_cache.dtype)
+
+
+def norm_rope_store_prefill(ratio: int, rows: torch.Tensor, plan_c: torch.Tensor, counts: Optional[torch.Tensor],
+                            norm_weight: torch.Tensor, eps: float, freqs: torch.Tensor, out_loc: torch.Tensor,
+                            kv_cache: torch.Tensor, in_layout: int = OUT_COMPACT, status: Optional[torch.Tensor] = None,
+                            stream=None) -> None:
+    """RMSNorm + RoPE of the pooled prefill rows, stored into ``kv_cache`` at ``out_loc[ragged_id]``."""
+    hd, rope_dim, ci, cc = _nr_common(rows, norm_weight, freqs, kv_cache)
+    _check(load_library().ckv_norm_rope_store_prefill(ratio, hd, rope_dim, ci, _ptr(rows), in_layout, rows.shape[0],
+                                                      _ptr(plan_c), _ptr(counts), plan_c.shape[0], _ptr(norm_weight),
+                                                      float(eps), _ptr(freqs), freqs.shape[0], _ptr(out_loc),
+                                                      out_loc.numel(), cc, _ptr(kv_cache), kv_cache.shape[0],
+                                                      _ptr(status), _stream(stream)),
+           "ckv_norm_rope_store_prefill")
+
+
+def norm_rope_store_decode(ratio: int, rows: torch.Tensor, plan_d: torch.Tensor, norm_weight: torch.Tensor,
+                           eps: float, freqs: torch.Tensor, out_loc: torch.Tensor, kv_cache: torch.Tensor,
+                           status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """RMSNorm + RoPE of the decode output rows (non-boundary rows stored as zeros) at ``out_loc[b]``."""
+    hd, rope_dim, ci, cc = _nr_common(rows, norm_weight, freqs, kv_cache)
+    if out_loc.numel() < plan_d.shape[0]:
+        raise ValueError("out_loc needs one entry per batch row")
+    _check(load_library().ckv_norm_rope_store_decode(ratio, hd, rope_dim, ci, _ptr(rows), _ptr(plan_d),
+                                                     plan_d.shape[0], _ptr(norm_weight), float(eps), _ptr(freqs),
+                                                     freqs.shape[0], _ptr(out_loc), cc, _ptr(kv_cache),
+                                                     kv_cache.shape[0], _ptr(status), _stream(stream)),
+           "ckv_norm_rope_store_decode")
 
 
 # ------------------------------------------------------------------------------ convenience

@@ -573,6 +573,6 @@ const char* ckv_error_string(int code) {
   }
 }
 
-int ckv_version(void) { return 100; }
+int ckv_version(void) { return 101; }
 
 }  // extern "C"

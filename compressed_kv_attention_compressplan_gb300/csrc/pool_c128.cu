@@ -393,10 +393,19 @@ struct PersistCfg {
   static_assert(NS % NG == 0, "each consumer group owns every NG-th stage");
 };
 
-// Decode plan row r: valid (in range) and on a page boundary?
+// Decode plan row r: valid (in range) and on a page boundary?  One coherent
+// 16-byte load that the compiler may not repeat later (a read-only load could
+// be re-issued after the scan's barriers, a second memory round trip).
 __device__ __forceinline__ bool decode_row(const PoolArgs& a, uint32_t r, bool& valid, bool& boundary,
                                            ckv_decode_plan_t& P) {
-  P = load_plan_d(a.plan_d + r);
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(a.plan_d + r));
+  P.seq_len = v.x;
+  P.write_loc = static_cast<int32_t>(v.y);
+  P.read_page_0 = static_cast<int32_t>(v.z);
+  P.read_page_1 = static_cast<int32_t>(v.w);
   valid = false;
   boundary = false;
   if (P.seq_len == kInvalidU32) return false;  // invalid record: zero output, nothing else
@@ -509,14 +518,14 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
     abort_flag = 0;
     fence_mbar_init();
   }
-  // the consumers' ape slice is loaded first, so that it overlaps the plan scan
   const int grp = t / NCG;
   const int tl = t % NCG;
   const int q = tl % T::QUADS;
   const int g = tl / T::QUADS;
   const int cq = 4 * q;
   F2 ape_r[16][2];
-  if (kDecode && warp < NC / 32) load_ape_regs<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
+  // the tensor map is a kernel parameter: fetch its descriptor while the plan is scanned
+  if (warp == NC / 32 && lane == 0) prefetch_map(kDecode ? &page_map : &in_map);
 
   pdl_wait();  // everything below may read what the previous kernel wrote
   pdl_release();
@@ -584,7 +593,6 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
 
   if (warp == NC / 32) {
     // ---------------- producer warp
-    if (lane == 0) prefetch_map(kDecode ? &page_map : &in_map);
     for (uint32_t n = 0; n < items; ++n) {
       const int stage = static_cast<int>(n % NS);
       const uint32_t phase = (n / NS) & 1u;
@@ -639,11 +647,10 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
 
   // ---------------- consumer warps: group grp takes items grp, grp + NG, ...
   // (decode: first the rows that read no page, while the first tiles load)
-  if constexpr (kDecode) {
-    decode_rows_without_window<TIn, TOut, NC>(a, trivrow, ntriv, t);
-  } else {
-    load_ape_regs<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
-  }
+  // (the ape slice is loaded after the plan scan, so that the scan's loads do
+  // not queue behind it)
+  load_ape_regs<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
+  if constexpr (kDecode) decode_rows_without_window<TIn, TOut, NC>(a, trivrow, ntriv, t);
   uint32_t local = 0;
   for (uint32_t n = grp; n < items; n += NG, ++local) {
     // one decision for the whole group (also orders the reuse of its reduction buffers)

@@ -191,13 +191,19 @@ def c4_decode(seed: int = 0, batch: int = 256, head_dim: int = 512) -> Workload:
                 seed, num_requests_state=batch)
 
 
-def c128_decode(seed: int = 0, batch: int = 512, head_dim: int = 512) -> Workload:
+def c128_decode_lengths(seed: int = 0, batch: int = 512):
+    """(rid, seq_lens) of the C128 decode workload: seq_len ~ U[1, 32768], a quarter on page boundaries."""
     g = _gen(seed, 1)
     seq_lens = torch.randint(1, 32768 + 1, (batch,), generator=g, dtype=torch.int64)
     forced = torch.randperm(batch, generator=_gen(seed, 3))[: batch // 4]
     seq_lens[forced] = 128 * torch.randint(1, 256 + 1, (forced.numel(),), generator=_gen(seed, 4),
                                            dtype=torch.int64)
     rid = torch.randperm(batch, generator=_gen(seed, 2))
+    return rid, seq_lens
+
+
+def c128_decode(seed: int = 0, batch: int = 512, head_dim: int = 512) -> Workload:
+    rid, seq_lens = c128_decode_lengths(seed, batch)
     return make("c128_decode", "decode", 128, head_dim, torch.bfloat16, torch.float32, TOKEN, rid, seq_lens,
                 None, seed, num_requests_state=batch)
 
@@ -211,16 +217,22 @@ def c4_prefill(seed: int = 0, batch: int = 64, head_dim: int = 512, max_prefix: 
                 seed, num_requests_state=batch)
 
 
-def c128_prefill(seed: int = 0, batch: int = 1024, head_dim: int = 512, num_long: int = 128,
-                 short_extend: int = 4, long_extend=(128, 16384), max_prefix: int = 65536) -> Workload:
+def c128_prefill_lengths(seed: int = 0, batch: int = 1024, num_long: int = 128, short_extend: int = 4,
+                         long_extend=(128, 16384), max_prefix: int = 65536):
+    """(rid, seq_lens, extend_lens) of the C128 prefill workload."""
     el = torch.full((batch,), short_extend, dtype=torch.int64)
     long_ids = torch.randperm(batch, generator=_gen(seed, 6))[:num_long]
     el[long_ids] = torch.randint(long_extend[0], long_extend[1] + 1, (num_long,), generator=_gen(seed, 5),
                                  dtype=torch.int64)
     pl = torch.randint(0, max_prefix + 1, (batch,), generator=_gen(seed, 1), dtype=torch.int64)
     rid = torch.randperm(batch, generator=_gen(seed, 2))
-    return make("c128_prefill", "prefill", 128, head_dim, torch.bfloat16, torch.float32, COMPACT, rid, pl + el,
-                el, seed, num_requests_state=batch, outlier_frac=0.01)
+    return rid, pl + el, el
+
+
+def c128_prefill(seed: int = 0, batch: int = 1024, head_dim: int = 512, **lengths) -> Workload:
+    rid, sl, el = c128_prefill_lengths(seed, batch, **lengths)
+    return make("c128_prefill", "prefill", 128, head_dim, torch.bfloat16, torch.float32, COMPACT, rid, sl, el,
+                seed, num_requests_state=batch, outlier_frac=0.01)
 
 
 def c128_prefill_mtp(seed: int = 0, batch: int = 1024, extend: int = 4, head_dim: int = 512,
@@ -251,6 +263,61 @@ NAMED = {
     "c4_prefill_mtp": c4_prefill_mtp,
     "c128_prefill_mtp": c128_prefill_mtp,
 }
+
+
+# ----------------------------------------------------------------------------- norm + RoPE + store inputs
+def rope_table(max_pos: int, rope_dim: int, base: float = 10000.0) -> torch.Tensor:
+    """fp32 [max_pos, rope_dim/2, 2]: cos / sin of pos * base^(-2i/rope_dim), formed in float64."""
+    inv = base ** (-torch.arange(0, rope_dim, 2, dtype=torch.float64) / rope_dim)
+    ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * inv[None, :]
+    return torch.stack([torch.cos(ang), torch.sin(ang)], dim=-1).to(torch.float32)
+
+
+@dataclasses.dataclass
+class NormRopeInputs:
+    """Inputs of the norm + RoPE + store step over the compressed rows of a workload."""
+    name: str
+    ratio: int
+    head_dim: int
+    rope_dim: int
+    rid: torch.Tensor
+    seq_lens: torch.Tensor
+    extend_lens: Optional[torch.Tensor]   # None: decode
+    rows: torch.Tensor        # fp32 [num_rows, head_dim] (prefill: compact, one per compress record)
+    weight: torch.Tensor      # fp32 [head_dim]
+    eps: float
+    freqs: torch.Tensor       # fp32 [max_pos, rope_dim/2, 2]
+    out_loc: torch.Tensor     # int64, one cache row per token (prefill) or per batch row (decode)
+    cache_rows: int
+    cache_dtype: torch.dtype
+
+
+def norm_rope_c128_prefill(seed: int = 0, head_dim: int = 512, rope_dim: int = 64) -> NormRopeInputs:
+    """The compressed rows of the C128 prefill workload (compact fp32) into a bf16 cache."""
+    rid, sl, el = c128_prefill_lengths(seed)
+    nq = int(el.sum())
+    # at least one row per compress record (a request adds at most extend_len / 128 + 1)
+    rows = normal((nq // 128 + rid.numel(), head_dim), torch.float32, 1.0, _seed(seed, 21))
+    weight = 1.0 + normal((head_dim,), torch.float32, 0.1, _seed(seed, 22))
+    cache_rows = nq  # every token owns a distinct cache row
+    out_loc = torch.randperm(cache_rows, generator=_gen(seed, 23)).to(torch.int64)
+    return NormRopeInputs("norm_rope_c128_prefill", 128, head_dim, rope_dim, rid, sl, el, rows, weight, 1e-6,
+                          rope_table(int(sl.max()) + 1, rope_dim), out_loc, cache_rows, torch.bfloat16)
+
+
+def norm_rope_c128_decode(seed: int = 0, head_dim: int = 512, rope_dim: int = 64) -> NormRopeInputs:
+    """The decode output rows of the C128 decode workload into a bf16 cache."""
+    rid, sl = c128_decode_lengths(seed)
+    batch = rid.numel()
+    rows = normal((batch, head_dim), torch.float32, 1.0, _seed(seed, 21))
+    weight = 1.0 + normal((head_dim,), torch.float32, 0.1, _seed(seed, 22))
+    cache_rows = 4 * batch
+    out_loc = torch.randperm(cache_rows, generator=_gen(seed, 23))[:batch].to(torch.int64)
+    return NormRopeInputs("norm_rope_c128_decode", 128, head_dim, rope_dim, rid, sl, None, rows, weight, 1e-6,
+                          rope_table(int(sl.max()) + 1, rope_dim), out_loc, cache_rows, torch.bfloat16)
+
+
+NORM_ROPE = {"norm_rope_c128_prefill": norm_rope_c128_prefill, "norm_rope_c128_decode": norm_rope_c128_decode}
 
 
 def random_prefill(ratio: int, head_dim: int, in_dtype, out_dtype, out_layout: str, prefix_lens, extend_lens,

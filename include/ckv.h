@@ -240,6 +240,48 @@ int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, vo
                         const void* kv_score_input, const void* ape, const ckv_decode_plan_t* plan_d,
                         uint32_t batch, void* out, uint32_t* d_status, ckv_stream_t stream);
 
+/* ------------------------------------------------------- norm, RoPE, store */
+/* The step after pooling (compressor_v2.py compress_norm_rope_store and the
+ * unified path's steps 2-4): every compressed row is normalised, rotated and
+ * stored into the KV cache.
+ *   y_c = x_c * norm_weight[c] / sqrt(mean_c(x_c^2) + eps)        (RMSNorm)
+ * then the last rope_dim channels turn as interleaved pairs (2i, 2i+1):
+ *   (a, b) -> (a*cos - b*sin, a*sin + b*cos),  (cos, sin) = freqs[pos][i],
+ * with pos = max(seq_len - ratio, 0) from the row's plan record, and y is
+ * written, rounded to cache_dtype, to kv_cache row out_loc.
+ *   rows       the pooled output (in_dtype CKV_F32 or CKV_BF16).
+ *   norm_weight fp32 [head_dim]; eps > 0 (else CKV_ERR_SIZE).
+ *   freqs      fp32 [max_pos, rope_dim/2, 2] (cos, sin); rope_dim a multiple
+ *              of 4, 0 <= rope_dim <= head_dim (else CKV_ERR_HEAD_DIM).  The
+ *              table and the channel split are the caller's (compressor_v2.py
+ *              takes both from the model).  With rope_dim 0 the table is
+ *              not read (freqs may be NULL).
+ *   kv_cache   [cache_rows, head_dim] of cache_dtype (CKV_BF16 or CKV_F32).
+ * Records whose position, row or out_loc falls outside the table, the rows
+ * or the cache are skipped with CKV_STATUS_BAD_INDEX.  Runs after the pooling
+ * of the same step on the same stream.
+ *
+ * Prefill: one record per CompressPlan entry (the first min(d_counts[0],
+ * capacity_c); all capacity_c when d_counts is NULL; invalid ones skipped).
+ * Its row is k (in_layout CKV_OUT_COMPACT) or ragged_id (CKV_OUT_TOKEN) of
+ * rows [n_rows, head_dim]; it is stored at out_loc[ragged_id] (out_loc is
+ * int64 [n_out_loc], indexed by token). */
+int ckv_norm_rope_store_prefill(int ratio, int head_dim, int rope_dim, int in_dtype, const void* rows,
+                                int in_layout, uint64_t n_rows, const ckv_compress_plan_t* plan_c,
+                                const uint32_t* d_counts, uint32_t capacity_c, const float* norm_weight, float eps,
+                                const float* freqs, uint32_t max_pos, const int64_t* out_loc, uint64_t n_out_loc,
+                                int cache_dtype, void* kv_cache, uint64_t cache_rows, uint32_t* d_status,
+                                ckv_stream_t stream);
+
+/* Decode: row b of rows [batch, head_dim] with DecodePlan record b; rows whose
+ * seq_len is not a multiple of the ratio are zeroed before the norm and are
+ * still stored, at out_loc[b] (int64 [batch]), as compressor_v2.py does with
+ * its dummy location 0. */
+int ckv_norm_rope_store_decode(int ratio, int head_dim, int rope_dim, int in_dtype, const void* rows,
+                               const ckv_decode_plan_t* plan_d, uint32_t batch, const float* norm_weight, float eps,
+                               const float* freqs, uint32_t max_pos, const int64_t* out_loc, int cache_dtype,
+                               void* kv_cache, uint64_t cache_rows, uint32_t* d_status, ckv_stream_t stream);
+
 /* ------------------------------------------------------------------ misc */
 /* Short text for a CKV_OK / CKV_ERR_* code (static storage). */
 const char* ckv_error_string(int code);

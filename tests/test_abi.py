@@ -46,6 +46,8 @@ def test_capacity_bounds(lib):
     assert ckv.capacity_write(4, 64, 10 ** 6) == 64 * 7
     assert ckv.capacity_write(128, 1024, 5000) == 5000
     assert ckv.capacity_compress(5, 1, 1) == 0
+    assert ckv.capacity_write_paged(4, 2, 100, 16) == 2 * 7 + 4 * (100 // 16 + 2)
+    assert ckv.capacity_write_paged(128, 1024, 5000, 256) == ckv.capacity_write(128, 1024, 5000)
 
 
 def test_argument_errors_are_returned_before_any_launch(lib):
@@ -60,4 +62,14 @@ def test_argument_errors_are_returned_before_any_launch(lib):
     assert lib.ckv_compress_pool_prefill(128, 512, 1, 0, None, 0, None, 10, None, None, None, 1, 9, None, None,
                                          None) == -5
     assert lib.ckv_compress_write(4, 2048, 1, None, 0, None, 0, None, None, 1, None, None) == -2
+    f = ctypes.c_float
+    nrd = lib.ckv_norm_rope_store_decode
+    assert nrd(4, 512, 64, 0, None, None, 1, None, f(0.0), None, 16, None, 1, None, 16, None, None) == -3  # eps
+    assert nrd(4, 512, 30, 0, None, None, 1, None, f(1e-6), None, 16, None, 1, None, 16, None, None) == -2
+    assert nrd(4, 512, 64, 7, None, None, 1, None, f(1e-6), None, 16, None, 1, None, 16, None, None) == -5
+    assert nrd(4, 512, 64, 0, None, None, 1, None, f(1e-6), None, 16, None, 1, None, 16, None, None) == -4
+    assert nrd(4, 512, 64, 0, None, None, 0, None, f(1e-6), None, 16, None, 1, None, 16, None, None) == 0
+    assert lib.ckv_plan_decode_paged(128, None, None, 0, 0, None, 0, 256, 256, None, 1, None, None, None) == -3
+    assert lib.ckv_plan_prefill_paged(4, None, None, 8, 1, None, 8, 16, 4, None, None, 1, 4, 4, 4, 0, None, None,
+                                      None, None, None) == -3  # a 4-row ring
     assert lib.ckv_error_string(-4) != lib.ckv_error_string(0)
