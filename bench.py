@@ -604,9 +604,13 @@ def bench_step(args, ws, rank, local):
     step_bytes = b5["total"] + b3["total"]
     # the decode kernel back to back over copies of its inputs that together exceed the L2 (a kernel of ~10 us
     # is not resolved by event nodes around it: they add the graph's node-to-node latency)
-    n_dec = copies_for(b3["decode"], dev)
-    dec_steady_us = steady_state_us(dec.steady_fns(n_dec))
-    dec_steady_gbs = b3["decode"] / (dec_steady_us * 1e-6) / 1e9
+    back_to_back = {}
+    if not args.no_back_to_back:
+        n_dec = copies_for(b3["decode"], dev)
+        us = steady_state_us(dec.steady_fns(n_dec))
+        gbs = b3["decode"] / (us * 1e-6) / 1e9
+        back_to_back = {"decode_back_to_back_us": us, "decode_back_to_back_gbs": gbs,
+                        "decode_back_to_back_frac": gbs / peak, "decode_back_to_back_copies": n_dec}
 
     # ---- end to end: inputs from pinned host memory, outputs back, inside the timed region
     h_kv5 = w5.kv_score.pin_memory()
@@ -662,8 +666,7 @@ def bench_step(args, ws, rank, local):
             "pool_prefill_us": pool_ms * 1e3, "pool_prefill_gbs": pool_gbs,
             "write_plus_plan_decode_us": float(seg_ms[:, 2].mean()) * 1e3,
             "decode_us": dec_ms * 1e3, "decode_gbs": dec_gbs, "decode_frac": dec_gbs / peak,
-            "decode_back_to_back_us": dec_steady_us, "decode_back_to_back_gbs": dec_steady_gbs,
-            "decode_back_to_back_frac": dec_steady_gbs / peak, "decode_back_to_back_copies": n_dec,
+            **back_to_back,
             "sum_of_kernel_segments_us": float(seg_ms.sum(1).mean()) * 1e3,
             "step_gbs": step_bytes / (float(step_ms.mean()) * 1e-3) / 1e9},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
@@ -725,7 +728,7 @@ def bench_config(args, name, ws, rank, local):
     main_ms = float(seg_ms[:, main_i].mean())
     gbs = b[main_key] / (main_ms * 1e-3) / 1e9
     steady = {}
-    if w.mode == "decode":
+    if w.mode == "decode" and not args.no_back_to_back:
         n = copies_for(b["decode"], dev)
         us = steady_state_us(r.steady_fns(n))
         sg = b["decode"] / (us * 1e-6) / 1e9
@@ -755,15 +758,18 @@ def bench_norm_rope(args, name, ws, rank, ckv, dev):
     ms = float(seg_ms[:, 0].mean())
     b = r.algorithmic_bytes()
     gbs = b / (ms * 1e-3) / 1e9
-    n = copies_for(b, dev)
-    us = steady_state_us(r.steady_fns(n))
-    sg = b / (us * 1e-6) / 1e9
+    steady = {}
+    if not args.no_back_to_back:
+        n = copies_for(b, dev)
+        us = steady_state_us(r.steady_fns(n))
+        sg = b / (us * 1e-6) / 1e9
+        steady = {"back_to_back_us": us, "back_to_back_gbs": sg, "back_to_back_frac": sg / peak,
+                  "back_to_back_copies": n}
     line = {"workload": name, "ratio": x.ratio, "head_dim": x.head_dim, "rope_dim": x.rope_dim,
             "records": r.records, "rows_read": r.boundary, "cache_dtype": str(x.cache_dtype).replace("torch.", ""),
             "rows_per_s": r.records / (ms * 1e-3), "us": ms * 1e3, "us_min": float(seg_ms[:, 0].min()) * 1e3,
             "main_kernel": "norm_rope_store_kernel", "main_bytes": b, "main_gbs": gbs, "main_frac": gbs / peak,
-            "peak_gbs": peak, "peak_kind": kind, "back_to_back_us": us, "back_to_back_gbs": sg,
-            "back_to_back_frac": sg / peak, "back_to_back_copies": n}
+            "peak_gbs": peak, "peak_kind": kind, **steady}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -809,6 +815,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true", help="with --config: scaled-down workloads for profiling")
+    ap.add_argument("--no-back-to-back", action="store_true",
+                    help="skip the back-to-back timing of short kernels (keeps a profiler's launch list to the step)")
     ap.add_argument("--ref-fraction", type=float, default=0.125,
                     help="share of the prefill compress records the reference arm pools per step")
     args = ap.parse_args()
