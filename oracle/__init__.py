@@ -98,6 +98,10 @@ def _load(path: str | None = None):
             lib.orc_plan_decode_paged.argtypes = [i32, vp, vp, i64, u32, vp, u64, i32, i32, vp, u32, vp]
             lib.orc_norm_rope_store.argtypes = [i32, i32, i32, i32, i32, vp, i32, u64, vp, u32, vp, ctypes.c_float,
                                                 vp, u32, vp, u64, i32, vp, u64]
+            lib.orc_plan_online_prefill.argtypes = [vp, vp, vp, u32, u32, i64, u32, i32, vp, vp]
+            lib.orc_online_prefill.argtypes = [i32, i32, i32, vp, u64, vp, u32, vp, vp, u32, i32, u32, vp]
+            lib.orc_plan_online_decode.argtypes = [vp, vp, u32, i64, vp]
+            lib.orc_online_decode.argtypes = [i32, i32, i32, vp, u64, vp, vp, vp, u32, vp]
             lib.orc_double_to_bf16.argtypes = [ctypes.c_double]
             lib.orc_double_to_bf16.restype = ctypes.c_uint16
             _lib = lib
@@ -287,6 +291,61 @@ def compress_prefill(ratio, hd, in_dtype, out_dtype, state: np.ndarray, inp, ape
                                 num_q_tokens=int(_i64(extend_lens).sum()), out_layout=out_layout)
     compress_write(ratio, hd, in_dtype, state, inp, pw, nw)
     return out, pc, pw
+
+
+def plan_online_prefill(rid, seq_lens, extend_lens, slot_offset: int = 0, num_q_tokens: int | None = None,
+                        cap_u: int | None = None, pad_invalid: bool = False, check: bool = True):
+    """Online-state prefill units (16 B records); returns (units, (num_units, num_c), rc)."""
+    rid, sl, el = _i64(rid), _i64(seq_lens), _i64(extend_lens)
+    nq = int(el.sum()) if num_q_tokens is None else int(num_q_tokens)
+    lib = _load()
+    counts = np.zeros(2, dtype=np.uint32)
+    if cap_u is None:
+        lib.orc_plan_online_prefill(_p(rid), _p(sl), _p(el), len(rid), nq, slot_offset, 0, 0,
+                                    _p(np.zeros((1, 16), np.uint8)), _p(counts))
+        cap_u = int(counts[0])
+    units = np.zeros((max(cap_u, 1), 16), dtype=np.uint8)
+    rc = lib.orc_plan_online_prefill(_p(rid), _p(sl), _p(el), len(rid), nq, slot_offset, cap_u, int(pad_invalid),
+                                     _p(units), _p(counts))
+    if check and rc:
+        raise OracleError(rc, "plan_online_prefill")
+    return units[:cap_u], (int(counts[0]), int(counts[1])), rc
+
+
+def online_prefill(hd, in_dtype, out_dtype, state: np.ndarray, inp, ape, units, out_layout=OUT_TOKEN,
+                   out_rows: int | None = None) -> np.ndarray:
+    """Runs the units through the online state (float64 ``[slots, 3 hd]``, updated in place)."""
+    assert state.dtype == np.float64 and state.flags["C_CONTIGUOUS"]
+    inp, ape, units = np.ascontiguousarray(inp), np.ascontiguousarray(ape), np.ascontiguousarray(units)
+    nq = inp.size // (2 * hd)
+    rows = nq if out_layout == OUT_TOKEN else int(out_rows)
+    out = np.zeros((max(rows, 1), hd), dtype=elem_np(out_dtype))
+    rc = _load().orc_online_prefill(hd, in_dtype, out_dtype, _p(state), state.size // (3 * hd), _p(inp), nq, _p(ape),
+                                    _p(units), units.shape[0], out_layout, rows, _p(out))
+    if rc:
+        raise OracleError(rc, "online_prefill")
+    return out[:rows]
+
+
+def plan_online_decode(rid, seq_lens, slot_offset: int = 0) -> np.ndarray:
+    rid, sl = _i64(rid), _i64(seq_lens)
+    out = np.zeros((len(rid), 16), dtype=np.uint8)
+    rc = _load().orc_plan_online_decode(_p(rid), _p(sl), len(rid), slot_offset, _p(out))
+    if rc:
+        raise OracleError(rc, "plan_online_decode")
+    return out
+
+
+def online_decode(hd, in_dtype, out_dtype, state: np.ndarray, inp, ape, plan_d) -> np.ndarray:
+    assert state.dtype == np.float64 and state.flags["C_CONTIGUOUS"]
+    inp, ape, plan_d = np.ascontiguousarray(inp), np.ascontiguousarray(ape), np.ascontiguousarray(plan_d)
+    batch = plan_d.shape[0]
+    out = np.zeros((max(batch, 1), hd), dtype=elem_np(out_dtype))
+    rc = _load().orc_online_decode(hd, in_dtype, out_dtype, _p(state), state.size // (3 * hd), _p(inp), _p(ape),
+                                   _p(plan_d), batch, _p(out))
+    if rc:
+        raise OracleError(rc, "online_decode")
+    return out[:batch]
 
 
 def norm_rope_store(ratio: int, mode: int, hd: int, rope_dim: int, in_dtype: int, rows, in_layout: int, plan,

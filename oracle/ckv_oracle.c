@@ -541,7 +541,187 @@ int orc_compress_history(int ratio, int hd, int in_dtype, int out_dtype, const v
   return ORC_OK;
 }
 
-/* Exposed for the rounding pin (bf16 RNE from a double). */
+/* ----- online C128 state ([cv2] _use_online_compress, generate_online) ---- */
+
+/* The online state pool keeps, per request slot, the running softmax of the
+ * current 128-token group instead of the group's 128 rows ([cv2] views the
+ * state buffer as [-1, 1, 3 * head_dim] when online compression is on; the
+ * online kernels and generate_online themselves are off-page).  Reading: for
+ * channel c the slot holds (m, l, a) = (running max of s, sum of exp(s - m),
+ * sum of kv * exp(s - m)) over the group's tokens so far; a token at position
+ * p with s = fp32(score + ape[p % 128]):
+ *   p % 128 == 0:  (m, l, a) <- (s, 1, kv)                       (a new group)
+ *   otherwise:     m' = max(m, s);  l <- l e^(m-m') + e^(s-m');
+ *                  a <- a e^(m-m') + kv e^(s-m');  m <- m'
+ * and when (p + 1) % 128 == 0 the group's row a / l is emitted -- exactly the
+ * window softmax of the C128 definition.  The slot of request rid is
+ * rid + slot_offset ([cv2] online_state_slot_offset).  The oracle keeps the
+ * state in double, [slots, 3 * hd] as (m | l | a). */
+
+typedef struct {
+  uint32_t position;   /* first position of the unit */
+  uint32_t ragged_cnt; /* ragged id of its first token (24 bits) | token count << 24 (1..128) */
+  int32_t slot;
+  uint32_t row_flags;  /* compact output row (24 bits) | flags << 24 */
+} orc_online_unit;
+enum { ORC_UNIT_LOAD = 1, ORC_UNIT_EMIT = 2, ORC_UNIT_STORE = 4 };
+
+/* Prefill units: the tokens of one request inside one 128-group, in the CPU
+ * loop order (requests in batch order, positions ascending).  A unit loads the
+ * slot when it starts inside a group, emits when it reaches the group's end
+ * (its compact output row is the running count of emitting units), and
+ * stores the slot when it holds the request's last token. */
+int orc_plan_online_prefill(const int64_t* rid, const int64_t* seq_lens, const int64_t* extend_lens, uint32_t batch,
+                            uint32_t num_q_tokens, int64_t slot_offset, uint32_t cap_u, int pad_invalid,
+                            void* units_out, uint32_t* counts) {
+  if (batch > 1024 || num_q_tokens >= (1u << 24)) return ORC_BAD_BATCH;
+  orc_online_unit* u = (orc_online_unit*)units_out;
+  uint64_t token_base = 0, nu = 0, nc = 0;
+  for (uint32_t b = 0; b < batch; ++b) {
+    const int64_t sl = seq_lens[b], el = extend_lens[b];
+    if (!(0 < el && el <= sl) || sl > INT32_MAX || rid[b] < 0 || rid[b] + slot_offset < 0 ||
+        rid[b] + slot_offset > INT32_MAX)
+      return ORC_BAD_LENGTH;
+    const int64_t pl = sl - el;
+    for (int64_t g = pl / 128; g <= (sl - 1) / 128; ++g) {
+      const int64_t p0 = pl > 128 * g ? pl : 128 * g;
+      const int64_t p1 = sl < 128 * g + 128 ? sl : 128 * g + 128; /* exclusive */
+      const int emit = p1 == 128 * g + 128;
+      if (nu < cap_u) {
+        u[nu].position = (uint32_t)p0;
+        u[nu].ragged_cnt = (uint32_t)(token_base + (uint64_t)(p0 - pl)) | ((uint32_t)(p1 - p0) << 24);
+        u[nu].slot = (int32_t)(rid[b] + slot_offset);
+        const uint32_t flags = (p0 % 128 != 0 ? ORC_UNIT_LOAD : 0) | (emit ? ORC_UNIT_EMIT : 0) |
+                               (p1 == sl ? ORC_UNIT_STORE : 0);
+        u[nu].row_flags = (uint32_t)(emit ? nc : 0xFFFFFFu) | (flags << 24);
+      }
+      ++nu;
+      nc += emit;
+    }
+    token_base += (uint64_t)el;
+  }
+  counts[0] = (uint32_t)nu;
+  counts[1] = (uint32_t)nc;
+  if (token_base != num_q_tokens) return ORC_BAD_TOTAL;
+  if (nu > cap_u) return ORC_CAPACITY;
+  if (pad_invalid && cap_u > nu) memset(u + nu, 0xFF, sizeof(orc_online_unit) * (cap_u - nu));
+  return ORC_OK;
+}
+
+/* One token into channel c's running state (double). */
+static void online_step(double* m, double* l, double* a, int first, double s, double kv) {
+  if (first && ORC_MUTANT != 18) { /* mutant 18: no reset at a group start */
+    *m = s;
+    *l = 1.0;
+    *a = kv;
+    return;
+  }
+  const double mn = s > *m ? s : *m;
+  const double c = exp(*m - mn), e = exp(s - mn);
+  *l = ORC_MUTANT == 19 ? *l + e : *l * c + e; /* mutant 19: the sum not rescaled */
+  *a = *a * c + kv * e;
+  *m = mn;
+}
+
+static double online_s(const void* row, int hd, int c, int in_dtype, const void* ape, int64_t p) {
+  const float score = load_elem(row, (size_t)hd + c, in_dtype);
+  const float bias = load_elem(ape, (size_t)((p + (ORC_MUTANT == 20)) % 128) * hd + c, in_dtype); /* 20 */
+  return (double)(float)(score + bias); /* one fp32 rounding, as the window form */
+}
+
+/* Prefill through the online state: every unit's tokens in order.  Output
+ * rows: token layout [num_q_tokens, hd] (an emitted row at the ragged id of
+ * its group's last token, every other row +0.0) or compact [out_rows, hd]
+ * (row = the unit's output row). */
+int orc_online_prefill(int hd, int in_dtype, int out_dtype, double* state, uint64_t slots, const void* input,
+                       uint32_t num_q_tokens, const void* ape, const void* units, uint32_t n_units, int out_layout,
+                       uint32_t out_rows, void* out) {
+  int rc = check_common(128, hd, in_dtype, out_dtype);
+  if (rc) return rc;
+  const int width = 2 * hd;
+  const size_t orow_bytes = (size_t)hd * elem_size(out_dtype);
+  if (out_layout == ORC_OUT_TOKEN) memset(out, 0, (size_t)num_q_tokens * orow_bytes);
+  const orc_online_unit* u = (const orc_online_unit*)units;
+  for (uint32_t k = 0; k < n_units; ++k) {
+    if (u[k].position == 0xFFFFFFFFu) continue;
+    const uint32_t ragged0 = u[k].ragged_cnt & 0xFFFFFFu, cnt = u[k].ragged_cnt >> 24;
+    const uint32_t flags = u[k].row_flags >> 24, orow = u[k].row_flags & 0xFFFFFFu;
+    if (u[k].slot < 0 || (uint64_t)u[k].slot >= slots || cnt == 0 || ragged0 + cnt > num_q_tokens)
+      return ORC_BAD_INDEX;
+    if ((flags & ORC_UNIT_EMIT) && out_layout == ORC_OUT_COMPACT && orow >= out_rows) return ORC_BAD_INDEX;
+    double* st = state + (size_t)u[k].slot * 3 * hd;
+    for (int c = 0; c < hd; ++c) {
+      double m = 0, l = 0, a = 0;
+      if (flags & ORC_UNIT_LOAD) {
+        m = st[c];
+        l = st[hd + c];
+        a = st[2 * hd + c];
+      }
+      for (uint32_t t = 0; t < cnt; ++t) {
+        const int64_t p = (int64_t)u[k].position + t;
+        const void* row = row_ptr(input, (int64_t)ragged0 + t, width, in_dtype);
+        online_step(&m, &l, &a, p % 128 == 0, online_s(row, hd, c, in_dtype, ape, p),
+                    (double)load_elem(row, (size_t)c, in_dtype));
+      }
+      if (flags & ORC_UNIT_STORE) {
+        st[c] = m;
+        st[hd + c] = l;
+        st[2 * hd + c] = a;
+      }
+      if (flags & ORC_UNIT_EMIT) {
+        const size_t r = out_layout == ORC_OUT_TOKEN ? (size_t)(ragged0 + cnt - 1) : (size_t)orow;
+        store_elem(out, r * hd + c, out_dtype, a / l);
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+/* Decode plan for the online state: {seq_len, slot, slot, slot}. */
+int orc_plan_online_decode(const int64_t* rid, const int64_t* seq_lens, uint32_t batch, int64_t slot_offset,
+                           void* plan_d_out) {
+  orc_plan_d* plan = (orc_plan_d*)plan_d_out;
+  for (uint32_t b = 0; b < batch; ++b) {
+    if (seq_lens[b] < 1 || seq_lens[b] > INT32_MAX || rid[b] < 0 || rid[b] + slot_offset < 0 ||
+        rid[b] + slot_offset > INT32_MAX)
+      return ORC_BAD_LENGTH;
+    const int32_t slot = (int32_t)(rid[b] + slot_offset);
+    plan[b].seq_len = (uint32_t)seq_lens[b];
+    plan[b].write_loc = slot;
+    plan[b].read_page_0 = slot;
+    plan[b].read_page_1 = slot;
+  }
+  return ORC_OK;
+}
+
+/* Decode through the online state: row b's token joins slot write_loc; the
+ * output is the group's row on a boundary, +0.0 otherwise. */
+int orc_online_decode(int hd, int in_dtype, int out_dtype, double* state, uint64_t slots, const void* input,
+                      const void* ape, const void* plan_d, uint32_t batch, void* out) {
+  int rc = check_common(128, hd, in_dtype, out_dtype);
+  if (rc) return rc;
+  const int width = 2 * hd;
+  memset(out, 0, (size_t)batch * (size_t)hd * elem_size(out_dtype));
+  const orc_plan_d* pd = (const orc_plan_d*)plan_d;
+  for (uint32_t b = 0; b < batch; ++b) {
+    if (pd[b].seq_len == 0xFFFFFFFFu) continue;
+    if (pd[b].write_loc < 0 || (uint64_t)pd[b].write_loc >= slots || pd[b].seq_len == 0) return ORC_BAD_INDEX;
+    const int64_t p = (int64_t)pd[b].seq_len - 1;
+    double* st = state + (size_t)pd[b].write_loc * 3 * hd;
+    const void* row = row_ptr(input, b, width, in_dtype);
+    for (int c = 0; c < hd; ++c) {
+      double m = st[c], l = st[hd + c], a = st[2 * hd + c];
+      online_step(&m, &l, &a, p % 128 == 0, online_s(row, hd, c, in_dtype, ape, p),
+                  (double)load_elem(row, (size_t)c, in_dtype));
+      st[c] = m;
+      st[hd + c] = l;
+      st[2 * hd + c] = a;
+      if ((p + 1) % 128 == 0) store_elem(out, (size_t)b * hd + c, out_dtype, a / l);
+    }
+  }
+  return ORC_OK;
+}
+
 /* ----- norm + RoPE + store ([cv2] compress_norm_rope_store step) ---------- */
 
 /* After pooling, each compressed row goes through RMSNorm (weight, eps), then
@@ -624,4 +804,5 @@ int orc_norm_rope_store(int ratio, int mode, int hd, int rope_dim, int in_dtype,
   return rc;
 }
 
+/* Exposed for the rounding pin (bf16 RNE from a double). */
 uint16_t orc_double_to_bf16(double x) { return double_to_bf16_bits(x); }

@@ -5,10 +5,12 @@ by one, a ragged id without its request offset, a wrong read page, a dropped
 term, a sign error, an input row off by one; in the SWA-paged planner: no
 page-end writes, the ring offset taken modulo the page size, records without
 state reads translated; in norm + RoPE: a rotation sign, the position, the
-rotated channels) must fail at least one pin."""
+rotated channels; in the online state: no reset at a group start, the sum not
+rescaled, an ape row off by one) must fail at least one pin."""
 import pytest
 
 from tests import test_oracle_norm_rope as N
+from tests import test_oracle_online as L
 from tests import test_oracle_paged as Q
 from tests import test_oracle_pins as P
 
@@ -30,6 +32,9 @@ MUTANTS = {
     15: "RoPE rotation sign",
     16: "RoPE position seq_len instead of seq_len - ratio",
     17: "RoPE on the first rope_dim channels",
+    18: "online state not reset at a group start",
+    19: "online sum not rescaled on a new maximum",
+    20: "online ape row off by one",
 }
 
 
@@ -53,6 +58,9 @@ def pins(o):
     yield lambda: N.test_matches_float64_torch(o, 1)
     yield lambda: N.test_rotation_keeps_pair_lengths_and_relative_positions(o)
     yield lambda: N.test_position_is_seq_len_minus_ratio(o)
+    yield lambda: L.test_online_plan_worked_example(o)
+    yield lambda: L.test_online_closed_forms(o)
+    yield lambda: L.test_online_schedules_equal_window_definition(o, 0)
 
 
 @pytest.mark.parametrize("mutant", sorted(MUTANTS))
