@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libckv.so")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["plan.cu", "write.cu", "pool_c4.cu", "pool_c128.cu", "norm_rope.cu", "api.cu"]
+SOURCES = ["plan.cu", "write.cu", "pool_c4.cu", "pool_c128.cu", "norm_rope.cu", "online.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-I", INCLUDE]
 

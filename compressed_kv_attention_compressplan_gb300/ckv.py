@@ -78,6 +78,13 @@ def load_library():
                                              vp, vp, vp]
         lib.ckv_compress_decode.argtypes = [i32, i32, i32, i32, vp, u64, vp, vp, vp, u32, vp, vp, vp]
         f32 = ctypes.c_float
+        lib.ckv_capacity_online_units.argtypes = [u32, u32]
+        lib.ckv_capacity_online_units.restype = u32
+        lib.ckv_plan_online_prefill.argtypes = [vp, vp, vp, u32, u32, i64, u32, i32, vp, vp, vp, vp]
+        lib.ckv_plan_online_decode.argtypes = [vp, vp, u32, i64, vp, vp, vp]
+        lib.ckv_compress_online_prefill.argtypes = [i32, i32, i32, vp, u64, vp, u32, vp, vp, vp, u32, i32, u32, vp,
+                                                    vp, vp]
+        lib.ckv_compress_online_decode.argtypes = [i32, i32, i32, vp, u64, vp, vp, vp, u32, vp, vp, vp]
         lib.ckv_norm_rope_store_prefill.argtypes = [i32, i32, i32, i32, vp, i32, u64, vp, vp, u32, vp, f32, vp, u32,
                                                     vp, u64, i32, vp, u64, vp, vp]
         lib.ckv_norm_rope_store_decode.argtypes = [i32, i32, i32, i32, vp, vp, u32, vp, f32, vp, u32, vp, i32, vp,
@@ -288,6 +295,76 @@ def compress_decode(ratio: int, head_dim: int, state: torch.Tensor, kv_score: to
                                               _ptr(state), _state_rows(state, ratio, head_dim), _ptr(kv_score),
                                               _ptr(ape), _ptr(plan_d), batch, _ptr(out), _ptr(status),
                                               _stream(stream)), "ckv_compress_decode")
+    return out[:batch]
+
+
+# ------------------------------------------------------------------------------ online C128 state
+def capacity_online_units(batch: int, num_q_tokens: int) -> int:
+    return int(load_library().ckv_capacity_online_units(batch, num_q_tokens))
+
+
+def plan_online_prefill(rid: torch.Tensor, seq_lens: torch.Tensor, extend_lens: torch.Tensor, num_q_tokens: int,
+                        slot_offset: int = 0, capacity_u: Optional[int] = None, pad_invalid: bool = False,
+                        counts: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None, stream=None):
+    """Returns ``(units [cap_u, 16] u8, counts [4] int32)``; counts = {num_c, num_units, min el, max el}."""
+    batch = rid.numel()
+    if capacity_u is None:
+        capacity_u = capacity_online_units(batch, num_q_tokens)
+    units = torch.empty(max(capacity_u, 1), 16, dtype=torch.uint8, device=rid.device)
+    if counts is None:
+        counts = torch.empty(4, dtype=torch.int32, device=rid.device)
+    _check(load_library().ckv_plan_online_prefill(_ptr(rid), _ptr(seq_lens), _ptr(extend_lens), batch, num_q_tokens,
+                                                  slot_offset, capacity_u, int(pad_invalid), _ptr(units),
+                                                  _ptr(counts), _ptr(status), _stream(stream)),
+           "ckv_plan_online_prefill")
+    return units[:capacity_u], counts
+
+
+def plan_online_decode(rid: torch.Tensor, seq_lens: torch.Tensor, slot_offset: int = 0,
+                       status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    batch = rid.numel()
+    plan_d = torch.empty(max(batch, 1), 16, dtype=torch.uint8, device=rid.device)
+    _check(load_library().ckv_plan_online_decode(_ptr(rid), _ptr(seq_lens), batch, slot_offset, _ptr(plan_d),
+                                                 _ptr(status), _stream(stream)), "ckv_plan_online_decode")
+    return plan_d[:batch]
+
+
+def _online_state(state: torch.Tensor, head_dim: int) -> int:
+    if state.dtype != torch.float32 or state.numel() % (3 * head_dim):
+        raise ValueError("the online state is fp32 [slots, 3 * head_dim]")
+    return state.numel() // (3 * head_dim)
+
+
+def compress_online_prefill(head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
+                            units: torch.Tensor, counts: Optional[torch.Tensor], out_layout: int = OUT_TOKEN,
+                            out_dtype: torch.dtype = torch.float32, out_rows: Optional[int] = None,
+                            out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """Folds the units' tokens into the state; token layout out [num_q_tokens, hd], compact [out_rows, hd]."""
+    nq = kv_score.shape[0]
+    if out is None:
+        rows = nq if out_layout == OUT_TOKEN else int(out_rows)
+        out = torch.empty(max(rows, 1), head_dim, dtype=out_dtype, device=kv_score.device)
+    rows = out.shape[0] if out_layout == OUT_COMPACT else nq
+    _check(load_library().ckv_compress_online_prefill(head_dim, dtype_code(kv_score.dtype), dtype_code(out.dtype),
+                                                      _ptr(state), _online_state(state, head_dim), _ptr(kv_score),
+                                                      nq, _ptr(ape), _ptr(units), _ptr(counts), units.shape[0],
+                                                      out_layout, rows, _ptr(out), _ptr(status), _stream(stream)),
+           "ckv_compress_online_prefill")
+    return out
+
+
+def compress_online_decode(head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
+                           plan_d: torch.Tensor, out_dtype: torch.dtype = torch.float32,
+                           out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    batch = plan_d.shape[0]
+    if out is None:
+        out = torch.empty(max(batch, 1), head_dim, dtype=out_dtype, device=kv_score.device)
+    _check(load_library().ckv_compress_online_decode(head_dim, dtype_code(kv_score.dtype), dtype_code(out.dtype),
+                                                     _ptr(state), _online_state(state, head_dim), _ptr(kv_score),
+                                                     _ptr(ape), _ptr(plan_d), batch, _ptr(out), _ptr(status),
+                                                     _stream(stream)), "ckv_compress_online_decode")
     return out[:batch]
 
 

@@ -1,0 +1,376 @@
+// online.cu -- C128 compression through an online state: one slot of
+// (m | l | a) x head_dim fp32 per request instead of a 128-row page
+// (compressor_v2.py _use_online_compress; the online kernels themselves are
+// off-page, the recurrence is derived in include/ckv.h).
+//
+// Both kernels fold tokens with the same per-channel step (online_fold), in
+// position order, and keep the state in fp32 between calls, so a sequence
+// folded in one prefill, in chunks or token by token gives the same bits.
+// Work unit of the prefill: one planner unit (one request's tokens inside one
+// 128-group); head_dim / 4 threads own 4 channels each and walk the unit's
+// tokens in order, the loads of 8 tokens (4 for fp32 rows) issued before
+// their arithmetic.
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace ckv {
+namespace {
+
+constexpr int kOnThreads = 256;
+// tokens whose loads are in flight at once (fewer for fp32 rows, twice as wide)
+template <typename TIn>
+struct Depth {
+  static constexpr int value = sizeof(TIn) == 2 ? 8 : 4;
+};
+
+struct OnlineArgs {
+  int head_dim;
+  int in_dtype;
+  int out_dtype;
+  float* state;
+  uint64_t slots;
+  const void* input;
+  uint32_t num_q_tokens;  // prefill: input rows; decode: batch
+  const void* ape;
+  const ckv_online_unit_t* units;
+  const ckv_decode_plan_t* plan_d;
+  const uint32_t* d_counts;
+  uint32_t capacity;  // prefill: capacity_u; decode: batch
+  int out_layout;
+  uint32_t out_rows;
+  void* out;
+  uint32_t* d_status;
+};
+
+// Running softmax of one channel over the tokens of a group so far.
+struct OnlineState {
+  float m, l, a, nml;  // nml = -m * log2(e), kept with m
+
+  __device__ __forceinline__ void start(float s, float kv) {
+    m = s;
+    l = 1.0f;
+    a = kv;
+    nml = neg_max_log2e(s);
+  }
+  // A token that raises the maximum rescales the sums by exp(m_old - s) and
+  // enters with weight 1; any other enters with weight exp(s - m).
+  __device__ __forceinline__ void fold(float s, float kv) {
+    if (s > m) {
+      const float nml_s = neg_max_log2e(s);
+      const float c = weight_of(m, nml_s);
+      l = __fmaf_rn(l, c, 1.0f);
+      a = __fmaf_rn(a, c, kv);
+      m = s;
+      nml = nml_s;
+    } else {
+      const float e = weight_of(s, nml);
+      l = __fadd_rn(l, e);
+      a = __fmaf_rn(kv, e, a);
+    }
+  }
+};
+
+__device__ __forceinline__ void online_token(OnlineState& st, bool first, float s, float kv) {
+  if (first) st.start(s, kv);
+  else st.fold(s, kv);
+}
+
+// The raw 4-channel chunk of one row: 8 bytes of bf16 or 16 of fp32, kept
+// unconverted while the loads of several tokens are in flight.
+template <typename T>
+struct Raw4;
+template <>
+struct Raw4<float> {
+  float4 v;
+  __device__ __forceinline__ void load(const float* p) { v = __ldg(reinterpret_cast<const float4*>(p)); }
+  __device__ __forceinline__ float get(int j) const { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; }
+};
+template <>
+struct Raw4<__nv_bfloat16> {
+  uint2 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = __ldg(reinterpret_cast<const uint2*>(p)); }
+  __device__ __forceinline__ float get(int j) const {
+    return j == 0 ? bf16lo(v.x) : j == 1 ? bf16hi(v.x) : j == 2 ? bf16lo(v.y) : bf16hi(v.y);
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ void load_quad(const T* p, float (&v)[4]);
+
+template <>
+__device__ __forceinline__ void load_quad<float>(const float* p, float (&v)[4]) {
+  const float4 f = __ldg(reinterpret_cast<const float4*>(p));
+  v[0] = f.x;
+  v[1] = f.y;
+  v[2] = f.z;
+  v[3] = f.w;
+}
+
+template <>
+__device__ __forceinline__ void load_quad<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  v[0] = bf16lo(u.x);
+  v[1] = bf16hi(u.x);
+  v[2] = bf16lo(u.y);
+  v[3] = bf16hi(u.y);
+}
+
+__device__ __forceinline__ void load_state(const float* st, int hd, int c0, OnlineState (&q)[4]) {
+  const float4 m = *reinterpret_cast<const float4*>(st + c0);
+  const float4 l = *reinterpret_cast<const float4*>(st + hd + c0);
+  const float4 a = *reinterpret_cast<const float4*>(st + 2 * hd + c0);
+  q[0] = {m.x, l.x, a.x, neg_max_log2e(m.x)};
+  q[1] = {m.y, l.y, a.y, neg_max_log2e(m.y)};
+  q[2] = {m.z, l.z, a.z, neg_max_log2e(m.z)};
+  q[3] = {m.w, l.w, a.w, neg_max_log2e(m.w)};
+}
+
+__device__ __forceinline__ void store_state(float* st, int hd, int c0, const OnlineState (&q)[4]) {
+  *reinterpret_cast<float4*>(st + c0) = make_float4(q[0].m, q[1].m, q[2].m, q[3].m);
+  *reinterpret_cast<float4*>(st + hd + c0) = make_float4(q[0].l, q[1].l, q[2].l, q[3].l);
+  *reinterpret_cast<float4*>(st + 2 * hd + c0) = make_float4(q[0].a, q[1].a, q[2].a, q[3].a);
+}
+
+template <typename TOut>
+__device__ __forceinline__ void store_quad(TOut* p, const float (&r)[4]) {
+  store_row_chunk<TOut, 4>(p, r);
+}
+
+template <typename TIn, typename TOut>
+__global__ __launch_bounds__(kOnThreads, 2) void online_prefill_kernel(const OnlineArgs a) {
+  pdl_wait();  // units, state and input may come from the previous kernels
+  pdl_release();
+  const int hd = a.head_dim;
+  const int tpu = hd / 4;                  // threads per unit
+  const int upb = kOnThreads / tpu;        // units per block round
+  const int lu = threadIdx.x / tpu;
+  const int c0 = 4 * (threadIdx.x % tpu);
+  const uint32_t n = count_or_capacity(a.d_counts, 1, a.capacity);
+  const TIn* input = static_cast<const TIn*>(a.input);
+  const TIn* ape = static_cast<const TIn*>(a.ape);
+  TOut* out = static_cast<TOut*>(a.out);
+  const size_t width = 2 * static_cast<size_t>(hd);
+  for (uint32_t base = blockIdx.x * upb; base < n; base += gridDim.x * upb) {
+    const uint32_t k = base + lu;
+    if (k >= n) continue;
+    const uint4 rec = __ldg(reinterpret_cast<const uint4*>(a.units + k));
+    if (rec.x == kInvalidU32) continue;
+    const uint32_t pos0 = rec.x;
+    const uint32_t ragged0 = rec.y & CKV_RAGGED_MASK;
+    const uint32_t cnt = rec.y >> CKV_UNIT_COUNT_SHIFT;
+    const int32_t slot = static_cast<int32_t>(rec.z);
+    const uint32_t orow = rec.w & CKV_RAGGED_MASK;
+    const uint32_t flags = rec.w >> CKV_UNIT_FLAGS_SHIFT;
+    const bool emit = flags & CKV_UNIT_EMIT;
+    const bool token = a.out_layout == CKV_OUT_TOKEN;
+    bool ok = slot >= 0 && static_cast<uint64_t>(slot) < a.slots && cnt >= 1 && cnt <= 128 &&
+              ragged0 + cnt <= a.num_q_tokens && (pos0 % 128) + cnt <= 128;
+    if (emit && !token) ok = ok && orow < a.out_rows;
+    if (!ok) {
+      if (c0 == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+      continue;
+    }
+    float* st = a.state + static_cast<size_t>(slot) * 3 * hd;
+    OnlineState q[4];
+    if (flags & CKV_UNIT_LOAD) load_state(st, hd, c0, q);
+    constexpr int kOnDepth = Depth<TIn>::value;
+    for (uint32_t t0 = 0; t0 < cnt; t0 += kOnDepth) {
+      Raw4<TIn> kv[kOnDepth], sc[kOnDepth], bias[kOnDepth];
+#pragma unroll
+      for (int d = 0; d < kOnDepth; ++d) {
+        if (t0 + d < cnt) {
+          const TIn* row = input + (static_cast<size_t>(ragged0) + t0 + d) * width;
+          kv[d].load(row + c0);
+          sc[d].load(row + hd + c0);
+          bias[d].load(ape + static_cast<size_t>((pos0 + t0 + d) % 128) * hd + c0);
+        }
+      }
+#pragma unroll
+      for (int d = 0; d < kOnDepth; ++d) {
+        if (t0 + d < cnt) {
+          const bool first = (pos0 + t0 + d) % 128 == 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            online_token(q[j], first, score_plus_bias(sc[d].get(j), bias[d].get(j)), kv[d].get(j));
+          if (token && !(emit && t0 + d + 1 == cnt))
+            store_zero_chunk<TOut, 4>(out + (static_cast<size_t>(ragged0) + t0 + d) * hd + c0);
+        }
+      }
+    }
+    if (flags & CKV_UNIT_STORE) store_state(st, hd, c0, q);
+    if (emit) {
+      const float r[4] = {finish(q[0].a, q[0].l), finish(q[1].a, q[1].l), finish(q[2].a, q[2].l),
+                          finish(q[3].a, q[3].l)};
+      const size_t row = token ? static_cast<size_t>(ragged0) + cnt - 1 : orow;
+      store_quad<TOut>(out + row * hd + c0, r);
+    }
+  }
+}
+
+template <typename TIn, typename TOut>
+__global__ __launch_bounds__(kOnThreads) void online_decode_kernel(const OnlineArgs a) {
+  pdl_wait();
+  pdl_release();
+  const int hd = a.head_dim;
+  const int tpu = hd / 4;
+  const uint32_t t = blockIdx.x * kOnThreads + threadIdx.x;
+  const uint32_t b = t / tpu;
+  const int c0 = 4 * static_cast<int>(t % tpu);
+  if (b >= a.capacity) return;
+  const TIn* input = static_cast<const TIn*>(a.input);
+  const TIn* ape = static_cast<const TIn*>(a.ape);
+  TOut* out = static_cast<TOut*>(a.out) + static_cast<size_t>(b) * hd + c0;
+  const ckv_decode_plan_t P = load_plan_d(a.plan_d + b);
+  const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (P.seq_len == kInvalidU32) {
+    store_quad<TOut>(out, zero);
+    return;
+  }
+  if (P.seq_len == 0 || P.write_loc < 0 || static_cast<uint64_t>(P.write_loc) >= a.slots) {
+    if (c0 == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+    store_quad<TOut>(out, zero);
+    return;
+  }
+  const uint32_t p = P.seq_len - 1;
+  const TIn* row = input + static_cast<size_t>(b) * 2 * hd;
+  float kv[4], sc[4], bias[4];
+  load_quad<TIn>(row + c0, kv);
+  load_quad<TIn>(row + hd + c0, sc);
+  load_quad<TIn>(ape + static_cast<size_t>(p % 128) * hd + c0, bias);
+  float* st = a.state + static_cast<size_t>(P.write_loc) * 3 * hd;
+  OnlineState q[4];
+  const bool first = p % 128 == 0;
+  if (!first) load_state(st, hd, c0, q);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) online_token(q[j], first, score_plus_bias(sc[j], bias[j]), kv[j]);
+  store_state(st, hd, c0, q);
+  if ((p + 1) % 128 == 0) {
+    const float r[4] = {finish(q[0].a, q[0].l), finish(q[1].a, q[1].l), finish(q[2].a, q[2].l),
+                        finish(q[3].a, q[3].l)};
+    store_quad<TOut>(out, r);
+  } else {
+    store_quad<TOut>(out, zero);
+  }
+}
+
+__global__ void plan_online_decode_kernel(const int64_t* rid, const int64_t* seq_lens, uint32_t batch,
+                                          int64_t slot_offset, ckv_decode_plan_t* plan_d, uint32_t* d_status) {
+  pdl_wait();
+  pdl_release();
+  const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  const int64_t sl = seq_lens[b], r = rid[b];
+  uint4 rec = make_uint4(kInvalidU32, kInvalidU32, kInvalidU32, kInvalidU32);
+  const int64_t slot = r + slot_offset;
+  if (sl >= 1 && sl <= INT32_MAX && r >= 0 && slot >= 0 && slot <= INT32_MAX) {
+    const uint32_t s32 = static_cast<uint32_t>(slot);
+    rec = make_uint4(static_cast<uint32_t>(sl), s32, s32, s32);
+  } else {
+    status_or(d_status, CKV_STATUS_BAD_LENGTH);
+  }
+  *reinterpret_cast<uint4*>(plan_d + b) = rec;
+}
+
+int check_online(const OnlineArgs& a) {
+  if (a.head_dim <= 0 || a.head_dim % 128 != 0 || a.head_dim > 1024) return CKV_ERR_HEAD_DIM;
+  if ((a.in_dtype != CKV_F32 && a.in_dtype != CKV_BF16) || (a.out_dtype != CKV_F32 && a.out_dtype != CKV_BF16) ||
+      (a.out_layout != CKV_OUT_TOKEN && a.out_layout != CKV_OUT_COMPACT))
+    return CKV_ERR_DTYPE;
+  if (a.capacity == 0) return CKV_OK;
+  if (!aligned16(a.state) || !aligned16(a.input) || !aligned16(a.ape) || !aligned16(a.out)) return CKV_ERR_POINTER;
+  return CKV_OK;
+}
+
+template <template <typename, typename> class K>
+int launch_typed(const OnlineArgs& a, dim3 grid, cudaStream_t s) {
+  const dim3 block(kOnThreads);
+  if (a.in_dtype == CKV_BF16) {
+    if (a.out_dtype == CKV_BF16) return launch_pdl(K<__nv_bfloat16, __nv_bfloat16>::fn, grid, block, 0, s, a);
+    return launch_pdl(K<__nv_bfloat16, float>::fn, grid, block, 0, s, a);
+  }
+  if (a.out_dtype == CKV_BF16) return launch_pdl(K<float, __nv_bfloat16>::fn, grid, block, 0, s, a);
+  return launch_pdl(K<float, float>::fn, grid, block, 0, s, a);
+}
+
+template <typename TIn, typename TOut>
+struct PrefillK {
+  static constexpr auto fn = online_prefill_kernel<TIn, TOut>;
+};
+template <typename TIn, typename TOut>
+struct DecodeK {
+  static constexpr auto fn = online_decode_kernel<TIn, TOut>;
+};
+
+}  // namespace
+}  // namespace ckv
+
+using namespace ckv;
+
+extern "C" int ckv_compress_online_prefill(int head_dim, int in_dtype, int out_dtype, float* state, uint64_t slots,
+                                           const void* kv_score_input, uint32_t num_q_tokens, const void* ape,
+                                           const ckv_online_unit_t* units, const uint32_t* d_counts,
+                                           uint32_t capacity_u, int out_layout, uint32_t out_rows, void* out,
+                                           uint32_t* d_status, ckv_stream_t stream) {
+  OnlineArgs a{};
+  a.head_dim = head_dim;
+  a.in_dtype = in_dtype;
+  a.out_dtype = out_dtype;
+  a.state = state;
+  a.slots = slots;
+  a.input = kv_score_input;
+  a.num_q_tokens = num_q_tokens;
+  a.ape = ape;
+  a.units = units;
+  a.d_counts = d_counts;
+  a.capacity = capacity_u;
+  a.out_layout = out_layout;
+  a.out_rows = out_rows;
+  a.out = out;
+  a.d_status = d_status;
+  const int rc = check_online(a);
+  if (rc || capacity_u == 0) return rc;
+  if (!aligned16(units) || (d_counts && (reinterpret_cast<uintptr_t>(d_counts) & 3u))) return CKV_ERR_POINTER;
+  const uint32_t upb = kOnThreads / (head_dim / 4);
+  uint32_t grid = (capacity_u + upb - 1) / upb;
+  grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 8u * static_cast<uint32_t>(sm_count())));
+  return launch_typed<PrefillK>(a, dim3(grid), reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ckv_compress_online_decode(int head_dim, int in_dtype, int out_dtype, float* state, uint64_t slots,
+                                          const void* kv_score_input, const void* ape,
+                                          const ckv_decode_plan_t* plan_d, uint32_t batch, void* out,
+                                          uint32_t* d_status, ckv_stream_t stream) {
+  OnlineArgs a{};
+  a.head_dim = head_dim;
+  a.in_dtype = in_dtype;
+  a.out_dtype = out_dtype;
+  a.state = state;
+  a.slots = slots;
+  a.input = kv_score_input;
+  a.num_q_tokens = batch;
+  a.ape = ape;
+  a.plan_d = plan_d;
+  a.capacity = batch;
+  a.out_layout = CKV_OUT_COMPACT;
+  a.out = out;
+  a.d_status = d_status;
+  const int rc = check_online(a);
+  if (rc || batch == 0) return rc;
+  if (!aligned16(plan_d)) return CKV_ERR_POINTER;
+  const uint64_t threads = static_cast<uint64_t>(batch) * (head_dim / 4);
+  const dim3 grid(static_cast<uint32_t>((threads + kOnThreads - 1) / kOnThreads));
+  return launch_typed<DecodeK>(a, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ckv_plan_online_decode(const int64_t* rid, const int64_t* seq_lens, uint32_t batch,
+                                      int64_t slot_offset, ckv_decode_plan_t* plan_d, uint32_t* d_status,
+                                      ckv_stream_t stream) {
+  if (batch == 0) return CKV_OK;
+  if (!rid || !seq_lens || !aligned16(plan_d)) return CKV_ERR_POINTER;
+  if ((reinterpret_cast<uintptr_t>(rid) | reinterpret_cast<uintptr_t>(seq_lens)) & 7u) return CKV_ERR_POINTER;
+  const uint32_t threads = 256;
+  return launch_pdl(plan_online_decode_kernel, dim3((batch + threads - 1) / threads), dim3(threads), 0,
+                    reinterpret_cast<cudaStream_t>(stream), rid, seq_lens, batch, slot_offset, plan_d, d_status);
+}

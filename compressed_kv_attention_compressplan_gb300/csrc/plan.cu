@@ -183,6 +183,11 @@ struct PrefillPlanArgs {
   uint64_t num_full;
   int32_t sps;
   int32_t ring;
+  // Online C128 state (online != 0): the second list holds one unit record per
+  // (request, 128-group touched by the extend) instead of write records.
+  int online;
+  int64_t slot_offset;
+  ckv_online_unit_t* units;
 };
 
 // Every CTA loads the <= 1024 request lengths, derives per request
@@ -223,8 +228,9 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
     const int64_t sl = a.seq_lens[tid];
     const int64_t el = a.extend_lens[tid];
     const int64_t r = a.rid[tid];
-    const bool ok = el > 0 && el <= sl && sl <= INT32_MAX && r >= 0 && r * slots + slots - 1 <= INT32_MAX &&
-                    el <= CKV_MAX_TOKENS;
+    const bool ok = el > 0 && el <= sl && sl <= INT32_MAX && r >= 0 && el <= CKV_MAX_TOKENS &&
+                    (a.online ? r + a.slot_offset >= 0 && r + a.slot_offset <= INT32_MAX
+                              : r * slots + slots - 1 <= INT32_MAX);
     el_eff = (el > 0 && el <= CKV_MAX_TOKENS) ? static_cast<uint32_t>(el) : 0u;
     el_min = el_max = el_eff;
     bool ok_paged = true;
@@ -247,8 +253,12 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
       }
       nc = static_cast<uint32_t>(s32 / R - pl / R);
       nw = static_cast<uint32_t>(s32 - wstart) + nextra;
+      if (a.online) {  // units: the 128-groups pl/128 .. (sl-1)/128; wstart keeps sl
+        nw = static_cast<uint32_t>((s32 - 1) / 128 - pl / 128 + 1);
+        s_wstart[tid] = s32;
+      }
       s_pl[tid] = pl;
-      s_wstart[tid] = wstart;
+      if (!a.online) s_wstart[tid] = wstart;
       s_rid[tid] = static_cast<int32_t>(r);
       s_pe0[tid] = pe0;
       s_nextra[tid] = nextra;
@@ -315,7 +325,7 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
   if (blockIdx.x == 0 && tid == 0) {
     uint32_t flags = s_flags;
     if (total_e != a.num_q_tokens) flags |= CKV_STATUS_BAD_TOTAL;
-    if (num_c > a.cap_c || num_w > a.cap_w) flags |= CKV_STATUS_CAPACITY;
+    if ((!a.online && num_c > a.cap_c) || num_w > a.cap_w) flags |= CKV_STATUS_CAPACITY;
     if (flags) status_or(a.d_status, flags);
     a.d_counts[0] = num_c;
     a.d_counts[1] = num_w;
@@ -369,7 +379,31 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
       }
       if (store) *reinterpret_cast<uint4*>(a.plan_c + k) = rec;
     }
-    if (k < a.cap_w) {
+    if (a.online && k < a.cap_w) {
+      uint4 rec = make_uint4(kInvalidU32, kInvalidU32, kInvalidU32, kInvalidU32);
+      bool store = a.pad_invalid != 0;
+      if (k < emit_w) {
+        uint32_t lo = 0, hi = B;
+        while (hi - lo > 1) {
+          const uint32_t mid = (lo + hi) >> 1;
+          if (s_off_w[mid] <= k) lo = mid; else hi = mid;
+        }
+        const uint32_t kk = k - s_off_w[lo];
+        const int32_t pl = s_pl[lo], sl = s_wstart[lo];
+        const int32_t g = pl / 128 + static_cast<int32_t>(kk);
+        const int32_t p0 = max(pl, 128 * g), p1 = min(sl, 128 * g + 128);
+        const bool emit = p1 == 128 * g + 128;
+        const uint32_t flags = (p0 % 128 != 0 ? CKV_UNIT_LOAD : 0u) | (emit ? CKV_UNIT_EMIT : 0u) |
+                               (p1 == sl ? CKV_UNIT_STORE : 0u);
+        rec = make_uint4(static_cast<uint32_t>(p0),
+                         (s_off_e[lo] + static_cast<uint32_t>(p0 - pl)) |
+                             (static_cast<uint32_t>(p1 - p0) << CKV_UNIT_COUNT_SHIFT),
+                         static_cast<uint32_t>(s_rid[lo] + a.slot_offset),
+                         (emit ? s_off_c[lo] + kk : CKV_RAGGED_MASK) | (flags << CKV_UNIT_FLAGS_SHIFT));
+        store = true;
+      }
+      if (store) *reinterpret_cast<uint4*>(a.units + k) = rec;
+    } else if (k < a.cap_w) {
       uint2 rec = make_uint2(kInvalidU32, kInvalidU32);
       bool store = a.pad_invalid != 0;
       if (k < emit_w) {
@@ -457,7 +491,11 @@ int launch_plan_prefill(PrefillPlanArgs a, cudaStream_t stream) {
        reinterpret_cast<uintptr_t>(a.extend_lens)) & 7u)
     return CKV_ERR_POINTER;
   if (a.cap_c > 0 && !aligned16(a.plan_c)) return CKV_ERR_POINTER;
-  if (a.cap_w > 0 && (a.plan_w == nullptr || (reinterpret_cast<uintptr_t>(a.plan_w) & 7u))) return CKV_ERR_POINTER;
+  if (a.online) {
+    if (a.cap_w > 0 && !aligned16(a.units)) return CKV_ERR_POINTER;
+  } else if (a.cap_w > 0 && (a.plan_w == nullptr || (reinterpret_cast<uintptr_t>(a.plan_w) & 7u))) {
+    return CKV_ERR_POINTER;
+  }
   const uint32_t work = std::max(a.cap_c, a.cap_w);
   uint32_t grid = (work + kPlanThreads - 1) / kPlanThreads;
   grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 2u * static_cast<uint32_t>(sm_count())));
@@ -501,6 +539,35 @@ int ckv_plan_prefill(int ratio, const int64_t* rid, const int64_t* seq_lens, con
   a.sps = 1;
   a.ring = 1;
   return launch_plan_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ckv_plan_online_prefill(const int64_t* rid, const int64_t* seq_lens, const int64_t* extend_lens,
+                            uint32_t batch, uint32_t num_q_tokens, int64_t slot_offset, uint32_t capacity_u,
+                            int pad_invalid, ckv_online_unit_t* units, uint32_t* d_counts, uint32_t* d_status,
+                            ckv_stream_t stream) {
+  PrefillPlanArgs a{};
+  a.ratio = 128;
+  a.rid = rid;
+  a.seq_lens = seq_lens;
+  a.extend_lens = extend_lens;
+  a.batch = batch;
+  a.num_q_tokens = num_q_tokens;
+  a.cap_c = 0;
+  a.cap_w = capacity_u;
+  a.pad_invalid = pad_invalid;
+  a.d_counts = d_counts;
+  a.d_status = d_status;
+  a.sps = 1;
+  a.ring = 1;
+  a.online = 1;
+  a.slot_offset = slot_offset;
+  a.units = units;
+  return launch_plan_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+uint32_t ckv_capacity_online_units(uint32_t batch, uint32_t num_q_tokens) {
+  const uint64_t u = static_cast<uint64_t>(num_q_tokens) / 128 + 2ull * batch;
+  return static_cast<uint32_t>(std::min<uint64_t>(u, num_q_tokens));
 }
 
 int ckv_plan_prefill_paged(int ratio, const int64_t* rid, const int32_t* req_to_token, int64_t r2t_stride,

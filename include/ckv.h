@@ -119,6 +119,24 @@ typedef struct ckv_decode_plan {
 #define CKV_RAGGED_MASK 0x00FFFFFFu
 #define CKV_BUFFER_LEN_SHIFT 24
 
+/* One online-state prefill unit (16 bytes): the tokens of one request that
+ * fall inside one 128-group (see "Online C128 state" below).  Invalid = all
+ * bytes 0xFF. */
+typedef struct ckv_online_unit {
+  uint32_t position;   /* position of the unit's first token */
+  uint32_t ragged_cnt; /* ragged id of that token (24 bits) | token count (1..128) << 24 */
+  int32_t slot;        /* the request's state slot */
+  uint32_t row_flags;  /* compact output row (24 bits, all ones when nothing is emitted) | flags << 24 */
+} ckv_online_unit_t;
+
+#define CKV_UNIT_COUNT_SHIFT 24
+#define CKV_UNIT_FLAGS_SHIFT 24
+enum {
+  CKV_UNIT_LOAD = 1u,  /* the unit starts inside a group: continue from the slot */
+  CKV_UNIT_EMIT = 2u,  /* the unit ends its group: emit the group's row */
+  CKV_UNIT_STORE = 4u  /* the unit holds the request's last token: store the slot */
+};
+
 /* Upper bounds a caller can size plan buffers with (host arithmetic only):
  * compress records <= num_q_tokens / ratio + batch, and
  * write records <= min(num_q_tokens, batch * (ratio == 4 ? 7 : 127)). */
@@ -239,6 +257,59 @@ int ckv_compress_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, v
 int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, void* state, uint64_t state_rows,
                         const void* kv_score_input, const void* ape, const ckv_decode_plan_t* plan_d,
                         uint32_t batch, void* out, uint32_t* d_status, ckv_stream_t stream);
+
+/* ------------------------------------------------------- online C128 state */
+/* compressor_v2.py can keep C128 state online: one slot of 3 * head_dim per
+ * request ([slots, 1, 3 * head_dim]) instead of a 128-row page; the online
+ * kernels and their plans (generate_online) are off-page, so this is a
+ * derivation.  Slot layout, fp32: m | l | a, each head_dim wide: per channel,
+ * over the tokens of the current 128-group so far, the running maximum m of
+ * s = fp32(score + ape[p % 128]), l = sum exp(s - m) and a = sum kv exp(s - m).
+ * A token at position p starts a new group when p % 128 == 0 ((m, l, a) =
+ * (s, 1, kv)) and otherwise folds in, rescaling by exp(m_old - m_new) when it
+ * raises the maximum; at (p + 1) % 128 == 0 the group's row a / l is emitted,
+ * which is the C128 window softmax.  The slot of request rid is
+ * rid + slot_offset (compressor_v2.py online_state_slot_offset).
+ *
+ * Prefill: ckv_plan_online_prefill emits one unit per (request, group that
+ * the request's extend touches), in batch order and position order, into
+ * units[capacity_u] (<= ckv_capacity_online_units); d_counts receives
+ * {num_c (units that emit), num_units, min extend_len, max extend_len}; the
+ * length checks, status bits and pad_invalid are those of ckv_plan_prefill.
+ * An emitting unit's compact output row is its rank among emitting units,
+ * i.e. the compress record order of the legacy planner. */
+uint32_t ckv_capacity_online_units(uint32_t batch, uint32_t num_q_tokens);
+
+int ckv_plan_online_prefill(const int64_t* rid, const int64_t* seq_lens, const int64_t* extend_lens,
+                            uint32_t batch, uint32_t num_q_tokens, int64_t slot_offset, uint32_t capacity_u,
+                            int pad_invalid, ckv_online_unit_t* units, uint32_t* d_counts, uint32_t* d_status,
+                            ckv_stream_t stream);
+
+/* Runs the first min(d_counts[1], capacity_u) units (all when d_counts is NULL)
+ * through the state (fp32 [slots, 3 * head_dim], read and written).  Outputs:
+ * CKV_OUT_TOKEN: out [num_q_tokens, head_dim], an emitted row at the ragged id
+ * of its group's last token and +0.0 in every other row the units cover;
+ * CKV_OUT_COMPACT: out [out_rows, head_dim], row = the unit's output row.
+ * Units naming a slot >= slots, rows past num_q_tokens or an output row >=
+ * out_rows are skipped with CKV_STATUS_BAD_INDEX.  Two units of one call must
+ * not name the same slot unless they are consecutive groups of one request
+ * (the planner's output satisfies this). */
+int ckv_compress_online_prefill(int head_dim, int in_dtype, int out_dtype, float* state, uint64_t slots,
+                                const void* kv_score_input, uint32_t num_q_tokens, const void* ape,
+                                const ckv_online_unit_t* units, const uint32_t* d_counts, uint32_t capacity_u,
+                                int out_layout, uint32_t out_rows, void* out, uint32_t* d_status,
+                                ckv_stream_t stream);
+
+/* Decode: plan record b = {seq_len, slot, slot, slot} (slot = rid + slot_offset);
+ * the compute folds row b of kv_score_input [batch, 2 * head_dim] into its
+ * slot and writes out row b: the group's row when seq_len % 128 == 0, +0.0
+ * otherwise.  Two rows of one batch must not name the same slot. */
+int ckv_plan_online_decode(const int64_t* rid, const int64_t* seq_lens, uint32_t batch, int64_t slot_offset,
+                           ckv_decode_plan_t* plan_d, uint32_t* d_status, ckv_stream_t stream);
+
+int ckv_compress_online_decode(int head_dim, int in_dtype, int out_dtype, float* state, uint64_t slots,
+                               const void* kv_score_input, const void* ape, const ckv_decode_plan_t* plan_d,
+                               uint32_t batch, void* out, uint32_t* d_status, ckv_stream_t stream);
 
 /* ------------------------------------------------------- norm, RoPE, store */
 /* The step after pooling (compressor_v2.py compress_norm_rope_store and the

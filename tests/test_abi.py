@@ -34,7 +34,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_record_sizes_match_header():
     text = open(HEADER).read()
-    for struct, size in [("ckv_compress_plan", 16), ("ckv_write_plan", 8), ("ckv_decode_plan", 16)]:
+    for struct, size in [("ckv_compress_plan", 16), ("ckv_write_plan", 8), ("ckv_decode_plan", 16),
+                         ("ckv_online_unit", 16)]:
         body = re.search(r"typedef struct %s \{(.*?)\}" % struct, text, flags=re.S).group(1)
         fields = re.findall(r"(u?int32_t)\s+\w+;", body)
         assert 4 * len(fields) == size, struct
@@ -48,6 +49,8 @@ def test_capacity_bounds(lib):
     assert ckv.capacity_compress(5, 1, 1) == 0
     assert ckv.capacity_write_paged(4, 2, 100, 16) == 2 * 7 + 4 * (100 // 16 + 2)
     assert ckv.capacity_write_paged(128, 1024, 5000, 256) == ckv.capacity_write(128, 1024, 5000)
+    assert ckv.capacity_online_units(3, 1000) == 1000 // 128 + 6
+    assert ckv.capacity_online_units(100, 40) == 40
 
 
 def test_argument_errors_are_returned_before_any_launch(lib):
@@ -72,4 +75,10 @@ def test_argument_errors_are_returned_before_any_launch(lib):
     assert lib.ckv_plan_decode_paged(128, None, None, 0, 0, None, 0, 256, 256, None, 1, None, None, None) == -3
     assert lib.ckv_plan_prefill_paged(4, None, None, 8, 1, None, 8, 16, 4, None, None, 1, 4, 4, 4, 0, None, None,
                                       None, None, None) == -3  # a 4-row ring
+    assert lib.ckv_compress_online_decode(100, 1, 0, None, 0, None, None, None, 1, None, None, None) == -2
+    assert lib.ckv_compress_online_prefill(512, 1, 0, None, 1, None, 8, None, None, None, 4, 9, 0, None, None,
+                                           None) == -5
+    assert lib.ckv_compress_online_prefill(512, 1, 0, None, 1, None, 8, None, None, None, 4, 0, 0, None, None,
+                                           None) == -4
+    assert lib.ckv_plan_online_prefill(None, None, None, 2000, 0, 0, 0, 0, None, vp(16), None, None) == -3
     assert lib.ckv_error_string(-4) != lib.ckv_error_string(0)

@@ -1,0 +1,179 @@
+"""GPU parity of the online C128 state (ckv_plan_online_prefill / _decode,
+ckv_compress_online_prefill / _decode) against the oracle.
+
+Bar: unit and decode plans bit-exact; the running maxima of the state
+bit-exact (a maximum of identically rounded scores); emitted rows within
+2e-6 * max|kv| of the window (fp32) or 1 ulp / that bound (bf16) against the
+whole-history window definition; the same bits on the GPU whether a sequence
+comes as one prefill, in chunks or token by token.
+"""
+import numpy as np
+import pytest
+import torch
+
+from compressed_kv_attention_compressplan_gb300 import workloads as wl
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env(oracle_mod):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from compressed_kv_attention_compressplan_gb300 import build as B
+    from compressed_kv_attention_compressplan_gb300 import ckv
+
+    B.build()
+    ckv.load_library()
+    return oracle_mod, ckv, torch.device("cuda")
+
+
+class OnlineGpuBackend:
+    def __init__(self, ckv, dev, slot_offset=0):
+        self.ckv, self.dev, self.off = ckv, dev, slot_offset
+        self.status = ckv.new_status(dev)
+
+    def prefill(self, ratio, hd, in_dt, out_dt, state, rows, ape, rid, sl, el):
+        c, d = self.ckv, self.dev
+        i64 = dict(dtype=torch.int64, device=d)
+        units, counts = c.plan_online_prefill(torch.tensor(rid, **i64), torch.tensor(sl, **i64),
+                                              torch.tensor(el, **i64), len(rows), self.off, status=self.status)
+        out = c.compress_online_prefill(hd, state, H.to_torch(rows, in_dt).to(d), H.to_torch(ape, in_dt).to(d), units,
+                                        counts, c.OUT_TOKEN, H.torch_dtype(out_dt), status=self.status)
+        return H.np_bits(out)
+
+    def decode(self, ratio, hd, in_dt, out_dt, state, rows, ape, rid, sl):
+        c, d = self.ckv, self.dev
+        i64 = dict(dtype=torch.int64, device=d)
+        pd = c.plan_online_decode(torch.tensor(rid, **i64), torch.tensor(sl, **i64), self.off, status=self.status)
+        out = c.compress_online_decode(hd, state, H.to_torch(rows, in_dt).to(d), H.to_torch(ape, in_dt).to(d), pd,
+                                       H.torch_dtype(out_dt), status=self.status)
+        return H.np_bits(out)
+
+
+@pytest.mark.parametrize("case", ["small", "batch1024", "long"])
+@pytest.mark.parametrize("pad", [False, True])
+def test_online_plans_bit_exact(env, case, pad):
+    o, ckv, dev = env
+    rng = np.random.default_rng(len(case) + pad)
+    if case == "small":
+        B, maxl = 6, 600
+    elif case == "batch1024":
+        B, maxl = 1024, 300
+    else:
+        B, maxl = 3, 40000
+    sl = rng.integers(1, maxl, B)
+    el = np.array([int(rng.integers(1, s + 1)) if rng.random() < 0.6 else int(s) for s in sl])
+    rid = rng.permutation(B + 5)[:B]
+    nq = int(el.sum())
+    cap = nq if pad else ckv.capacity_online_units(B, nq)
+    i64 = dict(dtype=torch.int64, device=dev)
+    status = ckv.new_status(dev)
+    units, counts = ckv.plan_online_prefill(torch.tensor(rid, **i64), torch.tensor(sl, **i64),
+                                            torch.tensor(el, **i64), nq, 7, cap, pad_invalid=pad, status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    want, (nu, nc), _ = o.plan_online_prefill(rid, sl, el, 7, nq, cap, pad_invalid=pad)
+    assert counts[:2].tolist() == [nc, nu]
+    n = cap if pad else nu
+    assert (units[:n].cpu().numpy() == want[:n]).all()
+    pd = ckv.plan_online_decode(torch.tensor(rid, **i64), torch.tensor(sl, **i64), 7, status=status)
+    assert (pd.cpu().numpy() == o.plan_online_decode(rid, sl, 7)).all()
+
+
+@pytest.mark.parametrize("in_dt,out_dt", [(1, 0), (0, 0), (1, 1)])
+def test_online_modes_bitwise_and_window_parity(env, in_dt, out_dt):
+    o, ckv, dev = env
+    hd = 512
+    rng = np.random.default_rng(3 + in_dt + 2 * out_dt)
+    nreq = 5
+    lens = [int(rng.integers(1, 3 * 128 + 80)) for _ in range(nreq)]
+    rids = [int(x) for x in rng.permutation(8)[:nreq]]
+    tdt = torch.bfloat16 if in_dt else torch.float32
+    g = torch.Generator().manual_seed(90 + in_dt)
+    hist = [wl.bits(torch.randn(n, 2 * hd, generator=g).to(tdt)).copy() for n in lens]
+    ape = wl.bits((torch.randn(128, hd, generator=g) * 0.5).to(tdt)).copy()
+    want = [o.compress_history(128, hd, in_dt, out_dt, h, ape) for h in hist]
+    backend = OnlineGpuBackend(ckv, dev, slot_offset=1)
+    results = {}
+    for mode in ["oneshot", "chunked", "decode", "mixed"]:
+        if mode == "oneshot":
+            sched = [[("prefill", n)] for n in lens]
+        elif mode == "chunked":
+            sched = [H.split_schedule(n, rng, 150, 0.0) for n in lens]
+        elif mode == "decode":
+            sched = [[("decode", 1)] * n for n in lens]
+        else:
+            sched = [H.split_schedule(n, rng, 70, 0.5) for n in lens]
+        state = torch.full((9, 3 * hd), float("nan"), device=dev)
+        results[mode] = H.run_schedule(backend, 128, hd, in_dt, out_dt, hist, rids, sched, ape, state)
+        assert int(backend.status[0]) == 0
+    view = np.uint16 if out_dt else np.uint32
+    for b in range(nreq):
+        ref = results["oneshot"][b]
+        for mode in ["chunked", "decode", "mixed"]:
+            assert (results[mode][b].view(view) == ref.view(view)).all(), (mode, b)
+        emit = [p for p in range(lens[b]) if (p + 1) % 128 == 0]
+        zero = np.setdiff1d(np.arange(lens[b]), emit)
+        assert (ref[zero].view(view) == 0).all()
+        if emit:
+            tok = hist[b]
+            kvmax = H.window_kv_absmax(128, hd, tok, tok, np.array(emit) + 1, np.array(emit),
+                                       np.zeros(len(emit), np.int64), np.zeros(len(emit)), np.zeros(len(emit)))
+            H.assert_pool_close(ref[emit], want[b][emit], out_dt, kvmax, f"online b={b}")
+
+
+def test_online_state_and_compact_rows(env):
+    """One prefill step from a state folded by the oracle: compact rows, the
+    state after it (maxima bit-exact, sums to fp32 accuracy) and bad units."""
+    o, ckv, dev = env
+    hd = 256
+    rng = np.random.default_rng(12)
+    B = 40
+    pl = rng.integers(0, 1000, B)
+    el = rng.integers(1, 600, B)
+    sl = pl + el
+    rid = rng.permutation(B)
+    g = torch.Generator().manual_seed(5)
+    ape = wl.bits((torch.randn(128, hd, generator=g) * 0.5).to(torch.bfloat16)).copy()
+    # the state of each request's current group, folded from synthetic prefix tokens by the oracle
+    st64 = np.zeros((B, 3 * hd))
+    part = pl % 128
+    for b in range(B):
+        if part[b]:
+            toks = wl.bits(torch.randn(int(part[b]), 2 * hd, generator=g).to(torch.bfloat16)).copy()
+            u, _, _ = o.plan_online_prefill([rid[b]], [int(pl[b])], [int(part[b])])
+            o.online_prefill(hd, 1, 0, st64, toks, ape, u)
+    st32 = st64.astype(np.float32)
+    st64 = st32.astype(np.float64)  # both sides start from the same fp32 values
+    nq = int(el.sum())
+    inp = wl.bits(torch.randn(nq, 2 * hd, generator=g).to(torch.bfloat16)).copy()
+    units, (nu, nc), _ = o.plan_online_prefill(rid, sl, el)
+    want = o.online_prefill(hd, 1, 0, st64, inp, ape, units, o.OUT_COMPACT, nc)
+    state = torch.from_numpy(st32.copy()).to(dev)
+    status = ckv.new_status(dev)
+    counts = torch.tensor([nc, nu, 0, 0], dtype=torch.int32, device=dev)
+    out = ckv.compress_online_prefill(hd, state, H.to_torch(inp, 1).to(dev), H.to_torch(ape, 1).to(dev),
+                                      torch.from_numpy(units).to(dev), counts, ckv.OUT_COMPACT, torch.float32,
+                                      out_rows=nc, status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    got = out.cpu().numpy()
+    scale = np.abs(H.bf16_to_f32(inp[:, :hd])).max()
+    assert np.abs(got - want).max() <= 4e-6 * scale
+    gs = state.cpu().numpy().reshape(B, 3, hd)
+    ws = st64.reshape(B, 3, hd)
+    assert (gs[:, 0] == ws[:, 0].astype(np.float32)).all(), "running maxima"
+    np.testing.assert_allclose(gs[:, 1], ws[:, 1], rtol=2e-5, atol=0)  # sums of positive weights
+    # weighted sums may cancel: bound them by the weight sum times max|kv|
+    assert (np.abs(gs[:, 2] - ws[:, 2]) <= 2e-5 * ws[:, 1] * scale).all()
+    # a unit naming a slot past the state is skipped and flagged
+    bad = units.copy()
+    bad.view(np.int32).reshape(-1, 4)[0, 2] = B + 100
+    status.zero_()
+    ckv.compress_online_prefill(hd, state, H.to_torch(inp, 1).to(dev), H.to_torch(ape, 1).to(dev),
+                                torch.from_numpy(bad).to(dev), counts, ckv.OUT_COMPACT, torch.float32, out_rows=nc,
+                                status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) & ckv.STATUS_BAD_INDEX
