@@ -23,9 +23,10 @@ copied back inside the timed region.
 
 ``--config NAME`` times one workload alone (c4_prefill_small, c4_decode,
 c128_decode, c4_prefill, c128_prefill, the speculative-decoding verify shapes
-c4_prefill_mtp / c128_prefill_mtp, and the norm + RoPE + store step on the
-C128 rows, norm_rope_c128_prefill / norm_rope_c128_decode; ``all`` for each
-in turn) and prints one line per workload.  ``--impl reference`` times the CPU oracle on the
+c4_prefill_mtp / c128_prefill_mtp, the norm + RoPE + store step on the
+C128 rows, norm_rope_c128_prefill / norm_rope_c128_decode, and the C128
+workloads through the online state, c128_online_prefill / c128_online_decode;
+``all`` for each in turn) and prints one line per workload.  ``--impl reference`` times the CPU oracle on the
 host cores over a bounded sample of the same step.
 """
 from __future__ import annotations
@@ -389,6 +390,81 @@ class NormRopeRunner:
         return self.boundary * x.head_dim * 4 + self.records * per_write + x.head_dim * 4
 
 
+class OnlineRunner:
+    """A C128 step through the online state.  Setup (not timed): the library
+    folds each request's earlier tokens of its current group into the state,
+    which is then kept as the pristine copy restored before every step."""
+
+    def __init__(self, ckv, x: wl.OnlineInputs, dev):
+        self.ckv, self.x, self.dev = ckv, x, dev
+        hd = x.head_dim
+        self.status = ckv.new_status(dev)
+        self.kv = x.kv_score.to(dev)
+        self.ape = x.ape.to(dev)
+        self.rid, self.sl = x.rid.to(dev), x.seq_lens.to(dev)
+        self.el = x.extend_lens.to(dev) if x.extend_lens is not None else None
+        batch = x.rid.numel()
+        self.state = torch.zeros(batch, 3 * hd, dtype=torch.float32, device=dev)
+        has = x.prefix_lens > 0
+        if bool(has.any()):
+            end = x.seq_lens - (x.extend_lens if x.extend_lens is not None else 1)
+            rows = x.prefix_rows.to(dev)
+            n = int(x.prefix_lens.sum())
+            units, counts = ckv.plan_online_prefill(x.rid[has].to(dev), end[has].to(dev),
+                                                    x.prefix_lens[has].to(dev), n, status=self.status)
+            ckv.compress_online_prefill(hd, self.state, rows, self.ape, units, counts, ckv.OUT_TOKEN,
+                                        status=self.status)
+        self.pristine = self.state.clone()
+        if x.mode == "prefill":
+            nq = int(x.extend_lens.sum())
+            self.cap_u = ckv.capacity_online_units(batch, nq)
+            self.units = torch.empty(self.cap_u, 16, dtype=torch.uint8, device=dev)
+            self.counts = torch.zeros(4, dtype=torch.int32, device=dev)
+            self.cap_c = ckv.capacity_compress(128, batch, nq)
+            self.out = torch.empty(self.cap_c, hd, dtype=x.out_dtype, device=dev)
+            self.plan()
+            torch.cuda.synchronize()
+            self.num_c, self.num_units = int(self.counts[0]), int(self.counts[1])
+            self.loads = int((x.prefix_lens > 0).sum())
+        else:
+            self.plan_d = torch.empty(batch, 16, dtype=torch.uint8, device=dev)
+            self.out = torch.empty(batch, hd, dtype=x.out_dtype, device=dev)
+            self.num_c = int((x.seq_lens % 128 == 0).sum())
+        torch.cuda.synchronize()
+
+    def plan(self):
+        c, x = self.ckv, self.x
+        if x.mode == "prefill":
+            c.plan_online_prefill(self.rid, self.sl, self.el, self.kv.shape[0], 0, self.cap_u, units=self.units,
+                                  counts=self.counts, status=self.status)
+        else:
+            c.plan_online_decode(self.rid, self.sl, 0, plan_d=self.plan_d, status=self.status)
+
+    def compute(self):
+        c, x = self.ckv, self.x
+        if x.mode == "prefill":
+            c.compress_online_prefill(x.head_dim, self.state, self.kv, self.ape, self.units, self.counts,
+                                      c.OUT_COMPACT, out=self.out, status=self.status)
+        else:
+            c.compress_online_decode(x.head_dim, self.state, self.kv, self.ape, self.plan_d, out=self.out,
+                                     status=self.status)
+
+    def restore(self):
+        self.state.copy_(self.pristine)
+
+    def algorithmic_bytes(self) -> int:
+        """Input rows, plan records, slots loaded and stored, the output and ape, each once."""
+        x = self.x
+        hd = x.head_dim
+        slot = 3 * hd * 4
+        batch = x.rid.numel()
+        if x.mode == "prefill":
+            return (self.kv.numel() * 2 + self.num_units * 16 + self.loads * slot + batch * slot +
+                    self.num_c * hd * elem(x.out_dtype) + 128 * hd * 2)
+        first = int(((x.seq_lens - 1) % 128 == 0).sum())
+        return (batch * (2 * hd * 2 + 16 + hd * elem(x.out_dtype) + slot) + (batch - first) * slot + 128 * hd * 2)
+
+
 def cudart():
     """The CUDA runtime library this process already loaded (through torch)."""
     global _cudart
@@ -706,6 +782,8 @@ def bench_config(args, name, ws, rank, local):
     dev = torch.device("cuda", local)
     if name in wl.NORM_ROPE:
         return bench_norm_rope(args, name, ws, rank, ckv, dev)
+    if name in wl.ONLINE:
+        return bench_online(args, name, ws, rank, ckv, dev)
     w = small_workload(name, args.seed + rank) if args.small else wl.NAMED[name](args.seed + rank)
     flush = l2_flush_buffer(dev)
     b = algorithmic_bytes(w)
@@ -774,6 +852,32 @@ def bench_norm_rope(args, name, ws, rank, ckv, dev):
         print(json.dumps(line), flush=True)
 
 
+def bench_online(args, name, ws, rank, ckv, dev):
+    """A C128 step through the online state (plan + fold); prints one line."""
+    x = wl.ONLINE[name](args.seed + rank)
+    flush = l2_flush_buffer(dev)
+    r = OnlineRunner(ckv, x, dev)
+    kname = "online_prefill" if x.mode == "prefill" else "online_decode"
+    step = StepGraph([("plan", r.plan), (kname, r.compute)])
+    seg_ms, _, _ = run_graph(step, flush, r.restore, args.steps, args.warmup, ws)
+    whole = StepGraph([("plan", r.plan), (kname, r.compute)], inner_events=False)
+    whole_ms, _, _ = run_graph(whole, flush, r.restore, args.steps, args.warmup, ws)
+    if int(r.status[0]):
+        raise RuntimeError(f"device status {int(r.status[0])}")
+    peak, kind = peaks()
+    b = r.algorithmic_bytes()
+    ms = float(seg_ms[:, 1].mean())
+    gbs = b / (ms * 1e-3) / 1e9
+    step_ms = float(whole_ms[:, 0].mean())
+    line = {"workload": name, "mode": x.mode, "head_dim": x.head_dim, "batch": x.rid.numel(),
+            "compress_rows": r.num_c, "rows_per_s": r.num_c / (step_ms * 1e-3), "ms_per_step": step_ms,
+            "segments_us": {n: float(seg_ms[:, i].mean()) * 1e3 for i, n in enumerate(step.names)},
+            "main_kernel": kname, "main_bytes": b, "main_gbs": gbs, "main_frac": gbs / peak, "peak_gbs": peak,
+            "peak_kind": kind}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def bench_reference(args, ws, rank):
     """The oracle as it stands on the host cores, each step a bounded sample."""
     if rank != 0:
@@ -811,7 +915,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="step",
-                    help="step (default) | all | " + " | ".join(list(wl.NAMED) + list(wl.NORM_ROPE)))
+                    help="step (default) | all | " + " | ".join(list(wl.NAMED) + list(wl.NORM_ROPE) + list(wl.ONLINE)))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true", help="with --config: scaled-down workloads for profiling")
@@ -828,7 +932,7 @@ def main():
     elif args.config == "step":
         bench_step(args, ws, rank, local)
     else:
-        names = list(wl.NAMED) + list(wl.NORM_ROPE) if args.config == "all" else [args.config]
+        names = list(wl.NAMED) + list(wl.NORM_ROPE) + list(wl.ONLINE) if args.config == "all" else [args.config]
         for n in names:
             bench_config(args, n, ws, rank, local)
     if ws > 1:

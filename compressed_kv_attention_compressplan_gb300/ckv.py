@@ -305,12 +305,14 @@ def capacity_online_units(batch: int, num_q_tokens: int) -> int:
 
 def plan_online_prefill(rid: torch.Tensor, seq_lens: torch.Tensor, extend_lens: torch.Tensor, num_q_tokens: int,
                         slot_offset: int = 0, capacity_u: Optional[int] = None, pad_invalid: bool = False,
-                        counts: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None, stream=None):
+                        units: Optional[torch.Tensor] = None, counts: Optional[torch.Tensor] = None,
+                        status: Optional[torch.Tensor] = None, stream=None):
     """Returns ``(units [cap_u, 16] u8, counts [4] int32)``; counts = {num_c, num_units, min el, max el}."""
     batch = rid.numel()
     if capacity_u is None:
         capacity_u = capacity_online_units(batch, num_q_tokens)
-    units = torch.empty(max(capacity_u, 1), 16, dtype=torch.uint8, device=rid.device)
+    if units is None:
+        units = torch.empty(max(capacity_u, 1), 16, dtype=torch.uint8, device=rid.device)
     if counts is None:
         counts = torch.empty(4, dtype=torch.int32, device=rid.device)
     _check(load_library().ckv_plan_online_prefill(_ptr(rid), _ptr(seq_lens), _ptr(extend_lens), batch, num_q_tokens,
@@ -321,9 +323,11 @@ def plan_online_prefill(rid: torch.Tensor, seq_lens: torch.Tensor, extend_lens: 
 
 
 def plan_online_decode(rid: torch.Tensor, seq_lens: torch.Tensor, slot_offset: int = 0,
-                       status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                       plan_d: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
     batch = rid.numel()
-    plan_d = torch.empty(max(batch, 1), 16, dtype=torch.uint8, device=rid.device)
+    if plan_d is None:
+        plan_d = torch.empty(max(batch, 1), 16, dtype=torch.uint8, device=rid.device)
     _check(load_library().ckv_plan_online_decode(_ptr(rid), _ptr(seq_lens), batch, slot_offset, _ptr(plan_d),
                                                  _ptr(status), _stream(stream)), "ckv_plan_online_decode")
     return plan_d[:batch]

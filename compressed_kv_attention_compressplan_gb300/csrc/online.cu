@@ -42,6 +42,12 @@ struct OnlineArgs {
   uint32_t out_rows;
   void* out;
   uint32_t* d_status;
+  // Prefill runs in two passes.  The first unit of a request may load its slot
+  // while the request's last unit (another unit, starting at a group start)
+  // would store it, so pass 0 folds every unit but leaves those stores out,
+  // and pass 1 -- a second launch, after every load -- refolds those last
+  // units (their tokens only) and stores their state.
+  int pass;
 };
 
 // Running softmax of one channel over the tokens of a group so far.
@@ -165,11 +171,13 @@ __global__ __launch_bounds__(kOnThreads, 2) void online_prefill_kernel(const Onl
     const uint32_t flags = rec.w >> CKV_UNIT_FLAGS_SHIFT;
     const bool emit = flags & CKV_UNIT_EMIT;
     const bool token = a.out_layout == CKV_OUT_TOKEN;
+    const bool late_store = (flags & CKV_UNIT_STORE) && !(flags & CKV_UNIT_LOAD) && (pos0 % 128) == 0;
+    if (a.pass == 1 && !late_store) continue;
     bool ok = slot >= 0 && static_cast<uint64_t>(slot) < a.slots && cnt >= 1 && cnt <= 128 &&
               ragged0 + cnt <= a.num_q_tokens && (pos0 % 128) + cnt <= 128;
     if (emit && !token) ok = ok && orow < a.out_rows;
     if (!ok) {
-      if (c0 == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+      if (c0 == 0 && a.pass == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
       continue;
     }
     float* st = a.state + static_cast<size_t>(slot) * 3 * hd;
@@ -194,13 +202,13 @@ __global__ __launch_bounds__(kOnThreads, 2) void online_prefill_kernel(const Onl
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             online_token(q[j], first, score_plus_bias(sc[d].get(j), bias[d].get(j)), kv[d].get(j));
-          if (token && !(emit && t0 + d + 1 == cnt))
+          if (a.pass == 0 && token && !(emit && t0 + d + 1 == cnt))
             store_zero_chunk<TOut, 4>(out + (static_cast<size_t>(ragged0) + t0 + d) * hd + c0);
         }
       }
     }
-    if (flags & CKV_UNIT_STORE) store_state(st, hd, c0, q);
-    if (emit) {
+    if ((flags & CKV_UNIT_STORE) && late_store == (a.pass == 1)) store_state(st, hd, c0, q);
+    if (emit && a.pass == 0) {
       const float r[4] = {finish(q[0].a, q[0].l), finish(q[1].a, q[1].l), finish(q[2].a, q[2].l),
                           finish(q[3].a, q[3].l)};
       const size_t row = token ? static_cast<size_t>(ragged0) + cnt - 1 : orow;
@@ -335,6 +343,10 @@ extern "C" int ckv_compress_online_prefill(int head_dim, int in_dtype, int out_d
   const uint32_t upb = kOnThreads / (head_dim / 4);
   uint32_t grid = (capacity_u + upb - 1) / upb;
   grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 8u * static_cast<uint32_t>(sm_count())));
+  a.pass = 0;
+  const int rc0 = launch_typed<PrefillK>(a, dim3(grid), reinterpret_cast<cudaStream_t>(stream));
+  if (rc0) return rc0;
+  a.pass = 1;
   return launch_typed<PrefillK>(a, dim3(grid), reinterpret_cast<cudaStream_t>(stream));
 }
 

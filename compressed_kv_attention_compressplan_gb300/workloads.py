@@ -320,6 +320,54 @@ def norm_rope_c128_decode(seed: int = 0, head_dim: int = 512, rope_dim: int = 64
 NORM_ROPE = {"norm_rope_c128_prefill": norm_rope_c128_prefill, "norm_rope_c128_decode": norm_rope_c128_decode}
 
 
+# ----------------------------------------------------------------------------- online C128 state inputs
+@dataclasses.dataclass
+class OnlineInputs:
+    """A C128 step through the online state.  The state of each request's
+    current group is not drawn: the earlier tokens of that group are
+    (prefix_rows, prefix_lens tokens per request, batch order), and the caller
+    folds them into the state before the step."""
+    name: str
+    mode: str                # "prefill" | "decode"
+    head_dim: int
+    rid: torch.Tensor
+    seq_lens: torch.Tensor
+    extend_lens: Optional[torch.Tensor]
+    kv_score: torch.Tensor   # bf16 [num_q_tokens or batch, 2 * head_dim]
+    ape: torch.Tensor        # bf16 [128, head_dim]
+    prefix_rows: torch.Tensor
+    prefix_lens: torch.Tensor
+    out_dtype: torch.dtype
+    out_layout: str
+
+
+def c128_online_prefill(seed: int = 0, head_dim: int = 512) -> OnlineInputs:
+    """The C128 prefill workload's lengths and inputs, through the online state."""
+    rid, sl, el = c128_prefill_lengths(seed)
+    nq = int(el.sum())
+    kv = normal((nq, 2 * head_dim), torch.bfloat16, 1.0, _seed(seed, 11))
+    set_score_outliers(kv, 128, head_dim, 0.01, 8.0, _gen(seed, 12))
+    ape = normal((128, head_dim), torch.bfloat16, 0.1, _seed(seed, 13))
+    part = (sl - el) % 128
+    prefix = normal((int(part.sum()), 2 * head_dim), torch.bfloat16, 1.0, _seed(seed, 31))
+    return OnlineInputs("c128_online_prefill", "prefill", head_dim, rid, sl, el, kv, ape, prefix, part,
+                        torch.float32, COMPACT)
+
+
+def c128_online_decode(seed: int = 0, head_dim: int = 512) -> OnlineInputs:
+    """The C128 decode workload's lengths and inputs, through the online state."""
+    rid, sl = c128_decode_lengths(seed)
+    kv = normal((rid.numel(), 2 * head_dim), torch.bfloat16, 1.0, _seed(seed, 11))
+    ape = normal((128, head_dim), torch.bfloat16, 0.1, _seed(seed, 13))
+    part = (sl - 1) % 128
+    prefix = normal((int(part.sum()), 2 * head_dim), torch.bfloat16, 1.0, _seed(seed, 31))
+    return OnlineInputs("c128_online_decode", "decode", head_dim, rid, sl, None, kv, ape, prefix, part,
+                        torch.float32, TOKEN)
+
+
+ONLINE = {"c128_online_prefill": c128_online_prefill, "c128_online_decode": c128_online_decode}
+
+
 def random_prefill(ratio: int, head_dim: int, in_dtype, out_dtype, out_layout: str, prefix_lens, extend_lens,
                    seed: int, num_requests_state: Optional[int] = None, rid=None,
                    state_fill: str = "normal", outlier_frac: float = 0.0) -> Workload:

@@ -291,9 +291,11 @@ int ckv_plan_online_prefill(const int64_t* rid, const int64_t* seq_lens, const i
  * of its group's last token and +0.0 in every other row the units cover;
  * CKV_OUT_COMPACT: out [out_rows, head_dim], row = the unit's output row.
  * Units naming a slot >= slots, rows past num_q_tokens or an output row >=
- * out_rows are skipped with CKV_STATUS_BAD_INDEX.  Two units of one call must
- * not name the same slot unless they are consecutive groups of one request
- * (the planner's output satisfies this). */
+ * out_rows are skipped with CKV_STATUS_BAD_INDEX.  Units of different
+ * requests must name different slots; the units of one request share its
+ * slot, and the library reads the slot for the request's first unit before
+ * any unit of the call stores it (two launches: the second one stores the
+ * state of last units that start at a group start). */
 int ckv_compress_online_prefill(int head_dim, int in_dtype, int out_dtype, float* state, uint64_t slots,
                                 const void* kv_score_input, uint32_t num_q_tokens, const void* ape,
                                 const ckv_online_unit_t* units, const uint32_t* d_counts, uint32_t capacity_u,

@@ -177,3 +177,91 @@ def test_online_state_and_compact_rows(env):
                                 status=status)
     torch.cuda.synchronize()
     assert int(status[0]) & ckv.STATUS_BAD_INDEX
+
+
+def _fold_prefix(o, ckv, dev, x, hd):
+    """Each side folds the requests' earlier tokens of their current group into its own state."""
+    batch = x.rid.numel()
+    st64 = np.zeros((batch, 3 * hd))
+    st = torch.zeros(batch, 3 * hd, dtype=torch.float32, device=dev)
+    has = (x.prefix_lens > 0).numpy()
+    end = (x.seq_lens - (x.extend_lens if x.extend_lens is not None else 1)).numpy()
+    n = int(x.prefix_lens.sum())
+    rows = wl.bits(x.prefix_rows)
+    ape = wl.bits(x.ape)
+    units, _, _ = o.plan_online_prefill(x.rid.numpy()[has], end[has], x.prefix_lens.numpy()[has])
+    o.online_prefill(hd, 1, 0, st64, rows, ape, units)
+    i64 = dict(dtype=torch.int64, device=dev)
+    gu, gc = ckv.plan_online_prefill(torch.tensor(x.rid.numpy()[has], **i64), torch.tensor(end[has], **i64),
+                                     torch.tensor(x.prefix_lens.numpy()[has], **i64), n)
+    ckv.compress_online_prefill(hd, st, x.prefix_rows.to(dev), x.ape.to(dev), gu, gc, ckv.OUT_TOKEN)
+    return st64, st
+
+
+@pytest.mark.slow
+def test_full_size_online_prefill(env):
+    """The C128 prefill workload through the online state, in the benchmark's
+    launch configuration; a seeded sample of emitted rows (and the first and
+    last) checked against the oracle folding the same units."""
+    o, ckv, dev = env
+    x = wl.c128_online_prefill(0)
+    hd = x.head_dim
+    st64, st = _fold_prefix(o, ckv, dev, x, hd)
+    nq = int(x.extend_lens.sum())
+    i64 = dict(dtype=torch.int64, device=dev)
+    status = ckv.new_status(dev)
+    units, counts = ckv.plan_online_prefill(x.rid.to(dev), x.seq_lens.to(dev), x.extend_lens.to(dev), nq,
+                                            status=status)
+    cap_c = ckv.capacity_compress(128, x.rid.numel(), nq)
+    out = ckv.compress_online_prefill(hd, st, x.kv_score.to(dev), x.ape.to(dev), units, counts, ckv.OUT_COMPACT,
+                                      out_rows=cap_c, status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    wu, (nu, nc), _ = o.plan_online_prefill(x.rid, x.seq_lens, x.extend_lens)
+    assert counts[:2].tolist() == [nc, nu] and (units[:nu].cpu().numpy() == wu).all()
+    w = wu.view(np.uint32).reshape(-1, 4)
+    emitting = np.nonzero((w[:, 3] >> 24) & 2)[0]
+    rng = np.random.default_rng(3)
+    pick = np.unique(np.concatenate([rng.choice(emitting, 200, replace=False), emitting[[0, -1]]]))
+    want = o.online_prefill(hd, 1, 0, st64, wl.bits(x.kv_score), wl.bits(x.ape), np.ascontiguousarray(wu[pick]),
+                            o.OUT_COMPACT, nc)
+    rows = (w[pick, 3] & 0xFFFFFF).astype(np.int64)
+    got = out[: nc].cpu().numpy()[rows]
+    kv_in = H.bf16_to_f32(wl.bits(x.kv_score)[:, :hd])
+    # per channel, the largest |kv| of the group's tokens (earlier tokens from the prefix rows)
+    pre_off = np.concatenate([[0], np.cumsum(x.prefix_lens.numpy())])
+    kv_pre = H.bf16_to_f32(wl.bits(x.prefix_rows)[:, :hd])
+    starts = np.concatenate([[0], np.cumsum(x.extend_lens.numpy())])
+    kvmax = np.zeros((len(pick), hd), np.float32)
+    for i, k in enumerate(pick):
+        r0, cnt = w[k, 1] & 0xFFFFFF, w[k, 1] >> 24
+        m = np.abs(kv_in[r0:r0 + cnt]).max(0)
+        if (w[k, 3] >> 24) & 1:
+            b = np.searchsorted(starts, r0, side="right") - 1
+            m = np.maximum(m, np.abs(kv_pre[pre_off[b]:pre_off[b + 1]]).max(0))
+        kvmax[i] = m
+    H.assert_pool_close(got, want[rows], 0, kvmax, "online prefill sample")
+
+
+@pytest.mark.slow
+def test_full_size_online_decode(env):
+    o, ckv, dev = env
+    x = wl.c128_online_decode(0)
+    hd = x.head_dim
+    st64, st = _fold_prefix(o, ckv, dev, x, hd)
+    status = ckv.new_status(dev)
+    pd = ckv.plan_online_decode(x.rid.to(dev), x.seq_lens.to(dev), status=status)
+    out = ckv.compress_online_decode(hd, st, x.kv_score.to(dev), x.ape.to(dev), pd, status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    wpd = o.plan_online_decode(x.rid, x.seq_lens)
+    assert (pd.cpu().numpy() == wpd).all()
+    want = o.online_decode(hd, 1, 0, st64, wl.bits(x.kv_score), wl.bits(x.ape), wpd)
+    got = out.cpu().numpy()
+    bnd = np.nonzero((x.seq_lens.numpy() % 128) == 0)[0]
+    assert (got[np.setdiff1d(np.arange(len(got)), bnd)].view(np.uint32) == 0).all()
+    pre_off = np.concatenate([[0], np.cumsum(x.prefix_lens.numpy())])
+    kv_pre = H.bf16_to_f32(wl.bits(x.prefix_rows)[:, :hd])
+    kv_in = H.bf16_to_f32(wl.bits(x.kv_score)[:, :hd])
+    kvmax = np.stack([np.maximum(np.abs(kv_in[b]), np.abs(kv_pre[pre_off[b]:pre_off[b + 1]]).max(0)) for b in bnd])
+    H.assert_pool_close(got[bnd], want[bnd], 0, kvmax, "online decode boundary rows")
