@@ -854,7 +854,10 @@ def bench_norm_rope(args, name, ws, rank, ckv, dev):
 
 def bench_online(args, name, ws, rank, ckv, dev):
     """A C128 step through the online state (plan + fold); prints one line."""
-    x = wl.ONLINE[name](args.seed + rank)
+    if args.small and name == "c128_online_prefill":  # profiler captures: 16 long requests, still > L2
+        x = wl.c128_online_prefill(args.seed + rank, num_long=16)
+    else:
+        x = wl.ONLINE[name](args.seed + rank)
     flush = l2_flush_buffer(dev)
     r = OnlineRunner(ckv, x, dev)
     kname = "online_prefill" if x.mode == "prefill" else "online_decode"

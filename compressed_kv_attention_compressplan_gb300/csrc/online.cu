@@ -8,9 +8,9 @@
 // folded in one prefill, in chunks or token by token gives the same bits.
 // Work unit of the prefill: one planner unit (one request's tokens inside one
 // 128-group); head_dim / 4 threads own 4 channels each and walk the unit's
-// tokens in order, the loads of 8 tokens (4 for fp32 rows) issued before
-// their arithmetic.
+// tokens in order, fed by a per-thread cp.async ring (see RingCfg).
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -19,11 +19,31 @@ namespace ckv {
 namespace {
 
 constexpr int kOnThreads = 256;
-// tokens whose loads are in flight at once (fewer for fp32 rows, twice as wide)
+// Each thread streams its own 4-channel slices of the unit's token rows (kv,
+// score) and ape rows into a private ring in shared memory with cp.async:
+// kStages stages of kTok tokens, kStages - 1 of them in flight while the
+// thread folds the oldest.  A thread reads only what it copied itself, so the
+// ring needs no barrier.  Slot (stage, token, k) of thread t sits at
+// ((stage * kTok + token) * 3 + k) * blockDim + t: a warp's accesses are
+// consecutive.
+constexpr int kStages = 4;
+constexpr int kTok = 2;
+
 template <typename TIn>
-struct Depth {
-  static constexpr int value = sizeof(TIn) == 2 ? 8 : 4;
+struct RingCfg {
+  using Raw = typename std::conditional<sizeof(TIn) == 2, uint2, uint4>::type;
+  static constexpr int kBytes = static_cast<int>(sizeof(Raw));
+  static constexpr int SMEM = kStages * kTok * 3 * kOnThreads * kBytes;
 };
+
+template <int BYTES>
+__device__ __forceinline__ void cp_async(void* smem_dst, const void* gsrc) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(d), "l"(gsrc), "n"(BYTES) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 struct OnlineArgs {
   int head_dim;
@@ -50,31 +70,30 @@ struct OnlineArgs {
   int pass;
 };
 
-// Running softmax of one channel over the tokens of a group so far.
+// Running softmax of one channel over the tokens of a group so far; m2 is
+// m * log2(e) rounded to fp32, recomputed from m whenever a slot is loaded.
 struct OnlineState {
-  float m, l, a, nml;  // nml = -m * log2(e), kept with m
+  float m, l, a, m2;
 
   __device__ __forceinline__ void start(float s, float kv) {
     m = s;
     l = 1.0f;
     a = kv;
-    nml = neg_max_log2e(s);
+    m2 = __fmul_rn(s, kLog2e);
   }
-  // A token that raises the maximum rescales the sums by exp(m_old - s) and
-  // enters with weight 1; any other enters with weight exp(s - m).
+  // With s2 = s * log2(e) and w = 2^-|s2 - m2|: a token that raises the
+  // maximum rescales the sums by w (= exp(m_old - s)) and enters with weight
+  // 1 (l = l w + 1, a = a w + kv); any other enters with weight w (= exp(s -
+  // m)): l = 1 w + l, a = kv w + a.  One exponential either way, chosen by
+  // selects so that a warp does not diverge.
   __device__ __forceinline__ void fold(float s, float kv) {
-    if (s > m) {
-      const float nml_s = neg_max_log2e(s);
-      const float c = weight_of(m, nml_s);
-      l = __fmaf_rn(l, c, 1.0f);
-      a = __fmaf_rn(a, c, kv);
-      m = s;
-      nml = nml_s;
-    } else {
-      const float e = weight_of(s, nml);
-      l = __fadd_rn(l, e);
-      a = __fmaf_rn(kv, e, a);
-    }
+    const bool up = s > m;
+    const float s2 = __fmul_rn(s, kLog2e);
+    const float w = ex2(-fabsf(__fsub_rn(s2, m2)));
+    l = __fmaf_rn(up ? l : 1.0f, w, up ? 1.0f : l);
+    a = __fmaf_rn(up ? a : kv, w, up ? kv : a);
+    m = up ? s : m;
+    m2 = up ? s2 : m2;
   }
 };
 
@@ -90,13 +109,14 @@ struct Raw4;
 template <>
 struct Raw4<float> {
   float4 v;
-  __device__ __forceinline__ void load(const float* p) { v = __ldg(reinterpret_cast<const float4*>(p)); }
+  __device__ __forceinline__ void from(const uint4& u) { v = make_float4(__uint_as_float(u.x), __uint_as_float(u.y),
+                                                                      __uint_as_float(u.z), __uint_as_float(u.w)); }
   __device__ __forceinline__ float get(int j) const { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; }
 };
 template <>
 struct Raw4<__nv_bfloat16> {
   uint2 v;
-  __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = __ldg(reinterpret_cast<const uint2*>(p)); }
+  __device__ __forceinline__ void from(const uint2& u) { v = u; }
   __device__ __forceinline__ float get(int j) const {
     return j == 0 ? bf16lo(v.x) : j == 1 ? bf16hi(v.x) : j == 2 ? bf16lo(v.y) : bf16hi(v.y);
   }
@@ -127,10 +147,10 @@ __device__ __forceinline__ void load_state(const float* st, int hd, int c0, Onli
   const float4 m = *reinterpret_cast<const float4*>(st + c0);
   const float4 l = *reinterpret_cast<const float4*>(st + hd + c0);
   const float4 a = *reinterpret_cast<const float4*>(st + 2 * hd + c0);
-  q[0] = {m.x, l.x, a.x, neg_max_log2e(m.x)};
-  q[1] = {m.y, l.y, a.y, neg_max_log2e(m.y)};
-  q[2] = {m.z, l.z, a.z, neg_max_log2e(m.z)};
-  q[3] = {m.w, l.w, a.w, neg_max_log2e(m.w)};
+  q[0] = {m.x, l.x, a.x, __fmul_rn(m.x, kLog2e)};
+  q[1] = {m.y, l.y, a.y, __fmul_rn(m.y, kLog2e)};
+  q[2] = {m.z, l.z, a.z, __fmul_rn(m.z, kLog2e)};
+  q[3] = {m.w, l.w, a.w, __fmul_rn(m.w, kLog2e)};
 }
 
 __device__ __forceinline__ void store_state(float* st, int hd, int c0, const OnlineState (&q)[4]) {
@@ -145,7 +165,11 @@ __device__ __forceinline__ void store_quad(TOut* p, const float (&r)[4]) {
 }
 
 template <typename TIn, typename TOut>
-__global__ __launch_bounds__(kOnThreads, 2) void online_prefill_kernel(const OnlineArgs a) {
+__global__ __launch_bounds__(kOnThreads, 4) void online_prefill_kernel(const OnlineArgs a) {
+  using Cfg = RingCfg<TIn>;
+  using Raw = typename Cfg::Raw;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Raw* ring = reinterpret_cast<Raw*>(smem_raw);
   pdl_wait();  // units, state and input may come from the previous kernels
   pdl_release();
   const int hd = a.head_dim;
@@ -183,27 +207,47 @@ __global__ __launch_bounds__(kOnThreads, 2) void online_prefill_kernel(const Onl
     float* st = a.state + static_cast<size_t>(slot) * 3 * hd;
     OnlineState q[4];
     if (flags & CKV_UNIT_LOAD) load_state(st, hd, c0, q);
-    constexpr int kOnDepth = Depth<TIn>::value;
-    for (uint32_t t0 = 0; t0 < cnt; t0 += kOnDepth) {
-      Raw4<TIn> kv[kOnDepth], sc[kOnDepth], bias[kOnDepth];
+    const uint32_t nblk = (cnt + kTok - 1) / kTok;
+    // the unit's first token row and ape row (a unit stays inside one group,
+    // so its ape rows are consecutive); tokens are offsets from these
+    const TIn* urow = input + static_cast<size_t>(ragged0) * width + c0;
+    const TIn* uape = ape + static_cast<size_t>(pos0 % 128) * hd + c0;
+    auto issue = [&](uint32_t blk) {
+      if (blk < nblk) {
+        Raw* dst = ring + static_cast<size_t>((blk % kStages) * kTok * 3) * kOnThreads + threadIdx.x;
 #pragma unroll
-      for (int d = 0; d < kOnDepth; ++d) {
-        if (t0 + d < cnt) {
-          const TIn* row = input + (static_cast<size_t>(ragged0) + t0 + d) * width;
-          kv[d].load(row + c0);
-          sc[d].load(row + hd + c0);
-          bias[d].load(ape + static_cast<size_t>((pos0 + t0 + d) % 128) * hd + c0);
+        for (int d = 0; d < kTok; ++d) {
+          const uint32_t t = blk * kTok + d;
+          if (t < cnt) {
+            const TIn* row = urow + t * static_cast<uint32_t>(width);
+            cp_async<Cfg::kBytes>(dst + (3 * d + 0) * kOnThreads, row);
+            cp_async<Cfg::kBytes>(dst + (3 * d + 1) * kOnThreads, row + hd);
+            cp_async<Cfg::kBytes>(dst + (3 * d + 2) * kOnThreads, uape + t * static_cast<uint32_t>(hd));
+          }
         }
       }
+      cp_async_commit();  // an empty group past the end keeps the count uniform
+    };
 #pragma unroll
-      for (int d = 0; d < kOnDepth; ++d) {
-        if (t0 + d < cnt) {
-          const bool first = (pos0 + t0 + d) % 128 == 0;
+    for (int b = 0; b < kStages - 1; ++b) issue(b);
+    for (uint32_t blk = 0; blk < nblk; ++blk) {
+      issue(blk + kStages - 1);
+      cp_async_wait<kStages - 1>();  // this thread's copies of block blk have landed
+      const Raw* src = ring + static_cast<size_t>((blk % kStages) * kTok * 3) * kOnThreads + threadIdx.x;
+#pragma unroll
+      for (int d = 0; d < kTok; ++d) {
+        const uint32_t t = blk * kTok + d;
+        if (t < cnt) {
+          Raw4<TIn> kv, sc, bias;
+          kv.from(src[(3 * d + 0) * kOnThreads]);
+          sc.from(src[(3 * d + 1) * kOnThreads]);
+          bias.from(src[(3 * d + 2) * kOnThreads]);
+          const bool first = (pos0 + t) % 128 == 0;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            online_token(q[j], first, score_plus_bias(sc[d].get(j), bias[d].get(j)), kv[d].get(j));
-          if (a.pass == 0 && token && !(emit && t0 + d + 1 == cnt))
-            store_zero_chunk<TOut, 4>(out + (static_cast<size_t>(ragged0) + t0 + d) * hd + c0);
+            online_token(q[j], first, score_plus_bias(sc.get(j), bias.get(j)), kv.get(j));
+          if (a.pass == 0 && token && !(emit && t + 1 == cnt))
+            store_zero_chunk<TOut, 4>(out + (static_cast<size_t>(ragged0) + t) * hd + c0);
         }
       }
     }
@@ -291,25 +335,41 @@ int check_online(const OnlineArgs& a) {
   return CKV_OK;
 }
 
-template <template <typename, typename> class K>
-int launch_typed(const OnlineArgs& a, dim3 grid, cudaStream_t s) {
-  const dim3 block(kOnThreads);
-  if (a.in_dtype == CKV_BF16) {
-    if (a.out_dtype == CKV_BF16) return launch_pdl(K<__nv_bfloat16, __nv_bfloat16>::fn, grid, block, 0, s, a);
-    return launch_pdl(K<__nv_bfloat16, float>::fn, grid, block, 0, s, a);
-  }
-  if (a.out_dtype == CKV_BF16) return launch_pdl(K<float, __nv_bfloat16>::fn, grid, block, 0, s, a);
-  return launch_pdl(K<float, float>::fn, grid, block, 0, s, a);
-}
-
 template <typename TIn, typename TOut>
 struct PrefillK {
   static constexpr auto fn = online_prefill_kernel<TIn, TOut>;
+  static constexpr int smem = RingCfg<TIn>::SMEM;
 };
 template <typename TIn, typename TOut>
 struct DecodeK {
   static constexpr auto fn = online_decode_kernel<TIn, TOut>;
+  static constexpr int smem = 0;
 };
+
+template <typename KT>
+int launch_one(const OnlineArgs& a, dim3 grid, cudaStream_t s) {
+  if (KT::smem > 48 * 1024) {
+    static bool done = false;  // per instantiation
+    if (!done) {
+      if (cudaFuncSetAttribute(KT::fn, cudaFuncAttributeMaxDynamicSharedMemorySize, KT::smem) != cudaSuccess) {
+        cudaGetLastError();
+        return CKV_ERR_LAUNCH;
+      }
+      done = true;
+    }
+  }
+  return launch_pdl(KT::fn, grid, dim3(kOnThreads), KT::smem, s, a);
+}
+
+template <template <typename, typename> class K>
+int launch_typed(const OnlineArgs& a, dim3 grid, cudaStream_t s) {
+  if (a.in_dtype == CKV_BF16) {
+    if (a.out_dtype == CKV_BF16) return launch_one<K<__nv_bfloat16, __nv_bfloat16>>(a, grid, s);
+    return launch_one<K<__nv_bfloat16, float>>(a, grid, s);
+  }
+  if (a.out_dtype == CKV_BF16) return launch_one<K<float, __nv_bfloat16>>(a, grid, s);
+  return launch_one<K<float, float>>(a, grid, s);
+}
 
 }  // namespace
 }  // namespace ckv

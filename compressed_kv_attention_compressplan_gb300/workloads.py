@@ -341,9 +341,9 @@ class OnlineInputs:
     out_layout: str
 
 
-def c128_online_prefill(seed: int = 0, head_dim: int = 512) -> OnlineInputs:
+def c128_online_prefill(seed: int = 0, head_dim: int = 512, num_long: int = 128) -> OnlineInputs:
     """The C128 prefill workload's lengths and inputs, through the online state."""
-    rid, sl, el = c128_prefill_lengths(seed)
+    rid, sl, el = c128_prefill_lengths(seed, num_long=num_long)
     nq = int(el.sum())
     kv = normal((nq, 2 * head_dim), torch.bfloat16, 1.0, _seed(seed, 11))
     set_score_outliers(kv, 128, head_dim, 0.01, 8.0, _gen(seed, 12))
