@@ -25,7 +25,7 @@
 // one channel slice (its ape slice stays in registers); a producer warp
 // streams the CTA's tiles through a shared-memory ring while the consumer
 // warps reduce the previous tiles.  Prefill tiles are 128 channels wide (64 KB,
-// 3 stages); decode tiles 64 channels (32 KB, 6 stages), and every decode CTA
+// 3 stages); decode tiles 64 channels (32 KB, 4 stages), and every decode CTA
 // first finds the page-boundary rows by a block-wide scan of the plan so that
 // the page reads are spread evenly over the SMs.  Decode batches too large for
 // that use a kernel with one CTA per (row, slice).
@@ -886,30 +886,39 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
                     Cfg::SMEM, s, a, slices, in_map, in_map);
 }
 
+// Persistent decode tiles: kDecCS channels (bf16; half for fp32) x 127 page
+// rows, kDecNS stages, kDecNG consumer groups.
+constexpr int kDecCS = 64;
+constexpr int kDecNS = 4;
+constexpr int kDecNG = 2;  // consumer groups reduce alternate tiles
+
 template <typename TIn, typename TOut>
 int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
   if (a.capacity == 0) return CKV_OK;
   if (a.state_rows == 0 || a.state_rows > 0x7FFFFFFFull) return CKV_ERR_SIZE;
+  constexpr int PCS = sizeof(TIn) == 2 ? kDecCS : kDecCS / 2;
+  const uint32_t pslices = static_cast<uint32_t>(a.head_dim / PCS);
+  const uint32_t per_slice = std::max<uint32_t>(1, static_cast<uint32_t>(sm_count()) / pslices);
+  // each CTA owns at most ceil(batch / per_slice) boundary rows and
+  // ceil(batch / grid) rows without a window: both lists live in shared memory
+  if ((a.capacity + per_slice - 1) / per_slice <= static_cast<uint32_t>(kOwnRows)) {
+    // persistent: every CTA scans the plan and streams its share of boundary tiles
+    alignas(64) CUtensorMap page_map;
+    int rc = make_map(&page_map, a.state_mut, a.in_dtype, 2ull * a.head_dim, a.state_rows, PCS, 127);
+    if (rc) return rc;
+    using Cfg = PersistCfg<TIn, PCS, kDecNS, kDecNG, true>;
+    static bool configured_p[64] = {};
+    rc = opt_in_smem(c128_persistent_kernel<TIn, TOut, PCS, kDecNS, kDecNG, true>, Cfg::SMEM, configured_p);
+    if (rc) return rc;
+    return launch_pdl(c128_persistent_kernel<TIn, TOut, PCS, kDecNS, kDecNG, true>, dim3(per_slice * pslices),
+                      dim3(Cfg::THREADS), Cfg::SMEM, s, a, pslices, page_map, page_map);
+  }
+  // very large batches: one CTA per (row, slice)
   constexpr int CS = DecodeCfg<TIn>::CS;
   const uint32_t slices = static_cast<uint32_t>(a.head_dim / CS);
   alignas(64) CUtensorMap page_map;
   int rc = make_map(&page_map, a.state_mut, a.in_dtype, 2ull * a.head_dim, a.state_rows, CS, 127);
   if (rc) return rc;
-  const uint32_t per_slice = std::max<uint32_t>(1, static_cast<uint32_t>(sm_count()) / slices);
-  // each CTA owns at most ceil(batch / per_slice) boundary rows and
-  // ceil(batch / grid) rows without a window: both lists live in shared memory
-  if ((a.capacity + per_slice - 1) / per_slice <= static_cast<uint32_t>(kOwnRows)) {
-    // persistent: every CTA scans the plan and streams its share of boundary tiles
-    constexpr int NS = 6;
-    constexpr int NG = 2;  // two consumer groups reduce alternate tiles
-    using Cfg = PersistCfg<TIn, CS, NS, NG, true>;
-    static bool configured_p[64] = {};
-    rc = opt_in_smem(c128_persistent_kernel<TIn, TOut, CS, NS, NG, true>, Cfg::SMEM, configured_p);
-    if (rc) return rc;
-    return launch_pdl(c128_persistent_kernel<TIn, TOut, CS, NS, NG, true>, dim3(per_slice * slices),
-                      dim3(Cfg::THREADS), Cfg::SMEM, s, a, slices, page_map, page_map);
-  }
-  // very large batches: one CTA per (row, slice)
   using Cfg = DecodeCfg<TIn>;
   const uint64_t tiles64 = static_cast<uint64_t>(a.capacity) * slices;
   if (tiles64 > 0x7FFFFFFFull) return CKV_ERR_SIZE;
