@@ -1,6 +1,7 @@
 """Parity at the seven named workloads' full sizes, in the launch configuration the
-benchmark times (capacities from ckv_capacity_*, no padding, plan -> pool ->
-write on one stream; plan -> decode).
+benchmark times (capacities from ckv_capacity_*, or num_q_tokens-sized plan
+buffers padded with the invalid record for the speculative-decoding
+workloads; plan -> pool -> write on one stream; plan -> decode).
 
 Plans and state buffers are compared with the oracle byte for byte; decode
 outputs in full; prefill outputs on a seeded sample of compress records that
