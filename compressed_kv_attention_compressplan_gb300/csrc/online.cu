@@ -1,5 +1,5 @@
 // online.cu -- C128 compression through an online state: one slot of
-// (m | l | a) x head_dim fp32 per request instead of a 128-row page
+// (m2 | l | a) x head_dim fp32 per request instead of a 128-row page
 // (compressor_v2.py _use_online_compress; the online kernels themselves are
 // off-page, the recurrence is derived in include/ckv.h).
 //
@@ -70,32 +70,57 @@ struct OnlineArgs {
   int pass;
 };
 
-// Running softmax of one channel over the tokens of a group so far; m2 is
-// m * log2(e) rounded to fp32, recomputed from m whenever a slot is loaded.
+// Running softmax of one channel over the tokens of a group so far, kept as
+// m2 = fp32(m * log2(e)) for the running maximum m of s, l and a.
 struct OnlineState {
-  float m, l, a, m2;
+  float m2, l, a;
 
   __device__ __forceinline__ void start(float s, float kv) {
-    m = s;
+    m2 = __fmul_rn(s, kLog2e);
     l = 1.0f;
     a = kv;
-    m2 = __fmul_rn(s, kLog2e);
   }
-  // With s2 = s * log2(e) and w = 2^-|s2 - m2|: a token that raises the
-  // maximum rescales the sums by w (= exp(m_old - s)) and enters with weight
-  // 1 (l = l w + 1, a = a w + kv); any other enters with weight w (= exp(s -
-  // m)): l = 1 w + l, a = kv w + a.  One exponential either way, chosen by
+  // With s2 = fp32(s * log2(e)) and w = 2^-|s2 - m2|: a token that raises the
+  // maximum rescales the sums by c = w (= exp(m_old - s)) and enters with
+  // weight e = 1; any other enters with weight e = w (c = 1).  Then
+  // l = l c + e and a = kv e + (a c).  One exponential either way, chosen by
   // selects so that a warp does not diverge.
   __device__ __forceinline__ void fold(float s, float kv) {
-    const bool up = s > m;
     const float s2 = __fmul_rn(s, kLog2e);
+    const bool up = s2 > m2;
     const float w = ex2(-fabsf(__fsub_rn(s2, m2)));
-    l = __fmaf_rn(up ? l : 1.0f, w, up ? 1.0f : l);
-    a = __fmaf_rn(up ? a : kv, w, up ? kv : a);
-    m = up ? s : m;
+    const float c = up ? w : 1.0f, e = up ? 1.0f : w;
+    l = __fmaf_rn(l, c, e);
+    a = __fmaf_rn(kv, e, __fmul_rn(a, c));
     m2 = up ? s2 : m2;
   }
 };
+
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+  F2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+
+// OnlineState::fold on two channels with packed fp32x2 arithmetic; lane for
+// lane the same operations, so the same bits.
+__device__ __forceinline__ void fold2(OnlineState& q0, OnlineState& q1, F2 s, F2 kv) {
+  const F2 s2 = f2_mul(s, f2_pack(kLog2e, kLog2e));
+  const F2 d = f2_fma(f2_pack(q0.m2, q1.m2), f2_pack(-1.0f, -1.0f), s2);  // s2 - m2, one rounding
+  float d0, d1, t0, t1;
+  f2_unpack(d, d0, d1);
+  f2_unpack(s2, t0, t1);
+  const bool u0 = t0 > q0.m2, u1 = t1 > q1.m2;
+  const float w0 = ex2(-fabsf(d0)), w1 = ex2(-fabsf(d1));
+  const F2 c = f2_pack(u0 ? w0 : 1.0f, u1 ? w1 : 1.0f);
+  const F2 e = f2_pack(u0 ? 1.0f : w0, u1 ? 1.0f : w1);
+  const F2 l = f2_fma(f2_pack(q0.l, q1.l), c, e);
+  const F2 a = f2_fma(kv, e, f2_mul(f2_pack(q0.a, q1.a), c));
+  f2_unpack(l, q0.l, q1.l);
+  f2_unpack(a, q0.a, q1.a);
+  q0.m2 = u0 ? t0 : q0.m2;
+  q1.m2 = u1 ? t1 : q1.m2;
+}
 
 __device__ __forceinline__ void online_token(OnlineState& st, bool first, float s, float kv) {
   if (first) st.start(s, kv);
@@ -109,6 +134,7 @@ struct Raw4;
 template <>
 struct Raw4<float> {
   float4 v;
+  __device__ __forceinline__ F2 pair(int h) const { return h == 0 ? f2_pack(v.x, v.y) : f2_pack(v.z, v.w); }
   __device__ __forceinline__ void from(const uint4& u) { v = make_float4(__uint_as_float(u.x), __uint_as_float(u.y),
                                                                       __uint_as_float(u.z), __uint_as_float(u.w)); }
   __device__ __forceinline__ float get(int j) const { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; }
@@ -116,6 +142,7 @@ struct Raw4<float> {
 template <>
 struct Raw4<__nv_bfloat16> {
   uint2 v;
+  __device__ __forceinline__ F2 pair(int h) const { return f2_from_bf16x2(h == 0 ? v.x : v.y); }
   __device__ __forceinline__ void from(const uint2& u) { v = u; }
   __device__ __forceinline__ float get(int j) const {
     return j == 0 ? bf16lo(v.x) : j == 1 ? bf16hi(v.x) : j == 2 ? bf16lo(v.y) : bf16hi(v.y);
@@ -147,14 +174,14 @@ __device__ __forceinline__ void load_state(const float* st, int hd, int c0, Onli
   const float4 m = *reinterpret_cast<const float4*>(st + c0);
   const float4 l = *reinterpret_cast<const float4*>(st + hd + c0);
   const float4 a = *reinterpret_cast<const float4*>(st + 2 * hd + c0);
-  q[0] = {m.x, l.x, a.x, __fmul_rn(m.x, kLog2e)};
-  q[1] = {m.y, l.y, a.y, __fmul_rn(m.y, kLog2e)};
-  q[2] = {m.z, l.z, a.z, __fmul_rn(m.z, kLog2e)};
-  q[3] = {m.w, l.w, a.w, __fmul_rn(m.w, kLog2e)};
+  q[0] = {m.x, l.x, a.x};
+  q[1] = {m.y, l.y, a.y};
+  q[2] = {m.z, l.z, a.z};
+  q[3] = {m.w, l.w, a.w};
 }
 
 __device__ __forceinline__ void store_state(float* st, int hd, int c0, const OnlineState (&q)[4]) {
-  *reinterpret_cast<float4*>(st + c0) = make_float4(q[0].m, q[1].m, q[2].m, q[3].m);
+  *reinterpret_cast<float4*>(st + c0) = make_float4(q[0].m2, q[1].m2, q[2].m2, q[3].m2);
   *reinterpret_cast<float4*>(st + hd + c0) = make_float4(q[0].l, q[1].l, q[2].l, q[3].l);
   *reinterpret_cast<float4*>(st + 2 * hd + c0) = make_float4(q[0].a, q[1].a, q[2].a, q[3].a);
 }
@@ -234,6 +261,8 @@ __global__ __launch_bounds__(kOnThreads, 4) void online_prefill_kernel(const Onl
       issue(blk + kStages - 1);
       cp_async_wait<kStages - 1>();  // this thread's copies of block blk have landed
       const Raw* src = ring + static_cast<size_t>((blk % kStages) * kTok * 3) * kOnThreads + threadIdx.x;
+      // only a unit's first token can start a group (a unit never crosses one)
+      const bool fresh = blk == 0 && pos0 % 128 == 0;
 #pragma unroll
       for (int d = 0; d < kTok; ++d) {
         const uint32_t t = blk * kTok + d;
@@ -242,10 +271,13 @@ __global__ __launch_bounds__(kOnThreads, 4) void online_prefill_kernel(const Onl
           kv.from(src[(3 * d + 0) * kOnThreads]);
           sc.from(src[(3 * d + 1) * kOnThreads]);
           bias.from(src[(3 * d + 2) * kOnThreads]);
-          const bool first = (pos0 + t) % 128 == 0;
+          if (d == 0 && fresh) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            online_token(q[j], first, score_plus_bias(sc.get(j), bias.get(j)), kv.get(j));
+            for (int j = 0; j < 4; ++j) q[j].start(score_plus_bias(sc.get(j), bias.get(j)), kv.get(j));
+          } else {
+            fold2(q[0], q[1], score_plus_bias2(sc.pair(0), bias.pair(0)), kv.pair(0));
+            fold2(q[2], q[3], score_plus_bias2(sc.pair(1), bias.pair(1)), kv.pair(1));
+          }
           if (a.pass == 0 && token && !(emit && t + 1 == cnt))
             store_zero_chunk<TOut, 4>(out + (static_cast<size_t>(ragged0) + t) * hd + c0);
         }

@@ -262,9 +262,10 @@ int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, vo
 /* compressor_v2.py can keep C128 state online: one slot of 3 * head_dim per
  * request ([slots, 1, 3 * head_dim]) instead of a 128-row page; the online
  * kernels and their plans (generate_online) are off-page, so this is a
- * derivation.  Slot layout, fp32: m | l | a, each head_dim wide: per channel,
- * over the tokens of the current 128-group so far, the running maximum m of
- * s = fp32(score + ape[p % 128]), l = sum exp(s - m) and a = sum kv exp(s - m).
+ * derivation.  Slot layout, fp32: m2 | l | a, each head_dim wide: per
+ * channel, over the tokens of the current 128-group so far, with m the running
+ * maximum of s = fp32(score + ape[p % 128]): m2 = fp32(m * log2(e)),
+ * l = sum exp(s - m) and a = sum kv exp(s - m).
  * A token at position p starts a new group when p % 128 == 0 ((m, l, a) =
  * (s, 1, kv)) and otherwise folds in, rescaling by exp(m_old - m_new) when it
  * raises the maximum; at (p + 1) % 128 == 0 the group's row a / l is emitted,

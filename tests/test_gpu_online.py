@@ -2,7 +2,8 @@
 ckv_compress_online_prefill / _decode) against the oracle.
 
 Bar: unit and decode plans bit-exact; the running maxima of the state
-bit-exact (a maximum of identically rounded scores); emitted rows within
+bit-exact (kept as fp32(m * log2 e), the product of a maximum of identically
+rounded scores); emitted rows within
 2e-6 * max|kv| of the window (fp32) or 1 ulp / that bound (bf16) against the
 whole-history window definition; the same bits on the GPU whether a sequence
 comes as one prefill, in chunks or token by token.
@@ -15,6 +16,8 @@ from compressed_kv_attention_compressplan_gb300 import workloads as wl
 from tests import helpers as H
 
 pytestmark = pytest.mark.gpu
+
+L2E = np.float32(1.4426950408889634)  # log2(e) in fp32: the library's m2 = fp32(m * log2(e))
 
 
 @pytest.fixture(scope="module")
@@ -147,11 +150,14 @@ def test_online_state_and_compact_rows(env):
             o.online_prefill(hd, 1, 0, st64, toks, ape, u)
     st32 = st64.astype(np.float32)
     st64 = st32.astype(np.float64)  # both sides start from the same fp32 values
+    # the library keeps m2 = fp32(m * log2(e)) in place of the maximum m
+    gpu_init = st32.copy()
+    gpu_init[:, :hd] = st32[:, :hd] * L2E
     nq = int(el.sum())
     inp = wl.bits(torch.randn(nq, 2 * hd, generator=g).to(torch.bfloat16)).copy()
     units, (nu, nc), _ = o.plan_online_prefill(rid, sl, el)
     want = o.online_prefill(hd, 1, 0, st64, inp, ape, units, o.OUT_COMPACT, nc)
-    state = torch.from_numpy(st32.copy()).to(dev)
+    state = torch.from_numpy(gpu_init).to(dev)
     status = ckv.new_status(dev)
     counts = torch.tensor([nc, nu, 0, 0], dtype=torch.int32, device=dev)
     out = ckv.compress_online_prefill(hd, state, H.to_torch(inp, 1).to(dev), H.to_torch(ape, 1).to(dev),
@@ -164,7 +170,7 @@ def test_online_state_and_compact_rows(env):
     assert np.abs(got - want).max() <= 4e-6 * scale
     gs = state.cpu().numpy().reshape(B, 3, hd)
     ws = st64.reshape(B, 3, hd)
-    assert (gs[:, 0] == ws[:, 0].astype(np.float32)).all(), "running maxima"
+    assert (gs[:, 0] == ws[:, 0].astype(np.float32) * L2E).all(), "running maxima"
     np.testing.assert_allclose(gs[:, 1], ws[:, 1], rtol=2e-5, atol=0)  # sums of positive weights
     # weighted sums may cancel: bound them by the weight sum times max|kv|
     assert (np.abs(gs[:, 2] - ws[:, 2]) <= 2e-5 * ws[:, 1] * scale).all()
