@@ -133,27 +133,6 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
 
 // ---------------------------------------------------------------- element helpers
 template <typename TIn>
-__device__ __forceinline__ void load4(const TIn* p, float (&v)[4]);
-
-template <>
-__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[4]) {
-  const uint2 u = *reinterpret_cast<const uint2*>(p);
-  v[0] = bf16lo(u.x);
-  v[1] = bf16hi(u.x);
-  v[2] = bf16lo(u.y);
-  v[3] = bf16hi(u.y);
-}
-
-template <>
-__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
-  const float4 u = *reinterpret_cast<const float4*>(p);
-  v[0] = u.x;
-  v[1] = u.y;
-  v[2] = u.z;
-  v[3] = u.w;
-}
-
-template <typename TIn>
 __device__ __forceinline__ void ldg4(const TIn* p, float (&v)[4]);
 
 template <>
