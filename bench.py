@@ -814,6 +814,7 @@ def bench_config(args, name, ws, rank, local):
                   "back_to_back_copies": n}
     line = {"workload": name, **w.describe(), "rows_per_step": b["rows"],
             "rows_per_s": b["rows"] / (float(step_ms.mean()) * 1e-3), "ms_per_step": float(step_ms.mean()),
+            "requests_per_s": w.batch / (float(step_ms.mean()) * 1e-3),
             "step_gbs": b["total"] / (float(step_ms.mean()) * 1e-3) / 1e9,
             "segments_us": {n: float(seg_ms[:, i].mean()) * 1e3 for i, n in enumerate(step.names)},
             "segments_us_min": {n: float(seg_ms[:, i].min()) * 1e3 for i, n in enumerate(step.names)},
