@@ -23,7 +23,8 @@ copied back inside the timed region.
 
 ``--config NAME`` times one workload alone (c4_prefill_small, c4_decode,
 c128_decode, c4_prefill, c128_prefill, the speculative-decoding verify shapes
-c4_prefill_mtp / c128_prefill_mtp, the norm + RoPE + store step on the
+c4_prefill_mtp / c128_prefill_mtp, the C4 prefill over SWA-paged state
+c4_prefill_paged, the norm + RoPE + store step on the
 C128 rows, norm_rope_c128_prefill / norm_rope_c128_decode, and the C128
 workloads through the online state, c128_online_prefill / c128_online_decode;
 ``all`` for each in turn) and prints one line per workload.  ``--impl reference`` times the CPU oracle on the
@@ -279,6 +280,25 @@ class PrefillRunner:
 
     def restore(self):
         self.state.copy_(self.pristine)
+
+
+class PagedPrefillRunner(PrefillRunner):
+    """A prefill over SWA-paged state: the paged planner translates positions through the token maps."""
+
+    def __init__(self, ckv, w: wl.Workload, maps: wl.PagedMaps, dev):
+        super().__init__(ckv, w, dev)
+        self.maps = maps
+        self.r2t = maps.req_to_token.to(dev)
+        self.f2s = maps.full_to_state.to(dev)
+        self.cap_w = ckv.capacity_write_paged(w.ratio, w.batch, w.num_q_tokens, maps.swa_page_size)
+        self.plan_w = torch.empty(max(self.cap_w, 1), 8, dtype=torch.uint8, device=dev)
+
+    def plan(self):
+        m = self.maps
+        self.ckv.plan_prefill_paged(self.w.ratio, self.rid, self.r2t, self.f2s, m.swa_page_size, m.ring_size, self.sl,
+                                    self.el, self.w.num_q_tokens, self.cap_c, self.cap_w, counts=self.counts,
+                                    status=self.status, plan_c=self.plan_c[: self.cap_c],
+                                    plan_w=self.plan_w[: self.cap_w])
 
 
 class DecodeRunner:
@@ -784,10 +804,26 @@ def bench_config(args, name, ws, rank, local):
         return bench_norm_rope(args, name, ws, rank, ckv, dev)
     if name in wl.ONLINE:
         return bench_online(args, name, ws, rank, ckv, dev)
-    w = small_workload(name, args.seed + rank) if args.small else wl.NAMED[name](args.seed + rank)
+    maps = None
+    if name in wl.PAGED:
+        w, maps = wl.PAGED[name](args.seed + rank)
+    else:
+        w = small_workload(name, args.seed + rank) if args.small else wl.NAMED[name](args.seed + rank)
     flush = l2_flush_buffer(dev)
     b = algorithmic_bytes(w)
-    if w.mode == "prefill":
+    if maps is not None:
+        r = PagedPrefillRunner(ckv, w, maps, dev)
+        segs = [("plan_prefill_paged", r.plan), ("pool_prefill", r.pool), ("write", r.write)]
+        r.plan()
+        torch.cuda.synchronize()
+        nw = int(r.counts[1])  # the paged write set (page ends included), from the planner
+        b["write"] = nw * (2 * w.width * elem(w.in_dtype) + 8)
+        # + the extra write records, and the map reads (4 + 8 bytes) of every translated position
+        b["plan"] += 8 * (nw - b["num_w"]) + 12 * (nw + 2 * b["num_c"])
+        b["num_w"] = nw
+        b["total"] = b["plan"] + b["pool"] + b["write"]
+        main_i, main_key = 1, "pool"
+    elif w.mode == "prefill":
         r = PrefillRunner(ckv, w, dev, padded=name.endswith("_mtp"))
         segs = [("plan_prefill", r.plan), ("pool_prefill", r.pool), ("write", r.write)]
         main_i, main_key = (1, "pool") if b["pool"] >= b["write"] else (2, "write")
@@ -919,7 +955,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="step",
-                    help="step (default) | all | " + " | ".join(list(wl.NAMED) + list(wl.NORM_ROPE) + list(wl.ONLINE)))
+                    help="step (default) | all | " + " | ".join(list(wl.NAMED) + list(wl.PAGED) + list(wl.NORM_ROPE) +
+                                                                 list(wl.ONLINE)))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true", help="with --config: scaled-down workloads for profiling")
@@ -936,7 +973,8 @@ def main():
     elif args.config == "step":
         bench_step(args, ws, rank, local)
     else:
-        names = list(wl.NAMED) + list(wl.NORM_ROPE) + list(wl.ONLINE) if args.config == "all" else [args.config]
+        names = (list(wl.NAMED) + list(wl.PAGED) + list(wl.NORM_ROPE) + list(wl.ONLINE) if args.config == "all"
+                 else [args.config])
         for n in names:
             bench_config(args, n, ws, rank, local)
     if ws > 1:

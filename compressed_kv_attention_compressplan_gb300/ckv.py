@@ -201,7 +201,8 @@ def plan_prefill_paged(ratio: int, rid: torch.Tensor, req_to_token: torch.Tensor
                        swa_page_size: int, ring_size: int, seq_lens: torch.Tensor, extend_lens: torch.Tensor,
                        num_q_tokens: int, capacity_c: Optional[int] = None, capacity_w: Optional[int] = None,
                        pad_invalid: bool = False, counts: Optional[torch.Tensor] = None,
-                       status: Optional[torch.Tensor] = None, stream=None):
+                       status: Optional[torch.Tensor] = None, stream=None, plan_c: Optional[torch.Tensor] = None,
+                       plan_w: Optional[torch.Tensor] = None):
     """SWA-paged prefill plans; req_to_token is ``[num_reqs, stride]`` int32, full_to_state int64."""
     batch = rid.numel()
     dev = rid.device
@@ -209,8 +210,10 @@ def plan_prefill_paged(ratio: int, rid: torch.Tensor, req_to_token: torch.Tensor
         capacity_c = capacity_compress(ratio, batch, num_q_tokens)
     if capacity_w is None:
         capacity_w = capacity_write_paged(ratio, batch, num_q_tokens, swa_page_size)
-    plan_c = torch.empty(max(capacity_c, 1), 16, dtype=torch.uint8, device=dev)
-    plan_w = torch.empty(max(capacity_w, 1), 8, dtype=torch.uint8, device=dev)
+    if plan_c is None:
+        plan_c = torch.empty(max(capacity_c, 1), 16, dtype=torch.uint8, device=dev)
+    if plan_w is None:
+        plan_w = torch.empty(max(capacity_w, 1), 8, dtype=torch.uint8, device=dev)
     if counts is None:
         counts = torch.empty(4, dtype=torch.int32, device=dev)
     r2t, stride, nreq, f2s, nfull = _paged_maps(req_to_token, full_to_state)

@@ -208,12 +208,17 @@ def c128_decode(seed: int = 0, batch: int = 512, head_dim: int = 512) -> Workloa
                 None, seed, num_requests_state=batch)
 
 
-def c4_prefill(seed: int = 0, batch: int = 64, head_dim: int = 512, max_prefix: int = 4096,
-               max_extend: int = 4096) -> Workload:
+def c4_prefill_lengths(seed: int = 0, batch: int = 64, max_prefix: int = 4096, max_extend: int = 4096):
+    """(rid, seq_lens, extend_lens) of the C4 prefill workload."""
     pl = torch.randint(0, max_prefix + 1, (batch,), generator=_gen(seed, 1), dtype=torch.int64)
     el = torch.randint(1, max_extend + 1, (batch,), generator=_gen(seed, 5), dtype=torch.int64)
     rid = torch.randperm(batch, generator=_gen(seed, 2))
-    return make("c4_prefill", "prefill", 4, head_dim, torch.bfloat16, torch.bfloat16, TOKEN, rid, pl + el, el,
+    return rid, pl + el, el
+
+
+def c4_prefill(seed: int = 0, batch: int = 64, head_dim: int = 512, **lengths) -> Workload:
+    rid, sl, el = c4_prefill_lengths(seed, batch, **lengths)
+    return make("c4_prefill", "prefill", 4, head_dim, torch.bfloat16, torch.bfloat16, TOKEN, rid, sl, el,
                 seed, num_requests_state=batch)
 
 
@@ -263,6 +268,54 @@ NAMED = {
     "c4_prefill_mtp": c4_prefill_mtp,
     "c128_prefill_mtp": c128_prefill_mtp,
 }
+
+
+# ----------------------------------------------------------------------------- SWA-paged state
+@dataclasses.dataclass
+class PagedMaps:
+    """The token maps of an SWA-paged pool, as the paged planners read them."""
+    swa_page_size: int
+    ring_size: int
+    req_to_token: torch.Tensor   # int32 [num_requests, stride]: full-pool slot of each position
+    full_to_state: torch.Tensor  # int64 [num_full_slots]: SWA slot of each full-pool slot
+    num_pages: int
+
+
+def swa_paged_maps(rid, seq_lens, num_requests: int, swa_page_size: int, ring_size: int, seed: int) -> PagedMaps:
+    """A seeded page-granular allocation: position p of request rid gets a full-pool slot (a seeded
+    permutation) and the SWA slot at offset p % swa_page_size of the request's (p // swa_page_size)-th
+    SWA page; the pages are handed out in seeded random order."""
+    sl = [int(x) for x in seq_lens]
+    stride = max(sl) if sl else 1
+    npages = [(x + swa_page_size - 1) // swa_page_size for x in sl]
+    num_pages = max(1, sum(npages))
+    pages = torch.randperm(num_pages, generator=_gen(seed, 41))
+    num_full = max(1, sum(sl))
+    full = torch.randperm(num_full, generator=_gen(seed, 42))
+    r2t = torch.full((num_requests, stride), -1, dtype=torch.int32)
+    f2s = torch.full((num_full,), -1, dtype=torch.int64)
+    fo = po = 0
+    for r, n, npg in zip([int(x) for x in rid], sl, npages):
+        p = torch.arange(n, dtype=torch.int64)
+        slots = full[fo:fo + n]
+        r2t[r, :n] = slots.to(torch.int32)
+        f2s[slots] = pages[po + p // swa_page_size] * swa_page_size + p % swa_page_size
+        fo += n
+        po += npg
+    return PagedMaps(swa_page_size, ring_size, r2t, f2s, num_pages)
+
+
+def c4_prefill_paged(seed: int = 0, head_dim: int = 512, swa_page_size: int = 128, ring_size: int = 8):
+    """The C4 prefill workload over SWA-paged state (128-token SWA pages, 8-row rings): (Workload, PagedMaps)."""
+    rid, sl, el = c4_prefill_lengths(seed)
+    maps = swa_paged_maps(rid, sl, rid.numel(), swa_page_size, ring_size, seed)
+    w = make("c4_prefill_paged", "prefill", 4, head_dim, torch.bfloat16, torch.bfloat16, TOKEN, rid, sl, el, seed,
+             num_requests_state=1, state_fill="sentinel")
+    w.state = normal((maps.num_pages * ring_size, width_of(4, head_dim)), torch.bfloat16, 1.0, _seed(seed, 14))
+    return w, maps
+
+
+PAGED = {"c4_prefill_paged": c4_prefill_paged}
 
 
 # ----------------------------------------------------------------------------- norm + RoPE + store inputs

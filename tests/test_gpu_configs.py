@@ -113,3 +113,40 @@ def test_decode_workload_full_size(env, name):
     nb = np.setdiff1d(np.arange(w.batch), bnd)
     assert (got[nb].view(np.uint16 if co else np.uint32) == 0).all()
     assert (H.np_bits(state_d).view(np.uint8) == st.view(np.uint8)).all(), "state after decode"
+
+
+def test_paged_prefill_workload_full_size(env):
+    """The C4 prefill workload over SWA-paged state (128-token SWA pages, 8-row
+    rings), in the benchmark's launch configuration: paged plans bit-exact,
+    sampled pooled rows, every zero row, and the state after the write."""
+    o, ckv, dev = env
+    w, m = wl.PAGED["c4_prefill_paged"](0)
+    R, hd, nq = w.ratio, w.head_dim, w.num_q_tokens
+    state_d = w.state.to(dev)
+    status = ckv.new_status(dev)
+    pc, pw, counts = ckv.plan_prefill_paged(R, w.rid.to(dev), m.req_to_token.to(dev), m.full_to_state.to(dev),
+                                            m.swa_page_size, m.ring_size, w.seq_lens.to(dev), w.extend_lens.to(dev),
+                                            nq, status=status)
+    out = ckv.compress_prefill(R, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), pc, pw, counts, ckv.OUT_TOKEN,
+                               w.out_dtype, status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    wc, ww, (nc, nw), _ = o.plan_prefill_paged(R, w.rid, m.req_to_token.numpy(), m.full_to_state.numpy(),
+                                               m.swa_page_size, m.ring_size, w.seq_lens, w.extend_lens)
+    assert counts[:2].tolist() == [nc, nw]
+    assert (pc[:nc].cpu().numpy() == wc).all() and (pw[:nw].cpu().numpy() == ww).all(), "paged plans"
+    st = wl.bits(w.state).copy()
+    inp = wl.bits(w.kv_score)
+    rng = np.random.default_rng(9)
+    sample = np.unique(np.concatenate([rng.choice(nc, min(nc, 256), replace=False), [0, nc - 1]]))
+    want = o.compress_pool_prefill(R, hd, 1, 1, st, inp, wl.bits(w.ape), np.ascontiguousarray(wc[sample]),
+                                   len(sample), nq, o.OUT_COMPACT)
+    f = H.plan_c_fields(wc[sample])
+    kvmax = H.window_kv_absmax(R, hd, st, inp, f["seq_len"], f["ragged_id"], f["buffer_len"], f["read_page_0"],
+                               f["read_page_1"])
+    got = H.np_bits(out)
+    H.assert_pool_close(got[f["ragged_id"]], want, 1, kvmax, "paged sampled records")
+    others = np.setdiff1d(np.arange(nq), H.plan_c_fields(wc)["ragged_id"])
+    assert (got[others] == 0).all(), "non-compress rows"
+    o.compress_write(R, hd, 1, st, inp, ww, nw)
+    assert (H.np_bits(state_d).view(np.uint8) == st.view(np.uint8)).all(), "state after write"

@@ -181,3 +181,20 @@ def test_full_size_inputs(env, name):
     untouched = np.ones(x.cache_rows, bool)
     untouched[stored] = False
     assert (got[untouched] == want[untouched]).all()
+
+
+def test_no_records(env):
+    o, ckv, dev = env
+    hd = 256
+    cache = torch.full((3, hd), 5.0, device=dev)
+    rows = torch.ones(4, hd, device=dev)
+    plan_c = torch.full((4, 16), 0xFF, dtype=torch.uint8, device=dev)  # all invalid
+    counts = torch.tensor([0, 0, 0, 0], dtype=torch.int32, device=dev)
+    status = ckv.new_status(dev)
+    freqs = torch.from_numpy(textbook_freqs(8, 64)).to(dev)
+    w = torch.ones(hd, device=dev)
+    loc = torch.zeros(4, dtype=torch.int64, device=dev)
+    ckv.norm_rope_store_prefill(4, rows, plan_c, counts, w, 1e-6, freqs, loc, cache, status=status)
+    ckv.norm_rope_store_prefill(4, rows, plan_c, None, w, 1e-6, freqs, loc, cache, status=status)
+    torch.cuda.synchronize()
+    assert (cache == 5.0).all() and int(status[0]) == 0

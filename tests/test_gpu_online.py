@@ -271,3 +271,23 @@ def test_full_size_online_decode(env):
     kv_in = H.bf16_to_f32(wl.bits(x.kv_score)[:, :hd])
     kvmax = np.stack([np.maximum(np.abs(kv_in[b]), np.abs(kv_pre[pre_off[b]:pre_off[b + 1]]).max(0)) for b in bnd])
     H.assert_pool_close(got[bnd], want[bnd], 0, kvmax, "online decode boundary rows")
+
+
+def test_online_empty_inputs(env):
+    """Batch 0 and capacity 0: zero counts, nothing launched that touches the state."""
+    o, ckv, dev = env
+    i64 = dict(dtype=torch.int64, device=dev)
+    e = torch.zeros(0, **i64)
+    status = ckv.new_status(dev)
+    units, counts = ckv.plan_online_prefill(e, e, e, 0, capacity_u=4, pad_invalid=True, status=status)
+    torch.cuda.synchronize()
+    assert counts[:2].tolist() == [0, 0] and int(status[0]) == 0
+    assert (units.cpu().numpy() == 0xFF).all()
+    state = torch.full((2, 3 * 128), 7.0, device=dev)
+    kv = torch.zeros(1, 256, dtype=torch.bfloat16, device=dev)
+    ape = torch.zeros(128, 128, dtype=torch.bfloat16, device=dev)
+    ckv.compress_online_prefill(128, state, kv, ape, units, counts, ckv.OUT_COMPACT, out_rows=1, status=status)
+    pd = ckv.plan_online_decode(e, e, status=status)
+    assert pd.shape[0] == 0
+    torch.cuda.synchronize()
+    assert (state == 7.0).all() and int(status[0]) == 0
