@@ -146,8 +146,8 @@ static int64_t legacy_loc(int ratio, int64_t rid, int64_t position) {
  *     s_i = fp32(score_i[c]) + fp32(ape[i][c])          (rounded in fp32)
  *     out[c] = sum_i kv_i[c] * exp(s_i - m) / sum_i exp(s_i - m),  m = max_i s_i
  * entries[i] points at the start of the kv_score row that holds window entry i,
- * or is NULL for an entry that is masked out (C4, first group: the pages set
- * kv = 0 and score = -1e9 there, whose weight exp(-1e9 - m) is exactly 0).
+ * or is NULL for an entry that is masked out (C4, first group: [c4] c4_forward
+ * sets kv = 0 and score = -1e9 there, whose weight exp(-1e9 - m) is exactly 0).
  * C4 columns: entries 0..3 are the previous group, read from the overlap halves
  * (kv at [0,hd), score at [2hd,3hd)); entries 4..7 read the main halves (kv at
  * [hd,2hd), score at [3hd,4hd)).  C128 columns: kv at [0,hd), score at [hd,2hd).

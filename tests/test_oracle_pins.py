@@ -1,4 +1,5 @@
-"""Pins of the CPU oracle against facts the pages and the mathematics fix.
+"""Pins of the CPU oracle against facts that c_plan.cuh, compressor_v2.py,
+c4.cuh and the mathematics fix.
 
 Nothing here compares the oracle with itself: the plan is checked against a
 hand-worked example and a brute-force enumeration of what the windows need,
