@@ -85,24 +85,32 @@ __global__ __launch_bounds__(kNrThreads) void norm_rope_store_kernel(const NormR
   const int hd = 128 * kChunks;
   const int base = hd - a.rope_dim;
   const int half = a.rope_dim / 2;
-  for (uint32_t k = blockIdx.x * (kNrThreads / 32) + (threadIdx.x >> 5); k < n; k += warps_total) {
+  // Each warp walks records k, k + warps_total, ...; the next record's plan
+  // entry is requested before the current record's data, so a record costs
+  // one memory round trip once the loop runs.
+  const uint4* plan = a.decode ? reinterpret_cast<const uint4*>(a.plan_d) : reinterpret_cast<const uint4*>(a.plan_c);
+  const uint4 kNone = make_uint4(kInvalidU32, kInvalidU32, kInvalidU32, kInvalidU32);
+  uint32_t k = blockIdx.x * (kNrThreads / 32) + (threadIdx.x >> 5);
+  uint4 rec = k < n ? __ldg(plan + k) : kNone;
+  for (; k < n; k += warps_total) {
+    const uint32_t kn = k + warps_total;
+    const uint4 cur = rec;
+    rec = kn < n ? __ldg(plan + kn) : kNone;
+    if (cur.x == kInvalidU32) continue;  // an invalid record (both kinds start with seq_len)
     uint64_t row, loc_index;
     int64_t pos;
     bool zero = false;
+    const uint32_t seq_len = cur.x;
     if (a.decode) {
-      const ckv_decode_plan_t P = load_plan_d(a.plan_d + k);
-      if (P.seq_len == kInvalidU32) continue;
       row = k;
       loc_index = k;
-      zero = P.seq_len % static_cast<uint32_t>(a.ratio) != 0;
-      pos = max(static_cast<int64_t>(P.seq_len) - a.ratio, int64_t{0});
+      zero = seq_len % static_cast<uint32_t>(a.ratio) != 0;
+      pos = max(static_cast<int64_t>(seq_len) - a.ratio, int64_t{0});
     } else {
-      const ckv_compress_plan_t P = load_plan_c(a.plan_c + k);
-      if (plan_c_invalid(P)) continue;
-      const uint32_t ragged = P.ragged_bl & CKV_RAGGED_MASK;
+      const uint32_t ragged = cur.y & CKV_RAGGED_MASK;
       row = a.in_layout == CKV_OUT_COMPACT ? k : ragged;
       loc_index = ragged;
-      pos = static_cast<int64_t>(P.seq_len) - a.ratio;
+      pos = static_cast<int64_t>(seq_len) - a.ratio;
     }
     // everything the record needs is requested at once (one memory round trip
     // after the plan record): its row, its cache location, its table row and
@@ -163,6 +171,26 @@ __global__ __launch_bounds__(kNrThreads) void norm_rope_store_kernel(const NormR
   }
 }
 
+// One wave: as many blocks as can be resident at once (the warps then loop).
+template <int kChunks>
+int launch_resident(const NormRopeArgs& a, cudaStream_t stream) {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, norm_rope_store_kernel<kChunks>, kNrThreads, 0) !=
+            cudaSuccess ||
+        nb <= 0) {
+      cudaGetLastError();
+      nb = 1;
+    }
+    per_sm = nb;
+  }
+  const uint32_t warps_per_cta = kNrThreads / 32;
+  uint32_t grid = (a.capacity + warps_per_cta - 1) / warps_per_cta;
+  grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, static_cast<uint32_t>(per_sm * sm_count())));
+  return launch_pdl(norm_rope_store_kernel<kChunks>, dim3(grid), dim3(kNrThreads), 0, stream, a);
+}
+
 int launch_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
   if (a.ratio != 4 && a.ratio != 128) return CKV_ERR_RATIO;
   if (a.head_dim <= 0 || a.head_dim % 128 != 0 || a.head_dim > 1024) return CKV_ERR_HEAD_DIM;
@@ -178,19 +206,15 @@ int launch_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
     return CKV_ERR_POINTER;
   if (a.decode ? !aligned16(a.plan_d) : !aligned16(a.plan_c)) return CKV_ERR_POINTER;
   if (a.d_counts && (reinterpret_cast<uintptr_t>(a.d_counts) & 3u)) return CKV_ERR_POINTER;
-  const uint32_t warps_per_cta = kNrThreads / 32;
-  uint32_t grid = (a.capacity + warps_per_cta - 1) / warps_per_cta;
-  grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 8u * static_cast<uint32_t>(sm_count())));
-  const dim3 g(grid), b(kNrThreads);
   switch (a.head_dim / 128) {
-    case 1: return launch_pdl(norm_rope_store_kernel<1>, g, b, 0, stream, a);
-    case 2: return launch_pdl(norm_rope_store_kernel<2>, g, b, 0, stream, a);
-    case 3: return launch_pdl(norm_rope_store_kernel<3>, g, b, 0, stream, a);
-    case 4: return launch_pdl(norm_rope_store_kernel<4>, g, b, 0, stream, a);
-    case 5: return launch_pdl(norm_rope_store_kernel<5>, g, b, 0, stream, a);
-    case 6: return launch_pdl(norm_rope_store_kernel<6>, g, b, 0, stream, a);
-    case 7: return launch_pdl(norm_rope_store_kernel<7>, g, b, 0, stream, a);
-    default: return launch_pdl(norm_rope_store_kernel<8>, g, b, 0, stream, a);
+    case 1: return launch_resident<1>(a, stream);
+    case 2: return launch_resident<2>(a, stream);
+    case 3: return launch_resident<3>(a, stream);
+    case 4: return launch_resident<4>(a, stream);
+    case 5: return launch_resident<5>(a, stream);
+    case 6: return launch_resident<6>(a, stream);
+    case 7: return launch_resident<7>(a, stream);
+    default: return launch_resident<8>(a, stream);
   }
 }
 
