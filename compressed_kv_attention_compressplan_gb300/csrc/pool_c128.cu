@@ -334,6 +334,22 @@ __device__ __forceinline__ void issue_tile(TIn* kv_s, const TIn* state, const TI
   }
 }
 
+// Issues decode tile n's copies into stage buffer kv_s: page slots 0..126 as
+// two 127-row boxes, entry 127 = the new token's input row (one thread).
+template <typename TIn, int CS>
+__device__ __forceinline__ void issue_decode_tile(TIn* kv_s, uint32_t bar, const CUtensorMap* page_map,
+                                                  const TIn* input, size_t width, int hd, int c0, uint32_t row,
+                                                  int32_t page) {
+  using T = TileCfg<TIn, CS>;
+  mbar_arrive_expect_tx(bar, T::TILE_BYTES);
+  const int y = static_cast<int>(static_cast<int64_t>(page) * 128);
+  tma_box_g2s(smem_addr(kv_s), page_map, c0, y, bar);
+  tma_box_g2s(smem_addr(kv_s + 128 * CS), page_map, hd + c0, y, bar);
+  const TIn* in_row = input + static_cast<size_t>(row) * width;
+  bulk_g2s(smem_addr(kv_s + 127 * CS), in_row + c0, T::SEG_BYTES, bar);
+  bulk_g2s(smem_addr(kv_s + 128 * CS + 127 * CS), in_row + hd + c0, T::SEG_BYTES, bar);
+}
+
 // Decodes and bounds-checks prefill record e.  Invalid (padding) records and
 // records that point outside the state / input return false.
 __device__ __forceinline__ bool prefill_record(const PoolArgs& a, uint32_t e, uint32_t& ragged, int& bl,
@@ -555,8 +571,15 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
 #pragma unroll
       for (int k = 0; k < kScanK; ++k) {
         if (take[k]) {
-          if (rank % stride == first)
-            own[rank / stride] = make_uint2(base + t * kScanK + k, static_cast<uint32_t>(P[k].read_page_0));
+          if (rank % stride == first) {
+            const uint32_t r = base + t * kScanK + k;
+            own[rank / stride] = make_uint2(r, static_cast<uint32_t>(P[k].read_page_0));
+            // the thread that finds this CTA's first tile issues it at once
+            // (stage 0 is free); the producer starts at the second
+            if (rank == first)
+              issue_decode_tile<TIn, CS>(reinterpret_cast<TIn*>(smem), smem_addr(&full_bar[0]), &page_map, input,
+                                         width, hd, c0, r, P[k].read_page_0);
+          }
           ++rank;
         }
       }
@@ -571,8 +594,8 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
   }
 
   if (warp == NC / 32) {
-    // ---------------- producer warp
-    for (uint32_t n = 0; n < items; ++n) {
+    // ---------------- producer warp (decode: tile 0 was issued by the scan)
+    for (uint32_t n = kDecode && items > 0 ? 1u : 0u; n < items; ++n) {
       const int stage = static_cast<int>(n % NS);
       const uint32_t phase = (n / NS) & 1u;
       if (!mbar_wait_bounded(smem_addr(&empty_bar[stage]), phase ^ 1u, kWaitLimitNs)) {
@@ -586,18 +609,9 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
       const uint32_t bar = smem_addr(&full_bar[stage]);
       TIn* kv_s = reinterpret_cast<TIn*>(smem + stage * T::TILE_BYTES);
       if constexpr (kDecode) {
-        // page slots 0..126 as two 127-row boxes; entry 127 = the new token's input row
         const uint2 rp = own[n];
-        const uint32_t b = rp.x;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar, T::TILE_BYTES);
-          const int y = static_cast<int>(static_cast<int64_t>(static_cast<int32_t>(rp.y)) * 128);
-          tma_box_g2s(smem_addr(kv_s), &page_map, c0, y, bar);
-          tma_box_g2s(smem_addr(kv_s + 128 * CS), &page_map, hd + c0, y, bar);
-          const TIn* row = input + static_cast<size_t>(b) * width;
-          bulk_g2s(smem_addr(kv_s + 127 * CS), row + c0, T::SEG_BYTES, bar);
-          bulk_g2s(smem_addr(kv_s + 128 * CS + 127 * CS), row + hd + c0, T::SEG_BYTES, bar);
-        }
+        if (lane == 0)
+          issue_decode_tile<TIn, CS>(kv_s, bar, &page_map, input, width, hd, c0, rp.x, static_cast<int32_t>(rp.y));
       } else {
         const uint32_t e = first + n * stride;
         uint32_t ragged = 0;
