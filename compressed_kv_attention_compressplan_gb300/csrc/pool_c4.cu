@@ -135,8 +135,14 @@ __global__ __launch_bounds__(kC4Threads, 2) void c4_pool_prefill_kernel(const Po
 // Decode: one unit per (row, chunk).  The new token's row is written to its
 // ring slot; at a group boundary the window's first 7 entries come from the
 // ring (none of them is the slot being written) and entry 7 is the new token.
+// The new token's chunk and the ape chunks do not depend on the plan record,
+// so they are requested together with it: a boundary row costs two memory
+// round trips (record + token + ape, then the ring rows), any other row one.
+constexpr int kC4DecodeThreads = 128;  // 128-thread blocks: a batch of 256 rows x 64 chunks covers every SM
+
 template <typename TIn, typename TOut>
-__global__ __launch_bounds__(kC4Threads) void c4_decode_kernel(const PoolArgs a, uint32_t chunks, uint32_t units) {
+__global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolArgs a, uint32_t chunks,
+                                                                     uint32_t units) {
   constexpr int VEC = C4Vec<TIn>::VEC;
   pdl_wait();
   pdl_release();
@@ -154,6 +160,12 @@ __global__ __launch_bounds__(kC4Threads) void c4_decode_kernel(const PoolArgs a,
   TOut* orow = out + static_cast<size_t>(b) * hd + c0;
 
   const ckv_decode_plan_t P = load_plan_d(a.plan_d + b);
+  const TIn* src = input + static_cast<size_t>(b) * width + c0;  // row b of the input always exists
+  const uint4 kv_ovl = ld_stream16(src), kv_main = ld_stream16(src + hd);
+  const uint4 sc_ovl = ld_stream16(src + 2 * hd), sc_main = ld_stream16(src + 3 * hd);
+  uint4 ap[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ap[i] = ld_cached16(ape + static_cast<size_t>(i) * hd + c0);
   if (P.seq_len == kInvalidU32) {
     store_zero_chunk<TOut, VEC>(orow);
     return;
@@ -169,9 +181,6 @@ __global__ __launch_bounds__(kC4Threads) void c4_decode_kernel(const PoolArgs a,
     store_zero_chunk<TOut, VEC>(orow);
     return;
   }
-  const TIn* src = input + static_cast<size_t>(b) * width + c0;
-  const uint4 kv_ovl = ld_stream16(src), kv_main = ld_stream16(src + hd);
-  const uint4 sc_ovl = ld_stream16(src + 2 * hd), sc_main = ld_stream16(src + 3 * hd);
   TIn* dst = state + static_cast<size_t>(P.write_loc) * width + c0;
   st16(dst, kv_ovl);
   st16(dst + hd, kv_main);
@@ -182,9 +191,7 @@ __global__ __launch_bounds__(kC4Threads) void c4_decode_kernel(const PoolArgs a,
     return;
   }
   const int first = P.seq_len == 4 ? 4 : 0;
-  uint4 kv[8], sc[8], ap[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) ap[i] = ld_cached16(ape + static_cast<size_t>(i) * hd + c0);
+  uint4 kv[8], sc[8];
 #pragma unroll
   for (int i = 0; i < 7; ++i) {
     if (i < first) {
@@ -221,11 +228,11 @@ template <typename TIn, typename TOut>
 int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
   constexpr int VEC = C4Vec<TIn>::VEC;
   const uint32_t chunks = static_cast<uint32_t>(a.head_dim / VEC);
-  const uint32_t threads = (kC4Threads / chunks) * chunks;
   const uint64_t units64 = static_cast<uint64_t>(a.capacity) * chunks;
   if (units64 == 0) return CKV_OK;
   if (units64 > 0xFFFFFFFFull) return CKV_ERR_SIZE;
   const uint32_t units = static_cast<uint32_t>(units64);
+  constexpr uint32_t threads = kC4DecodeThreads;
   return launch_pdl(c4_decode_kernel<TIn, TOut>, dim3((units + threads - 1) / threads), dim3(threads), 0, s, a,
                     chunks, units);
 }
