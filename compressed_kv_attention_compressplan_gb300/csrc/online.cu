@@ -7,43 +7,30 @@
 // position order, and keep the state in fp32 between calls, so a sequence
 // folded in one prefill, in chunks or token by token gives the same bits.
 // Work unit of the prefill: one planner unit (one request's tokens inside one
-// 128-group); head_dim / 4 threads own 4 channels each and walk the unit's
-// tokens in order, fed by a per-thread cp.async ring (see RingCfg).
+// 128-group, consecutive rows of the input and of ape); head_dim / 4 threads
+// own 4 channels each and walk the unit's tokens in order, fed from a
+// shared-memory ring that a producer warp fills with bulk copies (see
+// online_prefill_kernel).
 #include <algorithm>
-#include <type_traits>
 
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "launch.h"
 
 namespace ckv {
 namespace {
 
-constexpr int kOnThreads = 256;
-// Each thread streams its own 4-channel slices of the unit's token rows (kv,
-// score) and ape rows into a private ring in shared memory with cp.async:
-// kStages stages of kTok tokens, kStages - 1 of them in flight while the
-// thread folds the oldest.  A thread reads only what it copied itself, so the
-// ring needs no barrier.  Slot (stage, token, k) of thread t sits at
-// ((stage * kTok + token) * 3 + k) * blockDim + t: a warp's accesses are
-// consecutive.
-constexpr int kStages = 4;
-constexpr int kTok = 2;
+constexpr int kOnThreads = 256;  // decode
+// Prefill ring: kOnStages stages of kOnTok tokens; a stage holds the tokens'
+// input rows (kv | score, 2 * head_dim each) followed by their ape rows
+// (head_dim each), one bulk copy for each part.
+constexpr int kOnTok = 7;
+constexpr int kOnStages = 2;
 
 template <typename TIn>
-struct RingCfg {
-  using Raw = typename std::conditional<sizeof(TIn) == 2, uint2, uint4>::type;
-  static constexpr int kBytes = static_cast<int>(sizeof(Raw));
-  static constexpr int SMEM = kStages * kTok * 3 * kOnThreads * kBytes;
-};
-
-template <int BYTES>
-__device__ __forceinline__ void cp_async(void* smem_dst, const void* gsrc) {
-  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
-  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(d), "l"(gsrc), "n"(BYTES) : "memory");
+constexpr int prefill_smem_bytes(int hd) {
+  return kOnStages * kOnTok * 3 * hd * static_cast<int>(sizeof(TIn));
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 struct OnlineArgs {
   int head_dim;
@@ -127,23 +114,21 @@ __device__ __forceinline__ void online_token(OnlineState& st, bool first, float 
   else st.fold(s, kv);
 }
 
-// The raw 4-channel chunk of one row: 8 bytes of bf16 or 16 of fp32, kept
-// unconverted while the loads of several tokens are in flight.
+// The 4-channel chunk of one staged row: 8 bytes of bf16 or 16 of fp32.
 template <typename T>
 struct Raw4;
 template <>
 struct Raw4<float> {
   float4 v;
   __device__ __forceinline__ F2 pair(int h) const { return h == 0 ? f2_pack(v.x, v.y) : f2_pack(v.z, v.w); }
-  __device__ __forceinline__ void from(const uint4& u) { v = make_float4(__uint_as_float(u.x), __uint_as_float(u.y),
-                                                                      __uint_as_float(u.z), __uint_as_float(u.w)); }
+  __device__ __forceinline__ void load(const float* p) { v = *reinterpret_cast<const float4*>(p); }
   __device__ __forceinline__ float get(int j) const { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; }
 };
 template <>
 struct Raw4<__nv_bfloat16> {
   uint2 v;
   __device__ __forceinline__ F2 pair(int h) const { return f2_from_bf16x2(h == 0 ? v.x : v.y); }
-  __device__ __forceinline__ void from(const uint2& u) { v = u; }
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = *reinterpret_cast<const uint2*>(p); }
   __device__ __forceinline__ float get(int j) const {
     return j == 0 ? bf16lo(v.x) : j == 1 ? bf16hi(v.x) : j == 2 ? bf16lo(v.y) : bf16hi(v.y);
   }
@@ -191,103 +176,178 @@ __device__ __forceinline__ void store_quad(TOut* p, const float (&r)[4]) {
   store_row_chunk<TOut, 4>(p, r);
 }
 
+// A planner unit as the prefill kernel uses it.
+struct UnitInfo {
+  uint32_t pos0, ragged0, cnt, orow, flags;
+  int32_t slot;
+  bool late_store;
+};
+
+// Decodes unit record `rec` and decides whether this pass runs it: false for
+// padding, for units that belong to the other pass and for records that point
+// outside the state, the input or the output (those also set `bad`).  The
+// producer and the consumers of a CTA call it on the same records, so they
+// agree on the sequence of staged tokens.
+__device__ __forceinline__ bool unit_runs(const OnlineArgs& a, const uint4& rec, UnitInfo& u, bool& bad) {
+  bad = false;
+  if (rec.x == kInvalidU32) return false;
+  u.pos0 = rec.x;
+  u.ragged0 = rec.y & CKV_RAGGED_MASK;
+  u.cnt = rec.y >> CKV_UNIT_COUNT_SHIFT;
+  u.slot = static_cast<int32_t>(rec.z);
+  u.orow = rec.w & CKV_RAGGED_MASK;
+  u.flags = rec.w >> CKV_UNIT_FLAGS_SHIFT;
+  u.late_store = (u.flags & CKV_UNIT_STORE) && !(u.flags & CKV_UNIT_LOAD) && (u.pos0 % 128) == 0;
+  if (a.pass == 1 && !u.late_store) return false;
+  bool ok = u.slot >= 0 && static_cast<uint64_t>(u.slot) < a.slots && u.cnt >= 1 && u.cnt <= 128 &&
+            u.ragged0 + u.cnt <= a.num_q_tokens && (u.pos0 % 128) + u.cnt <= 128;
+  if ((u.flags & CKV_UNIT_EMIT) && a.out_layout != CKV_OUT_TOKEN) ok = ok && u.orow < a.out_rows;
+  bad = !ok;
+  return ok;
+}
+
+__device__ __forceinline__ uint4 load_unit(const OnlineArgs& a, uint32_t k, uint32_t n) {
+  return k < n ? __ldg(reinterpret_cast<const uint4*>(a.units + k))
+               : make_uint4(kInvalidU32, kInvalidU32, kInvalidU32, kInvalidU32);
+}
+
+// One CTA = head_dim / 4 consumer threads (4 channels each) + one producer
+// warp, persistent over units blockIdx.x, blockIdx.x + gridDim.x, ...  Lane 0
+// of the producer warp streams every unit's tokens, kOnTok per stage, into the
+// kOnStages-stage ring: one bulk copy of the tokens' input rows (consecutive
+// rows) and one of their ape rows (consecutive rows, since a unit never
+// crosses a group), completing the stage's full barrier; the consumers fold
+// the stage's tokens in order and release it through its empty barrier (one
+// arrival per consumer warp).  Each side reads the next unit's record one unit
+// ahead.  Every wait is bounded; on expiry CKV_STATUS_TIMEOUT is set and the
+// CTA stops, after the producer has waited (again bounded) for the copies it
+// issued.
 template <typename TIn, typename TOut>
-__global__ __launch_bounds__(kOnThreads, 4) void online_prefill_kernel(const OnlineArgs a) {
-  using Cfg = RingCfg<TIn>;
-  using Raw = typename Cfg::Raw;
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  Raw* ring = reinterpret_cast<Raw*>(smem_raw);
+__global__ __launch_bounds__(288) void online_prefill_kernel(const OnlineArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kOnStages];
+  __shared__ __align__(8) uint64_t empty_bar[kOnStages];
+  __shared__ volatile int abort_flag;
+  const int hd = a.head_dim;
+  const int tpu = hd / 4;  // consumer threads
+  const int t = threadIdx.x;
+  const size_t width = 2 * static_cast<size_t>(hd);
+  const uint32_t row_bytes = static_cast<uint32_t>(width * sizeof(TIn));
+  const uint32_t ape_bytes = static_cast<uint32_t>(hd * sizeof(TIn));
+  const uint32_t stage_bytes = kOnTok * (row_bytes + ape_bytes);
+  if (t == 0) {
+    for (int s = 0; s < kOnStages; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), static_cast<uint32_t>(tpu / 32));
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
   pdl_wait();  // units, state and input may come from the previous kernels
   pdl_release();
-  const int hd = a.head_dim;
-  const int tpu = hd / 4;                  // threads per unit
-  const int upb = kOnThreads / tpu;        // units per block round
-  const int lu = threadIdx.x / tpu;
-  const int c0 = 4 * (threadIdx.x % tpu);
   const uint32_t n = count_or_capacity(a.d_counts, 1, a.capacity);
   const TIn* input = static_cast<const TIn*>(a.input);
   const TIn* ape = static_cast<const TIn*>(a.ape);
+
+  if (t >= tpu) {
+    // ---------------- producer (lane 0 of the last warp)
+    if (t != tpu) return;
+    uint32_t g = 0;
+    uint4 rec = load_unit(a, blockIdx.x, n);
+    for (uint32_t k = blockIdx.x; k < n && !abort_flag; k += gridDim.x) {
+      const uint4 cur = rec;
+      rec = load_unit(a, k + gridDim.x, n);
+      UnitInfo u;
+      bool bad;
+      if (!unit_runs(a, cur, u, bad)) continue;
+      const TIn* rows = input + static_cast<size_t>(u.ragged0) * width;
+      const TIn* arows = ape + static_cast<size_t>(u.pos0 % 128) * hd;
+      for (uint32_t j = 0; j < u.cnt; j += kOnTok, ++g) {
+        const int stage = static_cast<int>(g % kOnStages);
+        if (!mbar_wait_bounded(smem_addr(&empty_bar[stage]), ((g / kOnStages) & 1u) ^ 1u, kWaitLimitNs)) {
+          status_or(a.d_status, CKV_STATUS_TIMEOUT);
+          abort_flag = 1;
+          break;
+        }
+        if (abort_flag) break;
+        const uint32_t ntok = min(static_cast<uint32_t>(kOnTok), u.cnt - j);
+        const uint32_t bar = smem_addr(&full_bar[stage]);
+        uint8_t* dst = smem + static_cast<size_t>(stage) * stage_bytes;
+        mbar_arrive_expect_tx(bar, ntok * (row_bytes + ape_bytes));
+        bulk_g2s(smem_addr(dst), rows + j * width, ntok * row_bytes, bar);
+        bulk_g2s(smem_addr(dst + kOnTok * row_bytes), arows + static_cast<size_t>(j) * hd, ntok * ape_bytes, bar);
+      }
+    }
+    // the last kOnStages copies issued (each in its own stage) have landed
+    // before the CTA can exit
+    for (uint32_t h = g > kOnStages ? g - kOnStages : 0u; h < g; ++h)
+      mbar_wait_bounded(smem_addr(&full_bar[h % kOnStages]), (h / kOnStages) & 1u, kWaitLimitNs);
+    return;
+  }
+
+  // ---------------- consumers: thread t owns channels c0 .. c0 + 3
+  const int c0 = 4 * t;
+  const int lane = t & 31;
+  const bool token = a.out_layout == CKV_OUT_TOKEN;
   TOut* out = static_cast<TOut*>(a.out);
-  const size_t width = 2 * static_cast<size_t>(hd);
-  for (uint32_t base = blockIdx.x * upb; base < n; base += gridDim.x * upb) {
-    const uint32_t k = base + lu;
-    if (k >= n) continue;
-    const uint4 rec = __ldg(reinterpret_cast<const uint4*>(a.units + k));
-    if (rec.x == kInvalidU32) continue;
-    const uint32_t pos0 = rec.x;
-    const uint32_t ragged0 = rec.y & CKV_RAGGED_MASK;
-    const uint32_t cnt = rec.y >> CKV_UNIT_COUNT_SHIFT;
-    const int32_t slot = static_cast<int32_t>(rec.z);
-    const uint32_t orow = rec.w & CKV_RAGGED_MASK;
-    const uint32_t flags = rec.w >> CKV_UNIT_FLAGS_SHIFT;
-    const bool emit = flags & CKV_UNIT_EMIT;
-    const bool token = a.out_layout == CKV_OUT_TOKEN;
-    const bool late_store = (flags & CKV_UNIT_STORE) && !(flags & CKV_UNIT_LOAD) && (pos0 % 128) == 0;
-    if (a.pass == 1 && !late_store) continue;
-    bool ok = slot >= 0 && static_cast<uint64_t>(slot) < a.slots && cnt >= 1 && cnt <= 128 &&
-              ragged0 + cnt <= a.num_q_tokens && (pos0 % 128) + cnt <= 128;
-    if (emit && !token) ok = ok && orow < a.out_rows;
-    if (!ok) {
-      if (c0 == 0 && a.pass == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+  uint32_t g = 0;
+  uint4 rec = load_unit(a, blockIdx.x, n);
+  for (uint32_t k = blockIdx.x; k < n; k += gridDim.x) {
+    const uint4 cur = rec;
+    rec = load_unit(a, k + gridDim.x, n);
+    UnitInfo u;
+    bool bad;
+    if (!unit_runs(a, cur, u, bad)) {
+      if (bad && c0 == 0 && a.pass == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
       continue;
     }
-    float* st = a.state + static_cast<size_t>(slot) * 3 * hd;
+    const bool emit = u.flags & CKV_UNIT_EMIT;
+    float* st = a.state + static_cast<size_t>(u.slot) * 3 * hd;
     OnlineState q[4];
-    if (flags & CKV_UNIT_LOAD) load_state(st, hd, c0, q);
-    const uint32_t nblk = (cnt + kTok - 1) / kTok;
-    // the unit's first token row and ape row (a unit stays inside one group,
-    // so its ape rows are consecutive); tokens are offsets from these
-    const TIn* urow = input + static_cast<size_t>(ragged0) * width + c0;
-    const TIn* uape = ape + static_cast<size_t>(pos0 % 128) * hd + c0;
-    auto issue = [&](uint32_t blk) {
-      if (blk < nblk) {
-        Raw* dst = ring + static_cast<size_t>((blk % kStages) * kTok * 3) * kOnThreads + threadIdx.x;
-#pragma unroll
-        for (int d = 0; d < kTok; ++d) {
-          const uint32_t t = blk * kTok + d;
-          if (t < cnt) {
-            const TIn* row = urow + t * static_cast<uint32_t>(width);
-            cp_async<Cfg::kBytes>(dst + (3 * d + 0) * kOnThreads, row);
-            cp_async<Cfg::kBytes>(dst + (3 * d + 1) * kOnThreads, row + hd);
-            cp_async<Cfg::kBytes>(dst + (3 * d + 2) * kOnThreads, uape + t * static_cast<uint32_t>(hd));
-          }
-        }
+    if (u.flags & CKV_UNIT_LOAD) load_state(st, hd, c0, q);
+    bool stop = false;
+    for (uint32_t j = 0; j < u.cnt; j += kOnTok, ++g) {
+      const int stage = static_cast<int>(g % kOnStages);
+      if (!mbar_wait_bounded(smem_addr(&full_bar[stage]), (g / kOnStages) & 1u, kWaitLimitNs)) {
+        status_or(a.d_status, CKV_STATUS_TIMEOUT);
+        abort_flag = 1;
+        stop = true;
+        break;
       }
-      cp_async_commit();  // an empty group past the end keeps the count uniform
-    };
+      const TIn* srow = reinterpret_cast<const TIn*>(smem + static_cast<size_t>(stage) * stage_bytes);
+      const TIn* sape = reinterpret_cast<const TIn*>(smem + static_cast<size_t>(stage) * stage_bytes +
+                                                      kOnTok * row_bytes);
 #pragma unroll
-    for (int b = 0; b < kStages - 1; ++b) issue(b);
-    for (uint32_t blk = 0; blk < nblk; ++blk) {
-      issue(blk + kStages - 1);
-      cp_async_wait<kStages - 1>();  // this thread's copies of block blk have landed
-      const Raw* src = ring + static_cast<size_t>((blk % kStages) * kTok * 3) * kOnThreads + threadIdx.x;
-      // only a unit's first token can start a group (a unit never crosses one)
-      const bool fresh = blk == 0 && pos0 % 128 == 0;
-#pragma unroll
-      for (int d = 0; d < kTok; ++d) {
-        const uint32_t t = blk * kTok + d;
-        if (t < cnt) {
+      for (int d = 0; d < kOnTok; ++d) {
+        const uint32_t tt = j + d;
+        if (tt < u.cnt) {
           Raw4<TIn> kv, sc, bias;
-          kv.from(src[(3 * d + 0) * kOnThreads]);
-          sc.from(src[(3 * d + 1) * kOnThreads]);
-          bias.from(src[(3 * d + 2) * kOnThreads]);
-          if (d == 0 && fresh) {
+          kv.load(srow + d * width + c0);
+          sc.load(srow + d * width + hd + c0);
+          bias.load(sape + d * hd + c0);
+          // only a unit's first token can start a group (a unit never crosses one)
+          if (tt == 0 && u.pos0 % 128 == 0) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) q[j].start(score_plus_bias(sc.get(j), bias.get(j)), kv.get(j));
+            for (int c = 0; c < 4; ++c) q[c].start(score_plus_bias(sc.get(c), bias.get(c)), kv.get(c));
           } else {
             fold2(q[0], q[1], score_plus_bias2(sc.pair(0), bias.pair(0)), kv.pair(0));
             fold2(q[2], q[3], score_plus_bias2(sc.pair(1), bias.pair(1)), kv.pair(1));
           }
-          if (a.pass == 0 && token && !(emit && t + 1 == cnt))
-            store_zero_chunk<TOut, 4>(out + (static_cast<size_t>(ragged0) + t) * hd + c0);
+          if (a.pass == 0 && token && !(emit && tt + 1 == u.cnt))
+            store_zero_chunk<TOut, 4>(out + (static_cast<size_t>(u.ragged0) + tt) * hd + c0);
         }
       }
+      // this warp no longer reads the stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
     }
-    if ((flags & CKV_UNIT_STORE) && late_store == (a.pass == 1)) store_state(st, hd, c0, q);
+    if (stop) break;
+    if ((u.flags & CKV_UNIT_STORE) && u.late_store == (a.pass == 1)) store_state(st, hd, c0, q);
     if (emit && a.pass == 0) {
       const float r[4] = {finish(q[0].a, q[0].l), finish(q[1].a, q[1].l), finish(q[2].a, q[2].l),
                           finish(q[3].a, q[3].l)};
-      const size_t row = token ? static_cast<size_t>(ragged0) + cnt - 1 : orow;
+      const size_t row = token ? static_cast<size_t>(u.ragged0) + u.cnt - 1 : u.orow;
       store_quad<TOut>(out + row * hd + c0, r);
     }
   }
@@ -367,30 +427,48 @@ int check_online(const OnlineArgs& a) {
   return CKV_OK;
 }
 
+// Prefill: head_dim / 4 consumer threads + the producer warp; as many CTAs as
+// fit on the GPU at once (at most one per unit).
+template <typename TIn, typename TOut>
+int launch_prefill(const OnlineArgs& a, cudaStream_t s) {
+  auto fn = online_prefill_kernel<TIn, TOut>;
+  const int smem = prefill_smem_bytes<TIn>(a.head_dim);
+  const int threads = a.head_dim / 4 + 32;
+  static bool configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CKV_ERR_LAUNCH;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, prefill_smem_bytes<TIn>(1024)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return CKV_ERR_LAUNCH;
+    }
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    return CKV_ERR_LAUNCH;
+  }
+  const uint32_t grid = std::max<uint32_t>(
+      1, std::min<uint32_t>(a.capacity, static_cast<uint32_t>(per_sm) * static_cast<uint32_t>(sm_count())));
+  return launch_pdl(fn, dim3(grid), dim3(threads), smem, s, a);
+}
+
 template <typename TIn, typename TOut>
 struct PrefillK {
-  static constexpr auto fn = online_prefill_kernel<TIn, TOut>;
-  static constexpr int smem = RingCfg<TIn>::SMEM;
+  static int launch(const OnlineArgs& a, dim3, cudaStream_t s) { return launch_prefill<TIn, TOut>(a, s); }
 };
 template <typename TIn, typename TOut>
 struct DecodeK {
-  static constexpr auto fn = online_decode_kernel<TIn, TOut>;
-  static constexpr int smem = 0;
+  static int launch(const OnlineArgs& a, dim3 grid, cudaStream_t s) {
+    return launch_pdl(online_decode_kernel<TIn, TOut>, grid, dim3(kOnThreads), 0, s, a);
+  }
 };
 
 template <typename KT>
 int launch_one(const OnlineArgs& a, dim3 grid, cudaStream_t s) {
-  if (KT::smem > 48 * 1024) {
-    static bool done = false;  // per instantiation
-    if (!done) {
-      if (cudaFuncSetAttribute(KT::fn, cudaFuncAttributeMaxDynamicSharedMemorySize, KT::smem) != cudaSuccess) {
-        cudaGetLastError();
-        return CKV_ERR_LAUNCH;
-      }
-      done = true;
-    }
-  }
-  return launch_pdl(KT::fn, grid, dim3(kOnThreads), KT::smem, s, a);
+  return KT::launch(a, grid, s);
 }
 
 template <template <typename, typename> class K>
@@ -432,14 +510,11 @@ extern "C" int ckv_compress_online_prefill(int head_dim, int in_dtype, int out_d
   const int rc = check_online(a);
   if (rc || capacity_u == 0) return rc;
   if (!aligned16(units) || (d_counts && (reinterpret_cast<uintptr_t>(d_counts) & 3u))) return CKV_ERR_POINTER;
-  const uint32_t upb = kOnThreads / (head_dim / 4);
-  uint32_t grid = (capacity_u + upb - 1) / upb;
-  grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 8u * static_cast<uint32_t>(sm_count())));
   a.pass = 0;
-  const int rc0 = launch_typed<PrefillK>(a, dim3(grid), reinterpret_cast<cudaStream_t>(stream));
+  const int rc0 = launch_typed<PrefillK>(a, dim3(1), reinterpret_cast<cudaStream_t>(stream));
   if (rc0) return rc0;
   a.pass = 1;
-  return launch_typed<PrefillK>(a, dim3(grid), reinterpret_cast<cudaStream_t>(stream));
+  return launch_typed<PrefillK>(a, dim3(1), reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int ckv_compress_online_decode(int head_dim, int in_dtype, int out_dtype, float* state, uint64_t slots,

@@ -34,6 +34,7 @@
 #include <algorithm>
 #include <cstring>
 
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -59,65 +60,8 @@ struct DecodeCfg : TileCfg<TIn, sizeof(TIn) == 2 ? 64 : 32> {
   static constexpr int SMEM = Base::TILE_BYTES + Base::RED_FLOATS * 4;
 };
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any real copy
-
-// ---------------------------------------------------------------- TMA / mbarrier
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Waits for the phase of parity `parity` to complete, for at most `limit_ns`.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > limit_ns) return false;
-  }
-}
-
-// One bulk global -> shared copy that completes `bytes` of the barrier's
-// transaction count.  dst and src 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
+// ---------------------------------------------------------------- tensor-map copies
+// (mbarrier and one-dimensional bulk-copy helpers: async_copy.cuh)
 // One 2-D tensor-map box (x = column, y = row) -> shared memory.
 __device__ __forceinline__ void tma_box_g2s(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
