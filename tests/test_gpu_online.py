@@ -85,11 +85,13 @@ def test_online_plans_bit_exact(env, case, pad):
     assert (pd.cpu().numpy() == o.plan_online_decode(rid, sl, 7)).all()
 
 
-@pytest.mark.parametrize("in_dt,out_dt", [(1, 0), (0, 0), (1, 1)])
-def test_online_modes_bitwise_and_window_parity(env, in_dt, out_dt):
+# head_dim 128 gives the prefill kernel its smallest CTA (one consumer warp);
+# 1024 with fp32 input its largest ring (288 threads, 168 KB of stages).
+@pytest.mark.parametrize("hd,in_dt,out_dt", [(512, 1, 0), (512, 0, 0), (512, 1, 1), (128, 1, 0), (384, 0, 1),
+                                             (1024, 0, 0), (1024, 1, 0)])
+def test_online_modes_bitwise_and_window_parity(env, hd, in_dt, out_dt):
     o, ckv, dev = env
-    hd = 512
-    rng = np.random.default_rng(3 + in_dt + 2 * out_dt)
+    rng = np.random.default_rng(3 + in_dt + 2 * out_dt + hd)
     nreq = 5
     lens = [int(rng.integers(1, 3 * 128 + 80)) for _ in range(nreq)]
     rids = [int(x) for x in rng.permutation(8)[:nreq]]
