@@ -26,6 +26,7 @@ constexpr int kOnThreads = 256;  // decode
 // (head_dim each), one bulk copy for each part.
 constexpr int kOnTok = 7;
 constexpr int kOnStages = 2;
+constexpr int kOnMaxThreads = 1024 / 4 + 32;  // prefill CTA at the largest head_dim: consumers + producer warp
 
 template <typename TIn>
 constexpr int prefill_smem_bytes(int hd) {
@@ -223,7 +224,7 @@ __device__ __forceinline__ uint4 load_unit(const OnlineArgs& a, uint32_t k, uint
 // CTA stops, after the producer has waited (again bounded) for the copies it
 // issued.
 template <typename TIn, typename TOut>
-__global__ __launch_bounds__(288) void online_prefill_kernel(const OnlineArgs a) {
+__global__ __launch_bounds__(kOnMaxThreads) void online_prefill_kernel(const OnlineArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kOnStages];
   __shared__ __align__(8) uint64_t empty_bar[kOnStages];
