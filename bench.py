@@ -78,7 +78,7 @@ def profiled_traffic(num_c: int):
         per = float(re.search(r"traffic_bytes_per_compress_record: ([0-9.]+)", text).group(1))
         want = re.search(r"source_sha256: ([0-9a-f]+)", text).group(1)
         h = hashlib.sha256()
-        for f in ("pool_c128.cu", "common.cuh"):
+        for f in ("pool_c128.cu", "common.cuh", "async_copy.cuh"):
             h.update(open(os.path.join(ROOT, "compressed_kv_attention_compressplan_gb300", "csrc", f), "rb").read())
         return per * num_c if h.hexdigest() == want else None
     except Exception:
