@@ -446,10 +446,16 @@ int launch_prefill(const OnlineArgs& a, cudaStream_t s) {
     }
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess || per_sm < 1) {
-    cudaGetLastError();
-    return CKV_ERR_LAUNCH;
+  // resident CTAs per SM, per device and head_dim / 128 (the occupancy query is not free on the host)
+  static int per_sm_cache[64][9] = {};
+  const int hi = a.head_dim / 128;
+  int per_sm = dev >= 0 && dev < 64 ? per_sm_cache[dev][hi] : 0;
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess || per_sm < 1) {
+      cudaGetLastError();
+      return CKV_ERR_LAUNCH;
+    }
+    if (dev >= 0 && dev < 64) per_sm_cache[dev][hi] = per_sm;
   }
   const uint32_t grid = std::max<uint32_t>(
       1, std::min<uint32_t>(a.capacity, static_cast<uint32_t>(per_sm) * static_cast<uint32_t>(sm_count())));
