@@ -112,6 +112,23 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _lengths(*ts: Optional[torch.Tensor]) -> int:
+    """Checks the per-request arrays (rid, seq_lens, extend_lens): int64, one
+    dimension, all of one length (the batch), which is returned.  The library
+    reads them as raw int64 arrays, so another dtype would be misread."""
+    batch = None
+    for t in ts:
+        if t is None:
+            continue
+        if t.dtype != torch.int64 or t.dim() != 1:
+            raise ValueError(f"per-request arrays must be 1-D int64 tensors (got {t.dtype}, {t.dim()}-D)")
+        if batch is None:
+            batch = t.numel()
+        elif t.numel() != batch:
+            raise ValueError(f"per-request arrays differ in length ({t.numel()} != {batch})")
+    return batch or 0
+
+
 def _stream(stream=None):
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
@@ -150,7 +167,7 @@ def new_status(device=None) -> torch.Tensor:
 def plan_decode(ratio: int, rid: torch.Tensor, seq_lens: torch.Tensor, plan_d: Optional[torch.Tensor] = None,
                 status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """DecodePlan records ``[batch, 16]`` uint8."""
-    batch = rid.numel()
+    batch = _lengths(rid, seq_lens)
     if plan_d is None:
         plan_d = torch.empty(max(batch, 1), 16, dtype=torch.uint8, device=rid.device)
     _check(load_library().ckv_plan_decode(ratio, _ptr(rid), _ptr(seq_lens), batch, _ptr(plan_d), _ptr(status),
@@ -165,7 +182,7 @@ def plan_prefill(ratio: int, rid: torch.Tensor, seq_lens: torch.Tensor, extend_l
                  status: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Returns ``(plan_c [cap_c,16] u8, plan_w [cap_w,8] u8, counts [4] int32)``; counts stay on the device:
     ``{num_c, num_w, min extend_len, max extend_len}``."""
-    batch = rid.numel()
+    batch = _lengths(rid, seq_lens, extend_lens)
     dev = rid.device
     if capacity_c is None:
         capacity_c = capacity_compress(ratio, batch, num_q_tokens)
@@ -204,7 +221,7 @@ def plan_prefill_paged(ratio: int, rid: torch.Tensor, req_to_token: torch.Tensor
                        status: Optional[torch.Tensor] = None, stream=None, plan_c: Optional[torch.Tensor] = None,
                        plan_w: Optional[torch.Tensor] = None):
     """SWA-paged prefill plans; req_to_token is ``[num_reqs, stride]`` int32, full_to_state int64."""
-    batch = rid.numel()
+    batch = _lengths(rid, seq_lens, extend_lens)
     dev = rid.device
     if capacity_c is None:
         capacity_c = capacity_compress(ratio, batch, num_q_tokens)
@@ -228,7 +245,7 @@ def plan_prefill_paged(ratio: int, rid: torch.Tensor, req_to_token: torch.Tensor
 def plan_decode_paged(ratio: int, rid: torch.Tensor, req_to_token: torch.Tensor, full_to_state: torch.Tensor,
                       swa_page_size: int, ring_size: int, seq_lens: torch.Tensor,
                       status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    batch = rid.numel()
+    batch = _lengths(rid, seq_lens)
     plan_d = torch.empty(max(batch, 1), 16, dtype=torch.uint8, device=rid.device)
     r2t, stride, nreq, f2s, nfull = _paged_maps(req_to_token, full_to_state)
     _check(load_library().ckv_plan_decode_paged(ratio, _ptr(rid), r2t, stride, nreq, f2s, nfull, swa_page_size,
@@ -311,7 +328,7 @@ def plan_online_prefill(rid: torch.Tensor, seq_lens: torch.Tensor, extend_lens: 
                         units: Optional[torch.Tensor] = None, counts: Optional[torch.Tensor] = None,
                         status: Optional[torch.Tensor] = None, stream=None):
     """Returns ``(units [cap_u, 16] u8, counts [4] int32)``; counts = {num_c, num_units, min el, max el}."""
-    batch = rid.numel()
+    batch = _lengths(rid, seq_lens, extend_lens)
     if capacity_u is None:
         capacity_u = capacity_online_units(batch, num_q_tokens)
     if units is None:
@@ -328,7 +345,7 @@ def plan_online_prefill(rid: torch.Tensor, seq_lens: torch.Tensor, extend_lens: 
 def plan_online_decode(rid: torch.Tensor, seq_lens: torch.Tensor, slot_offset: int = 0,
                        plan_d: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
                        stream=None) -> torch.Tensor:
-    batch = rid.numel()
+    batch = _lengths(rid, seq_lens)
     if plan_d is None:
         plan_d = torch.empty(max(batch, 1), 16, dtype=torch.uint8, device=rid.device)
     _check(load_library().ckv_plan_online_decode(_ptr(rid), _ptr(seq_lens), batch, slot_offset, _ptr(plan_d),

@@ -82,3 +82,20 @@ def test_argument_errors_are_returned_before_any_launch(lib):
                                            None) == -4
     assert lib.ckv_plan_online_prefill(None, None, None, 2000, 0, 0, 0, 0, None, vp(16), None, None) == -3
     assert lib.ckv_error_string(-4) != lib.ckv_error_string(0)
+
+
+def test_binding_rejects_wrong_per_request_arrays():
+    """rid / seq_lens / extend_lens reach the library as raw int64 arrays: the
+    binding must refuse other dtypes and arrays of different lengths."""
+    import torch
+
+    from compressed_kv_attention_compressplan_gb300 import ckv
+
+    i64 = torch.arange(5, dtype=torch.int64)
+    assert ckv._lengths(i64, i64.clone(), None) == 5
+    with pytest.raises(ValueError):
+        ckv._lengths(i64.to(torch.int32), i64)
+    with pytest.raises(ValueError):
+        ckv._lengths(i64, torch.arange(4, dtype=torch.int64))
+    with pytest.raises(ValueError):
+        ckv._lengths(i64.view(5, 1))
