@@ -157,3 +157,138 @@ def test_decode_step_replayed_from_a_graph(env, ratio):
         nb = np.setdiff1d(np.arange(batch), bnd)
         assert (got[nb].view(np.uint32) == 0).all()
         assert (H.np_bits(state).view(np.uint8) == st.view(np.uint8)).all(), "graph replay: state after decode"
+
+
+def _replay_matches_eager(step, restore, outputs, mixes, load):
+    """Captures `step` once; for every input mix, the graph replay leaves
+    `outputs` bit-identical to an eager call of `step` on the same inputs
+    (`restore` resets the state, outputs[0]; the other outputs start at zero)."""
+    g = torch.cuda.CUDAGraph()
+    step()  # eager once: first-call set-up happens outside the capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        step()
+    for m in mixes:
+        load(m)
+        restore()
+        for t in outputs[1:]:
+            t.zero_()
+        step()
+        torch.cuda.synchronize()
+        eager = [t.clone() for t in outputs]
+        restore()
+        for t in outputs[1:]:
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(eager, outputs):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+def test_online_steps_replayed_from_a_graph(env):
+    """The online C128 state: plan + fold (two launches) for a prefill, and the
+    decode fold, captured once and replayed on new length mixes."""
+    o, ckv, dev = env
+    hd, batch, nq = 256, 10, 700
+    rng = np.random.default_rng(91)
+    g = torch.Generator().manual_seed(92)
+    slots = batch + 4
+    init = torch.randn(slots, 3 * hd, generator=g)
+    init[:, hd:2 * hd] = 1.0 + init[:, hd:2 * hd].abs()  # weight sums are >= 1
+    init = init.to(dev)
+    state = init.clone()
+    ape = (torch.randn(128, hd, generator=g) * 0.5).to(torch.bfloat16).to(dev)
+    i64 = dict(dtype=torch.int64, device=dev)
+    rid, sl, el = torch.zeros(batch, **i64), torch.zeros(batch, **i64), torch.zeros(batch, **i64)
+    kv = torch.zeros(nq, 2 * hd, dtype=torch.bfloat16, device=dev)
+    cap_u = ckv.capacity_online_units(batch, nq)
+    cap_c = ckv.capacity_compress(128, batch, nq)
+    units = torch.empty(cap_u, 16, dtype=torch.uint8, device=dev)
+    counts = torch.empty(4, dtype=torch.int32, device=dev)
+    out = torch.empty(cap_c, hd, dtype=torch.float32, device=dev)
+    status = ckv.new_status(dev)
+    mixes = []
+    for el_m in _compositions(rng, nq, batch, 3):
+        pl_m = rng.integers(0, 400, batch)
+        mixes.append((torch.from_numpy(rng.permutation(slots)[:batch].astype(np.int64)),
+                      torch.from_numpy(pl_m + el_m), torch.from_numpy(el_m),
+                      torch.randn(nq, 2 * hd, generator=g).to(torch.bfloat16)))
+
+    def load(m):
+        for dst, src in zip((rid, sl, el, kv), m):
+            dst.copy_(src)
+
+    def step():
+        ckv.plan_online_prefill(rid, sl, el, nq, 0, cap_u, pad_invalid=True, units=units, counts=counts,
+                                status=status)
+        ckv.compress_online_prefill(hd, state, kv, ape, units, counts, ckv.OUT_COMPACT, out=out, status=status)
+
+    load(mixes[0])
+    _replay_matches_eager(step, lambda: state.copy_(init), [state, out], mixes, load)
+    assert int(status[0]) == 0
+
+    # decode
+    plan_d = torch.empty(batch, 16, dtype=torch.uint8, device=dev)
+    kvd = torch.zeros(batch, 2 * hd, dtype=torch.bfloat16, device=dev)
+    outd = torch.empty(batch, hd, dtype=torch.float32, device=dev)
+    dmixes = []
+    for k in range(3):
+        sl_m = rng.integers(1, 3000, batch)
+        sl_m[: 3 + k] = 128 * rng.integers(1, 20, 3 + k)
+        dmixes.append((torch.from_numpy(rng.permutation(slots)[:batch].astype(np.int64)), torch.from_numpy(sl_m),
+                       torch.randn(batch, 2 * hd, generator=g).to(torch.bfloat16)))
+
+    def dload(m):
+        for dst, src in zip((rid, sl, kvd), m):
+            dst.copy_(src)
+
+    def dstep():
+        ckv.plan_online_decode(rid, sl, 0, plan_d=plan_d, status=status)
+        ckv.compress_online_decode(hd, state, kvd, ape, plan_d, out=outd, status=status)
+
+    dload(dmixes[0])
+    _replay_matches_eager(dstep, lambda: state.copy_(init), [state, outd], dmixes, dload)
+    assert int(status[0]) == 0
+
+
+def test_norm_rope_store_replayed_from_a_graph(env):
+    """Decode, then RMSNorm + RoPE + store of its rows into a bf16 cache,
+    captured once and replayed on new decode batches."""
+    o, ckv, dev = env
+    ratio, hd, rope, batch = 128, 512, 64, 64
+    rng = np.random.default_rng(93)
+    mixes = []
+    for k in range(3):
+        sl_m = rng.integers(1, 3000, batch)
+        sl_m[: 10 + k] = 128 * rng.integers(1, 20, 10 + k)
+        w = wl.random_decode(ratio, hd, torch.bfloat16, torch.float32, sl_m, seed=94 + k, num_requests_state=80)
+        mixes.append((w.rid, w.seq_lens, w.kv_score, w.state,
+                      torch.from_numpy(rng.permutation(2 * batch)[:batch].astype(np.int64))))
+    w0 = wl.random_decode(ratio, hd, torch.bfloat16, torch.float32, mixes[0][1], seed=94, num_requests_state=80)
+    rid, sl, kv = w0.rid.to(dev), w0.seq_lens.to(dev), w0.kv_score.to(dev)
+    state0 = w0.state.to(dev)
+    state = state0.clone()
+    ape = w0.ape.to(dev)
+    loc = torch.zeros(batch, dtype=torch.int64, device=dev)
+    g = torch.Generator().manual_seed(95)
+    weight = (1.0 + 0.1 * torch.randn(hd, generator=g)).to(dev)
+    pos = torch.arange(4096, dtype=torch.float64)[:, None]
+    inv = 10000.0 ** (-torch.arange(0, rope, 2, dtype=torch.float64) / rope)
+    ang = pos * inv[None, :]
+    freqs = torch.stack([ang.cos(), ang.sin()], dim=-1).to(torch.float32).contiguous().to(dev)
+    cache = torch.zeros(2 * batch, hd, dtype=torch.bfloat16, device=dev)
+    plan_d = torch.empty(batch, 16, dtype=torch.uint8, device=dev)
+    rows = torch.empty(batch, hd, dtype=torch.float32, device=dev)
+    status = ckv.new_status(dev)
+
+    def load(m):
+        for dst, src in zip((rid, sl, kv, state0, loc), m):
+            dst.copy_(src)
+
+    def step():
+        ckv.plan_decode(ratio, rid, sl, plan_d, status)
+        ckv.compress_decode(ratio, hd, state, kv, ape, plan_d, torch.float32, out=rows, status=status)
+        ckv.norm_rope_store_decode(ratio, rows, plan_d, weight, 1e-6, freqs, loc, cache, status=status)
+
+    _replay_matches_eager(step, lambda: (state.copy_(state0), cache.zero_()), [state, rows, cache], mixes, load)
+    assert int(status[0]) == 0
