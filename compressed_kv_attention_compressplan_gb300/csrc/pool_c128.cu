@@ -14,7 +14,8 @@
 // 128 entries are consecutive rows of one tensor (a prefill window that lies
 // in the extend; the 127 page slots of a decode window) the tile is two 2-D
 // tensor-map boxes (kv slice, score slice); a prefill window that starts in the
-// state is gathered with 256 one-dimensional bulk copies, one per row segment.  The arithmetic then reads shared
+// state is two row ranges (page slots 0 .. buffer_len-1, then input rows), each
+// copied as a few boxes of 64, 16, 4 and 1 rows.  The arithmetic then reads shared
 // memory with 8 groups of 16 consecutive entries x CS/4 channel quads: pass 1
 // forms the scores and the exact per-channel maximum, pass 2 the group sums of
 // weights and weighted kv, pass 3 the fixed pairwise tree over the 8 groups.
@@ -261,21 +262,41 @@ __device__ __forceinline__ void load_ape_regs(const TIn* ape, int hd, int c0, in
   for (int k = 0; k < 16; ++k) ldg4x2<TIn>(ape + static_cast<size_t>(16 * g + k) * hd + c0 + cq, ape_r[k]);
 }
 
-// Issues the 256 bulk copies of one tile (called by all 32 lanes of a warp).
-template <typename TIn, int CS_>
-__device__ __forceinline__ void issue_tile(TIn* kv_s, const TIn* state, const TIn* input, size_t width, int hd,
-                                           int c0, uint32_t ragged, int bl, int64_t rp0, uint32_t bar, int lane) {
-  using Cfg = TileCfg<TIn, CS_>;
-  constexpr int CS = CS_;
+// Tensor maps for prefill windows that start in the state: the state and the
+// input, each with boxes of gather_height(k) rows x one channel slice.  A
+// row range of n < 128 rows then takes at most 10 boxes (64, 16 x 3, 4 x 3,
+// 1 x 3) per half: the copy engine handles a handful of operations per tile
+// instead of one per row.
+__host__ __device__ constexpr int gather_height(int k) { return 64 >> (2 * k); }  // 64, 16, 4, 1
+
+struct GatherMaps {
+  CUtensorMap state[4];
+  CUtensorMap input[4];
+};
+
+// Issues the copies of one prefill tile whose window starts in the state (one
+// thread): entries 0 .. bl-1 are page rows y_state .. y_state+bl-1, entries
+// bl .. 127 input rows y_input .. y_input+127-bl.
+template <typename TIn, int CS>
+__device__ __forceinline__ void issue_gather(TIn* kv_s, const GatherMaps& gm, int hd, int c0, int y_state,
+                                             int y_input, int bl, uint32_t bar) {
   TIn* sc_s = kv_s + 128 * CS;
+  int e = 0;
+  auto range = [&](const CUtensorMap* maps, int y, int n) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = lane + 32 * k;
-    const TIn* row = i < bl ? state + (static_cast<size_t>(rp0) * 128 + i) * width
-                            : input + (static_cast<size_t>(ragged) + i - 127) * width;
-    bulk_g2s(smem_addr(kv_s + i * CS), row + c0, Cfg::SEG_BYTES, bar);
-    bulk_g2s(smem_addr(sc_s + i * CS), row + hd + c0, Cfg::SEG_BYTES, bar);
-  }
+    for (int k = 0; k < 4; ++k) {
+      const int h = gather_height(k);
+      while (n >= h) {
+        tma_box_g2s(smem_addr(kv_s + e * CS), &maps[k], c0, y, bar);
+        tma_box_g2s(smem_addr(sc_s + e * CS), &maps[k], hd + c0, y, bar);
+        e += h;
+        y += h;
+        n -= h;
+      }
+    }
+  };
+  range(gm.state, y_state, bl);
+  range(gm.input, y_input, 128 - bl);
 }
 
 // Issues decode tile n's copies into stage buffer kv_s: page slots 0..126 as
@@ -420,7 +441,7 @@ __device__ __forceinline__ bool group_any(int grp, int n, bool pred) {
 template <typename TIn, typename TOut, int CS, int NS, int NG, bool kDecode>
 __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) void c128_persistent_kernel(
     const PoolArgs a, uint32_t slices, const __grid_constant__ CUtensorMap in_map,
-    const __grid_constant__ CUtensorMap page_map) {
+    const __grid_constant__ CUtensorMap page_map, const __grid_constant__ GatherMaps gather) {
   using T = TileCfg<TIn, CS>;
   using Cfg = PersistCfg<TIn, CS, NS, NG, kDecode>;
   constexpr int NCG = Cfg::NCG;
@@ -464,7 +485,11 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
   const int cq = 4 * q;
   F2 ape_r[16][2];
   // the tensor map is a kernel parameter: fetch its descriptor while the plan is scanned
-  if (warp == NC / 32 && lane == 0) prefetch_map(kDecode ? &page_map : &in_map);
+  if (warp == NC / 32) {
+    if (lane == 0) prefetch_map(kDecode ? &page_map : &in_map);
+    if (!kDecode && lane >= 1 && lane <= 8)
+      prefetch_map(lane <= 4 ? &gather.state[lane - 1] : &gather.input[lane - 5]);
+  }
 
   pdl_wait();  // everything below may read what the previous kernel wrote
   pdl_release();
@@ -572,8 +597,9 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
               tma_box_g2s(smem_addr(kv_s), &in_map, c0, static_cast<int>(ragged) - 127, bar);
               tma_box_g2s(smem_addr(kv_s + 128 * CS), &in_map, hd + c0, static_cast<int>(ragged) - 127, bar);
             }
-          } else {
-            issue_tile<TIn, CS>(kv_s, state, input, width, hd, c0, ragged, bl, rp0, bar, lane);
+          } else if (lane == 0) {
+            issue_gather<TIn, CS>(kv_s, gather, hd, c0, static_cast<int>(rp0 * 128),
+                                  static_cast<int>(ragged) - 127 + bl, bl, bar);
           }
         }
       }
@@ -813,14 +839,26 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
   // one persistent CTA per SM; every CTA serves one channel slice
   const uint32_t per_slice = std::max<uint32_t>(
       1, std::min<uint32_t>(static_cast<uint32_t>(sm_count()) / slices, std::max<uint32_t>(a.capacity, 1)));
+  // tensor-map row coordinates are 32-bit
+  if (a.state_rows > 0x7FFFFFFFull) return CKV_ERR_SIZE;
   alignas(64) CUtensorMap in_map;
+  alignas(64) GatherMaps gather;
   memset(&in_map, 0, sizeof in_map);
+  memset(&gather, 0, sizeof gather);
   if (a.num_q_tokens > 0) {
     rc = make_map(&in_map, a.input, a.in_dtype, 2ull * a.head_dim, a.num_q_tokens, CS, 128);
+    for (int k = 0; k < 4 && !rc; ++k)
+      rc = make_map(&gather.input[k], a.input, a.in_dtype, 2ull * a.head_dim, a.num_q_tokens, CS,
+                    gather_height(k));
+    if (rc) return rc;
+  }
+  if (a.state_rows > 0) {
+    for (int k = 0; k < 4 && !rc; ++k)
+      rc = make_map(&gather.state[k], a.state, a.in_dtype, 2ull * a.head_dim, a.state_rows, CS, gather_height(k));
     if (rc) return rc;
   }
   return launch_pdl(c128_persistent_kernel<TIn, TOut, CS, NS, 1, false>, dim3(per_slice * slices), dim3(Cfg::THREADS),
-                    Cfg::SMEM, s, a, slices, in_map, in_map);
+                    Cfg::SMEM, s, a, slices, in_map, in_map, gather);
 }
 
 // Persistent decode tiles: kDecCS channels (bf16; half for fp32) x 127 page
@@ -848,7 +886,7 @@ int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
     rc = opt_in_smem(c128_persistent_kernel<TIn, TOut, PCS, kDecNS, kDecNG, true>, Cfg::SMEM, configured_p);
     if (rc) return rc;
     return launch_pdl(c128_persistent_kernel<TIn, TOut, PCS, kDecNS, kDecNG, true>, dim3(per_slice * pslices),
-                      dim3(Cfg::THREADS), Cfg::SMEM, s, a, pslices, page_map, page_map);
+                      dim3(Cfg::THREADS), Cfg::SMEM, s, a, pslices, page_map, page_map, GatherMaps{});
   }
   // very large batches: one CTA per (row, slice)
   constexpr int CS = DecodeCfg<TIn>::CS;
