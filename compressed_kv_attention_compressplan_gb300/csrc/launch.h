@@ -2,6 +2,7 @@
 // translation units (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only; the encoder is fetched from the driver at run time)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -31,6 +32,12 @@ struct PoolArgs {
 };
 
 int sm_count();
+
+// Encodes a tiled tensor map of `rank` dimensions (dims[0] innermost; strides
+// in bytes for dims 1 .. rank-1; box extents per dimension) over `base`, of
+// dtype CKV_F32 / CKV_BF16, no swizzle, no fill.  CKV_OK or CKV_ERR_LAUNCH.
+int encode_tensor_map(CUtensorMap* map, int dtype, uint32_t rank, const void* base, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box);
 
 int launch_c4_pool_prefill(const PoolArgs& a, cudaStream_t s);
 int launch_c4_decode(const PoolArgs& a, cudaStream_t s);

@@ -777,39 +777,14 @@ __global__ __launch_bounds__(DecodeCfg<TIn>::THREADS, 6) void c128_decode_kernel
 }
 
 // ---------------------------------------------------------------- tensor maps
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encoder() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
 // A [rows, cols] row-major tensor read in boxes of [box_rows, box_cols].
 int make_map(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uint64_t rows, uint32_t box_cols,
              uint32_t box_rows) {
-  EncodeTiledFn fn = encoder();
-  if (fn == nullptr) return CKV_ERR_LAUNCH;
   const uint64_t esz = dtype == CKV_BF16 ? 2 : 4;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * esz};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, dtype == CKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? CKV_OK : CKV_ERR_LAUNCH;
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t strides[1] = {cols * esz};
+  const uint32_t box[2] = {box_cols, box_rows};
+  return encode_tensor_map(map, dtype, 2, base, dims, strides, box);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -921,6 +896,45 @@ int dispatch(const PoolArgs& a, cudaStream_t s) {
 }  // namespace
 
 int launch_c128_pool_prefill(const PoolArgs& a, cudaStream_t s) { return dispatch<false>(a, s); }
+
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+}  // namespace
+
+int encode_tensor_map(CUtensorMap* map, int dtype, uint32_t rank, const void* base, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box) {
+  EncodeTiledFn fn = encoder();
+  if (fn == nullptr || rank < 1 || rank > 5) return CKV_ERR_LAUNCH;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], estr[5];
+  for (uint32_t i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    estr[i] = 1;
+    if (i + 1 < rank) st[i] = strides_bytes[i];
+  }
+  const CUresult r = fn(map, dtype == CKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                        rank, const_cast<void*>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CKV_OK : CKV_ERR_LAUNCH;
+}
 int launch_c128_decode(const PoolArgs& a, cudaStream_t s) { return dispatch<true>(a, s); }
 
 }  // namespace ckv

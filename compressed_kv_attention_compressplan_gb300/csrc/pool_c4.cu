@@ -9,25 +9,39 @@
 // does not exist and entries 0..3 are left out (c4.cuh sets kv = 0 and
 // score = -1e9 there, which gives them weight exactly 0).
 //
-// Mapping: a "unit" is (event, 16-byte chunk of channels).  A thread owns one
-// chunk (8 bf16 or 4 fp32 channels) for the whole grid-stride loop, so the
-// ape slice it reads stays in L1; per event it issues 16 independent 16-byte
-// loads (kv and score of 8 entries) before any arithmetic.  The window is
-// small enough that the fp32 safe softmax runs entirely in registers.
+// Prefill: a producer warp stages each record's window in shared memory with
+// two tensor-map copies (see c4_pool_prefill_staged_kernel); consumer threads
+// own 16-byte channel chunks (8 bf16 or 4 fp32 channels).  Decode: one thread
+// per (row, chunk) with direct loads.  The window is small enough that the
+// fp32 safe softmax runs entirely in registers.
 #include <algorithm>
+#include <cstring>
 
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "launch.h"
 
 namespace ckv {
 namespace {
 
-constexpr int kC4Threads = 256;
-
 template <typename TIn>
 struct C4Vec {
   static constexpr int VEC = 16 / static_cast<int>(sizeof(TIn));  // channels per 16-byte chunk
 };
+
+// One 4-D tensor-map box (channel 0, block q0, both parts, rows from `row`)
+// -> shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_box4_g2s(uint32_t dst, const CUtensorMap* map, int q0, int row, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(q0), "r"(0), "r"(row), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 
 // The C4 window pool for VEC channels.  Entries below `first` are masked.
 // (Scalar form: with 16 kv/score vectors live, the packed fp32x2 form of the
@@ -55,80 +69,261 @@ __device__ __forceinline__ void c4_pool_chunk(const uint4 (&kv)[8], const uint4 
   }
 }
 
-template <typename TIn, typename TOut>
-__global__ __launch_bounds__(kC4Threads, 2) void c4_pool_prefill_kernel(const PoolArgs a, uint32_t chunks,
-                                                                     uint32_t units) {
-  constexpr int VEC = C4Vec<TIn>::VEC;
-  const int hd = a.head_dim;
-  const size_t width = 4 * static_cast<size_t>(hd);
-  const TIn* state = static_cast<const TIn*>(a.state);
-  const TIn* input = static_cast<const TIn*>(a.input);
-  const TIn* ape = static_cast<const TIn*>(a.ape);
-  TOut* out = static_cast<TOut*>(a.out);
-  const bool token = a.out_layout == CKV_OUT_TOKEN;
+// Prefill, staged by the TMA engine.  A C4 row, | kv-overlap | kv |
+// score-overlap | score |, is viewed as a 4-D tensor (channel within a block
+// of c4_block(hd) channels, block within a part -- the overlap quarter
+// then the main quarter, part -- kv or score, row), so that the overlap
+// halves of four consecutive rows (window entries 0..3) or their main halves
+// (entries 4..7) are ONE box: a record whose window lies in the input is two
+// copies.  Entries held in the ring come from the state through the same view
+// (a box of 4 rows when a whole group is in the state, else one row at a
+// time).  A producer warp issues the copies of kC4Recs(hd) consecutive
+// records per stage into a ring; the window of record r of a stage sits at
+// [entry][kv | score][head_dim] and consumer thread t owns 16-byte channel
+// chunk t % chunks of record t / chunks, running the same c4_pool_chunk as the
+// other C4 kernels (the rows are bit-identical to theirs).  Pseudo-record
+// num_c (token layout) zeroes the rows after the last compress row.
+constexpr int kC4StageBudget = 192 * 1024;  // ring bytes per CTA
 
+// Channels per block of the 4-D view: it must divide head_dim (a multiple of
+// 128) and stay within a box's 256-element limit.
+__host__ __device__ constexpr int c4_block(int hd) { return hd % 256 == 0 ? 256 : 128; }
+
+template <typename TIn>
+struct C4Stage {
+  __host__ __device__ static int chunks(int hd) { return hd / C4Vec<TIn>::VEC; }
+  // records per stage: enough that a stage keeps 256 consumer threads busy
+  __host__ __device__ static int recs(int hd) { return chunks(hd) >= 256 ? 1 : 256 / chunks(hd); }
+  __host__ __device__ static int active(int hd) { return recs(hd) * chunks(hd); }
+  // whole warps: the producer must be one warp of its own
+  __host__ __device__ static int consumers(int hd) { return (active(hd) + 31) / 32 * 32; }
+  __host__ __device__ static uint32_t bytes(int hd) {
+    return static_cast<uint32_t>(recs(hd)) * 16u * static_cast<uint32_t>(hd) * sizeof(TIn);
+  }
+  __host__ __device__ static int stages(int hd) {
+    const int n = kC4StageBudget / static_cast<int>(bytes(hd));
+    return n < 2 ? 2 : n > 8 ? 8 : n;
+  }
+};
+
+// The four views: input and state, boxes of 4 rows and of 1 row.
+struct C4Maps {
+  CUtensorMap in4, in1, st4, st1;
+};
+
+// A compress record as the staged kernel uses it (false: padding, or a record
+// pointing outside the state / input, which also sets `bad`).
+struct C4Rec {
+  uint32_t ragged;
+  int bl, first;
+  int64_t rp0, rp1;
+};
+
+__device__ __forceinline__ ckv_compress_plan_t c4_load_record(const PoolArgs& a, uint32_t e, uint32_t num_c) {
+  if (e < num_c) return load_plan_c(a.plan_c + e);
+  ckv_compress_plan_t P;
+  P.seq_len = kInvalidU32;
+  P.ragged_bl = kInvalidU32;
+  P.read_page_0 = P.read_page_1 = -1;
+  return P;
+}
+
+__device__ __forceinline__ bool c4_record(const PoolArgs& a, const ckv_compress_plan_t& P, C4Rec& r, bool& bad) {
+  bad = false;
+  if (plan_c_invalid(P)) return false;
+  r.ragged = P.ragged_bl & CKV_RAGGED_MASK;
+  r.bl = static_cast<int>(P.ragged_bl >> CKV_BUFFER_LEN_SHIFT);
+  r.first = P.seq_len == 4 ? 4 : 0;
+  r.rp0 = P.read_page_0;
+  r.rp1 = P.read_page_1;
+  bool ok = r.ragged < a.num_q_tokens && r.bl <= 7 && static_cast<int64_t>(r.ragged) - 7 + r.bl >= 0;
+  if (r.bl > r.first && r.first < 4) ok = ok && r.rp0 >= 0 && static_cast<uint64_t>(r.rp0) * 4 + 3 < a.state_rows;
+  if (r.bl > 4) ok = ok && r.rp1 >= 0 && static_cast<uint64_t>(r.rp1) * 4 + 3 < a.state_rows;
+  bad = !ok;
+  return ok;
+}
+
+// Issues the copies of record r's window into `win` ([8][2][hd] elements);
+// returns their bytes.  q = blocks per quarter.
+template <typename TIn>
+__device__ __forceinline__ uint32_t c4_issue_window(const C4Maps& m, const C4Rec& r, int hd, int q, TIn* win,
+                                                    uint32_t bar, bool issue) {
+  const uint32_t row_bytes = 2u * static_cast<uint32_t>(hd) * sizeof(TIn);  // one entry: kv + score halves
+  uint32_t bytes = 0;
+  for (int p = 0; p < 2; ++p) {
+    const int i0 = 4 * p;
+    if (p == 0 && r.first == 4) continue;  // the first group has no previous group
+    const int q0 = p == 0 ? 0 : q;
+    const int page_row = static_cast<int>((p == 0 ? r.rp0 : r.rp1) * 4);
+    if (i0 >= r.bl) {  // four input rows
+      if (issue)
+        tma_box4_g2s(smem_addr(win + static_cast<size_t>(2 * i0) * hd), &m.in4, q0,
+                     static_cast<int>(r.ragged) - 7 + i0, bar);
+      bytes += 4 * row_bytes;
+    } else if (i0 + 4 <= r.bl) {  // a whole 4-slot page of the ring
+      if (issue) tma_box4_g2s(smem_addr(win + static_cast<size_t>(2 * i0) * hd), &m.st4, q0, page_row, bar);
+      bytes += 4 * row_bytes;
+    } else {
+      for (int i = i0; i < i0 + 4; ++i) {
+        if (issue) {
+          if (i < r.bl)
+            tma_box4_g2s(smem_addr(win + static_cast<size_t>(2 * i) * hd), &m.st1, q0, page_row + (i & 3), bar);
+          else
+            tma_box4_g2s(smem_addr(win + static_cast<size_t>(2 * i) * hd), &m.in1, q0,
+                         static_cast<int>(r.ragged) - 7 + i, bar);
+        }
+        bytes += row_bytes;
+      }
+    }
+  }
+  return bytes;
+}
+
+template <typename TIn, typename TOut>
+__global__ __launch_bounds__(288, 1) void c4_pool_prefill_staged_kernel(const PoolArgs a,
+                                                                        const __grid_constant__ C4Maps maps) {
+  using S = C4Stage<TIn>;
+  constexpr int VEC = C4Vec<TIn>::VEC;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[8];
+  __shared__ __align__(8) uint64_t empty_bar[8];
+  __shared__ volatile int abort_flag;
+  const int hd = a.head_dim;
+  const int q = hd / c4_block(hd);
+  const int chunks = S::chunks(hd);
+  const int R = S::recs(hd);
+  const int NCT = S::consumers(hd);
+  const int NS = S::stages(hd);
+  const bool active = threadIdx.x < S::active(hd);
+  const uint32_t stage_bytes = S::bytes(hd);
+  const int t = threadIdx.x;
+  if (t == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), static_cast<uint32_t>(NCT / 32));
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
   pdl_wait();
   pdl_release();
-  const uint32_t gid = blockIdx.x * blockDim.x + threadIdx.x;
-  const uint32_t stride = gridDim.x * blockDim.x;  // a multiple of `chunks`
-  const uint32_t ch = gid % chunks;
-  const int c0 = static_cast<int>(ch) * VEC;
-
+  const bool token = a.out_layout == CKV_OUT_TOKEN;
   const uint32_t num_c = count_or_capacity(a.d_counts, 0, a.capacity);
-  for (uint32_t u = gid; u < units; u += stride) {
-    const uint32_t e = u / chunks;
-    if (e < num_c) {
-      const ckv_compress_plan_t P = load_plan_c(a.plan_c + e);
-      if (plan_c_invalid(P)) continue;
-      const uint32_t ragged = P.ragged_bl & CKV_RAGGED_MASK;
-      const int bl = static_cast<int>(P.ragged_bl >> CKV_BUFFER_LEN_SHIFT);
-      const int first = P.seq_len == 4 ? 4 : 0;
-      const int64_t rp0 = P.read_page_0, rp1 = P.read_page_1;
-      bool ok = ragged < a.num_q_tokens && bl <= 7 && static_cast<int64_t>(ragged) - 7 + bl >= 0;
-      if (bl > first && first < 4) ok = ok && rp0 >= 0 && static_cast<uint64_t>(rp0) * 4 + 3 < a.state_rows;
-      if (bl > 4) ok = ok && rp1 >= 0 && static_cast<uint64_t>(rp1) * 4 + 3 < a.state_rows;
-      if (!ok) {
-        if (ch == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
-        continue;
-      }
-      uint4 kv[8], sc[8], ap[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (i < first) {
-          kv[i] = sc[i] = make_uint4(0, 0, 0, 0);
-          continue;
+  const uint32_t n_rec = num_c + (token ? 1u : 0u);  // + the tail pseudo-record
+  const uint32_t n_grp = (n_rec + R - 1) / R;
+
+  if (t >= NCT) {
+    // ---------------- producer warp: lane r issues record r of the stage
+    const int lane = t - NCT;
+    if (lane < 4) prefetch_map(lane == 0 ? &maps.in4 : lane == 1 ? &maps.in1 : lane == 2 ? &maps.st4 : &maps.st1);
+    uint32_t g = 0;
+    // each lane's record of the next group is requested one group ahead
+    ckv_compress_plan_t nxt = c4_load_record(a, blockIdx.x * R + lane, lane < R ? num_c : 0u);
+    for (uint32_t grp = blockIdx.x; grp < n_grp && !abort_flag; grp += gridDim.x, ++g) {
+      const ckv_compress_plan_t cur = nxt;
+      nxt = c4_load_record(a, (grp + gridDim.x) * R + lane, lane < R ? num_c : 0u);
+      const int stage = static_cast<int>(g % NS);
+      if (!mbar_wait_bounded(smem_addr(&empty_bar[stage]), ((g / NS) & 1u) ^ 1u, kWaitLimitNs)) {
+        if (lane == 0) {
+          status_or(a.d_status, CKV_STATUS_TIMEOUT);
+          abort_flag = 1;
         }
-        const TIn* row = i < bl ? state + static_cast<size_t>((i < 4 ? rp0 : rp1) * 4 + (i & 3)) * width
-                                : input + (static_cast<size_t>(ragged) + i - 7) * width;
-        kv[i] = ld_stream16(row + (i < 4 ? 0 : hd) + c0);
-        sc[i] = ld_stream16(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
+        break;
       }
+      C4Rec rec;
+      bool bad;
+      const bool mine = lane < R && c4_record(a, cur, rec, bad);
+      TIn* win = reinterpret_cast<TIn*>(smem + static_cast<size_t>(stage) * stage_bytes) +
+                 static_cast<size_t>(lane) * 16 * hd;
+      const uint32_t bar = smem_addr(&full_bar[stage]);
+      uint32_t total = mine ? c4_issue_window<TIn>(maps, rec, hd, q, win, bar, false) : 0u;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ap[i] = ld_cached16(ape + static_cast<size_t>(i) * hd + c0);  // L1-resident
-      float res[VEC];
-      c4_pool_chunk<TIn, VEC>(kv, sc, ap, first, res);
-      const size_t orow = token ? ragged : e;
-      store_row_chunk<TOut, VEC>(out + orow * hd + c0, res);
-      if (token) {
-        // zero the rows between the previous compress row and this one
-        int64_t prev = -1;
-        if (e > 0) {
-          const ckv_compress_plan_t Q = load_plan_c(a.plan_c + e - 1);
-          prev = plan_c_invalid(Q) ? static_cast<int64_t>(ragged) : static_cast<int64_t>(Q.ragged_bl & CKV_RAGGED_MASK);
+      for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, off);
+      if (lane == 0) mbar_arrive_expect_tx(bar, total);  // announced before any copy is issued
+      __syncwarp();
+      if (mine) c4_issue_window<TIn>(maps, rec, hd, q, win, bar, true);
+    }
+    // the last NS stages issued have landed before the CTA can exit
+    for (uint32_t h = g > static_cast<uint32_t>(NS) ? g - NS : 0u; h < g; ++h)
+      mbar_wait_bounded(smem_addr(&full_bar[h % NS]), (h / NS) & 1u, kWaitLimitNs);
+    return;
+  }
+
+  // ---------------- consumers
+  const int r = t / chunks;
+  const int ch = t % chunks;
+  const int c0 = ch * VEC;
+  const int lane = t & 31;
+  TOut* out = static_cast<TOut*>(a.out);
+  const TIn* ape = static_cast<const TIn*>(a.ape);
+  uint4 ap[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    ap[i] = active ? ld_cached16(ape + static_cast<size_t>(i) * hd + c0) : make_uint4(0, 0, 0, 0);
+  uint32_t g = 0;
+  // this thread's record of the next group (and the one before it, for the
+  // zero rows of the token layout) are requested one group ahead
+  const uint32_t num_c_mine = active ? num_c : 0u;
+  ckv_compress_plan_t nxt = c4_load_record(a, blockIdx.x * R + r, num_c_mine);
+  ckv_compress_plan_t nxt_prev = c4_load_record(a, blockIdx.x * R + r - 1, blockIdx.x * R + r > 0 ? num_c_mine : 0u);
+  for (uint32_t grp = blockIdx.x; grp < n_grp; grp += gridDim.x, ++g) {
+    const ckv_compress_plan_t cur = nxt, cur_prev = nxt_prev;
+    const uint32_t en = (grp + gridDim.x) * R + r;
+    nxt = c4_load_record(a, en, num_c_mine);
+    nxt_prev = c4_load_record(a, en - 1, num_c_mine);
+    const int stage = static_cast<int>(g % NS);
+    if (!mbar_wait_bounded(smem_addr(&full_bar[stage]), (g / NS) & 1u, kWaitLimitNs)) {
+      status_or(a.d_status, CKV_STATUS_TIMEOUT);
+      abort_flag = 1;
+      break;
+    }
+    const uint32_t e = grp * R + r;
+    if (!active) {
+    } else if (e < num_c) {
+      C4Rec rec;
+      bool bad;
+      if (c4_record(a, cur, rec, bad)) {
+        const TIn* base = reinterpret_cast<const TIn*>(smem + static_cast<size_t>(stage) * stage_bytes) +
+                          static_cast<size_t>(r) * 16 * hd + c0;
+        uint4 kv[8], sc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (i < rec.first) {
+            kv[i] = sc[i] = make_uint4(0, 0, 0, 0);
+          } else {
+            kv[i] = *reinterpret_cast<const uint4*>(base + static_cast<size_t>(2 * i) * hd);
+            sc[i] = *reinterpret_cast<const uint4*>(base + static_cast<size_t>(2 * i + 1) * hd);
+          }
         }
-        for (int64_t r = prev + 1; r < static_cast<int64_t>(ragged); ++r)
-          store_zero_chunk<TOut, VEC>(out + static_cast<size_t>(r) * hd + c0);
+        float res[VEC];
+        c4_pool_chunk<TIn, VEC>(kv, sc, ap, rec.first, res);
+        const size_t orow = token ? rec.ragged : e;
+        store_row_chunk<TOut, VEC>(out + orow * hd + c0, res);
+        if (token) {  // zero the rows between the previous compress row and this one
+          int64_t prev = -1;
+          if (e > 0)
+            prev = plan_c_invalid(cur_prev) ? static_cast<int64_t>(rec.ragged)
+                                            : static_cast<int64_t>(cur_prev.ragged_bl & CKV_RAGGED_MASK);
+          for (int64_t row = prev + 1; row < static_cast<int64_t>(rec.ragged); ++row)
+            store_zero_chunk<TOut, VEC>(out + static_cast<size_t>(row) * hd + c0);
+        }
+      } else if (bad && ch == 0) {
+        status_or(a.d_status, CKV_STATUS_BAD_INDEX);
       }
-    } else if (token && e == num_c) {
-      // rows after the last compress row
+    } else if (token && e == num_c) {  // rows after the last compress row
       int64_t last = -1;
       if (num_c > 0) {
         const ckv_compress_plan_t Q = load_plan_c(a.plan_c + num_c - 1);
-        last = plan_c_invalid(Q) ? static_cast<int64_t>(a.num_q_tokens) : static_cast<int64_t>(Q.ragged_bl & CKV_RAGGED_MASK);
+        last = plan_c_invalid(Q) ? static_cast<int64_t>(a.num_q_tokens)
+                                 : static_cast<int64_t>(Q.ragged_bl & CKV_RAGGED_MASK);
       }
-      for (int64_t r = last + 1; r < static_cast<int64_t>(a.num_q_tokens); ++r)
-        store_zero_chunk<TOut, VEC>(out + static_cast<size_t>(r) * hd + c0);
+      for (int64_t row = last + 1; row < static_cast<int64_t>(a.num_q_tokens); ++row)
+        store_zero_chunk<TOut, VEC>(out + static_cast<size_t>(row) * hd + c0);
     }
+    // this warp no longer reads the stage
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
   }
 }
 
@@ -209,19 +404,54 @@ __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolA
   store_row_chunk<TOut, VEC>(orow, res);
 }
 
+// The 4-D view of a [rows, 4 * hd] C4 row tensor, boxes of `box_rows` rows.
+int c4_view(CUtensorMap* map, const void* base, int dtype, int hd, uint64_t rows, uint32_t box_rows) {
+  const uint64_t esz = dtype == CKV_BF16 ? 2 : 4;
+  const uint64_t blk = static_cast<uint64_t>(c4_block(hd));
+  const uint64_t q = static_cast<uint64_t>(hd) / blk;
+  const uint64_t dims[4] = {blk, 2 * q, 2, rows};
+  const uint64_t strides[3] = {blk * esz, 2ull * hd * esz, 4ull * hd * esz};
+  const uint32_t box[4] = {static_cast<uint32_t>(blk), static_cast<uint32_t>(q), 2, box_rows};
+  return encode_tensor_map(map, dtype, 4, base, dims, strides, box);
+}
+
 template <typename TIn, typename TOut>
 int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
-  constexpr int VEC = C4Vec<TIn>::VEC;
-  const uint32_t chunks = static_cast<uint32_t>(a.head_dim / VEC);
-  const uint32_t threads = (kC4Threads / chunks) * chunks;
-  const uint64_t units64 =
-      (static_cast<uint64_t>(a.capacity) + (a.out_layout == CKV_OUT_TOKEN ? 1 : 0)) * chunks;
-  if (units64 == 0) return CKV_OK;
-  if (units64 > 0xFFFFFFFFull) return CKV_ERR_SIZE;
-  const uint32_t units = static_cast<uint32_t>(units64);
-  uint32_t grid = (units + threads - 1) / threads;
-  grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 16u * static_cast<uint32_t>(sm_count())));
-  return launch_pdl(c4_pool_prefill_kernel<TIn, TOut>, dim3(grid), dim3(threads), 0, s, a, chunks, units);
+  using S = C4Stage<TIn>;
+  const int hd = a.head_dim;
+  const uint64_t recs = static_cast<uint64_t>(a.capacity) + (a.out_layout == CKV_OUT_TOKEN ? 1 : 0);
+  if (recs == 0) return CKV_OK;
+  // tensor-map row coordinates are 32-bit
+  if (a.num_q_tokens > 0x7FFFFFFFu || a.state_rows > 0x7FFFFFFFull) return CKV_ERR_SIZE;
+  auto fn = c4_pool_prefill_staged_kernel<TIn, TOut>;
+  const int smem = S::stages(hd) * static_cast<int>(S::bytes(hd));
+  const int threads = S::consumers(hd) + 32;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CKV_ERR_LAUNCH;
+  static bool configured[64] = {};
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kC4StageBudget) != cudaSuccess) {
+      cudaGetLastError();
+      return CKV_ERR_LAUNCH;
+    }
+    configured[dev] = true;
+  }
+  alignas(64) C4Maps maps;
+  memset(&maps, 0, sizeof maps);
+  int rc = CKV_OK;
+  if (a.num_q_tokens > 0) {
+    rc = c4_view(&maps.in4, a.input, a.in_dtype, hd, a.num_q_tokens, 4);
+    if (!rc) rc = c4_view(&maps.in1, a.input, a.in_dtype, hd, a.num_q_tokens, 1);
+  }
+  if (!rc && a.state_rows > 0) {
+    rc = c4_view(&maps.st4, a.state, a.in_dtype, hd, a.state_rows, 4);
+    if (!rc) rc = c4_view(&maps.st1, a.state, a.in_dtype, hd, a.state_rows, 1);
+  }
+  if (rc) return rc;
+  const uint64_t groups = (recs + S::recs(hd) - 1) / S::recs(hd);
+  const uint32_t grid =
+      static_cast<uint32_t>(std::max<uint64_t>(1, std::min<uint64_t>(groups, static_cast<uint64_t>(sm_count()))));
+  return launch_pdl(fn, dim3(grid), dim3(threads), smem, s, a, maps);
 }
 
 template <typename TIn, typename TOut>
