@@ -169,7 +169,9 @@ def _run_prefill_parity(env, ratio, hd, in_dt, out_dt, layout, pl, el, seed, sta
     assert (H.np_bits(state_d).view(np.uint8) == st.view(np.uint8)).all(), "state after write"
 
 
-@pytest.mark.parametrize("hd", [128, 384, 512])
+# head_dim 640 and 1024 give the staged C4 pool's row view its other shapes
+# (128-channel blocks, five per quarter; 1 KB-wide fp32 boxes)
+@pytest.mark.parametrize("hd", [128, 384, 512, 640, 1024])
 @pytest.mark.parametrize("dts", [("bf16", "f32"), ("bf16", "bf16"), ("f32", "f32"), ("f32", "bf16")])
 @pytest.mark.parametrize("layout", [0, 1])
 def test_c4_prefill_parity(env, hd, dts, layout):
