@@ -181,7 +181,7 @@ def test_c4_prefill_parity(env, hd, dts, layout):
     _run_prefill_parity(env, 4, hd, DT[dts[0]], DT[dts[1]], layout, pl, el, seed=hd + layout)
 
 
-@pytest.mark.parametrize("hd", [128, 512])
+@pytest.mark.parametrize("hd", [128, 384, 512, 1024])
 @pytest.mark.parametrize("dts", [("bf16", "f32"), ("bf16", "bf16"), ("f32", "f32"), ("f32", "bf16")])
 @pytest.mark.parametrize("layout", [0, 1])
 def test_c128_prefill_parity(env, hd, dts, layout):
