@@ -110,7 +110,7 @@ def prefill_events(ratio, sl, el):
 
 
 def algorithmic_bytes(w: wl.Workload) -> dict:
-    """Bytes each kernel must move at minimum, each counted once (see DESIGN)."""
+    """Bytes each kernel must move at minimum, each counted once."""
     hd, R, W = w.head_dim, w.ratio, w.window
     ein, eout = elem(w.in_dtype), elem(w.out_dtype)
     entry = 2 * hd * ein                      # one window entry: kv + score (C4: one half row)

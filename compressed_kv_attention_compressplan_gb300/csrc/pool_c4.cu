@@ -77,7 +77,7 @@ __device__ __forceinline__ void c4_pool_chunk(const uint4 (&kv)[8], const uint4 
 // (entries 4..7) are ONE box: a record whose window lies in the input is two
 // copies.  Entries held in the ring come from the state through the same view
 // (a box of 4 rows when a whole group is in the state, else one row at a
-// time).  A producer warp issues the copies of kC4Recs(hd) consecutive
+// time).  A producer warp issues the copies of C4Stage::recs(hd) consecutive
 // records per stage into a ring; the window of record r of a stage sits at
 // [entry][kv | score][head_dim] and consumer thread t owns 16-byte channel
 // chunk t % chunks of record t / chunks, running the same c4_pool_chunk as the
