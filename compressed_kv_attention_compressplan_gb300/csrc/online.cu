@@ -23,7 +23,9 @@ namespace {
 constexpr int kOnThreads = 256;  // decode
 // Prefill ring: kOnStages stages of kOnTok tokens; a stage holds the tokens'
 // input rows (kv | score, 2 * head_dim each) followed by their ape rows
-// (head_dim each), one bulk copy for each part.
+// (head_dim each), one bulk copy for each part.  7 x 2 is 42 KB at head_dim
+// 512 bf16: five CTAs fit on an SM, and resident CTAs decide the throughput
+// (deeper or wider rings that leave room for fewer CTAs are slower).
 constexpr int kOnTok = 7;
 constexpr int kOnStages = 2;
 constexpr int kOnMaxThreads = 1024 / 4 + 32;  // prefill CTA at the largest head_dim: consumers + producer warp
