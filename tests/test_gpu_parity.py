@@ -383,3 +383,19 @@ def test_c128_decode_large_batch_path_matches(env):
     mask[torch.as_tensor(pos, device=dev)] = False
     assert (out_big[mask].view(torch.int32) == 0).all()
     assert torch.equal(big_state.view(torch.int16), small_state.view(torch.int16))
+
+
+@pytest.mark.parametrize("ratio,dts", [(128, ("bf16", "f32")), (128, ("f32", "bf16")), (4, ("bf16", "bf16")),
+                                       (4, ("f32", "f32"))])
+def test_prefill_every_buffer_len(env, ratio, dts):
+    """Windows that start in the state with every possible number of state
+    entries: request r has prefix r and extends to the first boundary, so its
+    window holds r state entries (C128: 1 .. 127, every split of the state
+    and input row ranges into copies; C4: prefixes 1 .. 7 and later groups)."""
+    if ratio == 128:
+        pl = list(range(1, 128))
+        el = [128 - r for r in pl]
+    else:
+        pl = [1, 2, 3, 4, 5, 6, 7, 9, 10, 11, 13, 14, 15]
+        el = [(4 - r % 4) % 4 + 4 * (1 + r % 3) for r in pl]
+    _run_prefill_parity(env, ratio, 256, DT[dts[0]], DT[dts[1]], 1, pl, el, seed=77 + ratio)
