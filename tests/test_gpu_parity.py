@@ -399,3 +399,12 @@ def test_prefill_every_buffer_len(env, ratio, dts):
         pl = [1, 2, 3, 4, 5, 6, 7, 9, 10, 11, 13, 14, 15]
         el = [(4 - r % 4) % 4 + 4 * (1 + r % 3) for r in pl]
     _run_prefill_parity(env, ratio, 256, DT[dts[0]], DT[dts[1]], 1, pl, el, seed=77 + ratio)
+
+
+@pytest.mark.parametrize("ratio,pl,el", [(4, [3], [1]), (4, [1], [3]), (4, [6], [2]), (128, [100], [28]),
+                                         (128, [127], [1])])
+def test_prefill_inputs_shorter_than_a_box(env, ratio, pl, el):
+    """Ragged inputs of fewer rows than the pools' largest boxes (a handful of
+    new tokens whose window is mostly in the state)."""
+    for layout in (0, 1):
+        _run_prefill_parity(env, ratio, 256, DT["bf16"], DT["f32"], layout, pl, el, seed=5 + ratio)
