@@ -567,6 +567,19 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
     for (uint32_t n = kDecode && items > 0 ? 1u : 0u; n < items; ++n) {
       const int stage = static_cast<int>(n % NS);
       const uint32_t phase = (n / NS) & 1u;
+      // decode: at most two tiles ahead of the last that landed (tile n >= 2
+      // waits for tile n-2).  Every SM asking for its whole ring at once made
+      // each first tile wait for the whole burst; pacing the issue lets the
+      // first tiles land, and the reductions start, earlier.  (Tile n-2's
+      // stage is not refilled before tile n is issued, so its phase is exact.)
+      if (kDecode && n >= 2 &&
+          !mbar_wait_bounded(smem_addr(&full_bar[(n - 2) % NS]), ((n - 2) / NS) & 1u, kWaitLimitNs)) {
+        if (lane == 0) {
+          status_or(a.d_status, CKV_STATUS_TIMEOUT);
+          abort_flag = 1;
+        }
+        break;
+      }
       if (!mbar_wait_bounded(smem_addr(&empty_bar[stage]), phase ^ 1u, kWaitLimitNs)) {
         if (lane == 0) {
           status_or(a.d_status, CKV_STATUS_TIMEOUT);
