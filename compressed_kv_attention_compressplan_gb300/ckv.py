@@ -92,6 +92,8 @@ def load_library():
         lib.ckv_error_string.argtypes = [i32]
         lib.ckv_error_string.restype = ctypes.c_char_p
         lib.ckv_version.restype = i32
+        lib.ckv_set_wait_limit_ns.argtypes = [u64]
+        lib.ckv_set_wait_limit_ns.restype = u64
         _lib = lib
         return lib
 
@@ -156,6 +158,14 @@ def capacity_compress(ratio: int, batch: int, num_q_tokens: int) -> int:
 
 def capacity_write(ratio: int, batch: int, num_q_tokens: int) -> int:
     return int(load_library().ckv_capacity_write(ratio, batch, num_q_tokens))
+
+
+def set_wait_limit_ns(limit_ns: int) -> int:
+    """Sets the time limit of the staged kernels' waits on their copies for later launches
+    (0 restores the 2 s default) and returns the previous limit."""
+    if not 0 <= int(limit_ns) < 1 << 64:
+        raise ValueError("limit_ns must fit an unsigned 64-bit integer")
+    return int(load_library().ckv_set_wait_limit_ns(int(limit_ns)))
 
 
 def new_status(device=None) -> torch.Tensor:

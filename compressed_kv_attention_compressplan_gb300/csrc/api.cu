@@ -1,11 +1,16 @@
 // api.cu -- the compute entry points of the C ABI: argument checks on the
 // host, then dispatch to the ratio-specific launchers.
+#include <atomic>
+
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "launch.h"
 
 using namespace ckv;
 
 namespace {
+
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
 
 int check_pool_args(int ratio, int head_dim, int in_dtype, int out_dtype) {
   if (ratio != 4 && ratio != 128) return CKV_ERR_RATIO;
@@ -17,7 +22,17 @@ int check_pool_args(int ratio, int head_dim, int in_dtype, int out_dtype) {
 
 }  // namespace
 
+namespace ckv {
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+}  // namespace ckv
+
 extern "C" {
+
+uint64_t ckv_set_wait_limit_ns(uint64_t limit_ns) {
+  return g_wait_limit_ns.exchange(limit_ns == 0 ? kWaitLimitNs : limit_ns, std::memory_order_relaxed);
+}
 
 int ckv_compress_pool_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, const void* state,
                               uint64_t state_rows, const void* kv_score_input, uint32_t num_q_tokens,
@@ -50,6 +65,7 @@ int ckv_compress_pool_prefill(int ratio, int head_dim, int in_dtype, int out_dty
   a.out_layout = out_layout;
   a.out = out;
   a.d_status = d_status;
+  a.wait_ns = wait_limit_ns();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return ratio == 4 ? launch_c4_pool_prefill(a, s) : launch_c128_pool_prefill(a, s);
 }
@@ -96,6 +112,7 @@ int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, vo
   a.out_layout = CKV_OUT_TOKEN;
   a.out = out;
   a.d_status = d_status;
+  a.wait_ns = wait_limit_ns();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return ratio == 4 ? launch_c4_decode(a, s) : launch_c128_decode(a, s);
 }

@@ -3,7 +3,10 @@
 //
 // Every wait is bounded: mbar_wait_bounded gives up after a time limit and
 // reports it, so a copy that never completes turns into a status bit instead
-// of a hung kernel.
+// of a hung kernel.  The ordinary waits of a kernel use the limit passed in
+// its arguments (ckv_set_wait_limit_ns); a CTA that gives up still waits, with
+// the fixed kWaitLimitNs, for the copies it has issued to land before it
+// exits, so that no copy writes into shared memory the CTA no longer owns.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -11,7 +14,9 @@
 
 namespace ckv {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any real copy
+// 2 s, far beyond any real copy: the default limit of the ordinary waits, and
+// the limit of the waits for copies in flight before a CTA exits
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -44,6 +49,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// The same test without suspending the thread (test_wait never blocks).
+// try_wait, even given a suspend-time hint, may hold the thread until the
+// phase completes when that happens within a hardware-chosen window of
+// microseconds, so a limit shorter than that window is only observed by
+// polling test_wait against the timer.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Limits below this (1 ms) are polled with test_wait.
+constexpr uint64_t kShortWaitNs = 1000000ull;
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -52,12 +77,27 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Waits for the phase of parity `parity` to complete, for at most `limit_ns`.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns < kShortWaitNs) {
+    const uint64_t t0 = global_ns();
+    while (true) {
+      if (mbar_test_wait(bar, parity)) return true;
+      if (global_ns() - t0 > limit_ns) return false;
+    }
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (global_ns() - t0 > limit_ns) return false;
   }
+}
+
+// The same wait by all 32 lanes of a warp, which then take one decision: the
+// phase counts as complete only if every lane saw it complete.  After a
+// timeout the whole warp therefore leaves together, and no lane is left
+// waiting in a later warp-wide shuffle or __syncwarp for lanes that left.
+__device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar, parity, limit_ns));
 }
 
 // One bulk global -> shared copy that completes `bytes` of the barrier's

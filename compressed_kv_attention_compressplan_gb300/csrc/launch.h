@@ -29,9 +29,14 @@ struct PoolArgs {
   int out_layout;
   void* out;
   uint32_t* d_status;
+  uint64_t wait_ns;  // limit of the kernels' ordinary waits on asynchronous copies
 };
 
 int sm_count();
+
+// The limit, in ns, that launches made from now on give their kernels' ordinary
+// waits on asynchronous copies (ckv_set_wait_limit_ns).
+uint64_t wait_limit_ns();
 
 // Encodes a tiled tensor map of `rank` dimensions (dims[0] innermost; strides
 // in bytes for dims 1 .. rank-1; box extents per dimension) over `base`, of

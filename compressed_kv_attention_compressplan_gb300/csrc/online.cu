@@ -58,6 +58,7 @@ struct OnlineArgs {
   // and pass 1 -- a second launch, after every load -- refolds those last
   // units (their tokens only) and stores their state.
   int pass;
+  uint64_t wait_ns;  // limit of the ordinary waits on asynchronous copies
 };
 
 // Running softmax of one channel over the tokens of a group so far, kept as
@@ -268,7 +269,7 @@ __global__ __launch_bounds__(kOnMaxThreads) void online_prefill_kernel(const Onl
       const TIn* arows = ape + static_cast<size_t>(u.pos0 % 128) * hd;
       for (uint32_t j = 0; j < u.cnt; j += kOnTok, ++g) {
         const int stage = static_cast<int>(g % kOnStages);
-        if (!mbar_wait_bounded(smem_addr(&empty_bar[stage]), ((g / kOnStages) & 1u) ^ 1u, kWaitLimitNs)) {
+        if (!mbar_wait_bounded(smem_addr(&empty_bar[stage]), ((g / kOnStages) & 1u) ^ 1u, a.wait_ns)) {
           status_or(a.d_status, CKV_STATUS_TIMEOUT);
           abort_flag = 1;
           break;
@@ -312,7 +313,7 @@ __global__ __launch_bounds__(kOnMaxThreads) void online_prefill_kernel(const Onl
     bool stop = false;
     for (uint32_t j = 0; j < u.cnt; j += kOnTok, ++g) {
       const int stage = static_cast<int>(g % kOnStages);
-      if (!mbar_wait_bounded(smem_addr(&full_bar[stage]), (g / kOnStages) & 1u, kWaitLimitNs)) {
+      if (!warp_wait_bounded(smem_addr(&full_bar[stage]), (g / kOnStages) & 1u, a.wait_ns)) {
         status_or(a.d_status, CKV_STATUS_TIMEOUT);
         abort_flag = 1;
         stop = true;
@@ -516,6 +517,7 @@ extern "C" int ckv_compress_online_prefill(int head_dim, int in_dtype, int out_d
   a.out_rows = out_rows;
   a.out = out;
   a.d_status = d_status;
+  a.wait_ns = wait_limit_ns();
   const int rc = check_online(a);
   if (rc || capacity_u == 0) return rc;
   if (!aligned16(units) || (d_counts && (reinterpret_cast<uintptr_t>(d_counts) & 3u))) return CKV_ERR_POINTER;

@@ -567,7 +567,8 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
 
   if (warp == NC / 32) {
     // ---------------- producer warp (decode: tile 0 was issued by the scan)
-    for (uint32_t n = kDecode && items > 0 ? 1u : 0u; n < items; ++n) {
+    uint32_t n = kDecode && items > 0 ? 1u : 0u;  // tiles issued so far
+    for (; n < items; ++n) {
       const int stage = static_cast<int>(n % NS);
       const uint32_t phase = (n / NS) & 1u;
       // decode: at most two tiles ahead of the last that landed (tile n >= 2
@@ -576,21 +577,21 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
       // first tiles land, and the reductions start, earlier.  (Tile n-2's
       // stage is not refilled before tile n is issued, so its phase is exact.)
       if (kDecode && n >= 2 &&
-          !mbar_wait_bounded(smem_addr(&full_bar[(n - 2) % NS]), ((n - 2) / NS) & 1u, kWaitLimitNs)) {
+          !warp_wait_bounded(smem_addr(&full_bar[(n - 2) % NS]), ((n - 2) / NS) & 1u, a.wait_ns)) {
         if (lane == 0) {
           status_or(a.d_status, CKV_STATUS_TIMEOUT);
           abort_flag = 1;
         }
         break;
       }
-      if (!mbar_wait_bounded(smem_addr(&empty_bar[stage]), phase ^ 1u, kWaitLimitNs)) {
+      if (!warp_wait_bounded(smem_addr(&empty_bar[stage]), phase ^ 1u, a.wait_ns)) {
         if (lane == 0) {
           status_or(a.d_status, CKV_STATUS_TIMEOUT);
           abort_flag = 1;
         }
         break;
       }
-      if (abort_flag) break;
+      if (__any_sync(0xFFFFFFFFu, abort_flag != 0)) break;
       const uint32_t bar = smem_addr(&full_bar[stage]);
       TIn* kv_s = reinterpret_cast<TIn*>(smem + stage * T::TILE_BYTES);
       if constexpr (kDecode) {
@@ -621,6 +622,10 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
       }
       __syncwarp();
     }
+    // the last NS tiles issued (one per stage) have landed before the CTA can
+    // exit; after a timeout the consumers may have stopped waiting for them
+    for (uint32_t h = n > static_cast<uint32_t>(NS) ? n - NS : 0u; h < n; ++h)
+      mbar_wait_bounded(smem_addr(&full_bar[h % NS]), (h / NS) & 1u, kWaitLimitNs);
     return;
   }
 
@@ -636,7 +641,7 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
     if (group_any(grp, NCG, abort_flag != 0)) break;
     const int stage = static_cast<int>(n % NS);
     const uint32_t phase = (n / NS) & 1u;
-    if (!mbar_wait_bounded(smem_addr(&full_bar[stage]), phase, kWaitLimitNs)) {
+    if (!mbar_wait_bounded(smem_addr(&full_bar[stage]), phase, a.wait_ns)) {
       status_or(a.d_status, CKV_STATUS_TIMEOUT);
       abort_flag = 1;
     }
@@ -774,7 +779,7 @@ __global__ __launch_bounds__(DecodeCfg<TIn>::THREADS, 6) void c128_decode_kernel
   const int cq = 4 * q;
   const TIn* ape = static_cast<const TIn*>(a.ape) + static_cast<size_t>(16 * g) * hd + c0 + cq;
   auto ape_at = [&](int k, F2 (&v)[2]) { ldg4x2<TIn>(ape + static_cast<size_t>(k) * hd, v); };
-  if (!mbar_wait_bounded(bar, 0, kWaitLimitNs)) {
+  if (!mbar_wait_bounded(bar, 0, a.wait_ns)) {
     status_or(a.d_status, CKV_STATUS_TIMEOUT);
     mbar_wait_bounded(bar, 0, kWaitLimitNs);  // let copies in flight land before the CTA can exit
   }

@@ -220,11 +220,12 @@ __global__ __launch_bounds__(288, 1) void c4_pool_prefill_staged_kernel(const Po
     uint32_t g = 0;
     // each lane's record of the next group is requested one group ahead
     ckv_compress_plan_t nxt = c4_load_record(a, blockIdx.x * R + lane, lane < R ? num_c : 0u);
-    for (uint32_t grp = blockIdx.x; grp < n_grp && !abort_flag; grp += gridDim.x, ++g) {
+    for (uint32_t grp = blockIdx.x; grp < n_grp && !__any_sync(0xFFFFFFFFu, abort_flag != 0);
+         grp += gridDim.x, ++g) {
       const ckv_compress_plan_t cur = nxt;
       nxt = c4_load_record(a, (grp + gridDim.x) * R + lane, lane < R ? num_c : 0u);
       const int stage = static_cast<int>(g % NS);
-      if (!mbar_wait_bounded(smem_addr(&empty_bar[stage]), ((g / NS) & 1u) ^ 1u, kWaitLimitNs)) {
+      if (!warp_wait_bounded(smem_addr(&empty_bar[stage]), ((g / NS) & 1u) ^ 1u, a.wait_ns)) {
         if (lane == 0) {
           status_or(a.d_status, CKV_STATUS_TIMEOUT);
           abort_flag = 1;
@@ -273,7 +274,7 @@ __global__ __launch_bounds__(288, 1) void c4_pool_prefill_staged_kernel(const Po
     nxt = c4_load_record(a, en, num_c_mine);
     nxt_prev = c4_load_record(a, en - 1, num_c_mine);
     const int stage = static_cast<int>(g % NS);
-    if (!mbar_wait_bounded(smem_addr(&full_bar[stage]), (g / NS) & 1u, kWaitLimitNs)) {
+    if (!warp_wait_bounded(smem_addr(&full_bar[stage]), (g / NS) & 1u, a.wait_ns)) {
       status_or(a.d_status, CKV_STATUS_TIMEOUT);
       abort_flag = 1;
       break;

@@ -81,6 +81,23 @@ enum {
 
 enum { CKV_MAX_BATCH = 1024, CKV_MAX_TOKENS = (1 << 24) - 1 };
 
+/* ------------------------------------------------------------------ waits */
+/* The pooling kernels that stage their inputs through the TMA engine (C4 and
+ * C128 prefill pools, C128 decode, online prefill) wait on mbarriers for those
+ * copies.  Every such wait gives up after a time limit: the kernel then ORs
+ * CKV_STATUS_TIMEOUT into *d_status and its CTA stops, after waiting (up to
+ * 2 s) for the copies it has already issued, so that none of them lands in
+ * shared memory the CTA no longer owns.  The context stays usable.
+ *
+ * ckv_set_wait_limit_ns sets that limit, in nanoseconds, for every launch made
+ * after the call, process-wide (an atomic; calls from several threads are
+ * safe), and returns the previous limit.  0 restores the default, 2 s.  The
+ * outputs of a launch whose waits expired -- and, for a decode, the state row
+ * it writes -- are unspecified; a limit below a copy's latency (a few
+ * microseconds) makes the waits expire on purpose.  Host only: touches no
+ * device and cannot fail. */
+uint64_t ckv_set_wait_limit_ns(uint64_t limit_ns);
+
 /* ------------------------------------------------------------------ plans */
 /* One compress event (16 bytes).  seq_len = position + 1 (a multiple of the
  * ratio); ragged_bl = ragged_id | buffer_len << 24 where ragged_id is the row of

@@ -99,3 +99,17 @@ def test_binding_rejects_wrong_per_request_arrays():
         ckv._lengths(i64, torch.arange(4, dtype=torch.int64))
     with pytest.raises(ValueError):
         ckv._lengths(i64.view(5, 1))
+
+
+def test_wait_limit_setter(lib):
+    default = 2_000_000_000
+    prev = ckv.set_wait_limit_ns(0)            # whatever was set, back to the default
+    assert ckv.set_wait_limit_ns(1234) == default
+    assert ckv.set_wait_limit_ns(5) == 1234
+    assert ckv.set_wait_limit_ns(0) == 5       # 0 restores the default ...
+    assert ckv.set_wait_limit_ns(0) == default
+    assert ckv.set_wait_limit_ns(2 ** 64 - 1) == default
+    assert ckv.set_wait_limit_ns(prev if prev != default else 0) == 2 ** 64 - 1
+    with pytest.raises(ValueError):
+        ckv.set_wait_limit_ns(-1)
+    ckv.set_wait_limit_ns(0)
