@@ -1,12 +1,19 @@
 // async_copy.cuh -- mbarrier and bulk-copy (TMA engine) helpers shared by the
 // kernels that stage data in shared memory (sm_90+ PTX, used on sm_103a).
 //
-// Every wait is bounded: mbar_wait_bounded gives up after a time limit and
-// reports it, so a copy that never completes turns into a status bit instead
-// of a hung kernel.  The ordinary waits of a kernel use the limit passed in
-// its arguments (ckv_set_wait_limit_ns); a CTA that gives up still waits, with
-// the fixed kWaitLimitNs, for the copies it has issued to land before it
-// exits, so that no copy writes into shared memory the CTA no longer owns.
+// Every wait is bounded: it gives up after a time limit and reports it, so a
+// copy that never completes turns into a status bit instead of a hung kernel.
+// The ordinary waits of a kernel use the limit passed in its arguments
+// (ckv_set_wait_limit_ns); a CTA that gives up still waits, with the fixed
+// kWaitLimitNs, for the copies it has issued to land before it exits, so that
+// no copy writes into shared memory the CTA no longer owns.
+//
+// try_wait may hold a thread until the phase completes when that happens
+// within a hardware-chosen window of microseconds, so a limit shorter than
+// that window can only be observed by polling test_wait.  Each staged kernel
+// is therefore built twice: for limits of 1 ms and more (try_wait, the limit
+// read only once a first probe has failed) and for shorter ones (test_wait
+// polled against the timer); the launchers pick by the limit.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -50,10 +57,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // The same test without suspending the thread (test_wait never blocks).
-// try_wait, even given a suspend-time hint, may hold the thread until the
-// phase completes when that happens within a hardware-chosen window of
-// microseconds, so a limit shorter than that window is only observed by
-// polling test_wait against the timer.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -66,7 +69,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Limits below this (1 ms) are polled with test_wait.
+// Limits below this (1 ms) are polled with test_wait, by kernels built for
+// short waits (the kShortWaits instantiations, launched only for such limits).
 constexpr uint64_t kShortWaitNs = 1000000ull;
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -75,15 +79,10 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Waits for the phase of parity `parity` to complete, for at most `limit_ns`.
+// Waits for the phase of parity `parity` to complete, for at most about
+// `limit_ns` beyond try_wait's own window.  The first probe is the whole cost
+// of a phase that completes on time; the limit is read only after it.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (limit_ns < kShortWaitNs) {
-    const uint64_t t0 = global_ns();
-    while (true) {
-      if (mbar_test_wait(bar, parity)) return true;
-      if (global_ns() - t0 > limit_ns) return false;
-    }
-  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
@@ -92,12 +91,29 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// The same with a limit below try_wait's window: test_wait polled against
+// the timer.
+__device__ __forceinline__ bool mbar_poll_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// A kernel's ordinary wait on one of its copies.
+template <bool kShortWaits>
+__device__ __forceinline__ bool wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return kShortWaits ? mbar_poll_bounded(bar, parity, limit_ns) : mbar_wait_bounded(bar, parity, limit_ns);
+}
+
 // The same wait by all 32 lanes of a warp, which then take one decision: the
 // phase counts as complete only if every lane saw it complete.  After a
 // timeout the whole warp therefore leaves together, and no lane is left
 // waiting in a later warp-wide shuffle or __syncwarp for lanes that left.
-__device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar, parity, limit_ns));
+template <bool kShortWaits>
+__device__ __forceinline__ bool warp_wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(0xFFFFFFFFu, wait_for<kShortWaits>(bar, parity, limit_ns));
 }
 
 // One bulk global -> shared copy that completes `bytes` of the barrier's

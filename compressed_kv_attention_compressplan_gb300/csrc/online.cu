@@ -226,7 +226,7 @@ __device__ __forceinline__ uint4 load_unit(const OnlineArgs& a, uint32_t k, uint
 // ahead.  Every wait is bounded; on expiry CKV_STATUS_TIMEOUT is set and the
 // CTA stops, after the producer has waited (again bounded) for the copies it
 // issued.
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool kShortWaits>
 __global__ __launch_bounds__(kOnMaxThreads) void online_prefill_kernel(const OnlineArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kOnStages];
@@ -269,7 +269,7 @@ __global__ __launch_bounds__(kOnMaxThreads) void online_prefill_kernel(const Onl
       const TIn* arows = ape + static_cast<size_t>(u.pos0 % 128) * hd;
       for (uint32_t j = 0; j < u.cnt; j += kOnTok, ++g) {
         const int stage = static_cast<int>(g % kOnStages);
-        if (!mbar_wait_bounded(smem_addr(&empty_bar[stage]), ((g / kOnStages) & 1u) ^ 1u, a.wait_ns)) {
+        if (!wait_for<kShortWaits>(smem_addr(&empty_bar[stage]), ((g / kOnStages) & 1u) ^ 1u, a.wait_ns)) {
           status_or(a.d_status, CKV_STATUS_TIMEOUT);
           abort_flag = 1;
           break;
@@ -313,7 +313,10 @@ __global__ __launch_bounds__(kOnMaxThreads) void online_prefill_kernel(const Onl
     bool stop = false;
     for (uint32_t j = 0; j < u.cnt; j += kOnTok, ++g) {
       const int stage = static_cast<int>(g % kOnStages);
-      if (!warp_wait_bounded(smem_addr(&full_bar[stage]), (g / kOnStages) & 1u, a.wait_ns)) {
+      // each thread decides for itself: one that gives up leaves the kernel,
+      // and the warp's __syncwarp below waits only for lanes that have not
+      // exited (its stage is then never released, so the producer gives up too)
+      if (!wait_for<kShortWaits>(smem_addr(&full_bar[stage]), (g / kOnStages) & 1u, a.wait_ns)) {
         status_or(a.d_status, CKV_STATUS_TIMEOUT);
         abort_flag = 1;
         stop = true;
@@ -433,9 +436,9 @@ int check_online(const OnlineArgs& a) {
 
 // Prefill: head_dim / 4 consumer threads + the producer warp; as many CTAs as
 // fit on the GPU at once (at most one per unit).
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool kShortWaits>
 int launch_prefill(const OnlineArgs& a, cudaStream_t s) {
-  auto fn = online_prefill_kernel<TIn, TOut>;
+  auto fn = online_prefill_kernel<TIn, TOut, kShortWaits>;
   const int smem = prefill_smem_bytes<TIn>(a.head_dim);
   const int threads = a.head_dim / 4 + 32;
   static bool configured[64] = {};
@@ -467,7 +470,10 @@ int launch_prefill(const OnlineArgs& a, cudaStream_t s) {
 
 template <typename TIn, typename TOut>
 struct PrefillK {
-  static int launch(const OnlineArgs& a, dim3, cudaStream_t s) { return launch_prefill<TIn, TOut>(a, s); }
+  // kernels built for waits shorter than try_wait's window only for such limits
+  static int launch(const OnlineArgs& a, dim3, cudaStream_t s) {
+    return a.wait_ns < kShortWaitNs ? launch_prefill<TIn, TOut, true>(a, s) : launch_prefill<TIn, TOut, false>(a, s);
+  }
 };
 template <typename TIn, typename TOut>
 struct DecodeK {

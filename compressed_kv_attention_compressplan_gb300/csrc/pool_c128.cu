@@ -441,7 +441,7 @@ __device__ __forceinline__ bool group_any(int grp, int n, bool pred) {
   return r != 0;
 }
 
-template <typename TIn, typename TOut, int CS, int NS, int NG, bool kDecode>
+template <typename TIn, typename TOut, int CS, int NS, int NG, bool kDecode, bool kShortWaits>
 __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) void c128_persistent_kernel(
     const PoolArgs a, uint32_t slices, const __grid_constant__ CUtensorMap in_map,
     const __grid_constant__ CUtensorMap page_map, const __grid_constant__ GatherMaps gather) {
@@ -566,7 +566,9 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
   }
 
   if (warp == NC / 32) {
-    // ---------------- producer warp (decode: tile 0 was issued by the scan)
+    // ---------------- producer: lane 0 of the last warp alone issues every
+    // copy and takes every wait (decode: tile 0 was issued by the scan)
+    if (lane != 0) return;
     uint32_t n = kDecode && items > 0 ? 1u : 0u;  // tiles issued so far
     for (; n < items; ++n) {
       const int stage = static_cast<int>(n % NS);
@@ -576,28 +578,19 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
       // each first tile wait for the whole burst; pacing the issue lets the
       // first tiles land, and the reductions start, earlier.  (Tile n-2's
       // stage is not refilled before tile n is issued, so its phase is exact.)
-      if (kDecode && n >= 2 &&
-          !warp_wait_bounded(smem_addr(&full_bar[(n - 2) % NS]), ((n - 2) / NS) & 1u, a.wait_ns)) {
-        if (lane == 0) {
-          status_or(a.d_status, CKV_STATUS_TIMEOUT);
-          abort_flag = 1;
-        }
+      if ((kDecode && n >= 2 &&
+           !wait_for<kShortWaits>(smem_addr(&full_bar[(n - 2) % NS]), ((n - 2) / NS) & 1u, a.wait_ns)) ||
+          !wait_for<kShortWaits>(smem_addr(&empty_bar[stage]), phase ^ 1u, a.wait_ns)) {
+        status_or(a.d_status, CKV_STATUS_TIMEOUT);
+        abort_flag = 1;
         break;
       }
-      if (!warp_wait_bounded(smem_addr(&empty_bar[stage]), phase ^ 1u, a.wait_ns)) {
-        if (lane == 0) {
-          status_or(a.d_status, CKV_STATUS_TIMEOUT);
-          abort_flag = 1;
-        }
-        break;
-      }
-      if (__any_sync(0xFFFFFFFFu, abort_flag != 0)) break;
+      if (abort_flag) break;  // a consumer gave up: issue nothing more
       const uint32_t bar = smem_addr(&full_bar[stage]);
       TIn* kv_s = reinterpret_cast<TIn*>(smem + stage * T::TILE_BYTES);
       if constexpr (kDecode) {
         const uint2 rp = own[n];
-        if (lane == 0)
-          issue_decode_tile<TIn, CS>(kv_s, bar, &page_map, input, width, hd, c0, rp.x, static_cast<int32_t>(rp.y));
+        issue_decode_tile<TIn, CS>(kv_s, bar, &page_map, input, width, hd, c0, rp.x, static_cast<int32_t>(rp.y));
       } else {
         const uint32_t e = first + n * stride;
         uint32_t ragged = 0;
@@ -605,22 +598,18 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
         int64_t rp0 = 0;
         bool bad;
         const bool ok = prefill_record(a, e, ragged, bl, rp0, bad);
-        if (bad && lane == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
-        if (lane == 0) mbar_arrive_expect_tx(bar, ok ? T::TILE_BYTES : 0u);
-        __syncwarp();
+        if (bad) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+        mbar_arrive_expect_tx(bar, ok ? T::TILE_BYTES : 0u);
         if (ok) {
           if (bl == 0) {  // rows ragged-127 .. ragged of the input: two boxes
-            if (lane == 0) {
-              tma_box_g2s(smem_addr(kv_s), &in_map, c0, static_cast<int>(ragged) - 127, bar);
-              tma_box_g2s(smem_addr(kv_s + 128 * CS), &in_map, hd + c0, static_cast<int>(ragged) - 127, bar);
-            }
-          } else if (lane == 0) {
+            tma_box_g2s(smem_addr(kv_s), &in_map, c0, static_cast<int>(ragged) - 127, bar);
+            tma_box_g2s(smem_addr(kv_s + 128 * CS), &in_map, hd + c0, static_cast<int>(ragged) - 127, bar);
+          } else {
             issue_gather<TIn, CS>(kv_s, gather, hd, c0, static_cast<int>(rp0 * 128),
                                   static_cast<int>(ragged) - 127 + bl, bl, bar);
           }
         }
       }
-      __syncwarp();
     }
     // the last NS tiles issued (one per stage) have landed before the CTA can
     // exit; after a timeout the consumers may have stopped waiting for them
@@ -641,7 +630,7 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
     if (group_any(grp, NCG, abort_flag != 0)) break;
     const int stage = static_cast<int>(n % NS);
     const uint32_t phase = (n / NS) & 1u;
-    if (!mbar_wait_bounded(smem_addr(&full_bar[stage]), phase, a.wait_ns)) {
+    if (!wait_for<kShortWaits>(smem_addr(&full_bar[stage]), phase, a.wait_ns)) {
       status_or(a.d_status, CKV_STATUS_TIMEOUT);
       abort_flag = 1;
     }
@@ -706,7 +695,7 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
 }
 
 // ---------------------------------------------------------------- decode (one tile per CTA)
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool kShortWaits>
 __global__ __launch_bounds__(DecodeCfg<TIn>::THREADS, 6) void c128_decode_kernel(
     const PoolArgs a, uint32_t slices, uint32_t tiles, const __grid_constant__ CUtensorMap page_map) {
   using Cfg = DecodeCfg<TIn>;
@@ -779,7 +768,7 @@ __global__ __launch_bounds__(DecodeCfg<TIn>::THREADS, 6) void c128_decode_kernel
   const int cq = 4 * q;
   const TIn* ape = static_cast<const TIn*>(a.ape) + static_cast<size_t>(16 * g) * hd + c0 + cq;
   auto ape_at = [&](int k, F2 (&v)[2]) { ldg4x2<TIn>(ape + static_cast<size_t>(k) * hd, v); };
-  if (!mbar_wait_bounded(bar, 0, a.wait_ns)) {
+  if (!wait_for<kShortWaits>(bar, 0, a.wait_ns)) {
     status_or(a.d_status, CKV_STATUS_TIMEOUT);
     mbar_wait_bounded(bar, 0, kWaitLimitNs);  // let copies in flight land before the CTA can exit
   }
@@ -821,7 +810,7 @@ int opt_in_smem(K kernel, int bytes, bool* configured) {
   return CKV_OK;
 }
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool kShortWaits>
 int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
   constexpr int CS = sizeof(TIn) == 2 ? 128 : 64;
   constexpr int NS = 3;
@@ -830,7 +819,8 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
   const bool token = a.out_layout == CKV_OUT_TOKEN;
   if (a.capacity == 0 && !(token && a.num_q_tokens > 0)) return CKV_OK;
   static bool configured[64] = {};
-  int rc = opt_in_smem(c128_persistent_kernel<TIn, TOut, CS, NS, 1, false>, Cfg::SMEM, configured);
+  auto kernel = c128_persistent_kernel<TIn, TOut, CS, NS, 1, false, kShortWaits>;
+  int rc = opt_in_smem(kernel, Cfg::SMEM, configured);
   if (rc) return rc;
   // one persistent CTA per SM; every CTA serves one channel slice
   const uint32_t per_slice = std::max<uint32_t>(
@@ -853,8 +843,8 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
       rc = make_map(&gather.state[k], a.state, a.in_dtype, 2ull * a.head_dim, a.state_rows, CS, gather_height(k));
     if (rc) return rc;
   }
-  return launch_pdl(c128_persistent_kernel<TIn, TOut, CS, NS, 1, false>, dim3(per_slice * slices), dim3(Cfg::THREADS),
-                    Cfg::SMEM, s, a, slices, in_map, in_map, gather);
+  return launch_pdl(kernel, dim3(per_slice * slices), dim3(Cfg::THREADS), Cfg::SMEM, s, a, slices, in_map, in_map,
+                    gather);
 }
 
 // Persistent decode tiles: kDecCS channels (bf16; half for fp32) x 127 page
@@ -863,7 +853,7 @@ constexpr int kDecCS = 64;
 constexpr int kDecNS = 4;
 constexpr int kDecNG = 2;  // consumer groups reduce alternate tiles
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool kShortWaits>
 int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
   if (a.capacity == 0) return CKV_OK;
   if (a.state_rows == 0 || a.state_rows > 0x7FFFFFFFull) return CKV_ERR_SIZE;
@@ -879,10 +869,11 @@ int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
     if (rc) return rc;
     using Cfg = PersistCfg<TIn, PCS, kDecNS, kDecNG, true>;
     static bool configured_p[64] = {};
-    rc = opt_in_smem(c128_persistent_kernel<TIn, TOut, PCS, kDecNS, kDecNG, true>, Cfg::SMEM, configured_p);
+    auto kernel = c128_persistent_kernel<TIn, TOut, PCS, kDecNS, kDecNG, true, kShortWaits>;
+    rc = opt_in_smem(kernel, Cfg::SMEM, configured_p);
     if (rc) return rc;
-    return launch_pdl(c128_persistent_kernel<TIn, TOut, PCS, kDecNS, kDecNG, true>, dim3(per_slice * pslices),
-                      dim3(Cfg::THREADS), Cfg::SMEM, s, a, pslices, page_map, page_map, GatherMaps{});
+    return launch_pdl(kernel, dim3(per_slice * pslices), dim3(Cfg::THREADS), Cfg::SMEM, s, a, pslices, page_map,
+                      page_map, GatherMaps{});
   }
   // very large batches: one CTA per (row, slice)
   constexpr int CS = DecodeCfg<TIn>::CS;
@@ -894,24 +885,29 @@ int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
   const uint64_t tiles64 = static_cast<uint64_t>(a.capacity) * slices;
   if (tiles64 > 0x7FFFFFFFull) return CKV_ERR_SIZE;
   static bool configured[64] = {};
-  rc = opt_in_smem(c128_decode_kernel<TIn, TOut>, Cfg::SMEM, configured);
+  auto kernel = c128_decode_kernel<TIn, TOut, kShortWaits>;
+  rc = opt_in_smem(kernel, Cfg::SMEM, configured);
   if (rc) return rc;
   const uint32_t tiles = static_cast<uint32_t>(tiles64);
-  return launch_pdl(c128_decode_kernel<TIn, TOut>, dim3(tiles), dim3(Cfg::THREADS), Cfg::SMEM, s, a, slices, tiles,
-                    page_map);
+  return launch_pdl(kernel, dim3(tiles), dim3(Cfg::THREADS), Cfg::SMEM, s, a, slices, tiles, page_map);
+}
+
+template <bool kDecode, typename TIn, typename TOut>
+int launch_t(const PoolArgs& a, cudaStream_t s) {
+  // kernels built for waits shorter than try_wait's window only for such limits
+  if (a.wait_ns < kShortWaitNs)
+    return kDecode ? launch_decode_t<TIn, TOut, true>(a, s) : launch_prefill_t<TIn, TOut, true>(a, s);
+  return kDecode ? launch_decode_t<TIn, TOut, false>(a, s) : launch_prefill_t<TIn, TOut, false>(a, s);
 }
 
 template <bool kDecode>
 int dispatch(const PoolArgs& a, cudaStream_t s) {
   if (a.in_dtype == CKV_BF16) {
-    if (a.out_dtype == CKV_BF16)
-      return kDecode ? launch_decode_t<__nv_bfloat16, __nv_bfloat16>(a, s)
-                     : launch_prefill_t<__nv_bfloat16, __nv_bfloat16>(a, s);
-    return kDecode ? launch_decode_t<__nv_bfloat16, float>(a, s) : launch_prefill_t<__nv_bfloat16, float>(a, s);
+    if (a.out_dtype == CKV_BF16) return launch_t<kDecode, __nv_bfloat16, __nv_bfloat16>(a, s);
+    return launch_t<kDecode, __nv_bfloat16, float>(a, s);
   }
-  if (a.out_dtype == CKV_BF16)
-    return kDecode ? launch_decode_t<float, __nv_bfloat16>(a, s) : launch_prefill_t<float, __nv_bfloat16>(a, s);
-  return kDecode ? launch_decode_t<float, float>(a, s) : launch_prefill_t<float, float>(a, s);
+  if (a.out_dtype == CKV_BF16) return launch_t<kDecode, float, __nv_bfloat16>(a, s);
+  return launch_t<kDecode, float, float>(a, s);
 }
 
 }  // namespace

@@ -179,7 +179,7 @@ __device__ __forceinline__ uint32_t c4_issue_window(const C4Maps& m, const C4Rec
   return bytes;
 }
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool kShortWaits>
 __global__ __launch_bounds__(288, 1) void c4_pool_prefill_staged_kernel(const PoolArgs a,
                                                                         const __grid_constant__ C4Maps maps) {
   using S = C4Stage<TIn>;
@@ -225,7 +225,7 @@ __global__ __launch_bounds__(288, 1) void c4_pool_prefill_staged_kernel(const Po
       const ckv_compress_plan_t cur = nxt;
       nxt = c4_load_record(a, (grp + gridDim.x) * R + lane, lane < R ? num_c : 0u);
       const int stage = static_cast<int>(g % NS);
-      if (!warp_wait_bounded(smem_addr(&empty_bar[stage]), ((g / NS) & 1u) ^ 1u, a.wait_ns)) {
+      if (!warp_wait_for<kShortWaits>(smem_addr(&empty_bar[stage]), ((g / NS) & 1u) ^ 1u, a.wait_ns)) {
         if (lane == 0) {
           status_or(a.d_status, CKV_STATUS_TIMEOUT);
           abort_flag = 1;
@@ -274,7 +274,7 @@ __global__ __launch_bounds__(288, 1) void c4_pool_prefill_staged_kernel(const Po
     nxt = c4_load_record(a, en, num_c_mine);
     nxt_prev = c4_load_record(a, en - 1, num_c_mine);
     const int stage = static_cast<int>(g % NS);
-    if (!warp_wait_bounded(smem_addr(&full_bar[stage]), (g / NS) & 1u, a.wait_ns)) {
+    if (!warp_wait_for<kShortWaits>(smem_addr(&full_bar[stage]), (g / NS) & 1u, a.wait_ns)) {
       status_or(a.d_status, CKV_STATUS_TIMEOUT);
       abort_flag = 1;
       break;
@@ -416,7 +416,7 @@ int c4_view(CUtensorMap* map, const void* base, int dtype, int hd, uint64_t rows
   return encode_tensor_map(map, dtype, 4, base, dims, strides, box);
 }
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool kShortWaits>
 int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
   using S = C4Stage<TIn>;
   const int hd = a.head_dim;
@@ -424,7 +424,7 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
   if (recs == 0) return CKV_OK;
   // tensor-map row coordinates are 32-bit
   if (a.num_q_tokens > 0x7FFFFFFFu || a.state_rows > 0x7FFFFFFFull) return CKV_ERR_SIZE;
-  auto fn = c4_pool_prefill_staged_kernel<TIn, TOut>;
+  auto fn = c4_pool_prefill_staged_kernel<TIn, TOut, kShortWaits>;
   const int smem = S::stages(hd) * static_cast<int>(S::bytes(hd));
   const int threads = S::consumers(hd) + 32;
   int dev = 0;
@@ -470,11 +470,21 @@ int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+namespace {
+
+// kernels built for waits shorter than try_wait's window only for such limits
+template <typename TIn, typename TOut>
+int launch_prefill_w(const PoolArgs& a, cudaStream_t s) {
+  return a.wait_ns < kShortWaitNs ? launch_prefill_t<TIn, TOut, true>(a, s) : launch_prefill_t<TIn, TOut, false>(a, s);
+}
+
+}  // namespace
+
 int launch_c4_pool_prefill(const PoolArgs& a, cudaStream_t s) {
   if (a.in_dtype == CKV_BF16)
-    return a.out_dtype == CKV_BF16 ? launch_prefill_t<__nv_bfloat16, __nv_bfloat16>(a, s)
-                                   : launch_prefill_t<__nv_bfloat16, float>(a, s);
-  return a.out_dtype == CKV_BF16 ? launch_prefill_t<float, __nv_bfloat16>(a, s) : launch_prefill_t<float, float>(a, s);
+    return a.out_dtype == CKV_BF16 ? launch_prefill_w<__nv_bfloat16, __nv_bfloat16>(a, s)
+                                   : launch_prefill_w<__nv_bfloat16, float>(a, s);
+  return a.out_dtype == CKV_BF16 ? launch_prefill_w<float, __nv_bfloat16>(a, s) : launch_prefill_w<float, float>(a, s);
 }
 
 int launch_c4_decode(const PoolArgs& a, cudaStream_t s) {
