@@ -198,7 +198,9 @@ struct PrefillPlanArgs {
 // record k of the compress list belongs to the request b with
 // off_c[b] <= k < off_c[b+1] (binary search), whose (k - off_c[b])-th event is
 // at position (pl/R + k - off_c[b] + 1) * R - 1.  Likewise for writes, which
-// cover positions wstart .. sl-1.
+// cover positions wstart .. sl-1.  Built per ratio, so that every division by
+// R is a shift (the kernel is a chain of dependent steps, 32 warps per CTA).
+template <int kR>
 __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const PrefillPlanArgs a) {
   __shared__ uint32_t s_off_c[kMaxBatch + 1];
   __shared__ uint32_t s_off_w[kMaxBatch + 1];
@@ -216,8 +218,8 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int R = a.ratio;
-  const int64_t slots = R == 4 ? 8 : 128;
+  constexpr int R = kR;
+  constexpr int64_t slots = R == 4 ? 8 : 128;
   if (tid == 0) s_flags = 0;
   pdl_wait();
   pdl_release();
@@ -337,7 +339,7 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
   const bool usable = total_e == a.num_q_tokens;
   const uint32_t emit_c = usable ? min(num_c, a.cap_c) : 0u;
   const uint32_t emit_w = usable ? min(num_w, a.cap_w) : 0u;
-  const int W = R == 4 ? 8 : 128;
+  constexpr int W = R == 4 ? 8 : 128;
 
   const uint32_t stride = gridDim.x * blockDim.x;
   const uint32_t work = max(a.cap_c, a.cap_w);
@@ -499,7 +501,8 @@ int launch_plan_prefill(PrefillPlanArgs a, cudaStream_t stream) {
   const uint32_t work = std::max(a.cap_c, a.cap_w);
   uint32_t grid = (work + kPlanThreads - 1) / kPlanThreads;
   grid = std::max<uint32_t>(1, std::min<uint32_t>(grid, 2u * static_cast<uint32_t>(sm_count())));
-  return launch_pdl(plan_prefill_kernel, dim3(grid), dim3(kPlanThreads), 0, stream, a);
+  return launch_pdl(a.ratio == 4 ? plan_prefill_kernel<4> : plan_prefill_kernel<128>, dim3(grid), dim3(kPlanThreads),
+                    0, stream, a);
 }
 
 // Paged arguments shared by both paged planners: C4 needs a mapping; C128
