@@ -643,6 +643,6 @@ const char* ckv_error_string(int code) {
   }
 }
 
-int ckv_version(void) { return 101; }
+int ckv_version(void) { return 102; }
 
 }  // extern "C"

@@ -102,6 +102,7 @@ def test_binding_rejects_wrong_per_request_arrays():
 
 
 def test_wait_limit_setter(lib):
+    assert lib.ckv_version() >= 102  # the setter arrived with ABI 1.02
     default = 2_000_000_000
     prev = ckv.set_wait_limit_ns(0)            # whatever was set, back to the default
     assert ckv.set_wait_limit_ns(1234) == default
