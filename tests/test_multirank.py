@@ -1,7 +1,7 @@
 """The benchmark's N-process path on CPU (gloo, world size 2): requests are
 sharded by rank (independent workloads, no collective on the data path), the
 timing is the max over ranks, the row count is the sum, and the reference arm
-runs on rank 0 alone."""
+returns at once, printing nothing, on every rank but 0."""
 import os
 import socket
 import sys
@@ -36,7 +36,17 @@ def _worker(rank, world, port, q):
         bench.barrier(world)
         # each rank draws its own independent requests (seed + rank)
         w = wl.c4_prefill(seed=rank, batch=4, head_dim=128, max_prefix=64, max_extend=64)
-        q.put((rank, t, rows, w.seq_lens.tolist()))
+        # the reference arm: every rank but 0 returns at once, without work or output
+        ref_out = None
+        if rank != 0:
+            import contextlib
+            import io
+
+            buf = io.StringIO()
+            with contextlib.redirect_stdout(buf):
+                assert bench.bench_reference(None, world, rank) is None
+            ref_out = buf.getvalue()
+        q.put((rank, t, rows, w.seq_lens.tolist(), ref_out))
     finally:
         dist.destroy_process_group()
 
@@ -53,10 +63,11 @@ def test_two_rank_reduction_and_sharding():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    (r0, t0, rows0, sl0), (r1, t1, rows1, sl1) = res
+    (r0, t0, rows0, sl0, _), (r1, t1, rows1, sl1, ref1) = res
     assert t0 == t1 == 2.5            # max over ranks
     assert rows0 == rows1 == 30.0     # whole-job count
     assert sl0 != sl1                 # independent shards
+    assert ref1 == ""                 # the reference arm printed nothing on rank 1
 
 
 def test_reference_arm_other_ranks_do_no_work(capsys):
