@@ -38,6 +38,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -145,7 +146,8 @@ class ClockSampler:
 
     def __init__(self, device_index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples go to a scratch file; the JSON line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), f"ckv_clocks_{os.getpid()}.csv")
         sel = str(device_index)
         try:
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
@@ -157,7 +159,6 @@ class ClockSampler:
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", self.sel, f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
@@ -178,7 +179,13 @@ class ClockSampler:
         self.f.close()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        for line in lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 7:
                 continue

@@ -95,3 +95,31 @@ def test_decode_bytes_from_oracle_plans(oracle_mod, ratio):
     want += W * hd * 2
     assert got["decode"] == want
     assert got["rows"] == int((f["seq_len"] % ratio == 0).sum())
+
+
+def test_clock_sampler_summary():
+    """The clocks summary of the JSON line (median SM clock, max clock, throttle
+    reasons seen), parsed from nvidia-smi's CSV rows; the scratch file is removed."""
+    import os
+
+    c = bench.ClockSampler.__new__(bench.ClockSampler)
+    c.path = os.path.join(bench.tempfile.gettempdir(), f"ckv_clocks_test_{os.getpid()}.csv")
+    with open(c.path, "w") as f:
+        f.write("2070, 2070, 900.1, Not Active, Not Active, Not Active, Active\n"
+                "1995, 2070, 1000.0, Not Active, Not Active, Not Active, Not Active\n"
+                "2070, 2070, 1010.5, Not Active, Active, Not Active, Not Active\n"
+                "[N/A], 2070, 0, Not Active, Not Active, Not Active, Not Active\n")
+
+    class Proc:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    c.f = open(os.devnull, "w")
+    c.proc = Proc()
+    got = c.stop()
+    assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["hw_thermal_slowdown", "sw_power_cap"],
+                   "samples": 3}
+    assert not os.path.exists(c.path)
