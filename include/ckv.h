@@ -91,7 +91,8 @@ enum { CKV_MAX_BATCH = 1024, CKV_MAX_TOKENS = (1 << 24) - 1 };
  *
  * ckv_set_wait_limit_ns sets that limit, in nanoseconds, for every launch made
  * after the call, process-wide (an atomic; calls from several threads are
- * safe), and returns the previous limit.  0 restores the default, 2 s.  The
+ * safe), and returns the previous limit.  0 restores the default, 2 s.  A
+ * launch captured in a CUDA graph keeps the limit in force at its capture.  The
  * outputs of a launch whose waits expired -- and, for a decode, the state row
  * it writes -- are unspecified; a limit below a copy's latency (a few
  * microseconds) makes the waits expire on purpose.  Host only: touches no
