@@ -338,16 +338,19 @@ class DecodeRunner:
         self.state = w.state.to(dev)
         self.pristine = self.state.clone()
         self.plan_d = torch.empty(max(w.batch, 1), 16, dtype=torch.uint8, device=dev)
+        # C128: the planner also lists the page-boundary rows, so the decode reads its share of windows directly
+        self.order = ckv.new_decode_order(w.batch, dev) if w.ratio == 128 else None
         self.status = ckv.new_status(dev)
         self.out = torch.empty(max(w.batch, 1), w.head_dim, dtype=w.out_dtype, device=dev)
 
     def plan(self):
-        self.ckv.plan_decode(self.w.ratio, self.rid, self.sl, self.plan_d[: self.w.batch], self.status)
+        self.ckv.plan_decode(self.w.ratio, self.rid, self.sl, self.plan_d[: self.w.batch], self.status,
+                             order=self.order)
 
     def decode(self):
         self.ckv.compress_decode(self.w.ratio, self.w.head_dim, self.state, self.kv, self.ape,
                                  self.plan_d[: self.w.batch], self.w.out_dtype, self.out[: self.w.batch],
-                                 self.status)
+                                 self.status, order=self.order)
 
     def restore(self):
         self.state.copy_(self.pristine)
@@ -360,10 +363,11 @@ class DecodeRunner:
         for i in range(n):
             st = self.state if i == 0 else self.pristine.clone()
             kv, pd, out = self.kv.clone(), self.plan_d[: self.w.batch].clone(), self.out[: self.w.batch].clone()
+            order = None if self.order is None else self.order.clone()
 
-            def fn(st=st, kv=kv, pd=pd, out=out):
+            def fn(st=st, kv=kv, pd=pd, out=out, order=order):
                 self.ckv.compress_decode(self.w.ratio, self.w.head_dim, st, kv, self.ape, pd, self.w.out_dtype, out,
-                                         self.status)
+                                         self.status, order=order)
             fns.append(fn)
         return fns
 
@@ -658,6 +662,35 @@ def same_bytes_floor(nbytes: int, dev, peak: float) -> dict:
             "frac_of_peak": 2 * half / (best * 1e-6) / 1e9 / peak}
 
 
+def instep_by_difference(segments, flush, restore, reps: int) -> dict:
+    """In-step cost of every kernel of a step, free of event nodes between kernels: the median device time
+    of the whole step graph minus the median time of the same graph with that one kernel left out (the
+    other kernels keep their programmatic launch edges).  The variants are replayed in turn, `reps` times
+    each, every replay after a state restore and an L2 flush, with CUDA events around the graph only."""
+    graphs = [("step", StepGraph(segments, inner_events=False))]
+    for i, (name, _) in enumerate(segments):
+        graphs.append((name, StepGraph([s for j, s in enumerate(segments) if j != i], inner_events=False)))
+    times = {name: [] for name, _ in graphs}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for rep in range(reps + 2):
+        for name, g in graphs:
+            restore()
+            flush.zero_()
+            torch.cuda.synchronize()
+            e0.record()
+            g.replay()
+            e1.record()
+            e1.synchronize()
+            if rep >= 2:  # two untimed rounds first
+                times[name].append(e0.elapsed_time(e1) * 1e3)
+    med = {name: statistics.median(v) for name, v in times.items()}
+    out = {"step_us": med["step"]}
+    for name, _ in segments:
+        out[f"{name}_us"] = med["step"] - med[name]
+    out["sum_us"] = sum(out[f"{n}_us"] for n, _ in segments)
+    return out
+
+
 def run_graph(step: StepGraph, flush, restore, steps, warmup, ws, sampler=None):
     """Per-step segment times (ms) of `steps` timed replays after `warmup` untimed ones."""
     for _ in range(warmup):
@@ -681,6 +714,55 @@ def run_graph(step: StepGraph, flush, restore, steps, warmup, ws, sampler=None):
     barrier(ws)
     clocks = sampler.stop() if sampler else None
     return np.array(seg), wall, clocks
+
+
+def c4_kernels(args, ckv, dev, seed: int, peak: float) -> dict:
+    """The C4 kernels on their own workloads, reported beside the headline step (which is C128): the C4
+    ragged prefill (plan -> pool -> write) and the C4 decode (plan -> decode), each step in one graph,
+    per-kernel costs inside the step by difference, the pool's and the decode's fraction of the peak, and
+    the decode back to back against its same-bytes floor."""
+    w4 = wl.c4_prefill(seed)
+    w2 = wl.c4_decode(seed)
+    pre = PrefillRunner(ckv, w4, dev)
+    dec = DecodeRunner(ckv, w2, dev)
+    flush = l2_flush_buffer(dev)
+    b4, b2 = algorithmic_bytes(w4), algorithmic_bytes(w2)
+    reps = max(20, args.steps)
+    pre_seg = [("plan_prefill", pre.plan), ("pool_prefill", pre.pool), ("write", pre.write)]
+    dec_seg = [("plan_decode", dec.plan), ("decode", dec.decode)]
+    ip = instep_by_difference(pre_seg, flush, pre.restore, reps)
+    idc = instep_by_difference(dec_seg, flush, dec.restore, reps)
+    ev_p, _, _ = run_graph(StepGraph(pre_seg), flush, pre.restore, args.steps, args.warmup, 1)
+    ev_d, _, _ = run_graph(StepGraph(dec_seg), flush, dec.restore, args.steps, args.warmup, 1)
+    if int(pre.status[0]) or int(dec.status[0]):
+        raise RuntimeError(f"device status set: c4 prefill {int(pre.status[0])} decode {int(dec.status[0])}")
+    pool_ev_us = float(ev_p[:, 1].mean()) * 1e3
+    out = {
+        "c4_prefill": {"workload": "c4_prefill B=64, prefix U[0,4096], extend U[1,4096], hd 512, bf16 -> bf16 token",
+                       "num_c": b4["num_c"], "bytes": {"pool": b4["pool"], "write": b4["write"], "plan": b4["plan"]},
+                       "events_us": {n: float(ev_p[:, i].mean()) * 1e3 for i, (n, _) in enumerate(pre_seg)},
+                       "pool_events_frac": b4["pool"] / (pool_ev_us * 1e-6) / 1e9 / peak,
+                       "instep": ip,
+                       "pool_instep_frac": (b4["pool"] / (ip["pool_prefill_us"] * 1e-6) / 1e9 / peak
+                                            if ip["pool_prefill_us"] > 0 else None)},
+        "c4_decode": {"workload": "c4_decode B=256, seq_len U[1,8192], hd 512, bf16 -> f32", "rows": b2["rows"],
+                      "bytes": b2["decode"],
+                      "events_us": {n: float(ev_d[:, i].mean()) * 1e3 for i, (n, _) in enumerate(dec_seg)},
+                      "instep": idc,
+                      "decode_instep_frac": (b2["decode"] / (idc["decode_us"] * 1e-6) / 1e9 / peak
+                                             if idc["decode_us"] > 0 else None)},
+    }
+    if not args.no_back_to_back:
+        n = copies_for(b2["decode"], dev)
+        us = steady_state_us(dec.steady_fns(n))
+        floor = same_bytes_floor(b2["decode"], dev, peak)
+        best = min(floor["copy_us"], floor["elementwise_us"])
+        out["c4_decode"].update({"back_to_back_us": us,
+                                 "back_to_back_frac": b2["decode"] / (us * 1e-6) / 1e9 / peak,
+                                 "same_bytes_floor": floor, "floor_ratio": us / best})
+    del pre, dec
+    torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------------------------- CPU baseline (oracle)
@@ -729,13 +811,10 @@ def bench_step(args, ws, rank, local):
 
     def restore():
         pre.restore()
+        dec.restore()
 
-    def write_and_plan_d():
-        pre.write()
-        dec.plan()
-
-    segments = [("plan_prefill", pre.plan), ("pool_prefill", pre.pool), ("write+plan_decode", write_and_plan_d),
-                ("decode", dec.decode)]
+    segments = [("plan_prefill", pre.plan), ("pool_prefill", pre.pool), ("write", pre.write),
+                ("plan_decode", dec.plan), ("decode", dec.decode)]
     step = StepGraph(segments, inner_events=False)
     timed = StepGraph(segments, inner_events=True)
     launches_per_step = 5
@@ -758,9 +837,17 @@ def bench_step(args, ws, rank, local):
     peak, peak_kind = peaks()
     pool_ms = float(seg_ms[:, 1].mean())
     pool_gbs = b5["pool"] / (pool_ms * 1e-3) / 1e9
-    dec_ms = float(seg_ms[:, 3].mean())
+    dec_ms = float(seg_ms[:, 4].mean())
     dec_gbs = b3["decode"] / (dec_ms * 1e-3) / 1e9
     step_bytes = b5["total"] + b3["total"]
+    # every kernel's cost inside the timed step, by difference (no event nodes between the kernels)
+    instep = instep_by_difference(segments, flush, restore, reps=max(20, args.steps))
+    for key, nbytes in (("pool_prefill", b5["pool"]), ("write", b5["write"]), ("decode", b3["decode"])):
+        us = instep[f"{key}_us"]
+        instep[f"{key}_instep_gbs"] = nbytes / (us * 1e-6) / 1e9 if us > 0 else None
+        instep[f"{key}_instep_frac"] = instep[f"{key}_instep_gbs"] / peak if us > 0 else None
+    instep["method"] = ("median step time minus the median time of the step without that kernel; "
+                        f"{max(20, args.steps)} interleaved replays per variant, L2 flushed before each")
     # the decode kernel back to back over copies of its inputs that together exceed the L2 (a kernel of ~10 us
     # is not resolved by event nodes around it: they add the graph's node-to-node latency)
     back_to_back = {}
@@ -773,6 +860,16 @@ def bench_step(args, ws, rank, local):
                         "decode_back_to_back_frac": gbs / peak, "decode_back_to_back_copies": n_dec,
                         "decode_same_bytes_floor": floor,
                         "decode_vs_floor": min(floor["copy_us"], floor["elementwise_us"]) / us}
+        # the prefill write back to back, with its own same-bytes floor
+        n_w = copies_for(b5["write"], dev)
+        us = steady_state_us(pre.steady_fns(n_w, "write"))
+        gbs = b5["write"] / (us * 1e-6) / 1e9
+        floor = same_bytes_floor(b5["write"], dev, peak)
+        back_to_back.update({"write_back_to_back_us": us, "write_back_to_back_gbs": gbs,
+                             "write_back_to_back_frac": gbs / peak, "write_same_bytes_floor": floor,
+                             "write_vs_floor": min(floor["copy_us"], floor["elementwise_us"]) / us})
+        pre.restore()
+        torch.cuda.synchronize()
 
     # ---- end to end: inputs from pinned host memory, outputs back, inside the timed region
     h_kv5 = w5.kv_score.pin_memory()
@@ -826,11 +923,15 @@ def bench_step(args, ws, rank, local):
         "kernels": {
             "plan_prefill_us": float(seg_ms[:, 0].mean()) * 1e3,
             "pool_prefill_us": pool_ms * 1e3, "pool_prefill_gbs": pool_gbs,
-            "write_plus_plan_decode_us": float(seg_ms[:, 2].mean()) * 1e3,
+            "write_us": float(seg_ms[:, 2].mean()) * 1e3, "plan_decode_us": float(seg_ms[:, 3].mean()) * 1e3,
             "decode_us": dec_ms * 1e3, "decode_gbs": dec_gbs, "decode_frac": dec_gbs / peak,
+            "event_node_note": "the *_us above are timed with event nodes between the kernels; instep has "
+                               "the costs inside the timed step",
+            "instep": instep,
             **back_to_back,
             "sum_of_kernel_segments_us": float(seg_ms.sum(1).mean()) * 1e3,
             "step_gbs": step_bytes / (float(step_ms.mean()) * 1e-3) / 1e9},
+        "kernels_c4": c4_kernels(args, ckv, dev, seed, peak) if not args.no_c4 else None,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
@@ -1049,6 +1150,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true", help="with --config: scaled-down workloads for profiling")
+    ap.add_argument("--no-c4", action="store_true", help="skip the C4 kernels block of the step line")
     ap.add_argument("--no-back-to-back", action="store_true",
                     help="skip the back-to-back timing of short kernels (keeps a profiler's launch list to the step)")
     ap.add_argument("--ref-fraction", type=float, default=0.125,

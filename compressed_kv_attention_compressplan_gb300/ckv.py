@@ -63,20 +63,20 @@ def load_library():
         lib.ckv_capacity_compress.restype = u32
         lib.ckv_capacity_write.argtypes = [i32, u32, u32]
         lib.ckv_capacity_write.restype = u32
-        lib.ckv_plan_decode.argtypes = [i32, vp, vp, u32, vp, vp, vp]
+        lib.ckv_plan_decode.argtypes = [i32, vp, vp, u32, vp, vp, vp, vp]
         i64 = ctypes.c_int64
         lib.ckv_capacity_write_paged.argtypes = [i32, u32, u32, i32]
         lib.ckv_capacity_write_paged.restype = u32
         lib.ckv_plan_prefill_paged.argtypes = [i32, vp, vp, i64, u32, vp, u64, i32, i32, vp, vp, u32, u32, u32, u32,
                                                i32, vp, vp, vp, vp, vp]
-        lib.ckv_plan_decode_paged.argtypes = [i32, vp, vp, i64, u32, vp, u64, i32, i32, vp, u32, vp, vp, vp]
+        lib.ckv_plan_decode_paged.argtypes = [i32, vp, vp, i64, u32, vp, u64, i32, i32, vp, u32, vp, vp, vp, vp]
         lib.ckv_plan_prefill.argtypes = [i32, vp, vp, vp, u32, u32, u32, u32, i32, vp, vp, vp, vp, vp]
         lib.ckv_compress_write.argtypes = [i32, i32, i32, vp, u64, vp, u32, vp, vp, u32, vp, vp]
         lib.ckv_compress_pool_prefill.argtypes = [i32, i32, i32, i32, vp, u64, vp, u32, vp, vp, vp, u32, i32, vp,
                                                   vp, vp]
         lib.ckv_compress_prefill.argtypes = [i32, i32, i32, i32, vp, u64, vp, u32, vp, vp, vp, vp, u32, u32, i32,
                                              vp, vp, vp]
-        lib.ckv_compress_decode.argtypes = [i32, i32, i32, i32, vp, u64, vp, vp, vp, u32, vp, vp, vp]
+        lib.ckv_compress_decode.argtypes = [i32, i32, i32, i32, vp, u64, vp, vp, vp, vp, u32, vp, vp, vp]
         f32 = ctypes.c_float
         lib.ckv_capacity_online_units.argtypes = [u32, u32]
         lib.ckv_capacity_online_units.restype = u32
@@ -174,14 +174,28 @@ def new_status(device=None) -> torch.Tensor:
 
 
 # ------------------------------------------------------------------------------ plans
+def new_decode_order(batch: int, device=None) -> torch.Tensor:
+    """Storage for a decode batch's boundary-row list: ``[batch + 1, 8]`` uint8 (``ckv_decode_order_t``)."""
+    return torch.empty(batch + 1, 8, dtype=torch.uint8, device=device or "cuda")
+
+
+def _order(order: Optional[torch.Tensor], batch: int):
+    if order is None:
+        return None
+    if order.dtype != torch.uint8 or order.dim() != 2 or order.shape[1] != 8 or order.shape[0] < batch + 1:
+        raise ValueError("a decode order is a uint8 tensor [batch + 1, 8] (new_decode_order)")
+    return _ptr(order)
+
+
 def plan_decode(ratio: int, rid: torch.Tensor, seq_lens: torch.Tensor, plan_d: Optional[torch.Tensor] = None,
-                status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """DecodePlan records ``[batch, 16]`` uint8."""
+                status: Optional[torch.Tensor] = None, stream=None, order: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """DecodePlan records ``[batch, 16]`` uint8.  With ``order`` (``new_decode_order``), the batch's
+    page-boundary rows are also written there, in row order."""
     batch = _lengths(rid, seq_lens)
     if plan_d is None:
         plan_d = torch.empty(max(batch, 1), 16, dtype=torch.uint8, device=rid.device)
-    _check(load_library().ckv_plan_decode(ratio, _ptr(rid), _ptr(seq_lens), batch, _ptr(plan_d), _ptr(status),
-                                          _stream(stream)), "ckv_plan_decode")
+    _check(load_library().ckv_plan_decode(ratio, _ptr(rid), _ptr(seq_lens), batch, _ptr(plan_d),
+                                          _order(order, batch), _ptr(status), _stream(stream)), "ckv_plan_decode")
     return plan_d[:batch]
 
 
@@ -254,12 +268,14 @@ def plan_prefill_paged(ratio: int, rid: torch.Tensor, req_to_token: torch.Tensor
 
 def plan_decode_paged(ratio: int, rid: torch.Tensor, req_to_token: torch.Tensor, full_to_state: torch.Tensor,
                       swa_page_size: int, ring_size: int, seq_lens: torch.Tensor,
-                      status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                      status: Optional[torch.Tensor] = None, stream=None,
+                      order: Optional[torch.Tensor] = None) -> torch.Tensor:
     batch = _lengths(rid, seq_lens)
     plan_d = torch.empty(max(batch, 1), 16, dtype=torch.uint8, device=rid.device)
     r2t, stride, nreq, f2s, nfull = _paged_maps(req_to_token, full_to_state)
     _check(load_library().ckv_plan_decode_paged(ratio, _ptr(rid), r2t, stride, nreq, f2s, nfull, swa_page_size,
-                                                ring_size, _ptr(seq_lens), batch, _ptr(plan_d), _ptr(status), _stream(stream)),
+                                                ring_size, _ptr(seq_lens), batch, _ptr(plan_d), _order(order, batch),
+                                                _ptr(status), _stream(stream)),
            "ckv_plan_decode_paged")
     return plan_d[:batch]
 
@@ -317,14 +333,16 @@ def compress_prefill(ratio: int, head_dim: int, state: torch.Tensor, kv_score: t
 
 def compress_decode(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
                     plan_d: torch.Tensor, out_dtype: torch.dtype = torch.float32, out: Optional[torch.Tensor] = None,
-                    status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                    status: Optional[torch.Tensor] = None, stream=None,
+                    order: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode step over ``plan_d``; ``order`` is the boundary-row list plan_decode wrote for it (optional)."""
     batch = plan_d.shape[0]
     if out is None:
         out = torch.empty(max(batch, 1), head_dim, dtype=out_dtype, device=kv_score.device)
     _check(load_library().ckv_compress_decode(ratio, head_dim, dtype_code(kv_score.dtype), dtype_code(out.dtype),
                                               _ptr(state), _state_rows(state, ratio, head_dim), _ptr(kv_score),
-                                              _ptr(ape), _ptr(plan_d), batch, _ptr(out), _ptr(status),
-                                              _stream(stream)), "ckv_compress_decode")
+                                              _ptr(ape), _ptr(plan_d), _order(order, batch), batch, _ptr(out),
+                                              _ptr(status), _stream(stream)), "ckv_compress_decode")
     return out[:batch]
 
 
@@ -453,7 +471,9 @@ def prefill_step(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch
 def decode_step(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
                 rid: torch.Tensor, seq_lens: torch.Tensor, out_dtype: torch.dtype = torch.float32,
                 status: Optional[torch.Tensor] = None, stream=None):
-    """plan_decode -> decode.  Returns ``(out, plan_d)``."""
-    plan_d = plan_decode(ratio, rid, seq_lens, status=status, stream=stream)
-    out = compress_decode(ratio, head_dim, state, kv_score, ape, plan_d, out_dtype, status=status, stream=stream)
+    """plan_decode (with the boundary-row list) -> decode.  Returns ``(out, plan_d)``."""
+    order = new_decode_order(rid.numel(), rid.device)
+    plan_d = plan_decode(ratio, rid, seq_lens, status=status, stream=stream, order=order)
+    out = compress_decode(ratio, head_dim, state, kv_score, ape, plan_d, out_dtype, status=status, stream=stream,
+                          order=order)
     return out, plan_d

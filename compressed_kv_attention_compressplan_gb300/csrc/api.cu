@@ -31,7 +31,10 @@ uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed
 extern "C" {
 
 uint64_t ckv_set_wait_limit_ns(uint64_t limit_ns) {
-  return g_wait_limit_ns.exchange(limit_ns == 0 ? kWaitLimitNs : limit_ns, std::memory_order_relaxed);
+  // a limit beyond the ceiling would make `now - start > limit` unreachable
+  // in practice, i.e. the waits unbounded again
+  const uint64_t v = limit_ns == 0 ? kWaitLimitNs : (limit_ns > kWaitLimitMaxNs ? kWaitLimitMaxNs : limit_ns);
+  return g_wait_limit_ns.exchange(v, std::memory_order_relaxed);
 }
 
 int ckv_compress_pool_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, const void* state,
@@ -90,12 +93,14 @@ int ckv_compress_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, v
 
 int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, void* state, uint64_t state_rows,
                         const void* kv_score_input, const void* ape, const ckv_decode_plan_t* plan_d,
-                        uint32_t batch, void* out, uint32_t* d_status, ckv_stream_t stream) {
+                        const ckv_decode_order_t* order, uint32_t batch, void* out, uint32_t* d_status,
+                        ckv_stream_t stream) {
   int rc = check_pool_args(ratio, head_dim, in_dtype, out_dtype);
   if (rc) return rc;
   if (batch == 0) return CKV_OK;
   if (!aligned16(state) || !aligned16(kv_score_input) || !aligned16(ape) || !aligned16(plan_d) || !aligned16(out))
     return CKV_ERR_POINTER;
+  if (reinterpret_cast<uintptr_t>(order) & 7u) return CKV_ERR_POINTER;
   PoolArgs a{};
   a.ratio = ratio;
   a.head_dim = head_dim;
@@ -108,6 +113,7 @@ int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, vo
   a.num_q_tokens = batch;
   a.ape = ape;
   a.plan_d = plan_d;
+  a.order = order;
   a.capacity = batch;
   a.out_layout = CKV_OUT_TOKEN;
   a.out = out;

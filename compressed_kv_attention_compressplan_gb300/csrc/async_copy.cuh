@@ -24,6 +24,9 @@ namespace ckv {
 // 2 s, far beyond any real copy: the default limit of the ordinary waits, and
 // the limit of the waits for copies in flight before a CTA exits
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// the largest limit ckv_set_wait_limit_ns accepts (10 s); larger values are
+// clamped to it, so every wait stays bounded
+constexpr uint64_t kWaitLimitMaxNs = 10000000000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -24,6 +24,7 @@ struct PoolArgs {
   const void* ape;
   const ckv_compress_plan_t* plan_c;  // prefill
   const ckv_decode_plan_t* plan_d;    // decode
+  const ckv_decode_order_t* order;    // decode: boundary rows in row order (NULL: the kernel scans plan_d)
   const uint32_t* d_counts;           // prefill
   uint32_t capacity;                  // prefill: capacity_c; decode: batch
   int out_layout;

@@ -64,27 +64,102 @@ __device__ __forceinline__ uint32_t warp_min(uint32_t v) {
   return v;
 }
 
+// The legacy DecodePlan record of one row (c_plan.cuh
+// plan_compress_decode_legacy_kernel); rows with bad lengths get the invalid
+// record and set CKV_STATUS_BAD_LENGTH.
+__device__ __forceinline__ uint4 legacy_decode_record(int ratio, int64_t sl, int64_t r, uint32_t* d_status) {
+  const int64_t slots = ratio == 4 ? 8 : 128;
+  if (sl >= 1 && sl <= INT32_MAX && r >= 0 && r * slots + slots - 1 <= INT32_MAX) {
+    const int32_t p1 = static_cast<int32_t>(sl - 1);
+    const int32_t p0 = max(p1 - ratio, 0);
+    const int32_t rr = static_cast<int32_t>(r);
+    return make_uint4(static_cast<uint32_t>(sl), static_cast<uint32_t>(legacy_loc(ratio, rr, p1)),
+                      static_cast<uint32_t>(legacy_page(ratio, rr, p0)),
+                      static_cast<uint32_t>(legacy_page(ratio, rr, p1)));
+  }
+  status_or(d_status, CKV_STATUS_BAD_LENGTH);
+  return make_uint4(kInvalidU32, kInvalidU32, kInvalidU32, kInvalidU32);
+}
+
 __global__ void plan_decode_kernel(int ratio, const int64_t* __restrict__ rid, const int64_t* __restrict__ seq_lens,
                                    uint32_t batch, ckv_decode_plan_t* __restrict__ plan_d, uint32_t* d_status) {
   pdl_wait();
   pdl_release();
   const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
-  const int64_t sl = seq_lens[b];
-  const int64_t r = rid[b];
-  const int64_t slots = ratio == 4 ? 8 : 128;
-  uint4 rec = make_uint4(kInvalidU32, kInvalidU32, kInvalidU32, kInvalidU32);
-  if (sl >= 1 && sl <= INT32_MAX && r >= 0 && r * slots + slots - 1 <= INT32_MAX) {
-    const int32_t p1 = static_cast<int32_t>(sl - 1);
-    const int32_t p0 = max(p1 - ratio, 0);
-    const int32_t rr = static_cast<int32_t>(r);
-    rec = make_uint4(static_cast<uint32_t>(sl), static_cast<uint32_t>(legacy_loc(ratio, rr, p1)),
-                     static_cast<uint32_t>(legacy_page(ratio, rr, p0)),
-                     static_cast<uint32_t>(legacy_page(ratio, rr, p1)));
-  } else {
-    status_or(d_status, CKV_STATUS_BAD_LENGTH);
+  *reinterpret_cast<uint4*>(plan_d + b) = legacy_decode_record(ratio, seq_lens[b], rid[b], d_status);
+}
+
+// The boundary list of a decode batch next to its records: one CTA of
+// kPlanThreads threads walks the batch in chunks of K * kPlanThreads rows
+// (thread t takes rows chunk + K*t .. chunk + K*t + K-1), and a block-wide
+// exclusive scan of the per-thread counts of valid records with
+// seq_len % ratio == 0 places each such row's entry {row, read_page_0}, so
+// the list is in row order.  order[0] = {count, 0}.  rec_of(b) computes row
+// b's record (its loads are issued for all K rows before any is used).
+template <int K, typename RecOf>
+__device__ __forceinline__ void plan_decode_ordered_body(int ratio, uint32_t batch, ckv_decode_plan_t* plan_d,
+                                                         ckv_decode_order_t* order, RecOf rec_of) {
+  __shared__ uint32_t s_warp[kWarps];
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int warp = t >> 5;
+  uint32_t base = 0;
+  for (uint32_t chunk = 0; chunk < batch; chunk += K * kPlanThreads) {
+    uint4 rec[K];
+    bool take[K];
+    uint32_t cnt = 0;
+    rec_of(chunk + K * t, rec);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const uint32_t b = chunk + K * t + k;
+      take[k] = false;
+      if (b < batch) {
+        *reinterpret_cast<uint4*>(plan_d + b) = rec[k];
+        take[k] = rec[k].x != kInvalidU32 && rec[k].x % static_cast<uint32_t>(ratio) == 0;
+      }
+      cnt += take[k] ? 1u : 0u;
+    }
+    const uint32_t incl = warp_inclusive_sum(cnt, lane);
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    uint32_t pos = base + incl - cnt, total = 0;
+#pragma unroll 8
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t v = s_warp[w];
+      if (w < warp) pos += v;
+      total += v;
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      if (take[k]) {
+        *reinterpret_cast<uint2*>(order + 1 + pos) = make_uint2(chunk + K * t + k, rec[k].z);
+        ++pos;
+      }
+    }
+    base += total;
+    __syncthreads();  // s_warp is rewritten by the next chunk
   }
-  *reinterpret_cast<uint4*>(plan_d + b) = rec;
+  if (t == 0) *reinterpret_cast<uint2*>(order) = make_uint2(base, 0u);
+}
+
+template <int K>
+__global__ __launch_bounds__(kPlanThreads, 1) void plan_decode_ordered_kernel(
+    int ratio, const int64_t* __restrict__ rid, const int64_t* __restrict__ seq_lens, uint32_t batch,
+    ckv_decode_plan_t* __restrict__ plan_d, ckv_decode_order_t* __restrict__ order, uint32_t* d_status) {
+  pdl_wait();
+  pdl_release();
+  plan_decode_ordered_body<K>(ratio, batch, plan_d, order, [&](uint32_t b0, uint4 (&rec)[K]) {
+    int64_t sl[K], r[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      sl[k] = b0 + k < batch ? seq_lens[b0 + k] : 0;
+      r[k] = b0 + k < batch ? rid[b0 + k] : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+      rec[k] = b0 + k < batch ? legacy_decode_record(ratio, sl[k], r[k], d_status) : make_uint4(0, 0, 0, 0);
+  });
 }
 
 // c_plan.cuh compute_loc: an SWA slot swa lives in the ring of its SWA page,
@@ -130,13 +205,7 @@ struct DecodePagedArgs {
 // c_plan.cuh plan_compress_decode_kernel (C4 through the SWA mapping):
 // write_loc = ring(state of position seq_len-1), read pages of positions
 // max(seq_len-1-4, 0) and seq_len-1.
-__global__ void plan_decode_paged_kernel(const DecodePagedArgs a) {
-  pdl_wait();
-  pdl_release();
-  const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= a.batch) return;
-  const int64_t sl = a.seq_lens[b];
-  const int64_t r = a.rid[b];
+__device__ __forceinline__ uint4 paged_decode_record(const DecodePagedArgs& a, int64_t sl, int64_t r) {
   uint4 rec = make_uint4(kInvalidU32, kInvalidU32, kInvalidU32, kInvalidU32);
   if (sl >= 1 && sl <= INT32_MAX && r >= 0) {
     if (r < a.num_reqs && sl <= a.r2t_stride) {
@@ -156,7 +225,32 @@ __global__ void plan_decode_paged_kernel(const DecodePagedArgs a) {
   } else {
     status_or(a.d_status, CKV_STATUS_BAD_LENGTH);
   }
-  *reinterpret_cast<uint4*>(a.plan_d + b) = rec;
+  return rec;
+}
+
+__global__ void plan_decode_paged_kernel(const DecodePagedArgs a) {
+  pdl_wait();
+  pdl_release();
+  const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= a.batch) return;
+  *reinterpret_cast<uint4*>(a.plan_d + b) = paged_decode_record(a, a.seq_lens[b], a.rid[b]);
+}
+
+template <int K>
+__global__ __launch_bounds__(kPlanThreads, 1) void plan_decode_paged_ordered_kernel(const DecodePagedArgs a,
+                                                                                   ckv_decode_order_t* order) {
+  pdl_wait();
+  pdl_release();
+  plan_decode_ordered_body<K>(4, a.batch, a.plan_d, order, [&](uint32_t b0, uint4 (&rec)[K]) {
+    int64_t sl[K], r[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      sl[k] = b0 + k < a.batch ? a.seq_lens[b0 + k] : 0;
+      r[k] = b0 + k < a.batch ? a.rid[b0 + k] : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) rec[k] = b0 + k < a.batch ? paged_decode_record(a, sl[k], r[k]) : make_uint4(0, 0, 0, 0);
+  });
 }
 
 struct PrefillPlanArgs {
@@ -470,14 +564,24 @@ uint32_t ckv_capacity_write(int ratio, uint32_t batch, uint32_t num_q_tokens) {
 }
 
 int ckv_plan_decode(int ratio, const int64_t* rid, const int64_t* seq_lens, uint32_t batch,
-                    ckv_decode_plan_t* plan_d, uint32_t* d_status, ckv_stream_t stream) {
+                    ckv_decode_plan_t* plan_d, ckv_decode_order_t* order, uint32_t* d_status, ckv_stream_t stream) {
   if (ratio != 4 && ratio != 128) return CKV_ERR_RATIO;
-  if (batch == 0) return CKV_OK;
-  if (!rid || !seq_lens || !aligned16(plan_d)) return CKV_ERR_POINTER;
+  if (batch == 0 && order == nullptr) return CKV_OK;
+  if (batch > 0 && (!rid || !seq_lens || !aligned16(plan_d))) return CKV_ERR_POINTER;
   if ((reinterpret_cast<uintptr_t>(rid) | reinterpret_cast<uintptr_t>(seq_lens)) & 7u) return CKV_ERR_POINTER;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (order != nullptr) {
+    if (reinterpret_cast<uintptr_t>(order) & 7u) return CKV_ERR_POINTER;
+    // one CTA: the list is a block-wide scan over the whole batch
+    if (batch <= kPlanThreads)
+      return launch_pdl(plan_decode_ordered_kernel<1>, dim3(1), dim3(kPlanThreads), 0, s, ratio, rid, seq_lens, batch,
+                        plan_d, order, d_status);
+    return launch_pdl(plan_decode_ordered_kernel<4>, dim3(1), dim3(kPlanThreads), 0, s, ratio, rid, seq_lens, batch,
+                      plan_d, order, d_status);
+  }
   const uint32_t threads = 256;
-  return launch_pdl(plan_decode_kernel, dim3((batch + threads - 1) / threads), dim3(threads), 0,
-                    reinterpret_cast<cudaStream_t>(stream), ratio, rid, seq_lens, batch, plan_d, d_status);
+  return launch_pdl(plan_decode_kernel, dim3((batch + threads - 1) / threads), dim3(threads), 0, s, ratio, rid,
+                    seq_lens, batch, plan_d, d_status);
 }
 
 namespace {
@@ -609,18 +713,25 @@ int ckv_plan_prefill_paged(int ratio, const int64_t* rid, const int32_t* req_to_
 int ckv_plan_decode_paged(int ratio, const int64_t* rid, const int32_t* req_to_token, int64_t r2t_stride,
                           uint32_t num_reqs, const int64_t* full_to_state, uint64_t num_full_slots,
                           int32_t swa_page_size, int32_t ring_size, const int64_t* seq_lens, uint32_t batch,
-                          ckv_decode_plan_t* plan_d, uint32_t* d_status, ckv_stream_t stream) {
+                          ckv_decode_plan_t* plan_d, ckv_decode_order_t* order, uint32_t* d_status,
+                          ckv_stream_t stream) {
   const int rc = check_paged(ratio, req_to_token, r2t_stride, full_to_state, swa_page_size, ring_size);
   if (rc) return rc;
-  if (ratio == 128) return ckv_plan_decode(ratio, rid, seq_lens, batch, plan_d, d_status, stream);
-  if (batch == 0) return CKV_OK;
-  if (!rid || !seq_lens || !aligned16(plan_d)) return CKV_ERR_POINTER;
+  if (ratio == 128) return ckv_plan_decode(ratio, rid, seq_lens, batch, plan_d, order, d_status, stream);
+  if (batch == 0 && order == nullptr) return CKV_OK;
+  if (batch > 0 && (!rid || !seq_lens || !aligned16(plan_d))) return CKV_ERR_POINTER;
   if ((reinterpret_cast<uintptr_t>(rid) | reinterpret_cast<uintptr_t>(seq_lens)) & 7u) return CKV_ERR_POINTER;
   DecodePagedArgs a{rid, seq_lens, batch, req_to_token, r2t_stride, num_reqs, full_to_state, num_full_slots,
                     swa_page_size, ring_size, plan_d, d_status};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (order != nullptr) {
+    if (reinterpret_cast<uintptr_t>(order) & 7u) return CKV_ERR_POINTER;
+    if (batch <= kPlanThreads)
+      return launch_pdl(plan_decode_paged_ordered_kernel<1>, dim3(1), dim3(kPlanThreads), 0, s, a, order);
+    return launch_pdl(plan_decode_paged_ordered_kernel<4>, dim3(1), dim3(kPlanThreads), 0, s, a, order);
+  }
   const uint32_t threads = 256;
-  return launch_pdl(plan_decode_paged_kernel, dim3((batch + threads - 1) / threads), dim3(threads), 0,
-                    reinterpret_cast<cudaStream_t>(stream), a);
+  return launch_pdl(plan_decode_paged_kernel, dim3((batch + threads - 1) / threads), dim3(threads), 0, s, a);
 }
 
 uint32_t ckv_capacity_write_paged(int ratio, uint32_t batch, uint32_t num_q_tokens, int32_t swa_page_size) {
@@ -643,6 +754,6 @@ const char* ckv_error_string(int code) {
   }
 }
 
-int ckv_version(void) { return 102; }
+int ckv_version(void) { return 200; }
 
 }  // extern "C"

@@ -351,7 +351,8 @@ struct PersistCfg {
   using T = TileCfg<TIn, CS>;
   static constexpr int NCG = T::THREADS;   // threads of one consumer group
   static constexpr int NC = NG * NCG;      // all consumer threads
-  static constexpr int THREADS = NC + 32;  // + the producer warp
+  static constexpr int NSIDE = kDecode ? 64 : 0;  // decode: side warps for the rows that read no page
+  static constexpr int THREADS = NC + 32 + NSIDE;  // + the producer warp
   static constexpr int SMEM = NS * T::TILE_BYTES + 2 * NG * T::RED_FLOATS * 4 + (kDecode ? kOwnRows * 24 : 0);
   static_assert(NS % NG == 0, "each consumer group owns every NG-th stage");
 };
@@ -379,19 +380,36 @@ __device__ __forceinline__ bool decode_row(const PoolArgs& a, uint32_t r, bool& 
   return true;
 }
 
-// The rows of a decode step that read no page, by NTH threads of one CTA:
-// every row in `rows` ({row, write_loc, flags}) writes its new token to its
-// slot (never one of the 127 slots any window reads), and rows that emit
-// nothing get a zero output row.  Each thread owns fixed 16-byte chunk
-// positions and batches several rows, so its loads are all in flight at once.
+// Entry of the boundary list (ckv_decode_order_t, written by the previous
+// kernel: a coherent load).  Entries that point outside the batch or the
+// state come back as {kInvalidU32, 0}.
+__device__ __forceinline__ uint2 load_order_entry(const PoolArgs& a, uint32_t idx) {
+  uint2 v;
+  asm volatile("ld.global.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(a.order + idx));
+  const int32_t page = static_cast<int32_t>(v.y);
+  const bool ok = v.x < a.capacity && page >= 0 && static_cast<uint64_t>(page) * 128 + 127 < a.state_rows;
+  return ok ? v : make_uint2(kInvalidU32, 0u);
+}
+
+__device__ __forceinline__ uint32_t load_order_count(const PoolArgs& a) {
+  uint32_t v;
+  asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(a.order));
+  return v;
+}
+
+// The rows of a decode step that read no page: every row in `rows` ({row,
+// write_loc, flags}) writes its new token to its slot (never one of the 127
+// slots any window reads), and rows that emit nothing get a zero output row.
 constexpr uint32_t kRowValid = 1u, kRowBoundary = 2u;
 
+// They are written by the side warps (NTH threads), which do nothing else: a
+// batch of rows has all its input chunks in flight before the first store.
 template <typename TIn, typename TOut, int NTH>
-__device__ __forceinline__ void decode_rows_without_window(const PoolArgs& a, const uint4* rows, uint32_t nrows,
-                                                           int tl) {
+__device__ __forceinline__ void decode_rows_side(const PoolArgs& a, const uint4* rows, uint32_t nrows, int tl) {
   constexpr int kVec = 16 / static_cast<int>(sizeof(TIn));
   constexpr int kOutVec = 16 / static_cast<int>(sizeof(TOut));
-  constexpr int kRows = 4;  // rows per batch: all their loads are issued before any store
+  constexpr int kRows = 4;    // rows per batch
+  constexpr int kChunks = 4;  // 16-byte chunks per thread and row per round
   const int hd = a.head_dim;
   const int width = 2 * hd;
   const int in_chunks = width / kVec;
@@ -399,26 +417,59 @@ __device__ __forceinline__ void decode_rows_without_window(const PoolArgs& a, co
   const TIn* input = static_cast<const TIn*>(a.input);
   TIn* state = static_cast<TIn*>(a.state_mut);
   TOut* out = static_cast<TOut*>(a.out);
-  // thread position c: chunk c of the state copy, or chunk c - in_chunks of the zero row
-  for (int c = tl; c < in_chunks + out_chunks; c += NTH) {
-    for (uint32_t base = 0; base < nrows; base += kRows) {
-      uint4 v[kRows];
-      uint4 rec[kRows];
+  for (uint32_t base = 0; base < nrows; base += kRows) {
+    uint4 rec[kRows];
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        rec[k] = base + k < nrows ? rows[base + k] : make_uint4(0, 0, 0, 0);
-        if (c < in_chunks && (rec[k].z & kRowValid))
-          v[k] = ld_stream16(input + static_cast<size_t>(rec[k].x) * width + c * kVec);
-      }
+    for (int k = 0; k < kRows; ++k) rec[k] = base + k < nrows ? rows[base + k] : make_uint4(0, 0, 0, 0);
+    for (int cb = 0; cb < in_chunks; cb += kChunks * NTH) {
+      uint4 v[kRows][kChunks];
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        if (base + k >= nrows) break;
-        if (c < in_chunks) {
-          if (rec[k].z & kRowValid) st16(state + static_cast<size_t>(rec[k].y) * width + c * kVec, v[k]);
-        } else if (!((rec[k].z & kRowValid) && (rec[k].z & kRowBoundary))) {
-          st16(out + static_cast<size_t>(rec[k].x) * hd + (c - in_chunks) * kOutVec, make_uint4(0, 0, 0, 0));
+      for (int k = 0; k < kRows; ++k)
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+          const int c = cb + j * NTH + tl;
+          if (c < in_chunks && (rec[k].z & kRowValid))
+            v[k][j] = ld_stream16(input + static_cast<size_t>(rec[k].x) * width + c * kVec);
         }
-      }
+#pragma unroll
+      for (int k = 0; k < kRows; ++k)
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+          const int c = cb + j * NTH + tl;
+          if (c < in_chunks && (rec[k].z & kRowValid))
+            st16(state + static_cast<size_t>(rec[k].y) * width + c * kVec, v[k][j]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      if (base + k < nrows && !((rec[k].z & kRowValid) && (rec[k].z & kRowBoundary)))
+        for (int c = tl; c < out_chunks; c += NTH)
+          st16(out + static_cast<size_t>(rec[k].x) * hd + c * kOutVec, make_uint4(0, 0, 0, 0));
+    }
+  }
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// The ape slice into registers with loads the compiler keeps where they are
+// written (issued at once, used by the first tile).
+template <typename TIn>
+__device__ __forceinline__ void load_ape_regs_now(const TIn* ape, int hd, int c0, int g, int cq, F2 (&ape_r)[16][2]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const TIn* p = ape + static_cast<size_t>(16 * g + k) * hd + c0 + cq;
+    if constexpr (sizeof(TIn) == 2) {
+      uint32_t x, y;
+      asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "l"(p));
+      ape_r[k][0] = f2_from_bf16x2(x);
+      ape_r[k][1] = f2_from_bf16x2(y);
+    } else {
+      float x, y, z, w;
+      asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(x), "=f"(y), "=f"(z), "=f"(w) : "l"(p));
+      ape_r[k][0] = f2_pack(x, y);
+      ape_r[k][1] = f2_pack(z, w);
     }
   }
 }
@@ -494,11 +545,71 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
       prefetch_map(lane <= 4 ? &gather.state[lane - 1] : &gather.input[lane - 5]);
   }
 
+  const bool ordered = kDecode && a.order != nullptr;
+  if (ordered) {
+    // Warm the L2 (and the address translations) for this CTA's first loads
+    // while the previous kernel finishes: its list entries, the records and
+    // input rows of the rows it writes, its ape slice.  L2 is coherent, so
+    // lines the previous kernel still writes are read correctly after the wait.
+    const uint32_t B = a.capacity;
+    const uint32_t cap = B > first ? (B - first + stride - 1) / stride : 0u;
+    const uint32_t nt = B > blockIdx.x ? (B - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
+    if (t == 0) prefetch_l2(a.order);
+    if (static_cast<uint32_t>(t) < cap) prefetch_l2(a.order + 1 + first + t * stride);
+    if (static_cast<uint32_t>(t) < nt) prefetch_l2(a.plan_d + blockIdx.x + t * gridDim.x);
+    if (t < 128) prefetch_l2(static_cast<const TIn*>(a.ape) + static_cast<size_t>(t) * hd + c0);
+    const int lines = static_cast<int>(width * sizeof(TIn) / 128);  // of one input row
+    for (int i = t; i < static_cast<int>(nt) * lines; i += NT)
+      prefetch_l2(reinterpret_cast<const uint8_t*>(input) + (blockIdx.x + (i / lines) * static_cast<size_t>(gridDim.x)) *
+                                                                 width * sizeof(TIn) + (i % lines) * 128);
+  }
   pdl_wait();  // everything below may read what the previous kernel wrote
   pdl_release();
+  if (ordered && t < NC) load_ape_regs_now<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
   const uint32_t num_c = kDecode ? 0u : count_or_capacity(a.d_counts, 0, a.capacity);
   uint32_t items, ntriv = 0;
-  if constexpr (kDecode) {
+  __shared__ uint32_t s_count;
+  if (ordered) {
+    // The boundary list gives this CTA its windows directly: entries of rank
+    // first, first + stride, ... ({row, page}), loaded together with the
+    // records of the rows it writes (rows blockIdx, blockIdx + gridDim, ...)
+    // in one round of loads.  Thread 0 also loads the count and issues the
+    // first tile as soon as its entry is in (stage 0 is free; the producer
+    // starts at the second).  The host keeps both shares below kOwnRows.
+    const uint32_t B = a.capacity;
+    const uint32_t cap = B > first ? (B - first + stride - 1) / stride : 0u;
+    ntriv = B > blockIdx.x ? (B - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
+    const uint32_t count = t == 0 ? load_order_count(a) : 0u;
+    const uint32_t nk = cap > ntriv ? cap : ntriv;
+    for (uint32_t k = t; k < nk; k += NT) {
+      uint2 e = make_uint2(kInvalidU32, 0u);
+      if (k < cap) e = load_order_entry(a, 1 + first + k * stride);
+      if (k < ntriv) {
+        const uint32_t r = blockIdx.x + k * gridDim.x;
+        bool valid = false, boundary = false;
+        ckv_decode_plan_t P;
+        const bool rec = decode_row(a, r, valid, boundary, P);
+        trivrow[k] = make_uint4(r, static_cast<uint32_t>(P.write_loc),
+                                (valid ? kRowValid : 0u) | (boundary ? kRowBoundary : 0u), 0u);
+        if (rec && !valid) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+      }
+      if (k < cap) own[k] = e;
+      if (k == 0 && cap > 0 && first < count) {
+        if (e.x != kInvalidU32) {
+          issue_decode_tile<TIn, CS>(reinterpret_cast<TIn*>(smem), smem_addr(&full_bar[0]), &page_map, input, width,
+                                     hd, c0, e.x, static_cast<int32_t>(e.y));
+        } else {
+          status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+          mbar_arrive_expect_tx(smem_addr(&full_bar[0]), 0u);
+        }
+      }
+    }
+    if (t == 0) s_count = count;
+    __syncthreads();
+    const uint32_t total = s_count;
+    items = total > first ? (total - first + stride - 1) / stride : 0u;
+    if (items > cap) items = cap;
+  } else if constexpr (kDecode) {
     // Ranks of the page-boundary rows (in row order) by block-wide scans: in
     // each pass thread t looks at kScanK consecutive rows.  This CTA owns the
     // boundary rows of rank first, first + stride, ... ({row, page} pairs) and
@@ -565,8 +676,14 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
     items = num_c > first ? (num_c - first + stride - 1) / stride : 0u;
   }
 
+  if constexpr (kDecode) {
+    if (t >= NC + 32) {  // ---------------- side warps: the rows that read no page
+      decode_rows_side<TIn, TOut, Cfg::NSIDE>(a, trivrow, ntriv, t - (NC + 32));
+      return;
+    }
+  }
   if (warp == NC / 32) {
-    // ---------------- producer: lane 0 of the last warp alone issues every
+    // ---------------- producer: lane 0 of the producer warp alone issues every
     // copy and takes every wait (decode: tile 0 was issued by the scan)
     if (lane != 0) return;
     uint32_t n = kDecode && items > 0 ? 1u : 0u;  // tiles issued so far
@@ -590,7 +707,12 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
       TIn* kv_s = reinterpret_cast<TIn*>(smem + stage * T::TILE_BYTES);
       if constexpr (kDecode) {
         const uint2 rp = own[n];
-        issue_decode_tile<TIn, CS>(kv_s, bar, &page_map, input, width, hd, c0, rp.x, static_cast<int32_t>(rp.y));
+        if (rp.x != kInvalidU32) {
+          issue_decode_tile<TIn, CS>(kv_s, bar, &page_map, input, width, hd, c0, rp.x, static_cast<int32_t>(rp.y));
+        } else {  // a list entry outside the batch or the state
+          status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+          mbar_arrive_expect_tx(bar, 0u);
+        }
       } else {
         const uint32_t e = first + n * stride;
         uint32_t ragged = 0;
@@ -619,11 +741,9 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
   }
 
   // ---------------- consumer warps: group grp takes items grp, grp + NG, ...
-  // (decode: first the rows that read no page, while the first tiles load)
-  // (the ape slice is loaded after the plan scan, so that the scan's loads do
-  // not queue behind it)
-  load_ape_regs<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
-  if constexpr (kDecode) decode_rows_without_window<TIn, TOut, NC>(a, trivrow, ntriv, t);
+  // (without a boundary list the ape slice is loaded after the plan scan, so
+  // that the scan's loads do not queue behind it)
+  if (!ordered) load_ape_regs<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
   uint32_t local = 0;
   for (uint32_t n = grp; n < items; n += NG, ++local) {
     // one decision for the whole group (also orders the reuse of its reduction buffers)
@@ -639,6 +759,7 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
     size_t orow;
     if constexpr (kDecode) {
       orow = own[n].x;
+      ok = own[n].x != kInvalidU32;
     } else {
       e = first + n * stride;
       int bl = 0;

@@ -91,7 +91,8 @@ enum { CKV_MAX_BATCH = 1024, CKV_MAX_TOKENS = (1 << 24) - 1 };
  *
  * ckv_set_wait_limit_ns sets that limit, in nanoseconds, for every launch made
  * after the call, process-wide (an atomic; calls from several threads are
- * safe), and returns the previous limit.  0 restores the default, 2 s.  A
+ * safe), and returns the previous limit.  0 restores the default, 2 s; limits
+ * above 10 s are clamped to 10 s, so that every wait stays bounded.  A
  * launch captured in a CUDA graph keeps the limit in force at its capture.  The
  * outputs of a launch whose waits expired -- and, for a decode, the state row
  * it writes -- are unspecified; a limit below a copy's latency (a few
@@ -134,6 +135,19 @@ typedef struct ckv_decode_plan {
   int32_t read_page_1;
 } ckv_decode_plan_t;
 
+/* The page-boundary rows of a decode batch, in row order (8 bytes per
+ * entry; written by ckv_plan_decode / ckv_plan_decode_paged when asked for,
+ * read by ckv_compress_decode).  An array of batch + 1 entries: entry 0 is
+ * {count, 0}, entries 1 .. count are {row, read_page_0} of the rows whose
+ * record is valid and whose seq_len is a multiple of the ratio (the rows that
+ * emit a compressed row); entries past count are not written.  The pages
+ * define no such list: it lets the C128 decode hand out its windows to the
+ * SMs without every CTA scanning the whole plan first. */
+typedef struct ckv_decode_order {
+  uint32_t row;
+  int32_t page;
+} ckv_decode_order_t;
+
 #define CKV_RAGGED_MASK 0x00FFFFFFu
 #define CKV_BUFFER_LEN_SHIFT 24
 
@@ -164,9 +178,13 @@ uint32_t ckv_capacity_write(int ratio, uint32_t batch, uint32_t num_q_tokens);
 /* Decode plan (c_plan.cuh plan_compress_decode_legacy_kernel).
  * rid[batch], seq_lens[batch]: int64 device arrays (seq_len counts the new
  * token).  plan_d[batch]: output.  Rows with bad values get an invalid record
- * and set CKV_STATUS_BAD_LENGTH.  One launch of ceil(batch/256) x 256. */
+ * and set CKV_STATUS_BAD_LENGTH.  order: NULL, or an 8-byte aligned output
+ * of batch + 1 ckv_decode_order_t entries that receives the batch's
+ * page-boundary rows (see ckv_decode_order_t).  Without order: one launch of
+ * ceil(batch/256) x 256 threads; with order: one CTA of 1024 threads (a
+ * block-wide scan of the batch, so the list comes out in row order). */
 int ckv_plan_decode(int ratio, const int64_t* rid, const int64_t* seq_lens, uint32_t batch,
-                    ckv_decode_plan_t* plan_d, uint32_t* d_status, ckv_stream_t stream);
+                    ckv_decode_plan_t* plan_d, ckv_decode_order_t* order, uint32_t* d_status, ckv_stream_t stream);
 
 /* Prefill plans (c_plan.cuh plan_compress_prefill_kernel0 / _kernel_1 and the
  * CPU loop of plan_compress_prefill_legacy, whose order is reproduced exactly):
@@ -228,7 +246,8 @@ int ckv_plan_prefill_paged(int ratio, const int64_t* rid, const int32_t* req_to_
 int ckv_plan_decode_paged(int ratio, const int64_t* rid, const int32_t* req_to_token, int64_t r2t_stride,
                           uint32_t num_reqs, const int64_t* full_to_state, uint64_t num_full_slots,
                           int32_t swa_page_size, int32_t ring_size, const int64_t* seq_lens, uint32_t batch,
-                          ckv_decode_plan_t* plan_d, uint32_t* d_status, ckv_stream_t stream);
+                          ckv_decode_plan_t* plan_d, ckv_decode_order_t* order, uint32_t* d_status,
+                          ckv_stream_t stream);
 
 /* ------------------------------------------------------------------ compute */
 /* Prefill state write (c4.cuh c4_write / flash_c4_prefill<kWrite=true>,
@@ -271,10 +290,18 @@ int ckv_compress_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, v
  * seq_len % ratio == 0 emit the pool of the window (the new token's entry is
  * taken from the input row, the others from the state), otherwise write +0.0
  * to out row b.  kv_score_input is [batch, width], out is [batch, head_dim].
- * Two rows of one batch must not name the same request. */
+ * Two rows of one batch must not name the same request.
+ * order: NULL, or the list that ckv_plan_decode wrote next to plan_d (8-byte
+ * aligned, batch + 1 entries).  The C128 decode then reads only its own
+ * entries of the list instead of scanning the plan for the rows that emit;
+ * the C4 decode does not read it.  A list that does not match plan_d is a
+ * caller error: its entries are still bounds-checked (a row >= batch or a
+ * page outside the state is skipped with CKV_STATUS_BAD_INDEX), but the
+ * outputs are then unspecified. */
 int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, void* state, uint64_t state_rows,
                         const void* kv_score_input, const void* ape, const ckv_decode_plan_t* plan_d,
-                        uint32_t batch, void* out, uint32_t* d_status, ckv_stream_t stream);
+                        const ckv_decode_order_t* order, uint32_t batch, void* out, uint32_t* d_status,
+                        ckv_stream_t stream);
 
 /* ------------------------------------------------------- online C128 state */
 /* compressor_v2.py can keep C128 state online: one slot of 3 * head_dim per

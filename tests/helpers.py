@@ -72,6 +72,26 @@ def plan_d_fields(plan_d: np.ndarray) -> dict:
             "read_page_1": w[:, 3].view(np.int32).astype(np.int64)}
 
 
+def expected_decode_order(plan_d: np.ndarray, ratio: int) -> np.ndarray:
+    """The boundary-row list of a decode plan, derived from the oracle's records:
+    rows whose record is valid and whose seq_len is a multiple of the ratio, in
+    row order, as {row, read_page_0}; row 0 of the result is {count, 0}."""
+    f = plan_d_fields(plan_d)
+    valid = f["seq_len"] != 0xFFFFFFFF
+    rows = np.nonzero(valid & (f["seq_len"] % ratio == 0))[0]
+    out = np.zeros((len(rows) + 1, 2), np.uint32)
+    out[0, 0] = len(rows)
+    out[1:, 0] = rows
+    out[1:, 1] = f["read_page_0"][rows].astype(np.int32).view(np.uint32)
+    return out
+
+
+def decode_order_entries(order) -> np.ndarray:
+    """The written part of a device boundary-row list ([batch + 1, 8] uint8) as {row, page} uint32 pairs."""
+    a = order.cpu().numpy().reshape(-1, 8).view(np.uint32).reshape(-1, 2)
+    return a[: int(a[0, 0]) + 1]
+
+
 def state_row_of_entry(ratio: int, i: int, rp0: int, rp1: int) -> int:
     """State row a plan record names for window entry i (C4: half-ring pages of 4
     slots, entries 0..3 in read_page_0; C128: one 128-slot page)."""

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_record_sizes_match_header():
     text = open(HEADER).read()
     for struct, size in [("ckv_compress_plan", 16), ("ckv_write_plan", 8), ("ckv_decode_plan", 16),
-                         ("ckv_online_unit", 16)]:
+                         ("ckv_online_unit", 16), ("ckv_decode_order", 8)]:
         body = re.search(r"typedef struct %s \{(.*?)\}" % struct, text, flags=re.S).group(1)
         fields = re.findall(r"(u?int32_t)\s+\w+;", body)
         assert 4 * len(fields) == size, struct
@@ -56,12 +56,17 @@ def test_capacity_bounds(lib):
 def test_argument_errors_are_returned_before_any_launch(lib):
     vp = ctypes.c_void_p
     # bad ratio / head_dim / dtype / layout / pointers: rejected on the host
-    assert lib.ckv_plan_decode(3, None, None, 1, None, None, None) == -1
+    assert lib.ckv_plan_decode(3, None, None, 1, None, None, None, None) == -1
+    # the boundary-row list must be 8-byte aligned
+    assert lib.ckv_plan_decode(128, vp(8), vp(8), 1, vp(16), vp(12), None, None) == -4
     assert lib.ckv_plan_prefill(4, None, None, None, 2000, 0, 0, 0, 0, None, None, vp(16), None, None) == -3
     assert lib.ckv_plan_prefill(4, None, None, None, 1, 0, 0, 0, 0, None, None, vp(16), None, None) == -4
-    assert lib.ckv_compress_decode(4, 100, 1, 0, None, 0, None, None, None, 1, None, None, None) == -2
-    assert lib.ckv_compress_decode(4, 128, 7, 0, None, 0, None, None, None, 1, None, None, None) == -5
-    assert lib.ckv_compress_decode(4, 128, 1, 0, vp(8), 8, vp(16), vp(16), vp(16), 1, vp(16), None, None) == -4
+    assert lib.ckv_compress_decode(4, 100, 1, 0, None, 0, None, None, None, None, 1, None, None, None) == -2
+    assert lib.ckv_compress_decode(4, 128, 7, 0, None, 0, None, None, None, None, 1, None, None, None) == -5
+    assert lib.ckv_compress_decode(4, 128, 1, 0, vp(8), 8, vp(16), vp(16), vp(16), None, 1, vp(16), None,
+                                   None) == -4
+    assert lib.ckv_compress_decode(128, 512, 1, 0, vp(16), 8, vp(16), vp(16), vp(16), vp(12), 1, vp(16), None,
+                                   None) == -4
     assert lib.ckv_compress_pool_prefill(128, 512, 1, 0, None, 0, None, 10, None, None, None, 1, 9, None, None,
                                          None) == -5
     assert lib.ckv_compress_write(4, 2048, 1, None, 0, None, 0, None, None, 1, None, None) == -2
@@ -72,7 +77,8 @@ def test_argument_errors_are_returned_before_any_launch(lib):
     assert nrd(4, 512, 64, 7, None, None, 1, None, f(1e-6), None, 16, None, 1, None, 16, None, None) == -5
     assert nrd(4, 512, 64, 0, None, None, 1, None, f(1e-6), None, 16, None, 1, None, 16, None, None) == -4
     assert nrd(4, 512, 64, 0, None, None, 0, None, f(1e-6), None, 16, None, 1, None, 16, None, None) == 0
-    assert lib.ckv_plan_decode_paged(128, None, None, 0, 0, None, 0, 256, 256, None, 1, None, None, None) == -3
+    assert lib.ckv_plan_decode_paged(128, None, None, 0, 0, None, 0, 256, 256, None, 1, None, None, None,
+                                     None) == -3
     assert lib.ckv_plan_prefill_paged(4, None, None, 8, 1, None, 8, 16, 4, None, None, 1, 4, 4, 4, 0, None, None,
                                       None, None, None) == -3  # a 4-row ring
     assert lib.ckv_compress_online_decode(100, 1, 0, None, 0, None, None, None, 1, None, None, None) == -2
@@ -102,15 +108,17 @@ def test_binding_rejects_wrong_per_request_arrays():
 
 
 def test_wait_limit_setter(lib):
-    assert lib.ckv_version() >= 102  # the setter arrived with ABI 1.02
+    assert lib.ckv_version() >= 200  # ABI 2.00: decode boundary-row lists, clamped wait limit
     default = 2_000_000_000
     prev = ckv.set_wait_limit_ns(0)            # whatever was set, back to the default
     assert ckv.set_wait_limit_ns(1234) == default
     assert ckv.set_wait_limit_ns(5) == 1234
     assert ckv.set_wait_limit_ns(0) == 5       # 0 restores the default ...
     assert ckv.set_wait_limit_ns(0) == default
+    # limits beyond 10 s come back clamped: every wait stays bounded
     assert ckv.set_wait_limit_ns(2 ** 64 - 1) == default
-    assert ckv.set_wait_limit_ns(prev if prev != default else 0) == 2 ** 64 - 1
+    assert ckv.set_wait_limit_ns(20_000_000_000) == 10_000_000_000
+    assert ckv.set_wait_limit_ns(prev if prev != default else 0) == 10_000_000_000
     with pytest.raises(ValueError):
         ckv.set_wait_limit_ns(-1)
     ckv.set_wait_limit_ns(0)

@@ -87,19 +87,26 @@ def test_prefill_workload_full_size(env, name):
 
 
 @pytest.mark.parametrize("name", ["c4_decode", "c128_decode"])
-def test_decode_workload_full_size(env, name):
+@pytest.mark.parametrize("ordered", [True, False])
+def test_decode_workload_full_size(env, name, ordered):
+    """Every row of the decode workloads, through the boundary-row list (the
+    benchmark's path) and through the plan scan."""
     o, ckv, dev = env
     w = wl.NAMED[name](0)
     R, hd = w.ratio, w.head_dim
     ci, co = code(w.in_dtype), code(w.out_dtype)
     state_d = w.state.to(dev)
     status = ckv.new_status(dev)
-    out, pd = ckv.decode_step(R, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), w.rid.to(dev), w.seq_lens.to(dev),
-                              w.out_dtype, status=status)
+    order = ckv.new_decode_order(w.batch, dev) if ordered else None
+    pd = ckv.plan_decode(R, w.rid.to(dev), w.seq_lens.to(dev), status=status, order=order)
+    out = ckv.compress_decode(R, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), pd, w.out_dtype, status=status,
+                              order=order)
     torch.cuda.synchronize()
     assert int(status[0]) == 0
     wpd = o.plan_decode(R, w.rid, w.seq_lens)
     assert (pd.cpu().numpy() == wpd).all()
+    if ordered:
+        assert (H.decode_order_entries(order) == H.expected_decode_order(wpd, R)).all()
     st0 = wl.bits(w.state).copy()
     st = st0.copy()
     inp = wl.bits(w.kv_score)

@@ -107,7 +107,8 @@ def test_prefill_step_replayed_from_a_graph(env, ratio):
 
 
 @pytest.mark.parametrize("ratio", [4, 128])
-def test_decode_step_replayed_from_a_graph(env, ratio):
+@pytest.mark.parametrize("ordered", [True, False])
+def test_decode_step_replayed_from_a_graph(env, ratio, ordered):
     o, ckv, dev = env
     hd, in_dt, out_dt = 256, 1, 0
     batch = 97
@@ -124,10 +125,11 @@ def test_decode_step_replayed_from_a_graph(env, ratio):
     plan_d = torch.empty(batch, 16, dtype=torch.uint8, device=dev)
     out = torch.empty(batch, hd, dtype=torch.float32, device=dev)
     status = ckv.new_status(dev)
+    order = ckv.new_decode_order(batch, dev) if ordered else None
 
     def step():
-        ckv.plan_decode(ratio, rid, sl_d, plan_d, status)
-        ckv.compress_decode(ratio, hd, state, kv, ape, plan_d, torch.float32, out=out, status=status)
+        ckv.plan_decode(ratio, rid, sl_d, plan_d, status, order=order)
+        ckv.compress_decode(ratio, hd, state, kv, ape, plan_d, torch.float32, out=out, status=status, order=order)
 
     step()
     torch.cuda.synchronize()
@@ -146,6 +148,8 @@ def test_decode_step_replayed_from_a_graph(env, ratio):
         st = st0.copy()
         wpd = o.plan_decode(ratio, w.rid, w.seq_lens)
         assert (plan_d.cpu().numpy() == wpd).all()
+        if ordered:
+            assert (H.decode_order_entries(order) == H.expected_decode_order(wpd, ratio)).all()
         inp = wl.bits(w.kv_score)
         want = o.compress_decode(ratio, hd, in_dt, out_dt, st, inp, wl.bits(w.ape), wpd)
         got = H.np_bits(out)

@@ -103,7 +103,13 @@ def test_paged_decode_plan_bit_exact(env, ratio):
     torch.cuda.synchronize()
     assert int(status[0]) == 0
     omaps = (pool.r2t, pool.f2s) if ratio == 4 else (None, None)
-    assert (pd.cpu().numpy() == o.plan_decode_paged(ratio, rids, *omaps, S, ring, sl)).all()
+    want = o.plan_decode_paged(ratio, rids, *omaps, S, ring, sl)
+    assert (pd.cpu().numpy() == want).all()
+    order = ckv.new_decode_order(B, dev)
+    pd = ckv.plan_decode_paged(ratio, torch.tensor(rids, **i64), *maps, S, ring, torch.tensor(sl, **i64),
+                               status=status, order=order)
+    assert (pd.cpu().numpy() == want).all()
+    assert (H.decode_order_entries(order) == H.expected_decode_order(want, ratio)).all()
 
 
 def test_paged_bad_mapping_is_flagged(env):

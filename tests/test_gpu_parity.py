@@ -38,16 +38,43 @@ def _dev_i64(x, dev):
 
 # ----------------------------------------------------------------------------- plans
 @pytest.mark.parametrize("ratio", [4, 128])
-def test_plan_decode_bit_exact(env, ratio):
+@pytest.mark.parametrize("B", [777, 1024, 1500, 5000])
+def test_plan_decode_bit_exact(env, ratio, B):
+    """Records bit-exact against the oracle, with and without the boundary-row
+    list; the list (one CTA, chunks of 1024 or 4096 rows) equals the rows the
+    oracle's records mark as emitting, in row order."""
     o, ckv, dev = env
-    rng = np.random.default_rng(ratio)
-    B = 777
-    rid = rng.permutation(4096)[:B]
+    rng = np.random.default_rng(ratio + B)
+    rid = rng.permutation(8192)[:B]
     sl = rng.integers(1, 70000, B)
     sl[:40] = np.arange(1, 41)
     sl[40:80] = ratio * rng.integers(1, 300, 40)
+    sl[-3:] = ratio  # boundary rows at the tail of the last chunk
+    want = o.plan_decode(ratio, rid, sl)
     got = ckv.plan_decode(ratio, _dev_i64(rid, dev), _dev_i64(sl, dev)).cpu().numpy()
-    assert (got == o.plan_decode(ratio, rid, sl)).all()
+    assert (got == want).all()
+    order = ckv.new_decode_order(B, dev)
+    order.fill_(0xAB)
+    got = ckv.plan_decode(ratio, _dev_i64(rid, dev), _dev_i64(sl, dev), order=order).cpu().numpy()
+    assert (got == want).all()
+    assert (H.decode_order_entries(order) == H.expected_decode_order(want, ratio)).all()
+
+
+def test_plan_decode_order_skips_bad_rows_and_empty_batches(env):
+    o, ckv, dev = env
+    status = ckv.new_status(dev)
+    rid, sl = [0, -1, 2, 3], [128, 128, 0, 256]
+    order = ckv.new_decode_order(4, dev)
+    pd = ckv.plan_decode(128, _dev_i64(rid, dev), _dev_i64(sl, dev), status=status, order=order).cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(status[0]) & ckv.STATUS_BAD_LENGTH
+    ent = H.decode_order_entries(order)
+    assert ent[:, 0].tolist() == [2, 0, 3] and ent[1:, 1].tolist() == [0, 3]
+    assert (ent == H.expected_decode_order(pd, 128)).all()
+    empty = ckv.new_decode_order(0, dev)
+    empty.fill_(0xAB)
+    ckv.plan_decode(128, _dev_i64([], dev), _dev_i64([], dev), order=empty)
+    assert H.decode_order_entries(empty).tolist() == [[0, 0]]
 
 
 def _prefill_case(name, ratio, rng):
@@ -197,10 +224,21 @@ def test_c4_prefill_first_group_ignores_nan_state(env):
 
 
 # ----------------------------------------------------------------------------- decode
+def decode_through(ckv, ordered, ratio, hd, state_d, w, out_dtype, status, dev):
+    """plan_decode -> compress_decode, with the boundary-row list (decode_step) or without it."""
+    if ordered:
+        return ckv.decode_step(ratio, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), w.rid.to(dev),
+                               w.seq_lens.to(dev), out_dtype, status=status)
+    pd = ckv.plan_decode(ratio, w.rid.to(dev), w.seq_lens.to(dev), status=status)
+    out = ckv.compress_decode(ratio, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), pd, out_dtype, status=status)
+    return out, pd
+
+
 @pytest.mark.parametrize("ratio", [4, 128])
 @pytest.mark.parametrize("hd", [128, 512])
 @pytest.mark.parametrize("dts", [("bf16", "f32"), ("bf16", "bf16"), ("f32", "f32")])
-def test_decode_parity(env, ratio, hd, dts):
+@pytest.mark.parametrize("ordered", [True, False])
+def test_decode_parity(env, ratio, hd, dts, ordered):
     o, ckv, dev = env
     in_dt, out_dt = DT[dts[0]], DT[dts[1]]
     rng = np.random.default_rng(ratio + hd)
@@ -212,8 +250,7 @@ def test_decode_parity(env, ratio, hd, dts):
                          num_requests_state=256)
     state_d = w.state.to(dev)
     status = ckv.new_status(dev)
-    out, pd = ckv.decode_step(ratio, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), w.rid.to(dev),
-                              w.seq_lens.to(dev), H.torch_dtype(out_dt), status=status)
+    out, pd = decode_through(ckv, ordered, ratio, hd, state_d, w, H.torch_dtype(out_dt), status, dev)
     torch.cuda.synchronize()
     assert int(status[0]) == 0
     st0 = wl.bits(w.state).copy()
@@ -267,6 +304,31 @@ def test_out_of_range_records_are_flagged_not_faulted(env):
         ckv.compress_write(ratio, hd, w.state.to(dev), kv, pw, None, status=status)
         torch.cuda.synchronize()
         assert int(status[0]) & ckv.STATUS_BAD_INDEX
+
+
+def test_bad_order_entries_are_flagged_not_faulted(env):
+    """A boundary-row list that does not match the plan (a row past the batch, a
+    page outside the state, a count larger than the batch) is bounds-checked by
+    the C128 decode: those entries are skipped and reported, nothing faults, and
+    the rows the list does name correctly are pooled as usual."""
+    o, ckv, dev = env
+    hd = 128
+    w = wl.random_decode(128, hd, torch.bfloat16, torch.float32, [128, 256, 384, 5], seed=2, num_requests_state=4)
+    pd = ckv.plan_decode(128, w.rid.to(dev), w.seq_lens.to(dev))
+    good = ckv.new_decode_order(4, dev)
+    ckv.plan_decode(128, w.rid.to(dev), w.seq_lens.to(dev), order=good)
+    want = ckv.compress_decode(128, hd, w.state.to(dev), w.kv_score.to(dev), w.ape.to(dev), pd, order=good)
+    # count past the batch; row 0 and row 1 named correctly; a row past the batch; row 2 with a page
+    # outside the state (so row 2 is not pooled: its output is unspecified)
+    ent = torch.tensor([[100, 0], [0, int(w.rid[0])], [9, 0], [2, 10 ** 6], [1, int(w.rid[1])]], dtype=torch.int32)
+    bad = ent.view(torch.uint8).reshape(5, 8).to(dev)
+    status = ckv.new_status(dev)
+    state_d = w.state.to(dev)
+    out = ckv.compress_decode(128, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), pd, status=status, order=bad)
+    torch.cuda.synchronize()
+    assert int(status[0]) & ckv.STATUS_BAD_INDEX
+    assert torch.equal(out[0], want[0]) and torch.equal(out[1], want[1])
+    assert (out[3] == 0).all()               # not a boundary row: zeroed by its own record
 
 
 # ----------------------------------------------------------------------------- invariants on the GPU

@@ -88,7 +88,8 @@ def test_prefill_pool_wait_expiry(env, ratio):
     _expire_then_recover(ckv, run)
 
 
-def test_c128_decode_wait_expiry(env):
+@pytest.mark.parametrize("ordered", [True, False])
+def test_c128_decode_wait_expiry(env, ordered):
     ckv, dev = env
     hd, batch = 512, 512
     rng = np.random.default_rng(21)
@@ -103,7 +104,11 @@ def test_c128_decode_wait_expiry(env):
     def run():
         status.zero_()
         state.copy_(init)
-        out, _ = ckv.decode_step(128, hd, state, kv, ape, rid, seq, torch.float32, status=status)
+        if ordered:
+            out, _ = ckv.decode_step(128, hd, state, kv, ape, rid, seq, torch.float32, status=status)
+        else:
+            pd = ckv.plan_decode(128, rid, seq, status=status)
+            out = ckv.compress_decode(128, hd, state, kv, ape, pd, torch.float32, status=status)
         return [out, state], status
 
     _expire_then_recover(ckv, run)
