@@ -683,10 +683,13 @@ def instep_by_difference(segments, flush, restore, reps: int) -> dict:
             e1.synchronize()
             if rep >= 2:  # two untimed rounds first
                 times[name].append(e0.elapsed_time(e1) * 1e3)
-    med = {name: statistics.median(v) for name, v in times.items()}
-    out = {"step_us": med["step"]}
+    full = np.array(times["step"])
+    out = {"step_us": float(np.median(full)), "reps": reps}
     for name, _ in segments:
-        out[f"{name}_us"] = med["step"] - med[name]
+        # replays of one round ran back to back: the median of the paired differences
+        d = full - np.array(times[name])
+        out[f"{name}_us"] = float(np.median(d))
+        out[f"{name}_us_iqr"] = [float(np.percentile(d, 25)), float(np.percentile(d, 75))]
     out["sum_us"] = sum(out[f"{n}_us"] for n, _ in segments)
     return out
 
@@ -727,7 +730,7 @@ def c4_kernels(args, ckv, dev, seed: int, peak: float) -> dict:
     dec = DecodeRunner(ckv, w2, dev)
     flush = l2_flush_buffer(dev)
     b4, b2 = algorithmic_bytes(w4), algorithmic_bytes(w2)
-    reps = max(20, args.steps)
+    reps = max(200, 10 * args.steps)
     pre_seg = [("plan_prefill", pre.plan), ("pool_prefill", pre.pool), ("write", pre.write)]
     dec_seg = [("plan_decode", dec.plan), ("decode", dec.decode)]
     ip = instep_by_difference(pre_seg, flush, pre.restore, reps)
@@ -841,13 +844,14 @@ def bench_step(args, ws, rank, local):
     dec_gbs = b3["decode"] / (dec_ms * 1e-3) / 1e9
     step_bytes = b5["total"] + b3["total"]
     # every kernel's cost inside the timed step, by difference (no event nodes between the kernels)
-    instep = instep_by_difference(segments, flush, restore, reps=max(20, args.steps))
+    instep_reps = max(200, 10 * args.steps)
+    instep = instep_by_difference(segments, flush, restore, reps=instep_reps)
     for key, nbytes in (("pool_prefill", b5["pool"]), ("write", b5["write"]), ("decode", b3["decode"])):
         us = instep[f"{key}_us"]
         instep[f"{key}_instep_gbs"] = nbytes / (us * 1e-6) / 1e9 if us > 0 else None
         instep[f"{key}_instep_frac"] = instep[f"{key}_instep_gbs"] / peak if us > 0 else None
-    instep["method"] = ("median step time minus the median time of the step without that kernel; "
-                        f"{max(20, args.steps)} interleaved replays per variant, L2 flushed before each")
+    instep["method"] = ("median over rounds of (step time - time of the step without that kernel), each round "
+                        f"replaying every variant once; {instep_reps} rounds, L2 flushed before every replay")
     # the decode kernel back to back over copies of its inputs that together exceed the L2 (a kernel of ~10 us
     # is not resolved by event nodes around it: they add the graph's node-to-node latency)
     back_to_back = {}

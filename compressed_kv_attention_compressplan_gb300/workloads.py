@@ -394,9 +394,10 @@ class OnlineInputs:
     out_layout: str
 
 
-def c128_online_prefill(seed: int = 0, head_dim: int = 512, num_long: int = 128) -> OnlineInputs:
-    """The C128 prefill workload's lengths and inputs, through the online state."""
-    rid, sl, el = c128_prefill_lengths(seed, num_long=num_long)
+def c128_online_prefill(seed: int = 0, head_dim: int = 512, num_long: int = 128, lengths=None) -> OnlineInputs:
+    """The C128 prefill workload's lengths and inputs, through the online state (or the given
+    ``(rid, seq_lens, extend_lens)``)."""
+    rid, sl, el = c128_prefill_lengths(seed, num_long=num_long) if lengths is None else lengths
     nq = int(el.sum())
     kv = normal((nq, 2 * head_dim), torch.bfloat16, 1.0, _seed(seed, 11))
     set_score_outliers(kv, 128, head_dim, 0.01, 8.0, _gen(seed, 12))

@@ -283,9 +283,10 @@ def as_f32(a: np.ndarray) -> np.ndarray:
     return bf16_to_f32(a) if a.dtype == np.uint16 else a.astype(np.float32)
 
 
-def window_kv_absmax(ratio, hd, state, inp, seq_len, ragged, bl, rp0, rp1):
-    """max_i |kv_i[c]| over each event's window (masked entries excluded): [n, hd] float64.
-    ``state`` / ``inp`` are numpy row arrays (bf16 bits or fp32) of the kv_score layout."""
+def window_kv_absmax_loop(ratio, hd, state, inp, seq_len, ragged, bl, rp0, rp1):
+    """max_i |kv_i[c]| over each event's window (masked entries excluded): [n, hd] float64, one entry at a
+    time (the plain statement of window_kv_absmax, kept to check it).  ``state`` / ``inp`` are numpy row
+    arrays (bf16 bits or fp32) of the kv_score layout."""
     W = window(ratio)
     n = len(seq_len)
     out = np.zeros((n, hd))
@@ -300,6 +301,37 @@ def window_kv_absmax(ratio, hd, state, inp, seq_len, ragged, bl, rp0, rp1):
                 row = inp[int(ragged[k]) - (W - 1) + i]
             m = np.maximum(m, np.abs(as_f32(row[off:off + hd]).astype(np.float64)))
         out[k] = m
+    return out
+
+
+def window_kv_absmax(ratio, hd, state, inp, seq_len, ragged, bl, rp0, rp1, chunk: int = 64):
+    """The same as window_kv_absmax_loop, gathered a chunk of events at a time (full-size workloads)."""
+    W = window(ratio)
+    seq_len, ragged, bl = (np.asarray(x, np.int64) for x in (seq_len, ragged, bl))
+    rp0, rp1 = np.asarray(rp0, np.int64), np.asarray(rp1, np.int64)
+    n = len(seq_len)
+    out = np.zeros((n, hd))
+    i = np.arange(W)[None, :]
+    for s in range(0, n, chunk):
+        e = slice(s, min(n, s + chunk))
+        from_state = i < bl[e, None]
+        first = np.where((ratio == 4) & (seq_len[e] == 4), 4, 0)[:, None]
+        live = i >= first
+        if ratio == 4:
+            srow = np.where(i < 4, rp0[e, None], rp1[e, None]) * 4 + i % 4
+        else:
+            srow = rp0[e, None] * 128 + i
+        irow = ragged[e, None] - (W - 1) + i
+        # unused indices are clipped into range; their rows are masked out below
+        vs = state[np.clip(np.where(from_state & live, srow, 0), 0, len(state) - 1)]
+        vi = inp[np.clip(np.where(~from_state & live, irow, 0), 0, len(inp) - 1)]
+        rows = np.where(from_state[..., None], vs, vi)                     # [c, W, width]
+        if ratio == 4:
+            kv = np.where((i < 4)[..., None], rows[..., :hd], rows[..., hd:2 * hd])
+        else:
+            kv = rows[..., :hd]
+        a = np.abs(as_f32(kv).astype(np.float64))
+        out[e] = np.where(live[..., None], a, 0.0).max(1)
     return out
 
 

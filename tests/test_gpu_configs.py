@@ -4,9 +4,8 @@ buffers padded with the invalid record for the speculative-decoding
 workloads; plan -> pool -> write on one stream; plan -> decode).
 
 Plans and state buffers are compared with the oracle byte for byte; decode
-outputs in full; prefill outputs on a seeded sample of compress records that
-the oracle pools one by one, plus every non-compress row of token layouts
-(which must be +0.0).
+outputs in full; prefill outputs of every compress record (the oracle pools
+them all), plus every non-compress row of token layouts (which must be +0.0).
 """
 import numpy as np
 import pytest
@@ -68,16 +67,13 @@ def test_prefill_workload_full_size(env, name):
     st = wl.bits(w.state).copy()
     inp = wl.bits(w.kv_score)
     ape = wl.bits(w.ape)
-    rng = np.random.default_rng(7)
-    sample = np.unique(np.concatenate([rng.choice(nc, min(nc, 192), replace=False), [0, nc - 1]]))
-    want = o.compress_pool_prefill(R, hd, ci, co, st, inp, ape, np.ascontiguousarray(wc[sample]), len(sample), nq,
-                                   o.OUT_COMPACT)
-    f = H.plan_c_fields(wc[sample])
+    want = o.compress_pool_prefill(R, hd, ci, co, st, inp, ape, np.ascontiguousarray(wc), nc, nq, o.OUT_COMPACT)
+    f = H.plan_c_fields(wc)
     kvmax = H.window_kv_absmax(R, hd, st, inp, f["seq_len"], f["ragged_id"], f["buffer_len"], f["read_page_0"],
                                f["read_page_1"])
     got_all = H.np_bits(out)
-    rows = f["ragged_id"] if layout == ckv.OUT_TOKEN else sample
-    H.assert_pool_close(got_all[rows], want, co, kvmax, f"{name} sampled records")
+    rows = f["ragged_id"] if layout == ckv.OUT_TOKEN else np.arange(nc)
+    H.assert_pool_close(got_all[rows], want, co, kvmax, f"{name} every record")
     if layout == ckv.OUT_TOKEN:
         others = np.setdiff1d(np.arange(nq), H.plan_c_fields(wc)["ragged_id"])
         zero = got_all[others].view(np.uint16 if co else np.uint32)
@@ -125,7 +121,7 @@ def test_decode_workload_full_size(env, name, ordered):
 def test_paged_prefill_workload_full_size(env):
     """The C4 prefill workload over SWA-paged state (128-token SWA pages, 8-row
     rings), in the benchmark's launch configuration: paged plans bit-exact,
-    sampled pooled rows, every zero row, and the state after the write."""
+    every pooled row, every zero row, and the state after the write."""
     o, ckv, dev = env
     w, m = wl.PAGED["c4_prefill_paged"](0)
     R, hd, nq = w.ratio, w.head_dim, w.num_q_tokens
@@ -144,15 +140,13 @@ def test_paged_prefill_workload_full_size(env):
     assert (pc[:nc].cpu().numpy() == wc).all() and (pw[:nw].cpu().numpy() == ww).all(), "paged plans"
     st = wl.bits(w.state).copy()
     inp = wl.bits(w.kv_score)
-    rng = np.random.default_rng(9)
-    sample = np.unique(np.concatenate([rng.choice(nc, min(nc, 256), replace=False), [0, nc - 1]]))
-    want = o.compress_pool_prefill(R, hd, 1, 1, st, inp, wl.bits(w.ape), np.ascontiguousarray(wc[sample]),
-                                   len(sample), nq, o.OUT_COMPACT)
-    f = H.plan_c_fields(wc[sample])
+    want = o.compress_pool_prefill(R, hd, 1, 1, st, inp, wl.bits(w.ape), np.ascontiguousarray(wc), nc, nq,
+                                   o.OUT_COMPACT)
+    f = H.plan_c_fields(wc)
     kvmax = H.window_kv_absmax(R, hd, st, inp, f["seq_len"], f["ragged_id"], f["buffer_len"], f["read_page_0"],
                                f["read_page_1"])
     got = H.np_bits(out)
-    H.assert_pool_close(got[f["ragged_id"]], want, 1, kvmax, "paged sampled records")
+    H.assert_pool_close(got[f["ragged_id"]], want, 1, kvmax, "paged, every record")
     others = np.setdiff1d(np.arange(nq), H.plan_c_fields(wc)["ragged_id"])
     assert (got[others] == 0).all(), "non-compress rows"
     o.compress_write(R, hd, 1, st, inp, ww, nw)
