@@ -288,6 +288,20 @@ class PrefillRunner:
     def restore(self):
         self.state.copy_(self.pristine)
 
+    def plan_fns(self, n: int):
+        """n launches of the planner, each on its own copy of the lengths and of the plan buffers."""
+        c, w = self.ckv, self.w
+        fns = []
+        for _ in range(n):
+            rid, sl, el = self.rid.clone(), self.sl.clone(), self.el.clone()
+            pc, pw, cnt = self.plan_c.clone(), self.plan_w.clone(), self.counts.clone()
+
+            def fn(rid=rid, sl=sl, el=el, pc=pc, pw=pw, cnt=cnt):
+                c.plan_prefill(w.ratio, rid, sl, el, w.num_q_tokens, self.cap_c, self.cap_w, self.padded,
+                               pc[: self.cap_c], pw[: self.cap_w], cnt, self.status)
+            fns.append(fn)
+        return fns
+
     def steady_fns(self, n: int, which: str):
         """n launches of the pool or of the write, each on its own copy of the state, input, plan records
         and output (the plans are built once, before)."""
@@ -1006,6 +1020,7 @@ def bench_config(args, name, ws, rank, local):
     seg_ms, wall, _ = run_graph(step, flush, r.restore, args.steps, args.warmup, ws)
     whole = StepGraph(segs, inner_events=False)
     whole_ms, _, _ = run_graph(whole, flush, r.restore, args.steps, args.warmup, ws)
+    instep = instep_by_difference(segs, flush, r.restore, reps=max(200, 10 * args.steps))
     if int(r.status[0]):
         raise RuntimeError(f"device status {int(r.status[0])}")
     peak, kind = peaks()
@@ -1023,6 +1038,9 @@ def bench_config(args, name, ws, rank, local):
         steady = {"back_to_back_us": us, "back_to_back_gbs": sg, "back_to_back_frac": sg / peak,
                   "back_to_back_copies": n, "same_bytes_floor": floor,
                   "vs_floor": min(floor["copy_us"], floor["elementwise_us"]) / us}
+    if w.mode == "prefill" and maps is None and not args.no_back_to_back:
+        # the planner alone, back to back over copies of its inputs and outputs
+        steady["plan_back_to_back_us"] = steady_state_us(r.plan_fns(16))
     if w.mode == "decode" and not args.no_back_to_back:
         n = copies_for(b["decode"], dev)
         us = steady_state_us(r.steady_fns(n))
@@ -1037,6 +1055,7 @@ def bench_config(args, name, ws, rank, local):
             "step_gbs": b["total"] / (float(step_ms.mean()) * 1e-3) / 1e9,
             "segments_us": {n: float(seg_ms[:, i].mean()) * 1e3 for i, n in enumerate(step.names)},
             "segments_us_min": {n: float(seg_ms[:, i].min()) * 1e3 for i, n in enumerate(step.names)},
+            "instep": instep,
             "main_kernel": step.names[main_i], "main_bytes": b[main_key], "main_gbs": gbs, "main_frac": gbs / peak,
             "peak_gbs": peak, "peak_kind": kind, "algorithmic_bytes": b, **steady}
     if rank == 0:

@@ -9,6 +9,7 @@
 // chunk j, so each rotated pair sits in one lane; the sum of squares is a
 // lane-sequential sum followed by a fixed butterfly over the warp.
 #include <algorithm>
+#include <atomic>
 
 #include <cuda_bf16.h>
 
@@ -174,16 +175,21 @@ __global__ __launch_bounds__(kNrThreads) void norm_rope_store_kernel(const NormR
 // One wave: as many blocks as can be resident at once (the warps then loop).
 template <int kChunks>
 int launch_resident(const NormRopeArgs& a, cudaStream_t stream) {
-  static int per_sm = 0;
+  // per device; a failed query is not cached (the fallback of one block per SM is used for this launch only)
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CKV_ERR_LAUNCH;
+  const bool cached_dev = dev >= 0 && dev < 64;
+  int per_sm = cached_dev ? cache[dev].load(std::memory_order_relaxed) : 0;
   if (per_sm == 0) {
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, norm_rope_store_kernel<kChunks>, kNrThreads, 0) !=
-            cudaSuccess ||
-        nb <= 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_rope_store_kernel<kChunks>, kNrThreads, 0) ==
+            cudaSuccess &&
+        per_sm > 0) {
+      if (cached_dev) cache[dev].store(per_sm, std::memory_order_relaxed);
+    } else {
       cudaGetLastError();
-      nb = 1;
+      per_sm = 1;
     }
-    per_sm = nb;
   }
   const uint32_t warps_per_cta = kNrThreads / 32;
   uint32_t grid = (a.capacity + warps_per_cta - 1) / warps_per_cta;

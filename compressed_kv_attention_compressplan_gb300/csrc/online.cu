@@ -12,6 +12,7 @@
 // shared-memory ring that a producer warp fills with bulk copies (see
 // online_prefill_kernel).
 #include <algorithm>
+#include <atomic>
 
 #include "async_copy.cuh"
 #include "common.cuh"
@@ -441,27 +442,29 @@ int launch_prefill(const OnlineArgs& a, cudaStream_t s) {
   auto fn = online_prefill_kernel<TIn, TOut, kShortWaits>;
   const int smem = prefill_smem_bytes<TIn>(a.head_dim);
   const int threads = a.head_dim / 4 + 32;
-  static bool configured[64] = {};
+  // per-device caches (atomics: a repeated set-up by racing threads is harmless)
+  static std::atomic<bool> configured[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CKV_ERR_LAUNCH;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
+  const bool cached_dev = dev >= 0 && dev < 64;
+  if (!cached_dev || !configured[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, prefill_smem_bytes<TIn>(1024)) !=
         cudaSuccess) {
       cudaGetLastError();
       return CKV_ERR_LAUNCH;
     }
-    if (dev >= 0 && dev < 64) configured[dev] = true;
+    if (cached_dev) configured[dev].store(true, std::memory_order_release);
   }
   // resident CTAs per SM, per device and head_dim / 128 (the occupancy query is not free on the host)
-  static int per_sm_cache[64][9] = {};
+  static std::atomic<int> per_sm_cache[64][9];
   const int hi = a.head_dim / 128;
-  int per_sm = dev >= 0 && dev < 64 ? per_sm_cache[dev][hi] : 0;
+  int per_sm = cached_dev ? per_sm_cache[dev][hi].load(std::memory_order_relaxed) : 0;
   if (per_sm == 0) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess || per_sm < 1) {
       cudaGetLastError();
       return CKV_ERR_LAUNCH;
     }
-    if (dev >= 0 && dev < 64) per_sm_cache[dev][hi] = per_sm;
+    if (cached_dev) per_sm_cache[dev][hi].store(per_sm, std::memory_order_relaxed);
   }
   const uint32_t grid = std::max<uint32_t>(
       1, std::min<uint32_t>(a.capacity, static_cast<uint32_t>(per_sm) * static_cast<uint32_t>(sm_count())));

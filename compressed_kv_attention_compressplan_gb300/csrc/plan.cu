@@ -12,6 +12,7 @@
 // exclusive scans of the per-request counts, so the GPU plan is bit-identical
 // to the CPU loop, and the work is O(records) spread over the whole grid.
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "launch.h"
@@ -533,16 +534,19 @@ __global__ __launch_bounds__(kPlanThreads, 1) void plan_prefill_kernel(const Pre
 }  // namespace
 
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];  // per device (racing first calls store the same value)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
   if (dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return 148;  // not cached: a later call asks again
+    }
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 }  // namespace ckv

@@ -33,6 +33,7 @@
 #include <cuda.h>  // CUtensorMap and its enums (types only; the encoder is fetched at run time)
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "async_copy.cuh"
@@ -919,14 +920,19 @@ int make_map(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uint6
 }
 
 // ---------------------------------------------------------------- launchers
+// `configured` is a per-device cache (atomics: a repeated set-up by racing
+// threads is harmless).
 template <typename K>
-int opt_in_smem(K kernel, int bytes, bool* configured) {
+int opt_in_smem(K kernel, int bytes, std::atomic<bool>* configured) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CKV_ERR_LAUNCH;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+  const bool cached_dev = dev >= 0 && dev < 64;
+  if (!cached_dev || !configured[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+      cudaGetLastError();
       return CKV_ERR_LAUNCH;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    if (cached_dev) configured[dev].store(true, std::memory_order_release);
   }
   return CKV_OK;
 }
@@ -939,7 +945,7 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
   const uint32_t slices = static_cast<uint32_t>(a.head_dim / CS);
   const bool token = a.out_layout == CKV_OUT_TOKEN;
   if (a.capacity == 0 && !(token && a.num_q_tokens > 0)) return CKV_OK;
-  static bool configured[64] = {};
+  static std::atomic<bool> configured[64];
   auto kernel = c128_persistent_kernel<TIn, TOut, CS, NS, 1, false, kShortWaits>;
   int rc = opt_in_smem(kernel, Cfg::SMEM, configured);
   if (rc) return rc;
@@ -989,7 +995,7 @@ int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
     int rc = make_map(&page_map, a.state_mut, a.in_dtype, 2ull * a.head_dim, a.state_rows, PCS, 127);
     if (rc) return rc;
     using Cfg = PersistCfg<TIn, PCS, kDecNS, kDecNG, true>;
-    static bool configured_p[64] = {};
+    static std::atomic<bool> configured_p[64];
     auto kernel = c128_persistent_kernel<TIn, TOut, PCS, kDecNS, kDecNG, true, kShortWaits>;
     rc = opt_in_smem(kernel, Cfg::SMEM, configured_p);
     if (rc) return rc;
@@ -1005,7 +1011,7 @@ int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
   using Cfg = DecodeCfg<TIn>;
   const uint64_t tiles64 = static_cast<uint64_t>(a.capacity) * slices;
   if (tiles64 > 0x7FFFFFFFull) return CKV_ERR_SIZE;
-  static bool configured[64] = {};
+  static std::atomic<bool> configured[64];
   auto kernel = c128_decode_kernel<TIn, TOut, kShortWaits>;
   rc = opt_in_smem(kernel, Cfg::SMEM, configured);
   if (rc) return rc;
@@ -1040,17 +1046,18 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Fetched once, by the first caller (a function-local static: its
+// initialisation is thread-safe).
 EncodeTiledFn encoder() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+    return nullptr;
+  }();
   return fn;
 }
 }  // namespace

@@ -15,6 +15,7 @@
 // per (row, chunk) with direct loads.  The window is small enough that the
 // fp32 safe softmax runs entirely in registers.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "async_copy.cuh"
@@ -429,13 +430,13 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
   const int threads = S::consumers(hd) + 32;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CKV_ERR_LAUNCH;
-  static bool configured[64] = {};
-  if (!configured[dev]) {
+  static std::atomic<bool> configured[64];  // per device; a repeated set-up by racing threads is harmless
+  if (!configured[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kC4StageBudget) != cudaSuccess) {
       cudaGetLastError();
       return CKV_ERR_LAUNCH;
     }
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   alignas(64) C4Maps maps;
   memset(&maps, 0, sizeof maps);

@@ -90,6 +90,10 @@ def _prefill_case(name, ratio, rng):
         B = 1000
         pl = rng.integers(0, 5000, B)
         el = np.ones(B, np.int64)
+    elif name in ("uniform_32", "uniform_33"):  # the largest uniform extend of the per-request path, and one past it
+        B = 700
+        pl = rng.integers(0, 9000, B)
+        el = np.full(B, int(name[-2:]))
     elif name == "one_long":
         B = 1
         pl = np.array([rng.integers(0, 1000)])
@@ -105,7 +109,8 @@ def _prefill_case(name, ratio, rng):
 
 
 @pytest.mark.parametrize("ratio", [4, 128])
-@pytest.mark.parametrize("case", ["random", "mtp_uniform", "decode_like", "one_long", "max_batch_mixed"])
+@pytest.mark.parametrize("case", ["random", "mtp_uniform", "decode_like", "uniform_32", "uniform_33", "one_long",
+                                  "max_batch_mixed"])
 @pytest.mark.parametrize("pad", [False, True])
 def test_plan_prefill_bit_exact(env, ratio, case, pad):
     o, ckv, dev = env
@@ -144,6 +149,15 @@ def test_plan_prefill_empty_and_errors(env):
     torch.cuda.synchronize()
     assert counts[:2].tolist() == [3, 9] and int(status[0]) & ckv.STATUS_CAPACITY
     wc, ww, _, _ = o.plan_prefill(4, rid, sl, el, 13, 2, 3, check=False)
+    assert (pc.cpu().numpy() == wc).all() and (pw.cpu().numpy() == ww).all()
+    # the same with equal extends (the per-request emission of uniform batches), padded
+    rid, sl, el = [0, 1, 2], [8, 12, 7], [4, 4, 4]
+    status.zero_()
+    pc, pw, counts = ckv.plan_prefill(4, _dev_i64(rid, dev), _dev_i64(sl, dev), _dev_i64(el, dev), 12, 2, 5,
+                                      pad_invalid=True, status=status)
+    torch.cuda.synchronize()
+    assert counts[:2].tolist() == [3, 12] and int(status[0]) & ckv.STATUS_CAPACITY
+    wc, ww, _, _ = o.plan_prefill(4, rid, sl, el, 12, 2, 5, pad_invalid=True, check=False)
     assert (pc.cpu().numpy() == wc).all() and (pw.cpu().numpy() == ww).all()
     # bad lengths and a wrong token total: flagged, nothing emitted, no fault
     for sl_, el_, nq, bit in [([9, 5], [9, 6], 15, ckv.STATUS_BAD_LENGTH), ([9, 5], [9, 0], 9, ckv.STATUS_BAD_LENGTH),
