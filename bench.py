@@ -859,12 +859,14 @@ def bench_step(args, ws, rank, local):
     step_bytes = b5["total"] + b3["total"]
     # every kernel's cost inside the timed step, by difference (no event nodes between the kernels)
     instep_reps = max(200, 10 * args.steps)
-    instep = instep_by_difference(segments, flush, restore, reps=instep_reps)
+    instep = {} if args.no_instep else instep_by_difference(segments, flush, restore, reps=instep_reps)
     for key, nbytes in (("pool_prefill", b5["pool"]), ("write", b5["write"]), ("decode", b3["decode"])):
+        if args.no_instep:
+            break
         us = instep[f"{key}_us"]
         instep[f"{key}_instep_gbs"] = nbytes / (us * 1e-6) / 1e9 if us > 0 else None
         instep[f"{key}_instep_frac"] = instep[f"{key}_instep_gbs"] / peak if us > 0 else None
-    instep["method"] = ("median over rounds of (step time - time of the step without that kernel), each round "
+    instep["method"] = None if args.no_instep else ("median over rounds of (step time - time of the step without that kernel), each round "
                         f"replaying every variant once; {instep_reps} rounds, L2 flushed before every replay")
     # the decode kernel back to back over copies of its inputs that together exceed the L2 (a kernel of ~10 us
     # is not resolved by event nodes around it: they add the graph's node-to-node latency)
@@ -1020,7 +1022,7 @@ def bench_config(args, name, ws, rank, local):
     seg_ms, wall, _ = run_graph(step, flush, r.restore, args.steps, args.warmup, ws)
     whole = StepGraph(segs, inner_events=False)
     whole_ms, _, _ = run_graph(whole, flush, r.restore, args.steps, args.warmup, ws)
-    instep = instep_by_difference(segs, flush, r.restore, reps=max(200, 10 * args.steps))
+    instep = {} if args.no_instep else instep_by_difference(segs, flush, r.restore, reps=max(200, 10 * args.steps))
     if int(r.status[0]):
         raise RuntimeError(f"device status {int(r.status[0])}")
     peak, kind = peaks()
@@ -1174,6 +1176,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true", help="with --config: scaled-down workloads for profiling")
     ap.add_argument("--no-c4", action="store_true", help="skip the C4 kernels block of the step line")
+    ap.add_argument("--no-instep", action="store_true",
+                    help="skip the in-step costs by difference (200 rounds of every step variant), e.g. under ncu")
     ap.add_argument("--no-back-to-back", action="store_true",
                     help="skip the back-to-back timing of short kernels (keeps a profiler's launch list to the step)")
     ap.add_argument("--ref-fraction", type=float, default=0.125,

@@ -342,6 +342,10 @@ __device__ __forceinline__ bool prefill_record(const PoolArgs& a, uint32_t e, ui
 //            does the state write / zero output of rows blockIdx, blockIdx +
 //            gridDim, ... (the part of decode that reads no page).
 constexpr int kOwnRows = 512;   // decode: rows one CTA may own (boundary rows; rows it writes)
+// decode: tiles a producer keeps in flight (measured back to back on 512 rows
+// with the boundary-row list: lag 2 / 3 -> 9.23 / 9.09 us with 4 stages,
+// 9.25 / 9.10 us with 6)
+constexpr int kDecLag = 3;
 // decode: plan rows each thread examines per scan pass (measured with the
 // paced producer: 1 / 2 / 3 / 4 rows -> 10.17 / 9.22 / 9.56 / 9.85 us back to
 // back on 512 rows)
@@ -691,13 +695,15 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
     for (; n < items; ++n) {
       const int stage = static_cast<int>(n % NS);
       const uint32_t phase = (n / NS) & 1u;
-      // decode: at most two tiles ahead of the last that landed (tile n >= 2
-      // waits for tile n-2).  Every SM asking for its whole ring at once made
-      // each first tile wait for the whole burst; pacing the issue lets the
-      // first tiles land, and the reductions start, earlier.  (Tile n-2's
-      // stage is not refilled before tile n is issued, so its phase is exact.)
-      if ((kDecode && n >= 2 &&
-           !wait_for<kShortWaits>(smem_addr(&full_bar[(n - 2) % NS]), ((n - 2) / NS) & 1u, a.wait_ns)) ||
+      // decode: at most kDecLag tiles in flight (tile n >= kDecLag waits for
+      // tile n - kDecLag to land).  Every SM asking for its whole ring at once
+      // made each first tile wait for the whole burst; pacing the issue lets
+      // the first tiles land, and the reductions start, earlier.  (kDecLag <
+      // NS: that tile's stage is not refilled before tile n is issued, so its
+      // phase is exact.)
+      if ((kDecode && n >= static_cast<uint32_t>(kDecLag) &&
+           !wait_for<kShortWaits>(smem_addr(&full_bar[(n - kDecLag) % NS]), ((n - kDecLag) / NS) & 1u,
+                                  a.wait_ns)) ||
           !wait_for<kShortWaits>(smem_addr(&empty_bar[stage]), phase ^ 1u, a.wait_ns)) {
         status_or(a.d_status, CKV_STATUS_TIMEOUT);
         abort_flag = 1;
@@ -978,6 +984,7 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
 // rows, kDecNS stages, kDecNG consumer groups.
 constexpr int kDecCS = 64;
 constexpr int kDecNS = 4;
+static_assert(kDecLag < kDecNS, "the paced wait must name a stage that is not being refilled");
 constexpr int kDecNG = 2;  // consumer groups reduce alternate tiles
 
 template <typename TIn, typename TOut, bool kShortWaits>
