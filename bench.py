@@ -708,12 +708,27 @@ def instep_by_difference(segments, flush, restore, reps: int) -> dict:
     return out
 
 
+class nvtx_range:
+    """An NVTX range around a phase of the benchmark (visible in a profiler's timeline; free otherwise)."""
+
+    def __init__(self, name: str):
+        self.name = name
+
+    def __enter__(self):
+        torch.cuda.nvtx.range_push(self.name)
+
+    def __exit__(self, *exc):
+        torch.cuda.nvtx.range_pop()
+        return False
+
+
 def run_graph(step: StepGraph, flush, restore, steps, warmup, ws, sampler=None):
     """Per-step segment times (ms) of `steps` timed replays after `warmup` untimed ones."""
     for _ in range(warmup):
         restore()
         flush.zero_()
-        step.replay()
+        with nvtx_range("warmup step"):
+            step.replay()
     torch.cuda.synchronize()
     barrier(ws)
     torch.cuda.synchronize()
@@ -722,10 +737,12 @@ def run_graph(step: StepGraph, flush, restore, steps, warmup, ws, sampler=None):
     seg = []
     t0 = time.perf_counter()
     for _ in range(steps):
-        restore()
-        flush.zero_()
-        step.replay()
-        torch.cuda.synchronize()
+        with nvtx_range("restore + L2 flush"):
+            restore()
+            flush.zero_()
+        with nvtx_range("timed step"):
+            step.replay()
+            torch.cuda.synchronize()
         seg.append(step.times_ms())
     wall = time.perf_counter() - t0
     barrier(ws)
@@ -803,6 +820,34 @@ def oracle_step(o, w5, w3, frac5=1.0):
     return rows, time.perf_counter() - t0
 
 
+def oracle_step_threads(o, w5, w3, threads: int):
+    """The same oracle step with its independent parts spread over `threads` host threads (the C oracle
+    runs outside the GIL): the prefill's compress records in contiguous chunks, then its write records
+    in chunks (each writes its own state rows, after every pool), then the decode rows in chunks.  The
+    oracle itself is unchanged.  Returns (rows, seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    def chunks(n):
+        b = np.linspace(0, n, threads + 1).astype(np.int64)
+        return [(int(b[i]), int(b[i + 1])) for i in range(threads) if b[i + 1] > b[i]]
+
+    t0 = time.perf_counter()
+    pc, pw, (nc, nw), _ = o.plan_prefill(128, w5.rid, w5.seq_lens, w5.extend_lens)
+    st5 = wl.bits(w5.state).copy()
+    in5, ape5 = wl.bits(w5.kv_score), wl.bits(w5.ape)
+    st3 = wl.bits(w3.state).copy()
+    in3, ape3 = wl.bits(w3.kv_score), wl.bits(w3.ape)
+    pd = o.plan_decode(128, w3.rid, w3.seq_lens)
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda c: o.compress_pool_prefill(128, 512, o.BF16, o.F32, st5, in5, ape5, pc[c[0]:c[1]],
+                                                      c[1] - c[0], w5.num_q_tokens, o.OUT_COMPACT), chunks(nc)))
+        list(ex.map(lambda c: o.compress_write(128, 512, o.BF16, st5, in5, pw[c[0]:c[1]], c[1] - c[0]), chunks(nw)))
+        list(ex.map(lambda c: o.compress_decode(128, 512, o.BF16, o.F32, st3, in3[c[0]:c[1]], ape3, pd[c[0]:c[1]]),
+                    chunks(w3.batch)))
+    rows = nc + int((w3.seq_lens.numpy() % 128 == 0).sum())
+    return rows, time.perf_counter() - t0
+
+
 def cores_used() -> dict:
     try:
         aff = len(os.sched_getaffinity(0))
@@ -836,10 +881,12 @@ def bench_step(args, ws, rank, local):
     timed = StepGraph(segments, inner_events=True)
     launches_per_step = 5
     sampler = ClockSampler(local)
-    step_ms, wall, clocks = run_graph(step, flush, restore, args.steps, args.warmup, ws, sampler)
+    with nvtx_range("headline step"):
+        step_ms, wall, clocks = run_graph(step, flush, restore, args.steps, args.warmup, ws, sampler)
     step_ms = step_ms[:, 0]
     # per-kernel breakdown (event nodes between the kernels; not part of the headline)
-    seg_ms, _, _ = run_graph(timed, flush, restore, args.steps, args.warmup, ws)
+    with nvtx_range("per-kernel events"):
+        seg_ms, _, _ = run_graph(timed, flush, restore, args.steps, args.warmup, ws)
     if int(pre.status[0]) or int(dec.status[0]):
         raise RuntimeError(f"device status set: prefill {int(pre.status[0])} decode {int(dec.status[0])}")
     b5 = algorithmic_bytes(w5)
@@ -859,7 +906,8 @@ def bench_step(args, ws, rank, local):
     step_bytes = b5["total"] + b3["total"]
     # every kernel's cost inside the timed step, by difference (no event nodes between the kernels)
     instep_reps = max(200, 10 * args.steps)
-    instep = {} if args.no_instep else instep_by_difference(segments, flush, restore, reps=instep_reps)
+    with nvtx_range("in-step costs by difference"):
+        instep = {} if args.no_instep else instep_by_difference(segments, flush, restore, reps=instep_reps)
     for key, nbytes in (("pool_prefill", b5["pool"]), ("write", b5["write"]), ("decode", b3["decode"])):
         if args.no_instep:
             break
@@ -871,6 +919,7 @@ def bench_step(args, ws, rank, local):
     # the decode kernel back to back over copies of its inputs that together exceed the L2 (a kernel of ~10 us
     # is not resolved by event nodes around it: they add the graph's node-to-node latency)
     back_to_back = {}
+    torch.cuda.nvtx.range_push("back to back")
     if not args.no_back_to_back:
         n_dec = copies_for(b3["decode"], dev)
         us = steady_state_us(dec.steady_fns(n_dec))
@@ -890,8 +939,10 @@ def bench_step(args, ws, rank, local):
                              "write_vs_floor": min(floor["copy_us"], floor["elementwise_us"]) / us})
         pre.restore()
         torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
 
     # ---- end to end: inputs from pinned host memory, outputs back, inside the timed region
+    torch.cuda.nvtx.range_push("end to end")
     h_kv5 = w5.kv_score.pin_memory()
     h_len5 = [t.pin_memory() for t in (w5.rid, w5.seq_lens, w5.extend_lens)]
     h_kv3 = w3.kv_score.pin_memory()
@@ -921,6 +972,7 @@ def bench_step(args, ws, rank, local):
         torch.cuda.synchronize()
         if s > 0:  # the first pass warms the copy engines
             e2e_s += e0.elapsed_time(e1) / 1e3
+    torch.cuda.nvtx.range_pop()
     e2e_s = max_over_ranks(e2e_s, ws)
     e2e_value = sum_over_ranks(rows_per_step * e2e_steps, ws) / e2e_s
 
@@ -951,11 +1003,14 @@ def bench_step(args, ws, rank, local):
             **back_to_back,
             "sum_of_kernel_segments_us": float(seg_ms.sum(1).mean()) * 1e3,
             "step_gbs": step_bytes / (float(step_ms.mean()) * 1e-3) / 1e9},
-        "kernels_c4": c4_kernels(args, ckv, dev, seed, peak) if not args.no_c4 else None,
+        "kernels_c4": None,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if not args.no_c4:
+        with nvtx_range("C4 kernels"):
+            line["kernels_c4"] = c4_kernels(args, ckv, dev, seed, peak)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle as o
 
@@ -965,6 +1020,12 @@ def bench_step(args, ws, rank, local):
                                 "sample": "one whole step (all c128_prefill compress records + write, all "
                                           "c128_decode rows), single-threaded C, fp64 pool",
                                 "seconds": secs, **cores_used()}
+        n_thr = cores_used()["host_cores"] or 1
+        rows_t, secs_t = oracle_step_threads(o, w5, w3, n_thr)
+        line["cpu_baseline_threads"] = {"value": rows_t / secs_t, "unit": UNIT, "cores": n_thr, "kind": "oracle",
+                                        "sample": "the same step, its compress records, write records and decode "
+                                                  "rows split in contiguous chunks over one host thread per core",
+                                        "seconds": secs_t}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
