@@ -361,10 +361,14 @@ class DecodeRunner:
         self.ckv.plan_decode(self.w.ratio, self.rid, self.sl, self.plan_d[: self.w.batch], self.status,
                              order=self.order)
 
+    def hints(self):
+        """C128: the planner's rid / seq_lens, from which the decode prefetches its windows."""
+        return {} if self.order is None else {"rid_hint": self.rid, "seq_lens_hint": self.sl}
+
     def decode(self):
         self.ckv.compress_decode(self.w.ratio, self.w.head_dim, self.state, self.kv, self.ape,
                                  self.plan_d[: self.w.batch], self.w.out_dtype, self.out[: self.w.batch],
-                                 self.status, order=self.order)
+                                 self.status, order=self.order, **self.hints())
 
     def restore(self):
         self.state.copy_(self.pristine)
@@ -381,7 +385,7 @@ class DecodeRunner:
 
             def fn(st=st, kv=kv, pd=pd, out=out, order=order):
                 self.ckv.compress_decode(self.w.ratio, self.w.head_dim, st, kv, self.ape, pd, self.w.out_dtype, out,
-                                         self.status, order=order)
+                                         self.status, order=order, **self.hints())
             fns.append(fn)
         return fns
 

@@ -76,7 +76,7 @@ def load_library():
                                                   vp, vp]
         lib.ckv_compress_prefill.argtypes = [i32, i32, i32, i32, vp, u64, vp, u32, vp, vp, vp, vp, u32, u32, i32,
                                              vp, vp, vp]
-        lib.ckv_compress_decode.argtypes = [i32, i32, i32, i32, vp, u64, vp, vp, vp, vp, u32, vp, vp, vp]
+        lib.ckv_compress_decode.argtypes = [i32, i32, i32, i32, vp, u64, vp, vp, vp, vp, vp, vp, u32, vp, vp, vp]
         f32 = ctypes.c_float
         lib.ckv_capacity_online_units.argtypes = [u32, u32]
         lib.ckv_capacity_online_units.restype = u32
@@ -333,16 +333,23 @@ def compress_prefill(ratio: int, head_dim: int, state: torch.Tensor, kv_score: t
 
 def compress_decode(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
                     plan_d: torch.Tensor, out_dtype: torch.dtype = torch.float32, out: Optional[torch.Tensor] = None,
-                    status: Optional[torch.Tensor] = None, stream=None,
-                    order: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Decode step over ``plan_d``; ``order`` is the boundary-row list plan_decode wrote for it (optional)."""
+                    status: Optional[torch.Tensor] = None, stream=None, order: Optional[torch.Tensor] = None,
+                    rid_hint: Optional[torch.Tensor] = None, seq_lens_hint: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode step over ``plan_d``; ``order`` is the boundary-row list plan_decode wrote for it (optional);
+    ``rid_hint`` / ``seq_lens_hint`` are the arrays plan_decode read (optional, both or neither): the C128
+    decode prefetches windows from them before its dependency wait."""
     batch = plan_d.shape[0]
+    if (rid_hint is None) != (seq_lens_hint is None):
+        raise ValueError("rid_hint and seq_lens_hint go together")
+    if rid_hint is not None and _lengths(rid_hint, seq_lens_hint) != batch:
+        raise ValueError("the hints need one entry per batch row")
     if out is None:
         out = torch.empty(max(batch, 1), head_dim, dtype=out_dtype, device=kv_score.device)
     _check(load_library().ckv_compress_decode(ratio, head_dim, dtype_code(kv_score.dtype), dtype_code(out.dtype),
                                               _ptr(state), _state_rows(state, ratio, head_dim), _ptr(kv_score),
-                                              _ptr(ape), _ptr(plan_d), _order(order, batch), batch, _ptr(out),
-                                              _ptr(status), _stream(stream)), "ckv_compress_decode")
+                                              _ptr(ape), _ptr(plan_d), _order(order, batch), _ptr(rid_hint),
+                                              _ptr(seq_lens_hint), batch, _ptr(out), _ptr(status), _stream(stream)),
+           "ckv_compress_decode")
     return out[:batch]
 
 
@@ -475,5 +482,5 @@ def decode_step(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch.
     order = new_decode_order(rid.numel(), rid.device)
     plan_d = plan_decode(ratio, rid, seq_lens, status=status, stream=stream, order=order)
     out = compress_decode(ratio, head_dim, state, kv_score, ape, plan_d, out_dtype, status=status, stream=stream,
-                          order=order)
+                          order=order, rid_hint=rid, seq_lens_hint=seq_lens)
     return out, plan_d

@@ -93,14 +93,16 @@ int ckv_compress_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, v
 
 int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, void* state, uint64_t state_rows,
                         const void* kv_score_input, const void* ape, const ckv_decode_plan_t* plan_d,
-                        const ckv_decode_order_t* order, uint32_t batch, void* out, uint32_t* d_status,
-                        ckv_stream_t stream) {
+                        const ckv_decode_order_t* order, const int64_t* rid_hint, const int64_t* seq_lens_hint,
+                        uint32_t batch, void* out, uint32_t* d_status, ckv_stream_t stream) {
   int rc = check_pool_args(ratio, head_dim, in_dtype, out_dtype);
   if (rc) return rc;
   if (batch == 0) return CKV_OK;
   if (!aligned16(state) || !aligned16(kv_score_input) || !aligned16(ape) || !aligned16(plan_d) || !aligned16(out))
     return CKV_ERR_POINTER;
-  if (reinterpret_cast<uintptr_t>(order) & 7u) return CKV_ERR_POINTER;
+  if ((reinterpret_cast<uintptr_t>(order) | reinterpret_cast<uintptr_t>(rid_hint) |
+       reinterpret_cast<uintptr_t>(seq_lens_hint)) & 7u)
+    return CKV_ERR_POINTER;
   PoolArgs a{};
   a.ratio = ratio;
   a.head_dim = head_dim;
@@ -114,6 +116,8 @@ int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, vo
   a.ape = ape;
   a.plan_d = plan_d;
   a.order = order;
+  a.rid_hint = rid_hint != nullptr && seq_lens_hint != nullptr ? rid_hint : nullptr;
+  a.seq_hint = rid_hint != nullptr && seq_lens_hint != nullptr ? seq_lens_hint : nullptr;
   a.capacity = batch;
   a.out_layout = CKV_OUT_TOKEN;
   a.out = out;

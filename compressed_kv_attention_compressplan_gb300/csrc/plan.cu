@@ -148,8 +148,10 @@ template <int K>
 __global__ __launch_bounds__(kPlanThreads, 1) void plan_decode_ordered_kernel(
     int ratio, const int64_t* __restrict__ rid, const int64_t* __restrict__ seq_lens, uint32_t batch,
     ckv_decode_plan_t* __restrict__ plan_d, ckv_decode_order_t* __restrict__ order, uint32_t* d_status) {
-  pdl_wait();
+  // the decode that follows may launch at once: its CTAs then warm the L2
+  // while this kernel and its predecessor finish
   pdl_release();
+  pdl_wait();
   plan_decode_ordered_body<K>(ratio, batch, plan_d, order, [&](uint32_t b0, uint4 (&rec)[K]) {
     int64_t sl[K], r[K];
 #pragma unroll
@@ -240,8 +242,8 @@ __global__ void plan_decode_paged_kernel(const DecodePagedArgs a) {
 template <int K>
 __global__ __launch_bounds__(kPlanThreads, 1) void plan_decode_paged_ordered_kernel(const DecodePagedArgs a,
                                                                                    ckv_decode_order_t* order) {
+  pdl_release();  // as plan_decode_ordered_kernel
   pdl_wait();
-  pdl_release();
   plan_decode_ordered_body<K>(4, a.batch, a.plan_d, order, [&](uint32_t b0, uint4 (&rec)[K]) {
     int64_t sl[K], r[K];
 #pragma unroll

@@ -73,6 +73,13 @@ __device__ __forceinline__ void tma_box_g2s(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// One 2-D tensor-map box into L2 only (no shared memory, no barrier).
+__device__ __forceinline__ void tma_box_prefetch_l2(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -567,6 +574,27 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
     for (int i = t; i < static_cast<int>(nt) * lines; i += NT)
       prefetch_l2(reinterpret_cast<const uint8_t*>(input) + (blockIdx.x + (i / lines) * static_cast<size_t>(gridDim.x)) *
                                                                  width * sizeof(TIn) + (i % lines) * 128);
+  }
+  if (kDecode && a.seq_hint != nullptr) {
+    // Windows into L2 while the previous kernel drains: the rows this CTA
+    // writes (blockIdx, blockIdx + gridDim, ...) that end a page get their
+    // 127 page slots prefetched, every channel slice (whichever CTA pools
+    // them then finds them in L2).  The hints are read before the dependency
+    // wait, so they only steer prefetches: a stale value costs bandwidth,
+    // never a result; pages outside the state are not touched.
+    const uint32_t B = a.capacity;
+    const uint32_t nt = B > blockIdx.x ? (B - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
+    for (uint32_t k = t; k < nt; k += NT) {
+      const uint32_t r = blockIdx.x + k * gridDim.x;
+      int64_t sl, rid;
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(sl) : "l"(a.seq_hint + r));
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(rid) : "l"(a.rid_hint + r));
+      if (sl >= 128 && sl % 128 == 0 && rid >= 0 && rid < 0x7FFFFFFF / 128 &&
+          static_cast<uint64_t>(rid) * 128 + 127 < a.state_rows) {
+        const int y = static_cast<int>(rid * 128);
+        for (int x = 0; x < 2 * hd; x += CS) tma_box_prefetch_l2(&page_map, x, y);
+      }
+    }
   }
   pdl_wait();  // everything below may read what the previous kernel wrote
   pdl_release();

@@ -297,11 +297,19 @@ int ckv_compress_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, v
  * the C4 decode does not read it.  A list that does not match plan_d is a
  * caller error: its entries are still bounds-checked (a row >= batch or a
  * page outside the state is skipped with CKV_STATUS_BAD_INDEX), but the
- * outputs are then unspecified. */
+ * outputs are then unspecified.
+ * rid_hint, seq_lens_hint: NULL, or the int64 arrays [batch] the decode
+ * planner read (8-byte aligned; both or neither).  The C128 decode reads them
+ * BEFORE waiting for the previous kernel on the stream, only to prefetch the
+ * windows of page-boundary rows (page = rid, as both C128 decode planners
+ * give it) into L2 while that kernel finishes; nothing is computed from them.
+ * If the previous kernel is still writing them, a stale value only costs
+ * the bandwidth of a useless prefetch; pages outside the state are skipped.
+ * The C4 decode does not read them. */
 int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, void* state, uint64_t state_rows,
                         const void* kv_score_input, const void* ape, const ckv_decode_plan_t* plan_d,
-                        const ckv_decode_order_t* order, uint32_t batch, void* out, uint32_t* d_status,
-                        ckv_stream_t stream);
+                        const ckv_decode_order_t* order, const int64_t* rid_hint, const int64_t* seq_lens_hint,
+                        uint32_t batch, void* out, uint32_t* d_status, ckv_stream_t stream);
 
 /* ------------------------------------------------------- online C128 state */
 /* compressor_v2.py can keep C128 state online: one slot of 3 * head_dim per

@@ -61,12 +61,13 @@ def test_argument_errors_are_returned_before_any_launch(lib):
     assert lib.ckv_plan_decode(128, vp(8), vp(8), 1, vp(16), vp(12), None, None) == -4
     assert lib.ckv_plan_prefill(4, None, None, None, 2000, 0, 0, 0, 0, None, None, vp(16), None, None) == -3
     assert lib.ckv_plan_prefill(4, None, None, None, 1, 0, 0, 0, 0, None, None, vp(16), None, None) == -4
-    assert lib.ckv_compress_decode(4, 100, 1, 0, None, 0, None, None, None, None, 1, None, None, None) == -2
-    assert lib.ckv_compress_decode(4, 128, 7, 0, None, 0, None, None, None, None, 1, None, None, None) == -5
-    assert lib.ckv_compress_decode(4, 128, 1, 0, vp(8), 8, vp(16), vp(16), vp(16), None, 1, vp(16), None,
-                                   None) == -4
-    assert lib.ckv_compress_decode(128, 512, 1, 0, vp(16), 8, vp(16), vp(16), vp(16), vp(12), 1, vp(16), None,
-                                   None) == -4
+    dec = lib.ckv_compress_decode
+    assert dec(4, 100, 1, 0, None, 0, None, None, None, None, None, None, 1, None, None, None) == -2
+    assert dec(4, 128, 7, 0, None, 0, None, None, None, None, None, None, 1, None, None, None) == -5
+    assert dec(4, 128, 1, 0, vp(8), 8, vp(16), vp(16), vp(16), None, None, None, 1, vp(16), None, None) == -4
+    # the boundary-row list and the prefetch hints must be 8-byte aligned
+    assert dec(128, 512, 1, 0, vp(16), 8, vp(16), vp(16), vp(16), vp(12), None, None, 1, vp(16), None, None) == -4
+    assert dec(128, 512, 1, 0, vp(16), 8, vp(16), vp(16), vp(16), None, vp(20), vp(16), 1, vp(16), None, None) == -4
     assert lib.ckv_compress_pool_prefill(128, 512, 1, 0, None, 0, None, 10, None, None, None, 1, 9, None, None,
                                          None) == -5
     assert lib.ckv_compress_write(4, 2048, 1, None, 0, None, 0, None, None, 1, None, None) == -2

@@ -85,8 +85,8 @@ def test_prefill_workload_full_size(env, name):
 @pytest.mark.parametrize("name", ["c4_decode", "c128_decode"])
 @pytest.mark.parametrize("ordered", [True, False])
 def test_decode_workload_full_size(env, name, ordered):
-    """Every row of the decode workloads, through the boundary-row list (the
-    benchmark's path) and through the plan scan."""
+    """Every row of the decode workloads, through the boundary-row list with the
+    prefetch hints (the benchmark's path) and through the plan scan."""
     o, ckv, dev = env
     w = wl.NAMED[name](0)
     R, hd = w.ratio, w.head_dim
@@ -95,8 +95,9 @@ def test_decode_workload_full_size(env, name, ordered):
     status = ckv.new_status(dev)
     order = ckv.new_decode_order(w.batch, dev) if ordered else None
     pd = ckv.plan_decode(R, w.rid.to(dev), w.seq_lens.to(dev), status=status, order=order)
+    hints = {"rid_hint": w.rid.to(dev), "seq_lens_hint": w.seq_lens.to(dev)} if ordered else {}
     out = ckv.compress_decode(R, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), pd, w.out_dtype, status=status,
-                              order=order)
+                              order=order, **hints)
     torch.cuda.synchronize()
     assert int(status[0]) == 0
     wpd = o.plan_decode(R, w.rid, w.seq_lens)

@@ -129,7 +129,8 @@ def test_decode_step_replayed_from_a_graph(env, ratio, ordered):
 
     def step():
         ckv.plan_decode(ratio, rid, sl_d, plan_d, status, order=order)
-        ckv.compress_decode(ratio, hd, state, kv, ape, plan_d, torch.float32, out=out, status=status, order=order)
+        ckv.compress_decode(ratio, hd, state, kv, ape, plan_d, torch.float32, out=out, status=status, order=order,
+                            **({"rid_hint": rid, "seq_lens_hint": sl_d} if ordered else {}))
 
     step()
     torch.cuda.synchronize()

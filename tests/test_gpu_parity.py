@@ -320,6 +320,49 @@ def test_out_of_range_records_are_flagged_not_faulted(env):
         assert int(status[0]) & ckv.STATUS_BAD_INDEX
 
 
+@pytest.mark.parametrize("ratio", [4, 128])
+def test_decode_prefetch_hints_only_steer_prefetches(env, ratio):
+    """The rid / seq_lens hints are read before the decode's dependency wait,
+    so they may be stale: hints that name other rows, other pages, pages past
+    the state and negative ids leave every output and state byte as without
+    hints (and as the oracle's)."""
+    o, ckv, dev = env
+    hd = 512
+    rng = np.random.default_rng(ratio + 5)
+    B = 300
+    sl = rng.integers(1, 9000, B)
+    sl[:90] = ratio * rng.integers(1, 60, 90)
+    w = wl.random_decode(ratio, hd, torch.bfloat16, torch.float32, sl, seed=ratio + 5, num_requests_state=320)
+    order = ckv.new_decode_order(B, dev)
+    pd = ckv.plan_decode(ratio, w.rid.to(dev), w.seq_lens.to(dev), order=order)
+    outs = {}
+    for name, hints in [("none", None),
+                        ("right", (w.rid, w.seq_lens)),
+                        ("stale", (torch.from_numpy(rng.permutation(320)[:B]).to(torch.int64),
+                                   torch.from_numpy(ratio * rng.integers(1, 99, B)).to(torch.int64))),
+                        ("outside", (torch.full((B,), 10 ** 9, dtype=torch.int64), torch.full((B,), 128, dtype=torch.int64))),
+                        ("negative", (torch.full((B,), -5, dtype=torch.int64), torch.full((B,), -128, dtype=torch.int64)))]:
+        state_d = w.state.to(dev)
+        status = ckv.new_status(dev)
+        kw = {} if hints is None else {"rid_hint": hints[0].to(dev), "seq_lens_hint": hints[1].to(dev)}
+        out = ckv.compress_decode(ratio, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), pd, torch.float32,
+                                  status=status, order=order, **kw)
+        torch.cuda.synchronize()
+        assert int(status[0]) == 0, name
+        outs[name] = (H.np_bits(out).copy(), H.np_bits(state_d).copy())
+    for name in ("right", "stale", "outside", "negative"):
+        assert (outs[name][0].view(np.uint32) == outs["none"][0].view(np.uint32)).all(), name
+        assert (outs[name][1].view(np.uint8) == outs["none"][1].view(np.uint8)).all(), name
+    st = wl.bits(w.state).copy()
+    want = o.compress_decode(ratio, hd, 1, 0, st, wl.bits(w.kv_score), wl.bits(w.ape), o.plan_decode(ratio, w.rid, w.seq_lens))
+    f = H.plan_d_fields(pd.cpu().numpy())
+    bnd = np.nonzero(f["seq_len"] % ratio == 0)[0]
+    kvmax = H.window_kv_absmax(ratio, hd, wl.bits(w.state), wl.bits(w.kv_score), f["seq_len"][bnd], bnd,
+                               np.full(len(bnd), H.window(ratio) - 1), f["read_page_0"][bnd], f["read_page_1"][bnd])
+    H.assert_pool_close(outs["none"][0][bnd], want[bnd], 0, kvmax, "decode with hints")
+    assert (outs["none"][1].view(np.uint8) == st.view(np.uint8)).all()
+
+
 def test_bad_order_entries_are_flagged_not_faulted(env):
     """A boundary-row list that does not match the plan (a row past the batch, a
     page outside the state, a count larger than the batch) is bounds-checked by
