@@ -52,21 +52,36 @@ class OracleError(RuntimeError):
         self.code = code
 
 
-def build(force: bool = False, mutant: int = 0) -> str:
-    """Compile the oracle with gcc (plain C11, -O2, no fp contraction).
-
-    ``mutant`` > 0 builds a test-only variant with one planted mistake (the
-    mutation check of the pins); the oracle proper is mutant 0."""
-    os.makedirs(_LIB_DIR, exist_ok=True)
-    lib = _LIB if mutant == 0 else os.path.join(_LIB_DIR, f"libckv_oracle_mutant{mutant}.so")
-    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= os.path.getmtime(_SRC):
-        return lib
+def _compile(src: str, lib: str) -> str:
     tmp = lib + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-Wall", "-shared", "-fPIC",
-           f"-DORC_MUTANT={int(mutant)}", "-o", tmp, _SRC, "-lm"]
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-Wall", "-shared", "-fPIC", "-o", tmp,
+           src, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, lib)
     return lib
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C11, -O2, no fp contraction)."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    return _compile(_SRC, _LIB)
+
+
+def source() -> str:
+    """The oracle's C source (test-only use: the mutation check patches a copy)."""
+    return open(_SRC).read()
+
+
+def build_variant(text: str, tag: str) -> str:
+    """Test-only: compile another C source text (a patched copy of the oracle) to its own library under
+    _build/; route calls to it with use_library()."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    src = os.path.join(_LIB_DIR, f"ckv_oracle_{tag}.c")
+    with open(src, "w") as f:
+        f.write(text)
+    return _compile(src, os.path.join(_LIB_DIR, f"libckv_oracle_{tag}.so"))
 
 
 def use_library(path: str | None):

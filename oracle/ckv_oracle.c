@@ -24,12 +24,6 @@
 #include <math.h>
 #include <stdint.h>
 
-/* Test-only: a build with ORC_MUTANT = k > 0 plants one plausible mistake
- * (see the numbered sites below), so that the test-suite can show that every
- * such mistake fails at least one pin.  The oracle proper is ORC_MUTANT = 0. */
-#ifndef ORC_MUTANT
-#define ORC_MUTANT 0
-#endif
 #include <stdlib.h>
 #include <string.h>
 
@@ -163,7 +157,7 @@ static void pool_window(int ratio, int hd, int in_dtype, int out_dtype, const vo
       if (!entries[i]) continue;
       int sc_col = ratio == 4 ? (i < 4 ? 2 * hd : 3 * hd) + c : hd + c;
       float score = load_elem(entries[i], (size_t)sc_col, in_dtype);
-      int arow = ORC_MUTANT == 1 ? (i + 1) % W : i; /* mutant 1: ape row off by one */
+      int arow = i;
       float bias = load_elem(ape, (size_t)arow * hd + c, in_dtype);
       float si = score + bias; /* one fp32 rounding */
       s[i] = si;
@@ -173,11 +167,11 @@ static void pool_window(int ratio, int hd, int in_dtype, int out_dtype, const vo
     double num = 0.0, den = 0.0;
     for (int i = 0; i < W; ++i) {
       if (!entries[i]) continue;
-      int kv_col = (ratio == 4) ? (i < 4 ? (ORC_MUTANT == 2 ? hd : 0) : hd) + c : c; /* mutant 2: halves */
+      int kv_col = (ratio == 4) ? (i < 4 ? 0 : hd) + c : c;
       double kv = (double)load_elem(entries[i], (size_t)kv_col, in_dtype);
-      double w = ORC_MUTANT == 10 ? exp((double)m - (double)s[i]) : exp((double)s[i] - (double)m); /* 10: sign */
+      double w = exp((double)s[i] - (double)m);
       num += kv * w;
-      if (!(ORC_MUTANT == 9 && i == W - 1)) den += w; /* mutant 9: a dropped term */
+      den += w;
     }
     store_elem(out_row, (size_t)c, out_dtype, have ? num / den : 0.0);
   }
@@ -208,7 +202,7 @@ int orc_plan_decode(int ratio, const int64_t* rid, const int64_t* seq_lens, uint
     if (seq_lens[b] < 1 || seq_lens[b] > INT32_MAX || rid[b] < 0) return ORC_BAD_LENGTH;
     int64_t p1 = seq_lens[b] - 1;
     int64_t p0 = p1 - ratio > 0 ? p1 - ratio : 0;
-    int64_t loc = legacy_loc(ratio, rid[b], ORC_MUTANT == 6 ? p1 + 1 : p1); /* mutant 6: write slot */
+    int64_t loc = legacy_loc(ratio, rid[b], p1);
     if (loc > INT32_MAX) return ORC_BAD_INDEX;
     plan[b].seq_len = (uint32_t)seq_lens[b];
     plan[b].write_loc = (int32_t)loc;
@@ -245,14 +239,14 @@ int orc_plan_prefill(int ratio, const int64_t* rid, const int64_t* seq_lens, con
     const int64_t sl = seq_lens[b], el = extend_lens[b];
     if (!(0 < el && el <= sl) || sl > INT32_MAX || rid[b] < 0) return ORC_BAD_LENGTH;
     const int64_t pl = sl - el;
-    const int64_t first_w = (sl / ratio) * ratio - (ORC_MUTANT == 5 ? 0 : overlap); /* mutant 5: write set */
+    const int64_t first_w = (sl / ratio) * ratio - overlap;
     for (int64_t j = 0; j < el; ++j) {
       const int64_t p = pl + j;
-      const uint64_t ragged = (ORC_MUTANT == 7 ? 0 : token_base) + (uint64_t)j; /* mutant 7: ragged base */
+      const uint64_t ragged = token_base + (uint64_t)j;
       if ((p + 1) % ratio == 0) {
         if (nc < cap_c) {
-          const int64_t bl = W - (j + 1 < W ? j + 1 : W) - (ORC_MUTANT == 4 && j + 1 < W ? 1 : 0); /* 4 */
-          const int64_t p0 = ORC_MUTANT == 8 ? p : (p - ratio > 0 ? p - ratio : 0); /* mutant 8 */
+          const int64_t bl = W - (j + 1 < W ? j + 1 : W);
+          const int64_t p0 = p - ratio > 0 ? p - ratio : 0;
           pc[nc].seq_len = (uint32_t)(p + 1);
           pc[nc].ragged_bl = (uint32_t)ragged | ((uint32_t)bl << 24);
           pc[nc].read_page_0 = (int32_t)legacy_page(ratio, rid[b], p0);
@@ -293,7 +287,7 @@ static int64_t paged_row(const int32_t* r2t, int64_t stride, const int64_t* f2s,
   if (raw < 0 || (uint64_t)raw >= nfull) return -1;
   const int64_t swa = f2s[raw];
   if (swa < 0) return -1;
-  return (swa / sps) * ring + swa % (ORC_MUTANT == 13 ? sps : ring); /* mutant 13: ring offset */
+  return (swa / sps) * ring + swa % ring;
 }
 
 /* State row of position p under the paged addressing: C4 through the SWA
@@ -340,7 +334,7 @@ int orc_plan_prefill_paged(int ratio, const int64_t* rid, const int32_t* r2t, in
         if (nc < cap_c) {
           const int64_t bl = W - (j + 1 < W ? j + 1 : W);
           int64_t page0 = -1, page1 = b;
-          if (bl > 0 || ORC_MUTANT == 14) { /* mutant 14: records without state reads translated */
+          if (bl > 0) {
             const int64_t p0 = p - ratio > 0 ? p - ratio : 0;
             const int64_t row0 = paged_or_c128_row(ratio, r2t, stride, f2s, nfull, sps, ring, rid[b], p0);
             const int64_t row1 = paged_or_c128_row(ratio, r2t, stride, f2s, nfull, sps, ring, rid[b], p);
@@ -355,7 +349,7 @@ int orc_plan_prefill_paged(int ratio, const int64_t* rid, const int32_t* r2t, in
         }
         ++nc;
       }
-      if (p >= first_w || (ORC_MUTANT != 12 && ratio == 4 && p % sps >= sps - ratio)) { /* 12: page ends */
+      if (p >= first_w || (ratio == 4 && p % sps >= sps - ratio)) {
         if (nw < cap_w) {
           const int64_t row = paged_or_c128_row(ratio, r2t, stride, f2s, nfull, sps, ring, rid[b], p);
           if (row < 0) return ORC_BAD_INDEX;
@@ -436,7 +430,7 @@ int orc_compress_pool_prefill(int ratio, int hd, int in_dtype, int out_dtype, co
     const int64_t seq_len = P->seq_len;
     if (ragged >= num_q_tokens) { free(entries); return ORC_BAD_INDEX; }
     for (int i = 0; i < W; ++i) {
-      if (ORC_MUTANT != 3 && ratio == 4 && seq_len == 4 && i < 4) { /* first group: no previous group */
+      if (ratio == 4 && seq_len == 4 && i < 4) { /* first group: no previous group */
         entries[i] = NULL;
         continue;
       }
@@ -446,7 +440,7 @@ int orc_compress_pool_prefill(int ratio, int hd, int in_dtype, int out_dtype, co
         if (srow < 0 || (uint64_t)srow >= state_rows) { free(entries); return ORC_BAD_INDEX; }
         entries[i] = row_ptr(state, srow, width, in_dtype);
       } else {
-        int64_t irow = ragged - (W - 1) + i - (ORC_MUTANT == 11 ? 1 : 0); /* mutant 11: input row */
+        int64_t irow = ragged - (W - 1) + i;
         if (irow < 0) { free(entries); return ORC_BAD_INDEX; }
         entries[i] = row_ptr(input, irow, width, in_dtype);
       }
@@ -498,7 +492,7 @@ int orc_compress_decode(int ratio, int hd, int in_dtype, int out_dtype, void* st
     memcpy((char*)state + (size_t)P->write_loc * row_bytes, row_ptr(input, b, width, in_dtype), row_bytes);
     if (P->seq_len % (uint32_t)ratio != 0) continue;
     for (int i = 0; i < W; ++i) {
-      if (ORC_MUTANT != 3 && ratio == 4 && P->seq_len == 4 && i < 4) {
+      if (ratio == 4 && P->seq_len == 4 && i < 4) {
         entries[i] = NULL;
         continue;
       }
@@ -610,7 +604,7 @@ int orc_plan_online_prefill(const int64_t* rid, const int64_t* seq_lens, const i
 
 /* One token into channel c's running state (double). */
 static void online_step(double* m, double* l, double* a, int first, double s, double kv) {
-  if (first && ORC_MUTANT != 18) { /* mutant 18: no reset at a group start */
+  if (first) {
     *m = s;
     *l = 1.0;
     *a = kv;
@@ -618,14 +612,14 @@ static void online_step(double* m, double* l, double* a, int first, double s, do
   }
   const double mn = s > *m ? s : *m;
   const double c = exp(*m - mn), e = exp(s - mn);
-  *l = ORC_MUTANT == 19 ? *l + e : *l * c + e; /* mutant 19: the sum not rescaled */
+  *l = *l * c + e;
   *a = *a * c + kv * e;
   *m = mn;
 }
 
 static double online_s(const void* row, int hd, int c, int in_dtype, const void* ape, int64_t p) {
   const float score = load_elem(row, (size_t)hd + c, in_dtype);
-  const float bias = load_elem(ape, (size_t)((p + (ORC_MUTANT == 20)) % 128) * hd + c, in_dtype); /* 20 */
+  const float bias = load_elem(ape, (size_t)(p % 128) * hd + c, in_dtype);
   return (double)(float)(score + bias); /* one fp32 rounding, as the window form */
 }
 
@@ -762,7 +756,7 @@ int orc_norm_rope_store(int ratio, int mode, int hd, int rope_dim, int in_dtype,
       row = k;
       loc_index = k;
       zero = P->seq_len % (uint32_t)ratio != 0;
-      pos = (int64_t)P->seq_len - (ORC_MUTANT == 16 ? 0 : ratio); /* mutant 16: position */
+      pos = (int64_t)P->seq_len - ratio;
       if (pos < 0) pos = 0;
     } else {
       const orc_plan_c* P = (const orc_plan_c*)plan + k;
@@ -770,7 +764,7 @@ int orc_norm_rope_store(int ratio, int mode, int hd, int rope_dim, int in_dtype,
       const int64_t ragged = P->ragged_bl & 0x00FFFFFFu;
       row = in_layout == ORC_OUT_COMPACT ? (int64_t)k : ragged;
       loc_index = ragged;
-      pos = (int64_t)P->seq_len - (ORC_MUTANT == 16 ? 0 : ratio);
+      pos = (int64_t)P->seq_len - ratio;
     }
     /* the table is read only when there is something to rotate */
     if ((uint64_t)row >= n_rows || (uint64_t)loc_index >= n_loc || pos < 0 ||
@@ -790,12 +784,12 @@ int orc_norm_rope_store(int ratio, int mode, int hd, int rope_dim, int in_dtype,
     }
     const double r = 1.0 / sqrt(ss / hd + (double)eps);
     for (int c = 0; c < hd; ++c) y[c] = y[c] * r * (double)weight[c];
-    const int base = ORC_MUTANT == 17 ? 0 : hd - rope_dim; /* mutant 17: rope on the first channels */
+    const int base = hd - rope_dim;
     for (int i = 0; i < rope_dim / 2; ++i) {
       const double cs = freqs[((size_t)pos * (rope_dim / 2) + i) * 2];
       const double sn = freqs[((size_t)pos * (rope_dim / 2) + i) * 2 + 1];
       const double a = y[base + 2 * i], b = y[base + 2 * i + 1];
-      y[base + 2 * i] = ORC_MUTANT == 15 ? a * cs + b * sn : a * cs - b * sn; /* mutant 15: rotation sign */
+      y[base + 2 * i] = a * cs - b * sn;
       y[base + 2 * i + 1] = a * sn + b * cs;
     }
     for (int c = 0; c < hd; ++c) store_elem(cache, (size_t)loc * hd + c, cache_dtype, y[c]);

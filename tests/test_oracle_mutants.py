@@ -1,4 +1,4 @@
-"""Mutation check of the oracle's pins: each test-only oracle build with one
+"""Mutation check of the oracle's pins: a copy of the oracle's C source with one
 planted, plausible mistake (a wrong ape row, swapped kv halves, a missing
 first-group mask, buffer_len off by one, a short write set, a decode slot off
 by one, a ragged id without its request offset, a wrong read page, a dropped
@@ -6,7 +6,9 @@ term, a sign error, an input row off by one; in the SWA-paged planner: no
 page-end writes, the ring offset taken modulo the page size, records without
 state reads translated; in norm + RoPE: a rotation sign, the position, the
 rotated channels; in the online state: no reset at a group start, the sum not
-rescaled, an ape row off by one) must fail at least one pin."""
+rescaled, an ape row off by one) is compiled on its own and must fail at least
+one pin.  The mistakes are textual patches of the source (the first n
+occurrences of a fragment replaced), so the oracle itself carries no hooks."""
 import pytest
 
 from tests import test_oracle_norm_rope as N
@@ -14,27 +16,90 @@ from tests import test_oracle_online as L
 from tests import test_oracle_paged as Q
 from tests import test_oracle_pins as P
 
+# mutant -> (what it plants, [(fragment of the oracle source, its replacement, occurrences replaced)])
 MUTANTS = {
-    1: "ape row off by one",
-    2: "C4 overlap entries read the main kv half",
-    3: "first-group mask missing",
-    4: "buffer_len off by one",
-    5: "C4 write set without the overlap group",
-    6: "decode write slot off by one",
-    7: "ragged id without the request offset",
-    8: "read_page_0 of the current group",
-    9: "a dropped denominator term",
-    10: "sign error in the exponent",
-    11: "input row off by one",
-    12: "paged C4 write set without the SWA page ends",
-    13: "paged ring offset modulo the SWA page size",
-    14: "paged records without state reads translated",
-    15: "RoPE rotation sign",
-    16: "RoPE position seq_len instead of seq_len - ratio",
-    17: "RoPE on the first rope_dim channels",
-    18: "online state not reset at a group start",
-    19: "online sum not rescaled on a new maximum",
-    20: "online ape row off by one",
+    1: ('ape row off by one', [
+        ('int arow = i;',
+         'int arow = (i + 1) % W;', 1),
+    ]),
+    2: ('C4 overlap entries read the main kv half', [
+        ('int kv_col = (ratio == 4) ? (i < 4 ? 0 : hd) + c : c;',
+         'int kv_col = (ratio == 4) ? (i < 4 ? hd : hd) + c : c;', 1),
+    ]),
+    3: ('first-group mask missing', [
+        ('if (ratio == 4 && seq_len == 4 && i < 4) { /* first group: no previous group */',
+         'if (0) {', 1),
+        ('if (ratio == 4 && P->seq_len == 4 && i < 4) {',
+         'if (0) {', 1),
+    ]),
+    4: ('buffer_len off by one', [
+        ('const int64_t bl = W - (j + 1 < W ? j + 1 : W);',
+         'const int64_t bl = W - (j + 1 < W ? j + 1 : W) - (j + 1 < W ? 1 : 0);', 1),
+    ]),
+    5: ('C4 write set without the overlap group', [
+        ('const int64_t first_w = (sl / ratio) * ratio - overlap;',
+         'const int64_t first_w = (sl / ratio) * ratio - 0;', 1),
+    ]),
+    6: ('decode write slot off by one', [
+        ('int64_t loc = legacy_loc(ratio, rid[b], p1);',
+         'int64_t loc = legacy_loc(ratio, rid[b], p1 + 1);', 1),
+    ]),
+    7: ('ragged id without the request offset', [
+        ('const uint64_t ragged = token_base + (uint64_t)j;',
+         'const uint64_t ragged = 0 + (uint64_t)j;', 1),
+    ]),
+    8: ('read_page_0 of the current group', [
+        ('const int64_t p0 = p - ratio > 0 ? p - ratio : 0;',
+         'const int64_t p0 = p;', 1),
+    ]),
+    9: ('a dropped denominator term', [
+        ('den += w;',
+         'if (i != W - 1) den += w;', 1),
+    ]),
+    10: ('sign error in the exponent', [
+        ('double w = exp((double)s[i] - (double)m);',
+         'double w = exp((double)m - (double)s[i]);', 1),
+    ]),
+    11: ('input row off by one', [
+        ('int64_t irow = ragged - (W - 1) + i;',
+         'int64_t irow = ragged - (W - 1) + i - 1;', 1),
+    ]),
+    12: ('paged C4 write set without the SWA page ends', [
+        ('if (p >= first_w || (ratio == 4 && p % sps >= sps - ratio)) {',
+         'if (p >= first_w) {', 1),
+    ]),
+    13: ('paged ring offset modulo the SWA page size', [
+        ('return (swa / sps) * ring + swa % ring;',
+         'return (swa / sps) * ring + swa % sps;', 1),
+    ]),
+    14: ('paged records without state reads translated', [
+        ('if (bl > 0) {',
+         'if (1) {', 1),
+    ]),
+    15: ('RoPE rotation sign', [
+        ('y[base + 2 * i] = a * cs - b * sn;',
+         'y[base + 2 * i] = a * cs + b * sn;', 1),
+    ]),
+    16: ('RoPE position seq_len instead of seq_len - ratio', [
+        ('pos = (int64_t)P->seq_len - ratio;',
+         'pos = (int64_t)P->seq_len - 0;', 2),
+    ]),
+    17: ('RoPE on the first rope_dim channels', [
+        ('const int base = hd - rope_dim;',
+         'const int base = 0;', 1),
+    ]),
+    18: ('online state not reset at a group start', [
+        ('if (first) {',
+         'if (0) {', 1),
+    ]),
+    19: ('online sum not rescaled on a new maximum', [
+        ('*l = *l * c + e;',
+         '*l = *l + e;', 1),
+    ]),
+    20: ('online ape row off by one', [
+        ('const float bias = load_elem(ape, (size_t)(p % 128) * hd + c, in_dtype);',
+         'const float bias = load_elem(ape, (size_t)((p + 1) % 128) * hd + c, in_dtype);', 1),
+    ]),
 }
 
 
@@ -63,10 +128,18 @@ def pins(o):
     yield lambda: L.test_online_schedules_equal_window_definition(o, 0)
 
 
+def mutated_source(o, mutant):
+    text = o.source()
+    for fragment, replacement, n in MUTANTS[mutant][1]:
+        assert text.count(fragment) >= n, f"mutant {mutant}: {fragment!r} not in the oracle source"
+        text = text.replace(fragment, replacement, n)
+    return text
+
+
 @pytest.mark.parametrize("mutant", sorted(MUTANTS))
 def test_every_planted_mistake_fails_a_pin(oracle_mod, mutant):
     o = oracle_mod
-    path = o.build(mutant=mutant)
+    path = o.build_variant(mutated_source(o, mutant), f"mutant{mutant}")
     o.use_library(path)
     try:
         caught = None
@@ -76,7 +149,7 @@ def test_every_planted_mistake_fails_a_pin(oracle_mod, mutant):
             except Exception as e:  # an assertion, an oracle error code, a numpy error
                 caught = e
                 break
-        assert caught is not None, f"mutant {mutant} ({MUTANTS[mutant]}) passed every pin"
+        assert caught is not None, f"mutant {mutant} ({MUTANTS[mutant][0]}) passed every pin"
     finally:
         o.use_library(None)
 
