@@ -362,8 +362,8 @@ class DecodeRunner:
                              order=self.order)
 
     def hints(self):
-        """C128: the planner's rid / seq_lens, from which the decode prefetches its windows."""
-        return {} if self.order is None else {"rid_hint": self.rid, "seq_lens_hint": self.sl}
+        """The planner's rid / seq_lens, from which the decode prefetches its windows."""
+        return {"rid_hint": self.rid, "seq_lens_hint": self.sl}
 
     def decode(self):
         self.ckv.compress_decode(self.w.ratio, self.w.head_dim, self.state, self.kv, self.ape,

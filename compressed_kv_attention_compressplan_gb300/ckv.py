@@ -336,8 +336,8 @@ def compress_decode(ratio: int, head_dim: int, state: torch.Tensor, kv_score: to
                     status: Optional[torch.Tensor] = None, stream=None, order: Optional[torch.Tensor] = None,
                     rid_hint: Optional[torch.Tensor] = None, seq_lens_hint: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Decode step over ``plan_d``; ``order`` is the boundary-row list plan_decode wrote for it (optional);
-    ``rid_hint`` / ``seq_lens_hint`` are the arrays plan_decode read (optional, both or neither): the C128
-    decode prefetches windows from them before its dependency wait."""
+    ``rid_hint`` / ``seq_lens_hint`` are the arrays plan_decode read (optional, both or neither): the decode
+    prefetches its windows from them before its dependency wait."""
     batch = plan_d.shape[0]
     if (rid_hint is None) != (seq_lens_hint is None):
         raise ValueError("rid_hint and seq_lens_hint go together")

@@ -84,8 +84,8 @@ __device__ __forceinline__ uint4 legacy_decode_record(int ratio, int64_t sl, int
 
 __global__ void plan_decode_kernel(int ratio, const int64_t* __restrict__ rid, const int64_t* __restrict__ seq_lens,
                                    uint32_t batch, ckv_decode_plan_t* __restrict__ plan_d, uint32_t* d_status) {
+  pdl_release();  // the decode may launch at once and warm the L2 (see plan_decode_ordered_kernel)
   pdl_wait();
-  pdl_release();
   const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
   *reinterpret_cast<uint4*>(plan_d + b) = legacy_decode_record(ratio, seq_lens[b], rid[b], d_status);

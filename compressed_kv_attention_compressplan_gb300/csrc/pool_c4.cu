@@ -40,6 +40,10 @@ __device__ __forceinline__ void tma_box4_g2s(uint32_t dst, const CUtensorMap* ma
       : "memory");
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -333,18 +337,17 @@ __global__ __launch_bounds__(288, 1) void c4_pool_prefill_staged_kernel(const Po
 // ring slot; at a group boundary the window's first 7 entries come from the
 // ring (none of them is the slot being written) and entry 7 is the new token.
 // The new token's chunk and the ape chunks do not depend on the plan record,
-// so they are requested together with it: a boundary row costs two memory
-// round trips (record + token + ape, then the ring rows), any other row one.
+// so they are requested together with it, and so is the window that the
+// rid / seq_lens hints name when given: a boundary row then costs one memory
+// round trip when the record agrees with the hints (two otherwise), any
+// other row one.
 constexpr int kC4DecodeThreads = 128;  // 128-thread blocks: a batch of 256 rows x 64 chunks covers every SM
 
 template <typename TIn, typename TOut>
 __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolArgs a, uint32_t chunks,
                                                                      uint32_t units) {
   constexpr int VEC = C4Vec<TIn>::VEC;
-  pdl_wait();
-  pdl_release();
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
-  if (u >= units) return;
   const int hd = a.head_dim;
   const size_t width = 4 * static_cast<size_t>(hd);
   TIn* state = static_cast<TIn*>(a.state_mut);
@@ -354,6 +357,41 @@ __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolA
   const uint32_t b = u / chunks;
   const uint32_t ch = u % chunks;
   const int c0 = static_cast<int>(ch) * VEC;
+  bool h_ok = false;  // the hints name a boundary row whose legacy ring is inside the state
+  int64_t h_sl = 0, h_rid = 0;
+  if (u < units) {
+    // While the previous kernel finishes: this thread's plan record, its
+    // chunks of the new token and, from the rid / seq_lens hints (legacy ring
+    // rows rid * 8 + position % 8), the ring chunks its window reads, into
+    // L2.  Nothing read before the dependency wait is used after it except
+    // through the check below, so a stale hint only costs bandwidth.
+    const TIn* src = input + static_cast<size_t>(b) * width + c0;
+    if (ch % 8 == 0) prefetch_l2(a.plan_d + b);
+    prefetch_l2(src);
+    prefetch_l2(src + hd);
+    prefetch_l2(src + 2 * hd);
+    prefetch_l2(src + 3 * hd);
+    if (a.seq_hint != nullptr) {
+      int64_t sl, rid;
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(sl) : "l"(a.seq_hint + b));
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(rid) : "l"(a.rid_hint + b));
+      if (sl >= 4 && sl % 4 == 0 && rid >= 0 && static_cast<uint64_t>(rid) * 8 + 7 < a.state_rows) {
+        h_ok = true;
+        h_sl = sl;
+        h_rid = rid;
+        const int64_t p = sl - 1;
+        for (int i = sl == 4 ? 4 : 0; i < 7; ++i) {
+          const int64_t q = p - 7 + i;  // the position of window entry i
+          const TIn* row = state + static_cast<size_t>(rid * 8 + q % 8) * width;
+          prefetch_l2(row + (i < 4 ? 0 : hd) + c0);
+          prefetch_l2(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
+        }
+      }
+    }
+  }
+  pdl_wait();
+  pdl_release();
+  if (u >= units) return;
   TOut* orow = out + static_cast<size_t>(b) * hd + c0;
 
   const ckv_decode_plan_t P = load_plan_d(a.plan_d + b);
@@ -363,6 +401,20 @@ __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolA
   uint4 ap[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) ap[i] = ld_cached16(ape + static_cast<size_t>(i) * hd + c0);
+  // The window as the hints name it, requested together with the record (one
+  // round trip instead of two); used below only if the record names the same
+  // rows, whose slots no row of this step writes.
+  const int h_first = h_sl == 4 ? 4 : 0;
+  uint4 kv[8], sc[8];
+#pragma unroll
+  for (int i = 0; i < 7; ++i) {
+    kv[i] = sc[i] = make_uint4(0, 0, 0, 0);
+    if (h_ok && i >= h_first) {
+      const TIn* row = state + static_cast<size_t>(h_rid * 8 + (h_sl - 8 + i) % 8) * width;
+      kv[i] = ld_stream16(row + (i < 4 ? 0 : hd) + c0);
+      sc[i] = ld_stream16(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
+    }
+  }
   if (P.seq_len == kInvalidU32) {
     store_zero_chunk<TOut, VEC>(orow);
     return;
@@ -388,16 +440,21 @@ __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolA
     return;
   }
   const int first = P.seq_len == 4 ? 4 : 0;
-  uint4 kv[8], sc[8];
+  bool same = h_ok && h_sl == static_cast<int64_t>(P.seq_len);
 #pragma unroll
-  for (int i = 0; i < 7; ++i) {
-    if (i < first) {
-      kv[i] = sc[i] = make_uint4(0, 0, 0, 0);
-      continue;
+  for (int i = 0; i < 7; ++i)
+    if (i >= first) same = same && (i < 4 ? rp0 : rp1) * 4 + (i & 3) == h_rid * 8 + (h_sl - 8 + i) % 8;
+  if (!same) {  // the rows the record names
+#pragma unroll
+    for (int i = 0; i < 7; ++i) {
+      if (i < first) {
+        kv[i] = sc[i] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const TIn* row = state + static_cast<size_t>((i < 4 ? rp0 : rp1) * 4 + (i & 3)) * width;
+      kv[i] = ld_stream16(row + (i < 4 ? 0 : hd) + c0);
+      sc[i] = ld_stream16(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
     }
-    const TIn* row = state + static_cast<size_t>((i < 4 ? rp0 : rp1) * 4 + (i & 3)) * width;
-    kv[i] = ld_stream16(row + (i < 4 ? 0 : hd) + c0);
-    sc[i] = ld_stream16(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
   }
   kv[7] = kv_main;
   sc[7] = sc_main;

@@ -305,7 +305,9 @@ int ckv_compress_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, v
  * give it) into L2 while that kernel finishes; nothing is computed from them.
  * If the previous kernel is still writing them, a stale value only costs
  * the bandwidth of a useless prefetch; pages outside the state are skipped.
- * The C4 decode does not read them. */
+ * The C4 decode likewise prefetches the ring rows its windows read, assuming
+ * the legacy ring (rows rid * 8 .. rid * 8 + 7; with SWA-paged plans the
+ * prefetch misses and only costs bandwidth). */
 int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, void* state, uint64_t state_rows,
                         const void* kv_score_input, const void* ape, const ckv_decode_plan_t* plan_d,
                         const ckv_decode_order_t* order, const int64_t* rid_hint, const int64_t* seq_lens_hint,
