@@ -363,6 +363,40 @@ def test_decode_prefetch_hints_only_steer_prefetches(env, ratio):
     assert (outs["none"][1].view(np.uint8) == st.view(np.uint8)).all()
 
 
+@pytest.mark.parametrize("B", [3000, 28000])
+def test_c128_decode_large_batch_through_the_list(env, B):
+    """Large batches through the boundary-row list and the prefetch hints: at
+    28000 rows each persistent CTA owns ~370 list entries (more than its 352
+    threads, so its prologue takes two passes) and ~185 rows without a window;
+    every output row and state byte is compared with the oracle."""
+    o, ckv, dev = env
+    hd = 128
+    rng = np.random.default_rng(B)
+    sl = rng.integers(1, 4000, B)
+    sl[rng.permutation(B)[: B // 4]] = 128 * rng.integers(1, 30, B // 4)
+    w = wl.random_decode(128, hd, torch.bfloat16, torch.float32, sl, seed=B, num_requests_state=B + 3)
+    state_d = w.state.to(dev)
+    status = ckv.new_status(dev)
+    out, pd = ckv.decode_step(128, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), w.rid.to(dev),
+                              w.seq_lens.to(dev), torch.float32, status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    st0 = wl.bits(w.state).copy()
+    st = st0.copy()
+    wpd = o.plan_decode(128, w.rid, w.seq_lens)
+    assert (pd.cpu().numpy() == wpd).all()
+    want = o.compress_decode(128, hd, 1, 0, st, wl.bits(w.kv_score), wl.bits(w.ape), wpd)
+    got = H.np_bits(out)
+    f = H.plan_d_fields(wpd)
+    bnd = np.nonzero(f["seq_len"] % 128 == 0)[0]
+    kvmax = H.window_kv_absmax(128, hd, st0, wl.bits(w.kv_score), f["seq_len"][bnd], bnd, np.full(len(bnd), 127),
+                               f["read_page_0"][bnd], f["read_page_1"][bnd])
+    H.assert_pool_close(got[bnd], want[bnd], 0, kvmax, "large-batch decode boundary rows")
+    nb = np.setdiff1d(np.arange(B), bnd)
+    assert (got[nb].view(np.uint32) == 0).all()
+    assert (H.np_bits(state_d).view(np.uint8) == st.view(np.uint8)).all()
+
+
 def test_bad_order_entries_are_flagged_not_faulted(env):
     """A boundary-row list that does not match the plan (a row past the batch, a
     page outside the state, a count larger than the batch) is bounds-checked by
