@@ -1005,6 +1005,17 @@ def bench_step(args, ws, rank, local):
     e1.record(main)
     torch.cuda.synchronize()
     e2e_s = e0.elapsed_time(e1) / 1e3
+    # the host link's own rate on this machine: the step's input alone, one plain copy, three times
+    link = []
+    for _ in range(3):
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(up)
+        with torch.cuda.stream(up):
+            pre.kv.copy_(h_kv5, non_blocking=True)
+        l1.record(up)
+        torch.cuda.synchronize()
+        link.append(h_kv5.numel() * elem(w5.in_dtype) / (l0.elapsed_time(l1) * 1e-3) / 1e9)
+    link_gbs = float(np.median(link))
     del pre2, dec2, step2
     torch.cuda.nvtx.range_pop()
     e2e_s = max_over_ranks(e2e_s, ws)
@@ -1040,7 +1051,10 @@ def bench_step(args, ws, rank, local):
         "kernels_c4": None,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "steps": e2e_steps, "pipelined": "two sets of device buffers: the upload of step k+1 overlaps "
-                                              "step k, outputs read back on a third stream"},
+                                              "step k, outputs read back on a third stream",
+                "host_link_h2d_gbs": link_gbs,
+                "link_bound_ms_per_step": h2d / (link_gbs * 1e9) * 1e3,
+                "ms_per_step": e2e_s / e2e_steps * 1e3},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
