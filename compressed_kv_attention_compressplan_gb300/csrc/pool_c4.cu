@@ -30,6 +30,58 @@ struct C4Vec {
   static constexpr int VEC = 16 / static_cast<int>(sizeof(TIn));  // channels per 16-byte chunk
 };
 
+// The decode's unit: four channels of one row (8 bytes of bf16, 16 of fp32).
+// A decode batch is small, so its rows spread over few threads per SM, and
+// one unit's reduction is a chain of dependent instructions per channel: four
+// channels per thread halve that chain for bf16 and double the warps that
+// hide its latency.
+template <typename TIn>
+struct C4DecVec;
+template <>
+struct C4DecVec<float> {
+  using V = uint4;
+};
+template <>
+struct C4DecVec<__nv_bfloat16> {
+  using V = uint2;
+};
+constexpr int kC4DecVec = 4;
+
+__device__ __forceinline__ uint2 ld_stream8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+template <typename V>
+__device__ __forceinline__ V ld_stream_v(const void* p);
+template <>
+__device__ __forceinline__ uint4 ld_stream_v<uint4>(const void* p) { return ld_stream16(p); }
+template <>
+__device__ __forceinline__ uint2 ld_stream_v<uint2>(const void* p) { return ld_stream8(p); }
+
+template <typename V>
+__device__ __forceinline__ V ld_cached_v(const void* p) { return __ldg(reinterpret_cast<const V*>(p)); }
+
+template <typename V>
+__device__ __forceinline__ void st_v(void* p, const V& v) { *reinterpret_cast<V*>(p) = v; }
+
+template <typename V>
+__device__ __forceinline__ V zero_v();
+template <>
+__device__ __forceinline__ uint4 zero_v<uint4>() { return make_uint4(0, 0, 0, 0); }
+template <>
+__device__ __forceinline__ uint2 zero_v<uint2>() { return make_uint2(0, 0); }
+
+// Element j of a vector of TIn as fp32.
+template <typename TIn>
+__device__ __forceinline__ float unpack_v(const uint4& v, int j) { return unpack<TIn>(v, j); }
+template <typename TIn>
+__device__ __forceinline__ float unpack_v(const uint2& v, int j) {
+  const uint32_t w = sizeof(TIn) == 2 ? ((j >> 1) == 0 ? v.x : v.y) : (j == 0 ? v.x : v.y);
+  return sizeof(TIn) == 2 ? ((j & 1) ? bf16hi(w) : bf16lo(w)) : __uint_as_float(w);
+}
+
 // One 4-D tensor-map box (channel 0, block q0, both parts, rows from `row`)
 // -> shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_box4_g2s(uint32_t dst, const CUtensorMap* map, int q0, int row, uint32_t bar) {
@@ -51,16 +103,16 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
 // The C4 window pool for VEC channels.  Entries below `first` are masked.
 // (Scalar form: with 16 kv/score vectors live, the packed fp32x2 form of the
 // same operations needs more registers than this kernel can spare.)
-template <typename TIn, int VEC>
-__device__ __forceinline__ void c4_pool_chunk(const uint4 (&kv)[8], const uint4 (&sc)[8], const uint4 (&ap)[8],
-                                              int first, float (&res)[VEC]) {
+template <typename TIn, int VEC, typename V>
+__device__ __forceinline__ void c4_pool_chunk(const V (&kv)[8], const V (&sc)[8], const V (&ap)[8], int first,
+                                              float (&res)[VEC]) {
 #pragma unroll
   for (int j = 0; j < VEC; ++j) {
     float s[8];
     float m = -INFINITY;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      s[i] = score_plus_bias(unpack<TIn>(sc[i], j), unpack<TIn>(ap[i], j));
+      s[i] = score_plus_bias(unpack_v<TIn>(sc[i], j), unpack_v<TIn>(ap[i], j));
       if (i >= first) m = fmaxf(m, s[i]);
     }
     const float nml = neg_max_log2e(m);
@@ -68,7 +120,7 @@ __device__ __forceinline__ void c4_pool_chunk(const uint4 (&kv)[8], const uint4 
     acc.init();
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      if (i >= first) acc.add(unpack<TIn>(kv[i], j), weight_of(s[i], nml));
+      if (i >= first) acc.add(unpack_v<TIn>(kv[i], j), weight_of(s[i], nml));
     }
     res[j] = finish(acc.a, acc.l);
   }
@@ -333,20 +385,22 @@ __global__ __launch_bounds__(288, 1) void c4_pool_prefill_staged_kernel(const Po
   }
 }
 
-// Decode: one unit per (row, chunk).  The new token's row is written to its
-// ring slot; at a group boundary the window's first 7 entries come from the
-// ring (none of them is the slot being written) and entry 7 is the new token.
-// The new token's chunk and the ape chunks do not depend on the plan record,
-// so they are requested together with it, and so is the window that the
-// rid / seq_lens hints name when given: a boundary row then costs one memory
-// round trip when the record agrees with the hints (two otherwise), any
-// other row one.
-constexpr int kC4DecodeThreads = 128;  // 128-thread blocks: a batch of 256 rows x 64 chunks covers every SM
+// Decode: one unit per (row, 4 channels).  The new token's row is written to
+// its ring slot; at a group boundary the window's first 7 entries come from
+// the ring (none of them is the slot being written) and entry 7 is the new
+// token.  The new token's unit and the ape units do not depend on the plan
+// record, so they are requested together with it, and so is the window that
+// the rid / seq_lens hints name when given: a boundary row then costs one
+// memory round trip when the record agrees with the hints (two otherwise),
+// any other row one.
+constexpr int kC4DecodeThreads = 128;
 
 template <typename TIn, typename TOut>
 __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolArgs a, uint32_t chunks,
                                                                      uint32_t units) {
-  constexpr int VEC = C4Vec<TIn>::VEC;
+  using V = typename C4DecVec<TIn>::V;
+  constexpr int VEC = kC4DecVec;
+  constexpr int kLineUnits = 128 / static_cast<int>(sizeof(V));  // units per 128-byte line
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
   const int hd = a.head_dim;
   const size_t width = 4 * static_cast<size_t>(hd);
@@ -360,17 +414,20 @@ __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolA
   bool h_ok = false;  // the hints name a boundary row whose legacy ring is inside the state
   int64_t h_sl = 0, h_rid = 0;
   if (u < units) {
-    // While the previous kernel finishes: this thread's plan record, its
-    // chunks of the new token and, from the rid / seq_lens hints (legacy ring
-    // rows rid * 8 + position % 8), the ring chunks its window reads, into
-    // L2.  Nothing read before the dependency wait is used after it except
-    // through the check below, so a stale hint only costs bandwidth.
+    // While the previous kernel finishes: this row's plan record, its new
+    // token and, from the rid / seq_lens hints (legacy ring rows rid * 8 +
+    // position % 8), the ring lines its window reads, into L2 (one thread per
+    // 128-byte line).  Nothing read before the dependency wait is used after
+    // it except through the check below, so a stale hint only costs bandwidth.
+    const bool line = ch % kLineUnits == 0;
     const TIn* src = input + static_cast<size_t>(b) * width + c0;
-    if (ch % 8 == 0) prefetch_l2(a.plan_d + b);
-    prefetch_l2(src);
-    prefetch_l2(src + hd);
-    prefetch_l2(src + 2 * hd);
-    prefetch_l2(src + 3 * hd);
+    if (ch == 0) prefetch_l2(a.plan_d + b);
+    if (line) {
+      prefetch_l2(src);
+      prefetch_l2(src + hd);
+      prefetch_l2(src + 2 * hd);
+      prefetch_l2(src + 3 * hd);
+    }
     if (a.seq_hint != nullptr) {
       int64_t sl, rid;
       asm volatile("ld.global.u64 %0, [%1];" : "=l"(sl) : "l"(a.seq_hint + b));
@@ -379,12 +436,14 @@ __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolA
         h_ok = true;
         h_sl = sl;
         h_rid = rid;
-        const int64_t p = sl - 1;
-        for (int i = sl == 4 ? 4 : 0; i < 7; ++i) {
-          const int64_t q = p - 7 + i;  // the position of window entry i
-          const TIn* row = state + static_cast<size_t>(rid * 8 + q % 8) * width;
-          prefetch_l2(row + (i < 4 ? 0 : hd) + c0);
-          prefetch_l2(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
+        if (line) {
+          const int64_t p = sl - 1;
+          for (int i = sl == 4 ? 4 : 0; i < 7; ++i) {
+            const int64_t q = p - 7 + i;  // the position of window entry i
+            const TIn* row = state + static_cast<size_t>(rid * 8 + q % 8) * width;
+            prefetch_l2(row + (i < 4 ? 0 : hd) + c0);
+            prefetch_l2(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
+          }
         }
       }
     }
@@ -396,23 +455,23 @@ __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolA
 
   const ckv_decode_plan_t P = load_plan_d(a.plan_d + b);
   const TIn* src = input + static_cast<size_t>(b) * width + c0;  // row b of the input always exists
-  const uint4 kv_ovl = ld_stream16(src), kv_main = ld_stream16(src + hd);
-  const uint4 sc_ovl = ld_stream16(src + 2 * hd), sc_main = ld_stream16(src + 3 * hd);
-  uint4 ap[8];
+  const V kv_ovl = ld_stream_v<V>(src), kv_main = ld_stream_v<V>(src + hd);
+  const V sc_ovl = ld_stream_v<V>(src + 2 * hd), sc_main = ld_stream_v<V>(src + 3 * hd);
+  V ap[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) ap[i] = ld_cached16(ape + static_cast<size_t>(i) * hd + c0);
+  for (int i = 0; i < 8; ++i) ap[i] = ld_cached_v<V>(ape + static_cast<size_t>(i) * hd + c0);
   // The window as the hints name it, requested together with the record (one
   // round trip instead of two); used below only if the record names the same
   // rows, whose slots no row of this step writes.
   const int h_first = h_sl == 4 ? 4 : 0;
-  uint4 kv[8], sc[8];
+  V kv[8], sc[8];
 #pragma unroll
   for (int i = 0; i < 7; ++i) {
-    kv[i] = sc[i] = make_uint4(0, 0, 0, 0);
+    kv[i] = sc[i] = zero_v<V>();
     if (h_ok && i >= h_first) {
       const TIn* row = state + static_cast<size_t>(h_rid * 8 + (h_sl - 8 + i) % 8) * width;
-      kv[i] = ld_stream16(row + (i < 4 ? 0 : hd) + c0);
-      sc[i] = ld_stream16(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
+      kv[i] = ld_stream_v<V>(row + (i < 4 ? 0 : hd) + c0);
+      sc[i] = ld_stream_v<V>(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
     }
   }
   if (P.seq_len == kInvalidU32) {
@@ -431,10 +490,10 @@ __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolA
     return;
   }
   TIn* dst = state + static_cast<size_t>(P.write_loc) * width + c0;
-  st16(dst, kv_ovl);
-  st16(dst + hd, kv_main);
-  st16(dst + 2 * hd, sc_ovl);
-  st16(dst + 3 * hd, sc_main);
+  st_v<V>(dst, kv_ovl);
+  st_v<V>(dst + hd, kv_main);
+  st_v<V>(dst + 2 * hd, sc_ovl);
+  st_v<V>(dst + 3 * hd, sc_main);
   if (!boundary) {
     store_zero_chunk<TOut, VEC>(orow);
     return;
@@ -448,12 +507,12 @@ __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolA
 #pragma unroll
     for (int i = 0; i < 7; ++i) {
       if (i < first) {
-        kv[i] = sc[i] = make_uint4(0, 0, 0, 0);
+        kv[i] = sc[i] = zero_v<V>();
         continue;
       }
       const TIn* row = state + static_cast<size_t>((i < 4 ? rp0 : rp1) * 4 + (i & 3)) * width;
-      kv[i] = ld_stream16(row + (i < 4 ? 0 : hd) + c0);
-      sc[i] = ld_stream16(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
+      kv[i] = ld_stream_v<V>(row + (i < 4 ? 0 : hd) + c0);
+      sc[i] = ld_stream_v<V>(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
     }
   }
   kv[7] = kv_main;
@@ -515,8 +574,7 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
 
 template <typename TIn, typename TOut>
 int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
-  constexpr int VEC = C4Vec<TIn>::VEC;
-  const uint32_t chunks = static_cast<uint32_t>(a.head_dim / VEC);
+  const uint32_t chunks = static_cast<uint32_t>(a.head_dim / kC4DecVec);
   const uint64_t units64 = static_cast<uint64_t>(a.capacity) * chunks;
   if (units64 == 0) return CKV_OK;
   if (units64 > 0xFFFFFFFFull) return CKV_ERR_SIZE;
