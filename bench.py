@@ -19,7 +19,10 @@ is flushed by writing a buffer of twice its size.  Each step's four segments
 graph with event-record nodes between them; per-kernel times are those GPU
 timestamps.  ``e2e`` repeats the step through the same
 API with the step's inputs copied from pinned host memory and its outputs
-copied back inside the timed region.
+copied back inside the timed region.  Beside the step, the same line carries
+the C4 kernels on their own workloads (``kernels_c4``) and the
+speculative-decoding verify steps (``kernels_mtp``), each kernel's cost inside
+its step by difference and back to back.
 
 ``--config NAME`` times one workload alone (c4_prefill_small, c4_decode,
 c128_decode, c4_prefill, c128_prefill, the speculative-decoding verify shapes
@@ -803,6 +806,36 @@ def c4_kernels(args, ckv, dev, seed: int, peak: float) -> dict:
     return out
 
 
+def mtp_kernels(args, ckv, dev, seed: int, peak: float) -> dict:
+    """The speculative-decoding verify steps (1024 requests x extend 4, fixed-shape plan buffers padded with
+    the invalid record), reported beside the headline step: per-kernel costs inside each step by difference
+    and the planner, the pool and the write back to back (the write also against its same-bytes floor)."""
+    out = {}
+    for name in ("c128_prefill_mtp", "c4_prefill_mtp"):
+        w = wl.NAMED[name](seed)
+        r = PrefillRunner(ckv, w, dev, padded=True)
+        flush = l2_flush_buffer(dev)
+        b = algorithmic_bytes(w)
+        segs = [("plan_prefill", r.plan), ("pool_prefill", r.pool), ("write", r.write)]
+        ins = instep_by_difference(segs, flush, r.restore, max(200, 10 * args.steps))
+        if int(r.status[0]):
+            raise RuntimeError(f"device status set: {name} {int(r.status[0])}")
+        d = {"workload": f"{name}: 1024 requests x extend 4, prefix U[0,65536], hd 512, padded plans",
+             "bytes": {"pool": b["pool"], "write": b["write"], "plan": b["plan"]}, "num_c": b["num_c"],
+             "instep": ins}
+        if not args.no_back_to_back:
+            d["plan_back_to_back_us"] = steady_state_us(r.plan_fns(16))
+            d["pool_back_to_back_us"] = steady_state_us(r.steady_fns(copies_for(b["pool"], dev), "pool"))
+            us = steady_state_us(r.steady_fns(copies_for(b["write"], dev), "write"))
+            floor = same_bytes_floor(b["write"], dev, peak)
+            d.update({"write_back_to_back_us": us, "write_back_to_back_frac": b["write"] / (us * 1e-6) / 1e9 / peak,
+                      "write_vs_floor": min(floor["copy_us"], floor["elementwise_us"]) / us})
+        out[name] = d
+        del r
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------------- CPU baseline (oracle)
 def oracle_step(o, w5, w3, frac5=1.0):
     """The oracle over (a sample of) the step: C128 prefill pool + write, then
@@ -1049,6 +1082,7 @@ def bench_step(args, ws, rank, local):
             "sum_of_kernel_segments_us": float(seg_ms.sum(1).mean()) * 1e3,
             "step_gbs": step_bytes / (float(step_ms.mean()) * 1e-3) / 1e9},
         "kernels_c4": None,
+        "kernels_mtp": None,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "steps": e2e_steps, "pipelined": "two sets of device buffers: the upload of step k+1 overlaps "
                                               "step k, outputs read back on a third stream",
@@ -1061,6 +1095,9 @@ def bench_step(args, ws, rank, local):
     if not args.no_c4:
         with nvtx_range("C4 kernels"):
             line["kernels_c4"] = c4_kernels(args, ckv, dev, seed, peak)
+    if not args.no_mtp:
+        with nvtx_range("speculative-decoding verify steps"):
+            line["kernels_mtp"] = mtp_kernels(args, ckv, dev, seed, peak)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle as o
 
@@ -1143,14 +1180,17 @@ def bench_config(args, name, ws, rank, local):
     steady = {}
     if w.mode == "prefill" and main_ms < 0.05 and not args.no_back_to_back:
         # a short main kernel (the speculative-decoding verify steps): event nodes around ~10 us of work add
-        # the graph's node-to-node latency, so it is also timed back to back
+        # the graph's node-to-node latency, so it is also timed back to back (back_to_back_* = the main
+        # kernel, the one with more bytes; the other of pool and write under its own key)
         n = copies_for(b[main_key], dev)
         us = steady_state_us(r.steady_fns(n, main_key))
         sg = b[main_key] / (us * 1e-6) / 1e9
         floor = same_bytes_floor(b[main_key], dev, peak)
-        steady = {"back_to_back_us": us, "back_to_back_gbs": sg, "back_to_back_frac": sg / peak,
-                  "back_to_back_copies": n, "same_bytes_floor": floor,
+        steady = {"back_to_back_kernel": main_key, "back_to_back_us": us, "back_to_back_gbs": sg,
+                  "back_to_back_frac": sg / peak, "back_to_back_copies": n, "same_bytes_floor": floor,
                   "vs_floor": min(floor["copy_us"], floor["elementwise_us"]) / us}
+        other = "write" if main_key == "pool" else "pool"
+        steady[f"{other}_back_to_back_us"] = steady_state_us(r.steady_fns(copies_for(b[other], dev), other))
     if w.mode == "prefill" and maps is None and not args.no_back_to_back:
         # the planner alone, back to back over copies of its inputs and outputs
         steady["plan_back_to_back_us"] = steady_state_us(r.plan_fns(16))
@@ -1287,6 +1327,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true", help="with --config: scaled-down workloads for profiling")
     ap.add_argument("--no-c4", action="store_true", help="skip the C4 kernels block of the step line")
+    ap.add_argument("--no-mtp", action="store_true",
+                    help="skip the speculative-decoding verify steps block of the step line")
     ap.add_argument("--no-instep", action="store_true",
                     help="skip the in-step costs by difference (200 rounds of every step variant), e.g. under ncu")
     ap.add_argument("--no-back-to-back", action="store_true",

@@ -325,9 +325,8 @@ __device__ __forceinline__ void issue_decode_tile(TIn* kv_s, uint32_t bar, const
 
 // Decodes and bounds-checks prefill record e.  Invalid (padding) records and
 // records that point outside the state / input return false.
-__device__ __forceinline__ bool prefill_record(const PoolArgs& a, uint32_t e, uint32_t& ragged, int& bl,
-                                               int64_t& rp0, bool& bad) {
-  const ckv_compress_plan_t P = load_plan_c(a.plan_c + e);
+__device__ __forceinline__ bool prefill_record_of(const PoolArgs& a, const ckv_compress_plan_t& P, uint32_t& ragged,
+                                                  int& bl, int64_t& rp0, bool& bad) {
   bad = false;
   if (plan_c_invalid(P)) return false;
   ragged = P.ragged_bl & CKV_RAGGED_MASK;
@@ -337,6 +336,22 @@ __device__ __forceinline__ bool prefill_record(const PoolArgs& a, uint32_t e, ui
   if (bl > 0) ok = ok && rp0 >= 0 && static_cast<uint64_t>(rp0) * 128 + 127 < a.state_rows;
   bad = !ok;
   return ok;
+}
+
+__device__ __forceinline__ bool prefill_record(const PoolArgs& a, uint32_t e, uint32_t& ragged, int& bl,
+                                               int64_t& rp0, bool& bad) {
+  return prefill_record_of(a, load_plan_c(a.plan_c + e), ragged, bl, rp0, bad);
+}
+
+// Record e of the plan buffer, or the invalid record past its capacity.  A
+// record inside the buffer may be read before the count is known.
+__device__ __forceinline__ ckv_compress_plan_t plan_c_at(const PoolArgs& a, uint32_t e) {
+  if (e < a.capacity) return load_plan_c(a.plan_c + e);
+  ckv_compress_plan_t P;
+  P.seq_len = kInvalidU32;
+  P.ragged_bl = kInvalidU32;
+  P.read_page_0 = P.read_page_1 = -1;
+  return P;
 }
 
 // ---------------------------------------------------------------- persistent kernel
@@ -599,6 +614,9 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
   pdl_wait();  // everything below may read what the previous kernel wrote
   pdl_release();
   if (ordered && t < NC) load_ape_regs_now<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);
+  // prefill: the producer requests its first record together with the count
+  // instead of after it (one dependent round trip less before the first tile)
+  ckv_compress_plan_t rec_next = plan_c_at(a, !kDecode && t == NC ? first : kInvalidU32);
   const uint32_t num_c = kDecode ? 0u : count_or_capacity(a.d_counts, 0, a.capacity);
   uint32_t items, ntriv = 0;
   __shared__ uint32_t s_count;
@@ -749,12 +767,14 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
           mbar_arrive_expect_tx(bar, 0u);
         }
       } else {
-        const uint32_t e = first + n * stride;
+        // each record is requested one tile ahead
+        const ckv_compress_plan_t P = rec_next;
+        if (n + 1 < items) rec_next = plan_c_at(a, first + (n + 1) * stride);
         uint32_t ragged = 0;
         int bl = 0;
         int64_t rp0 = 0;
         bool bad;
-        const bool ok = prefill_record(a, e, ragged, bl, rp0, bad);
+        const bool ok = prefill_record_of(a, P, ragged, bl, rp0, bad);
         if (bad) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
         mbar_arrive_expect_tx(bar, ok ? T::TILE_BYTES : 0u);
         if (ok) {
@@ -785,10 +805,7 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
     if (group_any(grp, NCG, abort_flag != 0)) break;
     const int stage = static_cast<int>(n % NS);
     const uint32_t phase = (n / NS) & 1u;
-    if (!wait_for<kShortWaits>(smem_addr(&full_bar[stage]), phase, a.wait_ns)) {
-      status_or(a.d_status, CKV_STATUS_TIMEOUT);
-      abort_flag = 1;
-    }
+    // (prefill: the tile's record is requested before the wait for the tile)
     bool ok = true;
     uint32_t e = 0, ragged = 0;
     size_t orow;
@@ -802,6 +819,10 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
       bool bad;
       ok = prefill_record(a, e, ragged, bl, rp0, bad);
       orow = token ? ragged : e;
+    }
+    if (!wait_for<kShortWaits>(smem_addr(&full_bar[stage]), phase, a.wait_ns)) {
+      status_or(a.d_status, CKV_STATUS_TIMEOUT);
+      abort_flag = 1;
     }
     float* red_l = red_base + (2 * grp + (local & 1u)) * T::RED_FLOATS;
     float* red_a = red_l + 8 * CS;
