@@ -273,6 +273,8 @@ class PrefillRunner:
         self.layout = ckv.OUT_TOKEN if w.out_layout == wl.TOKEN else ckv.OUT_COMPACT
         rows = nq if self.layout == ckv.OUT_TOKEN else self.cap_c
         self.out = torch.empty(max(rows, 1), w.head_dim, dtype=w.out_dtype, device=dev)
+        # the planner's inputs, handed to the pool as prefetch hints (legacy state rows)
+        self.hints = (self.rid, self.sl, self.el)
 
     def plan(self):
         c = self.ckv
@@ -282,7 +284,7 @@ class PrefillRunner:
     def pool(self):
         self.ckv.compress_pool_prefill(self.w.ratio, self.w.head_dim, self.state, self.kv, self.ape,
                                        self.plan_c[: self.cap_c], self.counts, self.layout, self.w.out_dtype,
-                                       self.out, self.status)
+                                       self.out, self.status, hints=self.hints)
 
     def write(self):
         self.ckv.compress_write(self.w.ratio, self.w.head_dim, self.state, self.kv, self.plan_w[: self.cap_w],
@@ -319,7 +321,7 @@ class PrefillRunner:
             if which == "pool":
                 def fn(st=st, kv=kv, pc=pc, cnt=cnt, out=out):
                     c.compress_pool_prefill(w.ratio, w.head_dim, st, kv, self.ape, pc, cnt, self.layout, w.out_dtype,
-                                            out, self.status)
+                                            out, self.status, hints=self.hints)
             else:
                 def fn(st=st, kv=kv, pw=pw, cnt=cnt):
                     c.compress_write(w.ratio, w.head_dim, st, kv, pw, cnt, self.status)
@@ -337,6 +339,7 @@ class PagedPrefillRunner(PrefillRunner):
         self.f2s = maps.full_to_state.to(dev)
         self.cap_w = ckv.capacity_write_paged(w.ratio, w.batch, w.num_q_tokens, maps.swa_page_size)
         self.plan_w = torch.empty(max(self.cap_w, 1), 8, dtype=torch.uint8, device=dev)
+        self.hints = None  # the hints name legacy rows
 
     def plan(self):
         m = self.maps

@@ -73,9 +73,9 @@ def load_library():
         lib.ckv_plan_prefill.argtypes = [i32, vp, vp, vp, u32, u32, u32, u32, i32, vp, vp, vp, vp, vp]
         lib.ckv_compress_write.argtypes = [i32, i32, i32, vp, u64, vp, u32, vp, vp, u32, vp, vp]
         lib.ckv_compress_pool_prefill.argtypes = [i32, i32, i32, i32, vp, u64, vp, u32, vp, vp, vp, u32, i32, vp,
-                                                  vp, vp]
+                                                  ctypes.POINTER(PrefillHints), vp, vp]
         lib.ckv_compress_prefill.argtypes = [i32, i32, i32, i32, vp, u64, vp, u32, vp, vp, vp, vp, u32, u32, i32,
-                                             vp, vp, vp]
+                                             vp, ctypes.POINTER(PrefillHints), vp, vp]
         lib.ckv_compress_decode.argtypes = [i32, i32, i32, i32, vp, u64, vp, vp, vp, vp, vp, vp, u32, vp, vp, vp]
         f32 = ctypes.c_float
         lib.ckv_capacity_online_units.argtypes = [u32, u32]
@@ -296,11 +296,27 @@ def compress_write(ratio: int, head_dim: int, state: torch.Tensor, kv_score: tor
                                              _ptr(status), _stream(stream)), "ckv_compress_write")
 
 
+class PrefillHints(ctypes.Structure):
+    """ckv_prefill_hints_t: the planner's rid / seq_lens / extend_lens (device pointers) and batch."""
+    _fields_ = [("rid", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p), ("extend_lens", ctypes.c_void_p),
+                ("batch", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+
+def _hints(hints):
+    """``None`` or ``(rid, seq_lens, extend_lens)`` device tensors -> a ctypes pointer (or None)."""
+    if hints is None:
+        return None
+    rid, sl, el = hints
+    batch = _lengths(rid, sl, el)
+    return ctypes.pointer(PrefillHints(_ptr(rid), _ptr(sl), _ptr(el), batch, 0))
+
+
 def compress_pool_prefill(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
                           plan_c: torch.Tensor, counts: Optional[torch.Tensor] = None,
                           out_layout: int = OUT_TOKEN, out_dtype: torch.dtype = torch.float32,
                           out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                          stream=None) -> torch.Tensor:
+                          stream=None, hints=None) -> torch.Tensor:
+    """``hints``: ``None`` or the ``(rid, seq_lens, extend_lens)`` the planner read (prefetch only)."""
     nq = kv_score.shape[0]
     rows = nq if out_layout == OUT_TOKEN else plan_c.shape[0]
     if out is None:
@@ -308,7 +324,8 @@ def compress_pool_prefill(ratio: int, head_dim: int, state: torch.Tensor, kv_sco
     _check(load_library().ckv_compress_pool_prefill(ratio, head_dim, dtype_code(kv_score.dtype), dtype_code(out.dtype),
                                                     _ptr(state), _state_rows(state, ratio, head_dim), _ptr(kv_score),
                                                     nq, _ptr(ape), _ptr(plan_c), _ptr(counts), plan_c.shape[0],
-                                                    out_layout, _ptr(out), _ptr(status), _stream(stream)),
+                                                    out_layout, _ptr(out), _hints(hints), _ptr(status),
+                                                    _stream(stream)),
            "ckv_compress_pool_prefill")
     return out[:rows]
 
@@ -317,8 +334,8 @@ def compress_prefill(ratio: int, head_dim: int, state: torch.Tensor, kv_score: t
                      plan_c: torch.Tensor, plan_w: torch.Tensor, counts: Optional[torch.Tensor] = None,
                      out_layout: int = OUT_TOKEN, out_dtype: torch.dtype = torch.float32,
                      out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                     stream=None) -> torch.Tensor:
-    """Pool, then write the state (one stream, in that order)."""
+                     stream=None, hints=None) -> torch.Tensor:
+    """Pool, then write the state (one stream, in that order).  ``hints`` as compress_pool_prefill."""
     nq = kv_score.shape[0]
     rows = nq if out_layout == OUT_TOKEN else plan_c.shape[0]
     if out is None:
@@ -326,7 +343,7 @@ def compress_prefill(ratio: int, head_dim: int, state: torch.Tensor, kv_score: t
     _check(load_library().ckv_compress_prefill(ratio, head_dim, dtype_code(kv_score.dtype), dtype_code(out.dtype),
                                                _ptr(state), _state_rows(state, ratio, head_dim), _ptr(kv_score), nq,
                                                _ptr(ape), _ptr(plan_c), _ptr(plan_w), _ptr(counts), plan_c.shape[0],
-                                               plan_w.shape[0], out_layout, _ptr(out), _ptr(status),
+                                               plan_w.shape[0], out_layout, _ptr(out), _hints(hints), _ptr(status),
                                                _stream(stream)), "ckv_compress_prefill")
     return out[:rows]
 
@@ -471,7 +488,7 @@ def prefill_step(ratio: int, head_dim: int, state: torch.Tensor, kv_score: torch
     plan_c, plan_w, counts = plan_prefill(ratio, rid, seq_lens, extend_lens, kv_score.shape[0], status=status,
                                           stream=stream)
     out = compress_prefill(ratio, head_dim, state, kv_score, ape, plan_c, plan_w, counts, out_layout, out_dtype,
-                           status=status, stream=stream)
+                           status=status, stream=stream, hints=(rid, seq_lens, extend_lens))
     return out, plan_c, plan_w, counts
 
 

@@ -40,8 +40,8 @@ uint64_t ckv_set_wait_limit_ns(uint64_t limit_ns) {
 int ckv_compress_pool_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, const void* state,
                               uint64_t state_rows, const void* kv_score_input, uint32_t num_q_tokens,
                               const void* ape, const ckv_compress_plan_t* plan_c, const uint32_t* d_counts,
-                              uint32_t capacity_c, int out_layout, void* out, uint32_t* d_status,
-                              ckv_stream_t stream) {
+                              uint32_t capacity_c, int out_layout, void* out, const ckv_prefill_hints_t* hints,
+                              uint32_t* d_status, ckv_stream_t stream) {
   int rc = check_pool_args(ratio, head_dim, in_dtype, out_dtype);
   if (rc) return rc;
   if (out_layout != CKV_OUT_TOKEN && out_layout != CKV_OUT_COMPACT) return CKV_ERR_DTYPE;
@@ -52,6 +52,11 @@ int ckv_compress_pool_prefill(int ratio, int head_dim, int in_dtype, int out_dty
   if (capacity_c > 0 && (!aligned16(plan_c) || !aligned16(kv_score_input) || !aligned16(state)))
     return CKV_ERR_POINTER;
   if (d_counts && (reinterpret_cast<uintptr_t>(d_counts) & 3u)) return CKV_ERR_POINTER;
+  if (hints != nullptr && hints->batch > 0 &&
+      (hints->rid == nullptr || hints->seq_lens == nullptr || hints->extend_lens == nullptr ||
+       ((reinterpret_cast<uintptr_t>(hints->rid) | reinterpret_cast<uintptr_t>(hints->seq_lens) |
+         reinterpret_cast<uintptr_t>(hints->extend_lens)) & 7u)))
+    return CKV_ERR_POINTER;
   PoolArgs a{};
   a.ratio = ratio;
   a.head_dim = head_dim;
@@ -69,6 +74,14 @@ int ckv_compress_pool_prefill(int ratio, int head_dim, int in_dtype, int out_dty
   a.out = out;
   a.d_status = d_status;
   a.wait_ns = wait_limit_ns();
+  if (hints != nullptr && hints->batch > 0 && capacity_c > 0 &&
+      static_cast<uint64_t>(num_q_tokens) * (ratio == 4 ? 4u : 2u) * head_dim * (in_dtype == CKV_BF16 ? 2u : 4u) <=
+          CKV_PREFILL_HINT_MAX_INPUT_BYTES) {
+    a.rid_hint = hints->rid;
+    a.seq_hint = hints->seq_lens;
+    a.ext_hint = hints->extend_lens;
+    a.hint_batch = hints->batch;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return ratio == 4 ? launch_c4_pool_prefill(a, s) : launch_c128_pool_prefill(a, s);
 }
@@ -77,7 +90,7 @@ int ckv_compress_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, v
                          const void* kv_score_input, uint32_t num_q_tokens, const void* ape,
                          const ckv_compress_plan_t* plan_c, const ckv_write_plan_t* plan_w,
                          const uint32_t* d_counts, uint32_t capacity_c, uint32_t capacity_w, int out_layout,
-                         void* out, uint32_t* d_status, ckv_stream_t stream) {
+                         void* out, const ckv_prefill_hints_t* hints, uint32_t* d_status, ckv_stream_t stream) {
   // validate both halves before launching either
   int rc = check_pool_args(ratio, head_dim, in_dtype, out_dtype);
   if (rc) return rc;
@@ -85,7 +98,8 @@ int ckv_compress_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, v
                          (reinterpret_cast<uintptr_t>(plan_w) & 7u)))
     return CKV_ERR_POINTER;
   rc = ckv_compress_pool_prefill(ratio, head_dim, in_dtype, out_dtype, state, state_rows, kv_score_input,
-                                 num_q_tokens, ape, plan_c, d_counts, capacity_c, out_layout, out, d_status, stream);
+                                 num_q_tokens, ape, plan_c, d_counts, capacity_c, out_layout, out, hints, d_status,
+                                 stream);
   if (rc) return rc;
   return ckv_compress_write(ratio, head_dim, in_dtype, state, state_rows, kv_score_input, num_q_tokens, plan_w,
                             d_counts, capacity_w, d_status, stream);

@@ -119,6 +119,12 @@ __device__ __forceinline__ bool warp_wait_for(uint32_t bar, uint32_t parity, uin
   return __all_sync(0xFFFFFFFFu, wait_for<kShortWaits>(bar, parity, limit_ns));
 }
 
+// An L2 prefetch of `bytes` (a multiple of 16) from the 16-byte aligned
+// global address p.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // One bulk global -> shared copy that completes `bytes` of the barrier's
 // transaction count.  dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

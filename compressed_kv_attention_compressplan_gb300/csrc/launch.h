@@ -25,8 +25,10 @@ struct PoolArgs {
   const ckv_compress_plan_t* plan_c;  // prefill
   const ckv_decode_plan_t* plan_d;    // decode
   const ckv_decode_order_t* order;    // decode: boundary rows in row order (NULL: the kernel scans plan_d)
-  const int64_t* rid_hint;            // decode: the planner's rid / seq_lens, read before the dependency
-  const int64_t* seq_hint;            //   wait to prefetch windows into L2 (NULL: no prefetch)
+  const int64_t* rid_hint;            // the planner's rid / seq_lens (/ extend_lens: prefill), read before
+  const int64_t* seq_hint;            //   the dependency wait to prefetch windows into L2 (NULL: no
+  const int64_t* ext_hint;            //   prefetch)
+  uint32_t hint_batch;                // prefill: entries of the hint arrays
   const uint32_t* d_counts;           // prefill
   uint32_t capacity;                  // prefill: capacity_c; decode: batch
   int out_layout;

@@ -611,6 +611,28 @@ __global__ __launch_bounds__(PersistCfg<TIn, CS, NS, NG, kDecode>::THREADS, 1) v
       }
     }
   }
+  if (!kDecode && a.ext_hint != nullptr) {
+    // Prefill (small steps only, see the host): the windows that start in the
+    // state -- a request's first window when its prefix ends inside a page --
+    // into L2 while the planner runs: page rows rid*128 .. rid*128 + pl%128 - 1,
+    // contiguous, for every channel slice.  One thread per request; the hints
+    // are the planner's own inputs, read before the dependency wait, so they
+    // only steer prefetches.
+    for (uint32_t b = blockIdx.x + static_cast<uint32_t>(t) * gridDim.x; b < a.hint_batch;
+         b += static_cast<uint32_t>(NT) * gridDim.x) {
+      int64_t sl, el, rid;
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(sl) : "l"(a.seq_hint + b));
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(el) : "l"(a.ext_hint + b));
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(rid) : "l"(a.rid_hint + b));
+      const int64_t pl = sl - el;
+      if (el > 0 && pl > 0 && sl / 128 > pl / 128 && pl % 128 != 0 && rid >= 0 &&
+          rid < (int64_t{1} << 48) && static_cast<uint64_t>(rid) * 128 + 127 < a.state_rows) {
+        const uint8_t* p = reinterpret_cast<const uint8_t*>(state + static_cast<size_t>(rid) * 128 * width);
+        const uint32_t bytes = static_cast<uint32_t>(pl % 128) * static_cast<uint32_t>(width * sizeof(TIn));
+        for (uint32_t o = 0; o < bytes; o += 32768u) bulk_prefetch_l2(p + o, bytes - o < 32768u ? bytes - o : 32768u);
+      }
+    }
+  }
   pdl_wait();  // everything below may read what the previous kernel wrote
   pdl_release();
   if (ordered && t < NC) load_ape_regs_now<TIn>(static_cast<const TIn*>(a.ape), hd, c0, g, cq, ape_r);

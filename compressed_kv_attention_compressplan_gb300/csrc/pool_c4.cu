@@ -263,6 +263,39 @@ __global__ __launch_bounds__(288, 1) void c4_pool_prefill_staged_kernel(const Po
     fence_mbar_init();
   }
   __syncthreads();
+  if (a.ext_hint != nullptr) {
+    // Small steps only (see the host): while the planner runs, into L2 the
+    // state halves that each request's first window reads (legacy ring rows
+    // rid * 8 + position % 8; entries 0..3 take the overlap halves, 4..7 the
+    // main ones), one thread per request.  Line prefetches, not bulk ones: the
+    // copy engine takes bulk prefetches in order with the stage copies, and a
+    // thousand 1 KB ones ahead of them held the first stage back by ~8 us.
+    // (Prefetching the input too only moved time from the pool to the write.)
+    // The hints are the planner's own inputs, read before the dependency wait:
+    // they only steer prefetches.
+    const uint32_t half = static_cast<uint32_t>(hd) * sizeof(TIn);
+    const uint32_t row_bytes = 4u * half;
+    const uint8_t* st = static_cast<const uint8_t*>(a.state);
+    for (uint32_t b = blockIdx.x + static_cast<uint32_t>(t) * gridDim.x; b < a.hint_batch;
+         b += blockDim.x * gridDim.x) {
+      int64_t sl, el, rid;
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(sl) : "l"(a.seq_hint + b));
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(el) : "l"(a.ext_hint + b));
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(rid) : "l"(a.rid_hint + b));
+      const int64_t pl = sl - el;
+      if (el > 0 && pl > 0 && sl / 4 > pl / 4 && rid >= 0 && rid < (int64_t{1} << 48) &&
+          static_cast<uint64_t>(rid) * 8 + 7 < a.state_rows) {
+        const int64_t p = pl / 4 * 4 + 3;  // the request's first event
+        for (int i = p == 3 ? 4 : 0; i < 8 && p - 7 + i < pl; ++i) {
+          const uint8_t* row = st + static_cast<size_t>(rid * 8 + (p - 7 + i) % 8) * row_bytes;
+          for (uint32_t o = 0; o < half; o += 128) {
+            prefetch_l2(row + (i < 4 ? 0 : half) + o);
+            prefetch_l2(row + (i < 4 ? 2 : 3) * half + o);
+          }
+        }
+      }
+    }
+  }
   pdl_wait();
   pdl_release();
   const bool token = a.out_layout == CKV_OUT_TOKEN;

@@ -148,6 +148,28 @@ typedef struct ckv_decode_order {
   int32_t page;
 } ckv_decode_order_t;
 
+/* Prefetch hints for the prefill pool (32 bytes, host memory): the device
+ * arrays [batch] that ckv_plan_prefill read for this step (int64, 8-byte
+ * aligned; all three or none).  The pages define no such thing: the pool
+ * reads them BEFORE waiting for the previous kernel on the stream (normally
+ * the planner), only to prefetch into L2 the state rows of the windows they
+ * imply while that kernel runs (legacy rows: ring rid * 8 + position % 8 for
+ * C4, page rid * 128 + position % 128 for C128).  Nothing is computed from
+ * them: a stale or wrong value costs the bandwidth of a useless prefetch,
+ * rows outside the state are skipped, and with SWA-paged plans the prefetch
+ * simply misses.  The pool uses them only for small steps (input of at most
+ * CKV_PREFILL_HINT_MAX_INPUT_BYTES), where the windows' first loads, not the
+ * stream of windows, set the time. */
+typedef struct ckv_prefill_hints {
+  const int64_t* rid;
+  const int64_t* seq_lens;
+  const int64_t* extend_lens;
+  uint32_t batch;
+  uint32_t reserved; /* 0 */
+} ckv_prefill_hints_t;
+
+#define CKV_PREFILL_HINT_MAX_INPUT_BYTES (64ull << 20)
+
 #define CKV_RAGGED_MASK 0x00FFFFFFu
 #define CKV_BUFFER_LEN_SHIFT 24
 
@@ -270,12 +292,14 @@ int ckv_compress_write(int ratio, int head_dim, int dtype, void* state, uint64_t
  *                    compressed row, every other row is written with +0.0.
  *   CKV_OUT_COMPACT: out is [capacity_c, head_dim]; row k holds record k
  *                    (rows of invalid / missing records are left untouched).
- * ape is [W, head_dim] in the input dtype (W = 8 or 128).  Only reads the state. */
+ * ape is [W, head_dim] in the input dtype (W = 8 or 128).  Only reads the state.
+ * hints: NULL, or ckv_prefill_hints_t (see there); CKV_ERR_POINTER when its
+ * arrays are not all given or not 8-byte aligned. */
 int ckv_compress_pool_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, const void* state,
                               uint64_t state_rows, const void* kv_score_input, uint32_t num_q_tokens,
                               const void* ape, const ckv_compress_plan_t* plan_c, const uint32_t* d_counts,
-                              uint32_t capacity_c, int out_layout, void* out, uint32_t* d_status,
-                              ckv_stream_t stream);
+                              uint32_t capacity_c, int out_layout, void* out, const ckv_prefill_hints_t* hints,
+                              uint32_t* d_status, ckv_stream_t stream);
 
 /* Prefill step: ckv_compress_pool_prefill followed by ckv_compress_write on
  * the same stream (the order of c4.cuh FlashCompress4Kernel::run_prefill). */
@@ -283,7 +307,7 @@ int ckv_compress_prefill(int ratio, int head_dim, int in_dtype, int out_dtype, v
                          const void* kv_score_input, uint32_t num_q_tokens, const void* ape,
                          const ckv_compress_plan_t* plan_c, const ckv_write_plan_t* plan_w,
                          const uint32_t* d_counts, uint32_t capacity_c, uint32_t capacity_w, int out_layout,
-                         void* out, uint32_t* d_status, ckv_stream_t stream);
+                         void* out, const ckv_prefill_hints_t* hints, uint32_t* d_status, ckv_stream_t stream);
 
 /* Decode (c4.cuh flash_c4_decode; compressor_v2.py _c128_compress_decode_kernel):
  * for each row b, write input row b to state row plan_d[b].write_loc; when

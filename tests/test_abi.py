@@ -39,6 +39,11 @@ def test_record_sizes_match_header():
         body = re.search(r"typedef struct %s \{(.*?)\}" % struct, text, flags=re.S).group(1)
         fields = re.findall(r"(u?int32_t)\s+\w+;", body)
         assert 4 * len(fields) == size, struct
+    # the prefill hints: three pointers and two 32-bit words
+    body = re.search(r"typedef struct ckv_prefill_hints \{(.*?)\}", text, flags=re.S).group(1)
+    assert len(re.findall(r"const int64_t\*\s+\w+;", body)) == 3
+    assert len(re.findall(r"uint32_t\s+\w+;", body)) == 2
+    assert ctypes.sizeof(ckv.PrefillHints) == 32
 
 
 def test_capacity_bounds(lib):
@@ -68,8 +73,15 @@ def test_argument_errors_are_returned_before_any_launch(lib):
     # the boundary-row list and the prefetch hints must be 8-byte aligned
     assert dec(128, 512, 1, 0, vp(16), 8, vp(16), vp(16), vp(16), vp(12), None, None, 1, vp(16), None, None) == -4
     assert dec(128, 512, 1, 0, vp(16), 8, vp(16), vp(16), vp(16), None, vp(20), vp(16), 1, vp(16), None, None) == -4
-    assert lib.ckv_compress_pool_prefill(128, 512, 1, 0, None, 0, None, 10, None, None, None, 1, 9, None, None,
-                                         None) == -5
+    pool = lib.ckv_compress_pool_prefill
+    assert pool(128, 512, 1, 0, None, 0, None, 10, None, None, None, 1, 9, None, None, None, None) == -5
+    # prefetch hints: all three arrays or none, 8-byte aligned (checked before anything is launched)
+    H = ckv.PrefillHints
+    for h in (H(None, 8, 8, 4, 0), H(8, 8, None, 4, 0), H(8, 12, 8, 4, 0)):
+        assert pool(128, 512, 1, 0, vp(16), 128, vp(16), 10, vp(16), vp(16), None, 1, 1, vp(16), ctypes.pointer(h),
+                    None, None) == -4
+    assert lib.ckv_compress_prefill(4, 512, 1, 0, vp(16), 8, vp(16), 10, vp(16), vp(16), vp(16), None, 1, 1, 1,
+                                    vp(16), ctypes.pointer(H(8, 8, 12, 4, 0)), None, None) == -4
     assert lib.ckv_compress_write(4, 2048, 1, None, 0, None, 0, None, None, 1, None, None) == -2
     f = ctypes.c_float
     nrd = lib.ckv_norm_rope_store_decode
@@ -109,7 +121,7 @@ def test_binding_rejects_wrong_per_request_arrays():
 
 
 def test_wait_limit_setter(lib):
-    assert lib.ckv_version() >= 200  # ABI 2.00: decode boundary-row lists, clamped wait limit
+    assert lib.ckv_version() >= 210  # ABI 2.10: prefill prefetch hints (2.00: decode boundary-row lists)
     default = 2_000_000_000
     prev = ckv.set_wait_limit_ns(0)            # whatever was set, back to the default
     assert ckv.set_wait_limit_ns(1234) == default

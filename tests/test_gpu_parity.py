@@ -363,6 +363,52 @@ def test_decode_prefetch_hints_only_steer_prefetches(env, ratio):
     assert (outs["none"][1].view(np.uint8) == st.view(np.uint8)).all()
 
 
+@pytest.mark.parametrize("ratio", [4, 128])
+def test_prefill_prefetch_hints_only_steer_prefetches(env, ratio):
+    """The prefill pool reads the planner's rid / seq_lens / extend_lens before
+    its dependency wait, only to prefetch windows: hints that name other
+    requests, rows past the state, negative ids or lengths, or extends longer
+    than the sequence leave every output byte as without hints (and within the
+    bar of the oracle's)."""
+    o, ckv, dev = env
+    B = 300
+    w = (wl.c4_prefill_mtp if ratio == 4 else wl.c128_prefill_mtp)(ratio + 11, batch=B)
+    hd, nq = w.head_dim, w.num_q_tokens
+    ci, co = (1 if w.in_dtype == torch.bfloat16 else 0), (1 if w.out_dtype == torch.bfloat16 else 0)
+    layout = ckv.OUT_TOKEN if w.out_layout == wl.TOKEN else ckv.OUT_COMPACT
+    pc, pw, counts = ckv.plan_prefill(ratio, w.rid.to(dev), w.seq_lens.to(dev), w.extend_lens.to(dev), nq)
+    rng = np.random.default_rng(ratio)
+    i64 = lambda a: torch.as_tensor(np.asarray(a), dtype=torch.int64)
+    cases = [("none", None),
+             ("right", (w.rid, w.seq_lens, w.extend_lens)),
+             ("stale", (i64(rng.permutation(B)), i64(rng.integers(1, 70000, B)), i64(rng.integers(1, 300, B)))),
+             ("outside", (i64(np.full(B, 10 ** 12)), w.seq_lens, w.extend_lens)),
+             ("negative", (i64(np.full(B, -3)), i64(np.full(B, -130)), i64(np.full(B, -4)))),
+             ("long_extend", (w.rid, w.seq_lens, w.seq_lens + 5))]
+    outs = {}
+    for name, hints in cases:
+        status = ckv.new_status(dev)
+        hk = None if hints is None else tuple(t.to(dev) for t in hints)
+        out = ckv.compress_pool_prefill(ratio, hd, w.state.to(dev), w.kv_score.to(dev), w.ape.to(dev), pc, counts,
+                                        layout, w.out_dtype, status=status, hints=hk)
+        torch.cuda.synchronize()
+        assert int(status[0]) == 0, name
+        outs[name] = H.np_bits(out).copy()
+    wc, _, (nc, _), _ = o.plan_prefill(ratio, w.rid, w.seq_lens, w.extend_lens)
+    written = slice(None) if layout == ckv.OUT_TOKEN else slice(0, nc)  # compact rows past the count stay as they were
+    for name, _ in cases[1:]:
+        assert (outs[name][written].view(np.uint8) == outs["none"][written].view(np.uint8)).all(), name
+    st = wl.bits(w.state)
+    inp = wl.bits(w.kv_score)
+    want = o.compress_pool_prefill(ratio, hd, ci, co, st.copy(), inp, wl.bits(w.ape), np.ascontiguousarray(wc), nc,
+                                   nq, o.OUT_COMPACT)
+    f = H.plan_c_fields(wc)
+    kvmax = H.window_kv_absmax(ratio, hd, st, inp, f["seq_len"], f["ragged_id"], f["buffer_len"], f["read_page_0"],
+                               f["read_page_1"])
+    rows = f["ragged_id"] if layout == ckv.OUT_TOKEN else np.arange(nc)
+    H.assert_pool_close(outs["none"][rows], want, co, kvmax, "prefill pool with hints")
+
+
 @pytest.mark.parametrize("B", [3000, 28000])
 def test_c128_decode_large_batch_through_the_list(env, B):
     """Large batches through the boundary-row list and the prefetch hints: at
