@@ -40,7 +40,10 @@ def _compositions(rng, total, parts, count):
 
 
 @pytest.mark.parametrize("ratio", [4, 128])
-def test_prefill_step_replayed_from_a_graph(env, ratio):
+@pytest.mark.parametrize("hinted", [False, True])
+def test_prefill_step_replayed_from_a_graph(env, ratio, hinted):
+    """With ``hinted`` the pool also takes the planner's inputs as prefetch
+    hints (their contents change between replays, as the lengths do)."""
     o, ckv, dev = env
     hd, in_dt, out_dt = 256, 1, 0
     layout = wl.TOKEN if ratio == 4 else wl.COMPACT
@@ -66,7 +69,8 @@ def test_prefill_step_replayed_from_a_graph(env, ratio):
     def step():
         ckv.plan_prefill(ratio, rid, sl, el, nq, cap_c, cap_w, pad_invalid=True, plan_c=plan_c, plan_w=plan_w,
                          counts=counts, status=status)
-        ckv.compress_pool_prefill(ratio, hd, state, kv, ape, plan_c, counts, lay, out=out, status=status)
+        ckv.compress_pool_prefill(ratio, hd, state, kv, ape, plan_c, counts, lay, out=out, status=status,
+                                  hints=(rid, sl, el) if hinted else None)
         ckv.compress_write(ratio, hd, state, kv, plan_w, counts, status=status)
 
     step()  # eager once: first-call set-up (kernel attributes) happens outside the capture

@@ -185,10 +185,12 @@ def _run_prefill_parity(env, ratio, hd, in_dt, out_dt, layout, pl, el, seed, sta
     nq = w.num_q_tokens
     state_d = w.state.to(dev)
     status = ckv.new_status(dev)
-    pc, pw, counts = ckv.plan_prefill(ratio, w.rid.to(dev), w.seq_lens.to(dev), w.extend_lens.to(dev), nq,
-                                      status=status)
+    lens = (w.rid.to(dev), w.seq_lens.to(dev), w.extend_lens.to(dev))
+    pc, pw, counts = ckv.plan_prefill(ratio, *lens, nq, status=status)
+    # about half of the cases also hand the pool the planner's inputs as prefetch hints
+    hinted = zlib.crc32(f"{ratio},{hd},{in_dt},{out_dt},{layout},{seed}".encode()) & 1
     out = ckv.compress_prefill(ratio, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), pc, pw, counts, layout,
-                               H.torch_dtype(out_dt), status=status)
+                               H.torch_dtype(out_dt), status=status, hints=lens if hinted else None)
     torch.cuda.synchronize()
     assert int(status[0]) == 0
     st = wl.bits(w.state).copy()
