@@ -12,8 +12,8 @@
 // Prefill: a producer warp stages each record's window in shared memory with
 // two tensor-map copies (see c4_pool_prefill_staged_kernel); consumer threads
 // own 16-byte channel chunks (8 bf16 or 4 fp32 channels).  Decode: one thread
-// per (row, chunk) with direct loads.  The window is small enough that the
-// fp32 safe softmax runs entirely in registers.
+// per (row, 4 channels) with direct loads.  The window is small enough that
+// the fp32 safe softmax runs entirely in registers.
 #include <algorithm>
 #include <atomic>
 #include <cstring>
