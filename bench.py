@@ -1068,7 +1068,7 @@ def bench_step(args, ws, rank, local):
                    "l2": "flushed before every step (2x L2 written, then 2x L2 read), prefill state restored "
                          "outside the timing",
                    "algorithmic_bytes_per_step": step_bytes},
-        "roofline": {"bound": "hbm", "kernel": "c128_pool_kernel (prefill)", "achieved": pool_gbs, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": "c128_persistent_kernel (prefill pool)", "achieved": pool_gbs, "peak": peak,
                      "unit": "GB/s", "frac": pool_gbs / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "traffic": profiled_traffic(b5["num_c"]), "traffic_source": "profiles/c128_prefill_pool__c128_prefill_small.md "
                      "(ncu dram bytes per compress record x records)", "algorithmic_bytes": b5["pool"],
