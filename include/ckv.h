@@ -438,7 +438,8 @@ int ckv_norm_rope_store_decode(int ratio, int head_dim, int rope_dim, int in_dty
 /* ------------------------------------------------------------------ misc */
 /* Short text for a CKV_OK / CKV_ERR_* code (static storage). */
 const char* ckv_error_string(int code);
-/* Library ABI version: major * 100 + minor. */
+/* Library ABI version: major * 100 + minor (210: 2.00's decode boundary-row
+ * list and prefetch hints, plus the prefill prefetch hints). */
 int ckv_version(void);
 
 #ifdef __cplusplus
