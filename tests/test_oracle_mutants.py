@@ -6,8 +6,10 @@ term, a sign error, an input row off by one; in the SWA-paged planner: no
 page-end writes, the ring offset taken modulo the page size, records without
 state reads translated; in norm + RoPE: a rotation sign, the position, the
 rotated channels; in the online state: no reset at a group start, the sum not
-rescaled, an ape row off by one) is compiled on its own and must fail at least
-one pin.  The mistakes are textual patches of the source (the first n
+rescaled, an ape row off by one; and bf16 rounding by truncation, a decode
+page of the previous group, a write set a group too long, a decode that pools
+before it writes the new token, RMSNorm's eps outside the root, RoPE's cos and
+sin swapped) is compiled on its own and must fail at least one pin.  The mistakes are textual patches of the source (the first n
 occurrences of a fragment replaced), so the oracle itself carries no hooks."""
 import pytest
 
@@ -100,11 +102,46 @@ MUTANTS = {
         ('const float bias = load_elem(ape, (size_t)(p % 128) * hd + c, in_dtype);',
          'const float bias = load_elem(ape, (size_t)((p + 1) % 128) * hd + c, in_dtype);', 1),
     ]),
+    21: ('bf16 rounding by truncation', [
+        ('double r = ldexp(nearbyint(ldexp(a, -qexp)), qexp);', 'double r = ldexp(floor(ldexp(a, -qexp)), qexp);', 1),
+    ]),
+    22: ('decode read_page_1 of the previous group', [
+        ('plan[b].read_page_1 = (int32_t)legacy_page(ratio, rid[b], p1);',
+         'plan[b].read_page_1 = (int32_t)legacy_page(ratio, rid[b], p0);', 1),
+    ]),
+    23: ('prefill write set a group too long', [
+        ('const int64_t first_w = (sl / ratio) * ratio - overlap;',
+         'const int64_t first_w = (sl / ratio - 1) * ratio - overlap;', 1),
+    ]),
+    24: ('decode pools before writing the new token', [
+        ('    memcpy((char*)state + (size_t)P->write_loc * row_bytes, row_ptr(input, b, width, in_dtype), row_bytes);\n'
+         '    if (P->seq_len % (uint32_t)ratio != 0) continue;',
+         '    if (P->seq_len % (uint32_t)ratio != 0) {\n'
+         '      memcpy((char*)state + (size_t)P->write_loc * row_bytes, row_ptr(input, b, width, in_dtype), row_bytes);\n'
+         '      continue;\n'
+         '    }', 1),
+        ('    pool_window(ratio, hd, in_dtype, out_dtype, (const void* const*)entries, ape,\n'
+         '                (char*)out + (size_t)b * (size_t)hd * elem_size(out_dtype));\n  }\n  free(entries);\n  return ORC_OK;',
+         '    pool_window(ratio, hd, in_dtype, out_dtype, (const void* const*)entries, ape,\n'
+         '                (char*)out + (size_t)b * (size_t)hd * elem_size(out_dtype));\n'
+         '    memcpy((char*)state + (size_t)P->write_loc * row_bytes, row_ptr(input, b, width, in_dtype), row_bytes);\n'
+         '  }\n  free(entries);\n  return ORC_OK;', 1),
+    ]),
+    25: ('RMSNorm eps outside the root', [
+        ('const double r = 1.0 / sqrt(ss / hd + (double)eps);', 'const double r = 1.0 / (sqrt(ss / hd) + (double)eps);', 1),
+    ]),
+    26: ('RoPE cos and sin swapped', [
+        ('const double cs = freqs[((size_t)pos * (rope_dim / 2) + i) * 2];',
+         'const double cs = freqs[((size_t)pos * (rope_dim / 2) + i) * 2 + 1];', 1),
+        ('const double sn = freqs[((size_t)pos * (rope_dim / 2) + i) * 2 + 1];',
+         'const double sn = freqs[((size_t)pos * (rope_dim / 2) + i) * 2];', 1),
+    ]),
 }
 
 
 def pins(o):
     yield lambda: P.test_plan_worked_examples(o)
+    yield lambda: P.test_bf16_round_once(o)
     for ratio in (4, 128):
         yield lambda ratio=ratio: P.test_plan_bruteforce(o, ratio, 1)
         yield lambda ratio=ratio: P.test_equal_scores_give_window_mean(o, ratio)
@@ -120,6 +157,7 @@ def pins(o):
     yield lambda: Q.test_page_end_positions_are_written_before_first_write(o)
     yield lambda: Q.test_paged_schedules_equal_history(o, 0)
     yield lambda: N.test_constant_row_normalises_to_the_weight(o)
+    yield lambda: N.test_eps_sits_inside_the_root(o)
     yield lambda: N.test_matches_float64_torch(o, 1)
     yield lambda: N.test_rotation_keeps_pair_lengths_and_relative_positions(o)
     yield lambda: N.test_position_is_seq_len_minus_ratio(o)

@@ -61,6 +61,21 @@ def test_constant_row_normalises_to_the_weight(oracle_mod):
     assert (cache[3] == w).all()
 
 
+def test_eps_sits_inside_the_root(oracle_mod):
+    """A constant row c with eps comparable to c^2: every channel becomes
+    c * w / sqrt(c^2 + eps) (the RMSNorm definition), which for c = 1e-3 and
+    eps = 1e-6 is w / sqrt(2), far from w / (1 + 1e-3) (eps outside the root)
+    and from w (eps dropped)."""
+    o = oracle_mod
+    rng = np.random.default_rng(3)
+    w = (1 + 0.1 * rng.standard_normal(HD)).astype(np.float32)
+    rows = np.full((1, HD), 1e-3, np.float32)
+    cache = run(o, rows, decode_plan([8]), w, 1e-6, identity_freqs(8, ROPE), [5])
+    c = np.float64(np.float32(1e-3))
+    want = c * w.astype(np.float64) / np.sqrt(c * c + np.float64(np.float32(1e-6)))
+    assert np.abs(cache[5].astype(np.float64) - want).max() <= 4 * np.finfo(np.float32).eps * np.abs(want).max()
+
+
 @pytest.mark.parametrize("mode", [0, 1])
 def test_matches_float64_torch(oracle_mod, mode):
     o = oracle_mod
