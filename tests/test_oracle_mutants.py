@@ -9,7 +9,8 @@ rotated channels; in the online state: no reset at a group start, the sum not
 rescaled, an ape row off by one; and bf16 rounding by truncation, a decode
 page of the previous group, a write set a group too long, a decode that pools
 before it writes the new token, RMSNorm's eps outside the root, RoPE's cos and
-sin swapped) is compiled on its own and must fail at least one pin.  The mistakes are textual patches of the source (the first n
+sin swapped, padding with zero bytes, token-layout rows in plan order) is
+compiled on its own and must fail at least one pin.  The mistakes are textual patches of the source (the first n
 occurrences of a fragment replaced), so the oracle itself carries no hooks."""
 import pytest
 
@@ -130,6 +131,13 @@ MUTANTS = {
     25: ('RMSNorm eps outside the root', [
         ('const double r = 1.0 / sqrt(ss / hd + (double)eps);', 'const double r = 1.0 / (sqrt(ss / hd) + (double)eps);', 1),
     ]),
+    27: ('padding with zero bytes instead of the invalid record', [
+        ('if (cap_c > nc) memset(pc + nc, 0xFF, sizeof(orc_plan_c) * (cap_c - nc));',
+         'if (cap_c > nc) memset(pc + nc, 0x00, sizeof(orc_plan_c) * (cap_c - nc));', 1),
+    ]),
+    28: ('token layout rows in plan order', [
+        ('size_t orow = out_layout == ORC_OUT_TOKEN ? (size_t)ragged : (size_t)e;', 'size_t orow = (size_t)e;', 1),
+    ]),
     26: ('RoPE cos and sin swapped', [
         ('const double cs = freqs[((size_t)pos * (rope_dim / 2) + i) * 2];',
          'const double cs = freqs[((size_t)pos * (rope_dim / 2) + i) * 2 + 1];', 1),
@@ -142,6 +150,8 @@ MUTANTS = {
 def pins(o):
     yield lambda: P.test_plan_worked_examples(o)
     yield lambda: P.test_bf16_round_once(o)
+    yield lambda: P.test_plan_padding_capacity_and_validation(o)
+    yield lambda: P.test_prefill_token_layout_zero_rows_and_compact_order(o)
     for ratio in (4, 128):
         yield lambda ratio=ratio: P.test_plan_bruteforce(o, ratio, 1)
         yield lambda ratio=ratio: P.test_equal_scores_give_window_mean(o, ratio)
