@@ -1,7 +1,8 @@
 """Parity at the seven named workloads' full sizes, in the launch configuration the
 benchmark times (capacities from ckv_capacity_*, or num_q_tokens-sized plan
 buffers padded with the invalid record for the speculative-decoding
-workloads; plan -> pool -> write on one stream; plan -> decode).
+workloads; plan -> pool (with the planner's inputs as prefetch hints) ->
+write on one stream; plan -> decode).
 
 Plans and state buffers are compared with the oracle byte for byte; decode
 outputs in full; prefill outputs of every compress record (the oracle pools
@@ -51,10 +52,11 @@ def test_prefill_workload_full_size(env, name):
     kv_d = w.kv_score.to(dev)
     status = ckv.new_status(dev)
     layout = ckv.OUT_TOKEN if w.out_layout == wl.TOKEN else ckv.OUT_COMPACT
-    pc, pw, counts = ckv.plan_prefill(R, w.rid.to(dev), w.seq_lens.to(dev), w.extend_lens.to(dev), nq, cap_c, cap_w,
-                                      pad_invalid=padded, status=status)
+    lens = (w.rid.to(dev), w.seq_lens.to(dev), w.extend_lens.to(dev))
+    pc, pw, counts = ckv.plan_prefill(R, *lens, nq, cap_c, cap_w, pad_invalid=padded, status=status)
+    # with the planner's inputs as prefetch hints, as the benchmark launches it
     out = ckv.compress_prefill(R, hd, state_d, kv_d, w.ape.to(dev), pc, pw, counts, layout, w.out_dtype,
-                               status=status)
+                               status=status, hints=lens)
     torch.cuda.synchronize()
     assert int(status[0]) == 0
     wc, ww, (nc, nw), _ = o.plan_prefill(R, w.rid, w.seq_lens, w.extend_lens)
