@@ -102,6 +102,13 @@ def _prefill_case(name, ratio, rng):
         B = 1024
         pl = rng.integers(0, 65536, B)
         el = np.where(rng.random(B) < 0.875, 4, rng.integers(128, 2000, B))
+    elif name == "max_tokens":  # the largest step the 24-bit ragged ids allow: 2^24 - 1 tokens, 1024 requests
+        B = 1024
+        pl = rng.integers(0, 65536, B)
+        total = (1 << 24) - 1
+        el = np.full(B, total // B)
+        el[: total - int(el.sum())] += 1
+        assert int(el.sum()) == total
     else:
         raise ValueError(name)
     rid = rng.permutation(max(B, 2048))[:B]
@@ -110,7 +117,7 @@ def _prefill_case(name, ratio, rng):
 
 @pytest.mark.parametrize("ratio", [4, 128])
 @pytest.mark.parametrize("case", ["random", "mtp_uniform", "decode_like", "uniform_32", "uniform_33", "one_long",
-                                  "max_batch_mixed"])
+                                  "max_batch_mixed", "max_tokens"])
 @pytest.mark.parametrize("pad", [False, True])
 def test_plan_prefill_bit_exact(env, ratio, case, pad):
     o, ckv, dev = env
