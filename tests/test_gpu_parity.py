@@ -330,6 +330,44 @@ def test_out_of_range_records_are_flagged_not_faulted(env):
 
 
 @pytest.mark.parametrize("ratio", [4, 128])
+@pytest.mark.parametrize("padded", [False, True])
+def test_prefill_step_without_compress_records(env, ratio, padded):
+    """A step in which no request reaches a multiple of the ratio: no compress
+    record (padded plans: all records invalid).  Token layout: every output row
+    is +0.0; compact layout: the output is left as it was; the state write
+    still happens, bit for bit."""
+    o, ckv, dev = env
+    hd = 256
+    pl = [1, 130, 260, 5] if ratio == 128 else [1, 5, 9, 13]
+    el = [2, 3, 1, 2] if ratio == 128 else [2, 2, 1, 2]
+    w = wl.random_prefill(ratio, hd, torch.bfloat16, torch.float32, wl.TOKEN, pl, el, seed=9 + ratio,
+                          num_requests_state=6)
+    nq = w.num_q_tokens
+    lens = (w.rid.to(dev), w.seq_lens.to(dev), w.extend_lens.to(dev))
+    cap_c = nq if padded else ckv.capacity_compress(ratio, 4, nq)
+    cap_w = nq if padded else ckv.capacity_write(ratio, 4, nq)
+    for layout in (ckv.OUT_TOKEN, ckv.OUT_COMPACT):
+        status = ckv.new_status(dev)
+        state_d = w.state.to(dev)
+        pc, pw, counts = ckv.plan_prefill(ratio, *lens, nq, cap_c, cap_w, pad_invalid=padded, status=status)
+        rows = nq if layout == ckv.OUT_TOKEN else cap_c
+        out = torch.full((rows, hd), float("nan"), dtype=torch.float32, device=dev)
+        ckv.compress_prefill(ratio, hd, state_d, w.kv_score.to(dev), w.ape.to(dev), pc, pw, counts, layout,
+                             torch.float32, out=out, status=status, hints=lens)
+        torch.cuda.synchronize()
+        assert int(status[0]) == 0 and int(counts[0]) == 0
+        if layout == ckv.OUT_TOKEN:
+            assert (H.np_bits(out).view(np.uint32) == 0).all()
+        else:
+            assert torch.isnan(out).all()
+        st = wl.bits(w.state).copy()
+        _, ww, (nc, nw), _ = o.plan_prefill(ratio, w.rid, w.seq_lens, w.extend_lens)
+        assert nc == 0
+        o.compress_write(ratio, hd, 1, st, wl.bits(w.kv_score), ww, nw)
+        assert (H.np_bits(state_d).view(np.uint8) == st.view(np.uint8)).all()
+
+
+@pytest.mark.parametrize("ratio", [4, 128])
 def test_decode_prefetch_hints_only_steer_prefetches(env, ratio):
     """The rid / seq_lens hints are read before the decode's dependency wait,
     so they may be stale: hints that name other rows, other pages, pages past
