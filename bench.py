@@ -28,7 +28,8 @@ its step by difference and back to back.
 c128_decode, c4_prefill, c128_prefill, the speculative-decoding verify shapes
 c4_prefill_mtp / c128_prefill_mtp, the C4 prefill over SWA-paged state
 c4_prefill_paged, the norm + RoPE + store step on the
-C128 rows, norm_rope_c128_prefill / norm_rope_c128_decode, and the C128
+C128 rows, norm_rope_c128_prefill / norm_rope_c128_decode, the C4 decode with
+its norm + RoPE + store in two launches and fused, c4_decode_norm_rope, and the C128
 workloads through the online state, c128_online_prefill / c128_online_decode;
 ``all`` for each in turn) and prints one line per workload.  ``--impl reference`` times the CPU oracle on the
 host cores over a bounded sample of the same step.
@@ -1142,6 +1143,8 @@ def bench_config(args, name, ws, rank, local):
         return bench_norm_rope(args, name, ws, rank, ckv, dev)
     if name in wl.ONLINE:
         return bench_online(args, name, ws, rank, ckv, dev)
+    if name in wl.DECODE_NORM:
+        return bench_decode_norm(args, name, ws, rank, ckv, dev)
     maps = None
     if name in wl.PAGED:
         w, maps = wl.PAGED[name](args.seed + rank)
@@ -1249,6 +1252,58 @@ def bench_norm_rope(args, name, ws, rank, ckv, dev):
         print(json.dumps(line), flush=True)
 
 
+def bench_decode_norm(args, name, ws, rank, ckv, dev):
+    """The C4 decode followed by norm + RoPE + store: two launches (the decode's fp32 rows, then the norm
+    step over them) against the one fused launch; the planner before both.  Costs inside each step by
+    difference, and each form back to back; prints one line."""
+    x = wl.DECODE_NORM[name](args.seed + rank)
+    w = x.w
+    d = DecodeRunner(ckv, w, dev)
+    weight, freqs, loc = x.weight.to(dev), x.freqs.to(dev), x.out_loc.to(dev)
+    cache = torch.zeros(x.cache_rows, w.head_dim, dtype=x.cache_dtype, device=dev)
+    flush = l2_flush_buffer(dev)
+
+    def norm():
+        ckv.norm_rope_store_decode(4, d.out[: w.batch], d.plan_d[: w.batch], weight, x.eps, freqs, loc, cache,
+                                   status=d.status)
+
+    def fused():
+        ckv.compress_decode_norm_rope_store(w.head_dim, d.state, d.kv, d.ape, d.plan_d[: w.batch], weight, x.eps,
+                                            freqs, loc, cache, status=d.status, **d.hints())
+
+    reps = max(200, 10 * args.steps)
+    two = instep_by_difference([("plan_decode", d.plan), ("decode", d.decode), ("norm_rope_store", norm)], flush,
+                               d.restore, reps)
+    one = instep_by_difference([("plan_decode", d.plan), ("decode_norm_rope_store", fused)], flush, d.restore, reps)
+    if int(d.status[0]):
+        raise RuntimeError(f"device status {int(d.status[0])}")
+    line = {"workload": name, "ratio": 4, "head_dim": w.head_dim, "batch": w.batch, "rope_dim": x.rope_dim,
+            "cache_dtype": str(x.cache_dtype).replace("torch.", ""), "two_launches_instep": two,
+            "fused_instep": one}
+    if not args.no_back_to_back:
+        d.plan()
+        torch.cuda.synchronize()
+        n = copies_for(algorithmic_bytes(w)["decode"], dev)
+        two_fns, one_fns = [], []
+        for i in range(n):
+            st = d.state if i == 0 else d.pristine.clone()
+            kv, pd, out, lc = d.kv.clone(), d.plan_d[: w.batch].clone(), d.out[: w.batch].clone(), loc.clone()
+
+            def f2(st=st, kv=kv, pd=pd, out=out, lc=lc):
+                ckv.compress_decode(4, w.head_dim, st, kv, d.ape, pd, w.out_dtype, out, d.status, **d.hints())
+                ckv.norm_rope_store_decode(4, out, pd, weight, x.eps, freqs, lc, cache, status=d.status)
+
+            def f1(st=st, kv=kv, pd=pd, lc=lc):
+                ckv.compress_decode_norm_rope_store(w.head_dim, st, kv, d.ape, pd, weight, x.eps, freqs, lc, cache,
+                                                    status=d.status, **d.hints())
+            two_fns.append(f2)
+            one_fns.append(f1)
+        line.update({"two_launches_back_to_back_us": steady_state_us(two_fns),
+                     "fused_back_to_back_us": steady_state_us(one_fns), "back_to_back_copies": n})
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def bench_online(args, name, ws, rank, ckv, dev):
     """A C128 step through the online state (plan + fold); prints one line."""
     if args.small and name == "c128_online_prefill":  # profiler captures: 16 long requests, still > L2
@@ -1347,7 +1402,8 @@ def main():
     elif args.config == "step":
         bench_step(args, ws, rank, local)
     else:
-        names = (list(wl.NAMED) + list(wl.PAGED) + list(wl.NORM_ROPE) + list(wl.ONLINE) if args.config == "all"
+        names = (list(wl.NAMED) + list(wl.PAGED) + list(wl.NORM_ROPE) + list(wl.DECODE_NORM) + list(wl.ONLINE)
+                 if args.config == "all"
                  else [args.config])
         for n in names:
             bench_config(args, n, ws, rank, local)

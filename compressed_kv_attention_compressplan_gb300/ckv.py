@@ -89,6 +89,8 @@ def load_library():
                                                     vp, u64, i32, vp, u64, vp, vp]
         lib.ckv_norm_rope_store_decode.argtypes = [i32, i32, i32, i32, vp, vp, u32, vp, f32, vp, u32, vp, i32, vp,
                                                    u64, vp, vp]
+        lib.ckv_compress_decode_norm_rope_store.argtypes = [i32, i32, i32, i32, vp, u64, vp, vp, vp, vp, vp, u32, vp,
+                                                            f32, vp, u32, vp, i32, vp, u64, vp, vp]
         lib.ckv_error_string.argtypes = [i32]
         lib.ckv_error_string.restype = ctypes.c_char_p
         lib.ckv_version.restype = i32
@@ -478,6 +480,29 @@ def norm_rope_store_decode(ratio: int, rows: torch.Tensor, plan_d: torch.Tensor,
                                                      freqs.shape[0], _ptr(out_loc), cc, _ptr(kv_cache),
                                                      kv_cache.shape[0], _ptr(status), _stream(stream)),
            "ckv_norm_rope_store_decode")
+
+
+def compress_decode_norm_rope_store(head_dim: int, state: torch.Tensor, kv_score: torch.Tensor, ape: torch.Tensor,
+                                    plan_d: torch.Tensor, norm_weight: torch.Tensor, eps: float, freqs: torch.Tensor,
+                                    out_loc: torch.Tensor, kv_cache: torch.Tensor,
+                                    status: Optional[torch.Tensor] = None, stream=None,
+                                    rid_hint: Optional[torch.Tensor] = None,
+                                    seq_lens_hint: Optional[torch.Tensor] = None) -> None:
+    """The C4 decode fused with norm + RoPE + store: the state write, and each row's pooled row (+0.0 off a
+    group boundary) normalised, rotated and stored into ``kv_cache`` at ``out_loc[b]``."""
+    if norm_weight.dtype != torch.float32 or freqs.dtype != torch.float32 or freqs.dim() != 3 or freqs.shape[2] != 2:
+        raise ValueError("norm_weight must be fp32 [head_dim] and freqs fp32 [max_pos, rope_dim/2, 2]")
+    if (rid_hint is None) != (seq_lens_hint is None):
+        raise ValueError("rid_hint and seq_lens_hint go together")
+    batch = plan_d.shape[0]
+    if out_loc.dtype != torch.int64 or out_loc.numel() < batch:
+        raise ValueError("out_loc must be int64 with one entry per batch row")
+    _lengths(rid_hint, seq_lens_hint)
+    _check(load_library().ckv_compress_decode_norm_rope_store(
+        4, head_dim, 2 * freqs.shape[1], dtype_code(kv_score.dtype), _ptr(state), _state_rows(state, 4, head_dim),
+        _ptr(kv_score), _ptr(ape), _ptr(plan_d), _ptr(rid_hint), _ptr(seq_lens_hint), batch, _ptr(norm_weight),
+        float(eps), _ptr(freqs), freqs.shape[0], _ptr(out_loc), dtype_code(kv_cache.dtype), _ptr(kv_cache),
+        kv_cache.shape[0], _ptr(status), _stream(stream)), "ckv_compress_decode_norm_rope_store")
 
 
 # ------------------------------------------------------------------------------ convenience

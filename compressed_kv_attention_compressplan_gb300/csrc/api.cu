@@ -141,4 +141,55 @@ int ckv_compress_decode(int ratio, int head_dim, int in_dtype, int out_dtype, vo
   return ratio == 4 ? launch_c4_decode(a, s) : launch_c128_decode(a, s);
 }
 
+int ckv_compress_decode_norm_rope_store(int ratio, int head_dim, int rope_dim, int in_dtype, void* state,
+                                        uint64_t state_rows, const void* kv_score_input, const void* ape,
+                                        const ckv_decode_plan_t* plan_d, const int64_t* rid_hint,
+                                        const int64_t* seq_lens_hint, uint32_t batch, const float* norm_weight,
+                                        float eps, const float* freqs, uint32_t max_pos, const int64_t* out_loc,
+                                        int cache_dtype, void* kv_cache, uint64_t cache_rows, uint32_t* d_status,
+                                        ckv_stream_t stream) {
+  if (ratio != 4) return CKV_ERR_RATIO;
+  int rc = check_pool_args(ratio, head_dim, in_dtype, CKV_F32);
+  if (rc) return rc;
+  if (rope_dim < 0 || rope_dim % 4 != 0 || rope_dim > head_dim) return CKV_ERR_HEAD_DIM;
+  if (cache_dtype != CKV_F32 && cache_dtype != CKV_BF16) return CKV_ERR_DTYPE;
+  if (!(eps > 0.0f) || !(eps < 1e30f)) return CKV_ERR_SIZE;
+  if (batch == 0) return CKV_OK;
+  if (!aligned16(state) || !aligned16(kv_score_input) || !aligned16(ape) || !aligned16(plan_d) ||
+      !aligned16(norm_weight) || !aligned16(kv_cache) || (rope_dim > 0 && !aligned16(freqs)) || out_loc == nullptr)
+    return CKV_ERR_POINTER;
+  if ((reinterpret_cast<uintptr_t>(out_loc) | reinterpret_cast<uintptr_t>(rid_hint) |
+       reinterpret_cast<uintptr_t>(seq_lens_hint)) & 7u)
+    return CKV_ERR_POINTER;
+  PoolArgs a{};
+  a.ratio = ratio;
+  a.head_dim = head_dim;
+  a.in_dtype = in_dtype;
+  a.out_dtype = CKV_F32;
+  a.state = state;
+  a.state_mut = state;
+  a.state_rows = state_rows;
+  a.input = kv_score_input;
+  a.num_q_tokens = batch;
+  a.ape = ape;
+  a.plan_d = plan_d;
+  a.rid_hint = rid_hint != nullptr && seq_lens_hint != nullptr ? rid_hint : nullptr;
+  a.seq_hint = rid_hint != nullptr && seq_lens_hint != nullptr ? seq_lens_hint : nullptr;
+  a.capacity = batch;
+  a.out_layout = CKV_OUT_TOKEN;
+  a.d_status = d_status;
+  a.wait_ns = wait_limit_ns();
+  DecodeNormArgs n{};
+  n.rope_dim = rope_dim;
+  n.weight = norm_weight;
+  n.eps = eps;
+  n.freqs = freqs;
+  n.max_pos = max_pos;
+  n.out_loc = out_loc;
+  n.cache_dtype = cache_dtype;
+  n.cache = kv_cache;
+  n.cache_rows = cache_rows;
+  return launch_c4_decode_norm(a, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

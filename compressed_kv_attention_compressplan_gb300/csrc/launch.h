@@ -51,6 +51,21 @@ int encode_tensor_map(CUtensorMap* map, int dtype, uint32_t rank, const void* ba
 
 int launch_c4_pool_prefill(const PoolArgs& a, cudaStream_t s);
 int launch_c4_decode(const PoolArgs& a, cudaStream_t s);
+
+// The norm + RoPE + store half of the fused C4 decode (ckv_compress_decode_norm_rope_store).
+struct DecodeNormArgs {
+  int rope_dim;
+  const float* weight;   // [head_dim]
+  float eps;
+  const float* freqs;    // [max_pos, rope_dim/2, 2]
+  uint32_t max_pos;
+  const int64_t* out_loc;  // [batch]
+  int cache_dtype;
+  void* cache;           // [cache_rows, head_dim]
+  uint64_t cache_rows;
+};
+
+int launch_c4_decode_norm(const PoolArgs& a, const DecodeNormArgs& n, cudaStream_t s);
 int launch_c128_pool_prefill(const PoolArgs& a, cudaStream_t s);
 int launch_c128_decode(const PoolArgs& a, cudaStream_t s);
 

@@ -806,6 +806,6 @@ const char* ckv_error_string(int code) {
   }
 }
 
-int ckv_version(void) { return 210; }
+int ckv_version(void) { return 220; }
 
 }  // extern "C"

@@ -555,6 +555,173 @@ __global__ __launch_bounds__(kC4DecodeThreads) void c4_decode_kernel(const PoolA
   store_row_chunk<TOut, VEC>(orow, res);
 }
 
+// Decode fused with RMSNorm + RoPE + store (ckv_compress_decode_norm_rope_store):
+// the decode above, whose pooled row (fp32, or +0.0 off a group boundary)
+// goes through y_c = x_c * w_c / sqrt(mean(x^2) + eps), the RoPE pairs of the
+// last rope_dim channels at table row max(seq_len - 4, 0), and straight into
+// cache row out_loc[b] -- the composition of ckv_compress_decode (fp32 out)
+// and ckv_norm_rope_store_decode without the pooled rows in between.  A row's
+// units are consecutive threads of one block (a block of 128 threads holds
+// 128 / U rows of U = head_dim / 4 units, or one row when U does not divide
+// 128): the sum of squares is a warp butterfly, then a sum over the row's
+// warps in shared memory, in warp order.
+template <typename TIn>
+__global__ __launch_bounds__(256) void c4_decode_norm_kernel(const PoolArgs a, const DecodeNormArgs n, uint32_t chunks,
+                                                             uint32_t units) {
+  using V = typename C4DecVec<TIn>::V;
+  constexpr int VEC = kC4DecVec;
+  constexpr int kLineUnits = 128 / static_cast<int>(sizeof(V));
+  __shared__ float s_part[8];
+  const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
+  const bool live = u < units;
+  const int hd = a.head_dim;
+  const size_t width = 4 * static_cast<size_t>(hd);
+  TIn* state = static_cast<TIn*>(a.state_mut);
+  const TIn* input = static_cast<const TIn*>(a.input);
+  const TIn* ape = static_cast<const TIn*>(a.ape);
+  const uint32_t b = u / chunks;
+  const uint32_t ch = u % chunks;
+  const int c0 = static_cast<int>(ch) * VEC;
+  bool h_ok = false;
+  int64_t h_sl = 0, h_rid = 0;
+  if (live) {  // L2 prefetches from the hints, as in c4_decode_kernel
+    const bool line = ch % kLineUnits == 0;
+    const TIn* src = input + static_cast<size_t>(b) * width + c0;
+    if (ch == 0) prefetch_l2(a.plan_d + b);
+    if (line) {
+      prefetch_l2(src);
+      prefetch_l2(src + hd);
+      prefetch_l2(src + 2 * hd);
+      prefetch_l2(src + 3 * hd);
+    }
+    if (a.seq_hint != nullptr) {
+      int64_t sl, rid;
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(sl) : "l"(a.seq_hint + b));
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(rid) : "l"(a.rid_hint + b));
+      if (sl >= 4 && sl % 4 == 0 && rid >= 0 && static_cast<uint64_t>(rid) * 8 + 7 < a.state_rows) {
+        h_ok = true;
+        h_sl = sl;
+        h_rid = rid;
+        if (line) {
+          for (int i = sl == 4 ? 4 : 0; i < 7; ++i) {
+            const TIn* row = state + static_cast<size_t>(rid * 8 + (sl - 8 + i) % 8) * width;
+            prefetch_l2(row + (i < 4 ? 0 : hd) + c0);
+            prefetch_l2(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
+          }
+        }
+      }
+    }
+  }
+  pdl_wait();
+  pdl_release();
+  float x[VEC] = {0.0f, 0.0f, 0.0f, 0.0f};
+  bool stored = false;  // the row goes to the cache (every valid record)
+  int64_t pos = 0;
+  int64_t loc = -1;
+  float4 w = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (live) {
+    const ckv_decode_plan_t P = load_plan_d(a.plan_d + b);
+    const TIn* src = input + static_cast<size_t>(b) * width + c0;
+    const V kv_ovl = ld_stream_v<V>(src), kv_main = ld_stream_v<V>(src + hd);
+    const V sc_ovl = ld_stream_v<V>(src + 2 * hd), sc_main = ld_stream_v<V>(src + 3 * hd);
+    V ap[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ap[i] = ld_cached_v<V>(ape + static_cast<size_t>(i) * hd + c0);
+    loc = __ldg(n.out_loc + b);
+    w = __ldg(reinterpret_cast<const float4*>(n.weight + c0));
+    const int h_first = h_sl == 4 ? 4 : 0;
+    V kv[8], sc[8];
+#pragma unroll
+    for (int i = 0; i < 7; ++i) {
+      kv[i] = sc[i] = zero_v<V>();
+      if (h_ok && i >= h_first) {
+        const TIn* row = state + static_cast<size_t>(h_rid * 8 + (h_sl - 8 + i) % 8) * width;
+        kv[i] = ld_stream_v<V>(row + (i < 4 ? 0 : hd) + c0);
+        sc[i] = ld_stream_v<V>(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
+      }
+    }
+    if (P.seq_len != kInvalidU32) {
+      stored = true;
+      pos = max(static_cast<int64_t>(P.seq_len) - 4, int64_t{0});
+      const bool boundary = P.seq_len % 4 == 0;
+      const int64_t rp0 = P.read_page_0, rp1 = P.read_page_1;
+      bool ok = P.write_loc >= 0 && static_cast<uint64_t>(P.write_loc) < a.state_rows;
+      if (boundary)
+        ok = ok && rp0 >= 0 && rp1 >= 0 && static_cast<uint64_t>(rp0) * 4 + 3 < a.state_rows &&
+             static_cast<uint64_t>(rp1) * 4 + 3 < a.state_rows;
+      if (!ok) {
+        if (ch == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+      } else {
+        TIn* dst = state + static_cast<size_t>(P.write_loc) * width + c0;
+        st_v<V>(dst, kv_ovl);
+        st_v<V>(dst + hd, kv_main);
+        st_v<V>(dst + 2 * hd, sc_ovl);
+        st_v<V>(dst + 3 * hd, sc_main);
+        if (boundary) {
+          const int first = P.seq_len == 4 ? 4 : 0;
+          bool same = h_ok && h_sl == static_cast<int64_t>(P.seq_len);
+#pragma unroll
+          for (int i = 0; i < 7; ++i)
+            if (i >= first) same = same && (i < 4 ? rp0 : rp1) * 4 + (i & 3) == h_rid * 8 + (h_sl - 8 + i) % 8;
+          if (!same) {
+#pragma unroll
+            for (int i = 0; i < 7; ++i) {
+              if (i < first) {
+                kv[i] = sc[i] = zero_v<V>();
+                continue;
+              }
+              const TIn* row = state + static_cast<size_t>((i < 4 ? rp0 : rp1) * 4 + (i & 3)) * width;
+              kv[i] = ld_stream_v<V>(row + (i < 4 ? 0 : hd) + c0);
+              sc[i] = ld_stream_v<V>(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
+            }
+          }
+          kv[7] = kv_main;
+          sc[7] = sc_main;
+          c4_pool_chunk<TIn, VEC>(kv, sc, ap, first, x);
+        }
+      }
+    }
+  }
+  // RMS of the row: every thread of the block takes part (rows are whole warps)
+  float ss = 0.0f;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) s_part[warp] = ss;
+  __syncthreads();
+  const int row_warps = static_cast<int>(chunks) / 32;
+  const int w0 = warp / row_warps * row_warps;
+  float tot = 0.0f;
+  for (int k = 0; k < row_warps; ++k) tot += s_part[w0 + k];
+  if (!live || !stored) return;
+  const int base = hd - n.rope_dim;
+  const bool pos_ok = n.rope_dim == 0 || pos < n.max_pos;
+  if (!pos_ok || loc < 0 || static_cast<uint64_t>(loc) >= n.cache_rows) {
+    if (ch == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+    return;
+  }
+  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, static_cast<float>(hd)), n.eps)));
+  float y[4] = {x[0] * r * w.x, x[1] * r * w.y, x[2] * r * w.z, x[3] * r * w.w};
+  if (c0 >= base) {  // pairs (c0, c0+1) and (c0+2, c0+3)
+    const float4 cs = __ldg(reinterpret_cast<const float4*>(
+        n.freqs + (static_cast<size_t>(pos) * (n.rope_dim / 2) + (c0 - base) / 2) * 2));
+    const float a0 = y[0], b0 = y[1], a1 = y[2], b1 = y[3];
+    y[0] = a0 * cs.x - b0 * cs.y;
+    y[1] = a0 * cs.y + b0 * cs.x;
+    y[2] = a1 * cs.z - b1 * cs.w;
+    y[3] = a1 * cs.w + b1 * cs.z;
+  }
+  const size_t at = static_cast<size_t>(loc) * hd + c0;
+  if (n.cache_dtype == CKV_BF16) {
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(n.cache) + at) =
+        make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(n.cache) + at) = make_float4(y[0], y[1], y[2], y[3]);
+  }
+}
+
 // The 4-D view of a [rows, 4 * hd] C4 row tensor, boxes of `box_rows` rows.
 int c4_view(CUtensorMap* map, const void* base, int dtype, int hd, uint64_t rows, uint32_t box_rows) {
   const uint64_t esz = dtype == CKV_BF16 ? 2 : 4;
@@ -617,6 +784,18 @@ int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
                     chunks, units);
 }
 
+template <typename TIn>
+int launch_decode_norm_t(const PoolArgs& a, const DecodeNormArgs& n, cudaStream_t s) {
+  const uint32_t chunks = static_cast<uint32_t>(a.head_dim / kC4DecVec);  // units per row, a multiple of 32
+  const uint64_t units64 = static_cast<uint64_t>(a.capacity) * chunks;
+  if (units64 == 0) return CKV_OK;
+  if (units64 > 0xFFFFFFFFull) return CKV_ERR_SIZE;
+  const uint32_t units = static_cast<uint32_t>(units64);
+  const uint32_t threads = 128 % chunks == 0 ? 128u : chunks;  // whole rows per block
+  return launch_pdl(c4_decode_norm_kernel<TIn>, dim3((units + threads - 1) / threads), dim3(threads), 0, s, a, n,
+                    chunks, units);
+}
+
 }  // namespace
 
 namespace {
@@ -634,6 +813,10 @@ int launch_c4_pool_prefill(const PoolArgs& a, cudaStream_t s) {
     return a.out_dtype == CKV_BF16 ? launch_prefill_w<__nv_bfloat16, __nv_bfloat16>(a, s)
                                    : launch_prefill_w<__nv_bfloat16, float>(a, s);
   return a.out_dtype == CKV_BF16 ? launch_prefill_w<float, __nv_bfloat16>(a, s) : launch_prefill_w<float, float>(a, s);
+}
+
+int launch_c4_decode_norm(const PoolArgs& a, const DecodeNormArgs& n, cudaStream_t s) {
+  return a.in_dtype == CKV_BF16 ? launch_decode_norm_t<__nv_bfloat16>(a, n, s) : launch_decode_norm_t<float>(a, n, s);
 }
 
 int launch_c4_decode(const PoolArgs& a, cudaStream_t s) {

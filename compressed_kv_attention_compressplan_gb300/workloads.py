@@ -373,6 +373,33 @@ def norm_rope_c128_decode(seed: int = 0, head_dim: int = 512, rope_dim: int = 64
 NORM_ROPE = {"norm_rope_c128_prefill": norm_rope_c128_prefill, "norm_rope_c128_decode": norm_rope_c128_decode}
 
 
+@dataclasses.dataclass
+class DecodeNormInputs:
+    """A decode workload plus the norm + RoPE + store inputs of its output rows."""
+    w: "Workload"
+    rope_dim: int
+    weight: torch.Tensor      # fp32 [head_dim]
+    eps: float
+    freqs: torch.Tensor       # fp32 [max_pos, rope_dim/2, 2]
+    out_loc: torch.Tensor     # int64 [batch]
+    cache_rows: int
+    cache_dtype: torch.dtype
+
+
+def c4_decode_norm_rope(seed: int = 0, rope_dim: int = 64) -> DecodeNormInputs:
+    """The C4 decode workload whose output rows go through norm + RoPE into a bf16 cache."""
+    w = c4_decode(seed)
+    hd, batch = w.head_dim, w.batch
+    weight = 1.0 + normal((hd,), torch.float32, 0.1, _seed(seed, 22))
+    cache_rows = 4 * batch
+    out_loc = torch.randperm(cache_rows, generator=_gen(seed, 23))[:batch].to(torch.int64)
+    return DecodeNormInputs(w, rope_dim, weight, 1e-6, rope_table(int(w.seq_lens.max()) + 1, rope_dim), out_loc,
+                            cache_rows, torch.bfloat16)
+
+
+DECODE_NORM = {"c4_decode_norm_rope": c4_decode_norm_rope}
+
+
 # ----------------------------------------------------------------------------- online C128 state inputs
 @dataclasses.dataclass
 class OnlineInputs:

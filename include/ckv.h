@@ -435,11 +435,36 @@ int ckv_norm_rope_store_decode(int ratio, int head_dim, int rope_dim, int in_dty
                                const float* freqs, uint32_t max_pos, const int64_t* out_loc, int cache_dtype,
                                void* kv_cache, uint64_t cache_rows, uint32_t* d_status, ckv_stream_t stream);
 
+/* Decode with norm + RoPE + store in one launch, ratio 4 only (the step that
+ * compressor_v2.py runs after the C4 decode, fused; the pages run them as two
+ * steps): exactly ckv_compress_decode with an fp32 output followed by
+ * ckv_norm_rope_store_decode on that output -- the state write, the pooled
+ * row (or +0.0 off a group boundary) normalised, rotated at table row
+ * max(seq_len - 4, 0) and stored at kv_cache row out_loc[b] -- except that the
+ * pooled rows are never written to memory, and the RMS's fp32 sum of squares
+ * runs in another order (results agree within the norm step's rounding).  A
+ * row's 4-channel units are threads of one block, so the norm needs no second
+ * launch; the C128 decode spreads a row over several CTAs and has no such
+ * form (CKV_ERR_RATIO).  Arguments as in ckv_compress_decode (without order and
+ * out) and ckv_norm_rope_store_decode (without rows and in_dtype); out_loc is
+ * int64 [batch].  Invalid records store nothing; a row whose record points
+ * outside the state is flagged CKV_STATUS_BAD_INDEX, writes no state and stores
+ * the normalised zero row; a position outside the table or a location outside
+ * the cache is flagged and stores nothing. */
+int ckv_compress_decode_norm_rope_store(int ratio, int head_dim, int rope_dim, int in_dtype, void* state,
+                                        uint64_t state_rows, const void* kv_score_input, const void* ape,
+                                        const ckv_decode_plan_t* plan_d, const int64_t* rid_hint,
+                                        const int64_t* seq_lens_hint, uint32_t batch, const float* norm_weight,
+                                        float eps, const float* freqs, uint32_t max_pos, const int64_t* out_loc,
+                                        int cache_dtype, void* kv_cache, uint64_t cache_rows, uint32_t* d_status,
+                                        ckv_stream_t stream);
+
 /* ------------------------------------------------------------------ misc */
 /* Short text for a CKV_OK / CKV_ERR_* code (static storage). */
 const char* ckv_error_string(int code);
-/* Library ABI version: major * 100 + minor (210: 2.00's decode boundary-row
- * list and prefetch hints, plus the prefill prefetch hints). */
+/* Library ABI version: major * 100 + minor (220: 2.00's decode boundary-row
+ * list and prefetch hints, 2.10's prefill prefetch hints, and the fused C4
+ * decode + norm + RoPE + store). */
 int ckv_version(void);
 
 #ifdef __cplusplus

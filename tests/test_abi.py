@@ -100,6 +100,22 @@ def test_argument_errors_are_returned_before_any_launch(lib):
     assert lib.ckv_compress_online_prefill(512, 1, 0, None, 1, None, 8, None, None, None, 4, 0, 0, None, None,
                                            None) == -4
     assert lib.ckv_plan_online_prefill(None, None, None, 2000, 0, 0, 0, 0, None, vp(16), None, None) == -3
+    fused = lib.ckv_compress_decode_norm_rope_store
+    f32 = ctypes.c_float
+    ok = dict(state=vp(16), inp=vp(16), ape=vp(16), pd=vp(16), w=vp(16), fr=vp(16), loc=vp(16), cache=vp(16))
+
+    def call(ratio=4, hd=512, rope=64, in_dt=1, eps=1e-6, cache_dt=1, loc=vp(16), batch=3):
+        return fused(ratio, hd, rope, in_dt, ok["state"], 64, ok["inp"], ok["ape"], ok["pd"], None, None, batch,
+                     ok["w"], f32(eps), ok["fr"], 16, loc, cache_dt, ok["cache"], 16, None, None)
+    assert call(ratio=128) == -1      # the C128 decode has no fused form
+    assert call(hd=200) == -2
+    assert call(rope=30) == -2
+    assert call(in_dt=7) == -5
+    assert call(cache_dt=7) == -5
+    assert call(eps=0.0) == -3
+    assert call(loc=vp(12)) == -4     # out_loc must be 8-byte aligned
+    assert call(loc=None) == -4
+    assert call(batch=0) == 0         # nothing to do, nothing launched
     assert lib.ckv_error_string(-4) != lib.ckv_error_string(0)
 
 
@@ -121,7 +137,7 @@ def test_binding_rejects_wrong_per_request_arrays():
 
 
 def test_wait_limit_setter(lib):
-    assert lib.ckv_version() >= 210  # ABI 2.10: prefill prefetch hints (2.00: decode boundary-row lists)
+    assert lib.ckv_version() >= 220  # ABI 2.20: fused C4 decode + norm (2.10: prefill hints; 2.00: decode lists)
     default = 2_000_000_000
     prev = ckv.set_wait_limit_ns(0)            # whatever was set, back to the default
     assert ckv.set_wait_limit_ns(1234) == default

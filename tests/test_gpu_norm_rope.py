@@ -198,3 +198,81 @@ def test_no_records(env):
     ckv.norm_rope_store_prefill(4, rows, plan_c, None, w, 1e-6, freqs, loc, cache, status=status)
     torch.cuda.synchronize()
     assert (cache == 5.0).all() and int(status[0]) == 0
+
+
+@pytest.mark.parametrize("hd,rope", [(512, 64), (128, 64), (384, 32), (1024, 0)])
+@pytest.mark.parametrize("in_code,cache_code", [(1, 1), (1, 0), (0, 1)])
+@pytest.mark.parametrize("hinted", [False, True])
+def test_fused_c4_decode_norm_rope_store(env, hd, rope, in_code, cache_code, hinted):
+    """ckv_compress_decode_norm_rope_store against the same step in two
+    launches (decode with fp32 rows, then norm + RoPE + store on them): the
+    state bytes equal, every stored cache row within the norm step's bar (the
+    RMS's fp32 sum runs in another order), rows of invalid records untouched;
+    and the two-launch rows against the oracle."""
+    o, ckv, dev = env
+    rng = np.random.default_rng(hd + rope + 10 * in_code + cache_code + (5 if hinted else 0))
+    B = 257
+    sl = rng.integers(1, 3000, B)
+    on = rng.random(B) < 0.4
+    sl[on] = 4 * rng.integers(1, 750, int(on.sum()))
+    sl[:3] = [4, 8, 3]  # the first group (masked previous group), the second, none
+    w = wl.random_decode(4, hd, H.torch_dtype(in_code), torch.float32, sl, seed=hd + 3, num_requests_state=B + 7)
+    plan = o.plan_decode(4, w.rid, w.seq_lens)
+    plan[rng.random(B) < 0.04] = 0xFF  # a few padding records
+    weight = (1 + 0.2 * rng.standard_normal(hd)).astype(np.float32)
+    freqs = textbook_freqs(4096, rope) if rope else np.zeros((1, 0, 2), np.float32)
+    cache_rows = B + 40
+    loc = rng.permutation(cache_rows)[:B].astype(np.int64)
+    pd = torch.from_numpy(plan).to(dev)
+    args = dict(norm_weight=torch.from_numpy(weight).to(dev), eps=1e-6, freqs=torch.from_numpy(freqs).to(dev),
+                out_loc=torch.from_numpy(loc).to(dev))
+    kv, ape = w.kv_score.to(dev), w.ape.to(dev)
+    # two launches
+    st2 = w.state.to(dev)
+    cache2 = H.to_torch(_sentinel_cache(cache_rows, hd, cache_code), cache_code).to(dev)
+    status = ckv.new_status(dev)
+    rows = ckv.compress_decode(4, hd, st2, kv, ape, pd, torch.float32, status=status)
+    ckv.norm_rope_store_decode(4, rows, pd, args["norm_weight"], args["eps"], args["freqs"], args["out_loc"], cache2,
+                               status=status)
+    # one launch
+    st1 = w.state.to(dev)
+    cache1 = H.to_torch(_sentinel_cache(cache_rows, hd, cache_code), cache_code).to(dev)
+    hints = {"rid_hint": w.rid.to(dev), "seq_lens_hint": w.seq_lens.to(dev)} if hinted else {}
+    ckv.compress_decode_norm_rope_store(hd, st1, kv, ape, pd, kv_cache=cache1, status=status, **args, **hints)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    assert (H.np_bits(st1).view(np.uint8) == H.np_bits(st2).view(np.uint8)).all(), "state"
+    valid = H.plan_d_fields(plan)["seq_len"] != 0xFFFFFFFF
+    _compare(H.np_bits(cache1), H.np_bits(cache2), cache_code, loc[valid], hd, "fused against two launches")
+    # the two-launch rows against the oracle (decode with fp32 rows, then norm + RoPE + store)
+    st = wl.bits(w.state).copy()
+    pooled = o.compress_decode(4, hd, in_code, 0, st, wl.bits(w.kv_score), wl.bits(w.ape), plan)
+    want = _sentinel_cache(cache_rows, hd, cache_code)
+    o.norm_rope_store(4, 1, hd, rope, 0, H.np_bits(rows).copy(), 1, plan, weight, 1e-6, freqs, loc, cache_code, want)
+    _compare(H.np_bits(cache2), want, cache_code, loc[valid], hd, "two launches against the oracle")
+    f = H.plan_d_fields(plan)
+    bnd = np.nonzero(valid & (f["seq_len"] % 4 == 0))[0]
+    kvmax = H.window_kv_absmax(4, hd, wl.bits(w.state), wl.bits(w.kv_score), f["seq_len"][bnd], bnd,
+                               np.full(len(bnd), 7), f["read_page_0"][bnd], f["read_page_1"][bnd])
+    H.assert_pool_close(H.np_bits(rows)[bnd], pooled[bnd], 0, kvmax, "decode rows")
+
+
+def test_fused_c4_decode_norm_rope_store_bad_records(env):
+    """A location outside the cache or a position outside the table is flagged
+    and stores nothing; the other rows are stored."""
+    o, ckv, dev = env
+    hd, B = 256, 40
+    w = wl.random_decode(4, hd, torch.bfloat16, torch.float32, 4 * np.arange(1, B + 1), seed=8, num_requests_state=B)
+    pd = torch.from_numpy(o.plan_decode(4, w.rid, w.seq_lens)).to(dev)
+    loc = torch.arange(B, dtype=torch.int64, device=dev)
+    loc[5] = 10 ** 6
+    cache = torch.full((B, hd), float("nan"), device=dev)
+    status = ckv.new_status(dev)
+    freqs = torch.from_numpy(textbook_freqs(100, 64)).to(dev)  # rows with seq_len - 4 >= 100 fall outside
+    ckv.compress_decode_norm_rope_store(hd, w.state.to(dev), w.kv_score.to(dev), w.ape.to(dev), pd,
+                                        torch.ones(hd, device=dev), 1e-6, freqs, loc, cache, status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) & ckv.STATUS_BAD_INDEX
+    stored = torch.isfinite(cache).all(dim=1).cpu().numpy()
+    want = np.array([b != 5 and 4 * (b + 1) - 4 < 100 for b in range(B)])
+    assert (stored == want).all()
