@@ -764,8 +764,9 @@ def run_graph(step: StepGraph, flush, restore, steps, warmup, ws, sampler=None):
 def c4_kernels(args, ckv, dev, seed: int, peak: float) -> dict:
     """The C4 kernels on their own workloads, reported beside the headline step (which is C128): the C4
     ragged prefill (plan -> pool -> write) and the C4 decode (plan -> decode), each step in one graph,
-    per-kernel costs inside the step by difference, the pool's and the decode's fraction of the peak, and
-    the decode back to back against its same-bytes floor."""
+    per-kernel costs inside the step by difference, the pool's and the decode's fraction of the peak, the
+    decode back to back against its same-bytes floor, and the decode with its norm + RoPE + store in two
+    launches against the fused launch."""
     w4 = wl.c4_prefill(seed)
     w2 = wl.c4_decode(seed)
     pre = PrefillRunner(ckv, w4, dev)
@@ -805,6 +806,8 @@ def c4_kernels(args, ckv, dev, seed: int, peak: float) -> dict:
         out["c4_decode"].update({"back_to_back_us": us,
                                  "back_to_back_frac": b2["decode"] / (us * 1e-6) / 1e9 / peak,
                                  "same_bytes_floor": floor, "floor_ratio": us / best})
+    # the decode with its norm + RoPE + store: two launches against the fused one
+    out["c4_decode_norm_rope"] = decode_norm_measure(args, "c4_decode_norm_rope", seed, ckv, dev)
     del pre, dec
     torch.cuda.empty_cache()
     return out
@@ -1253,10 +1256,17 @@ def bench_norm_rope(args, name, ws, rank, ckv, dev):
 
 
 def bench_decode_norm(args, name, ws, rank, ckv, dev):
+    """The C4 decode followed by norm + RoPE + store, alone; prints one line."""
+    line = decode_norm_measure(args, name, args.seed + rank, ckv, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def decode_norm_measure(args, name, seed, ckv, dev) -> dict:
     """The C4 decode followed by norm + RoPE + store: two launches (the decode's fp32 rows, then the norm
     step over them) against the one fused launch; the planner before both.  Costs inside each step by
-    difference, and each form back to back; prints one line."""
-    x = wl.DECODE_NORM[name](args.seed + rank)
+    difference, and each form back to back."""
+    x = wl.DECODE_NORM[name](seed)
     w = x.w
     d = DecodeRunner(ckv, w, dev)
     weight, freqs, loc = x.weight.to(dev), x.freqs.to(dev), x.out_loc.to(dev)
@@ -1300,8 +1310,9 @@ def bench_decode_norm(args, name, ws, rank, ckv, dev):
             one_fns.append(f1)
         line.update({"two_launches_back_to_back_us": steady_state_us(two_fns),
                      "fused_back_to_back_us": steady_state_us(one_fns), "back_to_back_copies": n})
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    del d
+    torch.cuda.empty_cache()
+    return line
 
 
 def bench_online(args, name, ws, rank, ckv, dev):
