@@ -181,3 +181,46 @@ def test_paged_schedule_matches_one_shot(env):
         kvmax = H.window_kv_absmax(ratio, hd, h, h, seq, np.array(emit), np.zeros(len(emit), np.int64),
                                    np.zeros(len(emit)), np.zeros(len(emit)))
         H.assert_pool_close(outs[b][emit], want[emit], 0, kvmax, f"history b={b}")
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_paged_plans_random(env, case):
+    """Seeded random SWA-paged steps: page size 16 .. 256, ring 8 .. 64 rows, up to 200 requests with
+    prefix-cache hits, equal or mixed extends, padded or not; prefill and decode plans bit-exact."""
+    o, ckv, dev = env
+    rng = np.random.default_rng(90000 + case)
+    ratio = int(rng.choice([4, 128]))
+    S = int(rng.choice([16, 32, 64, 128, 256]))
+    ring = int(rng.choice([r for r in (8, 16, 32, 64) if S % r == 0])) if ratio == 4 else 128
+    B = int(rng.integers(1, 201))
+    max_sl = int(rng.choice([40, 300, 3000]))
+    sl = [int(rng.integers(1, max_sl + 1)) for _ in range(B)]
+    if rng.random() < 0.3:  # equal extends
+        e = int(rng.integers(1, 9))
+        sl = [max(s, e) for s in sl]
+        el = [e] * B
+    else:
+        el = [int(rng.integers(1, s + 1)) if rng.random() < 0.7 else s for s in sl]
+    pad = bool(rng.integers(2))
+    pool, rids = _pool_for(rng, B, sl, S, prefix_hits=bool(rng.integers(2)))
+    nq = int(sum(el))
+    i64 = dict(dtype=torch.int64, device=dev)
+    maps = (torch.from_numpy(pool.r2t).to(dev), torch.from_numpy(pool.f2s).to(dev)) if ratio == 4 else (None, None)
+    omaps = (pool.r2t, pool.f2s) if ratio == 4 else (None, None)
+    cap_c = nq if pad else ckv.capacity_compress(ratio, B, nq)
+    cap_w = nq if pad else ckv.capacity_write_paged(ratio, B, nq, S)
+    status = ckv.new_status(dev)
+    pc, pw, counts = ckv.plan_prefill_paged(ratio, torch.tensor(rids, **i64), *maps, S, ring, torch.tensor(sl, **i64),
+                                            torch.tensor(el, **i64), nq, cap_c, cap_w, pad_invalid=pad,
+                                            status=status)
+    pd = ckv.plan_decode_paged(ratio, torch.tensor(rids, **i64), *maps, S, ring, torch.tensor(sl, **i64),
+                               status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    wc, ww, (nc, nw), _ = o.plan_prefill_paged(ratio, rids, *omaps, S, ring, sl, el, nq, cap_c, cap_w,
+                                               pad_invalid=pad)
+    assert counts[:2].tolist() == [nc, nw]
+    n_c, n_w = (cap_c, cap_w) if pad else (nc, nw)
+    assert (pc[:n_c].cpu().numpy() == wc[:n_c]).all(), "compress plan"
+    assert (pw[:n_w].cpu().numpy() == ww[:n_w]).all(), "write plan"
+    assert (pd.cpu().numpy() == o.plan_decode_paged(ratio, rids, *omaps, S, ring, sl)).all(), "decode plan"
