@@ -129,6 +129,45 @@ def test_online_modes_bitwise_and_window_parity(env, hd, in_dt, out_dt):
             H.assert_pool_close(ref[emit], want[b][emit], out_dt, kvmax, f"online b={b}")
 
 
+@pytest.mark.parametrize("case", range(20))
+def test_online_random_schedules(env, case):
+    """Seeded random histories and schedules through the online state: head_dim
+    128 .. 1024, any dtype pair, 1 .. 8 requests of up to 700 tokens fed as
+    chunked prefills, decodes or a mix; every emitted row against the window
+    definition and bitwise equal to the one-shot prefill."""
+    o, ckv, dev = env
+    rng = np.random.default_rng(40000 + case)
+    hd = int(rng.choice([128, 256, 384, 512, 640, 768, 896, 1024]))
+    in_dt, out_dt = [(1, 0), (1, 1), (0, 0), (0, 1)][int(rng.integers(4))]
+    nreq = int(rng.integers(1, 9))
+    lens = [int(rng.integers(1, 701)) for _ in range(nreq)]
+    rids = [int(x) for x in rng.permutation(nreq + 3)[:nreq]]
+    tdt = torch.bfloat16 if in_dt else torch.float32
+    g = torch.Generator().manual_seed(500 + case)
+    hist = [wl.bits(torch.randn(n, 2 * hd, generator=g).to(tdt)).copy() for n in lens]
+    ape = wl.bits((torch.randn(128, hd, generator=g) * 0.5).to(tdt)).copy()
+    backend = OnlineGpuBackend(ckv, dev, slot_offset=int(rng.integers(0, 3)))
+    chunk = int(rng.choice([20, 70, 150, 400]))
+    dec_frac = float(rng.choice([0.0, 0.3, 0.7]))
+    results = {}
+    for mode, sched in [("oneshot", [[("prefill", n)] for n in lens]),
+                        ("random", [H.split_schedule(n, rng, chunk, dec_frac) for n in lens])]:
+        state = torch.full((nreq + 6, 3 * hd), float("nan"), device=dev)
+        results[mode] = H.run_schedule(backend, 128, hd, in_dt, out_dt, hist, rids, sched, ape, state)
+        assert int(backend.status[0]) == 0
+    view = np.uint16 if out_dt else np.uint32
+    for b in range(nreq):
+        ref = results["oneshot"][b]
+        assert (results["random"][b].view(view) == ref.view(view)).all(), b
+        emit = [p for p in range(lens[b]) if (p + 1) % 128 == 0]
+        if emit:
+            want = o.compress_history(128, hd, in_dt, out_dt, hist[b], ape)
+            tok = hist[b]
+            kvmax = H.window_kv_absmax(128, hd, tok, tok, np.array(emit) + 1, np.array(emit),
+                                       np.zeros(len(emit), np.int64), np.zeros(len(emit)), np.zeros(len(emit)))
+            H.assert_pool_close(ref[emit], want[emit], out_dt, kvmax, f"online random b={b}")
+
+
 def test_online_state_and_compact_rows(env):
     """One prefill step from a state folded by the oracle: compact rows, the
     state after it (maxima bit-exact, sums to fp32 accuracy) and bad units."""
