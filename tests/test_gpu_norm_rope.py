@@ -124,6 +124,64 @@ def test_prefill_parity(env, ratio, layout):
     _compare(H.np_bits(cache), want, 1, stored, hd, "prefill")
 
 
+@pytest.mark.parametrize("case", range(20))
+def test_random_norm_rope(env, case):
+    """Seeded random cases of both entry points: head_dim 128 .. 1024 (every
+    kChunks instance), rope_dim any multiple of 4 up to head_dim, row and cache
+    dtypes, ratio, layout; against the oracle with the same bar."""
+    o, ckv, dev = env
+    rng = np.random.default_rng(60000 + case)
+    ratio = int(rng.choice([4, 128]))
+    hd = 128 * int(rng.integers(1, 9))
+    rope = 4 * int(rng.integers(0, hd // 4 + 1))
+    in_code, cache_code = int(rng.integers(2)), int(rng.integers(2))
+    eps = float(rng.choice([1e-6, 1e-5, 1e-3]))
+    w = (1 + 0.2 * rng.standard_normal(hd)).astype(np.float32)
+    if rng.integers(2):  # decode
+        B = int(rng.integers(1, 400))
+        sl = rng.integers(1, 3000, B)
+        on = rng.random(B) < 0.5
+        sl[on] = ratio * rng.integers(1, max(2, 3000 // ratio), int(on.sum()))
+        plan = o.plan_decode(ratio, np.arange(B), sl)
+        rows = _rows(rng, B, hd, in_code)
+        freqs = textbook_freqs(3000 + ratio, rope) if rope else np.zeros((1, 0, 2), np.float32)
+        cache_rows = B + 20
+        loc = rng.permutation(cache_rows)[:B].astype(np.int64)
+        want = _sentinel_cache(cache_rows, hd, cache_code)
+        o.norm_rope_store(ratio, 1, hd, rope, in_code, rows, 1, plan, w, eps, freqs, loc, cache_code, want)
+        cache = H.to_torch(_sentinel_cache(cache_rows, hd, cache_code), cache_code).to(dev)
+        status = ckv.new_status(dev)
+        ckv.norm_rope_store_decode(ratio, H.to_torch(rows, in_code).to(dev), torch.from_numpy(plan).to(dev),
+                                   torch.from_numpy(w).to(dev), eps, torch.from_numpy(freqs).to(dev),
+                                   torch.from_numpy(loc).to(dev), cache, status=status)
+        stored = loc
+    else:  # prefill
+        layout = int(rng.integers(2))
+        B = int(rng.integers(1, 30))
+        pl = rng.integers(0, 2000, B)
+        el = rng.integers(1, 600, B)
+        sl = pl + el
+        nq = int(el.sum())
+        pc, _, (nc, _), _ = o.plan_prefill(ratio, np.arange(B), sl, el)
+        rows = _rows(rng, nq if layout == 0 else max(nc, 1), hd, in_code)
+        freqs = textbook_freqs(int(sl.max()) + 1, rope) if rope else np.zeros((1, 0, 2), np.float32)
+        cache_rows = nq + 5
+        loc = rng.permutation(cache_rows)[:nq].astype(np.int64)
+        want = _sentinel_cache(cache_rows, hd, cache_code)
+        o.norm_rope_store(ratio, 0, hd, rope, in_code, rows, layout, pc[:nc], w, eps, freqs, loc, cache_code, want)
+        cache = H.to_torch(_sentinel_cache(cache_rows, hd, cache_code), cache_code).to(dev)
+        status = ckv.new_status(dev)
+        pcd = torch.from_numpy(np.ascontiguousarray(pc[:max(nc, 1)])).to(dev)
+        counts = torch.tensor([nc, 0, 0, 0], dtype=torch.int32, device=dev)
+        ckv.norm_rope_store_prefill(ratio, H.to_torch(rows, in_code).to(dev), pcd, counts,
+                                    torch.from_numpy(w).to(dev), eps, torch.from_numpy(freqs).to(dev),
+                                    torch.from_numpy(loc).to(dev), cache, in_layout=layout, status=status)
+        stored = loc[H.plan_c_fields(pc[:nc])["ragged_id"]]
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    _compare(H.np_bits(cache), want, cache_code, stored, hd, f"random case {case}")
+
+
 def test_errors_and_bad_records(env):
     o, ckv, dev = env
     hd = 512
