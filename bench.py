@@ -1282,9 +1282,16 @@ def decode_norm_measure(args, name, seed, ckv, dev) -> dict:
                                             freqs, loc, cache, status=d.status, **d.hints())
 
     reps = max(200, 10 * args.steps)
-    two = instep_by_difference([("plan_decode", d.plan), ("decode", d.decode), ("norm_rope_store", norm)], flush,
-                               d.restore, reps)
-    one = instep_by_difference([("plan_decode", d.plan), ("decode_norm_rope_store", fused)], flush, d.restore, reps)
+    two_seg = [("plan_decode", d.plan), ("decode", d.decode), ("norm_rope_store", norm)]
+    one_seg = [("plan_decode", d.plan), ("decode_norm_rope_store", fused)]
+    if args.no_instep:  # one pass of each step (profiler captures)
+        for _, f in two_seg + one_seg:
+            f()
+        torch.cuda.synchronize()
+        two = one = {}
+    else:
+        two = instep_by_difference(two_seg, flush, d.restore, reps)
+        one = instep_by_difference(one_seg, flush, d.restore, reps)
     if int(d.status[0]):
         raise RuntimeError(f"device status {int(d.status[0])}")
     line = {"workload": name, "ratio": 4, "head_dim": w.head_dim, "batch": w.batch, "rope_dim": x.rope_dim,
