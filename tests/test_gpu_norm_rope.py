@@ -317,11 +317,14 @@ def test_fused_c4_decode_norm_rope_store(env, hd, rope, in_code, cache_code, hin
 
 def test_fused_c4_decode_norm_rope_store_bad_records(env):
     """A location outside the cache or a position outside the table is flagged
-    and stores nothing; the other rows are stored."""
+    and stores nothing; a record that writes outside the state is flagged and
+    stores the normalised zero row; the other rows are stored."""
     o, ckv, dev = env
     hd, B = 256, 40
     w = wl.random_decode(4, hd, torch.bfloat16, torch.float32, 4 * np.arange(1, B + 1), seed=8, num_requests_state=B)
-    pd = torch.from_numpy(o.plan_decode(4, w.rid, w.seq_lens)).to(dev)
+    plan = o.plan_decode(4, w.rid, w.seq_lens)
+    plan.view(np.int32).reshape(B, 4)[7, 1] = 2 ** 30  # row 7 writes outside the state
+    pd = torch.from_numpy(plan).to(dev)
     loc = torch.arange(B, dtype=torch.int64, device=dev)
     loc[5] = 10 ** 6
     cache = torch.full((B, hd), float("nan"), device=dev)
@@ -334,3 +337,4 @@ def test_fused_c4_decode_norm_rope_store_bad_records(env):
     stored = torch.isfinite(cache).all(dim=1).cpu().numpy()
     want = np.array([b != 5 and 4 * (b + 1) - 4 < 100 for b in range(B)])
     assert (stored == want).all()
+    assert (cache[7] == 0).all()  # no state written, the normalised zero row stored
