@@ -11,7 +11,9 @@
 //
 // Prefill: a producer warp stages each record's window in shared memory with
 // two tensor-map copies (see c4_pool_prefill_staged_kernel); consumer threads
-// own 16-byte channel chunks (8 bf16 or 4 fp32 channels).  Decode: one thread
+// own 16-byte channel chunks (8 bf16 or 4 fp32 channels).  Small steps load
+// the windows directly instead, one thread per record and chunk
+// (c4_pool_prefill_direct_kernel).  Decode: one thread
 // per (row, 4 channels) with direct loads.  The window is small enough that
 // the fp32 safe softmax runs entirely in registers.
 #include <algorithm>
@@ -428,6 +430,112 @@ __global__ __launch_bounds__(288, 1) void c4_pool_prefill_staged_kernel(const Po
   }
 }
 
+// Small steps, direct loads: one thread per (record, 16-byte channel chunk),
+// the grid one resident wave.  A thread requests its record (and the one
+// before it, for the zero rows of the token layout) together with the count
+// and the ape chunks, then its 16 window vectors at once, so a record costs
+// two memory round trips after the dependency wait; the staged kernel's chain
+// (count, record, copies issued, copies landed, stage handed over) is longer
+// than a whole launch of a step of a few thousand records takes this way.
+// Same c4_pool_chunk, so the rows are bit-identical to the other C4 kernels'.
+constexpr int kC4DirectThreads = 128;
+
+template <typename TIn, typename TOut>
+__global__ __launch_bounds__(kC4DirectThreads) void c4_pool_prefill_direct_kernel(const PoolArgs a, uint32_t chunks,
+                                                                                 uint32_t cap_units) {
+  constexpr int VEC = C4Vec<TIn>::VEC;
+  const int hd = a.head_dim;
+  const size_t width = 4 * static_cast<size_t>(hd);
+  const TIn* state = static_cast<const TIn*>(a.state);
+  const TIn* input = static_cast<const TIn*>(a.input);
+  const TIn* ape = static_cast<const TIn*>(a.ape);
+  TOut* out = static_cast<TOut*>(a.out);
+  const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  if (a.ext_hint != nullptr) {
+    // As in the staged kernel: the state halves of each request's first
+    // window into L2 while the planner runs, one 128-byte line of one entry's
+    // kv and score halves per item.  Only prefetches follow from the hints.
+    const uint32_t half = static_cast<uint32_t>(hd) * sizeof(TIn);
+    const uint32_t lines = half / 128;
+    const uint8_t* st = static_cast<const uint8_t*>(a.state);
+    const uint64_t items = static_cast<uint64_t>(a.hint_batch) * 8 * lines;
+    for (uint64_t k = tid; k < items; k += stride) {
+      const uint32_t b = static_cast<uint32_t>(k / (8 * lines));
+      const int i = static_cast<int>((k / lines) % 8);
+      const uint32_t o = static_cast<uint32_t>(k % lines) * 128;
+      int64_t sl, el, rid;
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(sl) : "l"(a.seq_hint + b));
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(el) : "l"(a.ext_hint + b));
+      asm volatile("ld.global.u64 %0, [%1];" : "=l"(rid) : "l"(a.rid_hint + b));
+      const int64_t pl = sl - el;
+      if (el > 0 && pl > 0 && sl / 4 > pl / 4 && rid >= 0 && rid < (int64_t{1} << 48) &&
+          static_cast<uint64_t>(rid) * 8 + 7 < a.state_rows) {
+        const int64_t p = pl / 4 * 4 + 3;  // the request's first event
+        if (i >= (p == 3 ? 4 : 0) && p - 7 + i < pl) {
+          const uint8_t* row = st + static_cast<size_t>(rid * 8 + (p - 7 + i) % 8) * 4 * half;
+          prefetch_l2(row + (i < 4 ? 0 : half) + o);
+          prefetch_l2(row + (i < 4 ? 2 : 3) * half + o);
+        }
+      }
+    }
+  }
+  pdl_wait();
+  pdl_release();
+  const bool token = a.out_layout == CKV_OUT_TOKEN;
+  const uint32_t num_c = count_or_capacity(a.d_counts, 0, a.capacity);
+  for (uint32_t u = tid; u < cap_units; u += stride) {
+    const uint32_t e = u / chunks;
+    const int c0 = static_cast<int>(u % chunks) * VEC;
+    // requested before num_c is known (both slots exist: e - 1 < e < capacity)
+    ckv_compress_plan_t P, Pp;
+    P.seq_len = Pp.seq_len = kInvalidU32;
+    if (e < a.capacity) P = load_plan_c(a.plan_c + e);
+    if (e > 0 && e - 1 < a.capacity) Pp = load_plan_c(a.plan_c + e - 1);
+    uint4 ap[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ap[i] = ld_cached16(ape + static_cast<size_t>(i) * hd + c0);
+    if (e > num_c || (e == num_c && !token)) break;  // u only grows
+    if (e == num_c) {  // token layout: the rows after the last compress row
+      const int64_t last = num_c == 0 ? -1
+                           : plan_c_invalid(Pp) ? static_cast<int64_t>(a.num_q_tokens)
+                                                : static_cast<int64_t>(Pp.ragged_bl & CKV_RAGGED_MASK);
+      for (int64_t row = last + 1; row < static_cast<int64_t>(a.num_q_tokens); ++row)
+        store_zero_chunk<TOut, VEC>(out + static_cast<size_t>(row) * hd + c0);
+      continue;
+    }
+    C4Rec rec;
+    bool bad;
+    if (!c4_record(a, P, rec, bad)) {
+      if (bad && c0 == 0) status_or(a.d_status, CKV_STATUS_BAD_INDEX);
+      continue;
+    }
+    uint4 kv[8], sc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      kv[i] = sc[i] = make_uint4(0, 0, 0, 0);
+      if (i >= rec.first) {
+        // entries held in the ring were checked inside the state by c4_record
+        const TIn* row = i < rec.bl ? state + static_cast<size_t>((i < 4 ? rec.rp0 : rec.rp1) * 4 + (i & 3)) * width
+                                    : input + (static_cast<size_t>(rec.ragged) + i - 7) * width;
+        kv[i] = ld_stream16(row + (i < 4 ? 0 : hd) + c0);
+        sc[i] = ld_stream16(row + (i < 4 ? 2 * hd : 3 * hd) + c0);
+      }
+    }
+    float res[VEC];
+    c4_pool_chunk<TIn, VEC>(kv, sc, ap, rec.first, res);
+    store_row_chunk<TOut, VEC>(out + (token ? static_cast<size_t>(rec.ragged) : e) * hd + c0, res);
+    if (token) {  // zero the rows between the previous compress row and this one
+      int64_t prev = -1;
+      if (e > 0)
+        prev = plan_c_invalid(Pp) ? static_cast<int64_t>(rec.ragged)
+                                  : static_cast<int64_t>(Pp.ragged_bl & CKV_RAGGED_MASK);
+      for (int64_t row = prev + 1; row < static_cast<int64_t>(rec.ragged); ++row)
+        store_zero_chunk<TOut, VEC>(out + static_cast<size_t>(row) * hd + c0);
+    }
+  }
+}
+
 // Decode: one unit per (row, 4 channels).  The new token's row is written to
 // its ring slot; at a group boundary the window's first 7 entries come from
 // the ring (none of them is the slot being written) and entry 7 is the new
@@ -784,6 +892,39 @@ int launch_prefill_t(const PoolArgs& a, cudaStream_t s) {
   return launch_pdl(fn, dim3(grid), dim3(threads), smem, s, a, maps);
 }
 
+// Resident blocks per SM of the direct kernel, per device (0: the query
+// failed; not cached, so a later launch asks again).
+template <typename TIn, typename TOut>
+int c4_direct_per_sm() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const bool cached_dev = dev >= 0 && dev < 64;
+  int per_sm = cached_dev ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (per_sm > 0) return per_sm;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, c4_pool_prefill_direct_kernel<TIn, TOut>,
+                                                    kC4DirectThreads, 0) != cudaSuccess ||
+      per_sm <= 0) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (cached_dev) cache[dev].store(per_sm, std::memory_order_relaxed);
+  return per_sm;
+}
+
+template <typename TIn, typename TOut>
+int launch_prefill_direct_t(const PoolArgs& a, int per_sm, cudaStream_t s) {
+  const uint32_t chunks = static_cast<uint32_t>(a.head_dim / C4Vec<TIn>::VEC);
+  const uint64_t units64 = (static_cast<uint64_t>(a.capacity) + (a.out_layout == CKV_OUT_TOKEN ? 1 : 0)) * chunks;
+  if (units64 == 0) return CKV_OK;
+  if (units64 > 0xFFFFFFFFull) return CKV_ERR_SIZE;
+  const uint64_t blocks = (units64 + kC4DirectThreads - 1) / kC4DirectThreads;
+  const uint32_t grid = static_cast<uint32_t>(
+      std::max<uint64_t>(1, std::min<uint64_t>(blocks, static_cast<uint64_t>(per_sm) * sm_count())));
+  return launch_pdl(c4_pool_prefill_direct_kernel<TIn, TOut>, dim3(grid), dim3(kC4DirectThreads), 0, s, a, chunks,
+                    static_cast<uint32_t>(units64));
+}
+
 template <typename TIn, typename TOut>
 int launch_decode_t(const PoolArgs& a, cudaStream_t s) {
   const uint32_t chunks = static_cast<uint32_t>(a.head_dim / kC4DecVec);
@@ -819,15 +960,29 @@ int launch_prefill_s(const PoolArgs& a, cudaStream_t s) {
                                   : launch_prefill_t<TIn, TOut, false, kSmall>(a, s);
 }
 
-// steps of at most eight full stages per SM take the small geometry (two CTAs
-// per SM, half the records per stage): 3.34 -> 2.80 us back to back on a
-// 16-record step, 7.51 -> 7.30 us on 1024 records, large steps unchanged
+// Steps of at most eight full stages per SM take the small geometry (two CTAs
+// per SM, half the records per stage: 3.34 -> 2.80 us back to back on a
+// 16-record step, large steps unchanged), and of those, steps whose records
+// fit 1.6 waves of the direct kernel take that one (16 records 2.77 -> 2.29
+// us, 1024 records 7.35 -> 6.44 us back to back; at 3.4 waves it took 20.6
+// against the staged 17.7 us).  The host knows the plan's capacity, not its
+// count, and a padded plan's capacity can be the token count, so the records
+// are bounded by the tokens instead: at most ceil(extend / 4) per request of
+// a batch of at most 1024, i.e. num_q_tokens / 4 + 768.
 template <typename TIn, typename TOut>
 int launch_prefill_w(const PoolArgs& a, cudaStream_t s) {
   using S = C4Stage<TIn>;
-  const bool small = S::recs(a.head_dim) >= 2 &&
-                     static_cast<uint64_t>(a.capacity) <= static_cast<uint64_t>(8) * sm_count() * S::recs(a.head_dim);
-  return small ? launch_prefill_s<TIn, TOut, true>(a, s) : launch_prefill_s<TIn, TOut, false>(a, s);
+  const int hd = a.head_dim;
+  const bool small = S::recs(hd) >= 2 &&
+                     static_cast<uint64_t>(a.capacity) <= static_cast<uint64_t>(8) * sm_count() * S::recs(hd);
+  if (!small) return launch_prefill_s<TIn, TOut, false>(a, s);
+  const int per_sm = c4_direct_per_sm<TIn, TOut>();
+  const uint64_t recs = std::min<uint64_t>(a.capacity, a.num_q_tokens / 4 + 768) +
+                        (a.out_layout == CKV_OUT_TOKEN ? 1 : 0);
+  const uint64_t units = recs * static_cast<uint64_t>(S::chunks(hd));
+  const uint64_t wave = static_cast<uint64_t>(per_sm) * sm_count() * kC4DirectThreads;
+  if (per_sm > 0 && units * 5 <= wave * 8) return launch_prefill_direct_t<TIn, TOut>(a, per_sm, s);
+  return launch_prefill_s<TIn, TOut, true>(a, s);
 }
 
 }  // namespace

@@ -84,7 +84,8 @@ enum { CKV_MAX_BATCH = 1024, CKV_MAX_TOKENS = (1 << 24) - 1 };
 /* ------------------------------------------------------------------ waits */
 /* The pooling kernels that stage their inputs through the TMA engine (C4 and
  * C128 prefill pools, C128 decode, online prefill) wait on mbarriers for those
- * copies.  Every such wait gives up after a time limit: the kernel then ORs
+ * copies (small C4 prefill steps, which load their windows directly, have no
+ * such waits).  Every such wait gives up after a time limit: the kernel then ORs
  * CKV_STATUS_TIMEOUT into *d_status and its CTA stops, after waiting (up to
  * 2 s) for the copies it has already issued, so that none of them lands in
  * shared memory the CTA no longer owns.  The context stays usable.
