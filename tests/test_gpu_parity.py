@@ -222,7 +222,7 @@ def _run_prefill_parity(env, ratio, hd, in_dt, out_dt, layout, pl, el, seed, sta
 # head_dim 640 and 1024 give the C4 pool its other widths (128-channel blocks,
 # five per quarter; 1 KB-wide fp32 rows).  Steps this small take the direct
 # kernel, except fp32 at 640 and 1024 (one record fills a stage); each launch
-# shape of the pool has its own cases in test_gpu_c4_paths.py.
+# shape of the pool has its own cases in test_gpu_pool_shapes.py.
 @pytest.mark.parametrize("hd", [128, 384, 512, 640, 1024])
 @pytest.mark.parametrize("dts", [("bf16", "f32"), ("bf16", "bf16"), ("f32", "f32"), ("f32", "bf16")])
 @pytest.mark.parametrize("layout", [0, 1])

@@ -1,5 +1,7 @@
-"""The C4 prefill pool's three launch shapes, each against the oracle on every
-record, for every head_dim class and dtype pair.
+"""The prefill pools' launch shapes, each against the oracle on every record,
+for every head_dim class and dtype pair.
+
+C4 prefill pool:
 
 The host picks the shape from what it knows before launch: the plan's
 capacity and the token count.
@@ -15,6 +17,14 @@ The cases are sized from those rules with margin: "small" at ~2.5 waves of
 the direct kernel, "direct2" at ~1.3 waves (some threads take a second
 record), "large" just past the small geometry's limit.  The small cases of
 test_gpu_parity.py all take the direct kernel.
+
+C128 prefill pool: one persistent CTA per (SM, channel slice) takes records
+first, first + stride, ... (stride = SMs / slices, or the capacity when that
+is smaller) through its TMA ring.  "ring" gives every CTA at least two
+records, "mixed" about half of the CTAs one and half two (the speculative-
+decoding verify step's shape, where the producer's record requested with the
+count and the consumers' record requested before the tile wait are the whole
+chain); the small cases of test_gpu_parity.py give every CTA at most one.
 """
 import numpy as np
 import pytest
@@ -67,3 +77,25 @@ def test_c4_prefill_pool_shapes(env, regime, hd, dts):
     pl = rng.integers(0, 1000, BATCH)
     layout = (hd // 128 + len(regime) + DT[dts[1]]) % 2
     _run_prefill_parity(env, 4, hd, DT[dts[0]], DT[dts[1]], layout, list(pl), list(el), seed=hd + len(regime))
+
+
+@pytest.mark.parametrize("regime", ["ring", "mixed"])
+@pytest.mark.parametrize("hd", [128, 384, 512, 1024])
+@pytest.mark.parametrize("dts", [("bf16", "f32"), ("bf16", "bf16"), ("f32", "f32"), ("f32", "bf16")])
+def test_c128_prefill_pool_shapes(env, regime, hd, dts):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    slices = hd // (128 if dts[0] == "bf16" else 64)
+    stride = sms // slices
+    want = 3 * stride if regime == "ring" else stride + stride // 2
+    rng = np.random.default_rng(hd * 5 + len(regime) + 3 * DT[dts[0]] + DT[dts[1]])
+    pl = rng.integers(1, 4096, BATCH)                     # most first windows start in the state
+    per = -(-want // BATCH)
+    el = 128 * per - pl % 128 + rng.integers(0, 128, BATCH)
+    o = env[0]
+    _, _, (nc, _), _ = o.plan_prefill(128, np.arange(BATCH), pl + el, el)
+    assert nc >= (2 * stride if regime == "ring" else stride + 1), nc
+    if regime == "mixed":
+        assert nc < 2 * stride, nc
+    layout = (hd // 128 + len(regime) + DT[dts[1]]) % 2
+    _run_prefill_parity(env, 128, hd, DT[dts[0]], DT[dts[1]], layout, list(pl), list(el), seed=hd + len(regime),
+                        outliers=0.01)
