@@ -14,10 +14,13 @@ on a page boundary), and the achieved HBM bandwidth of the dominant kernel
 
 Inputs live in HBM when the timed region starts.  Before every step (outside
 the timed region) the prefill state is restored from a pristine copy and L2
-is flushed by writing a buffer of twice its size.  Each step's four segments
-(plan_prefill | pool | write + plan_decode | decode) are captured in one CUDA
-graph with event-record nodes between them; per-kernel times are those GPU
-timestamps.  ``e2e`` repeats the step through the same
+is flushed (a buffer of twice its size written, then another one read).  The
+step is one CUDA graph whose kernels keep their programmatic launch edges,
+timed with CUDA events around it; a second graph of the same kernels with
+event-record nodes between them gives per-kernel times (the roofline's
+kernel time), and each kernel's cost inside the step is also taken by
+difference (the step graph against the same graph without that kernel, no
+event node between kernels).  ``e2e`` repeats the step through the same
 API with the step's inputs copied from pinned host memory and its outputs
 copied back inside the timed region.  Beside the step, the same line carries
 the C4 kernels on their own workloads (``kernels_c4``) and the
